@@ -1,0 +1,12 @@
+"""CPU oracle for the quantized-weight OUT_PROD (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU baseline /
+reference leg may import this package.  The library under
+``quantized_weight_out_gb300`` never does: it has no CPU fallback.
+"""
+from .quant_out_prod import (  # noqa: F401
+    F16, BF16, Q8_0, Q4_0, Q4_K,
+    f16_bits_to_f32, bf16_bits_to_f32,
+    decode_q8_0, decode_q4_0, decode_q4_k, decode_f16, decode_bf16,
+    dequant, row_bytes, out_prod, abs_bound, out_prod_at, q4_k_scale_min,
+)

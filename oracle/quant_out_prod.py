@@ -1,0 +1,216 @@
+"""Plain, slow, CPU oracle of the activation-gradient OUT_PROD through a
+resident quantized / half-precision weight.
+
+TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the bench's CPU
+baseline call this.  It shares no code with the CUDA library.
+
+What it computes
+----------------
+The llama.cpp fork's PR "cuda: out_prod accepts a quantized src0" (commit
+message and section "What") states that the backward of ``mul_mat(W, x)``
+with respect to ``x`` is ``out_prod(W, grad^T)``, and that the CPU backend's
+``out_prod_q_f32`` (every quantized ``src0``) is the oracle its CUDA route is
+compared against.  The pages print no index formula; the plainest reading,
+with ``W`` holding N rows (output features) of K values (input features) and
+the incoming gradient ``dY`` of shape [T, N], is
+
+    dX[t, k] = beta * dX0[t, k] + sum_n dY[t, n] * deq(W)[n, k]
+
+i.e. ``dX = dY @ deq(W)``.  ``beta`` follows BLAS: 0 means dX0 is not read.
+
+Steps (in this order, nothing fused or reordered):
+1. decode every stored row of W to F32 per its format definition; fp16 fields
+   are widened exactly (subnormals included), then the format's formula is
+   evaluated in F32;
+2. contract in F64: every F32 x F32 product is exact in F64;
+3. the acceptance bound  B[t, k] = sum_n |dY[t, n]| * |deq(W)[n, k]|  (F64).
+
+Block formats (little-endian), ggml's GGUF block types:
+* Q8_0  34 B / 32: fp16 d, int8 qs[32];          y_i = d * qs_i
+* Q4_0  18 B / 32: fp16 d, qs[16] (lo nibble = value j, hi = value j+16);
+                                                  y = d * (nib - 8)
+* Q4_K 144 B / 256: fp16 d, fp16 dmin, 12 B of 6-bit (sc, m) x 8, qs[128];
+                                                  y = (d*sc)*q - dmin*m
+* F16 / BF16: 2 B per value.
+
+Parity pins for each function live in tests/test_oracle.py.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+F16, BF16, Q8_0, Q4_0, Q4_K = 1, 2, 3, 4, 5
+
+_BLOCK = {F16: (1, 2), BF16: (1, 2), Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144)}
+
+
+def row_bytes(wtype: int, K: int) -> int:
+    """Stored bytes of one row of K values, or 0 if K does not fit the type."""
+    if wtype not in _BLOCK or K <= 0:
+        return 0
+    bs, bb = _BLOCK[wtype]
+    if K % bs:
+        return 0
+    return (K // bs) * bb
+
+
+# ----------------------------------------------------------------------------
+# scalar field decoders
+
+def f16_bits_to_f32(bits) -> np.ndarray:
+    """IEEE 754 binary16 -> float32, from the definition:
+    exponent 0 -> (-1)^s * 2^-14 * m/1024 (subnormal),
+    exponent 31 -> inf (m == 0) or NaN,
+    else        -> (-1)^s * 2^(e-15) * (1 + m/1024).
+    Every binary16 value is exactly representable in float32."""
+    h = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    s = (h >> 15) & 1
+    e = (h >> 10) & 0x1F
+    m = h & 0x3FF
+    sub = np.ldexp(m.astype(np.float64), -24)                 # m * 2^-24
+    nrm = np.ldexp((m + 1024).astype(np.float64), e - 25)    # (1024+m) * 2^(e-25)
+    mag = np.where(e == 0, sub, nrm)
+    mag = np.where(e == 31, np.where(m == 0, np.inf, np.nan), mag)
+    return np.where(s == 1, -mag, mag).astype(np.float32)
+
+
+def bf16_bits_to_f32(bits) -> np.ndarray:
+    """bfloat16 -> float32: the 16 bits are the top half of the float32 word."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32)
+
+
+def _le16(lo: np.ndarray, hi: np.ndarray) -> np.ndarray:
+    return lo.astype(np.uint16) | (hi.astype(np.uint16) << np.uint16(8))
+
+
+# ----------------------------------------------------------------------------
+# format decoders: stored bytes -> F32 [N, K]
+
+def _rows(W, N, K, wtype):
+    rb = row_bytes(wtype, K)
+    if rb == 0:
+        raise ValueError(f"K={K} does not fit type {wtype}")
+    W = np.asarray(W, dtype=np.uint8).reshape(-1)
+    if W.size != N * rb:
+        raise ValueError(f"expected {N * rb} bytes, got {W.size}")
+    return W.reshape(N, rb)
+
+
+def decode_q8_0(W, N: int, K: int) -> np.ndarray:
+    """Q8_0: y[i] = F32(d) * qs[i], exact in F32 (11-bit x 8-bit product)."""
+    blk = _rows(W, N, K, Q8_0).reshape(N, K // 32, 34)
+    d = f16_bits_to_f32(_le16(blk[..., 0], blk[..., 1]))
+    qs = blk[..., 2:34].view(np.int8).astype(np.float32)
+    return (d[..., None] * qs).reshape(N, K)
+
+
+def decode_q4_0(W, N: int, K: int) -> np.ndarray:
+    """Q4_0: value j (< 16) = low nibble of qs[j], value j+16 = high nibble;
+    y = F32(d) * (nib - 8), exact in F32."""
+    blk = _rows(W, N, K, Q4_0).reshape(N, K // 32, 18)
+    d = f16_bits_to_f32(_le16(blk[..., 0], blk[..., 1]))
+    qs = blk[..., 2:18]
+    nib = np.concatenate([qs & 0x0F, qs >> 4], axis=-1).astype(np.float32)
+    return (d[..., None] * (nib - np.float32(8.0))).reshape(N, K)
+
+
+def q4_k_scale_min(S: np.ndarray):
+    """The eight 6-bit (scale, min) pairs of a Q4_K super-block from its 12
+    packed bytes S[..., 0:12].  Sub-blocks 0..3 use the low 6 bits of S[j]
+    (scale) and S[j+4] (min); sub-blocks 4..7 take their low 4 bits from the
+    two nibbles of S[j+4] (j >= 4) and their high 2 bits from the top 2 bits
+    of S[j-4] (scale) and S[j] (min)."""
+    S = np.asarray(S, dtype=np.uint8).astype(np.int64)
+    sc = np.empty(S.shape[:-1] + (8,), dtype=np.int64)
+    mn = np.empty_like(sc)
+    for j in range(8):
+        if j < 4:
+            sc[..., j] = S[..., j] & 63
+            mn[..., j] = S[..., j + 4] & 63
+        else:
+            sc[..., j] = (S[..., j + 4] & 15) | ((S[..., j - 4] >> 6) << 4)
+            mn[..., j] = (S[..., j + 4] >> 4) | ((S[..., j] >> 6) << 4)
+    return sc, mn
+
+
+def decode_q4_k(W, N: int, K: int) -> np.ndarray:
+    """Q4_K: 256 values in 8 sub-blocks of 32.  For chunk c = 0..3 and
+    l = 0..31, value 64c+l is the low nibble of qs[32c+l] (sub-block 2c) and
+    value 64c+32+l the high nibble (sub-block 2c+1).
+    y = (F32(d) * sc) * q - F32(dmin) * m: both products exact in F32, one
+    rounding in the subtraction."""
+    blk = _rows(W, N, K, Q4_K).reshape(N, K // 256, 144)
+    d = f16_bits_to_f32(_le16(blk[..., 0], blk[..., 1]))
+    dmin = f16_bits_to_f32(_le16(blk[..., 2], blk[..., 3]))
+    sc, mn = q4_k_scale_min(blk[..., 4:16])
+    qs = blk[..., 16:144]
+    q = np.empty(blk.shape[:-1] + (256,), dtype=np.float32)
+    sub = np.empty(256, dtype=np.int64)
+    for c in range(4):
+        q[..., 64 * c: 64 * c + 32] = qs[..., 32 * c: 32 * c + 32] & 0x0F
+        q[..., 64 * c + 32: 64 * c + 64] = qs[..., 32 * c: 32 * c + 32] >> 4
+        sub[64 * c: 64 * c + 32] = 2 * c
+        sub[64 * c + 32: 64 * c + 64] = 2 * c + 1
+    dsc = d[..., None] * sc.astype(np.float32)       # [N, nb, 8], exact
+    dmm = dmin[..., None] * mn.astype(np.float32)    # [N, nb, 8], exact
+    y = dsc[..., sub] * q - dmm[..., sub]
+    return y.astype(np.float32).reshape(N, K)
+
+
+def decode_f16(W, N: int, K: int) -> np.ndarray:
+    b = _rows(W, N, K, F16).reshape(N, K, 2)
+    return f16_bits_to_f32(_le16(b[..., 0], b[..., 1]))
+
+
+def decode_bf16(W, N: int, K: int) -> np.ndarray:
+    b = _rows(W, N, K, BF16).reshape(N, K, 2)
+    return bf16_bits_to_f32(_le16(b[..., 0], b[..., 1]))
+
+
+_DECODERS = {F16: decode_f16, BF16: decode_bf16, Q8_0: decode_q8_0,
+             Q4_0: decode_q4_0, Q4_K: decode_q4_k}
+
+
+def dequant(wtype: int, W, N: int, K: int) -> np.ndarray:
+    """deq(W) as F32 [N, K] (the value rg_dequant must reproduce bit for bit)."""
+    if wtype not in _DECODERS:
+        raise ValueError(f"unknown weight type {wtype}")
+    return _DECODERS[wtype](W, N, K)
+
+
+# ----------------------------------------------------------------------------
+# the contraction
+
+def out_prod(wtype: int, W, N: int, K: int, dY, T: int, dX0=None, beta: float = 0.0,
+             Wd=None) -> np.ndarray:
+    """F64 [T, K]: beta*dX0 + dY @ deq(W), contracted over the N rows of W."""
+    if Wd is None:
+        Wd = dequant(wtype, W, N, K)
+    dY = np.asarray(dY, dtype=np.float32).reshape(T, N)
+    ref = dY.astype(np.float64) @ Wd.astype(np.float64)
+    if beta != 0.0:
+        ref = ref + float(np.float32(beta)) * np.asarray(dX0, dtype=np.float32).reshape(T, K).astype(np.float64)
+    return ref
+
+
+def abs_bound(dY, Wd) -> np.ndarray:
+    """F64 [T, K]: sum_n |dY[t, n]| * |deq(W)[n, k]|."""
+    return np.abs(np.asarray(dY, dtype=np.float64)) @ np.abs(np.asarray(Wd, dtype=np.float64))
+
+
+def out_prod_at(Wd, dY, ts, ks, dX0=None, beta: float = 0.0):
+    """Selected outputs one by one: (ref, bound) at pairs (ts[i], ks[i]).
+
+    Each is the F64 dot product of row ts[i] of dY with column ks[i] of deq(W)
+    (plus beta*dX0 there), for parity checks on sizes whose full product is
+    too large to form on the CPU."""
+    ts = np.asarray(ts, dtype=np.int64)
+    ks = np.asarray(ks, dtype=np.int64)
+    rows = np.asarray(dY, dtype=np.float32)[ts].astype(np.float64)   # [S, N]
+    cols = np.asarray(Wd, dtype=np.float32)[:, ks].T.astype(np.float64)  # [S, N]
+    ref = np.einsum("sn,sn->s", rows, cols)
+    bnd = np.einsum("sn,sn->s", np.abs(rows), np.abs(cols))
+    if beta != 0.0:
+        ref = ref + float(np.float32(beta)) * np.asarray(dX0, dtype=np.float32)[ts, ks].astype(np.float64)
+    return ref, bnd

@@ -1,0 +1,309 @@
+"""Seeded synthetic inputs for the quantized-weight OUT_PROD.
+
+This module only *produces* bytes and F32 arrays; it holds none of the
+operation's arithmetic (no decode, no contraction).  Both the CPU oracle and
+the CUDA path are fed from here, so the two always see identical inputs.
+
+Random numbers
+--------------
+Every value is a pure function of (seed, stream, field, index):
+
+* ``splitmix64`` - the output mix of SplitMix64 (Steele, Lea and Flood,
+  "Fast splittable pseudorandom number generators", OOPSLA 2014).  The i-th
+  draw of a stream is the (i+1)-th SplitMix64 output from the stream's key,
+  i.e. ``mix(key + (i + 1) * GAMMA)``.
+* uniforms in (0, 1] take the top 53 bits: ``((x >> 11) + 1) * 2**-53``.
+* normals use the cosine branch of Box and Muller (1958) on draws 2i and 2i+1.
+
+Formats written (little-endian, the block layouts of ggml's GGUF types):
+
+* Q8_0  34 B / 32 values: fp16 ``d`` then 32 int8 ``qs``.
+* Q4_0  18 B / 32 values: fp16 ``d`` then 16 bytes; value j<16 sits in the low
+  nibble of byte j, value j+16 in the high nibble.
+* Q4_K 144 B / 256 values: fp16 ``d``, fp16 ``dmin``, 12 bytes of 6-bit
+  (scale, min) pairs for 8 sub-blocks, 128 bytes of nibbles.
+* F16 / BF16: 2 B per value.
+
+The generator recipes follow the workload descriptions of the llama.cpp fork's
+PR "cuda: out_prod accepts a quantized src0" (the shapes a LoRA backward sees)
+as restated in the workload table below.
+"""
+from __future__ import annotations
+
+import dataclasses
+import os
+from concurrent.futures import ThreadPoolExecutor
+from typing import List, Optional
+
+import numpy as np
+
+# ----------------------------------------------------------------------------
+# weight type codes (the C ABI uses the same integers)
+F16, BF16, Q8_0, Q4_0, Q4_K = 1, 2, 3, 4, 5
+TYPE_NAMES = {F16: "f16", BF16: "bf16", Q8_0: "q8_0", Q4_0: "q4_0", Q4_K: "q4_k"}
+NAME_TO_TYPE = {v: k for k, v in TYPE_NAMES.items()}
+
+# (values per block, bytes per block)
+BLOCK = {F16: (1, 2), BF16: (1, 2), Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144)}
+
+
+def row_bytes(wtype: int, K: int) -> int:
+    """Bytes of one stored row of K values (0 when K does not fit the type)."""
+    if wtype not in BLOCK or K <= 0:
+        return 0
+    bs, bb = BLOCK[wtype]
+    if K % bs:
+        return 0
+    return K // bs * bb
+
+
+# ----------------------------------------------------------------------------
+# counter-based random numbers
+
+_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+_STREAM_MUL = np.uint64(0xD1B54A32D192ED03)
+
+
+def _mix(z: np.ndarray) -> np.ndarray:
+    z = np.asarray(z, dtype=np.uint64)
+    z = (z ^ (z >> np.uint64(30))) * _M1
+    z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def stream_key(seed: int, stream: int, field: int = 0) -> np.uint64:
+    """Key of one (seed, stream, field) sequence."""
+    with np.errstate(over="ignore"):
+        k = _mix(np.array([seed], dtype=np.uint64))[0]
+        k = _mix(np.array([k ^ (np.uint64(stream) * _STREAM_MUL)], dtype=np.uint64))[0]
+        k = _mix(np.array([k ^ (np.uint64(field + 1) * _GAMMA)], dtype=np.uint64))[0]
+    return np.uint64(k)
+
+
+def draws_u64(key: np.uint64, start: int, count: int) -> np.ndarray:
+    """Draws start..start+count-1 of the sequence with this key."""
+    idx = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        return _mix(np.uint64(key) + idx * _GAMMA)
+
+
+def uniform01(key: np.uint64, start: int, count: int) -> np.ndarray:
+    """Uniforms in (0, 1] (float64)."""
+    x = draws_u64(key, start, count)
+    return ((x >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
+
+
+_CHUNK = 1 << 20
+_THREADS = max(1, min(32, os.cpu_count() or 1))
+
+
+def _chunked(count: int, fill) -> None:
+    """Run fill(start, n) over chunks of [0, count) on a thread pool (numpy
+    releases the GIL inside its loops).  Results do not depend on chunking."""
+    spans = [(s, min(_CHUNK, count - s)) for s in range(0, count, _CHUNK)]
+    if len(spans) <= 1 or _THREADS == 1:
+        for s, n in spans:
+            fill(s, n)
+        return
+    with ThreadPoolExecutor(_THREADS) as ex:
+        list(ex.map(lambda sn: fill(*sn), spans))
+
+
+def normal_f32(seed: int, stream: int, count: int, sigma: float, field: int = 0) -> np.ndarray:
+    """``count`` draws of N(0, sigma^2), rounded to float32."""
+    key = stream_key(seed, stream, field)
+    out = np.empty(count, dtype=np.float32)
+
+    def fill(s, n):
+        u = uniform01(key, 2 * s, 2 * n)
+        u1, u2 = u[0::2], u[1::2]
+        z = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+        out[s:s + n] = (sigma * z).astype(np.float32)
+    _chunked(count, fill)
+    return out
+
+
+def uniform_int(seed: int, stream: int, count: int, modulus: int, field: int) -> np.ndarray:
+    """``count`` integers uniform on {0..modulus-1}; modulus divides 2**64."""
+    assert modulus & (modulus - 1) == 0
+    key = stream_key(seed, stream, field)
+    out = np.empty(count, dtype=np.int64)
+
+    def fill(s, n):
+        out[s:s + n] = (draws_u64(key, s, n) & np.uint64(modulus - 1)).astype(np.int64)
+    _chunked(count, fill)
+    return out
+
+
+# ----------------------------------------------------------------------------
+# encoders (F32 -> stored bits).  Round-to-nearest-even throughout.
+
+def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """IEEE binary16 bits of x, round to nearest even (numpy's cast)."""
+    return np.asarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """bfloat16 bits of finite x, round to nearest even."""
+    b = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (b + np.uint64(0x7FFF) + ((b >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    return r.astype(np.uint16)
+
+
+def _round_half_away(v: np.ndarray) -> np.ndarray:
+    return np.sign(v) * np.floor(np.abs(v) + np.float32(0.5))
+
+
+def _f16_le(bits: np.ndarray) -> np.ndarray:
+    """uint16 array [...] -> uint8 array [..., 2] little-endian."""
+    b = bits.astype(np.uint16)
+    return np.stack([(b & 0xFF).astype(np.uint8), (b >> 8).astype(np.uint8)], axis=-1)
+
+
+def quantize_q8_0(x: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Q8_0 blocks of x [N, K]: d = amax/127 stored fp16, q = round(x/d)."""
+    xb = np.asarray(x, dtype=np.float32).reshape(N, K // 32, 32)
+    amax = np.max(np.abs(xb), axis=-1)
+    d32 = (amax / np.float32(127.0)).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        v = np.where(d32[..., None] > 0, xb / d32[..., None], np.float32(0))
+    q = np.clip(_round_half_away(v.astype(np.float32)), -127, 127).astype(np.int8)
+    out = np.empty((N, K // 32, 34), dtype=np.uint8)
+    out[..., 0:2] = _f16_le(f32_to_f16_bits(d32))
+    out[..., 2:34] = q.view(np.uint8)
+    return out.reshape(-1)
+
+
+def quantize_q4_0(x: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Q4_0 blocks: d = mx/-8 (mx the signed value of largest magnitude, first
+    on ties), q = clamp(round(x/d) + 8, 0, 15)."""
+    xb = np.asarray(x, dtype=np.float32).reshape(N, K // 32, 32)
+    idx = np.argmax(np.abs(xb), axis=-1)
+    mx = np.take_along_axis(xb, idx[..., None], axis=-1)[..., 0]
+    d32 = (mx / np.float32(-8.0)).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        v = np.where(d32[..., None] != 0, xb / d32[..., None], np.float32(0))
+    q = np.clip(_round_half_away(v.astype(np.float32)) + 8, 0, 15).astype(np.uint8)
+    out = np.empty((N, K // 32, 18), dtype=np.uint8)
+    out[..., 0:2] = _f16_le(f32_to_f16_bits(d32))
+    out[..., 2:18] = q[..., :16] | (q[..., 16:] << 4)
+    return out.reshape(-1)
+
+
+def pack_q4_k(d_bits, dmin_bits, sc, m, q) -> np.ndarray:
+    """Pack Q4_K super-blocks from their fields.
+
+    d_bits, dmin_bits: [B] uint16; sc, m: [B, 8] ints in 0..63; q: [B, 256]
+    ints in 0..15 (value index order).  Returns uint8 [B, 144]."""
+    B = d_bits.shape[0]
+    sc = np.asarray(sc, dtype=np.uint8)
+    m = np.asarray(m, dtype=np.uint8)
+    q = np.asarray(q, dtype=np.uint8)
+    S = np.zeros((B, 12), dtype=np.uint8)
+    for j in range(4):
+        # sub-blocks 0..3: 6 bits in S[j] / S[j+4]; their top bits carry the
+        # 2 high bits of sub-blocks 4..7.
+        S[:, j] = (sc[:, j] & 63) | ((sc[:, j + 4] >> 4) << 6)
+        S[:, j + 4] = (m[:, j] & 63) | ((m[:, j + 4] >> 4) << 6)
+        S[:, j + 8] = (sc[:, j + 4] & 15) | ((m[:, j + 4] & 15) << 4)
+    qs = np.zeros((B, 128), dtype=np.uint8)
+    for c in range(4):
+        lo = q[:, 64 * c: 64 * c + 32]
+        hi = q[:, 64 * c + 32: 64 * c + 64]
+        qs[:, 32 * c: 32 * c + 32] = lo | (hi << 4)
+    out = np.empty((B, 144), dtype=np.uint8)
+    out[:, 0:2] = _f16_le(d_bits)
+    out[:, 2:4] = _f16_le(dmin_bits)
+    out[:, 4:16] = S
+    out[:, 16:144] = qs
+    return out
+
+
+# ----------------------------------------------------------------------------
+# weights and activations for one call
+
+def gen_weight(wtype: int, N: int, K: int, seed: int, stream: int) -> np.ndarray:
+    """Stored bytes of an N x K weight, uint8 [N * row_bytes(wtype, K)]."""
+    if row_bytes(wtype, K) == 0:
+        raise ValueError(f"K={K} does not fit type {wtype}")
+    if wtype == Q4_K:
+        nb = N * K // 256
+        d = np.abs(normal_f32(seed, stream, nb, 1e-3, field=1))
+        dmin = np.abs(normal_f32(seed, stream, nb, 1e-3, field=2))
+        sc = uniform_int(seed, stream, nb * 8, 64, field=3).reshape(nb, 8)
+        m = uniform_int(seed, stream, nb * 8, 64, field=4).reshape(nb, 8)
+        q = uniform_int(seed, stream, nb * 256, 16, field=5).reshape(nb, 256)
+        return pack_q4_k(f32_to_f16_bits(d), f32_to_f16_bits(dmin), sc, m, q).reshape(-1)
+    x = normal_f32(seed, stream, N * K, 0.02)
+    if wtype == Q8_0:
+        return quantize_q8_0(x, N, K)
+    if wtype == Q4_0:
+        return quantize_q4_0(x, N, K)
+    if wtype == F16:
+        return f32_to_f16_bits(x).view(np.uint8).copy()
+    if wtype == BF16:
+        return f32_to_bf16_bits(x).view(np.uint8).copy()
+    raise ValueError(f"unknown weight type {wtype}")
+
+
+@dataclasses.dataclass
+class Problem:
+    """One OUT_PROD call: dX[T,K] = beta*dX0 + dY[T,N] . deq(W)[N,K]."""
+    name: str
+    wtype: int
+    N: int
+    K: int
+    T: int
+    dy_sigma: float
+    beta: float = 0.0
+    stream_base: int = 0     # added to the W / dY / dX0 stream ids (1, 2, 3)
+    seed: int = 0
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.T * self.N * self.K
+
+    @property
+    def w_bytes(self) -> int:
+        return self.N * row_bytes(self.wtype, self.K)
+
+    def algorithmic_bytes(self) -> int:
+        """bytes(W) + 4T(N+K) (+4TK when beta != 0)."""
+        b = self.w_bytes + 4 * self.T * (self.N + self.K)
+        if self.beta != 0.0:
+            b += 4 * self.T * self.K
+        return b
+
+    def weight(self) -> np.ndarray:
+        return gen_weight(self.wtype, self.N, self.K, self.seed, 1 + self.stream_base)
+
+    def dy(self) -> np.ndarray:
+        return normal_f32(self.seed, 2 + self.stream_base, self.T * self.N,
+                          self.dy_sigma).reshape(self.T, self.N)
+
+    def dx0(self) -> Optional[np.ndarray]:
+        if self.beta == 0.0:
+            return None
+        return normal_f32(self.seed, 3 + self.stream_base, self.T * self.K,
+                          1e-3).reshape(self.T, self.K)
+
+
+def _layer_sweep(T: int = 8192) -> List[Problem]:
+    shapes = [("q", Q4_K, 4096, 4096), ("k", Q4_K, 1024, 4096), ("v", Q4_K, 1024, 4096),
+              ("o", Q4_K, 4096, 4096), ("gate", Q4_K, 14336, 4096),
+              ("up", Q4_K, 14336, 4096), ("down", Q8_0, 4096, 14336)]
+    return [Problem(f"layer7b_{nm}", wt, n, k, T, 1e-3, 0.0, 16 * i)
+            for i, (nm, wt, n, k) in enumerate(shapes)]
+
+
+# The workloads: each is a list of independent calls.
+WORKLOADS = {
+    "q8_0_256x256_t32": [Problem("q8_0_256x256_t32", Q8_0, 256, 256, 32, 1.0)],
+    "q4_0_4096x4096_t512": [Problem("q4_0_4096x4096_t512", Q4_0, 4096, 4096, 512, 1e-3)],
+    "q4_k_14336x4096_t2048": [Problem("q4_k_14336x4096_t2048", Q4_K, 14336, 4096, 2048, 1e-3)],
+    "f16_5120x17408_t4096_beta1": [Problem("f16_5120x17408_t4096_beta1", F16, 5120, 17408, 4096, 1e-3, 1.0)],
+    "bf16_5120x17408_t4096_beta1": [Problem("bf16_5120x17408_t4096_beta1", BF16, 5120, 17408, 4096, 1e-3, 1.0)],
+    "layer7b_t8192": _layer_sweep(8192),
+}

@@ -1,0 +1,418 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Each test checks the oracle against one of: hand-decoded blocks (fixtures
+under tests/golden, derived from the GGUF block definitions), an independent
+library routine (Python's struct half-float codec, numpy's float16, torch's
+bfloat16), closed forms, a brute-force pure-Python evaluation with exactly
+rounded sums, or an algebraic invariant.  The mutation tests at the end plant
+plausible mistakes in copies of the oracle's steps and check that a pin
+catches each of them.
+"""
+import math
+import os
+import struct
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import quant_out_prod as qop
+from quantized_weight_out_gb300 import inputs
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# ----------------------------------------------------------------------------
+# fixture readers
+
+def _read(golden_dir, name):
+    rows = []
+    with open(os.path.join(golden_dir, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+def _bits_equal(a, b):
+    a = np.asarray(a, dtype=np.float32).view(np.uint32)
+    b = np.asarray(b, dtype=np.float32).view(np.uint32)
+    return np.array_equal(a, b)
+
+
+# ----------------------------------------------------------------------------
+# hand-decoded blocks
+
+def test_q8_0_hand_block(golden_dir):
+    rows = dict((r[0], r[1:]) for r in _read(golden_dir, "q8_0_block.txt"))
+    W = np.frombuffer(bytes.fromhex(rows["hex"][0]), dtype=np.uint8)
+    want = np.array([float(v) for v in rows["values"]], dtype=np.float32)
+    got = oracle.decode_q8_0(W, 1, 32)[0]
+    assert _bits_equal(got, want)
+
+
+def test_q4_0_hand_block_nibble_order_and_negative_zero(golden_dir):
+    rows = dict((r[0], r[1:]) for r in _read(golden_dir, "q4_0_block.txt"))
+    W = np.frombuffer(bytes.fromhex(rows["hex"][0]), dtype=np.uint8)
+    want = np.array([float(v) for v in rows["values"]], dtype=np.float32)
+    got = oracle.decode_q4_0(W, 1, 32)[0]
+    # bitwise: includes the sign of the two zeros (d < 0 times 0 is -0.0)
+    assert _bits_equal(got, want)
+    assert np.signbit(got[8]) and np.signbit(got[23])
+
+
+def _q4_k_fixture(golden_dir):
+    rows = _read(golden_dir, "q4_k_superblock.txt")
+    kv = {}
+    ats, rng = [], None
+    for r in rows:
+        if r[0] == "at":
+            ats.append((int(r[1]), float(r[2])))
+        elif r[0] == "range":
+            rng = (int(r[1]), int(r[2]), float(r[3]))
+        else:
+            kv[r[0]] = r[1:]
+    blk = bytearray(144)
+    blk[0:2] = int(kv["d"][0], 16).to_bytes(2, "little")
+    blk[2:4] = int(kv["dmin"][0], 16).to_bytes(2, "little")
+    blk[4:16] = bytes.fromhex(kv["scales"][0])
+    for c in range(4):
+        for l in range(32):
+            blk[16 + 32 * c + l] = (l % 16) | (((l + c) % 16) << 4)
+    return np.frombuffer(bytes(blk), dtype=np.uint8), kv, ats, rng
+
+
+def test_q4_k_hand_superblock(golden_dir):
+    W, kv, ats, rng = _q4_k_fixture(golden_dir)
+    sc, mn = oracle.q4_k_scale_min(W[4:16])
+    assert list(sc) == [int(v) for v in kv["sc"]]
+    assert list(mn) == [int(v) for v in kv["m"]]
+    y = oracle.decode_q4_k(W, 1, 256)[0]
+    for i, v in ats:
+        assert y[i] == np.float32(v), (i, y[i], v)
+    lo, hi, v = rng
+    assert np.all(y[lo:hi] == np.float32(v))
+    assert math.fsum(float(x) for x in y) == float(kv["sum"][0])
+
+
+def test_half_codes_hand_decoded(golden_dir):
+    for kind, code, val in _read(golden_dir, "half_codes.txt"):
+        bits = np.array([int(code, 16)], dtype=np.uint16)
+        fn = oracle.f16_bits_to_f32 if kind == "f16" else oracle.bf16_bits_to_f32
+        got = fn(bits)[0]
+        assert _bits_equal(got, np.float32(float(val))), (kind, code, got, val)
+
+
+def test_f16_all_codes_against_numpy_and_struct():
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.f16_bits_to_f32(codes)
+    ref = codes.view(np.float16).astype(np.float32)
+    finite = np.isfinite(ref)
+    assert np.array_equal(got[finite].view(np.uint32), ref[finite].view(np.uint32))
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(np.isinf(got), np.isinf(ref))
+    # Python's own binary16 codec, independent of numpy
+    for c in (0x0001, 0x03FF, 0x0400, 0x3C00, 0x7BFF, 0x8001, 0xFBFF, 0xC000, 0x1234):
+        py = struct.unpack("<e", struct.pack("<H", c))[0]
+        assert float(oracle.f16_bits_to_f32(np.array([c], dtype=np.uint16))[0]) == py
+
+
+def test_bf16_all_codes_against_torch():
+    torch = pytest.importorskip("torch")
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.bf16_bits_to_f32(codes)
+    ref = torch.from_numpy(codes.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
+    finite = np.isfinite(ref)
+    assert np.array_equal(got[finite].view(np.uint32), ref[finite].view(np.uint32))
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+
+
+# ----------------------------------------------------------------------------
+# closed forms of the contraction
+
+def _all_ones_weight(wtype, N, K, variant=0):
+    """Every decoded value is 1.0 (variant 1 of Q4_K goes through the min term)."""
+    if wtype == inputs.Q8_0:
+        blk = bytes([0x00, 0x3C]) + bytes([1]) * 32
+        return np.frombuffer(blk * (N * K // 32), dtype=np.uint8)
+    if wtype == inputs.Q4_0:
+        blk = bytes([0x00, 0x3C]) + bytes([0x99]) * 16        # nibble 9 -> 9-8 = 1
+        return np.frombuffer(blk * (N * K // 32), dtype=np.uint8)
+    if wtype == inputs.Q4_K:
+        if variant == 0:   # d = 1, sc = 1, q = 1, dmin = 0
+            S = bytes([1, 1, 1, 1, 0, 0, 0, 0, 1, 1, 1, 1])
+            blk = bytes([0x00, 0x3C, 0x00, 0x00]) + S + bytes([0x11]) * 128
+        else:              # d = 1, sc = 1, q = 2, dmin = 1, m = 1: 2 - 1 = 1
+            S = bytes([1, 1, 1, 1, 1, 1, 1, 1, 0x11, 0x11, 0x11, 0x11])
+            blk = bytes([0x00, 0x3C, 0x00, 0x3C]) + S + bytes([0x22]) * 128
+        return np.frombuffer(blk * (N * K // 256), dtype=np.uint8)
+    if wtype == inputs.F16:
+        return np.frombuffer(bytes([0x00, 0x3C]) * (N * K), dtype=np.uint8)
+    if wtype == inputs.BF16:
+        return np.frombuffer(bytes([0x80, 0x3F]) * (N * K), dtype=np.uint8)
+    raise ValueError(wtype)
+
+
+CASES = [(inputs.Q8_0, 0), (inputs.Q4_0, 0), (inputs.Q4_K, 0), (inputs.Q4_K, 1),
+         (inputs.F16, 0), (inputs.BF16, 0)]
+
+
+@pytest.mark.parametrize("wtype,variant", CASES)
+def test_all_ones_times_one_hot(wtype, variant):
+    N, K, T = 64, 256, 5
+    W = _all_ones_weight(wtype, N, K, variant)
+    assert np.all(oracle.dequant(wtype, W, N, K) == 1.0)
+    dY = np.zeros((T, N), dtype=np.float32)
+    for t in range(T):
+        dY[t, (7 * t + 3) % N] = 1.0
+    assert np.all(oracle.out_prod(wtype, W, N, K, dY, T) == 1.0)
+
+
+@pytest.mark.parametrize("wtype", [inputs.Q8_0, inputs.Q4_0, inputs.Q4_K, inputs.F16, inputs.BF16])
+def test_one_hot_selects_rows(wtype):
+    """One-hot dY[t] = e_{n0(t)} gives dX[t, :] = deq(W)[n0(t), :] exactly:
+    the contraction runs over the rows of W, not its columns."""
+    N, K, T = 48, 512, 6
+    W = inputs.gen_weight(wtype, N, K, seed=5, stream=1)
+    Wd = oracle.dequant(wtype, W, N, K)
+    n0 = [(11 * t + 2) % N for t in range(T)]
+    dY = np.zeros((T, N), dtype=np.float32)
+    for t in range(T):
+        dY[t, n0[t]] = 1.0
+    ref = oracle.out_prod(wtype, W, N, K, dY, T)
+    for t in range(T):
+        assert np.array_equal(ref[t], Wd[n0[t]].astype(np.float64))
+
+
+def test_q4_k_min_path_closed_form():
+    """q = 0 everywhere: dX[t, k] = -sum_n dY[t, n] * dmin_n * m_{n, k // 32}."""
+    N, K, T = 20, 512, 3
+    nb = N * K // 256
+    rng = np.random.default_rng(3)
+    d = inputs.f32_to_f16_bits(np.abs(rng.normal(0, 1e-2, nb)).astype(np.float32))
+    dmin_f = np.abs(rng.normal(0, 1e-2, nb)).astype(np.float32)
+    dmin = inputs.f32_to_f16_bits(dmin_f)
+    sc = rng.integers(0, 64, (nb, 8))
+    m = rng.integers(0, 64, (nb, 8))
+    W = inputs.pack_q4_k(d, dmin, sc, m, np.zeros((nb, 256), dtype=np.int64)).reshape(-1)
+    dY = rng.normal(0, 1, (T, N)).astype(np.float32)
+    dmin_exact = dmin.view(np.float16).astype(np.float64).reshape(N, K // 256)
+    m_r = m.reshape(N, K // 256, 8)
+    want = np.zeros((T, K))
+    for t in range(T):
+        for k in range(K):
+            b, j = divmod(k // 32, 8)
+            want[t, k] = -math.fsum(float(dY[t, n]) * float(dmin_exact[n, b]) * int(m_r[n, b, j])
+                                    for n in range(N))
+    got = oracle.out_prod(inputs.Q4_K, W, N, K, dY, T)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------
+# brute force: an independent pure-Python decode and exactly rounded sums
+
+def _py_f16(b0, b1):
+    return struct.unpack("<e", bytes([b0, b1]))[0]
+
+
+def _py_decode(wtype, raw, N, K):
+    """Per-byte decode written from the block definitions, no numpy."""
+    rb = inputs.row_bytes(wtype, K)
+    out = [[0.0] * K for _ in range(N)]
+    for n in range(N):
+        row = raw[n * rb:(n + 1) * rb]
+        if wtype in (inputs.F16, inputs.BF16):
+            for k in range(K):
+                lo, hi = row[2 * k], row[2 * k + 1]
+                if wtype == inputs.F16:
+                    out[n][k] = _py_f16(lo, hi)
+                else:
+                    out[n][k] = struct.unpack("<f", bytes([0, 0, lo, hi]))[0]
+        elif wtype == inputs.Q8_0:
+            for b in range(K // 32):
+                blk = row[34 * b: 34 * b + 34]
+                d = _py_f16(blk[0], blk[1])
+                for i in range(32):
+                    q = blk[2 + i] - 256 if blk[2 + i] > 127 else blk[2 + i]
+                    out[n][32 * b + i] = d * q
+        elif wtype == inputs.Q4_0:
+            for b in range(K // 32):
+                blk = row[18 * b: 18 * b + 18]
+                d = _py_f16(blk[0], blk[1])
+                for j in range(16):
+                    out[n][32 * b + j] = d * ((blk[2 + j] & 15) - 8)
+                    out[n][32 * b + 16 + j] = d * ((blk[2 + j] >> 4) - 8)
+        elif wtype == inputs.Q4_K:
+            for b in range(K // 256):
+                blk = row[144 * b: 144 * b + 144]
+                d = _py_f16(blk[0], blk[1])
+                dmin = _py_f16(blk[2], blk[3])
+                S = blk[4:16]
+                for j in range(8):
+                    if j < 4:
+                        sc, m = S[j] & 63, S[j + 4] & 63
+                    else:
+                        sc = (S[j + 4] & 15) | ((S[j - 4] >> 6) << 4)
+                        m = (S[j + 4] >> 4) | ((S[j] >> 6) << 4)
+                    c, half = divmod(j, 2)
+                    for l in range(32):
+                        byte = blk[16 + 32 * c + l]
+                        q = (byte >> 4) if half else (byte & 15)
+                        # F32 evaluation: both products exact, one rounding
+                        v = np.float32(np.float32(d * sc) * q) - np.float32(dmin * m)
+                        out[n][256 * b + 64 * c + 32 * half + l] = float(v)
+    return out
+
+
+BRUTE = [(inputs.Q8_0, 40, 64, 3), (inputs.Q4_0, 33, 96, 2), (inputs.Q4_K, 12, 512, 2),
+         (inputs.F16, 24, 40, 3), (inputs.BF16, 24, 40, 3), (inputs.Q8_0, 7, 32, 1)]
+
+
+@pytest.mark.parametrize("wtype,N,K,T", BRUTE)
+def test_brute_force(wtype, N, K, T):
+    W = inputs.gen_weight(wtype, N, K, seed=11, stream=1)
+    dY = inputs.normal_f32(11, 2, T * N, 1.0).reshape(T, N)
+    raw = bytes(W)
+    Wpy = _py_decode(wtype, raw, N, K)
+    Wd = oracle.dequant(wtype, W, N, K)
+    assert _bits_equal(Wd, np.array(Wpy, dtype=np.float32))
+    ref = oracle.out_prod(wtype, W, N, K, dY, T)
+    bnd = oracle.abs_bound(dY, Wd)
+    for t in range(T):
+        for k in range(K):
+            exact = math.fsum(float(dY[t, n]) * Wpy[n][k] for n in range(N))
+            babs = math.fsum(abs(float(dY[t, n]) * Wpy[n][k]) for n in range(N))
+            assert abs(ref[t, k] - exact) <= 1e-12 * babs + 1e-300
+            assert abs(bnd[t, k] - babs) <= 1e-12 * babs + 1e-300
+
+
+# ----------------------------------------------------------------------------
+# invariants
+
+def test_linearity_and_beta():
+    N, K, T = 96, 256, 4
+    W = inputs.gen_weight(inputs.Q4_K, N, K, seed=2, stream=1)
+    Wd = oracle.dequant(inputs.Q4_K, W, N, K)
+    d1 = inputs.normal_f32(2, 2, T * N, 1.0).reshape(T, N)
+    d2 = inputs.normal_f32(2, 3, T * N, 1.0).reshape(T, N)
+    a, b = np.float32(0.5), np.float32(-2.0)   # powers of two keep a*d1 + b*d2 exact-ish
+    lhs = oracle.out_prod(inputs.Q4_K, W, N, K, (a * d1 + b * d2).astype(np.float32), T)
+    rhs = float(a) * oracle.out_prod(inputs.Q4_K, W, N, K, d1, T) + \
+        float(b) * oracle.out_prod(inputs.Q4_K, W, N, K, d2, T)
+    B = oracle.abs_bound(np.abs(a * d1) + np.abs(b * d2), Wd)
+    assert np.all(np.abs(lhs - rhs) <= 1e-6 * B + 1e-12)
+    dX0 = inputs.normal_f32(2, 4, T * K, 1.0).reshape(T, K)
+    beta = 0.75
+    with_beta = oracle.out_prod(inputs.Q4_K, W, N, K, d1, T, dX0, beta)
+    base = oracle.out_prod(inputs.Q4_K, W, N, K, d1, T)
+    assert np.allclose(with_beta, base + beta * dX0.astype(np.float64), rtol=1e-15, atol=0)
+    # beta = 0 never reads dX0, even when it is NaN
+    nan0 = np.full((T, K), np.nan, dtype=np.float32)
+    assert np.array_equal(oracle.out_prod(inputs.Q4_K, W, N, K, d1, T, nan0, 0.0), base)
+
+
+def test_out_prod_at_matches_full():
+    N, K, T = 64, 256, 7
+    W = inputs.gen_weight(inputs.Q8_0, N, K, seed=9, stream=1)
+    dY = inputs.normal_f32(9, 2, T * N, 1.0).reshape(T, N)
+    dX0 = inputs.normal_f32(9, 3, T * K, 1.0).reshape(T, K)
+    Wd = oracle.dequant(inputs.Q8_0, W, N, K)
+    full = oracle.out_prod(inputs.Q8_0, W, N, K, dY, T, dX0, 1.0)
+    bnd = oracle.abs_bound(dY, Wd)
+    ts = np.array([0, 3, 6, 6, 1])
+    ks = np.array([0, 255, 17, 128, 64])
+    ref, b = oracle.out_prod_at(Wd, dY, ts, ks, dX0, 1.0)
+    assert np.allclose(ref, full[ts, ks], rtol=1e-13, atol=1e-15)
+    assert np.allclose(b, bnd[ts, ks], rtol=1e-13)
+
+
+def test_sizes():
+    # the dense F32 copy of a 5120 x 17408 weight: the "356 MB" of the PR's
+    # memory note (llama.cpp fork PR "cuda: out_prod accepts a quantized src0", "What")
+    assert 5120 * 17408 * 4 == 356_515_840
+    # stored row bytes from the block sizes: 34 B / 32, 18 B / 32, 144 B / 256, 2 B / value
+    assert oracle.row_bytes(oracle.Q8_0, 256) == 272
+    assert oracle.row_bytes(oracle.Q4_0, 4096) == 2304
+    assert oracle.row_bytes(oracle.Q4_K, 4096) == 2304
+    assert oracle.row_bytes(oracle.F16, 17408) == 34816
+    assert oracle.row_bytes(oracle.Q8_0, 14336) == 15232
+    assert 256 * 272 == 69_632 and 4096 * 2304 == 9_437_184
+    assert 14336 * 2304 == 33_030_144 and 5120 * 34816 == 178_257_920
+    assert oracle.row_bytes(oracle.Q4_K, 300) == 0 and oracle.row_bytes(oracle.Q8_0, 48) == 0
+
+
+def test_q4_k_pack_roundtrip_through_oracle():
+    rng = np.random.default_rng(0)
+    nb = 50
+    sc = rng.integers(0, 64, (nb, 8))
+    m = rng.integers(0, 64, (nb, 8))
+    blk = inputs.pack_q4_k(np.zeros(nb, np.uint16), np.zeros(nb, np.uint16), sc, m,
+                           rng.integers(0, 16, (nb, 256)))
+    sc2, m2 = oracle.q4_k_scale_min(blk[:, 4:16])
+    assert np.array_equal(sc, sc2) and np.array_equal(m, m2)
+
+
+# ----------------------------------------------------------------------------
+# planted mistakes: each mutant of an oracle step must fail one of the pins
+
+def _mut_q4_0_swapped_nibbles(W, N, K):
+    blk = qop._rows(W, N, K, qop.Q4_0).reshape(N, K // 32, 18)
+    d = qop.f16_bits_to_f32(qop._le16(blk[..., 0], blk[..., 1]))
+    qs = blk[..., 2:18]
+    nib = np.concatenate([qs >> 4, qs & 0x0F], axis=-1).astype(np.float32)
+    return (d[..., None] * (nib - 8)).reshape(N, K)
+
+
+def _mut_q4_0_select_zero(W, N, K):
+    y = qop.decode_q4_0(W, N, K)
+    return np.where(y == 0, np.float32(0.0), y)   # drops the sign of zero
+
+
+def _mut_q4_k_wrong_high_bits(W, N, K):
+    real = qop.q4_k_scale_min
+
+    def bad(S):
+        sc, mn = real(S)
+        S = np.asarray(S, dtype=np.int64)
+        for j in range(4, 8):
+            sc[..., j] = (S[..., j + 4] & 15) | ((S[..., j] >> 6) << 4)   # j instead of j-4
+        return sc, mn
+    qop.q4_k_scale_min = bad
+    try:
+        return qop.decode_q4_k(W, N, K)
+    finally:
+        qop.q4_k_scale_min = real
+
+
+def test_mutants_are_caught(golden_dir):
+    rows = dict((r[0], r[1:]) for r in _read(golden_dir, "q4_0_block.txt"))
+    W = np.frombuffer(bytes.fromhex(rows["hex"][0]), dtype=np.uint8)
+    want = np.array([float(v) for v in rows["values"]], dtype=np.float32)
+    assert not _bits_equal(_mut_q4_0_swapped_nibbles(W, 1, 32)[0], want)
+    assert not _bits_equal(_mut_q4_0_select_zero(W, 1, 32)[0], want)
+    Wk, kv, ats, rng = _q4_k_fixture(golden_dir)
+    yk = _mut_q4_k_wrong_high_bits(Wk, 1, 256)[0]
+    assert any(yk[i] != np.float32(v) for i, v in ats)
+
+
+def test_transposed_contraction_is_caught():
+    """Contracting over K (dY @ deq(W).T) instead of N breaks the one-hot pin."""
+    N, K, T = 32, 32, 3
+    W = inputs.gen_weight(inputs.Q8_0, N, K, seed=5, stream=1)
+    Wd = oracle.dequant(inputs.Q8_0, W, N, K)
+    dY = np.zeros((T, N), dtype=np.float32)
+    dY[0, 4] = dY[1, 9] = dY[2, 30] = 1.0
+    wrong = dY.astype(np.float64) @ Wd.T.astype(np.float64)
+    assert not all(np.array_equal(wrong[t], Wd[n].astype(np.float64))
+                   for t, n in enumerate([4, 9, 30]))
+
+
+def test_dropped_beta_is_caught():
+    N, K, T = 32, 256, 2
+    W = inputs.gen_weight(inputs.Q4_K, N, K, seed=5, stream=1)
+    dY = inputs.normal_f32(5, 2, T * N, 1.0).reshape(T, N)
+    dX0 = inputs.normal_f32(5, 3, T * K, 1.0).reshape(T, K)
+    good = oracle.out_prod(inputs.Q4_K, W, N, K, dY, T, dX0, 1.0)
+    dropped = oracle.out_prod(inputs.Q4_K, W, N, K, dY, T)
+    assert not np.allclose(good, dropped)
