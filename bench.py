@@ -1,0 +1,355 @@
+"""Throughput of the quantized-weight OUT_PROD on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of every call of the workload (default: the backward of
+the seven projections of a 7B-shaped decoder layer at T = 8192 tokens: q/k/v/o
+and gate/up in Q4_K, down in Q8_0), each call one rg_out_prod through the C
+ABI with inputs resident in HBM.  Prints one JSON line (rank 0).
+
+  value       whole-job TFLOP/s = sum 2*T*N*K over the step / step time
+  e2e         the same with host inputs: pinned host -> device copies of W
+              and dY and the device -> host copy of dX inside the timed loop
+  roofline    the tensor-core kernel's achieved TFLOP/s over the measured
+              dense bf16/fp16 peak (MEASURED_PEAKS.json, sustained figure)
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload
+
+--impl reference times the CPU oracle itself (the only baseline this method
+has; its pages publish no GPU throughput) on a bounded sample per step.
+Multi-GPU (torchrun): every rank runs its own replica of the workload
+(replicas only: the calls are independent); the step time is the max over
+ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantized_weight_out_gb300 import inputs  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "pci.bus_id,utilization.gpu")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = bus_id
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            c = [x.strip() for x in line.split(",")]
+            if len(c) < 10:
+                continue
+            if self.bus_id and self.bus_id.lower() not in c[8].lower():
+                continue
+            rows.append(c)
+        if not rows:
+            return None
+        load = [r for r in rows if r[9].isdigit() and int(r[9]) > 50] or rows
+        sm = [float(r[0]) for r in load if r[0].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in load for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(load[0][1]) if load[0][1].replace(".", "").isdigit() else None,
+                "reasons": reasons, "samples": len(load),
+                "power_w_max": max(float(r[2]) for r in load if r[2].replace(".", "").isdigit())}
+
+
+def _bus_id(torch, dev):
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample
+
+def oracle_sample(problems, rows: int):
+    """Time the oracle as it stands on the first `rows` rows of dY of every
+    call: decode each W (oracle.dequant), then contract (oracle.out_prod).
+    Returns (flops done, seconds, description)."""
+    import oracle
+    data = []
+    for p in problems:
+        W = p.weight()
+        dY = p.dy()[:rows].copy()
+        dX0 = p.dx0()
+        data.append((p, W, dY, None if dX0 is None else dX0[:rows].copy()))
+    t0 = time.perf_counter()
+    flops = 0
+    for p, W, dY, dX0 in data:
+        Wd = oracle.dequant(p.wtype, W, p.N, p.K)
+        oracle.out_prod(p.wtype, W, p.N, p.K, dY, rows, dX0, p.beta, Wd=Wd)
+        flops += 2 * rows * p.N * p.K
+    dt = time.perf_counter() - t0
+    return flops, dt, f"every call of the workload, first {rows} rows of dY, full decode of W"
+
+
+# ---------------------------------------------------------------------------
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="layer7b_t8192", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=64, help="dY rows per call in the CPU sample")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _dtype_name(problems):
+    return "bf16" if all(p.wtype == inputs.BF16 for p in problems) else \
+        "f16" if all(p.wtype != inputs.BF16 for p in problems) else "f16+bf16"
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    problems = inputs.WORKLOADS[args.workload]
+    rows = args.cpu_rows
+    for _ in range(args.warmup):
+        oracle_sample(problems, rows)
+    times, flops = [], 0
+    for _ in range(args.steps):
+        f, dt, desc = oracle_sample(problems, rows)
+        times.append(dt)
+        flops = f
+    ms = 1e3 * sum(times) / len(times)
+    value = flops / (ms * 1e-3) / 1e12
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": "out_prod TFLOP/s (2*T*N*K / time)", "value": value,
+            "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "sample_rows_per_call": rows},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = _dist()
+    from quantized_weight_out_gb300 import binding as rg
+    from quantized_weight_out_gb300 import build as rgbuild
+    rgbuild.build()
+    rg.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    problems = inputs.WORKLOADS[args.workload]
+
+    # inputs: generated on the host, pinned copies for the end-to-end leg,
+    # device copies resident for the kernel leg
+    host, devbuf = [], []
+    for p in problems:
+        W = torch.from_numpy(p.weight()).pin_memory()
+        dY = torch.from_numpy(p.dy()).pin_memory()
+        dX0 = p.dx0()
+        dXh = torch.empty((p.T, p.K), dtype=torch.float32).pin_memory()
+        host.append((W, dY, dXh))
+        devbuf.append((W.to(dev), dY.to(dev),
+                       torch.from_numpy(dX0).to(dev) if dX0 is not None
+                       else torch.zeros((p.T, p.K), device=dev)))
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    variants = [rg.rg_select_variant(p.wtype, p.N, p.K, p.T) for p in problems]
+
+    def step(events=None):
+        for i, p in enumerate(problems):
+            W, dY, dX = devbuf[i]
+            if events is not None:
+                events[i][0].record(stream)
+            st = rg.rg_out_prod(p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, stream)
+            if events is not None:
+                events[i][1].record(stream)
+            if st != 0:
+                raise RuntimeError(f"rg_out_prod: {rg.strerror(st)}")
+
+    for _ in range(args.warmup):
+        step()
+    rg.check(rg.rg_check(stream), "warmup")
+
+    per_call = [[] for _ in problems]
+    sampler = ClockSampler(_bus_id(torch, dev))
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+            for _ in problems] for _ in range(args.steps)]
+    ev0.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    rg.check(rg.rg_check(stream), "timed region")
+    ms_total = ev0.elapsed_time(ev1)
+    for s in range(args.steps):
+        for i in range(len(problems)):
+            per_call[i].append(evs[s][i][0].elapsed_time(evs[s][i][1]))
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    flops_step = sum(p.flops for p in problems)
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+
+    # end to end: host buffers, copies inside the timed loop
+    e2e = None
+    if not args.no_e2e:
+        h2d = sum(h[0].numel() * h[0].element_size() + h[1].numel() * 4 for h in host)
+        d2h = sum(p.T * p.K * 4 for p in problems)
+
+        def e2e_step():
+            for i, p in enumerate(problems):
+                W, dY, dX = devbuf[i]
+                W.copy_(host[i][0], non_blocking=True)
+                dY.copy_(host[i][1], non_blocking=True)
+                st = rg.rg_out_prod(p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, stream)
+                if st != 0:
+                    raise RuntimeError(rg.strerror(st))
+                host[i][2].copy_(dX, non_blocking=True)
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1) / args.steps
+        if world > 1:
+            t = torch.tensor([ems], device=dev, dtype=torch.float64)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * flops_step / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems}
+
+    # roofline of the tensor-core launches (the dominant kernel)
+    peaks, src = _peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    tc = [i for i, v in enumerate(variants) if v == rg.RG_VARIANT_TC]
+    tc_flops = sum(problems[i].flops for i in tc)
+    tc_ms = sum(statistics.mean(per_call[i]) for i in tc) if tc else 0.0
+    achieved = tc_flops / (tc_ms * 1e-3) / 1e12 if tc_ms > 0 else None
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak if achieved else None, "traffic": None,
+            "peak_source": f"{src} bf16_tflops_sustained (dense fp16 = bf16 nominal)",
+            "kernel": "rg_out_prod tensor-core launches (dY conversion + fused decode GEMM)"}
+
+    calls = []
+    for i, p in enumerate(problems):
+        t = statistics.median(per_call[i]) * 1e-3
+        calls.append({"name": p.name, "wtype": inputs.TYPE_NAMES[p.wtype], "N": p.N, "K": p.K,
+                      "T": p.T, "variant": int(variants[i]), "ms": t * 1e3,
+                      "tflops": p.flops / t / 1e12,
+                      "effective_gbs": p.algorithmic_bytes() / t / 1e9,
+                      "roofline_frac": max(p.flops / (peak * 1e12),
+                                           p.algorithmic_bytes() / (peaks["hbm_gbs"] * 1e9)) / t})
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        f, dt, desc = oracle_sample(problems, args.cpu_rows)
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+               "kind": "oracle", "sample": desc, "seconds": dt}
+
+    launches_per_call = {rg.RG_VARIANT_TC: 2, rg.RG_VARIANT_SMALLT: 1, rg.RG_VARIANT_SIMT32: 1}
+    gpu_launches = args.steps * sum(launches_per_call[v] for v in variants)
+    step_bytes = sum(p.algorithmic_bytes() for p in problems)
+    line = {
+        "metric": "out_prod TFLOP/s (2*T*N*K / time)", "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": _dtype_name(problems), "data": "synthetic",
+        "config": {"workload": args.workload, "calls": len(problems),
+                   "flops_per_step": flops_step, "algorithmic_bytes_per_step": step_bytes,
+                   "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step > 129 MB); no flush",
+                   "parallelism": f"replicas x{world}"},
+        "effective_gbs": world * step_bytes / (ms_step * 1e-3) / 1e9,
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
+        "clocks": clocks, "per_call": calls,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

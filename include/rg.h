@@ -1,0 +1,160 @@
+/*
+ * rg.h - activation-gradient OUT_PROD through a resident quantized or
+ * half-precision weight, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation.  The llama.cpp fork's PR "cuda: out_prod accepts a quantized
+ * src0" (commit message and section "What") gives the backward of
+ * mul_mat(W, x) with respect to x as out_prod(W, grad^T), taken over every
+ * quantized, F16 and BF16 src0 with F32 src1/dst.  With W stored as N rows of
+ * K values (blocks run along K) and the incoming gradient dY of shape [T, N]:
+ *
+ *     dX[t, k] = beta * dX[t, k] + sum_{n < N} dY[t, n] * deq(W)[n, k]
+ *
+ * deq() is the block decode of the weight's storage type (rg_dequant).  The
+ * PR's route copies deq(W) to a dense F32 pool buffer and runs SGEMM on it;
+ * the Retrograd page "CUDA status", section "Limitations", adds a budgeted,
+ * sliced version of that copy and an in-place decoder for small outputs.
+ * This library instead decodes the packed blocks inside the GEMM, straight
+ * into tensor-core operand tiles, so no dense copy of W ever exists.
+ *
+ * Conventions for every call below.
+ *  - Pointers to data are DEVICE pointers (cudaMalloc / PyTorch storage) and
+ *    stay owned by the caller; the library never frees or retains them.
+ *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream.  Work is enqueued asynchronously; nothing here synchronizes
+ *    except rg_check and the blocking variants named as such.
+ *  - Arguments are validated on the host before anything is enqueued; on any
+ *    error status nothing has been launched and outputs are untouched.
+ *  - Layouts: W is N rows of rg_row_bytes(wtype, K) bytes each, rows
+ *    contiguous; dY is [T, N] row-major F32; dX and `out` are [T, K] and
+ *    [N, K] row-major F32.  W, dY, dX and out must be 16-byte aligned.
+ *  - Sizes: 0 <= T, N, K <= 2^31 - 1.  T == 0 or K == 0 is an empty output
+ *    (RG_OK, nothing launched, pointers may be NULL).  N == 0 is an empty
+ *    contraction: dX = beta * dX (dX = 0 when beta == 0).
+ *  - K must be a multiple of 256 for Q8_0, Q4_0 and Q4_K (whole 256-value
+ *    tiles of every block type) and a multiple of 8 for F16 and BF16
+ *    (16-byte rows); otherwise RG_ERR_SHAPE.
+ *  - Every device-side wait is bounded (about 2 s); a wait that gives up
+ *    records RG_ERR_TIMEOUT in a per-device status word that rg_check reads.
+ */
+#ifndef RG_H
+#define RG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Weight storage types (ggml's GGUF block types of the same names). */
+typedef enum {
+    RG_F16 = 1,   /* IEEE binary16, 2 B per value                                   */
+    RG_BF16 = 2,  /* bfloat16, 2 B per value                                         */
+    RG_Q8_0 = 3,  /* 34 B / 32 values: fp16 d, int8 q[32]; value d*q                 */
+    RG_Q4_0 = 4,  /* 18 B / 32 values: fp16 d, 16 B nibbles (lo = j, hi = j+16);
+                     value d*(q-8)                                                   */
+    RG_Q4_K = 5   /* 144 B / 256 values: fp16 d, fp16 dmin, 12 B of 6-bit (sc, m)
+                     for 8 sub-blocks of 32, 128 B nibbles; value d*sc*q - dmin*m    */
+} rg_wtype;
+
+typedef enum {
+    RG_OK = 0,
+    RG_ERR_ARG = -1,     /* NULL pointer where data is needed, negative or too large size */
+    RG_ERR_TYPE = -2,    /* unknown wtype, or unknown variant                              */
+    RG_ERR_SHAPE = -3,   /* K not a multiple of 256 (quantized) or 8 (F16/BF16)            */
+    RG_ERR_ALIGN = -4,   /* W, dY, dX or out not 16-byte aligned                           */
+    RG_ERR_CUDA = -5,    /* a CUDA runtime/driver call or a launch failed                  */
+    RG_ERR_TIMEOUT = -6  /* a bounded device-side wait gave up (reported by rg_check)      */
+} rg_status;
+
+/* Kernel variants of rg_out_prod_variant. */
+typedef enum {
+    RG_VARIANT_AUTO = 0,   /* the shape dispatcher's choice (what rg_out_prod runs)        */
+    RG_VARIANT_TC = 1,     /* fused decode + tcgen05 tensor-core GEMM, fp16/bf16 operands,
+                              F32 accumulation in tensor memory                             */
+    RG_VARIANT_SMALLT = 2, /* small-T, weight-bandwidth-bound: coalesced 16-byte weight
+                              loads, decode in registers, F32 FMA, cluster reduction        */
+    RG_VARIANT_SIMT32 = 3  /* exact F32 decode and F32 FMA with blocked accumulation: the
+                              full-precision variant (slow; a correctness reference)        */
+} rg_variant;
+
+/*
+ * dX = beta * dX + dY . deq(W)   (see the top of this file).
+ *
+ * wtype: rg_wtype.  W: N * rg_row_bytes(wtype, K) bytes.  dY: [T, N] F32.
+ * dX: [T, K] F32, read only when beta != 0 (with beta == 0 its old contents,
+ * NaN included, are ignored).  The variant is chosen from (wtype, T, N, K);
+ * the environment variable RG_VARIANT=auto|tc|smallt|simt32, read once per
+ * process, overrides that choice.  Asynchronous on `stream`.
+ *
+ * Scratch: the tensor-core variant converts dY once to fp16/bf16 in a device
+ * workspace of rg_workspace_bytes() bytes.  rg_out_prod takes it
+ * stream-ordered from a per-device memory pool owned by the library
+ * (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`); the pool keeps its
+ * memory, so only the first call of a given size reaches the driver.  Use
+ * rg_out_prod_ws to supply the workspace and allocate nothing at all.
+ */
+int rg_out_prod(int wtype, const void* W, int64_t N, int64_t K,
+                const float* dY, int64_t T, float* dX, float beta, void* stream);
+
+/* rg_out_prod with an explicit variant (rg_variant; RG_VARIANT_AUTO = dispatch).
+ * RG_VARIANT ignored.  Same contract as rg_out_prod. */
+int rg_out_prod_variant(int variant, int wtype, const void* W, int64_t N, int64_t K,
+                        const float* dY, int64_t T, float* dX, float beta, void* stream);
+
+/* Device workspace bytes that rg_out_prod_ws needs for this call (0 if none). */
+size_t rg_workspace_bytes(int variant, int wtype, int64_t N, int64_t K, int64_t T);
+
+/* rg_out_prod_variant with a caller-owned device workspace of at least
+ * rg_workspace_bytes(variant, wtype, N, K, T) bytes, 256-byte aligned
+ * (RG_ERR_ARG if smaller, RG_ERR_ALIGN if misaligned).  Allocates nothing and
+ * does not synchronize.  Calls that share a workspace must be ordered on
+ * one stream. */
+int rg_out_prod_ws(int variant, int wtype, const void* W, int64_t N, int64_t K,
+                   const float* dY, int64_t T, float* dX, float beta,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* The variant RG_VARIANT_AUTO picks for this shape (ignores RG_VARIANT). */
+int rg_select_variant(int wtype, int64_t N, int64_t K, int64_t T);
+
+/*
+ * out[n, k] = deq(W)[n, k] as F32, bit-exact: every decoded value is an exact
+ * F32 (Q8_0: 11-bit x 8-bit product; Q4_0: 11-bit x 4-bit; F16/BF16: widened)
+ * except Q4_K, whose (d*sc)*q - dmin*m is rounded once, to nearest even.
+ * Signed zeros are kept (d < 0 times a zero code is -0.0).  This is the role
+ * of the PR's ggml_get_to_fp32_cuda converters.  Enqueued on the legacy
+ * default stream; out: [N, K] F32, 16-byte aligned.
+ */
+int rg_dequant(int wtype, const void* W, int64_t N, int64_t K, float* out);
+
+/* rg_dequant on `stream`. */
+int rg_dequant_async(int wtype, const void* W, int64_t N, int64_t K, float* out, void* stream);
+
+/* Stored bytes of one row of K values: K/32*34 (Q8_0), K/32*18 (Q4_0),
+ * K/256*144 (Q4_K), 2K (F16, BF16); 0 for an unknown type or a K that is not
+ * a whole number of blocks. */
+size_t rg_row_bytes(int wtype, int64_t K);
+
+/* Static, NUL-terminated description of a status code. */
+const char* rg_strerror(int status);
+
+/* Synchronizes `stream`, then reads and clears the current device's status
+ * word.  Returns RG_ERR_TIMEOUT if a kernel gave up a bounded wait since the
+ * last check, RG_ERR_CUDA if the stream reports an error, else RG_OK. */
+int rg_check(void* stream);
+
+/* Library version, (major << 16) | minor. */
+int rg_version(void);
+
+/* Test hook for failure detection: enqueues one kernel whose single wait can
+ * never complete, so that it gives up after timeout_ms (1..60000; else
+ * RG_ERR_ARG) and records RG_ERR_TIMEOUT for the next rg_check.  The context
+ * stays usable. */
+int rg_debug_wait_probe(int timeout_ms, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RG_H */

@@ -1,0 +1,317 @@
+// rg_api.cu - the C ABI of librg: argument validation, the T/N/K shape
+// dispatcher, per-device state (status word, SM count), workspaces and the
+// tensor-map encoder.  Every compute step runs in the kernels of the other
+// translation units; nothing here touches the data.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "rg_internal.cuh"
+#include "rg_launch.h"
+
+namespace rg {
+
+// The per-device status word: a kernel that gives up a bounded wait records
+// RG_ERR_TIMEOUT here; rg_check reads and clears it.
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxDim = 2147483647;
+
+std::mutex g_mu;
+bool g_dev_ready[kMaxDevices];
+DevInfo g_dev[kMaxDevices];
+
+struct Env {
+  int variant = RG_VARIANT_AUTO;
+  unsigned long long wait_limit_ns = 2000ull * 1000 * 1000;
+  int inject_stall = 0;
+};
+
+const Env& env() {
+  static const Env e = [] {
+    Env r;
+    if (const char* v = std::getenv("RG_VARIANT")) {
+      if (!std::strcmp(v, "tc")) r.variant = RG_VARIANT_TC;
+      else if (!std::strcmp(v, "smallt")) r.variant = RG_VARIANT_SMALLT;
+      else if (!std::strcmp(v, "simt32")) r.variant = RG_VARIANT_SIMT32;
+    }
+    if (const char* v = std::getenv("RG_WAIT_TIMEOUT_MS")) {
+      const long long ms = std::atoll(v);
+      if (ms > 0) r.wait_limit_ns = static_cast<unsigned long long>(ms) * 1000000ull;
+    }
+    if (const char* v = std::getenv("RG_DEBUG_INJECT_STALL")) r.inject_stall = std::atoi(v) != 0;
+    return r;
+  }();
+  return e;
+}
+
+// Facts about the current device, queried once per device.
+int current_dev(DevInfo** out) {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return RG_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_dev_ready[d]) {
+    DevInfo info{};
+    info.device = d;
+    if (cudaDeviceGetAttribute(&info.num_sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess)
+      return RG_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&info.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                               d) != cudaSuccess)
+      return RG_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return RG_ERR_CUDA;
+    info.status = static_cast<int*>(p);
+    info.wait_limit_ns = env().wait_limit_ns;
+    g_dev[d] = info;
+    g_dev_ready[d] = true;
+  }
+  *out = &g_dev[d];
+  return RG_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t row_bytes_i(int wtype, int64_t K) {
+  if (wtype < RG_F16 || wtype > RG_Q4_K || K < 0) return 0;
+  const int bv = block_values(wtype);
+  if (K % bv) return 0;
+  return K / bv * block_bytes(wtype);
+}
+
+// Shared validation of the OUT_PROD arguments.  Returns RG_OK and sets
+// *empty when there is nothing to launch.
+int validate(int wtype, const void* W, int64_t N, int64_t K, const float* dY, int64_t T,
+             const float* dX, bool* empty) {
+  *empty = false;
+  if (wtype < RG_F16 || wtype > RG_Q4_K) return RG_ERR_TYPE;
+  if (N < 0 || K < 0 || T < 0 || N > kMaxDim || K > kMaxDim || T > kMaxDim) return RG_ERR_ARG;
+  const int64_t kmul = is_quant(wtype) ? 256 : 8;
+  if (K % kmul) return RG_ERR_SHAPE;
+  if (T == 0 || K == 0) {
+    *empty = true;
+    return RG_OK;
+  }
+  if (!dX) return RG_ERR_ARG;
+  if (!aligned16(dX)) return RG_ERR_ALIGN;
+  if (N > 0) {
+    if (!W || !dY) return RG_ERR_ARG;
+    if (!aligned16(W) || !aligned16(dY)) return RG_ERR_ALIGN;
+  }
+  return RG_OK;
+}
+
+int select_variant(int wtype, int64_t N, int64_t K, int64_t T) {
+  (void)wtype;
+  (void)N;
+  (void)K;
+  if (T <= 32) return RG_VARIANT_SMALLT;
+  return RG_VARIANT_TC;
+}
+
+size_t tc_workspace(int64_t N, int64_t T) {
+  const size_t b = static_cast<size_t>(T) * static_cast<size_t>(tc_dy16_ld(N)) * 2;
+  return (b + 255) / 256 * 256;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? RG_OK : RG_ERR_CUDA; }
+
+// One stream-ordered memory pool per device for rg_out_prod's own workspace:
+// allocations are cached by the pool (release threshold: never), so a steady
+// state of calls does not reach the driver, and stream capture records them as
+// graph memory nodes.
+cudaMemPool_t g_pool[kMaxDevices];
+bool g_pool_ready[kMaxDevices];
+
+int pool_for(int d, cudaMemPool_t* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_pool_ready[d]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = d;
+    if (cudaMemPoolCreate(&g_pool[d], &props) != cudaSuccess) return RG_ERR_CUDA;
+    uint64_t keep = ~0ull;
+    if (cudaMemPoolSetAttribute(g_pool[d], cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess)
+      return RG_ERR_CUDA;
+    g_pool_ready[d] = true;
+  }
+  *out = g_pool[d];
+  return RG_OK;
+}
+
+int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float* dY, int64_t T,
+        float* dX, float beta, void* ws, size_t ws_bytes, bool own_ws, cudaStream_t stream) {
+  bool empty = false;
+  int st = validate(wtype, W, N, K, dY, T, dX, &empty);
+  if (st != RG_OK || empty) return st;
+  if (variant < RG_VARIANT_AUTO || variant > RG_VARIANT_SIMT32) return RG_ERR_TYPE;
+  DevInfo* dev = nullptr;
+  if ((st = current_dev(&dev)) != RG_OK) return st;
+  if (N == 0) return from_cuda(launch_scale(dX, T * K, beta, *dev, stream));
+  if (variant == RG_VARIANT_AUTO) variant = select_variant(wtype, N, K, T);
+
+  switch (variant) {
+    case RG_VARIANT_SIMT32:
+      return from_cuda(launch_simt32(wtype, W, N, K, dY, T, dX, beta, *dev, stream));
+    case RG_VARIANT_SMALLT:
+      return from_cuda(launch_smallt(wtype, W, N, K, dY, T, dX, beta, *dev, stream));
+    default:
+      break;
+  }
+  // tensor-core path: dY -> 16-bit operand copy, then the fused GEMM
+  const size_t need = tc_workspace(N, T);
+  void* buf = ws;
+  cudaMemPool_t pool{};
+  if (own_ws) {
+    if ((st = pool_for(dev->device, &pool)) != RG_OK) return st;
+    if (cudaMallocFromPoolAsync(&buf, need, pool, stream) != cudaSuccess) return RG_ERR_CUDA;
+  } else {
+    if (!ws || ws_bytes < need) return RG_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return RG_ERR_ALIGN;
+  }
+  const bool bf16 = wtype == RG_BF16;
+  const int64_t ld = tc_dy16_ld(N);
+  cudaError_t e = launch_convert_dy(dY, T, N, ld, bf16, static_cast<uint16_t*>(buf), *dev, stream);
+  if (e == cudaSuccess)
+    e = launch_tc(wtype, W, N, K, static_cast<const uint16_t*>(buf), ld, T, dX, beta, *dev,
+                  stream, env().inject_stall);
+  if (own_ws) {
+    const cudaError_t f = cudaFreeAsync(buf, stream);
+    if (e == cudaSuccess) e = f;
+  }
+  return from_cuda(e);
+}
+
+}  // namespace
+
+CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                      uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes, uint32_t box0,
+                      uint32_t box1, CUtensorMapSwizzle swizzle) {
+  using Fn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                          const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                          CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                          CUtensorMapFloatOOBfill);
+  static Fn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<Fn>(p);
+  }();
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  const cuuint64_t dims[2] = {dim0, dim1};
+  const cuuint64_t strides[1] = {stride1_bytes};
+  const cuuint32_t box[2] = {box0, box1};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace rg
+
+using namespace rg;
+
+extern "C" {
+
+int rg_out_prod(int wtype, const void* W, int64_t N, int64_t K, const float* dY, int64_t T,
+                float* dX, float beta, void* stream) {
+  return run(env().variant, wtype, W, N, K, dY, T, dX, beta, nullptr, 0, true,
+             static_cast<cudaStream_t>(stream));
+}
+
+int rg_out_prod_variant(int variant, int wtype, const void* W, int64_t N, int64_t K,
+                        const float* dY, int64_t T, float* dX, float beta, void* stream) {
+  return run(variant, wtype, W, N, K, dY, T, dX, beta, nullptr, 0, true,
+             static_cast<cudaStream_t>(stream));
+}
+
+size_t rg_workspace_bytes(int variant, int wtype, int64_t N, int64_t K, int64_t T) {
+  if (variant == RG_VARIANT_AUTO) variant = select_variant(wtype, N, K, T);
+  if (variant != RG_VARIANT_TC || N <= 0 || T <= 0 || K <= 0) return 0;
+  return tc_workspace(N, T);
+}
+
+int rg_out_prod_ws(int variant, int wtype, const void* W, int64_t N, int64_t K, const float* dY,
+                   int64_t T, float* dX, float beta, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  return run(variant, wtype, W, N, K, dY, T, dX, beta, workspace, workspace_bytes, false,
+             static_cast<cudaStream_t>(stream));
+}
+
+int rg_select_variant(int wtype, int64_t N, int64_t K, int64_t T) {
+  return select_variant(wtype, N, K, T);
+}
+
+int rg_dequant_async(int wtype, const void* W, int64_t N, int64_t K, float* out, void* stream) {
+  if (wtype < RG_F16 || wtype > RG_Q4_K) return RG_ERR_TYPE;
+  if (N < 0 || K < 0 || N > kMaxDim || K > kMaxDim) return RG_ERR_ARG;
+  const int64_t kmul = is_quant(wtype) ? 256 : 8;
+  if (K % kmul) return RG_ERR_SHAPE;
+  if (N == 0 || K == 0) return RG_OK;
+  if (!W || !out) return RG_ERR_ARG;
+  if (!aligned16(W) || !aligned16(out)) return RG_ERR_ALIGN;
+  DevInfo* dev = nullptr;
+  int st = current_dev(&dev);
+  if (st != RG_OK) return st;
+  return from_cuda(launch_dequant(wtype, W, N, K, out, *dev, static_cast<cudaStream_t>(stream)));
+}
+
+int rg_dequant(int wtype, const void* W, int64_t N, int64_t K, float* out) {
+  return rg_dequant_async(wtype, W, N, K, out, nullptr);
+}
+
+size_t rg_row_bytes(int wtype, int64_t K) {
+  return static_cast<size_t>(row_bytes_i(wtype, K));
+}
+
+const char* rg_strerror(int status) {
+  switch (status) {
+    case RG_OK: return "ok";
+    case RG_ERR_ARG: return "invalid argument (null pointer, negative or too large size, small workspace)";
+    case RG_ERR_TYPE: return "unknown weight type or variant";
+    case RG_ERR_SHAPE: return "K is not a multiple of 256 (quantized types) or 8 (F16/BF16)";
+    case RG_ERR_ALIGN: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case RG_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case RG_ERR_TIMEOUT: return "a bounded device-side wait gave up";
+    default: return "unknown status";
+  }
+}
+
+int rg_check(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return RG_ERR_CUDA;
+  DevInfo* dev = nullptr;
+  int st = current_dev(&dev);
+  if (st != RG_OK) return st;
+  int v = 0;
+  if (cudaMemcpy(&v, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return RG_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return RG_ERR_CUDA;
+  }
+  return v;
+}
+
+int rg_debug_wait_probe(int timeout_ms, void* stream) {
+  if (timeout_ms <= 0 || timeout_ms > 60000) return RG_ERR_ARG;
+  DevInfo* dev = nullptr;
+  int st = current_dev(&dev);
+  if (st != RG_OK) return st;
+  return from_cuda(launch_wait_probe(*dev, static_cast<unsigned long long>(timeout_ms) * 1000000ull,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+int rg_version(void) { return (0 << 16) | 1; }
+
+}  // extern "C"

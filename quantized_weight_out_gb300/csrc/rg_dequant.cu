@@ -1,0 +1,140 @@
+// rg_dequant.cu - elementwise kernels: the bit-exact block decode to F32
+// (rg_dequant), the dY -> fp16/bf16 operand conversion of the tensor-core
+// path, the N == 0 scale, and the bounded-wait probe.
+//
+// The decode is the role of the converters that the llama.cpp fork's PR
+// "cuda: out_prod accepts a quantized src0" (section "What") runs before its
+// SGEMM (ggml_get_to_fp32_cuda); here it is a stand-alone call whose output
+// must equal the format definition bit for bit.
+#include <algorithm>
+
+#include "rg_internal.cuh"
+#include "rg_launch.h"
+
+namespace rg {
+
+// One thread per 8 consecutive values of a row: decode, two 16-byte stores.
+template <int WT>
+__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict__ W, int64_t N,
+                                                      int64_t K, int64_t rb,
+                                                      float* __restrict__ out) {
+  const int64_t gpr = K >> 3;  // 8-value groups per row
+  const int64_t total = N * gpr;
+  for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t n = g / gpr;
+    const int k0 = static_cast<int>(g - n * gpr) << 3;
+    float v[8];
+    decode8_f32<WT>(W + n * rb, k0, v);
+    float4* o = reinterpret_cast<float4*>(out + n * K + k0);
+    o[0] = make_float4(v[0], v[1], v[2], v[3]);
+    o[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+}
+
+static int grid_for(int64_t work_items, int threads, const DevInfo& dev) {
+  const int64_t blocks = (work_items + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
+  return static_cast<int>(std::max<int64_t>(1, std::min(blocks, cap)));
+}
+
+cudaError_t launch_dequant(int wtype, const void* W, int64_t N, int64_t K, float* out,
+                           const DevInfo& dev, cudaStream_t stream) {
+  const int64_t rb = K / block_values(wtype) * block_bytes(wtype);
+  const int grid = grid_for(N * (K >> 3), 256, dev);
+  const uint8_t* w = static_cast<const uint8_t*>(W);
+  switch (wtype) {
+    case RG_F16: dequant_kernel<RG_F16><<<grid, 256, 0, stream>>>(w, N, K, rb, out); break;
+    case RG_BF16: dequant_kernel<RG_BF16><<<grid, 256, 0, stream>>>(w, N, K, rb, out); break;
+    case RG_Q8_0: dequant_kernel<RG_Q8_0><<<grid, 256, 0, stream>>>(w, N, K, rb, out); break;
+    case RG_Q4_0: dequant_kernel<RG_Q4_0><<<grid, 256, 0, stream>>>(w, N, K, rb, out); break;
+    case RG_Q4_K: dequant_kernel<RG_Q4_K><<<grid, 256, 0, stream>>>(w, N, K, rb, out); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// dY [T, N] F32 -> [T, ld] 16-bit, round to nearest even.  One thread per 8
+// values; 16-byte loads when every row is 16-byte aligned (N % 4 == 0).
+template <bool BF16>
+__global__ void __launch_bounds__(256) convert_dy_kernel(const float* __restrict__ dY, int64_t T,
+                                                         int64_t N, int64_t ld,
+                                                         uint16_t* __restrict__ out) {
+  const int64_t cpr = (N + 7) >> 3;
+  const int64_t total = T * cpr;
+  const bool vec = (N & 3) == 0;
+  for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = g / cpr;
+    const int64_t n0 = (g - t * cpr) << 3;
+    const float* src = dY + t * N + n0;
+    float v[8];
+    if (vec && n0 + 8 <= N) {
+      const float4 a = __ldcs(reinterpret_cast<const float4*>(src));
+      const float4 b = __ldcs(reinterpret_cast<const float4*>(src) + 1);
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+      v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = (n0 + i < N) ? src[i] : 0.0f;
+    }
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (BF16) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h);
+      } else {
+        const __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+    }
+    *reinterpret_cast<uint4*>(out + t * ld + n0) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t ld, bool bf16,
+                              uint16_t* out, const DevInfo& dev, cudaStream_t stream) {
+  const int grid = grid_for(T * ((N + 7) >> 3), 256, dev);
+  if (bf16)
+    convert_dy_kernel<true><<<grid, 256, 0, stream>>>(dY, T, N, ld, out);
+  else
+    convert_dy_kernel<false><<<grid, 256, 0, stream>>>(dY, T, N, ld, out);
+  return cudaGetLastError();
+}
+
+__global__ void __launch_bounds__(256) scale_kernel(float* __restrict__ x, int64_t count,
+                                                    float beta) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < count;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    x[i] = beta == 0.0f ? 0.0f : beta * x[i];
+}
+
+cudaError_t launch_scale(float* dX, int64_t count, float beta, const DevInfo& dev,
+                         cudaStream_t stream) {
+  scale_kernel<<<grid_for(count, 256, dev), 256, 0, stream>>>(dX, count, beta);
+  return cudaGetLastError();
+}
+
+// One thread waits on an mbarrier that nothing arrives on.
+__global__ void wait_probe_kernel(WaitCtl ctl) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_addr(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait(smem_addr(&bar), 0, ctl, &abort_flag);
+  __syncthreads();
+}
+
+cudaError_t launch_wait_probe(const DevInfo& dev, unsigned long long limit_ns,
+                              cudaStream_t stream) {
+  WaitCtl ctl{dev.status, limit_ns};
+  wait_probe_kernel<<<1, 32, 0, stream>>>(ctl);
+  return cudaGetLastError();
+}
+
+}  // namespace rg

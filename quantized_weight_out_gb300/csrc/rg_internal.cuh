@@ -1,0 +1,288 @@
+// rg_internal.cuh - device helpers shared by the librg kernels (sm_103a).
+//
+// Inline PTX wrappers for mbarrier, TMA (cp.async.bulk.tensor), the 5th
+// generation tensor core (tcgen05: tensor-memory alloc, mma, commit, ld), the
+// bounded waits every kernel uses, and the exact F32 block decoders used by
+// the dequant, SIMT and small-T kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/rg.h"
+
+namespace rg {
+
+// ---------------------------------------------------------------------------
+// storage formats: values per block, bytes per block
+
+__host__ __device__ constexpr int block_values(int wt) {
+  return wt == RG_Q4_K ? 256 : (wt == RG_Q8_0 || wt == RG_Q4_0) ? 32 : 1;
+}
+__host__ __device__ constexpr int block_bytes(int wt) {
+  return wt == RG_Q4_K ? 144 : wt == RG_Q8_0 ? 34 : wt == RG_Q4_0 ? 18 : 2;
+}
+__host__ __device__ constexpr bool is_quant(int wt) {
+  return wt == RG_Q8_0 || wt == RG_Q4_0 || wt == RG_Q4_K;
+}
+
+// Everything a kernel needs to report a wait that gave up.
+struct WaitCtl {
+  int* status;                   // per-device status word (global memory)
+  unsigned long long limit_ns;   // give up after this long
+};
+
+// ---------------------------------------------------------------------------
+// small device utilities
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void report_timeout(int* status) {
+  atomicCAS(status, 0, (int)RG_ERR_TIMEOUT);
+}
+
+// fp16 bits -> F32 (exact: every binary16 value is a float32).
+__device__ __forceinline__ float f16_to_f32(uint16_t h) {
+  return __half2float(__ushort_as_half(h));
+}
+// bf16 bits -> F32 (the bits are the top half of the float32 word).
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait until the phase with this parity has completed.  Gives up when the
+// CTA's abort flag is raised or after ctl.limit_ns; a thread that gives up on
+// its own raises the abort flag and records RG_ERR_TIMEOUT.  Returns false on
+// giving up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl,
+                                          volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > ctl.limit_ns) {
+        *abort_flag = 1;
+        report_timeout(ctl.status);
+        return false;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA
+
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 2D tiled load of one box at element coordinates (x inner, y outer) into
+// shared memory; completion is counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (the tensor core reads operands through it).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 (one CTA per MMA: cta_group::1)
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far
+// has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+// D(tmem) (+)= A(smem desc) x B(smem desc), fp16/bf16 inputs, F32 accumulate.
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 consecutive 32-bit TMEM columns of this warp's 32 lanes (lane i of the
+// warp reads TMEM lane base+i), waited for before returning.
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+      " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+      " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31},"
+      " [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of the tcgen05 MMA: start address, leading
+// and stride byte offsets (all >> 4), descriptor version 1 (bits 46-47),
+// 128-byte swizzle (layout code 2 in bits 61-63).  Tiles are 1024-byte
+// aligned, so the base-offset field stays 0.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma.kind::f16: F32 accumulator (bit 4),
+// A and B both F16 (0) or both BF16 (1) in bits 7-9 / 10-12, A MN-major
+// (bit 15), B K-major (bit 16 clear), N >> 3 in bits 17-22, M >> 4 in 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool a_mn_major,
+                                                 bool b_mn_major) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------
+// exact F32 decode of 8 consecutive values of a stored row
+//
+// row: the row's first byte (global or shared memory, at least 2-byte
+// aligned); k0: first value, a multiple of 8.  out[i] = deq(W)[row][k0 + i],
+// bit for bit: Q8_0 d*q and Q4_0 d*(q-8) are exact products (signed zero
+// kept, since a product is taken rather than a select); Q4_K's
+// (d*sc)*q - dmin*m has exact products and one rounding, so fused or
+// unfused evaluation gives the same word.
+
+__device__ __forceinline__ uint16_t ld_u16(const uint8_t* p) {
+  return *reinterpret_cast<const uint16_t*>(p);
+}
+
+__device__ __forceinline__ void q4k_scale_min(const uint8_t* S, int j, int& sc, int& m) {
+  if (j < 4) {
+    sc = S[j] & 63;
+    m = S[j + 4] & 63;
+  } else {
+    sc = (S[j + 4] & 15) | ((S[j - 4] >> 6) << 4);
+    m = (S[j + 4] >> 4) | ((S[j] >> 6) << 4);
+  }
+}
+
+template <int WT>
+__device__ __forceinline__ void decode8_f32(const uint8_t* row, int k0, float (&out)[8]) {
+  if constexpr (WT == RG_F16 || WT == RG_BF16) {
+    const uint4 v = *reinterpret_cast<const uint4*>(row + 2 * k0);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint16_t lo = static_cast<uint16_t>(w[i] & 0xFFFFu);
+      const uint16_t hi = static_cast<uint16_t>(w[i] >> 16);
+      out[2 * i] = WT == RG_F16 ? f16_to_f32(lo) : bf16_to_f32(lo);
+      out[2 * i + 1] = WT == RG_F16 ? f16_to_f32(hi) : bf16_to_f32(hi);
+    }
+  } else if constexpr (WT == RG_Q8_0) {
+    const uint8_t* blk = row + (k0 >> 5) * 34;
+    const float d = f16_to_f32(ld_u16(blk));
+    const int8_t* qs = reinterpret_cast<const int8_t*>(blk + 2 + (k0 & 31));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) out[i] = d * static_cast<float>(qs[i]);
+  } else if constexpr (WT == RG_Q4_0) {
+    const uint8_t* blk = row + (k0 >> 5) * 18;
+    const float d = f16_to_f32(ld_u16(blk));
+    const int j = k0 & 31;  // 0, 8, 16 or 24
+    const uint8_t* qs = blk + 2 + (j & 15);
+    const int shift = j >= 16 ? 4 : 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      out[i] = d * static_cast<float>(static_cast<int>((qs[i] >> shift) & 15) - 8);
+  } else if constexpr (WT == RG_Q4_K) {
+    const uint8_t* blk = row + (k0 >> 8) * 144;
+    const float d = f16_to_f32(ld_u16(blk));
+    const float dmin = f16_to_f32(ld_u16(blk + 2));
+    const int e = k0 & 255;
+    const int c = e >> 6, half = (e >> 5) & 1, l0 = e & 31;
+    int sc, m;
+    q4k_scale_min(blk + 4, 2 * c + half, sc, m);
+    const float ds = d * static_cast<float>(sc);
+    const float dm = dmin * static_cast<float>(m);
+    const uint8_t* qs = blk + 16 + 32 * c + l0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int q = half ? (qs[i] >> 4) : (qs[i] & 15);
+      out[i] = ds * static_cast<float>(q) - dm;
+    }
+  }
+}
+
+}  // namespace rg

@@ -1,0 +1,69 @@
+// rg_launch.h - host-side launchers shared between the librg translation
+// units (not part of the public C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/rg.h"
+
+namespace rg {
+
+struct WaitCtl;
+
+// Per-device facts the launchers need.
+struct DevInfo {
+  int device;
+  int num_sms;
+  int max_smem_optin;   // bytes of dynamic shared memory a block may opt into
+  int* status;          // device address of this device's status word
+  unsigned long long wait_limit_ns;
+};
+
+// All launchers enqueue on `stream` and return cudaSuccess or the launch
+// error; arguments are already validated by the entry points.
+cudaError_t launch_dequant(int wtype, const void* W, int64_t N, int64_t K, float* out,
+                           const DevInfo& dev, cudaStream_t stream);
+
+// dY [T, N] F32 -> out [T, ld] fp16 (bf16 when `bf16`), rows padded to ld.
+cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t ld, bool bf16,
+                              uint16_t* out, const DevInfo& dev, cudaStream_t stream);
+
+// dX = beta * dX (beta == 0: dX = 0), the N == 0 case.
+cudaError_t launch_scale(float* dX, int64_t count, float beta, const DevInfo& dev,
+                         cudaStream_t stream);
+
+cudaError_t launch_simt32(int wtype, const void* W, int64_t N, int64_t K, const float* dY,
+                          int64_t T, float* dX, float beta, const DevInfo& dev,
+                          cudaStream_t stream);
+
+cudaError_t launch_smallt(int wtype, const void* W, int64_t N, int64_t K, const float* dY,
+                          int64_t T, float* dX, float beta, const DevInfo& dev,
+                          cudaStream_t stream);
+
+// Tensor-core path.  dy16 is the converted dY with row stride ld_dy16 values.
+struct TcPlan {
+  int bt;        // t-columns per tile (MMA N): 128 or 256
+  int n_ktiles;  // ceil(K / 128)
+  int n_ttiles;  // ceil(T / bt)
+  int n_chunks;  // ceil(N / 64)
+  int grid;      // persistent CTAs
+};
+TcPlan plan_tc(int64_t N, int64_t K, int64_t T, const DevInfo& dev);
+int64_t tc_dy16_ld(int64_t N);
+cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
+                      int64_t ld_dy16, int64_t T, float* dX, float beta, const DevInfo& dev,
+                      cudaStream_t stream, int inject_stall);
+
+// A kernel whose one wait can never complete; it must give up after
+// `limit_ns`, record RG_ERR_TIMEOUT and return.
+cudaError_t launch_wait_probe(const DevInfo& dev, unsigned long long limit_ns,
+                              cudaStream_t stream);
+
+// cuTensorMapEncodeTiled, resolved from the driver at first use.
+CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                      uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes, uint32_t box0,
+                      uint32_t box1, CUtensorMapSwizzle swizzle);
+
+}  // namespace rg

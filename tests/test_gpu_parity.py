@@ -1,0 +1,210 @@
+"""GPU parity: every kernel through the C ABI against the CPU oracle.
+
+Bars (from the acceptance of the method):
+  * rg_dequant: bit-exact F32 words (signed zeros included);
+  * tensor-core and small-T variants: |dX - ref| <= 5e-3 * B + 1e-7;
+  * full-F32 SIMT variant:             |dX - ref| <= 1e-5 * B + 1e-7;
+where ref is the oracle's F64 result and B[t, k] = sum_n |dY[t, n]| |deq(W)[n, k]|.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from quantized_weight_out_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+TYPES = [inputs.Q8_0, inputs.Q4_0, inputs.Q4_K, inputs.F16, inputs.BF16]
+TOL = {1: 5e-3, 2: 5e-3, 3: 1e-5}  # per variant: tc, smallt, simt32
+
+
+@pytest.fixture(scope="module")
+def rg():
+    from quantized_weight_out_gb300 import binding, build
+    build.build()
+    binding.load()
+    return binding
+
+
+def _dev():
+    return torch.device("cuda:0")
+
+
+def run_out_prod(rg, variant, wtype, W, N, K, dY, T, dX0=None, beta=0.0, fill=float("nan")):
+    dev = _dev()
+    Wd = torch.from_numpy(np.ascontiguousarray(W)).to(dev)
+    dYd = torch.from_numpy(np.ascontiguousarray(dY, dtype=np.float32)).to(dev)
+    if dX0 is not None:
+        dX = torch.from_numpy(np.ascontiguousarray(dX0, dtype=np.float32)).to(dev)
+    else:
+        dX = torch.full((T, K), fill, dtype=torch.float32, device=dev)
+    s = torch.cuda.current_stream()
+    st = rg.rg_out_prod_variant(variant, wtype, Wd, N, K, dYd, T, dX, beta, s)
+    rg.check(st, "rg_out_prod_variant")
+    rg.check(rg.rg_check(s), "rg_check")
+    return dX.cpu().numpy()
+
+
+def assert_within(got, ref, bnd, tol, what=""):
+    err = np.abs(got.astype(np.float64) - ref)
+    lim = tol * bnd + 1e-7
+    bad = ~(err <= lim)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} outside the bound; "
+                             f"first {idx.tolist()}, err {err[bad][:5]}, lim {lim[bad][:5]}")
+
+
+# ----------------------------------------------------------------------------
+# rg_dequant: bit-exact
+
+@pytest.mark.parametrize("wtype", TYPES)
+@pytest.mark.parametrize("N,K", [(3, 256), (77, 768), (130, 2048)])
+def test_dequant_bit_exact(rg, wtype, N, K):
+    W = inputs.gen_weight(wtype, N, K, seed=1, stream=1)
+    ref = oracle.dequant(wtype, W, N, K)
+    out = torch.full((N, K), float("nan"), device=_dev())
+    rg.check(rg.rg_dequant(wtype, torch.from_numpy(W).to(_dev()), N, K, out))
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_dequant_negative_zero_and_extremes(rg):
+    """Hand blocks with d < 0 and zero codes decode to -0.0; fp16 extremes."""
+    q40 = bytes.fromhex("00c0f0e1d2c3b4a5968778695a4b3c2d1e0f") * 8     # 256 values
+    q80 = bytes.fromhex("0038807ff2f3f4f5f6f7f8f9fafbfcfdfeff000102030405060708090a0b0c0d0e0f")
+    q80 = (bytes([0x00, 0xBC]) + bytes([0]) * 32) * 4 + q80 * 4             # d = -1, q = 0
+    f16 = np.array([0x0001, 0x8000, 0x7BFF, 0xFBFF, 0x0400, 0x3C00, 0x8001, 0x03FF], np.uint16)
+    cases = [(inputs.Q4_0, np.frombuffer(q40, np.uint8)), (inputs.Q8_0, np.frombuffer(q80, np.uint8)),
+             (inputs.F16, np.tile(f16, 32).view(np.uint8)), (inputs.BF16, np.tile(f16, 32).view(np.uint8))]
+    for wtype, W in cases:
+        ref = oracle.dequant(wtype, W, 1, 256)
+        out = torch.zeros((1, 256), device=_dev())
+        rg.check(rg.rg_dequant(wtype, torch.from_numpy(W.copy()).to(_dev()), 1, 256, out))
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32)), wtype
+
+
+# ----------------------------------------------------------------------------
+# OUT_PROD: every variant, several tiles and ragged tails
+
+SHAPES = [  # (N, K, T): N ragged against the 64-row stage, T against 128/256-row tiles
+    (200, 512, 300),
+    (64, 256, 1),
+    (1000, 768, 520),
+    (77, 1024, 33),
+]
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("wtype", TYPES)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_out_prod_parity(rg, variant, wtype, shape):
+    N, K, T = shape
+    W = inputs.gen_weight(wtype, N, K, seed=3, stream=1)
+    dY = inputs.normal_f32(3, 2, T * N, 1e-3).reshape(T, N)
+    Wd = oracle.dequant(wtype, W, N, K)
+    ref = oracle.out_prod(wtype, W, N, K, dY, T, Wd=Wd)
+    bnd = oracle.abs_bound(dY, Wd)
+    got = run_out_prod(rg, variant, wtype, W, N, K, dY, T)
+    assert_within(got, ref, bnd, TOL[variant], f"variant {variant} type {wtype} {shape}")
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("beta", [1.0, 0.5, -2.0])
+def test_beta_accumulates(rg, variant, beta):
+    N, K, T = 192, 512, 130
+    wtype = inputs.Q4_K
+    W = inputs.gen_weight(wtype, N, K, seed=4, stream=1)
+    dY = inputs.normal_f32(4, 2, T * N, 1e-3).reshape(T, N)
+    dX0 = inputs.normal_f32(4, 3, T * K, 1e-3).reshape(T, K)
+    Wd = oracle.dequant(wtype, W, N, K)
+    ref = oracle.out_prod(wtype, W, N, K, dY, T, dX0, beta, Wd=Wd)
+    bnd = oracle.abs_bound(dY, Wd)
+    got = run_out_prod(rg, variant, wtype, W, N, K, dY, T, dX0, beta)
+    # beta*dX0 is one F32 rounding: allow 2^-24 |beta dX0| on top of the bound
+    assert_within(got, ref, bnd + np.abs(beta * dX0) * (2.0 ** -24) / TOL[variant], TOL[variant])
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3])
+def test_beta_zero_ignores_nan(rg, variant):
+    N, K, T = 96, 256, 40
+    W = inputs.gen_weight(inputs.Q8_0, N, K, seed=5, stream=1)
+    dY = inputs.normal_f32(5, 2, T * N, 1.0).reshape(T, N)
+    got = run_out_prod(rg, variant, inputs.Q8_0, W, N, K, dY, T, fill=float("nan"))
+    assert np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("variant", [2, 3])
+@pytest.mark.parametrize("wtype", TYPES)
+def test_one_hot_f32_variants_equal_rows(rg, variant, wtype):
+    """F32 variants: one-hot dY reproduces rows of deq(W) exactly."""
+    N, K, T = 80, 512, 6
+    W = inputs.gen_weight(wtype, N, K, seed=6, stream=1)
+    Wd = oracle.dequant(wtype, W, N, K)
+    n0 = [(13 * t + 5) % N for t in range(T)]
+    dY = np.zeros((T, N), np.float32)
+    dY[np.arange(T), n0] = 1.0
+    got = run_out_prod(rg, variant, wtype, W, N, K, dY, T)
+    for t in range(T):
+        assert np.array_equal(np.abs(got[t]), np.abs(Wd[n0[t]])), (t,)
+
+
+@pytest.mark.parametrize("wtype", TYPES)
+def test_all_ones_closed_form_tc(rg, wtype):
+    """All-ones weight times one-hot dY gives exactly 1 on the tensor cores too."""
+    from test_oracle import _all_ones_weight
+    N, K, T = 128, 512, 260
+    W = _all_ones_weight(wtype, N, K)
+    dY = np.zeros((T, N), np.float32)
+    dY[np.arange(T), (7 * np.arange(T) + 3) % N] = 1.0
+    got = run_out_prod(rg, 1, wtype, W, N, K, dY, T)
+    assert np.all(got == 1.0)
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+def test_empty_contraction_scales(rg, variant):
+    T, K = 5, 256
+    dX0 = inputs.normal_f32(7, 3, T * K, 1.0).reshape(T, K)
+    got = run_out_prod(rg, variant, inputs.Q4_0, np.zeros(0, np.uint8), 0, K,
+                       np.zeros((T, 0), np.float32), T, dX0, 0.5)
+    assert np.array_equal(got, (np.float32(0.5) * dX0).astype(np.float32))
+    got0 = run_out_prod(rg, variant, inputs.Q4_0, np.zeros(0, np.uint8), 0, K,
+                        np.zeros((T, 0), np.float32), T, fill=float("nan"))
+    assert np.all(got0 == 0.0)
+
+
+def test_workspace_entry_point_matches(rg):
+    N, K, T = 300, 512, 270
+    wtype = inputs.Q4_0
+    W = inputs.gen_weight(wtype, N, K, seed=8, stream=1)
+    dY = inputs.normal_f32(8, 2, T * N, 1e-3).reshape(T, N)
+    a = run_out_prod(rg, 1, wtype, W, N, K, dY, T)
+    need = rg.rg_workspace_bytes(1, wtype, N, K, T)
+    ws = torch.empty(need, dtype=torch.uint8, device=_dev())
+    dev = _dev()
+    dX = torch.empty((T, K), device=dev)
+    s = torch.cuda.current_stream()
+    args = (1, wtype, torch.from_numpy(W).to(dev), N, K, torch.from_numpy(dY).to(dev), T, dX, 0.0)
+    assert rg.rg_out_prod_ws(*args, ws, need - 1, s) == rg.RG_ERR_ARG
+    rg.check(rg.rg_out_prod_ws(*args, ws, need, s))
+    rg.check(rg.rg_check(s))
+    assert np.array_equal(dX.cpu().numpy(), a)   # same kernels, same order: identical
+
+
+def test_timeout_probe_reports_and_context_survives(rg):
+    s = torch.cuda.current_stream()
+    rg.check(rg.rg_check(s))
+    rg.check(rg.rg_debug_wait_probe(200, s))
+    assert rg.rg_check(s) == rg.RG_ERR_TIMEOUT
+    assert rg.rg_check(s) == rg.RG_OK     # read-and-clear
+    N, K, T = 64, 256, 40                 # the context still computes
+    W = inputs.gen_weight(inputs.Q8_0, N, K, seed=9, stream=1)
+    dY = inputs.normal_f32(9, 2, T * N, 1.0).reshape(T, N)
+    got = run_out_prod(rg, 1, inputs.Q8_0, W, N, K, dY, T)
+    Wd = oracle.dequant(inputs.Q8_0, W, N, K)
+    assert_within(got, oracle.out_prod(inputs.Q8_0, W, N, K, dY, T, Wd=Wd),
+                  oracle.abs_bound(dY, Wd), 5e-3)
