@@ -136,7 +136,7 @@ def oracle_sample(problems, rows: int):
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="layer7b_t8192", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
