@@ -110,25 +110,30 @@ def _bus_id(torch, dev):
 # ---------------------------------------------------------------------------
 # CPU oracle on a bounded sample
 
-def oracle_sample(problems, rows: int):
-    """Time the oracle as it stands on the first `rows` rows of dY of every
-    call: decode each W (oracle.dequant), then contract (oracle.out_prod).
-    Returns (flops done, seconds, description)."""
+def oracle_sample(problems, t_rows: int, n_rows: int | None = None):
+    """Time the oracle as it stands on a slice of every call of the workload:
+    the first `t_rows` rows of dY and the first `n_rows` rows of W (all of
+    them when None), i.e. decode that slice of W (oracle.dequant) and contract
+    it (oracle.out_prod).  Returns (flops done, seconds, description)."""
     import oracle
     data = []
     for p in problems:
-        W = p.weight()
-        dY = p.dy()[:rows].copy()
+        n = p.N if n_rows is None else min(n_rows, p.N)
+        rb = inputs.row_bytes(p.wtype, p.K)
+        W = p.weight()[: n * rb].copy()
+        dY = np.ascontiguousarray(p.dy()[:t_rows, :n])
         dX0 = p.dx0()
-        data.append((p, W, dY, None if dX0 is None else dX0[:rows].copy()))
+        data.append((p, n, W, dY, None if dX0 is None else dX0[:t_rows].copy()))
     t0 = time.perf_counter()
     flops = 0
-    for p, W, dY, dX0 in data:
-        Wd = oracle.dequant(p.wtype, W, p.N, p.K)
-        oracle.out_prod(p.wtype, W, p.N, p.K, dY, rows, dX0, p.beta, Wd=Wd)
-        flops += 2 * rows * p.N * p.K
+    for p, n, W, dY, dX0 in data:
+        Wd = oracle.dequant(p.wtype, W, n, p.K)
+        oracle.out_prod(p.wtype, W, n, p.K, dY, t_rows, dX0, p.beta, Wd=Wd)
+        flops += 2 * t_rows * n * p.K
     dt = time.perf_counter() - t0
-    return flops, dt, f"every call of the workload, first {rows} rows of dY, full decode of W"
+    what = "all" if n_rows is None else f"the first {n_rows}"
+    return flops, dt, (f"every call of the workload: first {t_rows} rows of dY, {what} rows of W "
+                       "(decode + F64 contraction)")
 
 
 # ---------------------------------------------------------------------------
@@ -140,7 +145,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="layer7b_t8192", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-rows", type=int, default=64, help="dY rows per call in the CPU sample")
+    ap.add_argument("--cpu-rows", type=int, default=256, help="dY rows per call, CPU baseline sample")
+    ap.add_argument("--ref-rows", type=int, default=32, help="dY rows per call, reference-arm step")
+    ap.add_argument("--ref-wrows", type=int, default=512, help="W rows per call, reference-arm step")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -163,12 +170,12 @@ def run_reference(args):
     if rank != 0:
         return
     problems = inputs.WORKLOADS[args.workload]
-    rows = args.cpu_rows
+    rows = args.ref_rows
     for _ in range(args.warmup):
-        oracle_sample(problems, rows)
+        oracle_sample(problems, rows, args.ref_wrows)
     times, flops = [], 0
     for _ in range(args.steps):
-        f, dt, desc = oracle_sample(problems, rows)
+        f, dt, desc = oracle_sample(problems, rows, args.ref_wrows)
         times.append(dt)
         flops = f
     ms = 1e3 * sum(times) / len(times)
@@ -178,7 +185,8 @@ def run_reference(args):
             "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "sample_rows_per_call": rows},
+            "config": {"workload": args.workload, "sample_rows_per_call": rows,
+                       "sample_w_rows_per_call": args.ref_wrows},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -266,23 +274,44 @@ def run_ours(args):
         h2d = sum(h[0].numel() * h[0].element_size() + h[1].numel() * 4 for h in host)
         d2h = sum(p.T * p.K * 4 for p in problems)
 
+        # copies on two side streams, overlapped with compute on `stream`:
+        # H2D(i) -> rg_out_prod(i) -> D2H(i), with the write-after-read hazards
+        # across steps ordered by events
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in problems]
+        ev_done = [torch.cuda.Event() for _ in problems]
+        ev_out = [torch.cuda.Event() for _ in problems]
+
         def e2e_step():
             for i, p in enumerate(problems):
                 W, dY, dX = devbuf[i]
-                W.copy_(host[i][0], non_blocking=True)
-                dY.copy_(host[i][1], non_blocking=True)
+                s_in.wait_event(ev_done[i])
+                with torch.cuda.stream(s_in):
+                    W.copy_(host[i][0], non_blocking=True)
+                    dY.copy_(host[i][1], non_blocking=True)
+                ev_in[i].record(s_in)
+                stream.wait_event(ev_in[i])
+                stream.wait_event(ev_out[i])
                 st = rg.rg_out_prod(p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, stream)
                 if st != 0:
                     raise RuntimeError(rg.strerror(st))
-                host[i][2].copy_(dX, non_blocking=True)
+                ev_done[i].record(stream)
+                s_out.wait_event(ev_done[i])
+                with torch.cuda.stream(s_out):
+                    host[i][2].copy_(dX, non_blocking=True)
+                ev_out[i].record(s_out)
+
         e2e_step()
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        s_in.wait_event(e0)
         for _ in range(args.steps):
             e2e_step()
+        for ev in ev_out:
+            stream.wait_event(ev)
         e1.record(stream)
         torch.cuda.synchronize()
         ems = e0.elapsed_time(e1) / args.steps

@@ -306,4 +306,6 @@ WORKLOADS = {
     "f16_5120x17408_t4096_beta1": [Problem("f16_5120x17408_t4096_beta1", F16, 5120, 17408, 4096, 1e-3, 1.0)],
     "bf16_5120x17408_t4096_beta1": [Problem("bf16_5120x17408_t4096_beta1", BF16, 5120, 17408, 4096, 1e-3, 1.0)],
     "layer7b_t8192": _layer_sweep(8192),
+    # the sweep's largest call alone (profiling a full-size launch)
+    "layer7b_gate_t8192": [_layer_sweep(8192)[4]],
 }
