@@ -75,8 +75,10 @@ typedef enum {
                               F32 accumulation in tensor memory                             */
     RG_VARIANT_SMALLT = 2, /* small-T, weight-bandwidth-bound: coalesced 16-byte weight
                               loads, decode in registers, F32 FMA, cluster reduction        */
-    RG_VARIANT_SIMT32 = 3  /* exact F32 decode and F32 FMA with blocked accumulation: the
+    RG_VARIANT_SIMT32 = 3, /* exact F32 decode and F32 FMA with blocked accumulation: the
                               full-precision variant (slow; a correctness reference)        */
+    RG_VARIANT_TC_SINGLE = 4, /* RG_VARIANT_TC with one-CTA 128 x 128 tiles                */
+    RG_VARIANT_TC_PAIR = 5    /* RG_VARIANT_TC with two-CTA (cta_group::2) 256 x 256 tiles  */
 } rg_variant;
 
 /*
@@ -85,8 +87,8 @@ typedef enum {
  * wtype: rg_wtype.  W: N * rg_row_bytes(wtype, K) bytes.  dY: [T, N] F32.
  * dX: [T, K] F32, read only when beta != 0 (with beta == 0 its old contents,
  * NaN included, are ignored).  The variant is chosen from (wtype, T, N, K);
- * the environment variable RG_VARIANT=auto|tc|smallt|simt32, read once per
- * process, overrides that choice.  Asynchronous on `stream`.
+ * the environment variable RG_VARIANT=auto|tc|tc1|tc2|smallt|simt32, read
+ * once per process, overrides that choice.  Asynchronous on `stream`.
  *
  * Scratch: the tensor-core variant converts dY once to fp16/bf16 in a device
  * workspace of rg_workspace_bytes() bytes.  rg_out_prod takes it
@@ -98,8 +100,9 @@ typedef enum {
 int rg_out_prod(int wtype, const void* W, int64_t N, int64_t K,
                 const float* dY, int64_t T, float* dX, float beta, void* stream);
 
-/* rg_out_prod with an explicit variant (rg_variant; RG_VARIANT_AUTO = dispatch).
- * RG_VARIANT ignored.  Same contract as rg_out_prod. */
+/* rg_out_prod with an explicit variant (rg_variant; RG_VARIANT_AUTO = dispatch;
+ * RG_VARIANT_TC picks its tile shape from the problem, TC_SINGLE / TC_PAIR
+ * force one).  RG_VARIANT ignored.  Same contract as rg_out_prod. */
 int rg_out_prod_variant(int variant, int wtype, const void* W, int64_t N, int64_t K,
                         const float* dY, int64_t T, float* dX, float beta, void* stream);
 

@@ -38,6 +38,8 @@ const Env& env() {
     Env r;
     if (const char* v = std::getenv("RG_VARIANT")) {
       if (!std::strcmp(v, "tc")) r.variant = RG_VARIANT_TC;
+      else if (!std::strcmp(v, "tc1")) r.variant = RG_VARIANT_TC_SINGLE;
+      else if (!std::strcmp(v, "tc2")) r.variant = RG_VARIANT_TC_PAIR;
       else if (!std::strcmp(v, "smallt")) r.variant = RG_VARIANT_SMALLT;
       else if (!std::strcmp(v, "simt32")) r.variant = RG_VARIANT_SIMT32;
     }
@@ -151,7 +153,7 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
   bool empty = false;
   int st = validate(wtype, W, N, K, dY, T, dX, &empty);
   if (st != RG_OK || empty) return st;
-  if (variant < RG_VARIANT_AUTO || variant > RG_VARIANT_SIMT32) return RG_ERR_TYPE;
+  if (variant < RG_VARIANT_AUTO || variant > RG_VARIANT_TC_PAIR) return RG_ERR_TYPE;
   DevInfo* dev = nullptr;
   if ((st = current_dev(&dev)) != RG_OK) return st;
   if (N == 0) return from_cuda(launch_scale(dX, T * K, beta, *dev, stream));
@@ -181,7 +183,8 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
   cudaError_t e = launch_convert_dy(dY, T, N, ld, bf16, static_cast<uint16_t*>(buf), *dev, stream);
   if (e == cudaSuccess)
     e = launch_tc(wtype, W, N, K, static_cast<const uint16_t*>(buf), ld, T, dX, beta, *dev,
-                  stream, env().inject_stall);
+                  stream, variant == RG_VARIANT_TC_SINGLE ? 1 : variant == RG_VARIANT_TC_PAIR ? 2 : 0,
+                  env().inject_stall);
   if (own_ws) {
     const cudaError_t f = cudaFreeAsync(buf, stream);
     if (e == cudaSuccess) e = f;
@@ -237,7 +240,9 @@ int rg_out_prod_variant(int variant, int wtype, const void* W, int64_t N, int64_
 
 size_t rg_workspace_bytes(int variant, int wtype, int64_t N, int64_t K, int64_t T) {
   if (variant == RG_VARIANT_AUTO) variant = select_variant(wtype, N, K, T);
-  if (variant != RG_VARIANT_TC || N <= 0 || T <= 0 || K <= 0) return 0;
+  const bool tc = variant == RG_VARIANT_TC || variant == RG_VARIANT_TC_SINGLE ||
+                  variant == RG_VARIANT_TC_PAIR;
+  if (!tc || N <= 0 || T <= 0 || K <= 0) return 0;
   return tc_workspace(N, T);
 }
 

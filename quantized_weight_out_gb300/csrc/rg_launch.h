@@ -44,17 +44,19 @@ cudaError_t launch_smallt(int wtype, const void* W, int64_t N, int64_t K, const 
 
 // Tensor-core path.  dy16 is the converted dY with row stride ld_dy16 values.
 struct TcPlan {
-  int bt;        // t-columns per tile (MMA N): 128 or 256
-  int n_ktiles;  // ceil(K / 128)
-  int n_ttiles;  // ceil(T / bt)
-  int n_chunks;  // ceil(N / 64)
-  int grid;      // persistent CTAs
+  int cg;        // CTAs per MMA: 2 (cta_group::2, 256 x 256 tiles) or 1 (128 x 128)
+  int bt;        // t-columns per tile (MMA N): 256 (cg 2) or 128 (cg 1)
+  int n_kunits;  // tiles along k: ceil(K / (128 * cg))
+  int n_ttiles;  // tiles along t: ceil(T / bt)
+  int n_chunks;  // ceil(N / 64) contraction stages per tile
+  int grid;      // persistent CTAs (a multiple of cg), before the occupancy cap
 };
-TcPlan plan_tc(int64_t N, int64_t K, int64_t T, const DevInfo& dev);
+// cg_force: 0 = choose from the shape, 1 or 2 = that tile configuration.
+TcPlan plan_tc(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force);
 int64_t tc_dy16_ld(int64_t N);
 cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
                       int64_t ld_dy16, int64_t T, float* dX, float beta, const DevInfo& dev,
-                      cudaStream_t stream, int inject_stall);
+                      cudaStream_t stream, int cg_force, int inject_stall);
 
 // A kernel whose one wait can never complete; it must give up after
 // `limit_ns`, record RG_ERR_TIMEOUT and return.

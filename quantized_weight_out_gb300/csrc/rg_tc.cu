@@ -4,26 +4,33 @@
 // The llama.cpp fork's PR "cuda: out_prod accepts a quantized src0" (section
 // "What") reaches this product by writing deq(W) to a dense F32 pool copy and
 // running cuBLAS SGEMM on it, and names a fused dequant-GEMM as the follow-on.
-// This kernel is that fused GEMM, built for sm_103a:
+// This kernel is that fused GEMM, built for sm_103a.
 //
-//  * orientation: the tensor core computes D[k, t] = sum_n deq(W)[n, k] *
-//    dY[t, n], i.e. A = deq(W)^T (M = 128 values of k, MN-major: k is
-//    contiguous in a stored row) and B = dY^T (N = BT values of t, K-major:
-//    n is contiguous in a row of dY).  The contraction runs over the rows n
-//    of W, so each block's scale belongs to one contraction row and is folded
-//    into the operand while decoding.
-//  * one CTA per SM (persistent), warp-specialised:
-//      warp 0      TMA producer: packed W rows (or F16/BF16 tiles, already
-//                  in operand layout) and the 16-bit dY tile, per stage;
-//      warp 1      tensor-memory owner and MMA issuer (one thread);
-//      warps 4-7   decoders: packed blocks in shared memory -> fp16 operand
-//                  tile in the 128-byte-swizzled layout the MMA reads;
-//      warps 8-11  epilogue: tcgen05.ld -> beta*dX + acc -> global.
-//  * F32 accumulators live in tensor memory, two per CTA (2 x BT columns), so
-//    the epilogue of one tile overlaps the main loop of the next.
-//  * every wait is bounded; a wait that gives up raises the CTA's abort flag,
-//    records RG_ERR_TIMEOUT, and the CTA drains its in-flight copies and MMAs
-//    before freeing tensor memory and returning.
+//  * Orientation: the tensor core computes D[k, t] = sum_n deq(W)[n, k] *
+//    dY[t, n], i.e. A = deq(W)^T (M along k, MN-major: k is contiguous in a
+//    stored row) and B = dY^T (N along t, K-major: n is contiguous in a row
+//    of dY).  The contraction runs over the rows n of W, so every block scale
+//    belongs to one contraction row and is folded into the operand while
+//    decoding; it could not be applied in the epilogue.
+//  * CG = 2 (the main configuration): a cluster of two CTAs on the two SMs of
+//    a pair computes a 256(k) x 256(t) tile with tcgen05.mma.cta_group::2
+//    (M = 256, N = 256).  Each CTA decodes its own 128 values of k into its
+//    A half and TMA-loads its own 128 rows of t into its B half; the even CTA
+//    issues the MMAs and commits to both CTAs' barriers.  Per SM this halves
+//    the dY operand traffic of a one-CTA 128 x 256 tile.
+//    CG = 1: one CTA, M = 128, N = 128, for shapes with few tiles.
+//  * Persistent, warp-specialised, 512 threads per CTA:
+//      warp 0      TMA producer (packed W window or F16/BF16 operand tile, and
+//                  the 16-bit dY tile, per stage of 64 contraction rows);
+//      warp 1      tensor-memory owner and (even CTA) MMA issuer;
+//      warps 4-11  decoders: packed blocks -> fp16 operand tile, 128-byte
+//                  swizzled, MN-major (for F16/BF16 they only relay);
+//      warps 12-15 epilogue: tcgen05.ld -> beta*dX + acc -> global.
+//  * F32 accumulators in tensor memory, two per CTA (2 x BT columns): the
+//    epilogue of one tile overlaps the main loop of the next.
+//  * Every wait is bounded; a wait that gives up raises the CTA's abort flag
+//    and records RG_ERR_TIMEOUT, and the CTA drains its in-flight copies and
+//    MMAs before freeing tensor memory and returning.
 #include <algorithm>
 
 #include "rg_internal.cuh"
@@ -32,12 +39,16 @@
 namespace rg {
 namespace tc {
 
-constexpr int BM = 128;           // k-values per tile (MMA M)
+constexpr int BM = 128;           // values of k per CTA (A rows of M per CTA)
 constexpr int BC = 64;            // contraction rows (n) per pipeline stage
 constexpr int UMMA_K = 16;        // contraction rows per tcgen05.mma (16-bit inputs)
-constexpr int NUM_THREADS = 384;  // 12 warps
+constexpr int B_ROWS = 128;       // rows of t per CTA in a B stage
+constexpr int NUM_THREADS = 512;  // 16 warps
+constexpr int DEC_WARP0 = 4, DEC_WARPS = 8, EPI_WARP0 = 12;
 constexpr int A_STAGE = BC * BM * 2;      // 16 KB: 64 rows of n x 128 fp16 values of k
 constexpr int A_COLBLK = BC * 128;        // 8 KB: one 64-value column block of k
+constexpr int B_STAGE = B_ROWS * 128;     // 16 KB: 128 rows of t x 64 16-bit values of n
+constexpr int SMEM_BUDGET = 224 * 1024;
 
 // Bytes of one packed W row that a 128-value tile loads (16-byte multiples):
 // Q8_0 4 blocks = 136 B inside a 144 B window, Q4_0 72 B inside 80 B, Q4_K
@@ -47,26 +58,29 @@ __host__ __device__ constexpr int p_row_bytes() {
   return WT == RG_Q8_0 ? 144 : WT == RG_Q4_0 ? 80 : WT == RG_Q4_K ? 144 : 0;
 }
 
-template <int WT, int BT>
+template <int WT, int CG, int BT>
 struct Cfg {
   static constexpr bool QUANT = is_quant(WT);
   static constexpr bool BF = WT == RG_BF16;
-  static constexpr int B_STAGE = BT * 128;  // BT rows of t x 64 16-bit values of n
-  static constexpr int P_STAGE = QUANT ? BC * p_row_bytes<WT>() : 0;
-  static constexpr int STAGE = A_STAGE + B_STAGE + ((P_STAGE + 1023) / 1024) * 1024;
-  static constexpr int S = std::min(6, (200 * 1024) / STAGE);
+  static constexpr int P_STAGE = QUANT ? ((BC * p_row_bytes<WT>() + 1023) / 1024) * 1024 : 0;
+  static constexpr int STAGE = A_STAGE + B_STAGE + P_STAGE;
+  static constexpr int S = std::min(8, SMEM_BUDGET / STAGE);
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + S * A_STAGE;
   static constexpr int OFF_P = OFF_B + S * B_STAGE;
-  static constexpr int OFF_BAR = OFF_P + S * ((P_STAGE + 1023) / 1024) * 1024;
+  static constexpr int OFF_BAR = OFF_P + S * P_STAGE;
   // barriers: full_tma[S], full_dec[S], empty[S], acc_full[2], acc_empty[2], drain
   static constexpr int NUM_BARS = 3 * S + 5;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024 B alignment
-  static constexpr uint32_t TMA_BYTES = (QUANT ? P_STAGE : A_STAGE) + B_STAGE;
+  static constexpr uint32_t TMA_BYTES = (QUANT ? BC * p_row_bytes<WT>() : A_STAGE) + B_STAGE;
   static constexpr uint32_t TMEM_COLS = 2 * BT;
-  static constexpr uint32_t IDESC = idesc_f16(BF, BM, BT, /*A MN-major*/ true, /*B*/ false);
-  static_assert(S >= 2, "pipeline needs at least two stages");
+  static constexpr int MMA_M = BM * CG;
+  static constexpr uint32_t IDESC = idesc_f16(BF, MMA_M, BT, /*A MN-major*/ true, /*B*/ false);
+  static constexpr uint32_t FULL_DEC_COUNT = DEC_WARPS * CG;
+  static constexpr uint32_t ACC_EMPTY_COUNT = 4 * CG;
+  static_assert(BT / CG == B_ROWS, "each CTA holds 128 rows of t in a B stage");
+  static_assert(S >= 3, "pipeline depth");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -79,20 +93,35 @@ __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Bytes 0..3 of `b` are small unsigned integers u (< 256).  Returns the two
-// fp16 values 1024 + u of bytes (lo_sel) packed as a half2: 0x64 is the high
-// byte of 1024.0 in binary16, whose unit in the last place is 1, so the low
+// Bytes of `b` are small unsigned integers u (< 256).  Returns the two fp16
+// values 1024 + u of the bytes `sel` picks, packed as a half2: 0x64 is the
+// high byte of 1024.0 in binary16, whose unit in the last place is 1, so the
 // byte lands in the mantissa exactly.
-__device__ __forceinline__ __half2 bytes_to_h2_plus1024(uint32_t b, uint32_t sel) {
+__device__ __forceinline__ __half2 bytes_plus1024(uint32_t b, uint32_t sel) {
   return u32_as_h2(__byte_perm(b, 0x64646464u, sel));
 }
 constexpr uint32_t SEL_B01 = 0x5140;  // bytes 0,1 -> (lo half, hi half)
 constexpr uint32_t SEL_B23 = 0x7362;  // bytes 2,3
 
+// Four bytes x = 4 values each (q + bias already unsigned) -> two half2 of
+// (1024 + u - off) * d.
+__device__ __forceinline__ void four_scaled(uint32_t u, __half2 off, __half2 d, uint32_t& o0,
+                                            uint32_t& o1) {
+  o0 = h2_as_u32(__hmul2(__hsub2(bytes_plus1024(u, SEL_B01), off), d));
+  o1 = h2_as_u32(__hmul2(__hsub2(bytes_plus1024(u, SEL_B23), off), d));
+}
+// Four nibble values in bytes -> two half2 of q * ds + nm (Q4_K).
+__device__ __forceinline__ void four_affine(uint32_t u, __half2 magic, __half2 ds, __half2 nm,
+                                            uint32_t& o0, uint32_t& o1) {
+  o0 = h2_as_u32(__hfma2(__hsub2(bytes_plus1024(u, SEL_B01), magic), ds, nm));
+  o1 = h2_as_u32(__hfma2(__hsub2(bytes_plus1024(u, SEL_B23), magic), ds, nm));
+}
+
 // Store a 16-byte chunk (8 fp16 values of k = 8*cidx .. 8*cidx+7 of the tile)
 // of contraction row n into the A stage: MN-major, 128-byte swizzle (chunk c
 // of a 128-byte row r sits at position c ^ (r mod 8)); column blocks of 64
-// values of k are A_COLBLK apart.
+// values of k are A_COLBLK apart.  Lanes that store the same cidx for eight
+// consecutive rows hit eight distinct 16-byte bank groups.
 __device__ __forceinline__ void st_a_chunk(uint8_t* a, int n, int cidx, uint32_t x, uint32_t y,
                                            uint32_t z, uint32_t w) {
   const int jb = cidx >> 3, cc = cidx & 7;
@@ -100,98 +129,159 @@ __device__ __forceinline__ void st_a_chunk(uint8_t* a, int n, int cidx, uint32_t
       make_uint4(x, y, z, w);
 }
 
-__device__ __forceinline__ uint32_t ld2_u16(const uint8_t* p) {  // 4 bytes at a 2-byte boundary
-  const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
-  return static_cast<uint32_t>(q[0]) | (static_cast<uint32_t>(q[1]) << 16);
+// Words of a packed row held in registers: chunks of 16 bytes from C0 on.
+// word_at(x) = the 4 bytes at byte offset x from the first loaded chunk.
+template <int NW>
+struct RowWords {
+  uint32_t w[NW];
+  __device__ __forceinline__ uint32_t word_at(int x) const {
+    const int i = x >> 2, sh = x & 3;
+    return sh == 0 ? w[i] : __funnelshift_r(w[i], w[i + 1], 8 * sh);
+  }
+};
+template <int C0, int C1>
+__device__ __forceinline__ RowWords<4 * (C1 - C0 + 1)> load_chunks(const uint8_t* row) {
+  RowWords<4 * (C1 - C0 + 1)> r;
+#pragma unroll
+  for (int c = 0; c <= C1 - C0; ++c) {
+    const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * (C0 + c));
+    r.w[4 * c] = v.x;
+    r.w[4 * c + 1] = v.y;
+    r.w[4 * c + 2] = v.z;
+    r.w[4 * c + 3] = v.w;
+  }
+  return r;
 }
 
-// Decode one stage: P holds BC packed rows of one 128-value tile (row stride
-// p_row_bytes), A receives the fp16 operand.  dtid = 0..127.  kt = the tile's
-// index along k (selects the byte offset inside the loaded window, or the
-// half of the Q4_K super-block).
+// Q8_0 block starting at byte S of a row window: fp16 d, 32 int8 q.
+// Writes its 32 values as chunks 4b .. 4b+3 of row n.
+template <int S>
+__device__ __forceinline__ void dec_q8_block(const uint8_t* row, uint8_t* A, int n, int b) {
+  constexpr int C0 = S / 16;
+  constexpr int C1 = (S + ((S & 3) == 0 ? 35 : 33)) / 16;
+  const auto r = load_chunks<C0, C1>(row);
+  constexpr int X = S - 16 * C0;
+  const __half2 d2 = __half2half2(__ushort_as_half(static_cast<uint16_t>(r.word_at(X) & 0xFFFFu)));
+  const __half2 off = __float2half2_rn(1152.0f);  // 1024 + 128 (int8 sign bias)
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t o[4];
+    four_scaled(r.word_at(X + 2 + 8 * q) ^ 0x80808080u, off, d2, o[0], o[1]);
+    four_scaled(r.word_at(X + 6 + 8 * q) ^ 0x80808080u, off, d2, o[2], o[3]);
+    st_a_chunk(A, n, 4 * b + q, o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Q4_0 block starting at byte S: fp16 d, 16 bytes of nibbles (low = value j,
+// high = value j + 16).  Writes chunks 4b .. 4b+3 of row n.
+template <int S>
+__device__ __forceinline__ void dec_q4_0_block(const uint8_t* row, uint8_t* A, int n, int b) {
+  constexpr int C0 = S / 16;
+  constexpr int C1 = (S + ((S & 3) == 0 ? 19 : 17)) / 16;
+  const auto r = load_chunks<C0, C1>(row);
+  constexpr int X = S - 16 * C0;
+  const __half2 d2 = __half2half2(__ushort_as_half(static_cast<uint16_t>(r.word_at(X) & 0xFFFFu)));
+  const __half2 off = __float2half2_rn(1032.0f);  // 1024 + 8 (the Q4_0 zero point)
+  uint32_t lo[8], hi[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w = r.word_at(X + 2 + 4 * j);
+    four_scaled(w & 0x0F0F0F0Fu, off, d2, lo[2 * j], lo[2 * j + 1]);
+    four_scaled((w >> 4) & 0x0F0F0F0Fu, off, d2, hi[2 * j], hi[2 * j + 1]);
+  }
+  st_a_chunk(A, n, 4 * b, lo[0], lo[1], lo[2], lo[3]);
+  st_a_chunk(A, n, 4 * b + 1, lo[4], lo[5], lo[6], lo[7]);
+  st_a_chunk(A, n, 4 * b + 2, hi[0], hi[1], hi[2], hi[3]);
+  st_a_chunk(A, n, 4 * b + 3, hi[4], hi[5], hi[6], hi[7]);
+}
+
+__device__ __forceinline__ uint32_t byte_of(uint32_t h1, uint32_t h2, uint32_t h3, int i) {
+  const uint32_t w = i < 4 ? h1 : (i < 8 ? h2 : h3);
+  return (w >> (8 * (i & 3))) & 0xFFu;
+}
+
+// Decode one stage.  P: BC packed rows (row stride p_row_bytes) of this CTA's
+// 128-value tile; A: the fp16 operand.  dtid = 0..255; kt = the CTA's tile
+// index along k in units of 128 (byte offset in the window, or Q4_K half).
+// Lanes of a warp take consecutive rows n with the same block, so loads and
+// stores of eight consecutive lanes fall into eight distinct bank groups.
 template <int WT>
 __device__ __forceinline__ void decode_stage(const uint8_t* __restrict__ P, uint8_t* __restrict__ A,
                                              int dtid, int kt) {
   constexpr int PR = p_row_bytes<WT>();
+  const int n = dtid & 63;
+  const int sel = dtid >> 6;  // warp-uniform: 0..3
+  const uint8_t* row = P + n * PR;
   if constexpr (WT == RG_Q8_0) {
-    // unit = (row n, block b of 4, quarter q of 4): 8 values -> one chunk
-    const int off = (kt * 136) & 15;
-    const __half2 bias = __float2half2_rn(1152.0f);  // 1024 + 128 (int8 sign bias)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int u = dtid + 128 * i;
-      const int n = u >> 4, b = (u >> 2) & 3, q = u & 3;
-      const uint8_t* blk = P + n * PR + off + 34 * b;
-      const __half2 d2 = __half2half2(__ushort_as_half(ld_u16(blk)));
-      const uint32_t w0 = ld2_u16(blk + 2 + 8 * q) ^ 0x80808080u;
-      const uint32_t w1 = ld2_u16(blk + 6 + 8 * q) ^ 0x80808080u;
-      const uint32_t o0 = h2_as_u32(__hmul2(__hsub2(bytes_to_h2_plus1024(w0, SEL_B01), bias), d2));
-      const uint32_t o1 = h2_as_u32(__hmul2(__hsub2(bytes_to_h2_plus1024(w0, SEL_B23), bias), d2));
-      const uint32_t o2 = h2_as_u32(__hmul2(__hsub2(bytes_to_h2_plus1024(w1, SEL_B01), bias), d2));
-      const uint32_t o3 = h2_as_u32(__hmul2(__hsub2(bytes_to_h2_plus1024(w1, SEL_B23), bias), d2));
-      st_a_chunk(A, n, 4 * b + q, o0, o1, o2, o3);
+    // one block of 34 B (32 values) per thread; window offset 0 or 8
+    const int s = (kt & 1) * 4 + sel;  // selects (offset, block)
+    switch (s) {
+      case 0: dec_q8_block<0>(row, A, n, 0); break;
+      case 1: dec_q8_block<34>(row, A, n, 1); break;
+      case 2: dec_q8_block<68>(row, A, n, 2); break;
+      case 3: dec_q8_block<102>(row, A, n, 3); break;
+      case 4: dec_q8_block<8>(row, A, n, 0); break;
+      case 5: dec_q8_block<42>(row, A, n, 1); break;
+      case 6: dec_q8_block<76>(row, A, n, 2); break;
+      default: dec_q8_block<110>(row, A, n, 3); break;
     }
   } else if constexpr (WT == RG_Q4_0) {
-    // unit = (row n, block b of 4, half h): 16 values (low or high nibbles)
-    const int off = (kt * 72) & 15;
-    const __half2 bias = __float2half2_rn(1032.0f);  // 1024 + 8 (the Q4_0 zero point)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int u = dtid + 128 * i;
-      const int n = u >> 3, b = (u >> 1) & 3, h = u & 1;
-      const uint8_t* blk = P + n * PR + off + 18 * b;
-      const __half2 d2 = __half2half2(__ushort_as_half(ld_u16(blk)));
-      uint32_t o[8];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t w = ld2_u16(blk + 2 + 4 * j);
-        w = (h ? (w >> 4) : w) & 0x0F0F0F0Fu;
-        o[2 * j] = h2_as_u32(__hmul2(__hsub2(bytes_to_h2_plus1024(w, SEL_B01), bias), d2));
-        o[2 * j + 1] = h2_as_u32(__hmul2(__hsub2(bytes_to_h2_plus1024(w, SEL_B23), bias), d2));
-      }
-      st_a_chunk(A, n, 4 * b + 2 * h, o[0], o[1], o[2], o[3]);
-      st_a_chunk(A, n, 4 * b + 2 * h + 1, o[4], o[5], o[6], o[7]);
+    const int s = (kt & 1) * 4 + sel;
+    switch (s) {
+      case 0: dec_q4_0_block<0>(row, A, n, 0); break;
+      case 1: dec_q4_0_block<18>(row, A, n, 1); break;
+      case 2: dec_q4_0_block<36>(row, A, n, 2); break;
+      case 3: dec_q4_0_block<54>(row, A, n, 3); break;
+      case 4: dec_q4_0_block<8>(row, A, n, 0); break;
+      case 5: dec_q4_0_block<26>(row, A, n, 1); break;
+      case 6: dec_q4_0_block<44>(row, A, n, 2); break;
+      default: dec_q4_0_block<62>(row, A, n, 3); break;
     }
   } else if constexpr (WT == RG_Q4_K) {
-    // unit = (row n, chunk cl of 2, part p of 4): qs bytes 8p..8p+7 of chunk
-    // c = 2*(kt & 1) + cl give 8 values of sub-block 2c (low nibbles) and 8
-    // of sub-block 2c+1 (high nibbles).
-    const int h2 = kt & 1;
-    const __half2 magic = __float2half2_rn(1024.0f);
+    // chunk c = 2*(kt & 1) + cl of the super-block: 16 bytes of nibbles
+    // (l = 16*hh .. 16*hh+15) give 16 values of sub-block 2c (low nibbles)
+    // and 16 of sub-block 2c+1 (high nibbles)
+    const int cl = sel >> 1, hh = sel & 1;
+    const int c = 2 * (kt & 1) + cl;
+    const uint4 hdr = *reinterpret_cast<const uint4*>(row);
+    const uint4 qv = *reinterpret_cast<const uint4*>(row + 16 + 32 * c + 16 * hh);
+    const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x & 0xFFFFu)));
+    const float dmin = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x >> 16)));
+    int sc[2], m[2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int u = dtid + 128 * i;
-      const int n = u >> 3, cl = (u >> 2) & 1, p = u & 3;
-      const int c = 2 * h2 + cl;
-      const uint8_t* sb = P + n * PR;
-      const float d = f16_to_f32(ld_u16(sb));
-      const float dmin = f16_to_f32(ld_u16(sb + 2));
-      int sc0, m0, sc1, m1;
-      q4k_scale_min(sb + 4, 2 * c, sc0, m0);
-      q4k_scale_min(sb + 4, 2 * c + 1, sc1, m1);
-      const __half2 ds0 = __float2half2_rn(d * static_cast<float>(sc0));
-      const __half2 nm0 = __float2half2_rn(-(dmin * static_cast<float>(m0)));
-      const __half2 ds1 = __float2half2_rn(d * static_cast<float>(sc1));
-      const __half2 nm1 = __float2half2_rn(-(dmin * static_cast<float>(m1)));
-      const uint2 qv = *reinterpret_cast<const uint2*>(sb + 16 + 32 * c + 8 * p);
-      const uint32_t l0 = qv.x & 0x0F0F0F0Fu, l1 = qv.y & 0x0F0F0F0Fu;
-      const uint32_t g0 = (qv.x >> 4) & 0x0F0F0F0Fu, g1 = (qv.y >> 4) & 0x0F0F0F0Fu;
-      uint32_t lo[4], hi[4];
-      lo[0] = h2_as_u32(__hfma2(__hsub2(bytes_to_h2_plus1024(l0, SEL_B01), magic), ds0, nm0));
-      lo[1] = h2_as_u32(__hfma2(__hsub2(bytes_to_h2_plus1024(l0, SEL_B23), magic), ds0, nm0));
-      lo[2] = h2_as_u32(__hfma2(__hsub2(bytes_to_h2_plus1024(l1, SEL_B01), magic), ds0, nm0));
-      lo[3] = h2_as_u32(__hfma2(__hsub2(bytes_to_h2_plus1024(l1, SEL_B23), magic), ds0, nm0));
-      hi[0] = h2_as_u32(__hfma2(__hsub2(bytes_to_h2_plus1024(g0, SEL_B01), magic), ds1, nm1));
-      hi[1] = h2_as_u32(__hfma2(__hsub2(bytes_to_h2_plus1024(g0, SEL_B23), magic), ds1, nm1));
-      hi[2] = h2_as_u32(__hfma2(__hsub2(bytes_to_h2_plus1024(g1, SEL_B01), magic), ds1, nm1));
-      hi[3] = h2_as_u32(__hfma2(__hsub2(bytes_to_h2_plus1024(g1, SEL_B23), magic), ds1, nm1));
-      st_a_chunk(A, n, 8 * cl + p, lo[0], lo[1], lo[2], lo[3]);
-      st_a_chunk(A, n, 8 * cl + 4 + p, hi[0], hi[1], hi[2], hi[3]);
+    for (int h = 0; h < 2; ++h) {
+      const int j = 2 * c + h;
+      if (j < 4) {
+        sc[h] = byte_of(hdr.y, hdr.z, hdr.w, j) & 63;
+        m[h] = byte_of(hdr.y, hdr.z, hdr.w, j + 4) & 63;
+      } else {
+        const uint32_t e = byte_of(hdr.y, hdr.z, hdr.w, j + 4);
+        sc[h] = (e & 15) | ((byte_of(hdr.y, hdr.z, hdr.w, j - 4) >> 6) << 4);
+        m[h] = (e >> 4) | ((byte_of(hdr.y, hdr.z, hdr.w, j) >> 6) << 4);
+      }
     }
+    const __half2 magic = __float2half2_rn(1024.0f);
+    const __half2 ds0 = __float2half2_rn(d * static_cast<float>(sc[0]));
+    const __half2 nm0 = __float2half2_rn(-(dmin * static_cast<float>(m[0])));
+    const __half2 ds1 = __float2half2_rn(d * static_cast<float>(sc[1]));
+    const __half2 nm1 = __float2half2_rn(-(dmin * static_cast<float>(m[1])));
+    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+    uint32_t lo[8], hi[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      four_affine(qw[j] & 0x0F0F0F0Fu, magic, ds0, nm0, lo[2 * j], lo[2 * j + 1]);
+      four_affine((qw[j] >> 4) & 0x0F0F0F0Fu, magic, ds1, nm1, hi[2 * j], hi[2 * j + 1]);
+    }
+    // values 64*cl + 16*hh + 0..15 (low) and 64*cl + 32 + 16*hh + 0..15 (high)
+    const int cb = 8 * cl + 2 * hh;
+    st_a_chunk(A, n, cb, lo[0], lo[1], lo[2], lo[3]);
+    st_a_chunk(A, n, cb + 1, lo[4], lo[5], lo[6], lo[7]);
+    st_a_chunk(A, n, cb + 4, hi[0], hi[1], hi[2], hi[3]);
+    st_a_chunk(A, n, cb + 5, hi[4], hi[5], hi[6], hi[7]);
   }
 }
 
-// Byte offset (16-byte multiple) of the window a k-tile loads from a packed row.
+// Byte offset (16-byte multiple) of the window a 128-value tile kt loads from a packed row.
 template <int WT>
 __device__ __forceinline__ int p_window_start(int kt) {
   if constexpr (WT == RG_Q8_0) return (kt * 136) & ~15;
@@ -201,17 +291,17 @@ __device__ __forceinline__ int p_window_start(int kt) {
 
 // --- the kernel -----------------------------------------------------------------
 
-template <int WT, int BT>
+template <int WT, int CG, int BT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     out_prod_tc_kernel(const __grid_constant__ CUtensorMap map_w,
                        const __grid_constant__ CUtensorMap map_y, float* __restrict__ dX,
-                       float beta, int T, int K, int n_ktiles, int n_tiles, int n_chunks,
+                       float beta, int T, int K, int n_kunits, int n_tiles, int n_chunks,
                        WaitCtl ctl, int inject_stall) {
-  using C = Cfg<WT, BT>;
+  using C = Cfg<WT, CG, BT>;
   constexpr int S = C::S;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // align inside the shared window (pointer arithmetic keeps the shared space)
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem + C::OFF_A;
   uint8_t* sB = smem + C::OFF_B;
   uint8_t* sP = smem + C::OFF_P;
@@ -226,16 +316,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit = blockIdx.x / CG, n_units = gridDim.x / CG;
+
+  // arrive on the MMA-issuing CTA's copy of a barrier
+  auto arrive_leader = [&](uint32_t bar) {
+    if constexpr (CG == 2)
+      mbar_arrive_cluster(mapa_shared(bar, 0));
+    else
+      mbar_arrive(bar);
+  };
+  auto wait_pair = [&](uint32_t bar, uint32_t parity) {
+    if constexpr (CG == 2)
+      return mbar_wait_cluster(bar, parity, ctl, abort_flag);
+    else
+      return mbar_wait(bar, parity, ctl, abort_flag);
+  };
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_tma(s), 1);
-      mbar_init(full_dec(s), 4);
+      mbar_init(full_dec(s), C::FULL_DEC_COUNT);
       mbar_init(empty(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(acc_full(a), 1);
-      mbar_init(acc_empty(a), 4);
+      mbar_init(acc_empty(a), C::ACC_EMPTY_COUNT);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -244,13 +351,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_map(&map_y);
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (CG == 2) {
+      tmem_alloc2(smem_addr(tmem_slot), C::TMEM_COLS);
+      tmem_relinquish2();
+    } else {
+      tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CG == 2)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+
+  // tile -> (k unit, t tile); this CTA's 128-value k tile and B rows
+  auto ktile_of = [&](int tile) { return (tile % n_kunits) * CG + static_cast<int>(rank); };
+  auto ttile_of = [&](int tile) { return tile / n_kunits; };
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -259,26 +378,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t pending = 0, pend_ph = 0;  // stages with a copy in flight, and its phase
     bool ok = true;
     bool skip_first = inject_stall != 0;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-      const int kt = tile % n_ktiles, tt = tile / n_ktiles;
+    for (int tile = unit; tile < n_tiles && ok; tile += n_units) {
+      const int kt = ktile_of(tile), tt = ttile_of(tile);
+      const int ty = tt * BT + static_cast<int>(rank) * B_ROWS;
       for (int c = 0; c < n_chunks; ++c) {
-        ok = mbar_wait(empty(s), ph ^ 1u, ctl, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
+        ok = __all_sync(0xffffffffu, mbar_wait(empty(s), ph ^ 1u, ctl, abort_flag));
         if (!ok) break;
         if (lane == 0) {
           if (skip_first) {
-            skip_first = false;  // fault-injection: this stage never fills
+            skip_first = false;  // fault injection: this stage never fills
           } else {
             mbar_arrive_expect_tx(full_tma(s), C::TMA_BYTES);
             if constexpr (C::QUANT) {
-              tma_load_2d(smem_addr(sP + s * (C::STAGE - A_STAGE - C::B_STAGE)), &map_w,
-                          full_tma(s), p_window_start<WT>(kt) / 4, c * BC);
+              tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_tma(s),
+                          p_window_start<WT>(kt) / 4, c * BC);
             } else {
               tma_load_2d(smem_addr(sA + s * A_STAGE), &map_w, full_tma(s), kt * BM, c * BC);
               tma_load_2d(smem_addr(sA + s * A_STAGE + A_COLBLK), &map_w, full_tma(s),
                           kt * BM + 64, c * BC);
             }
-            tma_load_2d(smem_addr(sB + s * C::B_STAGE), &map_y, full_tma(s), c * BC, tt * BT);
+            tma_load_2d(smem_addr(sB + s * B_STAGE), &map_y, full_tma(s), c * BC, ty);
             pending |= 1u << s;
             pend_ph = (pend_ph & ~(1u << s)) | (ph << s);
           }
@@ -288,84 +407,100 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     if (!ok && lane == 0) {
-      // drain: every copy this thread started must land before the CTA exits
-      WaitCtl quick{ctl.status, ctl.limit_ns};
+      // drain: every copy this thread started lands before the CTA exits
       volatile int no_abort = 0;
       for (int st = 0; st < S; ++st)
-        if (pending & (1u << st)) (void)mbar_wait(full_tma(st), (pend_ph >> st) & 1u, quick, &no_abort);
+        if (pending & (1u << st)) (void)mbar_wait(full_tma(st), (pend_ph >> st) & 1u, ctl, &no_abort);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    int s = 0;
-    uint32_t ph = 0;
-    bool ok = true;
-    int j = 0;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++j) {
-      const int a = j & 1;
-      const uint32_t aph = (static_cast<uint32_t>(j) >> 1) & 1u;
-      ok = __all_sync(0xffffffffu, mbar_wait(acc_empty(a), aph ^ 1u, ctl, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * BT);
-      for (int c = 0; c < n_chunks; ++c) {
-        bool got = mbar_wait(full_tma(s), ph, ctl, abort_flag);
-        if constexpr (C::QUANT) got = got && mbar_wait(full_dec(s), ph, ctl, abort_flag);
-        ok = __all_sync(0xffffffffu, got);
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a_base = smem_addr(sA + s * A_STAGE);
-          const uint32_t b_base = smem_addr(sB + s * C::B_STAGE);
-#pragma unroll
-          for (int kk = 0; kk < BC / UMMA_K; ++kk) {
-            // A: MN-major, k-column blocks 8 KB apart (LBO), 8-row groups of n 1 KB apart (SBO)
-            const uint64_t ad = sdesc_sw128(a_base + kk * (UMMA_K * 128), A_COLBLK, 1024);
-            // B: K-major, 16 values of n = 32 bytes along the swizzled row; 8-row groups 1 KB apart
-            const uint64_t bd = sdesc_sw128(b_base + kk * (UMMA_K * 2), 16, 1024);
-            tc_mma_f16(d_tmem, ad, bd, C::IDESC, (c | kk) != 0 ? 1u : 0u);
-          }
-          tc_commit(empty(s));
-        }
-        __syncwarp();
-        if (++s == S) { s = 0; ph ^= 1u; }
-      }
-      if (!ok) break;
-      if (lane == 0) tc_commit(acc_full(a));
-      __syncwarp();
-    }
-    if (!ok && lane == 0) {
-      // drain: all MMAs this thread issued complete before tensor memory is freed
-      tc_commit(drain_bar);
-      volatile int no_abort = 0;
-      (void)mbar_wait(drain_bar, 0, ctl, &no_abort);
-    }
-  } else if (warp >= 4 && warp < 8) {
-    // ---------------- decoders ----------------
-    if constexpr (C::QUANT) {
-      const int dtid = threadIdx.x - 128;
+    // ---------------- MMA issuer (the even CTA of a pair) ----------------
+    if (leader) {
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        const int kt = tile % n_ktiles;
+      int j = 0;
+      for (int tile = unit; tile < n_tiles && ok; tile += n_units, ++j) {
+        const int a = j & 1;
+        const uint32_t aph = (static_cast<uint32_t>(j) >> 1) & 1u;
+        ok = __all_sync(0xffffffffu, wait_pair(acc_empty(a), aph ^ 1u));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * BT);
         for (int c = 0; c < n_chunks; ++c) {
-          ok = __all_sync(0xffffffffu, mbar_wait(full_tma(s), ph, ctl, abort_flag));
+          bool got = mbar_wait(full_tma(s), ph, ctl, abort_flag);
+          got = got && wait_pair(full_dec(s), ph);
+          ok = __all_sync(0xffffffffu, got);
           if (!ok) break;
-          decode_stage<WT>(sP + s * (C::STAGE - A_STAGE - C::B_STAGE), sA + s * A_STAGE, dtid, kt);
-          fence_proxy_async_smem();
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a_base = smem_addr(sA + s * A_STAGE);
+            const uint32_t b_base = smem_addr(sB + s * B_STAGE);
+#pragma unroll
+            for (int kk = 0; kk < BC / UMMA_K; ++kk) {
+              // A: MN-major, k-column blocks 8 KB apart (LBO), 8-row groups of n 1 KB apart (SBO)
+              const uint64_t ad = sdesc_sw128(a_base + kk * (UMMA_K * 128), A_COLBLK, 1024);
+              // B: K-major, 16 values of n = 32 bytes along the swizzled row; 8-row groups 1 KB apart
+              const uint64_t bd = sdesc_sw128(b_base + kk * (UMMA_K * 2), 16, 1024);
+              const uint32_t acc = (c | kk) != 0 ? 1u : 0u;
+              if constexpr (CG == 2)
+                tc_mma_f16_pair(d_tmem, ad, bd, C::IDESC, acc);
+              else
+                tc_mma_f16(d_tmem, ad, bd, C::IDESC, acc);
+            }
+            if constexpr (CG == 2)
+              tc_commit_pair(empty(s), 0x3);
+            else
+              tc_commit(empty(s));
+          }
           __syncwarp();
-          if (lane == 0) mbar_arrive(full_dec(s));
           if (++s == S) { s = 0; ph ^= 1u; }
         }
+        if (!ok) break;
+        if (lane == 0) {
+          if constexpr (CG == 2)
+            tc_commit_pair(acc_full(a), 0x3);
+          else
+            tc_commit(acc_full(a));
+        }
+        __syncwarp();
+      }
+      if (!ok && lane == 0) {
+        // drain: every MMA this thread issued completes before tensor memory is freed
+        if constexpr (CG == 2)
+          tc_commit_pair(drain_bar, 0x1);
+        else
+          tc_commit(drain_bar);
+        volatile int no_abort = 0;
+        (void)mbar_wait(drain_bar, 0, ctl, &no_abort);
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= DEC_WARP0 && warp < DEC_WARP0 + DEC_WARPS) {
+    // ---------------- decoders (relays for F16/BF16) ----------------
+    const int dtid = threadIdx.x - DEC_WARP0 * 32;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int tile = unit; tile < n_tiles && ok; tile += n_units) {
+      const int kt = ktile_of(tile);
+      for (int c = 0; c < n_chunks; ++c) {
+        ok = __all_sync(0xffffffffu, mbar_wait(full_tma(s), ph, ctl, abort_flag));
+        if (!ok) break;
+        if constexpr (C::QUANT) {
+          decode_stage<WT>(sP + s * C::P_STAGE, sA + s * A_STAGE, dtid, kt);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) arrive_leader(full_dec(s));
+        if (++s == S) { s = 0; ph ^= 1u; }
+      }
+    }
+  } else if (warp >= EPI_WARP0) {
     // ---------------- epilogue ----------------
     const int eq = warp & 3;  // TMEM lanes 32*eq .. 32*eq+31
     bool ok = true;
     int j = 0;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++j) {
-      const int kt = tile % n_ktiles, tt = tile / n_ktiles;
+    for (int tile = unit; tile < n_tiles && ok; tile += n_units, ++j) {
+      const int kt = ktile_of(tile), tt = ttile_of(tile);
       const int a = j & 1;
       const uint32_t aph = (static_cast<uint32_t>(j) >> 1) & 1u;
       ok = __all_sync(0xffffffffu, mbar_wait(acc_full(a), aph, ctl, abort_flag));
@@ -375,34 +510,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool kin = k < K;
 #pragma unroll 1
       for (int cb = 0; cb < BT / 32; ++cb) {
+        const int tb = tt * BT + 32 * cb;
+        float old[32];
+        if (beta != 0.0f && kin) {
+          // all loads of the column block first: one round trip, not 32
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            old[i] = (tb + i < T) ? dX[static_cast<int64_t>(tb + i) * K + k] : 0.0f;
+        }
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * eq) << 16) +
                                static_cast<uint32_t>(a * BT + 32 * cb),
                            r);
-        const int tb = tt * BT + 32 * cb;
         if (kin) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const int t = tb + i;
-            if (t < T) {
-              float* o = dX + static_cast<int64_t>(t) * K + k;
+            if (tb + i < T) {
               const float v = __uint_as_float(r[i]);
-              *o = beta != 0.0f ? fmaf(beta, *o, v) : v;
+              dX[static_cast<int64_t>(tb + i) * K + k] = beta != 0.0f ? fmaf(beta, old[i], v) : v;
             }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty(a));
+      if (lane == 0) arrive_leader(acc_empty(a));
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CG == 2)
+    cluster_sync();
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (CG == 2)
+      tmem_dealloc2(tmem_base, C::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
@@ -412,46 +558,78 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 int64_t tc_dy16_ld(int64_t N) { return (N + 7) / 8 * 8; }
 
-TcPlan plan_tc(int64_t N, int64_t K, int64_t T, const DevInfo& dev) {
+TcPlan plan_tc(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force) {
   TcPlan p{};
-  p.n_ktiles = static_cast<int>((K + tc::BM - 1) / tc::BM);
   p.n_chunks = static_cast<int>((N + tc::BC - 1) / tc::BC);
-  const int64_t tiles256 = p.n_ktiles * ((T + 255) / 256);
-  p.bt = tiles256 >= dev.num_sms ? 256 : 128;
-  p.n_ttiles = static_cast<int>((T + p.bt - 1) / p.bt);
-  const int64_t tiles = static_cast<int64_t>(p.n_ktiles) * p.n_ttiles;
-  p.grid = static_cast<int>(std::min<int64_t>(tiles, dev.num_sms));
+  const int64_t pair_tiles = ((K + 255) / 256) * ((T + 255) / 256);
+  const bool pair = cg_force ? cg_force == 2 : pair_tiles * 2 >= dev.num_sms;
+  if (pair) {
+    p.cg = 2;
+    p.bt = 256;
+    p.n_kunits = static_cast<int>((K + 255) / 256);
+    p.n_ttiles = static_cast<int>((T + 255) / 256);
+  } else {
+    p.cg = 1;
+    p.bt = 128;
+    p.n_kunits = static_cast<int>((K + 127) / 128);
+    p.n_ttiles = static_cast<int>((T + 127) / 128);
+  }
+  const int64_t tiles = static_cast<int64_t>(p.n_kunits) * p.n_ttiles;
+  const int64_t units = std::min<int64_t>(tiles, dev.num_sms / p.cg);
+  p.grid = static_cast<int>(units * p.cg);
   return p;
 }
 
-template <int WT, int BT>
+template <int WT, int CG, int BT>
 static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my, float* dX,
                                float beta, int T, int K, const TcPlan& p, const DevInfo& dev,
                                cudaStream_t stream, int inject) {
-  using C = tc::Cfg<WT, BT>;
-  auto kern = tc::out_prod_tc_kernel<WT, BT>;
+  using C = tc::Cfg<WT, CG, BT>;
+  auto kern = tc::out_prod_tc_kernel<WT, CG, BT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   WaitCtl ctl{dev.status, dev.wait_limit_ns};
-  const int n_tiles = p.n_ktiles * p.n_ttiles;
-  kern<<<p.grid, tc::NUM_THREADS, C::SMEM_BYTES, stream>>>(mw, my, dX, beta, T, K, p.n_ktiles,
-                                                          n_tiles, p.n_chunks, ctl, inject);
-  return cudaGetLastError();
+  const int n_tiles = p.n_kunits * p.n_ttiles;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(tc::NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // persistent grid: no more clusters than can be resident at once
+  static int max_clusters[64] = {0};
+  int& mc = max_clusters[dev.device & 63];
+  if (mc == 0) {
+    cfg.gridDim = dim3(static_cast<unsigned>(CG * (dev.num_sms / CG)), 1, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0)
+      n = dev.num_sms / CG;
+    mc = n;
+  }
+  const int units = std::min(p.grid / CG, mc);
+  cfg.gridDim = dim3(static_cast<unsigned>(units * CG), 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, mw, my, dX, beta, T, K, p.n_kunits, n_tiles, p.n_chunks,
+                            ctl, inject);
 }
 
 template <int WT>
 static cudaError_t launch_tc_w(const CUtensorMap& mw, const CUtensorMap& my, float* dX,
                                float beta, int T, int K, const TcPlan& p, const DevInfo& dev,
                                cudaStream_t stream, int inject) {
-  if (p.bt == 256) return launch_tc_t<WT, 256>(mw, my, dX, beta, T, K, p, dev, stream, inject);
-  return launch_tc_t<WT, 128>(mw, my, dX, beta, T, K, p, dev, stream, inject);
+  if (p.cg == 2) return launch_tc_t<WT, 2, 256>(mw, my, dX, beta, T, K, p, dev, stream, inject);
+  return launch_tc_t<WT, 1, 128>(mw, my, dX, beta, T, K, p, dev, stream, inject);
 }
 
 cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
                       int64_t ld_dy16, int64_t T, float* dX, float beta, const DevInfo& dev,
-                      cudaStream_t stream, int inject_stall) {
-  const TcPlan p = plan_tc(N, K, T, dev);
+                      cudaStream_t stream, int cg_force, int inject_stall) {
+  const TcPlan p = plan_tc(N, K, T, dev, cg_force);
   CUtensorMap mw, my;
   CUresult r;
   if (is_quant(wtype)) {
@@ -467,7 +645,7 @@ cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   r = encode_tiled(&my, CU_TENSOR_MAP_DATA_TYPE_UINT16, dy16, static_cast<uint64_t>(N),
                    static_cast<uint64_t>(T), static_cast<uint64_t>(ld_dy16) * 2, tc::BC,
-                   static_cast<uint32_t>(p.bt), CU_TENSOR_MAP_SWIZZLE_128B);
+                   tc::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   const int t = static_cast<int>(T), k = static_cast<int>(K);
   switch (wtype) {

@@ -17,7 +17,8 @@ pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
 
 TYPES = [inputs.Q8_0, inputs.Q4_0, inputs.Q4_K, inputs.F16, inputs.BF16]
-TOL = {1: 5e-3, 2: 5e-3, 3: 1e-5}  # per variant: tc, smallt, simt32
+TOL = {1: 5e-3, 2: 5e-3, 3: 1e-5, 4: 5e-3, 5: 5e-3}  # tc, smallt, simt32, tc1, tc2
+ALL_VARIANTS = [1, 2, 3, 4, 5]
 
 
 @pytest.fixture(scope="module")
@@ -99,7 +100,7 @@ SHAPES = [  # (N, K, T): N ragged against the 64-row stage, T against 128/256-ro
 ]
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("variant", ALL_VARIANTS)
 @pytest.mark.parametrize("wtype", TYPES)
 @pytest.mark.parametrize("shape", SHAPES)
 def test_out_prod_parity(rg, variant, wtype, shape):
@@ -113,7 +114,7 @@ def test_out_prod_parity(rg, variant, wtype, shape):
     assert_within(got, ref, bnd, TOL[variant], f"variant {variant} type {wtype} {shape}")
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("variant", ALL_VARIANTS)
 @pytest.mark.parametrize("beta", [1.0, 0.5, -2.0])
 def test_beta_accumulates(rg, variant, beta):
     N, K, T = 192, 512, 130
@@ -129,7 +130,7 @@ def test_beta_accumulates(rg, variant, beta):
     assert_within(got, ref, bnd + np.abs(beta * dX0) * (2.0 ** -24) / TOL[variant], TOL[variant])
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("variant", ALL_VARIANTS)
 def test_beta_zero_ignores_nan(rg, variant):
     N, K, T = 96, 256, 40
     W = inputs.gen_weight(inputs.Q8_0, N, K, seed=5, stream=1)
@@ -153,19 +154,35 @@ def test_one_hot_f32_variants_equal_rows(rg, variant, wtype):
         assert np.array_equal(np.abs(got[t]), np.abs(Wd[n0[t]])), (t,)
 
 
+@pytest.mark.parametrize("variant", [4, 5])
 @pytest.mark.parametrize("wtype", TYPES)
-def test_all_ones_closed_form_tc(rg, wtype):
+def test_all_ones_closed_form_tc(rg, variant, wtype):
     """All-ones weight times one-hot dY gives exactly 1 on the tensor cores too."""
     from test_oracle import _all_ones_weight
     N, K, T = 128, 512, 260
-    W = _all_ones_weight(wtype, N, K)
+    W = _all_ones_weight(wtype, N, K).copy()
     dY = np.zeros((T, N), np.float32)
     dY[np.arange(T), (7 * np.arange(T) + 3) % N] = 1.0
-    got = run_out_prod(rg, 1, wtype, W, N, K, dY, T)
+    got = run_out_prod(rg, variant, wtype, W, N, K, dY, T)
     assert np.all(got == 1.0)
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+@pytest.mark.parametrize("wtype", TYPES)
+def test_pair_tiles_many_waves(rg, wtype):
+    """Enough 256 x 256 tiles that the pair kernel's persistent CTAs loop over
+    several tiles each (both accumulators, ragged N and T)."""
+    N, K, T = 520, 4096, 1300
+    W = inputs.gen_weight(wtype, N, K, seed=12, stream=1)
+    dY = inputs.normal_f32(12, 2, T * N, 1e-3).reshape(T, N)
+    Wd = oracle.dequant(wtype, W, N, K)
+    ref = oracle.out_prod(wtype, W, N, K, dY, T, Wd=Wd)
+    bnd = oracle.abs_bound(dY, Wd)
+    for variant in (1, 5):
+        got = run_out_prod(rg, variant, wtype, W, N, K, dY, T)
+        assert_within(got, ref, bnd, 5e-3, f"variant {variant} type {wtype}")
+
+
+@pytest.mark.parametrize("variant", [0] + ALL_VARIANTS)
 def test_empty_contraction_scales(rg, variant):
     T, K = 5, 256
     dX0 = inputs.normal_f32(7, 3, T * K, 1.0).reshape(T, K)
