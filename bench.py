@@ -141,16 +141,28 @@ def oracle_sample(problems, t_rows: int, n_rows: int | None = None):
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="layer7b_t8192", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--workload", default="layer7b_t8192")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=256, help="dY rows per call, CPU baseline sample")
     ap.add_argument("--ref-rows", type=int, default=32, help="dY rows per call, reference-arm step")
     ap.add_argument("--ref-wrows", type=int, default=512, help="W rows per call, reference-arm step")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
     ap.add_argument("--no-e2e", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--custom", default=None,
+                    help="a custom call instead of --workload, e.g. q8_0:4096x14336:t8192:beta0")
+    ap.add_argument("--variant", default="auto", choices=["auto", "tc", "tc1", "tc2", "smallt", "simt32"],
+                    help="force a kernel variant (rg_out_prod_variant)")
+    args = ap.parse_args()
+    if args.custom:
+        wt, nk, t, b = args.custom.split(":")
+        n, k = nk.split("x")
+        prob = inputs.Problem(args.custom, inputs.NAME_TO_TYPE[wt], int(n), int(k), int(t[1:]),
+                              1e-3, float(b[4:]))
+        inputs.WORKLOADS[args.custom] = [prob]
+        args.workload = args.custom
+    return args
 
 
 def _dist():
@@ -222,14 +234,20 @@ def run_ours(args):
                        else torch.zeros((p.T, p.K), device=dev)))
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    variants = [rg.rg_select_variant(p.wtype, p.N, p.K, p.T) for p in problems]
+    forced = rg.VARIANTS[args.variant]
+    variants = [forced if forced else rg.rg_select_variant(p.wtype, p.N, p.K, p.T) for p in problems]
+
+    def call(p, W, dY, dX):
+        if forced:
+            return rg.rg_out_prod_variant(forced, p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, stream)
+        return rg.rg_out_prod(p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, stream)
 
     def step(events=None):
         for i, p in enumerate(problems):
             W, dY, dX = devbuf[i]
             if events is not None:
                 events[i][0].record(stream)
-            st = rg.rg_out_prod(p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, stream)
+            st = call(p, W, dY, dX)
             if events is not None:
                 events[i][1].record(stream)
             if st != 0:
@@ -292,7 +310,7 @@ def run_ours(args):
                 ev_in[i].record(s_in)
                 stream.wait_event(ev_in[i])
                 stream.wait_event(ev_out[i])
-                st = rg.rg_out_prod(p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, stream)
+                st = call(p, W, dY, dX)
                 if st != 0:
                     raise RuntimeError(rg.strerror(st))
                 ev_done[i].record(stream)
@@ -325,7 +343,8 @@ def run_ours(args):
     # roofline of the tensor-core launches (the dominant kernel)
     peaks, src = _peaks()
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    tc = [i for i, v in enumerate(variants) if v == rg.RG_VARIANT_TC]
+    tc = [i for i, v in enumerate(variants)
+          if v in (rg.RG_VARIANT_TC, rg.RG_VARIANT_TC_SINGLE, rg.RG_VARIANT_TC_PAIR)]
     tc_flops = sum(problems[i].flops for i in tc)
     tc_ms = sum(statistics.mean(per_call[i]) for i in tc) if tc else 0.0
     achieved = tc_flops / (tc_ms * 1e-3) / 1e12 if tc_ms > 0 else None
@@ -350,7 +369,8 @@ def run_ours(args):
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
                "kind": "oracle", "sample": desc, "seconds": dt}
 
-    launches_per_call = {rg.RG_VARIANT_TC: 2, rg.RG_VARIANT_SMALLT: 1, rg.RG_VARIANT_SIMT32: 1}
+    launches_per_call = {rg.RG_VARIANT_TC: 2, rg.RG_VARIANT_TC_SINGLE: 2, rg.RG_VARIANT_TC_PAIR: 2,
+                         rg.RG_VARIANT_SMALLT: 1, rg.RG_VARIANT_SIMT32: 1}
     gpu_launches = args.steps * sum(launches_per_call[v] for v in variants)
     step_bytes = sum(p.algorithmic_bytes() for p in problems)
     line = {

@@ -50,6 +50,7 @@ struct TcPlan {
   int n_ttiles;  // tiles along t: ceil(T / bt)
   int n_chunks;  // ceil(N / 64) contraction stages per tile
   int grid;      // persistent CTAs (a multiple of cg), before the occupancy cap
+  int band;      // k units per rasterization band (tile order), set at launch
 };
 // cg_force: 0 = choose from the shape, 1 or 2 = that tile configuration.
 TcPlan plan_tc(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force);

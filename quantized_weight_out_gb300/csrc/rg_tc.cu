@@ -23,8 +23,9 @@
 //      warp 0      TMA producer (packed W window or F16/BF16 operand tile, and
 //                  the 16-bit dY tile, per stage of 64 contraction rows);
 //      warp 1      tensor-memory owner and (even CTA) MMA issuer;
-//      warps 4-11  decoders: packed blocks -> fp16 operand tile, 128-byte
-//                  swizzled, MN-major (for F16/BF16 they only relay);
+//      warp 2      (follower CTA) relays its decoded stages to the issuing CTA;
+//      warps 4-11  decoders, one per stage slot: packed blocks -> fp16 operand
+//                  tile, 128-byte swizzled, MN-major (idle for F16/BF16);
 //      warps 12-15 epilogue: tcgen05.ld -> beta*dX + acc -> global.
 //  * F32 accumulators in tensor memory, two per CTA (2 x BT columns): the
 //    epilogue of one tile overlaps the main loop of the next.
@@ -64,23 +65,30 @@ struct Cfg {
   static constexpr bool BF = WT == RG_BF16;
   static constexpr int P_STAGE = QUANT ? ((BC * p_row_bytes<WT>() + 1023) / 1024) * 1024 : 0;
   static constexpr int STAGE = A_STAGE + B_STAGE + P_STAGE;
-  static constexpr int S = std::min(8, SMEM_BUDGET / STAGE);
+  // quantized: four slots, each decoded by two warps; F16/BF16: as deep as fits
+  static constexpr int S = QUANT ? 4 : std::min(8, SMEM_BUDGET / STAGE);
+  static constexpr int WARPS_PER_SLOT = QUANT ? DEC_WARPS / S : 0;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + S * A_STAGE;
   static constexpr int OFF_P = OFF_B + S * B_STAGE;
   static constexpr int OFF_BAR = OFF_P + S * P_STAGE;
-  // barriers: full_tma[S], full_dec[S], empty[S], acc_full[2], acc_empty[2], drain
-  static constexpr int NUM_BARS = 3 * S + 5;
+  // barriers: full_p, full_ab, full_dec, dec_done, empty (S each), acc_full[2],
+  // acc_empty[2], drain
+  static constexpr int NUM_BARS = 5 * S + 5;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024 B alignment
-  static constexpr uint32_t TMA_BYTES = (QUANT ? BC * p_row_bytes<WT>() : A_STAGE) + B_STAGE;
+  static constexpr uint32_t P_BYTES = QUANT ? BC * p_row_bytes<WT>() : 0;
+  // operand bytes of one stage over the whole pair (B halves, and A for F16/BF16)
+  static constexpr uint32_t AB_BYTES_PAIR = CG * (B_STAGE + (QUANT ? 0 : A_STAGE));
   static constexpr uint32_t TMEM_COLS = 2 * BT;
   static constexpr int MMA_M = BM * CG;
   static constexpr uint32_t IDESC = idesc_f16(BF, MMA_M, BT, /*A MN-major*/ true, /*B*/ false);
-  static constexpr uint32_t FULL_DEC_COUNT = DEC_WARPS * CG;
+  // the slot's decoder warps, plus a follower's relay
+  static constexpr uint32_t FULL_DEC_COUNT = (QUANT ? DEC_WARPS / S : 1) + (CG == 2 ? 1 : 0);
   static constexpr uint32_t ACC_EMPTY_COUNT = 4 * CG;
   static_assert(BT / CG == B_ROWS, "each CTA holds 128 rows of t in a B stage");
   static_assert(S >= 3, "pipeline depth");
+  static_assert(!QUANT || S * WARPS_PER_SLOT == DEC_WARPS, "decoder warps split evenly over slots");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -200,84 +208,87 @@ __device__ __forceinline__ uint32_t byte_of(uint32_t h1, uint32_t h2, uint32_t h
   return (w >> (8 * (i & 3))) & 0xFFu;
 }
 
-// Decode one stage.  P: BC packed rows (row stride p_row_bytes) of this CTA's
-// 128-value tile; A: the fp16 operand.  dtid = 0..255; kt = the CTA's tile
-// index along k in units of 128 (byte offset in the window, or Q4_K half).
-// Lanes of a warp take consecutive rows n with the same block, so loads and
-// stores of eight consecutive lanes fall into eight distinct bank groups.
-template <int WT>
-__device__ __forceinline__ void decode_stage(const uint8_t* __restrict__ P, uint8_t* __restrict__ A,
-                                             int dtid, int kt) {
+// Q4_K: 16 bytes of nibbles of chunk c (values 64c + 16hh .. +15 from the low
+// nibbles, sub-block 2c; 64c + 32 + 16hh .. +15 from the high nibbles,
+// sub-block 2c+1) of the super-block at `row`; chunk cl of this CTA's half.
+template <int H2, int CL, int HH>
+__device__ __forceinline__ void dec_q4_k_part(const uint8_t* row, uint8_t* A, int n) {
+  constexpr int c = 2 * H2 + CL;
+  const uint4 hdr = *reinterpret_cast<const uint4*>(row);
+  const uint4 qv = *reinterpret_cast<const uint4*>(row + 16 + 32 * c + 16 * HH);
+  const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x & 0xFFFFu)));
+  const float dmin = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x >> 16)));
+  int sc[2], m[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = 2 * c + h;
+    if (j < 4) {
+      sc[h] = byte_of(hdr.y, hdr.z, hdr.w, j) & 63;
+      m[h] = byte_of(hdr.y, hdr.z, hdr.w, j + 4) & 63;
+    } else {
+      const uint32_t e = byte_of(hdr.y, hdr.z, hdr.w, j + 4);
+      sc[h] = (e & 15) | ((byte_of(hdr.y, hdr.z, hdr.w, j - 4) >> 6) << 4);
+      m[h] = (e >> 4) | ((byte_of(hdr.y, hdr.z, hdr.w, j) >> 6) << 4);
+    }
+  }
+  const __half2 magic = __float2half2_rn(1024.0f);
+  const __half2 ds0 = __float2half2_rn(d * static_cast<float>(sc[0]));
+  const __half2 nm0 = __float2half2_rn(-(dmin * static_cast<float>(m[0])));
+  const __half2 ds1 = __float2half2_rn(d * static_cast<float>(sc[1]));
+  const __half2 nm1 = __float2half2_rn(-(dmin * static_cast<float>(m[1])));
+  const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+  uint32_t lo[8], hi[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    four_affine(qw[j] & 0x0F0F0F0Fu, magic, ds0, nm0, lo[2 * j], lo[2 * j + 1]);
+    four_affine((qw[j] >> 4) & 0x0F0F0F0Fu, magic, ds1, nm1, hi[2 * j], hi[2 * j + 1]);
+  }
+  constexpr int cb = 8 * CL + 2 * HH;
+  st_a_chunk(A, n, cb, lo[0], lo[1], lo[2], lo[3]);
+  st_a_chunk(A, n, cb + 1, lo[4], lo[5], lo[6], lo[7]);
+  st_a_chunk(A, n, cb + 4, hi[0], hi[1], hi[2], hi[3]);
+  st_a_chunk(A, n, cb + 5, hi[4], hi[5], hi[6], hi[7]);
+}
+
+// One warp decodes a whole stage: P holds BC packed rows (row stride
+// p_row_bytes) of this CTA's 128-value tile, A receives the fp16 operand.
+// Item i of lane l is row n = l + 32*(i & 1) and block (or Q4_K part) i >> 1:
+// eight independent blocks per lane, and the lanes of a load or store sit on
+// consecutive rows, i.e. in distinct bank groups.  ODD = the tile's k index is
+// odd (window offset 8 for Q8_0 / Q4_0, second half of a Q4_K super-block).
+template <int WT, int ODD, int NPART>
+__device__ __forceinline__ void decode_stage_warp(const uint8_t* __restrict__ P,
+                                                  uint8_t* __restrict__ A, int lane, int part) {
   constexpr int PR = p_row_bytes<WT>();
-  const int n = dtid & 63;
-  const int sel = dtid >> 6;  // warp-uniform: 0..3
-  const uint8_t* row = P + n * PR;
-  if constexpr (WT == RG_Q8_0) {
-    // one block of 34 B (32 values) per thread; window offset 0 or 8
-    const int s = (kt & 1) * 4 + sel;  // selects (offset, block)
-    switch (s) {
-      case 0: dec_q8_block<0>(row, A, n, 0); break;
-      case 1: dec_q8_block<34>(row, A, n, 1); break;
-      case 2: dec_q8_block<68>(row, A, n, 2); break;
-      case 3: dec_q8_block<102>(row, A, n, 3); break;
-      case 4: dec_q8_block<8>(row, A, n, 0); break;
-      case 5: dec_q8_block<42>(row, A, n, 1); break;
-      case 6: dec_q8_block<76>(row, A, n, 2); break;
-      default: dec_q8_block<110>(row, A, n, 3); break;
-    }
-  } else if constexpr (WT == RG_Q4_0) {
-    const int s = (kt & 1) * 4 + sel;
-    switch (s) {
-      case 0: dec_q4_0_block<0>(row, A, n, 0); break;
-      case 1: dec_q4_0_block<18>(row, A, n, 1); break;
-      case 2: dec_q4_0_block<36>(row, A, n, 2); break;
-      case 3: dec_q4_0_block<54>(row, A, n, 3); break;
-      case 4: dec_q4_0_block<8>(row, A, n, 0); break;
-      case 5: dec_q4_0_block<26>(row, A, n, 1); break;
-      case 6: dec_q4_0_block<44>(row, A, n, 2); break;
-      default: dec_q4_0_block<62>(row, A, n, 3); break;
-    }
-  } else if constexpr (WT == RG_Q4_K) {
-    // chunk c = 2*(kt & 1) + cl of the super-block: 16 bytes of nibbles
-    // (l = 16*hh .. 16*hh+15) give 16 values of sub-block 2c (low nibbles)
-    // and 16 of sub-block 2c+1 (high nibbles)
-    const int cl = sel >> 1, hh = sel & 1;
-    const int c = 2 * (kt & 1) + cl;
-    const uint4 hdr = *reinterpret_cast<const uint4*>(row);
-    const uint4 qv = *reinterpret_cast<const uint4*>(row + 16 + 32 * c + 16 * hh);
-    const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x & 0xFFFFu)));
-    const float dmin = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x >> 16)));
-    int sc[2], m[2];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int j = 2 * c + h;
-      if (j < 4) {
-        sc[h] = byte_of(hdr.y, hdr.z, hdr.w, j) & 63;
-        m[h] = byte_of(hdr.y, hdr.z, hdr.w, j + 4) & 63;
-      } else {
-        const uint32_t e = byte_of(hdr.y, hdr.z, hdr.w, j + 4);
-        sc[h] = (e & 15) | ((byte_of(hdr.y, hdr.z, hdr.w, j - 4) >> 6) << 4);
-        m[h] = (e >> 4) | ((byte_of(hdr.y, hdr.z, hdr.w, j) >> 6) << 4);
-      }
+  for (int i = 0; i < 8; ++i) {
+    if ((i & (NPART - 1)) != part) continue;  // this warp's share of the items
+    const int n = lane + 32 * (i & 1);
+    const uint8_t* row = P + n * PR;
+    constexpr int dummy = 0;
+    (void)dummy;
+    switch (i >> 1) {
+      case 0:
+        if constexpr (WT == RG_Q8_0) dec_q8_block<8 * ODD + 0>(row, A, n, 0);
+        else if constexpr (WT == RG_Q4_0) dec_q4_0_block<8 * ODD + 0>(row, A, n, 0);
+        else dec_q4_k_part<ODD, 0, 0>(row, A, n);
+        break;
+      case 1:
+        if constexpr (WT == RG_Q8_0) dec_q8_block<8 * ODD + 34>(row, A, n, 1);
+        else if constexpr (WT == RG_Q4_0) dec_q4_0_block<8 * ODD + 18>(row, A, n, 1);
+        else dec_q4_k_part<ODD, 0, 1>(row, A, n);
+        break;
+      case 2:
+        if constexpr (WT == RG_Q8_0) dec_q8_block<8 * ODD + 68>(row, A, n, 2);
+        else if constexpr (WT == RG_Q4_0) dec_q4_0_block<8 * ODD + 36>(row, A, n, 2);
+        else dec_q4_k_part<ODD, 1, 0>(row, A, n);
+        break;
+      default:
+        if constexpr (WT == RG_Q8_0) dec_q8_block<8 * ODD + 102>(row, A, n, 3);
+        else if constexpr (WT == RG_Q4_0) dec_q4_0_block<8 * ODD + 54>(row, A, n, 3);
+        else dec_q4_k_part<ODD, 1, 1>(row, A, n);
+        break;
     }
-    const __half2 magic = __float2half2_rn(1024.0f);
-    const __half2 ds0 = __float2half2_rn(d * static_cast<float>(sc[0]));
-    const __half2 nm0 = __float2half2_rn(-(dmin * static_cast<float>(m[0])));
-    const __half2 ds1 = __float2half2_rn(d * static_cast<float>(sc[1]));
-    const __half2 nm1 = __float2half2_rn(-(dmin * static_cast<float>(m[1])));
-    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-    uint32_t lo[8], hi[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      four_affine(qw[j] & 0x0F0F0F0Fu, magic, ds0, nm0, lo[2 * j], lo[2 * j + 1]);
-      four_affine((qw[j] >> 4) & 0x0F0F0F0Fu, magic, ds1, nm1, hi[2 * j], hi[2 * j + 1]);
-    }
-    // values 64*cl + 16*hh + 0..15 (low) and 64*cl + 32 + 16*hh + 0..15 (high)
-    const int cb = 8 * cl + 2 * hh;
-    st_a_chunk(A, n, cb, lo[0], lo[1], lo[2], lo[3]);
-    st_a_chunk(A, n, cb + 1, lo[4], lo[5], lo[6], lo[7]);
-    st_a_chunk(A, n, cb + 4, hi[0], hi[1], hi[2], hi[3]);
-    st_a_chunk(A, n, cb + 5, hi[4], hi[5], hi[6], hi[7]);
   }
 }
 
@@ -290,13 +301,25 @@ __device__ __forceinline__ int p_window_start(int kt) {
 }
 
 // --- the kernel -----------------------------------------------------------------
+//
+// Barriers (8 bytes each, per stage s unless noted):
+//   full_p[s]    packed W window landed in this CTA (quantized types; local TMA)
+//   full_ab[s]   operand tiles of the whole pair landed: on the MMA-issuing
+//                CTA, armed once by its producer with the pair's byte count;
+//                both CTAs' TMA loads complete on it
+//   full_dec[s]  this stage's A is decoded in every CTA: the issuing CTA's own
+//                decoder warps arrive locally, a follower's relay thread once
+//   dec_done[s]  (follower) its decoder warps are done; the relay forwards it
+//   empty[s]     the MMAs that read stage s completed (multicast commit)
+//   acc_full[2], acc_empty[2]   the two tensor-memory accumulators
+//   drain        local: the MMAs issued so far completed (abort path)
 
 template <int WT, int CG, int BT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     out_prod_tc_kernel(const __grid_constant__ CUtensorMap map_w,
                        const __grid_constant__ CUtensorMap map_y, float* __restrict__ dX,
-                       float beta, int T, int K, int n_kunits, int n_tiles, int n_chunks,
-                       WaitCtl ctl, int inject_stall) {
+                       float beta, int T, int K, int n_kunits, int n_ttiles, int band,
+                       int n_chunks, WaitCtl ctl, int inject_stall) {
   using C = Cfg<WT, CG, BT>;
   constexpr int S = C::S;
   extern __shared__ uint8_t smem_raw[];
@@ -306,12 +329,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* sB = smem + C::OFF_B;
   uint8_t* sP = smem + C::OFF_P;
   const uint32_t bar0 = smem_addr(smem + C::OFF_BAR);
-  auto full_tma = [&](int s) { return bar0 + 8u * s; };
-  auto full_dec = [&](int s) { return bar0 + 8u * (S + s); };
-  auto empty = [&](int s) { return bar0 + 8u * (2 * S + s); };
-  auto acc_full = [&](int a) { return bar0 + 8u * (3 * S + a); };
-  auto acc_empty = [&](int a) { return bar0 + 8u * (3 * S + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * (3 * S + 4);
+  auto full_p = [&](int s) { return bar0 + 8u * s; };
+  auto full_ab = [&](int s) { return bar0 + 8u * (S + s); };
+  auto full_dec = [&](int s) { return bar0 + 8u * (2 * S + s); };
+  auto dec_done = [&](int s) { return bar0 + 8u * (3 * S + s); };
+  auto empty = [&](int s) { return bar0 + 8u * (4 * S + s); };
+  auto acc_full = [&](int a) { return bar0 + 8u * (5 * S + a); };
+  auto acc_empty = [&](int a) { return bar0 + 8u * (5 * S + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (5 * S + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -319,15 +344,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
   const bool leader = rank == 0;
   const int unit = blockIdx.x / CG, n_units = gridDim.x / CG;
+  const int n_tiles = n_kunits * n_ttiles;
 
-  // arrive on the MMA-issuing CTA's copy of a barrier
-  auto arrive_leader = [&](uint32_t bar) {
-    if constexpr (CG == 2)
-      mbar_arrive_cluster(mapa_shared(bar, 0));
-    else
-      mbar_arrive(bar);
-  };
-  auto wait_pair = [&](uint32_t bar, uint32_t parity) {
+  auto wait_any = [&](uint32_t bar, uint32_t parity) {
     if constexpr (CG == 2)
       return mbar_wait_cluster(bar, parity, ctl, abort_flag);
     else
@@ -336,8 +355,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_tma(s), 1);
+      mbar_init(full_p(s), 1);
+      mbar_init(full_ab(s), 1);
       mbar_init(full_dec(s), C::FULL_DEC_COUNT);
+      mbar_init(dec_done(s), C::QUANT ? C::WARPS_PER_SLOT : 1);
       mbar_init(empty(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -367,38 +388,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // tile -> (k unit, t tile); this CTA's 128-value k tile and B rows
-  auto ktile_of = [&](int tile) { return (tile % n_kunits) * CG + static_cast<int>(rank); };
-  auto ttile_of = [&](int tile) { return tile / n_kunits; };
+  // tile -> (k unit, t tile): bands of `band` k units; inside a band the t
+  // tiles run outer, so the band's slice of W stays in L2 while every t tile
+  // of dY passes by once per band
+  auto coords = [&](int tile, int& ku, int& tt) {
+    const int per_band = band * n_ttiles;
+    const int b = tile / per_band, r = tile - b * per_band;
+    const int gk = min(band, n_kunits - b * band);
+    tt = r / gk;
+    ku = b * band + (r - tt * gk);
+  };
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
+    const uint32_t ab_bar_leader = CG == 2 ? mapa_shared(full_ab(0), 0) : full_ab(0);
     int s = 0;
     uint32_t ph = 0;
-    uint32_t pending = 0, pend_ph = 0;  // stages with a copy in flight, and its phase
+    uint32_t pend_p = 0, pend_ab = 0, pend_ph = 0;  // stages with copies in flight
     bool ok = true;
     bool skip_first = inject_stall != 0;
     for (int tile = unit; tile < n_tiles && ok; tile += n_units) {
-      const int kt = ktile_of(tile), tt = ttile_of(tile);
+      int ku, tt;
+      coords(tile, ku, tt);
+      const int kt = ku * CG + static_cast<int>(rank);
       const int ty = tt * BT + static_cast<int>(rank) * B_ROWS;
       for (int c = 0; c < n_chunks; ++c) {
         ok = __all_sync(0xffffffffu, mbar_wait(empty(s), ph ^ 1u, ctl, abort_flag));
         if (!ok) break;
         if (lane == 0) {
+          const uint32_t abar = ab_bar_leader + 8u * s;
           if (skip_first) {
             skip_first = false;  // fault injection: this stage never fills
           } else {
-            mbar_arrive_expect_tx(full_tma(s), C::TMA_BYTES);
-            if constexpr (C::QUANT) {
-              tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_tma(s),
-                          p_window_start<WT>(kt) / 4, c * BC);
-            } else {
-              tma_load_2d(smem_addr(sA + s * A_STAGE), &map_w, full_tma(s), kt * BM, c * BC);
-              tma_load_2d(smem_addr(sA + s * A_STAGE + A_COLBLK), &map_w, full_tma(s),
-                          kt * BM + 64, c * BC);
+            if (leader) {
+              mbar_arrive_expect_tx(full_ab(s), C::AB_BYTES_PAIR);
+              pend_ab |= 1u << s;
             }
-            tma_load_2d(smem_addr(sB + s * B_STAGE), &map_y, full_tma(s), c * BC, ty);
-            pending |= 1u << s;
+            if constexpr (C::QUANT) {
+              mbar_arrive_expect_tx(full_p(s), C::P_BYTES);
+              tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_p(s),
+                          p_window_start<WT>(kt) / 4, c * BC);
+              pend_p |= 1u << s;
+            } else {
+              const uint32_t a_dst = smem_addr(sA + s * A_STAGE);
+              if constexpr (CG == 2) {
+                tma_load_2d_pair(a_dst, &map_w, abar, kt * BM, c * BC);
+                tma_load_2d_pair(a_dst + A_COLBLK, &map_w, abar, kt * BM + 64, c * BC);
+              } else {
+                tma_load_2d(a_dst, &map_w, abar, kt * BM, c * BC);
+                tma_load_2d(a_dst + A_COLBLK, &map_w, abar, kt * BM + 64, c * BC);
+              }
+            }
+            if constexpr (CG == 2)
+              tma_load_2d_pair(smem_addr(sB + s * B_STAGE), &map_y, abar, c * BC, ty);
+            else
+              tma_load_2d(smem_addr(sB + s * B_STAGE), &map_y, abar, c * BC, ty);
             pend_ph = (pend_ph & ~(1u << s)) | (ph << s);
           }
         }
@@ -407,10 +451,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     if (!ok && lane == 0) {
-      // drain: every copy this thread started lands before the CTA exits
+      // drain: the copies this CTA started land before it leaves.  Local
+      // barriers are waited on; a follower's operand halves complete on the
+      // issuing CTA's barrier, which that CTA drains, and the follower waits
+      // out a copy's latency many times over.
       volatile int no_abort = 0;
-      for (int st = 0; st < S; ++st)
-        if (pending & (1u << st)) (void)mbar_wait(full_tma(st), (pend_ph >> st) & 1u, ctl, &no_abort);
+      for (int st = 0; st < S; ++st) {
+        const uint32_t p = (pend_ph >> st) & 1u;
+        if (pend_p & (1u << st)) (void)mbar_wait(full_p(st), p, ctl, &no_abort);
+        if (pend_ab & (1u << st)) (void)mbar_wait(full_ab(st), p, ctl, &no_abort);
+      }
+      if (!leader) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
+      }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (the even CTA of a pair) ----------------
@@ -422,13 +477,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int tile = unit; tile < n_tiles && ok; tile += n_units, ++j) {
         const int a = j & 1;
         const uint32_t aph = (static_cast<uint32_t>(j) >> 1) & 1u;
-        ok = __all_sync(0xffffffffu, wait_pair(acc_empty(a), aph ^ 1u));
+        ok = __all_sync(0xffffffffu, wait_any(acc_empty(a), aph ^ 1u));
         if (!ok) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * BT);
         for (int c = 0; c < n_chunks; ++c) {
-          bool got = mbar_wait(full_tma(s), ph, ctl, abort_flag);
-          got = got && wait_pair(full_dec(s), ph);
+          bool got = wait_any(full_ab(s), ph);
+          if constexpr (C::QUANT) got = got && wait_any(full_dec(s), ph);
           ok = __all_sync(0xffffffffu, got);
           if (!ok) break;
           tc_fence_after();
@@ -474,33 +529,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         (void)mbar_wait(drain_bar, 0, ctl, &no_abort);
       }
     }
-  } else if (warp >= DEC_WARP0 && warp < DEC_WARP0 + DEC_WARPS) {
-    // ---------------- decoders (relays for F16/BF16) ----------------
-    const int dtid = threadIdx.x - DEC_WARP0 * 32;
-    int s = 0;
-    uint32_t ph = 0;
-    bool ok = true;
-    for (int tile = unit; tile < n_tiles && ok; tile += n_units) {
-      const int kt = ktile_of(tile);
-      for (int c = 0; c < n_chunks; ++c) {
-        ok = __all_sync(0xffffffffu, mbar_wait(full_tma(s), ph, ctl, abort_flag));
-        if (!ok) break;
-        if constexpr (C::QUANT) {
-          decode_stage<WT>(sP + s * C::P_STAGE, sA + s * A_STAGE, dtid, kt);
-          fence_proxy_async_smem();
+  } else if (warp == 2) {
+    // ---------------- relay (a follower's decoded stages -> the issuing CTA) ----------------
+    if constexpr (CG == 2 && C::QUANT) {
+      if (!leader) {
+        const uint32_t dec_leader = mapa_shared(full_dec(0), 0);
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int tile = unit; tile < n_tiles && ok; tile += n_units) {
+          for (int c = 0; c < n_chunks; ++c) {
+            ok = __all_sync(0xffffffffu, mbar_wait(dec_done(s), ph, ctl, abort_flag));
+            if (!ok) break;
+            if (lane == 0) mbar_arrive_cluster(dec_leader + 8u * s);
+            __syncwarp();
+            if (++s == S) { s = 0; ph ^= 1u; }
+          }
         }
-        __syncwarp();
-        if (lane == 0) arrive_leader(full_dec(s));
-        if (++s == S) { s = 0; ph ^= 1u; }
+      }
+    }
+  } else if (warp >= DEC_WARP0 && warp < DEC_WARP0 + DEC_WARPS) {
+    // ---------------- decoders: warps own stage slots ----------------
+    // (the warps of a slot take its phases in order, so a parity wait can
+    // never be satisfied by the slot's previous phase)
+    if constexpr (C::QUANT) {
+      constexpr int WPS = C::WARPS_PER_SLOT;
+      const int s = (warp - DEC_WARP0) / WPS;
+      const int part = (warp - DEC_WARP0) % WPS;
+      {
+        const uint32_t done_bar = (leader ? full_dec(0) : dec_done(0)) + 8u * s;
+        const int total = ((n_tiles - unit + n_units - 1) / n_units) * n_chunks;  // stages of this CTA
+        uint32_t ph = 0;
+        for (int g = s; g < total; g += S, ph ^= 1u) {
+          int ku, tt;
+          coords(unit + (g / n_chunks) * n_units, ku, tt);
+          const int kt = ku * CG + static_cast<int>(rank);
+          if (!__all_sync(0xffffffffu, mbar_wait(full_p(s), ph, ctl, abort_flag))) break;
+          if (kt & 1)
+            decode_stage_warp<WT, 1, WPS>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part);
+          else
+            decode_stage_warp<WT, 0, WPS>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(done_bar);
+        }
       }
     }
   } else if (warp >= EPI_WARP0) {
     // ---------------- epilogue ----------------
     const int eq = warp & 3;  // TMEM lanes 32*eq .. 32*eq+31
+    const uint32_t empty_leader = CG == 2 ? mapa_shared(acc_empty(0), 0) : acc_empty(0);
     bool ok = true;
     int j = 0;
     for (int tile = unit; tile < n_tiles && ok; tile += n_units, ++j) {
-      const int kt = ktile_of(tile), tt = ttile_of(tile);
+      int ku, tt;
+      coords(tile, ku, tt);
+      const int kt = ku * CG + static_cast<int>(rank);
       const int a = j & 1;
       const uint32_t aph = (static_cast<uint32_t>(j) >> 1) & 1u;
       ok = __all_sync(0xffffffffu, mbar_wait(acc_full(a), aph, ctl, abort_flag));
@@ -534,7 +618,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) arrive_leader(acc_empty(a));
+      if (lane == 0) {
+        if constexpr (CG == 2)
+          mbar_arrive_cluster(empty_leader + 8u * a);
+        else
+          mbar_arrive(acc_empty(a));
+      }
     }
   }
 
@@ -590,7 +679,6 @@ static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my, flo
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   WaitCtl ctl{dev.status, dev.wait_limit_ns};
-  const int n_tiles = p.n_kunits * p.n_ttiles;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(tc::NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
@@ -614,8 +702,8 @@ static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my, flo
   }
   const int units = std::min(p.grid / CG, mc);
   cfg.gridDim = dim3(static_cast<unsigned>(units * CG), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, mw, my, dX, beta, T, K, p.n_kunits, n_tiles, p.n_chunks,
-                            ctl, inject);
+  return cudaLaunchKernelEx(&cfg, kern, mw, my, dX, beta, T, K, p.n_kunits, p.n_ttiles, p.band,
+                            p.n_chunks, ctl, inject);
 }
 
 template <int WT>
@@ -629,7 +717,11 @@ static cudaError_t launch_tc_w(const CUtensorMap& mw, const CUtensorMap& my, flo
 cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
                       int64_t ld_dy16, int64_t T, float* dX, float beta, const DevInfo& dev,
                       cudaStream_t stream, int cg_force, int inject_stall) {
-  const TcPlan p = plan_tc(N, K, T, dev, cg_force);
+  TcPlan p = plan_tc(N, K, T, dev, cg_force);
+  // band of k units whose slice of W fits comfortably in L2 (48 MB)
+  const double w_per_value = is_quant(wtype) ? static_cast<double>(block_bytes(wtype)) / block_values(wtype) : 2.0;
+  const double slice = static_cast<double>(N) * (tc::BM * p.cg) * w_per_value;
+  p.band = static_cast<int>(std::max(1.0, std::min<double>(p.n_kunits, 48.0 * 1024 * 1024 / slice)));
   CUtensorMap mw, my;
   CUresult r;
   if (is_quant(wtype)) {
