@@ -23,9 +23,9 @@
 //      warp 0      TMA producer (packed W window or F16/BF16 operand tile, and
 //                  the 16-bit dY tile, per stage of 64 contraction rows);
 //      warp 1      tensor-memory owner and (even CTA) MMA issuer;
-//      warp 2      (follower CTA) relays its decoded stages to the issuing CTA;
-//      warps 4-11  decoders, one per stage slot: packed blocks -> fp16 operand
-//                  tile, 128-byte swizzled, MN-major (idle for F16/BF16);
+//      warps 2-11  decoders, two per stage slot: packed blocks -> fp16
+//                  operand tile, 128-byte swizzled, MN-major; a follower's
+//                  warps arrive on the issuing CTA's barrier (idle for F16/BF16);
 //      warps 12-15 epilogue: tcgen05.ld -> beta*dX + acc -> global.
 //  * F32 accumulators in tensor memory, two per CTA (2 x BT columns): the
 //    epilogue of one tile overlaps the main loop of the next.
@@ -45,7 +45,7 @@ constexpr int BC = 64;            // contraction rows (n) per pipeline stage
 constexpr int UMMA_K = 16;        // contraction rows per tcgen05.mma (16-bit inputs)
 constexpr int B_ROWS = 128;       // rows of t per CTA in a B stage
 constexpr int NUM_THREADS = 512;  // 16 warps
-constexpr int DEC_WARP0 = 4, DEC_WARPS = 8, EPI_WARP0 = 12;
+constexpr int DEC_WARP0 = 2, DEC_WARPS = 10, EPI_WARP0 = 12;
 constexpr int A_STAGE = BC * BM * 2;      // 16 KB: 64 rows of n x 128 fp16 values of k
 constexpr int A_COLBLK = BC * 128;        // 8 KB: one 64-value column block of k
 constexpr int B_STAGE = B_ROWS * 128;     // 16 KB: 128 rows of t x 64 16-bit values of n
@@ -65,16 +65,16 @@ struct Cfg {
   static constexpr bool BF = WT == RG_BF16;
   static constexpr int P_STAGE = QUANT ? ((BC * p_row_bytes<WT>() + 1023) / 1024) * 1024 : 0;
   static constexpr int STAGE = A_STAGE + B_STAGE + P_STAGE;
-  // quantized: four slots, each decoded by two warps; F16/BF16: as deep as fits
-  static constexpr int S = QUANT ? 4 : std::min(8, SMEM_BUDGET / STAGE);
+  // quantized: five slots, each decoded by two warps; F16/BF16: as deep as fits
+  static constexpr int S = QUANT ? 5 : std::min(8, SMEM_BUDGET / STAGE);
   static constexpr int WARPS_PER_SLOT = QUANT ? DEC_WARPS / S : 0;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + S * A_STAGE;
   static constexpr int OFF_P = OFF_B + S * B_STAGE;
   static constexpr int OFF_BAR = OFF_P + S * P_STAGE;
-  // barriers: full_p, full_ab, full_dec, dec_done, empty (S each), acc_full[2],
+  // barriers: full_p, full_ab, full_dec, empty (S each), acc_full[2],
   // acc_empty[2], drain
-  static constexpr int NUM_BARS = 5 * S + 5;
+  static constexpr int NUM_BARS = 4 * S + 5;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024 B alignment
   static constexpr uint32_t P_BYTES = QUANT ? BC * p_row_bytes<WT>() : 0;
@@ -83,8 +83,8 @@ struct Cfg {
   static constexpr uint32_t TMEM_COLS = 2 * BT;
   static constexpr int MMA_M = BM * CG;
   static constexpr uint32_t IDESC = idesc_f16(BF, MMA_M, BT, /*A MN-major*/ true, /*B*/ false);
-  // the slot's decoder warps, plus a follower's relay
-  static constexpr uint32_t FULL_DEC_COUNT = (QUANT ? DEC_WARPS / S : 1) + (CG == 2 ? 1 : 0);
+  // the slot's decoder warps of every CTA of the pair
+  static constexpr uint32_t FULL_DEC_COUNT = (QUANT ? WARPS_PER_SLOT : 1) * CG;
   static constexpr uint32_t ACC_EMPTY_COUNT = 4 * CG;
   static_assert(BT / CG == B_ROWS, "each CTA holds 128 rows of t in a B stage");
   static_assert(S >= 3, "pipeline depth");
@@ -307,9 +307,8 @@ __device__ __forceinline__ int p_window_start(int kt) {
 //   full_ab[s]   operand tiles of the whole pair landed: on the MMA-issuing
 //                CTA, armed once by its producer with the pair's byte count;
 //                both CTAs' TMA loads complete on it
-//   full_dec[s]  this stage's A is decoded in every CTA: the issuing CTA's own
-//                decoder warps arrive locally, a follower's relay thread once
-//   dec_done[s]  (follower) its decoder warps are done; the relay forwards it
+//   full_dec[s]  this stage's A is decoded in every CTA: every decoder warp
+//                of the slot, in either CTA, arrives on the issuing CTA's copy
 //   empty[s]     the MMAs that read stage s completed (multicast commit)
 //   acc_full[2], acc_empty[2]   the two tensor-memory accumulators
 //   drain        local: the MMAs issued so far completed (abort path)
@@ -332,11 +331,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto full_p = [&](int s) { return bar0 + 8u * s; };
   auto full_ab = [&](int s) { return bar0 + 8u * (S + s); };
   auto full_dec = [&](int s) { return bar0 + 8u * (2 * S + s); };
-  auto dec_done = [&](int s) { return bar0 + 8u * (3 * S + s); };
-  auto empty = [&](int s) { return bar0 + 8u * (4 * S + s); };
-  auto acc_full = [&](int a) { return bar0 + 8u * (5 * S + a); };
-  auto acc_empty = [&](int a) { return bar0 + 8u * (5 * S + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * (5 * S + 4);
+  auto empty = [&](int s) { return bar0 + 8u * (3 * S + s); };
+  auto acc_full = [&](int a) { return bar0 + 8u * (4 * S + a); };
+  auto acc_empty = [&](int a) { return bar0 + 8u * (4 * S + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (4 * S + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -358,7 +356,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(full_p(s), 1);
       mbar_init(full_ab(s), 1);
       mbar_init(full_dec(s), C::FULL_DEC_COUNT);
-      mbar_init(dec_done(s), C::QUANT ? C::WARPS_PER_SLOT : 1);
       mbar_init(empty(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -529,25 +526,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         (void)mbar_wait(drain_bar, 0, ctl, &no_abort);
       }
     }
-  } else if (warp == 2) {
-    // ---------------- relay (a follower's decoded stages -> the issuing CTA) ----------------
-    if constexpr (CG == 2 && C::QUANT) {
-      if (!leader) {
-        const uint32_t dec_leader = mapa_shared(full_dec(0), 0);
-        int s = 0;
-        uint32_t ph = 0;
-        bool ok = true;
-        for (int tile = unit; tile < n_tiles && ok; tile += n_units) {
-          for (int c = 0; c < n_chunks; ++c) {
-            ok = __all_sync(0xffffffffu, mbar_wait(dec_done(s), ph, ctl, abort_flag));
-            if (!ok) break;
-            if (lane == 0) mbar_arrive_cluster(dec_leader + 8u * s);
-            __syncwarp();
-            if (++s == S) { s = 0; ph ^= 1u; }
-          }
-        }
-      }
-    }
   } else if (warp >= DEC_WARP0 && warp < DEC_WARP0 + DEC_WARPS) {
     // ---------------- decoders: warps own stage slots ----------------
     // (the warps of a slot take its phases in order, so a parity wait can
@@ -557,12 +535,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int s = (warp - DEC_WARP0) / WPS;
       const int part = (warp - DEC_WARP0) % WPS;
       {
-        const uint32_t done_bar = (leader ? full_dec(0) : dec_done(0)) + 8u * s;
+        // a follower's warps arrive on the issuing CTA's barrier directly
+        const uint32_t done_bar = CG == 2 ? mapa_shared(full_dec(s), 0) : full_dec(s);
         const int total = ((n_tiles - unit + n_units - 1) / n_units) * n_chunks;  // stages of this CTA
+        // walk this warp's stages s, s + S, ... without per-stage divisions
+        int tile = unit, c = s;
+        while (c >= n_chunks) { c -= n_chunks; tile += n_units; }
+        int ku, tt;
+        if (tile < n_tiles) coords(tile, ku, tt);
         uint32_t ph = 0;
         for (int g = s; g < total; g += S, ph ^= 1u) {
-          int ku, tt;
-          coords(unit + (g / n_chunks) * n_units, ku, tt);
           const int kt = ku * CG + static_cast<int>(rank);
           if (!__all_sync(0xffffffffu, mbar_wait(full_p(s), ph, ctl, abort_flag))) break;
           if (kt & 1)
@@ -571,7 +553,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             decode_stage_warp<WT, 0, WPS>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part);
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(done_bar);
+          if (lane == 0) {
+            if constexpr (CG == 2)
+              mbar_arrive_cluster(done_bar);
+            else
+              mbar_arrive(done_bar);
+          }
+          c += S;
+          if (c >= n_chunks) {
+            while (c >= n_chunks) { c -= n_chunks; tile += n_units; }
+            if (tile < n_tiles) coords(tile, ku, tt);
+          }
         }
       }
     }
