@@ -40,6 +40,23 @@ from quantized_weight_out_gb300 import inputs  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 
 
+def _traffic_record():
+    """DRAM bytes per tensor-core launch from the committed ncu summary, or
+    None when the kernel source has changed since those counters were taken."""
+    import hashlib
+    rec = os.path.join(ROOT, "profiles", "tc_traffic.json")
+    src = os.path.join(ROOT, "quantized_weight_out_gb300", "csrc", "rg_tc.cu")
+    if not (os.path.exists(rec) and os.path.exists(src)):
+        return None, None
+    with open(rec) as f:
+        d = json.load(f)
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    if d.get("source_sha256") != sha:
+        return None, d.get("workload")
+    return d.get("dram_bytes_per_launch"), d.get("workload")
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -242,11 +259,15 @@ def run_ours(args):
             return rg.rg_out_prod_variant(forced, p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, stream)
         return rg.rg_out_prod(p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, stream)
 
+    is_tc = [v in (rg.RG_VARIANT_TC, rg.RG_VARIANT_TC_SINGLE, rg.RG_VARIANT_TC_PAIR) for v in variants]
+
     def step(events=None):
         for i, p in enumerate(problems):
             W, dY, dX = devbuf[i]
             if events is not None:
                 events[i][0].record(stream)
+                if is_tc[i]:  # the library records these around its GEMM kernel
+                    rg.rg_profile_next_gemm(events[i][2], events[i][3])
             st = call(p, W, dY, dX)
             if events is not None:
                 events[i][1].record(stream)
@@ -258,6 +279,7 @@ def run_ours(args):
     rg.check(rg.rg_check(stream), "warmup")
 
     per_call = [[] for _ in problems]
+    per_gemm = [[] for _ in problems]
     sampler = ClockSampler(_bus_id(torch, dev))
     if world > 1:
         torch.distributed.barrier()
@@ -265,8 +287,15 @@ def run_ours(args):
     sampler.start()
     time.sleep(0.3)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)]
             for _ in problems] for _ in range(args.steps)]
+    # torch creates an event's handle at its first record; record every event
+    # once so the library gets real handles (its later records are the ones timed)
+    for row in evs:
+        for quad in row:
+            for e in quad:
+                e.record(stream)
+    torch.cuda.synchronize()
     ev0.record(stream)
     for s in range(args.steps):
         step(evs[s])
@@ -278,6 +307,8 @@ def run_ours(args):
     for s in range(args.steps):
         for i in range(len(problems)):
             per_call[i].append(evs[s][i][0].elapsed_time(evs[s][i][1]))
+            if is_tc[i]:
+                per_gemm[i].append(evs[s][i][2].elapsed_time(evs[s][i][3]))
     if world > 1:
         t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -343,21 +374,29 @@ def run_ours(args):
     # roofline of the tensor-core launches (the dominant kernel)
     peaks, src = _peaks()
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    tc = [i for i, v in enumerate(variants)
-          if v in (rg.RG_VARIANT_TC, rg.RG_VARIANT_TC_SINGLE, rg.RG_VARIANT_TC_PAIR)]
+    traffic, traffic_wl = _traffic_record()
+    if traffic_wl is not None and traffic_wl != args.workload:
+        traffic = None
+    tc = [i for i in range(len(problems)) if is_tc[i]]
     tc_flops = sum(problems[i].flops for i in tc)
-    tc_ms = sum(statistics.mean(per_call[i]) for i in tc) if tc else 0.0
-    achieved = tc_flops / (tc_ms * 1e-3) / 1e12 if tc_ms > 0 else None
+    gemm_ms = sum(statistics.mean(per_gemm[i]) for i in tc) if tc else 0.0
+    call_ms = sum(statistics.mean(per_call[i]) for i in tc) if tc else 0.0
+    achieved = tc_flops / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak if achieved else None, "traffic": None,
+            "frac": achieved / peak if achieved else None, "traffic": traffic,
+            "traffic_unit": "bytes per launch (ncu dram read+write, profiles/tc_traffic.json)",
             "peak_source": f"{src} bf16_tflops_sustained (dense fp16 = bf16 nominal)",
-            "kernel": "rg_out_prod tensor-core launches (dY conversion + fused decode GEMM)"}
+            "kernel": "out_prod_tc_kernel (fused decode + tcgen05 GEMM), events around each launch",
+            "launches_per_step": len(tc), "flops_per_launch": tc_flops / max(1, len(tc)),
+            "ms_per_launch": gemm_ms / max(1, len(tc)),
+            "dy_conversion_share_of_calls": (call_ms - gemm_ms) / call_ms if call_ms > 0 else None}
 
     calls = []
     for i, p in enumerate(problems):
         t = statistics.median(per_call[i]) * 1e-3
         calls.append({"name": p.name, "wtype": inputs.TYPE_NAMES[p.wtype], "N": p.N, "K": p.K,
                       "T": p.T, "variant": int(variants[i]), "ms": t * 1e3,
+                      "gemm_ms": statistics.median(per_gemm[i]) if per_gemm[i] else None,
                       "tflops": p.flops / t / 1e12,
                       "effective_gbs": p.algorithmic_bytes() / t / 1e9,
                       "roofline_frac": max(p.flops / (peak * 1e12),

@@ -150,6 +150,14 @@ int rg_check(void* stream);
 /* Library version, (major << 16) | minor. */
 int rg_version(void);
 
+/* Measurement aid: the next tensor-core OUT_PROD call (rg_out_prod* choosing
+ * a TC variant) made from this host thread records the CUDA event `before`
+ * on its stream right before its GEMM kernel and `after` right after it
+ * (cudaEvent_t handles passed as void*), so the kernel alone can be timed
+ * inside a larger timed region; the dY conversion is outside the pair.  The
+ * events are used once, then forgotten.  NULL, NULL clears.  Returns RG_OK. */
+int rg_profile_next_gemm(void* before, void* after);
+
 /* Test hook for failure detection: enqueues one kernel whose single wait can
  * never complete, so that it gives up after timeout_ms (1..60000; else
  * RG_ERR_ARG) and records RG_ERR_TIMEOUT for the next rg_check.  The context

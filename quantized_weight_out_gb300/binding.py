@@ -38,6 +38,7 @@ SIGNATURES = [
     ("rg_check", _I, [_VP]),
     ("rg_version", _I, []),
     ("rg_debug_wait_probe", _I, [_I, _VP]),
+    ("rg_profile_next_gemm", _I, [_VP, _VP]),
 ]
 
 _lib = None
@@ -136,6 +137,18 @@ def rg_version() -> int:
 
 def rg_debug_wait_probe(timeout_ms, stream=None) -> int:
     return load().rg_debug_wait_probe(timeout_ms, _stream(stream))
+
+
+def _event(e):
+    if e is None:
+        return None
+    if isinstance(e, int):
+        return e
+    return int(e.cuda_event)
+
+
+def rg_profile_next_gemm(before, after) -> int:
+    return load().rg_profile_next_gemm(_event(before), _event(after))
 
 
 def check(status: int, what: str = "") -> None:

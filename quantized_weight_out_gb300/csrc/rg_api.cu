@@ -123,6 +123,10 @@ size_t tc_workspace(int64_t N, int64_t T) {
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? RG_OK : RG_ERR_CUDA; }
 
+// rg_profile_next_gemm: events for the next tensor-core launch of this thread
+thread_local cudaEvent_t t_prof_before = nullptr;
+thread_local cudaEvent_t t_prof_after = nullptr;
+
 // One stream-ordered memory pool per device for rg_out_prod's own workspace:
 // allocations are cached by the pool (release threshold: never), so a steady
 // state of calls does not reach the driver, and stream capture records them as
@@ -181,10 +185,14 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
   const bool bf16 = wtype == RG_BF16;
   const int64_t ld = tc_dy16_ld(N);
   cudaError_t e = launch_convert_dy(dY, T, N, ld, bf16, static_cast<uint16_t*>(buf), *dev, stream);
+  cudaEvent_t ev0 = t_prof_before, ev1 = t_prof_after;
+  t_prof_before = t_prof_after = nullptr;
+  if (e == cudaSuccess && ev0) e = cudaEventRecord(ev0, stream);
   if (e == cudaSuccess)
     e = launch_tc(wtype, W, N, K, static_cast<const uint16_t*>(buf), ld, T, dX, beta, *dev,
                   stream, variant == RG_VARIANT_TC_SINGLE ? 1 : variant == RG_VARIANT_TC_PAIR ? 2 : 0,
                   env().inject_stall);
+  if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, stream);
   if (own_ws) {
     const cudaError_t f = cudaFreeAsync(buf, stream);
     if (e == cudaSuccess) e = f;
@@ -318,5 +326,11 @@ int rg_debug_wait_probe(int timeout_ms, void* stream) {
 }
 
 int rg_version(void) { return (0 << 16) | 1; }
+
+int rg_profile_next_gemm(void* before, void* after) {
+  t_prof_before = static_cast<cudaEvent_t>(before);
+  t_prof_after = static_cast<cudaEvent_t>(after);
+  return RG_OK;
+}
 
 }  // extern "C"
