@@ -118,6 +118,39 @@ int rg_out_prod_ws(int variant, int wtype, const void* W, int64_t N, int64_t K,
                    const float* dY, int64_t T, float* dX, float beta,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes of the fixed device scratch behind rg_out_prod_noalloc. */
+#define RG_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * rg_out_prod for callers that cannot allocate device memory.  (This entry
+ * point has no counterpart in the pages this library follows; it is a
+ * convenience of this implementation.)
+ *
+ * Who needs it: code that must not call cudaMalloc or a memory pool at all,
+ * e.g. a runtime that owns every byte of device memory through its own
+ * allocator and forbids others, a callback or real-time path that cannot
+ * afford the allocator's locking or implicit device synchronization, or an
+ * embedding that runs under an allocation guard.  rg_out_prod takes its dY
+ * workspace from a memory pool; rg_out_prod_ws needs a buffer the caller
+ * allocated.  This call needs neither: the tensor-core path converts dY into
+ * a fixed scratch array compiled into the library (RG_NOALLOC_SCRATCH_BYTES,
+ * 32 MiB), which every GPU that loads the library keeps until the process
+ * exits.  It calls no cudaMalloc, cudaFree or pool routine.
+ *
+ * Same arguments, layouts and results as rg_out_prod (same kernels, same
+ * variant choice).  Limits: when the chosen variant is a tensor-core one, the
+ * 16-bit copy of dY, T * (N rounded up to 8) * 2 bytes, must fit the scratch,
+ * else RG_ERR_ARG and nothing is launched (e.g. T = 2048 allows N <= 8192).
+ * The scratch is shared by every call on a device and keeps the last call's
+ * contents (each call overwrites what it reads; nothing needs clearing), so
+ * calls that may overlap on the GPU (different streams, or different host
+ * threads) race on it: order them on one stream.  The first call on a device
+ * looks up the scratch's device address (a runtime query, no allocation);
+ * make that first call before any stream capture.
+ */
+int rg_out_prod_noalloc(int wtype, const void* W, int64_t N, int64_t K,
+                        const float* dY, int64_t T, float* dX, float beta, void* stream);
+
 /* The variant RG_VARIANT_AUTO picks for this shape (ignores RG_VARIANT). */
 int rg_select_variant(int wtype, int64_t N, int64_t K, int64_t T);
 

@@ -39,7 +39,10 @@ SIGNATURES = [
     ("rg_version", _I, []),
     ("rg_debug_wait_probe", _I, [_I, _VP]),
     ("rg_profile_next_gemm", _I, [_VP, _VP]),
+    ("rg_out_prod_noalloc", _I, [_I, _VP, _I64, _I64, _VP, _I64, _VP, _F, _VP]),
 ]
+
+RG_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _lib = None
 _lock = threading.Lock()
@@ -91,6 +94,11 @@ def rg_out_prod(wtype, W, N, K, dY, T, dX, beta, stream=None) -> int:
 
 def rg_out_prod_variant(variant, wtype, W, N, K, dY, T, dX, beta, stream=None) -> int:
     return load().rg_out_prod_variant(variant, wtype, _ptr(W), N, K, _ptr(dY), T, _ptr(dX), beta,
+                                      _stream(stream))
+
+
+def rg_out_prod_noalloc(wtype, W, N, K, dY, T, dX, beta, stream=None) -> int:
+    return load().rg_out_prod_noalloc(wtype, _ptr(W), N, K, _ptr(dY), T, _ptr(dX), beta,
                                       _stream(stream))
 
 

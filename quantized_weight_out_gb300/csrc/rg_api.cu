@@ -18,6 +18,12 @@ namespace rg {
 // RG_ERR_TIMEOUT here; rg_check reads and clears it.
 __device__ int g_status_word;
 
+// Scratch of rg_out_prod_noalloc: the tensor-core path's 16-bit copy of dY
+// lives in this fixed array instead of in memory allocated per call.  It is
+// part of the library's device image, so every GPU that loads the library
+// holds it (RG_NOALLOC_SCRATCH_BYTES) until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[RG_NOALLOC_SCRATCH_BYTES];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -152,6 +158,25 @@ int pool_for(int d, cudaMemPool_t* out) {
   return RG_OK;
 }
 
+// Device address of g_noalloc_scratch on device d (which must be current),
+// looked up once per device.  Host code must not use the symbol itself: on
+// the host it names a stand-in, not device memory.
+void* g_noalloc_ptr[kMaxDevices];
+bool g_noalloc_ready[kMaxDevices];
+
+int noalloc_scratch(int d, void** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_noalloc_ready[d]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return RG_ERR_CUDA;
+    g_noalloc_ptr[d] = p;
+    g_noalloc_ready[d] = true;
+  }
+  *out = g_noalloc_ptr[d];
+  return RG_OK;
+}
+
 int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float* dY, int64_t T,
         float* dX, float beta, void* ws, size_t ws_bytes, bool own_ws, cudaStream_t stream) {
   bool empty = false;
@@ -258,6 +283,28 @@ int rg_out_prod_ws(int variant, int wtype, const void* W, int64_t N, int64_t K, 
                    int64_t T, float* dX, float beta, void* workspace, size_t workspace_bytes,
                    void* stream) {
   return run(variant, wtype, W, N, K, dY, T, dX, beta, workspace, workspace_bytes, false,
+             static_cast<cudaStream_t>(stream));
+}
+
+int rg_out_prod_noalloc(int wtype, const void* W, int64_t N, int64_t K, const float* dY,
+                        int64_t T, float* dX, float beta, void* stream) {
+  bool empty = false;
+  int st = validate(wtype, W, N, K, dY, T, dX, &empty);
+  if (st != RG_OK || empty) return st;
+  int variant = env().variant;
+  if (variant == RG_VARIANT_AUTO) variant = select_variant(wtype, N, K, T);
+  const bool tc = variant == RG_VARIANT_TC || variant == RG_VARIANT_TC_SINGLE ||
+                  variant == RG_VARIANT_TC_PAIR;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  if (tc && N > 0) {
+    if (tc_workspace(N, T) > static_cast<size_t>(RG_NOALLOC_SCRATCH_BYTES)) return RG_ERR_ARG;
+    DevInfo* dev = nullptr;
+    if ((st = current_dev(&dev)) != RG_OK) return st;
+    if ((st = noalloc_scratch(dev->device, &ws)) != RG_OK) return st;
+    ws_bytes = static_cast<size_t>(RG_NOALLOC_SCRATCH_BYTES);
+  }
+  return run(variant, wtype, W, N, K, dY, T, dX, beta, ws, ws_bytes, false,
              static_cast<cudaStream_t>(stream));
 }
 
