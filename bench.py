@@ -136,11 +136,9 @@ def oracle_sample(problems, t_rows: int, n_rows: int | None = None):
     data = []
     for p in problems:
         n = p.N if n_rows is None else min(n_rows, p.N)
-        rb = inputs.row_bytes(p.wtype, p.K)
-        W = p.weight()[: n * rb].copy()
-        dY = np.ascontiguousarray(p.dy()[:t_rows, :n])
-        dX0 = p.dx0()
-        data.append((p, n, W, dY, None if dX0 is None else dX0[:t_rows].copy()))
+        W = p.weight(n)
+        dY = np.ascontiguousarray(p.dy(t_rows)[:, :n])
+        data.append((p, n, W, dY, p.dx0(t_rows)))
     t0 = time.perf_counter()
     flops = 0
     for p, n, W, dY, dX0 in data:
@@ -162,7 +160,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="layer7b_t8192")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-rows", type=int, default=256, help="dY rows per call, CPU baseline sample")
+    ap.add_argument("--cpu-rows", type=int, default=1024, help="dY rows per call, CPU baseline sample")
     ap.add_argument("--ref-rows", type=int, default=32, help="dY rows per call, reference-arm step")
     ap.add_argument("--ref-wrows", type=int, default=512, help="W rows per call, reference-arm step")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
@@ -187,6 +185,24 @@ def _dist():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x over all ranks (the step time of a job is its
+    slowest rank's); x itself without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_replica_step: int, ms_per_step: float, world: int) -> float:
+    """Whole-job throughput of `world` replicas, each doing the step's flops,
+    timed by the slowest rank."""
+    return world * flops_per_replica_step / (ms_per_step * 1e-3) / 1e12
 
 
 def _dtype_name(problems):
@@ -309,13 +325,10 @@ def run_ours(args):
             per_call[i].append(evs[s][i][0].elapsed_time(evs[s][i][1]))
             if is_tc[i]:
                 per_gemm[i].append(evs[s][i][2].elapsed_time(evs[s][i][3]))
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
     flops_step = sum(p.flops for p in problems)
-    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    value = job_tflops(flops_step, ms_step, world)
 
     # end to end: host buffers, copies inside the timed loop
     e2e = None
@@ -363,12 +376,8 @@ def run_ours(args):
             stream.wait_event(ev)
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1) / args.steps
-        if world > 1:
-            t = torch.tensor([ems], device=dev, dtype=torch.float64)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * flops_step / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
+        ems = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+        e2e = {"value": job_tflops(flops_step, ems, world), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems}
 
     # roofline of the tensor-core launches (the dominant kernel)

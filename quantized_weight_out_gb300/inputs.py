@@ -276,18 +276,24 @@ class Problem:
             b += 4 * self.T * self.K
         return b
 
-    def weight(self) -> np.ndarray:
-        return gen_weight(self.wtype, self.N, self.K, self.seed, 1 + self.stream_base)
+    # Every generator is counter-based in row-major order, so the first `rows`
+    # rows of an input are exactly what a smaller call would generate.
 
-    def dy(self) -> np.ndarray:
-        return normal_f32(self.seed, 2 + self.stream_base, self.T * self.N,
-                          self.dy_sigma).reshape(self.T, self.N)
+    def weight(self, rows: Optional[int] = None) -> np.ndarray:
+        n = self.N if rows is None else min(rows, self.N)
+        return gen_weight(self.wtype, n, self.K, self.seed, 1 + self.stream_base)
 
-    def dx0(self) -> Optional[np.ndarray]:
+    def dy(self, rows: Optional[int] = None) -> np.ndarray:
+        t = self.T if rows is None else min(rows, self.T)
+        return normal_f32(self.seed, 2 + self.stream_base, t * self.N,
+                          self.dy_sigma).reshape(t, self.N)
+
+    def dx0(self, rows: Optional[int] = None) -> Optional[np.ndarray]:
         if self.beta == 0.0:
             return None
-        return normal_f32(self.seed, 3 + self.stream_base, self.T * self.K,
-                          1e-3).reshape(self.T, self.K)
+        t = self.T if rows is None else min(rows, self.T)
+        return normal_f32(self.seed, 3 + self.stream_base, t * self.K,
+                          1e-3).reshape(t, self.K)
 
 
 def _layer_sweep(T: int = 8192) -> List[Problem]:

@@ -72,3 +72,13 @@ def test_workloads_and_row_bytes():
     assert w["f16_5120x17408_t4096_beta1"][0].beta == 1.0
     assert sum(p.flops for p in w["layer7b_t8192"]) == 3_573_412_790_272
     assert w["q4_k_14336x4096_t2048"][0].w_bytes == 33_030_144
+
+
+def test_row_prefixes_are_smaller_calls():
+    """The first rows of every generated input equal a smaller call's."""
+    for wt in (inputs.Q8_0, inputs.Q4_0, inputs.Q4_K, inputs.F16, inputs.BF16):
+        p = inputs.Problem("x", wt, 40, 512, 12, 1e-3, 1.0, stream_base=32)
+        rb = inputs.row_bytes(wt, 512)
+        assert np.array_equal(p.weight()[: 7 * rb], p.weight(7))
+        assert np.array_equal(p.dy()[:5], p.dy(5))
+        assert np.array_equal(p.dx0()[:3], p.dx0(3))
