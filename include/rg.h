@@ -73,8 +73,10 @@ typedef enum {
     RG_VARIANT_AUTO = 0,   /* the shape dispatcher's choice (what rg_out_prod runs)        */
     RG_VARIANT_TC = 1,     /* fused decode + tcgen05 tensor-core GEMM, fp16/bf16 operands,
                               F32 accumulation in tensor memory                             */
-    RG_VARIANT_SMALLT = 2, /* small-T, weight-bandwidth-bound: coalesced 16-byte weight
-                              loads, decode in registers, F32 FMA, cluster reduction        */
+    RG_VARIANT_SMALLT = 2, /* small-T, weight-bandwidth-bound: a warp streams whole rows
+                              of W (vector loads), exact F32 decode in registers, F32 FMA
+                              with up to 8 dY rows; rows split over many CTAs, partial
+                              sums added in a fixed order by a second kernel          */
     RG_VARIANT_SIMT32 = 3, /* exact F32 decode and F32 FMA with blocked accumulation: the
                               full-precision variant (slow; a correctness reference)        */
     RG_VARIANT_TC_SINGLE = 4, /* RG_VARIANT_TC with one-CTA 128 x 128 tiles                */
@@ -90,8 +92,9 @@ typedef enum {
  * the environment variable RG_VARIANT=auto|tc|tc1|tc2|smallt|simt32, read
  * once per process, overrides that choice.  Asynchronous on `stream`.
  *
- * Scratch: the tensor-core variant converts dY once to fp16/bf16 in a device
- * workspace of rg_workspace_bytes() bytes.  rg_out_prod takes it
+ * Scratch: the tensor-core variant converts dY once to fp16/bf16, and the
+ * small-T variant writes per-CTA partial sums, in a device workspace of
+ * rg_workspace_bytes() bytes.  rg_out_prod takes it
  * stream-ordered from a per-device memory pool owned by the library
  * (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`); the pool keeps its
  * memory, so only the first call of a given size reaches the driver.  Use

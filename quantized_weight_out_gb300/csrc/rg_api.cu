@@ -127,6 +127,18 @@ size_t tc_workspace(int64_t N, int64_t T) {
   return (b + 255) / 256 * 256;
 }
 
+bool is_tc(int variant) {
+  return variant == RG_VARIANT_TC || variant == RG_VARIANT_TC_SINGLE ||
+         variant == RG_VARIANT_TC_PAIR;
+}
+
+// Workspace bytes of a resolved (non-auto) variant; N, K, T > 0.
+size_t workspace_for(int variant, int64_t N, int64_t K, int64_t T, const DevInfo& dev) {
+  if (is_tc(variant)) return tc_workspace(N, T);
+  if (variant == RG_VARIANT_SMALLT) return (plan_smallt(N, K, T, dev).workspace + 255) / 256 * 256;
+  return 0;
+}
+
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? RG_OK : RG_ERR_CUDA; }
 
 // rg_profile_next_gemm: events for the next tensor-core launch of this thread
@@ -188,16 +200,11 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
   if (N == 0) return from_cuda(launch_scale(dX, T * K, beta, *dev, stream));
   if (variant == RG_VARIANT_AUTO) variant = select_variant(wtype, N, K, T);
 
-  switch (variant) {
-    case RG_VARIANT_SIMT32:
-      return from_cuda(launch_simt32(wtype, W, N, K, dY, T, dX, beta, *dev, stream));
-    case RG_VARIANT_SMALLT:
-      return from_cuda(launch_smallt(wtype, W, N, K, dY, T, dX, beta, *dev, stream));
-    default:
-      break;
-  }
-  // tensor-core path: dY -> 16-bit operand copy, then the fused GEMM
-  const size_t need = tc_workspace(N, T);
+  if (variant == RG_VARIANT_SIMT32)
+    return from_cuda(launch_simt32(wtype, W, N, K, dY, T, dX, beta, *dev, stream));
+  // the small-T and tensor-core paths take a workspace: partial sums, or the
+  // 16-bit copy of dY
+  const size_t need = workspace_for(variant, N, K, T, *dev);
   void* buf = ws;
   cudaMemPool_t pool{};
   if (own_ws) {
@@ -207,9 +214,19 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
     if (!ws || ws_bytes < need) return RG_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return RG_ERR_ALIGN;
   }
+  cudaError_t e = cudaSuccess;
+  if (variant == RG_VARIANT_SMALLT) {
+    e = launch_smallt(wtype, W, N, K, dY, T, dX, beta, static_cast<float*>(buf),
+                      plan_smallt(N, K, T, *dev), *dev, stream);
+    if (own_ws) {
+      const cudaError_t f = cudaFreeAsync(buf, stream);
+      if (e == cudaSuccess) e = f;
+    }
+    return from_cuda(e);
+  }
   const bool bf16 = wtype == RG_BF16;
   const int64_t ld = tc_dy16_ld(N);
-  cudaError_t e = launch_convert_dy(dY, T, N, ld, bf16, static_cast<uint16_t*>(buf), *dev, stream);
+  e = launch_convert_dy(dY, T, N, ld, bf16, static_cast<uint16_t*>(buf), *dev, stream);
   cudaEvent_t ev0 = t_prof_before, ev1 = t_prof_after;
   t_prof_before = t_prof_after = nullptr;
   if (e == cudaSuccess && ev0) e = cudaEventRecord(ev0, stream);
@@ -273,10 +290,12 @@ int rg_out_prod_variant(int variant, int wtype, const void* W, int64_t N, int64_
 
 size_t rg_workspace_bytes(int variant, int wtype, int64_t N, int64_t K, int64_t T) {
   if (variant == RG_VARIANT_AUTO) variant = select_variant(wtype, N, K, T);
-  const bool tc = variant == RG_VARIANT_TC || variant == RG_VARIANT_TC_SINGLE ||
-                  variant == RG_VARIANT_TC_PAIR;
-  if (!tc || N <= 0 || T <= 0 || K <= 0) return 0;
-  return tc_workspace(N, T);
+  if (N <= 0 || T <= 0 || K <= 0) return 0;
+  if (is_tc(variant)) return tc_workspace(N, T);
+  if (variant != RG_VARIANT_SMALLT) return 0;
+  DevInfo* dev = nullptr;
+  if (current_dev(&dev) != RG_OK) return 0;
+  return workspace_for(variant, N, K, T, *dev);
 }
 
 int rg_out_prod_ws(int variant, int wtype, const void* W, int64_t N, int64_t K, const float* dY,
@@ -293,16 +312,17 @@ int rg_out_prod_noalloc(int wtype, const void* W, int64_t N, int64_t K, const fl
   if (st != RG_OK || empty) return st;
   int variant = env().variant;
   if (variant == RG_VARIANT_AUTO) variant = select_variant(wtype, N, K, T);
-  const bool tc = variant == RG_VARIANT_TC || variant == RG_VARIANT_TC_SINGLE ||
-                  variant == RG_VARIANT_TC_PAIR;
   void* ws = nullptr;
   size_t ws_bytes = 0;
-  if (tc && N > 0) {
-    if (tc_workspace(N, T) > static_cast<size_t>(RG_NOALLOC_SCRATCH_BYTES)) return RG_ERR_ARG;
+  if (N > 0) {
     DevInfo* dev = nullptr;
     if ((st = current_dev(&dev)) != RG_OK) return st;
-    if ((st = noalloc_scratch(dev->device, &ws)) != RG_OK) return st;
-    ws_bytes = static_cast<size_t>(RG_NOALLOC_SCRATCH_BYTES);
+    const size_t need = workspace_for(variant, N, K, T, *dev);
+    if (need > 0) {
+      if (need > static_cast<size_t>(RG_NOALLOC_SCRATCH_BYTES)) return RG_ERR_ARG;
+      if ((st = noalloc_scratch(dev->device, &ws)) != RG_OK) return st;
+      ws_bytes = static_cast<size_t>(RG_NOALLOC_SCRATCH_BYTES);
+    }
   }
   return run(variant, wtype, W, N, K, dY, T, dX, beta, ws, ws_bytes, false,
              static_cast<cudaStream_t>(stream));

@@ -38,9 +38,21 @@ cudaError_t launch_simt32(int wtype, const void* W, int64_t N, int64_t K, const 
                           int64_t T, float* dX, float beta, const DevInfo& dev,
                           cudaStream_t stream);
 
+// Small-T path: rows of W split over n_splits CTAs per 256-value tile and
+// dY chunk of tb rows; partial sums go to a workspace of `workspace` bytes
+// ([n_splits][T][K] F32), then a second kernel adds them with beta * dX.
+struct SmalltPlan {
+  int tb;              // dY rows per pass: 1, 2, 4 or 8
+  int n_ktiles;        // ceil(K / 256)
+  int n_tchunks;       // ceil(T / tb)
+  int n_splits;        // CTAs along N per tile
+  int rows_per_split;  // rows of W per CTA (multiple of 8)
+  size_t workspace;    // bytes of partial sums
+};
+SmalltPlan plan_smallt(int64_t N, int64_t K, int64_t T, const DevInfo& dev);
 cudaError_t launch_smallt(int wtype, const void* W, int64_t N, int64_t K, const float* dY,
-                          int64_t T, float* dX, float beta, const DevInfo& dev,
-                          cudaStream_t stream);
+                          int64_t T, float* dX, float beta, float* part, const SmalltPlan& p,
+                          const DevInfo& dev, cudaStream_t stream);
 
 // Tensor-core path.  dy16 is the converted dY with row stride ld_dy16 values.
 struct TcPlan {

@@ -53,7 +53,7 @@ def test_dispatch(lib):
     assert rg.rg_select_variant(inputs.Q4_K, 14336, 4096, 2048) == rg.RG_VARIANT_TC
     assert rg.rg_workspace_bytes(rg.RG_VARIANT_TC, inputs.Q4_K, 14336, 4096, 2048) == 2048 * 14336 * 2
     assert rg.rg_workspace_bytes(rg.RG_VARIANT_TC, inputs.Q4_K, 13, 4096, 3) == 3 * 16 * 2 + 160
-    assert rg.rg_workspace_bytes(rg.RG_VARIANT_SMALLT, inputs.Q4_K, 14336, 4096, 8) == 0
+    assert rg.rg_workspace_bytes(rg.RG_VARIANT_SIMT32, inputs.Q4_K, 14336, 4096, 8) == 0
 
 
 BAD = 0x1000  # never dereferenced: every case below fails validation first
