@@ -116,9 +116,11 @@ int validate(int wtype, const void* W, int64_t N, int64_t K, const float* dY, in
 
 int select_variant(int wtype, int64_t N, int64_t K, int64_t T) {
   (void)wtype;
-  (void)N;
-  (void)K;
-  if (T <= 32) return RG_VARIANT_SMALLT;
+  // a few rows of dY, or a problem too small to fill a tensor-core pipeline:
+  // the weight-streaming SIMT kernel; else the tensor cores (which split the
+  // contraction over idle SMs when the output is small)
+  const double flops = 2.0 * static_cast<double>(T) * static_cast<double>(N) * static_cast<double>(K);
+  if (T <= 2 || (T <= 32 && flops <= 268435456.0)) return RG_VARIANT_SMALLT;
   return RG_VARIANT_TC;
 }
 
@@ -132,9 +134,22 @@ bool is_tc(int variant) {
          variant == RG_VARIANT_TC_PAIR;
 }
 
+int cg_force_of(int variant) {
+  return variant == RG_VARIANT_TC_SINGLE ? 1 : variant == RG_VARIANT_TC_PAIR ? 2 : 0;
+}
+
+// Tensor-core workspace: the 16-bit dY copy, then (split contraction) the
+// partial-sum slabs, each 256-byte aligned.
+size_t tc_partial_offset(int64_t N, int64_t T) { return tc_workspace(N, T); }
+size_t tc_workspace_total(int variant, int64_t N, int64_t K, int64_t T, const DevInfo& dev) {
+  const int64_t splits = tc_partial_splits(N, K, T, dev, cg_force_of(variant));
+  const size_t parts = static_cast<size_t>(splits) * static_cast<size_t>(T) * static_cast<size_t>(K) * 4;
+  return tc_partial_offset(N, T) + (parts + 255) / 256 * 256;
+}
+
 // Workspace bytes of a resolved (non-auto) variant; N, K, T > 0.
 size_t workspace_for(int variant, int64_t N, int64_t K, int64_t T, const DevInfo& dev) {
-  if (is_tc(variant)) return tc_workspace(N, T);
+  if (is_tc(variant)) return tc_workspace_total(variant, N, K, T, dev);
   if (variant == RG_VARIANT_SMALLT) return (plan_smallt(N, K, T, dev).workspace + 255) / 256 * 256;
   return 0;
 }
@@ -231,9 +246,9 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
   t_prof_before = t_prof_after = nullptr;
   if (e == cudaSuccess && ev0) e = cudaEventRecord(ev0, stream);
   if (e == cudaSuccess)
-    e = launch_tc(wtype, W, N, K, static_cast<const uint16_t*>(buf), ld, T, dX, beta, *dev,
-                  stream, variant == RG_VARIANT_TC_SINGLE ? 1 : variant == RG_VARIANT_TC_PAIR ? 2 : 0,
-                  env().inject_stall);
+    e = launch_tc(wtype, W, N, K, static_cast<const uint16_t*>(buf), ld, T, dX, beta,
+                  reinterpret_cast<float*>(static_cast<char*>(buf) + tc_partial_offset(N, T)), *dev,
+                  stream, cg_force_of(variant), env().inject_stall);
   if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, stream);
   if (own_ws) {
     const cudaError_t f = cudaFreeAsync(buf, stream);
@@ -244,9 +259,89 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
 
 }  // namespace
 
+namespace {
+
+// Recently encoded tensor maps: encoding is a driver call of a few
+// microseconds, and a training step calls with the same tensors every time.
+struct MapKey {
+  const void* base;
+  uint64_t dim0, dim1, stride1;
+  uint32_t box0, box1;
+  int dtype, swizzle, device;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && dim0 == o.dim0 && dim1 == o.dim1 && stride1 == o.stride1 &&
+           box0 == o.box0 && box1 == o.box1 && dtype == o.dtype && swizzle == o.swizzle &&
+           device == o.device;
+  }
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  uint64_t stamp;
+  bool used;
+};
+constexpr int kMapCache = 64;
+std::mutex g_map_mu;
+MapEntry g_maps[kMapCache];
+uint64_t g_map_clock = 0;
+
+// (kernel, device) pairs whose dynamic shared memory limit is already set
+struct AttrEntry {
+  const void* func;
+  int device, bytes;
+};
+constexpr int kAttrCache = 256;
+std::mutex g_attr_mu;
+AttrEntry g_attrs[kAttrCache];
+int g_n_attrs = 0;
+
+}  // namespace
+
+cudaError_t ensure_smem_attr(const void* func, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  for (int i = 0; i < g_n_attrs; ++i)
+    if (g_attrs[i].func == func && g_attrs[i].device == dev && g_attrs[i].bytes >= bytes)
+      return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && g_n_attrs < kAttrCache) g_attrs[g_n_attrs++] = AttrEntry{func, dev, bytes};
+  return e;
+}
+
 CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                       uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes, uint32_t box0,
                       uint32_t box1, CUtensorMapSwizzle swizzle) {
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return CUDA_ERROR_INVALID_CONTEXT;
+  const MapKey key{base, dim0, dim1, stride1_bytes, box0, box1, static_cast<int>(dtype),
+                   static_cast<int>(swizzle), device};
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    for (MapEntry& m : g_maps)
+      if (m.used && m.key == key) {
+        m.stamp = ++g_map_clock;
+        *map = m.map;
+        return CUDA_SUCCESS;
+      }
+  }
+  const CUresult r = encode_tiled_uncached(map, dtype, base, dim0, dim1, stride1_bytes, box0, box1,
+                                           swizzle);
+  if (r != CUDA_SUCCESS) return r;
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  MapEntry* slot = &g_maps[0];
+  for (MapEntry& m : g_maps) {
+    if (!m.used) { slot = &m; break; }
+    if (m.stamp < slot->stamp) slot = &m;
+  }
+  *slot = MapEntry{key, *map, ++g_map_clock, true};
+  return CUDA_SUCCESS;
+}
+
+CUresult encode_tiled_uncached(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                               uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes, uint32_t box0,
+                               uint32_t box1, CUtensorMapSwizzle swizzle) {
   using Fn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                           const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
                           CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
@@ -291,10 +386,9 @@ int rg_out_prod_variant(int variant, int wtype, const void* W, int64_t N, int64_
 size_t rg_workspace_bytes(int variant, int wtype, int64_t N, int64_t K, int64_t T) {
   if (variant == RG_VARIANT_AUTO) variant = select_variant(wtype, N, K, T);
   if (N <= 0 || T <= 0 || K <= 0) return 0;
-  if (is_tc(variant)) return tc_workspace(N, T);
-  if (variant != RG_VARIANT_SMALLT) return 0;
+  if (!is_tc(variant) && variant != RG_VARIANT_SMALLT) return 0;
   DevInfo* dev = nullptr;
-  if (current_dev(&dev) != RG_OK) return 0;
+  if (current_dev(&dev) != RG_OK) return is_tc(variant) ? tc_workspace(N, T) : 0;
   return workspace_for(variant, N, K, T, *dev);
 }
 

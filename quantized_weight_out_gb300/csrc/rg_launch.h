@@ -63,22 +63,39 @@ struct TcPlan {
   int n_chunks;  // ceil(N / 64) contraction stages per tile
   int grid;      // persistent CTAs (a multiple of cg), before the occupancy cap
   int band;      // k units per rasterization band (tile order), set at launch
+  int n_splits;  // contraction split into this many ranges of n_chunks stages
 };
 // cg_force: 0 = choose from the shape, 1 or 2 = that tile configuration.
 TcPlan plan_tc(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force);
 int64_t tc_dy16_ld(int64_t N);
+// part: [n_splits][T][K] F32 partial sums when the plan splits the
+// contraction (tc_partial_splits > 0), else unused.
 cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
-                      int64_t ld_dy16, int64_t T, float* dX, float beta, const DevInfo& dev,
-                      cudaStream_t stream, int cg_force, int inject_stall);
+                      int64_t ld_dy16, int64_t T, float* dX, float beta, float* part,
+                      const DevInfo& dev, cudaStream_t stream, int cg_force, int inject_stall);
+// Number of partial-sum slabs the tensor-core plan needs (0 when unsplit).
+int64_t tc_partial_splits(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force);
+
+// dX = beta * dX + sum of n_splits slabs of TK floats, in slab order.
+cudaError_t launch_reduce_partials(const float* part, int n_splits, int64_t TK, float* dX,
+                                   float beta, const DevInfo& dev, cudaStream_t stream);
 
 // A kernel whose one wait can never complete; it must give up after
 // `limit_ns`, record RG_ERR_TIMEOUT and return.
 cudaError_t launch_wait_probe(const DevInfo& dev, unsigned long long limit_ns,
                               cudaStream_t stream);
 
-// cuTensorMapEncodeTiled, resolved from the driver at first use.
+// cuTensorMapEncodeTiled (resolved from the driver at first use), through a
+// small cache of recently encoded maps keyed by address, shape and device.
 CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                       uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes, uint32_t box0,
                       uint32_t box1, CUtensorMapSwizzle swizzle);
+CUresult encode_tiled_uncached(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                               uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes, uint32_t box0,
+                               uint32_t box1, CUtensorMapSwizzle swizzle);
+
+// Raise `func`'s dynamic shared memory limit to `bytes` on the current device,
+// once per (kernel, device).
+cudaError_t ensure_smem_attr(const void* func, int bytes);
 
 }  // namespace rg

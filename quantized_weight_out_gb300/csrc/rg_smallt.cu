@@ -6,10 +6,11 @@
 //
 // Every weight value is read from memory once per pass of up to 8 dY rows,
 // decoded exactly to F32 in registers, and multiplied in F32 by each dY row.
-//  * A warp walks whole rows of W: lane l owns values 8l .. 8l+7 of a
-//    256-value tile, so the 32 lanes read one contiguous row segment (16-byte
-//    loads for F16/BF16, 8-byte loads of Q4_K nibbles, 2-byte loads of the
-//    34/18-byte Q8_0/Q4_0 blocks) and several rows are in flight per warp.
+//  * A producer warp streams the CTA's rows of W (its 256-value tile of each
+//    row) with TMA into an 8-stage shared-memory ring of 32-row tiles, so
+//    enough bytes are in flight without holding them in registers.
+//  * A consumer warp takes whole rows: lane l owns values 8l .. 8l+7, reads
+//    their bytes from shared memory and decodes them in registers.
 //  * The rows are split over many CTAs (grid.y) so that the whole GPU streams
 //    W; each CTA sums its eight warps in a fixed order and writes its partial
 //    tile to a workspace, and a second kernel adds the partials in split
@@ -22,8 +23,7 @@
 namespace rg {
 namespace smt {
 
-constexpr int THREADS = 256;   // 8 warps
-constexpr int ROWS = 256;      // dY columns (= W rows) staged per chunk
+constexpr int THREADS = 256;   // 8 consumer warps (plus one producer warp)
 
 // Raw bytes one lane needs from a row for its 8 values (a 256-value tile).
 template <int WT>
@@ -31,32 +31,25 @@ struct Raw {
   uint32_t v[WT == RG_Q4_K ? 6 : WT == RG_Q8_0 || WT == RG_Q4_0 ? 3 : 4];
 };
 
-__device__ __forceinline__ uint32_t ldg_u16(const uint8_t* p) {
-  return static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(p)));
-}
-
-// tile: first byte of the row's 256-value tile (16-byte aligned)
+// The bytes one lane needs for its 8 values, from a row tile staged in
+// shared memory (tile: the row's 256-value tile, 16-byte aligned).
 template <int WT>
-__device__ __forceinline__ void load_raw(const uint8_t* tile, int lane, Raw<WT>& r) {
+__device__ __forceinline__ void load_raw_smem(const uint8_t* tile, int lane, Raw<WT>& r) {
   if constexpr (WT == RG_F16 || WT == RG_BF16) {
-    const uint4 q = __ldg(reinterpret_cast<const uint4*>(tile) + lane);
+    const uint4 q = reinterpret_cast<const uint4*>(tile)[lane];
     r.v[0] = q.x; r.v[1] = q.y; r.v[2] = q.z; r.v[3] = q.w;
-  } else if constexpr (WT == RG_Q8_0) {
-    const uint8_t* blk = tile + 34 * (lane >> 2);          // 4 lanes per 32-value block
-    const uint8_t* q = blk + 2 + 8 * (lane & 3);
-    r.v[0] = ldg_u16(blk);
-    r.v[1] = ldg_u16(q) | (ldg_u16(q + 2) << 16);
-    r.v[2] = ldg_u16(q + 4) | (ldg_u16(q + 6) << 16);
-  } else if constexpr (WT == RG_Q4_0) {
-    const uint8_t* blk = tile + 18 * (lane >> 2);
-    const uint8_t* q = blk + 2 + 8 * (lane & 1);           // low nibbles for lane&3 < 2, high after
-    r.v[0] = ldg_u16(blk);
-    r.v[1] = ldg_u16(q) | (ldg_u16(q + 2) << 16);
-    r.v[2] = ldg_u16(q + 4) | (ldg_u16(q + 6) << 16);
-  } else {  // Q4_K: header (d, dmin, 12 scale bytes) and 8 nibble bytes
-    const uint4 h = __ldg(reinterpret_cast<const uint4*>(tile));
+  } else if constexpr (WT == RG_Q8_0 || WT == RG_Q4_0) {
+    constexpr int BB = WT == RG_Q8_0 ? 34 : 18;
+    const uint8_t* blk = tile + BB * (lane >> 2);
+    const uint8_t* q = blk + 2 + 8 * (WT == RG_Q8_0 ? (lane & 3) : (lane & 1));
+    const uint16_t* q16 = reinterpret_cast<const uint16_t*>(q);
+    r.v[0] = *reinterpret_cast<const uint16_t*>(blk);
+    r.v[1] = static_cast<uint32_t>(q16[0]) | (static_cast<uint32_t>(q16[1]) << 16);
+    r.v[2] = static_cast<uint32_t>(q16[2]) | (static_cast<uint32_t>(q16[3]) << 16);
+  } else {
+    const uint4 h = *reinterpret_cast<const uint4*>(tile);
     const int c = lane >> 3, l0 = 8 * (lane & 3);
-    const uint2 q = __ldg(reinterpret_cast<const uint2*>(tile + 16 + 32 * c + l0));
+    const uint2 q = *reinterpret_cast<const uint2*>(tile + 16 + 32 * c + l0);
     r.v[0] = h.x; r.v[1] = h.y; r.v[2] = h.z; r.v[3] = h.w; r.v[4] = q.x; r.v[5] = q.y;
   }
 }
@@ -116,22 +109,79 @@ __device__ __forceinline__ void decode_raw(const Raw<WT>& r, int lane, float (&w
   }
 }
 
+// Bytes of one row's 256-value tile.
+template <int WT>
+__host__ __device__ constexpr int tile_bytes() {
+  return (256 / block_values(WT)) * block_bytes(WT);
+}
+
+constexpr int BR = 32;       // rows of W per pipeline stage
+constexpr int STAGES = 8;    // stages in flight per CTA
+constexpr int CONSUMERS = 8; // consumer warps; warp 8 is the TMA producer
+constexpr int MAX_ROWS = 512;
+
 // grid (ceil(K/256), n_splits, ceil(T/TB)); partial sums of rows
 // [split * rows_per_split, +rows_per_split) to part[(split * T + t) * K + k].
-template <int WT, int TB, int RU>
-__global__ void __launch_bounds__(THREADS, 2)
-    smallt_kernel(const uint8_t* __restrict__ W, int64_t rb, int N, int K,
+// A producer warp streams the CTA's rows of W, tile by tile of BR rows, into
+// an 8-stage ring with TMA; eight consumer warps decode from shared memory.
+template <int WT, int TB>
+__global__ void __launch_bounds__(THREADS + 32, TB >= 8 ? 1 : 2)
+    smallt_kernel(const __grid_constant__ CUtensorMap map_w, int N, int K,
                   const float* __restrict__ dY, int T, float* __restrict__ part,
-                  int rows_per_split) {
-  __shared__ float ys[TB][ROWS];
-  __shared__ __align__(16) float red[4][TB][256];
+                  int rows_per_split, WaitCtl ctl) {
+  constexpr int TBYTES = tile_bytes<WT>();
+  extern __shared__ __align__(128) uint8_t sm[];
+  uint8_t* stage_buf = sm;                                              // STAGES x BR x TBYTES
+  float* ys = reinterpret_cast<float*>(sm + STAGES * BR * TBYTES);      // [TB][MAX_ROWS]
+  float* red = ys + TB * MAX_ROWS;                                      // [4][TB][256]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red + 4 * TB * 256);    // full[S], empty[S]
+  __shared__ int abort_flag_s;
+  volatile int* abort_flag = &abort_flag_s;
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kt = blockIdx.x, split = blockIdx.y;
   const int t0 = blockIdx.z * TB;
   const int nbeg = split * rows_per_split;
-  const int nend = min(N, nbeg + rows_per_split);
-  const bool kvalid = kt * 256 + 8 * lane < K;
-  const int64_t tile_off = static_cast<int64_t>(kt) * (256 / block_values(WT)) * block_bytes(WT);
+  const int nrows = max(0, min(N, nbeg + rows_per_split) - nbeg);
+  const int n_tiles = (nrows + BR - 1) / BR;
+  const uint32_t bar0 = smem_addr(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), CONSUMERS);
+    }
+    abort_flag_s = 0;
+    fence_mbar_init();
+  }
+  // this CTA's slice of dY, [TB][nrows]
+  for (int idx = threadIdx.x; idx < TB * MAX_ROWS; idx += THREADS + 32) {
+    const int t = idx / MAX_ROWS, r = idx - t * MAX_ROWS;
+    ys[idx] = (t0 + t < T && r < nrows) ? __ldg(dY + static_cast<int64_t>(t0 + t) * N + nbeg + r) : 0.0f;
+  }
+  __syncthreads();
+
+  if (warp == CONSUMERS) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      uint32_t ph = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int s = i % STAGES;
+        if (!mbar_wait(empty(s), ph ^ 1u, ctl, abort_flag)) break;
+        mbar_arrive_expect_tx(full(s), BR * TBYTES);
+        tma_load_2d(smem_addr(stage_buf + s * BR * TBYTES), &map_w, full(s), kt * (TBYTES / 4),
+                    nbeg + i * BR);
+        if (s == STAGES - 1) ph ^= 1u;
+      }
+      // drain: the copies started land before the CTA leaves
+      volatile int no_abort = 0;
+      for (int i = max(0, n_tiles - STAGES); i < n_tiles; ++i)
+        (void)mbar_wait(full(i % STAGES), static_cast<uint32_t>(i / STAGES) & 1u, ctl, &no_abort);
+    }
+    __syncwarp();
+  }
 
   float acc[TB][8];
 #pragma unroll
@@ -139,63 +189,68 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[t][i] = 0.0f;
 
-  for (int c0 = nbeg; c0 < nend; c0 += ROWS) {
-    const int cn = min(ROWS, nend - c0);
-    for (int idx = threadIdx.x; idx < TB * ROWS; idx += THREADS) {
-      const int t = idx / ROWS, r = idx - t * ROWS;
-      ys[t][r] = (t0 + t < T && r < cn) ? __ldg(dY + static_cast<int64_t>(t0 + t) * N + c0 + r) : 0.0f;
-    }
-    __syncthreads();
-    if (kvalid) {
-      for (int r = warp; r < cn; r += 8 * RU) {
-        Raw<WT> raw[RU];
+  if (warp < CONSUMERS) {
+    const bool kvalid = kt * 256 + 8 * lane < K;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int s = i % STAGES;
+      if (!__all_sync(0xffffffffu, mbar_wait(full(s), static_cast<uint32_t>(i / STAGES) & 1u, ctl,
+                                             abort_flag)))
+        break;
+      if (kvalid) {
+        const uint8_t* tile = stage_buf + s * BR * TBYTES;
+        Raw<WT> raw[BR / CONSUMERS];
 #pragma unroll
-        for (int u = 0; u < RU; ++u) {
-          const int rr = r + 8 * u;
-          if (rr < cn) load_raw<WT>(W + static_cast<int64_t>(c0 + rr) * rb + tile_off, lane, raw[u]);
-        }
+        for (int u = 0; u < BR / CONSUMERS; ++u) load_raw_smem<WT>(tile + (warp + CONSUMERS * u) * TBYTES, lane, raw[u]);
 #pragma unroll
-        for (int u = 0; u < RU; ++u) {
-          const int rr = r + 8 * u;
-          if (rr < cn) {
+        for (int u = 0; u < BR / CONSUMERS; ++u) {
+          const int r = i * BR + warp + CONSUMERS * u;  // row within the CTA's slice
+          if (r < nrows) {
             float w[8];
             decode_raw<WT>(raw[u], lane, w);
 #pragma unroll
             for (int t = 0; t < TB; ++t) {
-              const float y = ys[t][rr];
+              const float y = ys[t * MAX_ROWS + r];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) acc[t][i] = fmaf(y, w[i], acc[t][i]);
+              for (int q = 0; q < 8; ++q) acc[t][q] = fmaf(y, w[q], acc[t][q]);
             }
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty(s));
     }
-    __syncthreads();
   }
 
-  // the CTA's eight warps, summed in a fixed order: (w + 4) into w, then 0..3
-  if (warp >= 4) {
+  // the CTA's eight consumer warps, summed in a fixed order: (w + 4) into w, then 0..3
+  if (warp >= 4 && warp < CONSUMERS) {
 #pragma unroll
     for (int t = 0; t < TB; ++t)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) red[warp - 4][t][8 * lane + i] = acc[t][i];
+      for (int q = 0; q < 8; ++q) red[((warp - 4) * TB + t) * 256 + 8 * lane + q] = acc[t][q];
   }
   __syncthreads();
   if (warp < 4) {
 #pragma unroll
     for (int t = 0; t < TB; ++t)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) red[warp][t][8 * lane + i] += acc[t][i];
+      for (int q = 0; q < 8; ++q) red[(warp * TB + t) * 256 + 8 * lane + q] += acc[t][q];
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < TB * 256; idx += THREADS) {
+  for (int idx = threadIdx.x; idx < TB * 256; idx += THREADS + 32) {
     const int t = idx >> 8, kk = idx & 255;
     const int gt = t0 + t, gk = kt * 256 + kk;
     if (gt < T && gk < K) {
-      const float s = ((red[0][t][kk] + red[1][t][kk]) + red[2][t][kk]) + red[3][t][kk];
-      part[(static_cast<int64_t>(split) * T + gt) * K + gk] = s;
+      const float sum = ((red[(0 * TB + t) * 256 + kk] + red[(1 * TB + t) * 256 + kk]) +
+                         red[(2 * TB + t) * 256 + kk]) + red[(3 * TB + t) * 256 + kk];
+      part[(static_cast<int64_t>(split) * T + gt) * K + gk] = sum;
     }
   }
+}
+
+template <int WT, int TB>
+constexpr size_t smem_bytes() {
+  return static_cast<size_t>(STAGES) * BR * tile_bytes<WT>() + sizeof(float) * TB * MAX_ROWS +
+         sizeof(float) * 4 * TB * 256 + 16 * STAGES;
 }
 
 // dX = beta * dX + sum over splits (in split order), four values per thread.
@@ -229,6 +284,7 @@ SmalltPlan plan_smallt(int64_t N, int64_t K, int64_t T, const DevInfo& dev) {
   const int64_t target = static_cast<int64_t>(dev.num_sms) * 4;
   int64_t splits = (target + p.n_ktiles * p.n_tchunks - 1) / (p.n_ktiles * p.n_tchunks);
   splits = std::max<int64_t>(1, std::min<int64_t>(splits, (N + 63) / 64));
+  splits = std::max<int64_t>(splits, (N + smt::MAX_ROWS - 1) / smt::MAX_ROWS);
   int64_t rows = (N + splits - 1) / splits;
   rows = (rows + 7) / 8 * 8;
   p.rows_per_split = static_cast<int>(rows);
@@ -238,28 +294,36 @@ SmalltPlan plan_smallt(int64_t N, int64_t K, int64_t T, const DevInfo& dev) {
 }
 
 template <int WT, int TB>
-static cudaError_t launch_smallt_t(const void* W, int64_t N, int64_t K, const float* dY,
-                                   int64_t T, float* part, const SmalltPlan& p,
+static cudaError_t launch_smallt_t(const CUtensorMap& map, int64_t N, int64_t K, const float* dY,
+                                   int64_t T, float* part, const SmalltPlan& p, const DevInfo& dev,
                                    cudaStream_t stream) {
-  constexpr int RU = TB <= 4 ? 8 : 4;
-  const int64_t rb = K / block_values(WT) * block_bytes(WT);
+  auto kern = smt::smallt_kernel<WT, TB>;
+  constexpr size_t smem = smt::smem_bytes<WT, TB>();
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(p.n_ktiles), static_cast<unsigned>(p.n_splits),
                   static_cast<unsigned>(p.n_tchunks));
-  smt::smallt_kernel<WT, TB, RU><<<grid, smt::THREADS, 0, stream>>>(
-      static_cast<const uint8_t*>(W), rb, static_cast<int>(N), static_cast<int>(K), dY,
-      static_cast<int>(T), part, p.rows_per_split);
+  WaitCtl ctl{dev.status, dev.wait_limit_ns};
+  kern<<<grid, smt::THREADS + 32, smem, stream>>>(map, static_cast<int>(N), static_cast<int>(K), dY,
+                                                   static_cast<int>(T), part, p.rows_per_split, ctl);
   return cudaGetLastError();
 }
 
 template <int WT>
 static cudaError_t launch_smallt_w(const void* W, int64_t N, int64_t K, const float* dY,
-                                   int64_t T, float* part, const SmalltPlan& p,
+                                   int64_t T, float* part, const SmalltPlan& p, const DevInfo& dev,
                                    cudaStream_t stream) {
+  // W as rows of 32-bit words; one box = BR rows x one 256-value tile
+  const uint64_t rb = static_cast<uint64_t>(K / block_values(WT) * block_bytes(WT));
+  CUtensorMap map;
+  if (encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rb / 4, static_cast<uint64_t>(N), rb,
+                   smt::tile_bytes<WT>() / 4, smt::BR, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   switch (p.tb) {
-    case 1: return launch_smallt_t<WT, 1>(W, N, K, dY, T, part, p, stream);
-    case 2: return launch_smallt_t<WT, 2>(W, N, K, dY, T, part, p, stream);
-    case 4: return launch_smallt_t<WT, 4>(W, N, K, dY, T, part, p, stream);
-    default: return launch_smallt_t<WT, 8>(W, N, K, dY, T, part, p, stream);
+    case 1: return launch_smallt_t<WT, 1>(map, N, K, dY, T, part, p, dev, stream);
+    case 2: return launch_smallt_t<WT, 2>(map, N, K, dY, T, part, p, dev, stream);
+    case 4: return launch_smallt_t<WT, 4>(map, N, K, dY, T, part, p, dev, stream);
+    default: return launch_smallt_t<WT, 8>(map, N, K, dY, T, part, p, dev, stream);
   }
 }
 
@@ -269,18 +333,22 @@ cudaError_t launch_smallt(int wtype, const void* W, int64_t N, int64_t K, const 
   if (p.n_tchunks > 65535 || p.n_splits > 65535) return cudaErrorInvalidConfiguration;
   cudaError_t e;
   switch (wtype) {
-    case RG_F16: e = launch_smallt_w<RG_F16>(W, N, K, dY, T, part, p, stream); break;
-    case RG_BF16: e = launch_smallt_w<RG_BF16>(W, N, K, dY, T, part, p, stream); break;
-    case RG_Q8_0: e = launch_smallt_w<RG_Q8_0>(W, N, K, dY, T, part, p, stream); break;
-    case RG_Q4_0: e = launch_smallt_w<RG_Q4_0>(W, N, K, dY, T, part, p, stream); break;
-    case RG_Q4_K: e = launch_smallt_w<RG_Q4_K>(W, N, K, dY, T, part, p, stream); break;
+    case RG_F16: e = launch_smallt_w<RG_F16>(W, N, K, dY, T, part, p, dev, stream); break;
+    case RG_BF16: e = launch_smallt_w<RG_BF16>(W, N, K, dY, T, part, p, dev, stream); break;
+    case RG_Q8_0: e = launch_smallt_w<RG_Q8_0>(W, N, K, dY, T, part, p, dev, stream); break;
+    case RG_Q4_0: e = launch_smallt_w<RG_Q4_0>(W, N, K, dY, T, part, p, dev, stream); break;
+    case RG_Q4_K: e = launch_smallt_w<RG_Q4_K>(W, N, K, dY, T, part, p, dev, stream); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  const int64_t TK = T * K;
+  return launch_reduce_partials(part, p.n_splits, T * K, dX, beta, dev, stream);
+}
+
+cudaError_t launch_reduce_partials(const float* part, int n_splits, int64_t TK, float* dX,
+                                   float beta, const DevInfo& dev, cudaStream_t stream) {
   const int64_t blocks = std::min<int64_t>((TK / 4 + 255) / 256, static_cast<int64_t>(dev.num_sms) * 8);
   smt::smallt_reduce<<<static_cast<unsigned>(std::max<int64_t>(1, blocks)), 256, 0, stream>>>(
-      part, p.n_splits, TK, dX, beta);
+      part, n_splits, TK, dX, beta);
   return cudaGetLastError();
 }
 

@@ -318,7 +318,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     out_prod_tc_kernel(const __grid_constant__ CUtensorMap map_w,
                        const __grid_constant__ CUtensorMap map_y, float* __restrict__ dX,
                        float beta, int T, int K, int n_kunits, int n_ttiles, int band,
-                       int n_chunks, WaitCtl ctl, int inject_stall) {
+                       int n_chunks, int n_splits, float* __restrict__ part, WaitCtl ctl,
+                       int inject_stall) {
   using C = Cfg<WT, CG, BT>;
   constexpr int S = C::S;
   extern __shared__ uint8_t smem_raw[];
@@ -342,7 +343,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
   const bool leader = rank == 0;
   const int unit = blockIdx.x / CG, n_units = gridDim.x / CG;
-  const int n_tiles = n_kunits * n_ttiles;
+  // work items: (tile, split); a split covers chunks [split * n_chunks, +n_chunks)
+  // of the contraction (chunks past N are zero-filled by TMA and add nothing)
+  const int n_tiles = n_kunits * n_ttiles * n_splits;
+  const int n_tiles1 = n_kunits * n_ttiles;
 
   auto wait_any = [&](uint32_t bar, uint32_t parity) {
     if constexpr (CG == 2)
@@ -388,7 +392,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // tile -> (k unit, t tile): bands of `band` k units; inside a band the t
   // tiles run outer, so the band's slice of W stays in L2 while every t tile
   // of dY passes by once per band
-  auto coords = [&](int tile, int& ku, int& tt) {
+  auto coords = [&](int item, int& ku, int& tt) {
+    const int tile = item % n_tiles1;
     const int per_band = band * n_ttiles;
     const int b = tile / per_band, r = tile - b * per_band;
     const int gk = min(band, n_kunits - b * band);
@@ -407,6 +412,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int tile = unit; tile < n_tiles && ok; tile += n_units) {
       int ku, tt;
       coords(tile, ku, tt);
+      const int cbase = (tile / n_tiles1) * n_chunks;  // first contraction chunk of the split
       const int kt = ku * CG + static_cast<int>(rank);
       const int ty = tt * BT + static_cast<int>(rank) * B_ROWS;
       for (int c = 0; c < n_chunks; ++c) {
@@ -424,22 +430,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if constexpr (C::QUANT) {
               mbar_arrive_expect_tx(full_p(s), C::P_BYTES);
               tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_p(s),
-                          p_window_start<WT>(kt) / 4, c * BC);
+                          p_window_start<WT>(kt) / 4, (cbase + c) * BC);
               pend_p |= 1u << s;
             } else {
               const uint32_t a_dst = smem_addr(sA + s * A_STAGE);
               if constexpr (CG == 2) {
-                tma_load_2d_pair(a_dst, &map_w, abar, kt * BM, c * BC);
-                tma_load_2d_pair(a_dst + A_COLBLK, &map_w, abar, kt * BM + 64, c * BC);
+                tma_load_2d_pair(a_dst, &map_w, abar, kt * BM, (cbase + c) * BC);
+                tma_load_2d_pair(a_dst + A_COLBLK, &map_w, abar, kt * BM + 64, (cbase + c) * BC);
               } else {
-                tma_load_2d(a_dst, &map_w, abar, kt * BM, c * BC);
-                tma_load_2d(a_dst + A_COLBLK, &map_w, abar, kt * BM + 64, c * BC);
+                tma_load_2d(a_dst, &map_w, abar, kt * BM, (cbase + c) * BC);
+                tma_load_2d(a_dst + A_COLBLK, &map_w, abar, kt * BM + 64, (cbase + c) * BC);
               }
             }
             if constexpr (CG == 2)
-              tma_load_2d_pair(smem_addr(sB + s * B_STAGE), &map_y, abar, c * BC, ty);
+              tma_load_2d_pair(smem_addr(sB + s * B_STAGE), &map_y, abar, (cbase + c) * BC, ty);
             else
-              tma_load_2d(smem_addr(sB + s * B_STAGE), &map_y, abar, c * BC, ty);
+              tma_load_2d(smem_addr(sB + s * B_STAGE), &map_y, abar, (cbase + c) * BC, ty);
             pend_ph = (pend_ph & ~(1u << s)) | (ph << s);
           }
         }
@@ -584,15 +590,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const int k = kt * BM + 32 * eq + lane;
       const bool kin = k < K;
+      // split contraction: raw partial sums to part[split] (beta in the reduce)
+      float* out = part ? part + static_cast<int64_t>(tile / n_tiles1) * T * K : dX;
+      const float b = part ? 0.0f : beta;
 #pragma unroll 1
       for (int cb = 0; cb < BT / 32; ++cb) {
         const int tb = tt * BT + 32 * cb;
         float old[32];
-        if (beta != 0.0f && kin) {
+        if (b != 0.0f && kin) {
           // all loads of the column block first: one round trip, not 32
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            old[i] = (tb + i < T) ? dX[static_cast<int64_t>(tb + i) * K + k] : 0.0f;
+            old[i] = (tb + i < T) ? out[static_cast<int64_t>(tb + i) * K + k] : 0.0f;
         }
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * eq) << 16) +
@@ -603,7 +612,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int i = 0; i < 32; ++i) {
             if (tb + i < T) {
               const float v = __uint_as_float(r[i]);
-              dX[static_cast<int64_t>(tb + i) * K + k] = beta != 0.0f ? fmaf(beta, old[i], v) : v;
+              out[static_cast<int64_t>(tb + i) * K + k] = b != 0.0f ? fmaf(b, old[i], v) : v;
             }
           }
         }
@@ -639,36 +648,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 int64_t tc_dy16_ld(int64_t N) { return (N + 7) / 8 * 8; }
 
+// Tile shape and contraction split from a small cost model: a stage (64
+// contraction rows of one tile) costs about the same time in either tile
+// shape (the decoders bound it), pair tiles cover 4x the outputs on 2 SMs,
+// items run in waves over the persistent units, and a split adds the partial
+// slabs' write + read (plus one dX read for beta) at ~6 TB/s.
 TcPlan plan_tc(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force) {
-  TcPlan p{};
-  p.n_chunks = static_cast<int>((N + tc::BC - 1) / tc::BC);
-  const int64_t pair_tiles = ((K + 255) / 256) * ((T + 255) / 256);
-  const bool pair = cg_force ? cg_force == 2 : pair_tiles * 2 >= dev.num_sms;
-  if (pair) {
-    p.cg = 2;
-    p.bt = 256;
-    p.n_kunits = static_cast<int>((K + 255) / 256);
-    p.n_ttiles = static_cast<int>((T + 255) / 256);
-  } else {
-    p.cg = 1;
-    p.bt = 128;
-    p.n_kunits = static_cast<int>((K + 127) / 128);
-    p.n_ttiles = static_cast<int>((T + 127) / 128);
+  const int64_t chunks = (N + tc::BC - 1) / tc::BC;
+  const double stage_us = 0.45, bw_bytes_per_us = 6.0e6;
+  TcPlan best{};
+  double best_t = -1.0;
+  for (int cg = 1; cg <= 2; ++cg) {
+    if (cg_force && cg != cg_force) continue;
+    const int64_t bt = cg == 2 ? 256 : 128;
+    const int64_t nku = (K + 128 * cg - 1) / (128 * cg), ntt = (T + bt - 1) / bt;
+    const int64_t tiles = nku * ntt, avail = dev.num_sms / cg;
+    for (int64_t s = 1; s <= 16; ++s) {
+      const int64_t cps = (chunks + s - 1) / s;
+      if (s > 1 && cps < 8) break;  // at least 8 stages per split
+      const int64_t waves = (tiles * s + avail - 1) / avail;
+      double t = static_cast<double>(waves) * static_cast<double>(cps) * stage_us;
+      if (s > 1) t += static_cast<double>(2 * s + 2) * static_cast<double>(T * K) * 4.0 / bw_bytes_per_us;
+      if (best_t < 0 || t < best_t * 0.98) {
+        best_t = t;
+        best = TcPlan{};
+        best.cg = cg;
+        best.bt = static_cast<int>(bt);
+        best.n_kunits = static_cast<int>(nku);
+        best.n_ttiles = static_cast<int>(ntt);
+        best.n_splits = static_cast<int>(s);
+        best.n_chunks = static_cast<int>(cps);
+        best.grid = static_cast<int>(std::min(tiles * s, avail) * cg);
+      }
+    }
   }
-  const int64_t tiles = static_cast<int64_t>(p.n_kunits) * p.n_ttiles;
-  const int64_t units = std::min<int64_t>(tiles, dev.num_sms / p.cg);
-  p.grid = static_cast<int>(units * p.cg);
-  return p;
+  return best;
 }
 
 template <int WT, int CG, int BT>
 static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my, float* dX,
-                               float beta, int T, int K, const TcPlan& p, const DevInfo& dev,
-                               cudaStream_t stream, int inject) {
+                               float beta, int T, int K, const TcPlan& p, float* part,
+                               const DevInfo& dev, cudaStream_t stream, int inject) {
   using C = tc::Cfg<WT, CG, BT>;
   auto kern = tc::out_prod_tc_kernel<WT, CG, BT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_BYTES);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   WaitCtl ctl{dev.status, dev.wait_limit_ns};
   cudaLaunchConfig_t cfg = {};
@@ -695,21 +718,23 @@ static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my, flo
   const int units = std::min(p.grid / CG, mc);
   cfg.gridDim = dim3(static_cast<unsigned>(units * CG), 1, 1);
   return cudaLaunchKernelEx(&cfg, kern, mw, my, dX, beta, T, K, p.n_kunits, p.n_ttiles, p.band,
-                            p.n_chunks, ctl, inject);
+                            p.n_chunks, p.n_splits, part, ctl, inject);
 }
 
 template <int WT>
 static cudaError_t launch_tc_w(const CUtensorMap& mw, const CUtensorMap& my, float* dX,
-                               float beta, int T, int K, const TcPlan& p, const DevInfo& dev,
-                               cudaStream_t stream, int inject) {
-  if (p.cg == 2) return launch_tc_t<WT, 2, 256>(mw, my, dX, beta, T, K, p, dev, stream, inject);
-  return launch_tc_t<WT, 1, 128>(mw, my, dX, beta, T, K, p, dev, stream, inject);
+                               float beta, int T, int K, const TcPlan& p, float* part,
+                               const DevInfo& dev, cudaStream_t stream, int inject) {
+  if (p.cg == 2) return launch_tc_t<WT, 2, 256>(mw, my, dX, beta, T, K, p, part, dev, stream, inject);
+  return launch_tc_t<WT, 1, 128>(mw, my, dX, beta, T, K, p, part, dev, stream, inject);
 }
 
 cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
-                      int64_t ld_dy16, int64_t T, float* dX, float beta, const DevInfo& dev,
-                      cudaStream_t stream, int cg_force, int inject_stall) {
+                      int64_t ld_dy16, int64_t T, float* dX, float beta, float* part,
+                      const DevInfo& dev, cudaStream_t stream, int cg_force, int inject_stall) {
   TcPlan p = plan_tc(N, K, T, dev, cg_force);
+  if (p.n_splits > 1 && part == nullptr) return cudaErrorInvalidValue;
+  float* partial = p.n_splits > 1 ? part : nullptr;
   // band of k units whose slice of W fits comfortably in L2 (48 MB)
   const double w_per_value = is_quant(wtype) ? static_cast<double>(block_bytes(wtype)) / block_values(wtype) : 2.0;
   const double slice = static_cast<double>(N) * (tc::BM * p.cg) * w_per_value;
@@ -732,14 +757,22 @@ cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint
                    tc::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   const int t = static_cast<int>(T), k = static_cast<int>(K);
+  cudaError_t e;
   switch (wtype) {
-    case RG_F16: return launch_tc_w<RG_F16>(mw, my, dX, beta, t, k, p, dev, stream, inject_stall);
-    case RG_BF16: return launch_tc_w<RG_BF16>(mw, my, dX, beta, t, k, p, dev, stream, inject_stall);
-    case RG_Q8_0: return launch_tc_w<RG_Q8_0>(mw, my, dX, beta, t, k, p, dev, stream, inject_stall);
-    case RG_Q4_0: return launch_tc_w<RG_Q4_0>(mw, my, dX, beta, t, k, p, dev, stream, inject_stall);
-    case RG_Q4_K: return launch_tc_w<RG_Q4_K>(mw, my, dX, beta, t, k, p, dev, stream, inject_stall);
+    case RG_F16: e = launch_tc_w<RG_F16>(mw, my, dX, beta, t, k, p, partial, dev, stream, inject_stall); break;
+    case RG_BF16: e = launch_tc_w<RG_BF16>(mw, my, dX, beta, t, k, p, partial, dev, stream, inject_stall); break;
+    case RG_Q8_0: e = launch_tc_w<RG_Q8_0>(mw, my, dX, beta, t, k, p, partial, dev, stream, inject_stall); break;
+    case RG_Q4_0: e = launch_tc_w<RG_Q4_0>(mw, my, dX, beta, t, k, p, partial, dev, stream, inject_stall); break;
+    case RG_Q4_K: e = launch_tc_w<RG_Q4_K>(mw, my, dX, beta, t, k, p, partial, dev, stream, inject_stall); break;
     default: return cudaErrorInvalidValue;
   }
+  if (e != cudaSuccess || p.n_splits == 1) return e;
+  return launch_reduce_partials(partial, p.n_splits, T * K, dX, beta, dev, stream);
+}
+
+int64_t tc_partial_splits(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force) {
+  const TcPlan p = plan_tc(N, K, T, dev, cg_force);
+  return p.n_splits > 1 ? p.n_splits : 0;
 }
 
 }  // namespace rg

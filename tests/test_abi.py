@@ -49,7 +49,9 @@ def test_strerror_and_version(lib):
 
 
 def test_dispatch(lib):
-    assert rg.rg_select_variant(inputs.Q8_0, 256, 256, 32) == rg.RG_VARIANT_SMALLT
+    assert rg.rg_select_variant(inputs.Q8_0, 4096, 4096, 2) == rg.RG_VARIANT_SMALLT
+    assert rg.rg_select_variant(inputs.Q8_0, 256, 256, 32) == rg.RG_VARIANT_SMALLT   # 4 MFLOP
+    assert rg.rg_select_variant(inputs.Q8_0, 4096, 4096, 32) == rg.RG_VARIANT_TC
     assert rg.rg_select_variant(inputs.Q4_K, 14336, 4096, 2048) == rg.RG_VARIANT_TC
     assert rg.rg_workspace_bytes(rg.RG_VARIANT_TC, inputs.Q4_K, 14336, 4096, 2048) == 2048 * 14336 * 2
     assert rg.rg_workspace_bytes(rg.RG_VARIANT_TC, inputs.Q4_K, 13, 4096, 3) == 3 * 16 * 2 + 160

@@ -225,3 +225,21 @@ def test_timeout_probe_reports_and_context_survives(rg):
     Wd = oracle.dequant(inputs.Q8_0, W, N, K)
     assert_within(got, oracle.out_prod(inputs.Q8_0, W, N, K, dY, T, Wd=Wd),
                   oracle.abs_bound(dY, Wd), 5e-3)
+
+
+@pytest.mark.parametrize("variant", [1, 4, 5])
+@pytest.mark.parametrize("wtype", TYPES)
+@pytest.mark.parametrize("beta", [0.0, 1.0])
+def test_split_contraction(rg, variant, wtype, beta):
+    """Few output tiles and a long contraction: the tensor-core kernel splits
+    the rows of W over CTAs and a second kernel adds the partial tiles."""
+    N, K, T = 2050, 512, 100        # ragged N: the last split runs past the end of W
+    W = inputs.gen_weight(wtype, N, K, seed=31, stream=1)
+    dY = inputs.normal_f32(31, 2, T * N, 1e-3).reshape(T, N)
+    dX0 = inputs.normal_f32(31, 3, T * K, 1e-3).reshape(T, K) if beta else None
+    Wd = oracle.dequant(wtype, W, N, K)
+    ref = oracle.out_prod(wtype, W, N, K, dY, T, dX0, beta, Wd=Wd)
+    bnd = oracle.abs_bound(dY, Wd)
+    got = run_out_prod(rg, variant, wtype, W, N, K, dY, T, dX0, beta)
+    extra = np.abs(beta * dX0) * 2.0 ** -24 / 5e-3 if beta else 0.0
+    assert_within(got, ref, bnd + extra, 5e-3, f"split variant {variant} type {wtype}")
