@@ -152,6 +152,45 @@ def oracle_sample(problems, t_rows: int, n_rows: int | None = None):
 
 
 # ---------------------------------------------------------------------------
+# the route the method replaces: a dense F32 copy of W, then a full-F32 GEMM
+
+def second_reference(torch, rg, problems, devbuf, stream, dev, flush_buf, reps: int = 5):
+    """Time rg_dequant into a dense F32 [N, K] buffer followed by cuBLAS SGEMM
+    (TF32 off) for every call of the workload, on the resident inputs.  dX
+    buffers are overwritten (the timed leg has already run)."""
+    tf32 = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        wf = torch.empty(max(p.N * p.K for p in problems), dtype=torch.float32, device=dev)
+
+        def one():
+            for i, p in enumerate(problems):
+                W, dY, dX = devbuf[i]
+                w = wf[:p.N * p.K].view(p.N, p.K)
+                rg.check(rg.rg_dequant_async(p.wtype, W, p.N, p.K, w, stream), "rg_dequant_async")
+                if p.beta != 0.0:
+                    dX.addmm_(dY, w, beta=p.beta)
+                else:
+                    torch.mm(dY, w, out=dX)
+
+        times = []
+        for r in range(2 + reps):
+            if flush_buf is not None:
+                flush_buf.fill_(0.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            one()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if r >= 2:
+                times.append(a.elapsed_time(b))
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = tf32
+    return {"ms_per_step": statistics.median(times), "unit": "TFLOP/s", "reps": reps,
+            "what": "rg_dequant to a dense F32 copy of W, then cuBLAS SGEMM with TF32 off "
+                    "(median of the reps)",
+            "extra_bytes_per_step": sum(8 * p.N * p.K for p in problems)}
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -165,6 +204,8 @@ def parse():
     ap.add_argument("--ref-wrows", type=int, default=512, help="W rows per call, reference-arm step")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-second-ref", action="store_true",
+                    help="skip timing rg_dequant + cuBLAS SGEMM (the dense-F32 route)")
     ap.add_argument("--custom", default=None,
                     help="a custom call instead of --workload, e.g. q8_0:4096x14336:t8192:beta0")
     ap.add_argument("--variant", default="auto", choices=["auto", "tc", "tc1", "tc2", "smallt", "simt32"],
@@ -276,6 +317,18 @@ def run_ours(args):
         return rg.rg_out_prod(p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, stream)
 
     is_tc = [v in (rg.RG_VARIANT_TC, rg.RG_VARIANT_TC_SINGLE, rg.RG_VARIANT_TC_PAIR) for v in variants]
+    plans = []
+    for p in problems:
+        info = rg.rg_plan_info()
+        rg.check(rg.rg_plan(forced, p.wtype, p.N, p.K, p.T, info), "rg_plan")
+        plans.append(info.as_dict())
+
+    # inputs that fit in L2: a write of twice its size between steps, outside
+    # the timed calls (the step time is then the sum of the calls' own times)
+    step_bytes = sum(p.algorithmic_bytes() for p in problems)
+    flush_buf = None
+    if step_bytes < 2 * L2_BYTES:
+        flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
     def step(events=None):
         for i, p in enumerate(problems):
@@ -292,6 +345,8 @@ def run_ours(args):
 
     for _ in range(args.warmup):
         step()
+        if flush_buf is not None:
+            flush_buf.fill_(0.0)
     rg.check(rg.rg_check(stream), "warmup")
 
     per_call = [[] for _ in problems]
@@ -312,10 +367,14 @@ def run_ours(args):
             for e in quad:
                 e.record(stream)
     torch.cuda.synchronize()
+    launches0 = rg.rg_launch_count()
     ev0.record(stream)
     for s in range(args.steps):
         step(evs[s])
+        if flush_buf is not None:
+            flush_buf.fill_(float(s))
     ev1.record(stream)
+    launches = rg.rg_launch_count() - launches0
     torch.cuda.synchronize()
     clocks = sampler.stop()
     rg.check(rg.rg_check(stream), "timed region")
@@ -325,6 +384,8 @@ def run_ours(args):
             per_call[i].append(evs[s][i][0].elapsed_time(evs[s][i][1]))
             if is_tc[i]:
                 per_gemm[i].append(evs[s][i][2].elapsed_time(evs[s][i][3]))
+    if flush_buf is not None:
+        ms_total = sum(sum(c) for c in per_call)
     ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
     flops_step = sum(p.flops for p in problems)
@@ -408,8 +469,15 @@ def run_ours(args):
                       "gemm_ms": statistics.median(per_gemm[i]) if per_gemm[i] else None,
                       "tflops": p.flops / t / 1e12,
                       "effective_gbs": p.algorithmic_bytes() / t / 1e9,
+                      "plan": plans[i],
                       "roofline_frac": max(p.flops / (peak * 1e12),
                                            p.algorithmic_bytes() / (peaks["hbm_gbs"] * 1e9)) / t})
+
+    second = None if args.no_second_ref else second_reference(torch, rg, problems, devbuf, stream,
+                                                                   dev, flush_buf)
+    if second is not None:
+        second["ms_per_step"] = max_over_ranks(second["ms_per_step"], dev)
+        second["value"] = job_tflops(flops_step, second["ms_per_step"], world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -417,10 +485,13 @@ def run_ours(args):
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
                "kind": "oracle", "sample": desc, "seconds": dt}
 
-    launches_per_call = {rg.RG_VARIANT_TC: 2, rg.RG_VARIANT_TC_SINGLE: 2, rg.RG_VARIANT_TC_PAIR: 2,
-                         rg.RG_VARIANT_SMALLT: 1, rg.RG_VARIANT_SIMT32: 1}
-    gpu_launches = args.steps * sum(launches_per_call[v] for v in variants)
-    step_bytes = sum(p.algorithmic_bytes() for p in problems)
+    planned = args.steps * sum(pl["launches"] for pl in plans)
+    if launches != planned:
+        raise RuntimeError(f"{launches} kernel launches in the timed region, the plans say {planned}")
+    l2 = (f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step > 129 MB); no flush"
+          if flush_buf is None else
+          f"inputs fit in L2 ({step_bytes / 1e6:.1f} MB per step): a {2 * L2_BYTES >> 20} MB write "
+          "between steps flushes it; step time = sum of the calls' event times")
     line = {
         "metric": "out_prod TFLOP/s (2*T*N*K / time)", "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -428,11 +499,10 @@ def run_ours(args):
         "dtype": _dtype_name(problems), "data": "synthetic",
         "config": {"workload": args.workload, "calls": len(problems),
                    "flops_per_step": flops_step, "algorithmic_bytes_per_step": step_bytes,
-                   "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step > 129 MB); no flush",
-                   "parallelism": f"replicas x{world}"},
+                   "l2": l2, "parallelism": f"replicas x{world}"},
         "effective_gbs": world * step_bytes / (ms_step * 1e-3) / 1e9,
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
-        "clocks": clocks, "per_call": calls,
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "clocks": clocks, "second_reference": second, "per_call": calls,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

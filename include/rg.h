@@ -157,6 +157,34 @@ int rg_out_prod_noalloc(int wtype, const void* W, int64_t N, int64_t K,
 /* The variant RG_VARIANT_AUTO picks for this shape (ignores RG_VARIANT). */
 int rg_select_variant(int wtype, int64_t N, int64_t K, int64_t T);
 
+/* How one OUT_PROD call of a shape runs on the current device: a report for
+ * measurement (the redundant-decode count the method trades for not storing
+ * an F32 copy of W), filled in without launching or allocating anything. */
+typedef struct rg_plan_info {
+  int32_t variant;          /* the variant that runs (never RG_VARIANT_AUTO) */
+  int32_t cta_group;        /* tensor-core variants: CTAs per MMA (1 or 2); else 0 */
+  int32_t tile_k;           /* output tile: values along K ... */
+  int32_t tile_t;           /* ... by rows along T (dY rows one pass over W serves) */
+  int32_t n_splits;         /* contraction over N split into this many partial sums (1: none) */
+  int32_t grid;             /* CTAs of the main kernel (tensor-core: before the residency cap) */
+  int32_t launches;         /* kernels one call enqueues */
+  int32_t reserved;         /* 0 */
+  int64_t decode_ops;       /* weight values decoded per call: ceil(T / tile_t) * N * K */
+  int64_t workspace_bytes;  /* what rg_out_prod_ws needs for this variant */
+} rg_plan_info;
+
+/* Fills *out for `variant` (RG_VARIANT_AUTO: the shape's choice) and returns
+ * RG_OK; RG_ERR_TYPE, RG_ERR_ARG (out NULL, negative or too large sizes) or
+ * RG_ERR_SHAPE as rg_out_prod validates them; RG_ERR_CUDA without a current
+ * CUDA device (the plan depends on its SM count).  T == 0 or K == 0: nothing
+ * runs (launches 0); N == 0: one kernel scales dX by beta. */
+int rg_plan(int variant, int wtype, int64_t N, int64_t K, int64_t T, rg_plan_info* out);
+
+/* Kernels this library has enqueued in this process (all devices and entry
+ * points, successful launches only): a measurement aid, read before and after
+ * a region to count its launches. */
+uint64_t rg_launch_count(void);
+
 /*
  * out[n, k] = deq(W)[n, k] as F32, bit-exact: every decoded value is an exact
  * F32 (Q8_0: 11-bit x 8-bit product; Q4_0: 11-bit x 4-bit; F16/BF16: widened)
@@ -190,7 +218,8 @@ int rg_version(void);
  * a TC variant) made from this host thread records the CUDA event `before`
  * on its stream right before its GEMM kernel and `after` right after it
  * (cudaEvent_t handles passed as void*), so the kernel alone can be timed
- * inside a larger timed region; the dY conversion is outside the pair.  The
+ * inside a larger timed region; the dY conversion is outside the pair, the
+ * partial-sum reduction of a split contraction inside it.  The
  * events are used once, then forgotten.  NULL, NULL clears.  Returns RG_OK. */
 int rg_profile_next_gemm(void* before, void* after);
 

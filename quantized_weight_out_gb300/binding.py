@@ -23,6 +23,18 @@ RG_VARIANT_AUTO, RG_VARIANT_TC, RG_VARIANT_SMALLT, RG_VARIANT_SIMT32 = 0, 1, 2, 
 RG_VARIANT_TC_SINGLE, RG_VARIANT_TC_PAIR = 4, 5
 VARIANTS = {"auto": 0, "tc": 1, "smallt": 2, "simt32": 3, "tc1": 4, "tc2": 5}
 
+class rg_plan_info(ctypes.Structure):
+    """include/rg.h rg_plan_info."""
+    _fields_ = [("variant", ctypes.c_int32), ("cta_group", ctypes.c_int32),
+                ("tile_k", ctypes.c_int32), ("tile_t", ctypes.c_int32),
+                ("n_splits", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("launches", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("decode_ops", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
+
+
 # (name, restype, argtypes) of every exported function
 _I64, _VP, _F, _I, _SZ = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int, ctypes.c_size_t
 SIGNATURES = [
@@ -40,6 +52,8 @@ SIGNATURES = [
     ("rg_debug_wait_probe", _I, [_I, _VP]),
     ("rg_profile_next_gemm", _I, [_VP, _VP]),
     ("rg_out_prod_noalloc", _I, [_I, _VP, _I64, _I64, _VP, _I64, _VP, _F, _VP]),
+    ("rg_plan", _I, [_I, _I, _I64, _I64, _I64, ctypes.POINTER(rg_plan_info)]),
+    ("rg_launch_count", ctypes.c_uint64, []),
 ]
 
 RG_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -114,6 +128,14 @@ def rg_out_prod_ws(variant, wtype, W, N, K, dY, T, dX, beta, workspace, workspac
 
 def rg_select_variant(wtype, N, K, T) -> int:
     return load().rg_select_variant(wtype, N, K, T)
+
+
+def rg_plan(variant, wtype, N, K, T, out: rg_plan_info) -> int:
+    return load().rg_plan(variant, wtype, N, K, T, ctypes.byref(out))
+
+
+def rg_launch_count() -> int:
+    return int(load().rg_launch_count())
 
 
 def rg_dequant(wtype, W, N, K, out) -> int:

@@ -14,6 +14,8 @@
 
 namespace rg {
 
+std::atomic<unsigned long long> g_launch_count{0};
+
 // The per-device status word: a kernel that gives up a bounded wait records
 // RG_ERR_TIMEOUT here; rg_check reads and clears it.
 __device__ int g_status_word;
@@ -425,6 +427,54 @@ int rg_out_prod_noalloc(int wtype, const void* W, int64_t N, int64_t K, const fl
 int rg_select_variant(int wtype, int64_t N, int64_t K, int64_t T) {
   return select_variant(wtype, N, K, T);
 }
+
+int rg_plan(int variant, int wtype, int64_t N, int64_t K, int64_t T, rg_plan_info* out) {
+  if (!out) return RG_ERR_ARG;
+  if (wtype < RG_F16 || wtype > RG_Q4_K) return RG_ERR_TYPE;
+  if (variant < RG_VARIANT_AUTO || variant > RG_VARIANT_TC_PAIR) return RG_ERR_TYPE;
+  if (N < 0 || K < 0 || T < 0 || N > kMaxDim || K > kMaxDim || T > kMaxDim) return RG_ERR_ARG;
+  if (K % (is_quant(wtype) ? 256 : 8)) return RG_ERR_SHAPE;
+  DevInfo* dev = nullptr;
+  const int st = current_dev(&dev);
+  if (st != RG_OK) return st;
+  rg_plan_info r{};
+  r.variant = variant == RG_VARIANT_AUTO ? select_variant(wtype, N, K, T) : variant;
+  r.n_splits = 1;
+  if (T == 0 || K == 0 || N == 0) {
+    r.launches = (T == 0 || K == 0) ? 0 : 1;
+    *out = r;
+    return RG_OK;
+  }
+  int64_t tile_t = 0;
+  if (is_tc(r.variant)) {
+    const TcPlan p = plan_tc(N, K, T, *dev, cg_force_of(r.variant));
+    r.cta_group = p.cg;
+    r.tile_k = 128 * p.cg;
+    tile_t = p.bt;
+    r.n_splits = p.n_splits;
+    r.grid = p.grid;
+    r.launches = p.n_splits > 1 ? 3 : 2;  // dY conversion, GEMM, partial reduction
+  } else if (r.variant == RG_VARIANT_SMALLT) {
+    const SmalltPlan p = plan_smallt(N, K, T, *dev);
+    r.tile_k = 256;
+    tile_t = p.tb;
+    r.n_splits = p.n_splits;
+    r.grid = p.n_ktiles * p.n_splits * p.n_tchunks;
+    r.launches = 2;  // row-split partial sums, their reduction
+  } else {
+    r.tile_k = 64;
+    tile_t = 64;
+    r.grid = static_cast<int32_t>(((K + 63) / 64) * ((T + 63) / 64));
+    r.launches = 1;
+  }
+  r.tile_t = static_cast<int32_t>(tile_t);
+  r.decode_ops = (T + tile_t - 1) / tile_t * N * K;
+  r.workspace_bytes = static_cast<int64_t>(workspace_for(r.variant, N, K, T, *dev));
+  *out = r;
+  return RG_OK;
+}
+
+uint64_t rg_launch_count(void) { return g_launch_count.load(std::memory_order_relaxed); }
 
 int rg_dequant_async(int wtype, const void* W, int64_t N, int64_t K, float* out, void* stream) {
   if (wtype < RG_F16 || wtype > RG_Q4_K) return RG_ERR_TYPE;

@@ -51,7 +51,7 @@ cudaError_t launch_dequant(int wtype, const void* W, int64_t N, int64_t K, float
     case RG_Q4_K: dequant_kernel<RG_Q4_K><<<grid, 256, 0, stream>>>(w, N, K, rb, out); break;
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 // dY [T, N] F32 -> [T, ld] 16-bit, round to nearest even.  One thread per 8
@@ -100,7 +100,7 @@ cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t ld,
     convert_dy_kernel<true><<<grid, 256, 0, stream>>>(dY, T, N, ld, out);
   else
     convert_dy_kernel<false><<<grid, 256, 0, stream>>>(dY, T, N, ld, out);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 __global__ void __launch_bounds__(256) scale_kernel(float* __restrict__ x, int64_t count,
@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(256) scale_kernel(float* __restrict__ x, int64
 cudaError_t launch_scale(float* dX, int64_t count, float beta, const DevInfo& dev,
                          cudaStream_t stream) {
   scale_kernel<<<grid_for(count, 256, dev), 256, 0, stream>>>(dX, count, beta);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 // One thread waits on an mbarrier that nothing arrives on.
@@ -134,7 +134,7 @@ cudaError_t launch_wait_probe(const DevInfo& dev, unsigned long long limit_ns,
                               cudaStream_t stream) {
   WaitCtl ctl{dev.status, limit_ns};
   wait_probe_kernel<<<1, 32, 0, stream>>>(ctl);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 }  // namespace rg

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/rg.h"
 
 namespace rg {
@@ -20,6 +22,14 @@ struct DevInfo {
   int* status;          // device address of this device's status word
   unsigned long long wait_limit_ns;
 };
+
+// Kernels launched by this library (rg_launch_count); every launcher passes
+// its launch status through counted().
+extern std::atomic<unsigned long long> g_launch_count;
+inline cudaError_t counted(cudaError_t e) {
+  if (e == cudaSuccess) g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
 
 // All launchers enqueue on `stream` and return cudaSuccess or the launch
 // error; arguments are already validated by the entry points.

@@ -111,7 +111,7 @@ cudaError_t launch_simt32(int wtype, const void* W, int64_t N, int64_t K, const 
     case RG_Q4_K: simt32_kernel<RG_Q4_K><<<grid, 256, 0, stream>>>(w, rb, n, k, dY, t, dX, beta); break;
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 }  // namespace rg

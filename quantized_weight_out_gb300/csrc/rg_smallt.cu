@@ -306,7 +306,7 @@ static cudaError_t launch_smallt_t(const CUtensorMap& map, int64_t N, int64_t K,
   WaitCtl ctl{dev.status, dev.wait_limit_ns};
   kern<<<grid, smt::THREADS + 32, smem, stream>>>(map, static_cast<int>(N), static_cast<int>(K), dY,
                                                    static_cast<int>(T), part, p.rows_per_split, ctl);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 template <int WT>
@@ -349,7 +349,7 @@ cudaError_t launch_reduce_partials(const float* part, int n_splits, int64_t TK, 
   const int64_t blocks = std::min<int64_t>((TK / 4 + 255) / 256, static_cast<int64_t>(dev.num_sms) * 8);
   smt::smallt_reduce<<<static_cast<unsigned>(std::max<int64_t>(1, blocks)), 256, 0, stream>>>(
       part, n_splits, TK, dX, beta);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 }  // namespace rg

@@ -717,8 +717,8 @@ static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my, flo
   }
   const int units = std::min(p.grid / CG, mc);
   cfg.gridDim = dim3(static_cast<unsigned>(units * CG), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, mw, my, dX, beta, T, K, p.n_kunits, p.n_ttiles, p.band,
-                            p.n_chunks, p.n_splits, part, ctl, inject);
+  return counted(cudaLaunchKernelEx(&cfg, kern, mw, my, dX, beta, T, K, p.n_kunits, p.n_ttiles, p.band,
+                            p.n_chunks, p.n_splits, part, ctl, inject));
 }
 
 template <int WT>

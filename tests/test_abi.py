@@ -58,6 +58,19 @@ def test_dispatch(lib):
     assert rg.rg_workspace_bytes(rg.RG_VARIANT_SIMT32, inputs.Q4_K, 14336, 4096, 8) == 0
 
 
+def test_plan_validates_before_needing_a_device(lib):
+    info = rg.rg_plan_info()
+    assert rg.rg_plan(0, 9, 64, 256, 8, info) == rg.RG_ERR_TYPE
+    assert rg.rg_plan(6, inputs.Q8_0, 64, 256, 8, info) == rg.RG_ERR_TYPE
+    assert rg.rg_plan(0, inputs.Q8_0, 64, 200, 8, info) == rg.RG_ERR_SHAPE
+    assert rg.rg_plan(0, inputs.F16, 64, 12, 8, info) == rg.RG_ERR_SHAPE
+    assert rg.rg_plan(0, inputs.Q8_0, -1, 256, 8, info) == rg.RG_ERR_ARG
+    assert rg.rg_plan(0, inputs.Q8_0, 64, 256, 1 << 31, info) == rg.RG_ERR_ARG
+    assert lib.rg_plan(0, inputs.Q8_0, 64, 256, 8, None) == rg.RG_ERR_ARG
+    assert ctypes.sizeof(rg.rg_plan_info) == 48
+    assert rg.rg_launch_count() >= 0
+
+
 BAD = 0x1000  # never dereferenced: every case below fails validation first
 
 

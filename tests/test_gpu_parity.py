@@ -243,3 +243,36 @@ def test_split_contraction(rg, variant, wtype, beta):
     got = run_out_prod(rg, variant, wtype, W, N, K, dY, T, dX0, beta)
     extra = np.abs(beta * dX0) * 2.0 ** -24 / 5e-3 if beta else 0.0
     assert_within(got, ref, bnd + extra, 5e-3, f"split variant {variant} type {wtype}")
+
+
+# ----------------------------------------------------------------------------
+# rg_plan agrees with what a call launches
+
+@pytest.mark.parametrize("variant", [0] + ALL_VARIANTS)
+@pytest.mark.parametrize("wtype,N,K,T", [(inputs.Q4_K, 2050, 512, 100), (inputs.Q8_0, 1024, 4096, 600),
+                                         (inputs.Q4_0, 300, 256, 3), (inputs.F16, 64, 1024, 40)])
+def test_plan_matches_the_call(rg, variant, wtype, N, K, T):
+    info = rg.rg_plan_info()
+    rg.check(rg.rg_plan(variant, wtype, N, K, T, info), "rg_plan")
+    expect = variant if variant else rg.rg_select_variant(wtype, N, K, T)
+    assert info.variant == expect
+    assert info.decode_ops == -(-T // info.tile_t) * N * K
+    assert info.workspace_bytes == rg.rg_workspace_bytes(expect, wtype, N, K, T)
+    assert (info.cta_group in (1, 2)) == (expect in (1, 4, 5))
+    assert info.n_splits >= 1 and info.grid >= 1
+    W = inputs.gen_weight(wtype, N, K, seed=5, stream=1)
+    dY = inputs.normal_f32(5, 2, T * N, 1e-3).reshape(T, N)
+    torch.cuda.synchronize()
+    before = rg.rg_launch_count()
+    got = run_out_prod(rg, variant, wtype, W, N, K, dY, T)
+    assert rg.rg_launch_count() - before == info.launches
+    ref = oracle.out_prod(wtype, W, N, K, dY, T)
+    assert_within(got, ref, oracle.abs_bound(dY, oracle.dequant(wtype, W, N, K)), TOL[expect], "plan")
+
+
+def test_plan_of_empty_shapes(rg):
+    info = rg.rg_plan_info()
+    rg.check(rg.rg_plan(0, inputs.Q8_0, 64, 256, 0, info))
+    assert info.launches == 0 and info.decode_ops == 0
+    rg.check(rg.rg_plan(0, inputs.Q8_0, 0, 256, 8, info))
+    assert info.launches == 1 and info.decode_ops == 0
