@@ -150,9 +150,10 @@ size_t tc_workspace_total(int variant, int64_t N, int64_t K, int64_t T, const De
 }
 
 // Workspace bytes of a resolved (non-auto) variant; N, K, T > 0.
-size_t workspace_for(int variant, int64_t N, int64_t K, int64_t T, const DevInfo& dev) {
+size_t workspace_for(int variant, int wtype, int64_t N, int64_t K, int64_t T, const DevInfo& dev) {
   if (is_tc(variant)) return tc_workspace_total(variant, N, K, T, dev);
-  if (variant == RG_VARIANT_SMALLT) return (plan_smallt(N, K, T, dev).workspace + 255) / 256 * 256;
+  if (variant == RG_VARIANT_SMALLT)
+    return (plan_smallt(wtype, N, K, T, dev).workspace + 255) / 256 * 256;
   return 0;
 }
 
@@ -221,7 +222,7 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
     return from_cuda(launch_simt32(wtype, W, N, K, dY, T, dX, beta, *dev, stream));
   // the small-T and tensor-core paths take a workspace: partial sums, or the
   // 16-bit copy of dY
-  const size_t need = workspace_for(variant, N, K, T, *dev);
+  const size_t need = workspace_for(variant, wtype, N, K, T, *dev);
   void* buf = ws;
   cudaMemPool_t pool{};
   if (own_ws) {
@@ -234,7 +235,7 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
   cudaError_t e = cudaSuccess;
   if (variant == RG_VARIANT_SMALLT) {
     e = launch_smallt(wtype, W, N, K, dY, T, dX, beta, static_cast<float*>(buf),
-                      plan_smallt(N, K, T, *dev), *dev, stream);
+                      plan_smallt(wtype, N, K, T, *dev), *dev, stream);
     if (own_ws) {
       const cudaError_t f = cudaFreeAsync(buf, stream);
       if (e == cudaSuccess) e = f;
@@ -391,7 +392,7 @@ size_t rg_workspace_bytes(int variant, int wtype, int64_t N, int64_t K, int64_t 
   if (!is_tc(variant) && variant != RG_VARIANT_SMALLT) return 0;
   DevInfo* dev = nullptr;
   if (current_dev(&dev) != RG_OK) return is_tc(variant) ? tc_workspace(N, T) : 0;
-  return workspace_for(variant, N, K, T, *dev);
+  return workspace_for(variant, wtype, N, K, T, *dev);
 }
 
 int rg_out_prod_ws(int variant, int wtype, const void* W, int64_t N, int64_t K, const float* dY,
@@ -413,7 +414,7 @@ int rg_out_prod_noalloc(int wtype, const void* W, int64_t N, int64_t K, const fl
   if (N > 0) {
     DevInfo* dev = nullptr;
     if ((st = current_dev(&dev)) != RG_OK) return st;
-    const size_t need = workspace_for(variant, N, K, T, *dev);
+    const size_t need = workspace_for(variant, wtype, N, K, T, *dev);
     if (need > 0) {
       if (need > static_cast<size_t>(RG_NOALLOC_SCRATCH_BYTES)) return RG_ERR_ARG;
       if ((st = noalloc_scratch(dev->device, &ws)) != RG_OK) return st;
@@ -455,7 +456,7 @@ int rg_plan(int variant, int wtype, int64_t N, int64_t K, int64_t T, rg_plan_inf
     r.grid = p.grid;
     r.launches = p.n_splits > 1 ? 3 : 2;  // dY conversion, GEMM, partial reduction
   } else if (r.variant == RG_VARIANT_SMALLT) {
-    const SmalltPlan p = plan_smallt(N, K, T, *dev);
+    const SmalltPlan p = plan_smallt(wtype, N, K, T, *dev);
     r.tile_k = 256;
     tile_t = p.tb;
     r.n_splits = p.n_splits;
@@ -469,7 +470,7 @@ int rg_plan(int variant, int wtype, int64_t N, int64_t K, int64_t T, rg_plan_inf
   }
   r.tile_t = static_cast<int32_t>(tile_t);
   r.decode_ops = (T + tile_t - 1) / tile_t * N * K;
-  r.workspace_bytes = static_cast<int64_t>(workspace_for(r.variant, N, K, T, *dev));
+  r.workspace_bytes = static_cast<int64_t>(workspace_for(r.variant, wtype, N, K, T, *dev));
   *out = r;
   return RG_OK;
 }

@@ -61,6 +61,16 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t h) {
   return __uint_as_float(static_cast<uint32_t>(h) << 16);
 }
 
+// Byte B of x (an unsigned integer u < 256) as the F32 value u - bias, exactly
+// and without the integer-conversion unit: the word 0x4B0000uu is the float
+// 2^23 + u (u sits in the low mantissa bits), and subtracting 2^23 + bias is
+// exact for these small integers.
+template <int B>
+__device__ __forceinline__ float byte_minus(uint32_t x, float two23_plus_bias) {
+  return __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7440u | B)) - two23_plus_bias;
+}
+constexpr float kTwo23 = 8388608.0f;  // 2^23
+
 // ---------------------------------------------------------------------------
 // mbarrier
 

@@ -59,7 +59,8 @@ struct SmalltPlan {
   int rows_per_split;  // rows of W per CTA (multiple of 8)
   size_t workspace;    // bytes of partial sums
 };
-SmalltPlan plan_smallt(int64_t N, int64_t K, int64_t T, const DevInfo& dev);
+// Sized so that the grid fills the GPU once at the kernel's residency.
+SmalltPlan plan_smallt(int wtype, int64_t N, int64_t K, int64_t T, const DevInfo& dev);
 cudaError_t launch_smallt(int wtype, const void* W, int64_t N, int64_t K, const float* dY,
                           int64_t T, float* dX, float beta, float* part, const SmalltPlan& p,
                           const DevInfo& dev, cudaStream_t stream);

@@ -71,19 +71,26 @@ __device__ __forceinline__ void decode_raw(const Raw<WT>& r, int lane, float (&w
       w[2 * i + 1] = WT == RG_F16 ? f16_to_f32(hi) : bf16_to_f32(hi);
     }
   } else if constexpr (WT == RG_Q8_0) {
+    // int8 q as the byte q + 128, then d * q: an exact product
     const float d = f16_to_f32(static_cast<uint16_t>(r.v[0]));
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int8_t q = static_cast<int8_t>((r.v[1 + (i >> 2)] >> (8 * (i & 3))) & 0xFFu);
-      w[i] = d * static_cast<float>(q);
+    for (int j = 0; j < 2; ++j) {
+      const uint32_t x = r.v[1 + j] ^ 0x80808080u;
+      w[4 * j + 0] = d * byte_minus<0>(x, kTwo23 + 128.0f);
+      w[4 * j + 1] = d * byte_minus<1>(x, kTwo23 + 128.0f);
+      w[4 * j + 2] = d * byte_minus<2>(x, kTwo23 + 128.0f);
+      w[4 * j + 3] = d * byte_minus<3>(x, kTwo23 + 128.0f);
     }
   } else if constexpr (WT == RG_Q4_0) {
     const float d = f16_to_f32(static_cast<uint16_t>(r.v[0]));
     const int shift = (lane & 2) ? 4 : 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int q = static_cast<int>((r.v[1 + (i >> 2)] >> (8 * (i & 3) + shift)) & 15u);
-      w[i] = d * static_cast<float>(q - 8);
+    for (int j = 0; j < 2; ++j) {
+      const uint32_t x = (r.v[1 + j] >> shift) & 0x0F0F0F0Fu;
+      w[4 * j + 0] = d * byte_minus<0>(x, kTwo23 + 8.0f);
+      w[4 * j + 1] = d * byte_minus<1>(x, kTwo23 + 8.0f);
+      w[4 * j + 2] = d * byte_minus<2>(x, kTwo23 + 8.0f);
+      w[4 * j + 3] = d * byte_minus<3>(x, kTwo23 + 8.0f);
     }
   } else {
     const float d = f16_to_f32(static_cast<uint16_t>(r.v[0] & 0xFFFFu));
@@ -99,12 +106,17 @@ __device__ __forceinline__ void decode_raw(const Raw<WT>& r, int lane, float (&w
       sc = (byte_at(S, j + 4) & 15) | ((byte_at(S, j - 4) >> 6) << 4);
       m = (byte_at(S, j + 4) >> 4) | ((byte_at(S, j) >> 6) << 4);
     }
+    // (d * sc) * q - dmin * m: the product is exact (at most 21 bits), so the
+    // fused form rounds once, like the definition
     const float ds = d * static_cast<float>(sc);
-    const float dm = dmin * static_cast<float>(m);
+    const float ndm = -(dmin * static_cast<float>(m));
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int q = static_cast<int>((r.v[4 + (i >> 2)] >> (8 * (i & 3) + 4 * half)) & 15u);
-      w[i] = ds * static_cast<float>(q) - dm;
+    for (int jj = 0; jj < 2; ++jj) {
+      const uint32_t x = (r.v[4 + jj] >> (4 * half)) & 0x0F0F0F0Fu;
+      w[4 * jj + 0] = fmaf(ds, byte_minus<0>(x, kTwo23), ndm);
+      w[4 * jj + 1] = fmaf(ds, byte_minus<1>(x, kTwo23), ndm);
+      w[4 * jj + 2] = fmaf(ds, byte_minus<2>(x, kTwo23), ndm);
+      w[4 * jj + 3] = fmaf(ds, byte_minus<3>(x, kTwo23), ndm);
     }
   }
 }
@@ -115,26 +127,231 @@ __host__ __device__ constexpr int tile_bytes() {
   return (256 / block_values(WT)) * block_bytes(WT);
 }
 
-constexpr int BR = 32;       // rows of W per pipeline stage
-constexpr int STAGES = 8;    // stages in flight per CTA
+// The row-per-lane consumers (quantized W, one or two rows of dY) take 64
+// rows per stage (two per lane) in a 4-deep ring; the row-per-warp consumers
+// 32 rows in an 8-deep ring: the same bytes in flight either way.
+template <int WT, int TB>
+constexpr bool rows_path() { return TB <= 2 && is_quant(WT); }
+template <int WT, int TB>
+constexpr int stage_rows() { return rows_path<WT, TB>() ? 64 : 32; }
+template <int WT, int TB>
+constexpr int n_stages() { return rows_path<WT, TB>() ? 4 : 8; }
 constexpr int CONSUMERS = 8; // consumer warps; warp 8 is the TMA producer
 constexpr int MAX_ROWS = 512;
+
+// --- one and two rows of dY: a block per warp, a row per lane ---------------
+// Warp g of the eight consumers owns block g of every row's 256-value tile
+// (the g-th Q8_0 or Q4_0 block, the g-th Q4_K sub-block, values 32g .. 32g+31
+// of F16/BF16) and lane l takes row l of each 32-row stage.  Every offset
+// inside a row is then a compile-time constant: the block's bytes come out
+// of 16-byte shared loads with constant shifts, its scale is folded into dY
+// once per row (F32 products; the acceptance bound covers the reassociation),
+// and a value costs one byte permute plus half a packed F32 add and half a
+// packed F32 fused multiply-add per row of dY.  The 32 lanes' partial sums of
+// the block's 32 values are combined by a fixed butterfly at the end.
+
+typedef unsigned long long f32x2;  // two F32 values in one 64-bit register
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(f32x2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// Two bytes (B, B+1) of x as the F32 pair (u - bias, u' - bias), exactly.
+template <int B>
+__device__ __forceinline__ f32x2 bytes2(uint32_t x, f32x2 neg_two23_bias) {
+  return add2(pack2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7440u | B)),
+                    __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7440u | (B + 1)))),
+              neg_two23_bias);
+}
+
+// Add one row's block g (its 32 values times each dY row) into acc; Q4_K's
+// min term goes to msum, subtracted once at the end.  g is the warp's index,
+// uniform over the warp: one code path serves all eight warps.
+template <int WT, int TB>
+__device__ __forceinline__ void row_block(const uint8_t* row, int g, const float (&y)[TB],
+                                          f32x2 (&acc)[TB][16], float (&msum)[TB]) {
+  static_assert(is_quant(WT), "quantized types only");
+  if constexpr (WT == RG_Q8_0 || WT == RG_Q4_0) {
+    // the block starts at byte X = g * (34 or 18), an even offset: read the
+    // aligned words around it; off2 = the block starts 2 bytes into a word
+    constexpr int BB = WT == RG_Q8_0 ? 34 : 18, NQ = WT == RG_Q8_0 ? 8 : 4;
+    const int X = BB * g;
+    const uint32_t* wp = reinterpret_cast<const uint32_t*>(row + (X & ~3));
+    const bool off2 = (X & 2) != 0;
+    uint32_t w[NQ + 1];
+#pragma unroll
+    for (int i = 0; i <= NQ; ++i) w[i] = wp[i];
+    const float d = f16_to_f32(static_cast<uint16_t>(off2 ? (w[0] >> 16) : (w[0] & 0xFFFFu)));
+    // quant word j = the 4 bytes at X + 2 + 4j
+    uint32_t q[NQ];
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) q[j] = off2 ? w[j + 1] : __funnelshift_r(w[j], w[j + 1], 16);
+    f32x2 yd[TB];
+#pragma unroll
+    for (int t = 0; t < TB; ++t) yd[t] = pack2(y[t] * d, y[t] * d);
+    if constexpr (WT == RG_Q8_0) {
+      const f32x2 nb = pack2(-(kTwo23 + 128.0f), -(kTwo23 + 128.0f));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t x = q[j] ^ 0x80808080u;  // int8 q -> byte q + 128
+        const f32x2 q01 = bytes2<0>(x, nb), q23 = bytes2<2>(x, nb);
+#pragma unroll
+        for (int t = 0; t < TB; ++t) {
+          acc[t][2 * j] = fma2(yd[t], q01, acc[t][2 * j]);
+          acc[t][2 * j + 1] = fma2(yd[t], q23, acc[t][2 * j + 1]);
+        }
+      }
+    } else {
+      const f32x2 nb = pack2(-(kTwo23 + 8.0f), -(kTwo23 + 8.0f));
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = q[j] & 0x0F0F0F0Fu, hi = (q[j] >> 4) & 0x0F0F0F0Fu;  // values 4j.., 16+4j..
+        const f32x2 l01 = bytes2<0>(lo, nb), l23 = bytes2<2>(lo, nb);
+        const f32x2 h01 = bytes2<0>(hi, nb), h23 = bytes2<2>(hi, nb);
+#pragma unroll
+        for (int t = 0; t < TB; ++t) {
+          acc[t][2 * j] = fma2(yd[t], l01, acc[t][2 * j]);
+          acc[t][2 * j + 1] = fma2(yd[t], l23, acc[t][2 * j + 1]);
+          acc[t][8 + 2 * j] = fma2(yd[t], h01, acc[t][8 + 2 * j]);
+          acc[t][9 + 2 * j] = fma2(yd[t], h23, acc[t][9 + 2 * j]);
+        }
+      }
+    }
+  } else {
+    // sub-block g = 2c + h: nibble h of bytes 32c .. 32c+31 of the quants
+    const int c = g >> 1, h = g & 1;
+    const uint4 hd = *reinterpret_cast<const uint4*>(row);
+    const uint4 qa = *reinterpret_cast<const uint4*>(row + 16 + 32 * c);
+    const uint4 qb = *reinterpret_cast<const uint4*>(row + 32 + 32 * c);
+    const float d = f16_to_f32(static_cast<uint16_t>(hd.x & 0xFFFFu));
+    const float dmin = f16_to_f32(static_cast<uint16_t>(hd.x >> 16));
+    // the 6-bit scale and min of sub-block g from header bytes 4..15
+    auto hb = [&](int i) {
+      const uint32_t wd = i < 4 ? hd.y : (i < 8 ? hd.z : hd.w);
+      return (wd >> (8 * (i & 3))) & 0xFFu;
+    };
+    uint32_t sc, m;
+    if (g < 4) {
+      sc = hb(g) & 63u;
+      m = hb(g + 4) & 63u;
+    } else {
+      sc = (hb(g + 4) & 15u) | ((hb(g - 4) >> 6) << 4);
+      m = (hb(g + 4) >> 4) | ((hb(g) >> 6) << 4);
+    }
+    const float ds = d * static_cast<float>(sc), dm = dmin * static_cast<float>(m);
+    const f32x2 nb = pack2(-kTwo23, -kTwo23);
+    f32x2 yd[TB];
+#pragma unroll
+    for (int t = 0; t < TB; ++t) {
+      yd[t] = pack2(y[t] * ds, y[t] * ds);
+      msum[t] = fmaf(y[t], dm, msum[t]);
+    }
+    const uint32_t qw[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t x = (qw[j] >> (4 * h)) & 0x0F0F0F0Fu;
+      const f32x2 q01 = bytes2<0>(x, nb), q23 = bytes2<2>(x, nb);
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        acc[t][2 * j] = fma2(yd[t], q01, acc[t][2 * j]);
+        acc[t][2 * j + 1] = fma2(yd[t], q23, acc[t][2 * j + 1]);
+      }
+    }
+  }
+}
+
+// The consumer warp of block g: every stage's rows (row = lane, then lane +
+// 32), then the butterfly over lanes and the block's partial sums to part.
+template <int WT, int TB, int TBYTES, int BR, int STAGES_>
+__device__ __forceinline__ void consume_rows(int g, const uint8_t* stage_buf, const float* ys,
+                                             uint32_t bar0,
+                                             int n_tiles, int nrows, int lane, int kt, int K,
+                                             int t0, int T, int split, float* part, WaitCtl ctl,
+                                             volatile int* abort_flag) {
+  f32x2 acc[TB][16];
+  float msum[TB];
+#pragma unroll
+  for (int t = 0; t < TB; ++t) {
+    msum[t] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[t][i] = 0ull;  // (+0.0f, +0.0f)
+  }
+  for (int i = 0; i < n_tiles; ++i) {
+    const int s = i % STAGES_;
+    if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * s, static_cast<uint32_t>(i / STAGES_) & 1u,
+                                           ctl, abort_flag)))
+      break;
+#pragma unroll 1
+    for (int u = 0; u < BR / 32; ++u) {
+      const int r = i * BR + 32 * u + lane;  // this lane's rows within the CTA's slice
+      if (r < nrows) {
+        float y[TB];
+#pragma unroll
+        for (int t = 0; t < TB; ++t) y[t] = ys[t * MAX_ROWS + r];
+        row_block<WT, TB>(stage_buf + (s * BR + 32 * u + lane) * TBYTES, g, y, acc, msum);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar0 + 8u * (STAGES_ + s));
+  }
+#pragma unroll
+  for (int t = 0; t < TB; ++t) {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      unpack2(acc[t][i], v[2 * i], v[2 * i + 1]);
+      if constexpr (WT == RG_Q4_K) {
+        v[2 * i] -= msum[t];
+        v[2 * i + 1] -= msum[t];
+      }
+    }
+    // reduce-scatter over the 32 lanes: afterwards lane l holds value l
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int j = 0; j < o; ++j) {
+        const float send = up ? v[j] : v[j + o];
+        const float keep = up ? v[j + o] : v[j];
+        v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+    const int gt = t0 + t, gk = kt * 256 + 32 * g + lane;
+    if (gt < T && gk < K) part[(static_cast<int64_t>(split) * T + gt) * K + gk] = v[0];
+  }
+}
 
 // grid (ceil(K/256), n_splits, ceil(T/TB)); partial sums of rows
 // [split * rows_per_split, +rows_per_split) to part[(split * T + t) * K + k].
 // A producer warp streams the CTA's rows of W, tile by tile of BR rows, into
 // an 8-stage ring with TMA; eight consumer warps decode from shared memory.
 template <int WT, int TB>
-__global__ void __launch_bounds__(THREADS + 32, TB >= 8 ? 1 : 2)
+__global__ void __launch_bounds__(THREADS + 32, rows_path<WT, TB>() && TB == 1 ? 3 : (TB >= 8 ? 1 : 2))
     smallt_kernel(const __grid_constant__ CUtensorMap map_w, int N, int K,
                   const float* __restrict__ dY, int T, float* __restrict__ part,
                   int rows_per_split, WaitCtl ctl) {
   constexpr int TBYTES = tile_bytes<WT>();
+  constexpr int BR = stage_rows<WT, TB>(), STAGES = n_stages<WT, TB>();
   extern __shared__ __align__(128) uint8_t sm[];
   uint8_t* stage_buf = sm;                                              // STAGES x BR x TBYTES
   float* ys = reinterpret_cast<float*>(sm + STAGES * BR * TBYTES);      // [TB][MAX_ROWS]
-  float* red = ys + TB * MAX_ROWS;                                      // [4][TB][256]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(red + 4 * TB * 256);    // full[S], empty[S]
+  float* red = ys + TB * MAX_ROWS;                                      // [4][TB][256] (8 values a lane)
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(red + (rows_path<WT, TB>() ? 0 : 4 * TB * 256));  // full[S], empty[S]
   __shared__ int abort_flag_s;
   volatile int* abort_flag = &abort_flag_s;
 
@@ -156,12 +373,16 @@ __global__ void __launch_bounds__(THREADS + 32, TB >= 8 ? 1 : 2)
     abort_flag_s = 0;
     fence_mbar_init();
   }
-  // this CTA's slice of dY, [TB][nrows]
-  for (int idx = threadIdx.x; idx < TB * MAX_ROWS; idx += THREADS + 32) {
-    const int t = idx / MAX_ROWS, r = idx - t * MAX_ROWS;
-    ys[idx] = (t0 + t < T && r < nrows) ? __ldg(dY + static_cast<int64_t>(t0 + t) * N + nbeg + r) : 0.0f;
-  }
   __syncthreads();
+  if (warp < CONSUMERS) {
+    // this CTA's slice of dY, [TB][nrows], staged by the consumers while the
+    // producer's first copies are in flight
+    for (int idx = threadIdx.x; idx < TB * MAX_ROWS; idx += THREADS) {
+      const int t = idx / MAX_ROWS, r = idx - t * MAX_ROWS;
+      ys[idx] = (t0 + t < T && r < nrows) ? __ldg(dY + static_cast<int64_t>(t0 + t) * N + nbeg + r) : 0.0f;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");  // the consumer warps only
+  }
 
   if (warp == CONSUMERS) {
     // ---------------- producer ----------------
@@ -183,6 +404,13 @@ __global__ void __launch_bounds__(THREADS + 32, TB >= 8 ? 1 : 2)
     __syncwarp();
   }
 
+  if constexpr (rows_path<WT, TB>()) {
+    // quantized, one and two rows of dY: a block per warp, a row per lane
+    if (warp < CONSUMERS)
+      consume_rows<WT, TB, TBYTES, BR, STAGES>(warp, stage_buf, ys, bar0, n_tiles, nrows, lane, kt,
+                                               K, t0, T, split, part, ctl, abort_flag);
+    return;
+  } else {
   float acc[TB][8];
 #pragma unroll
   for (int t = 0; t < TB; ++t)
@@ -245,12 +473,14 @@ __global__ void __launch_bounds__(THREADS + 32, TB >= 8 ? 1 : 2)
       part[(static_cast<int64_t>(split) * T + gt) * K + gk] = sum;
     }
   }
+  }
 }
 
 template <int WT, int TB>
 constexpr size_t smem_bytes() {
-  return static_cast<size_t>(STAGES) * BR * tile_bytes<WT>() + sizeof(float) * TB * MAX_ROWS +
-         sizeof(float) * 4 * TB * 256 + 16 * STAGES;
+  return static_cast<size_t>(n_stages<WT, TB>()) * stage_rows<WT, TB>() * tile_bytes<WT>() +
+         sizeof(float) * TB * MAX_ROWS + (rows_path<WT, TB>() ? 0 : sizeof(float) * 4 * TB * 256) +
+         16 * n_stages<WT, TB>();
 }
 
 // dX = beta * dX + sum over splits (in split order), four values per thread.
@@ -260,7 +490,19 @@ __global__ void __launch_bounds__(256) smallt_reduce(const float* __restrict__ p
   for (int64_t i = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) * 4; i < TK;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x * 4) {
     float4 s = *reinterpret_cast<const float4*>(part + i);
-    for (int p = 1; p < n_splits; ++p) {
+    int p = 1;
+    // eight loads in flight, then the adds in split order
+    for (; p + 8 <= n_splits; p += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = *reinterpret_cast<const float4*>(part + static_cast<int64_t>(p + u) * TK + i);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        s.x += v[u].x; s.y += v[u].y; s.z += v[u].z; s.w += v[u].w;
+      }
+    }
+    for (; p < n_splits; ++p) {
       const float4 v = *reinterpret_cast<const float4*>(part + static_cast<int64_t>(p) * TK + i);
       s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
     }
@@ -274,16 +516,93 @@ __global__ void __launch_bounds__(256) smallt_reduce(const float* __restrict__ p
   }
 }
 
+// The same sum for few outputs and many splits, where one thread per output
+// would wait out its loads one after another: a warp per four outputs, lane
+// p loading split p0 + p; each group of 32 splits is added by a fixed xor
+// tree and the groups in order.
+__global__ void __launch_bounds__(256) smallt_reduce_wide(const float* __restrict__ part,
+                                                          int n_splits, int64_t TK,
+                                                          float* __restrict__ dX, float beta) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t q = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; q * 4 < TK;
+       q += nw) {
+    const int64_t i = q * 4;
+    float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int p0 = 0; p0 < n_splits; p0 += 32) {
+      float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (p0 + lane < n_splits)
+        v = *reinterpret_cast<const float4*>(part + static_cast<int64_t>(p0 + lane) * TK + i);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+        v.z += __shfl_xor_sync(0xffffffffu, v.z, o);
+        v.w += __shfl_xor_sync(0xffffffffu, v.w, o);
+      }
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+    if (lane == 0) {
+      float4* o = reinterpret_cast<float4*>(dX + i);
+      if (beta != 0.0f) {
+        const float4 x = *o;
+        s.x = fmaf(beta, x.x, s.x); s.y = fmaf(beta, x.y, s.y);
+        s.z = fmaf(beta, x.z, s.z); s.w = fmaf(beta, x.w, s.w);
+      }
+      *o = s;
+    }
+  }
+}
+
 }  // namespace smt
 
-SmalltPlan plan_smallt(int64_t N, int64_t K, int64_t T, const DevInfo& dev) {
+// Resident CTAs per SM of smallt_kernel<WT, TB> on this device (queried once).
+template <int WT, int TB>
+static int smallt_residency(const DevInfo& dev) {
+  static int cache[64] = {0};
+  int& c = cache[dev.device & 63];
+  if (c == 0) {
+    auto kern = smt::smallt_kernel<WT, TB>;
+    constexpr size_t smem = smt::smem_bytes<WT, TB>();
+    int n = 0;
+    if (ensure_smem_attr(reinterpret_cast<const void*>(kern), static_cast<int>(smem)) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, smt::THREADS + 32, smem) != cudaSuccess ||
+        n <= 0)
+      n = 1;
+    c = n;
+  }
+  return c;
+}
+
+template <int WT>
+static int smallt_residency_tb(int tb, const DevInfo& dev) {
+  switch (tb) {
+    case 1: return smallt_residency<WT, 1>(dev);
+    case 2: return smallt_residency<WT, 2>(dev);
+    case 4: return smallt_residency<WT, 4>(dev);
+    default: return smallt_residency<WT, 8>(dev);
+  }
+}
+
+SmalltPlan plan_smallt(int wtype, int64_t N, int64_t K, int64_t T, const DevInfo& dev) {
   SmalltPlan p{};
   p.tb = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
   p.n_ktiles = static_cast<int>((K + 255) / 256);
   p.n_tchunks = static_cast<int>((T + p.tb - 1) / p.tb);
-  const int64_t target = static_cast<int64_t>(dev.num_sms) * 4;
-  int64_t splits = (target + p.n_ktiles * p.n_tchunks - 1) / (p.n_ktiles * p.n_tchunks);
-  splits = std::max<int64_t>(1, std::min<int64_t>(splits, (N + 63) / 64));
+  int per_sm = 1;
+  switch (wtype) {
+    case RG_F16: per_sm = smallt_residency_tb<RG_F16>(p.tb, dev); break;
+    case RG_BF16: per_sm = smallt_residency_tb<RG_BF16>(p.tb, dev); break;
+    case RG_Q8_0: per_sm = smallt_residency_tb<RG_Q8_0>(p.tb, dev); break;
+    case RG_Q4_0: per_sm = smallt_residency_tb<RG_Q4_0>(p.tb, dev); break;
+    default: per_sm = smallt_residency_tb<RG_Q4_K>(p.tb, dev); break;
+  }
+  // one wave of resident CTAs; rows split no finer than 64 per CTA and no
+  // coarser than the staged slice of dY allows
+  const int64_t capacity = static_cast<int64_t>(dev.num_sms) * per_sm;
+  const int64_t tiles = static_cast<int64_t>(p.n_ktiles) * p.n_tchunks;
+  int64_t splits = std::max<int64_t>(1, capacity / tiles);
+  splits = std::min<int64_t>(splits, (N + 63) / 64);
   splits = std::max<int64_t>(splits, (N + smt::MAX_ROWS - 1) / smt::MAX_ROWS);
   int64_t rows = (N + splits - 1) / splits;
   rows = (rows + 7) / 8 * 8;
@@ -294,13 +613,20 @@ SmalltPlan plan_smallt(int64_t N, int64_t K, int64_t T, const DevInfo& dev) {
 }
 
 template <int WT, int TB>
-static cudaError_t launch_smallt_t(const CUtensorMap& map, int64_t N, int64_t K, const float* dY,
+static cudaError_t launch_smallt_t(const void* W, int64_t N, int64_t K, const float* dY,
                                    int64_t T, float* part, const SmalltPlan& p, const DevInfo& dev,
                                    cudaStream_t stream) {
   auto kern = smt::smallt_kernel<WT, TB>;
   constexpr size_t smem = smt::smem_bytes<WT, TB>();
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  // W as rows of 32-bit words; one box = a stage of rows x one 256-value tile
+  const uint64_t rb = static_cast<uint64_t>(K / block_values(WT) * block_bytes(WT));
+  CUtensorMap map;
+  if (encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rb / 4, static_cast<uint64_t>(N), rb,
+                   smt::tile_bytes<WT>() / 4, smt::stage_rows<WT, TB>(),
+                   CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(p.n_ktiles), static_cast<unsigned>(p.n_splits),
                   static_cast<unsigned>(p.n_tchunks));
   WaitCtl ctl{dev.status, dev.wait_limit_ns};
@@ -313,17 +639,11 @@ template <int WT>
 static cudaError_t launch_smallt_w(const void* W, int64_t N, int64_t K, const float* dY,
                                    int64_t T, float* part, const SmalltPlan& p, const DevInfo& dev,
                                    cudaStream_t stream) {
-  // W as rows of 32-bit words; one box = BR rows x one 256-value tile
-  const uint64_t rb = static_cast<uint64_t>(K / block_values(WT) * block_bytes(WT));
-  CUtensorMap map;
-  if (encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rb / 4, static_cast<uint64_t>(N), rb,
-                   smt::tile_bytes<WT>() / 4, smt::BR, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
   switch (p.tb) {
-    case 1: return launch_smallt_t<WT, 1>(map, N, K, dY, T, part, p, dev, stream);
-    case 2: return launch_smallt_t<WT, 2>(map, N, K, dY, T, part, p, dev, stream);
-    case 4: return launch_smallt_t<WT, 4>(map, N, K, dY, T, part, p, dev, stream);
-    default: return launch_smallt_t<WT, 8>(map, N, K, dY, T, part, p, dev, stream);
+    case 1: return launch_smallt_t<WT, 1>(W, N, K, dY, T, part, p, dev, stream);
+    case 2: return launch_smallt_t<WT, 2>(W, N, K, dY, T, part, p, dev, stream);
+    case 4: return launch_smallt_t<WT, 4>(W, N, K, dY, T, part, p, dev, stream);
+    default: return launch_smallt_t<WT, 8>(W, N, K, dY, T, part, p, dev, stream);
   }
 }
 
@@ -346,7 +666,15 @@ cudaError_t launch_smallt(int wtype, const void* W, int64_t N, int64_t K, const 
 
 cudaError_t launch_reduce_partials(const float* part, int n_splits, int64_t TK, float* dX,
                                    float beta, const DevInfo& dev, cudaStream_t stream) {
-  const int64_t blocks = std::min<int64_t>((TK / 4 + 255) / 256, static_cast<int64_t>(dev.num_sms) * 8);
+  // latency regime (a warp per four outputs fits in one wave): the wide form
+  const int64_t quads = TK / 4;
+  if (n_splits >= 4 && quads * 32 <= static_cast<int64_t>(dev.num_sms) * 2048) {
+    const int64_t blocks = (quads * 32 + 255) / 256;
+    smt::smallt_reduce_wide<<<static_cast<unsigned>(std::max<int64_t>(1, blocks)), 256, 0, stream>>>(
+        part, n_splits, TK, dX, beta);
+    return counted(cudaGetLastError());
+  }
+  const int64_t blocks = std::min<int64_t>((quads + 255) / 256, static_cast<int64_t>(dev.num_sms) * 8);
   smt::smallt_reduce<<<static_cast<unsigned>(std::max<int64_t>(1, blocks)), 256, 0, stream>>>(
       part, n_splits, TK, dX, beta);
   return counted(cudaGetLastError());
