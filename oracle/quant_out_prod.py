@@ -31,6 +31,13 @@ Block formats (little-endian), ggml's GGUF block types:
                                                   y = d * (nib - 8)
 * Q4_K 144 B / 256: fp16 d, fp16 dmin, 12 B of 6-bit (sc, m) x 8, qs[128];
                                                   y = (d*sc)*q - dmin*m
+* Q4_1  20 B / 32: fp16 d, fp16 m, qs[16] (nibbles as Q4_0); y = d * nib + m
+* Q5_0  22 B / 32: fp16 d, qh (32-bit LE: bit i = fifth bit of value i),
+                   qs[16] (nibbles as Q4_0);      y = d * (q - 16)
+* Q5_1  24 B / 32: fp16 d, fp16 m, qh, qs[16];     y = d * q + m
+* Q5_K 176 B / 256: fp16 d, fp16 dmin, 12 B (sc, m) as Q4_K, qh[32], qs[128]:
+                   the nibbles of Q4_K plus bit 2c (low) / 2c+1 (high) of
+                   qh[l] as the fifth bit;        y = (d*sc)*q - dmin*m
 * F16 / BF16: 2 B per value.
 
 Parity pins for each function live in tests/test_oracle.py.
@@ -40,8 +47,10 @@ from __future__ import annotations
 import numpy as np
 
 F16, BF16, Q8_0, Q4_0, Q4_K = 1, 2, 3, 4, 5
+Q4_1, Q5_0, Q5_1, Q5_K = 6, 7, 8, 9
 
-_BLOCK = {F16: (1, 2), BF16: (1, 2), Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144)}
+_BLOCK = {F16: (1, 2), BF16: (1, 2), Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144),
+          Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q5_K: (256, 176)}
 
 
 def row_bytes(wtype: int, K: int) -> int:
@@ -158,6 +167,76 @@ def decode_q4_k(W, N: int, K: int) -> np.ndarray:
     return y.astype(np.float32).reshape(N, K)
 
 
+def _nibbles_32(qs: np.ndarray) -> np.ndarray:
+    """The 32 nibbles of a 32-value block's qs[16]: value j < 16 is the low
+    nibble of qs[j], value j + 16 the high nibble (int64)."""
+    qs = qs.astype(np.int64)
+    return np.concatenate([qs & 0x0F, qs >> 4], axis=-1)
+
+
+def _fifth_bits_32(qh4: np.ndarray) -> np.ndarray:
+    """Bit i (i = 0..31) of the little-endian 32-bit word in qh4[..., 0:4]:
+    the fifth bit of value i of a Q5_0 / Q5_1 block (int64)."""
+    qh4 = qh4.astype(np.int64)
+    word = qh4[..., 0] | (qh4[..., 1] << 8) | (qh4[..., 2] << 16) | (qh4[..., 3] << 24)
+    return (word[..., None] >> np.arange(32, dtype=np.int64)) & 1
+
+
+def decode_q4_1(W, N: int, K: int) -> np.ndarray:
+    """Q4_1: y = F32(d) * nib + F32(m); the product is exact (11-bit x 4-bit),
+    the sum rounds once."""
+    blk = _rows(W, N, K, Q4_1).reshape(N, K // 32, 20)
+    d = f16_bits_to_f32(_le16(blk[..., 0], blk[..., 1]))
+    m = f16_bits_to_f32(_le16(blk[..., 2], blk[..., 3]))
+    nib = _nibbles_32(blk[..., 4:20]).astype(np.float32)
+    return (d[..., None] * nib + m[..., None]).reshape(N, K)
+
+
+def decode_q5_0(W, N: int, K: int) -> np.ndarray:
+    """Q5_0: q = nibble + 16 * (bit i of qh) for value i; y = F32(d) * (q - 16),
+    exact (11-bit x 5-bit)."""
+    blk = _rows(W, N, K, Q5_0).reshape(N, K // 32, 22)
+    d = f16_bits_to_f32(_le16(blk[..., 0], blk[..., 1]))
+    q = _nibbles_32(blk[..., 6:22]) + 16 * _fifth_bits_32(blk[..., 2:6])
+    return (d[..., None] * (q - 16).astype(np.float32)).reshape(N, K)
+
+
+def decode_q5_1(W, N: int, K: int) -> np.ndarray:
+    """Q5_1: q = nibble + 16 * (bit i of qh); y = F32(d) * q + F32(m), the
+    product exact, the sum rounded once."""
+    blk = _rows(W, N, K, Q5_1).reshape(N, K // 32, 24)
+    d = f16_bits_to_f32(_le16(blk[..., 0], blk[..., 1]))
+    m = f16_bits_to_f32(_le16(blk[..., 2], blk[..., 3]))
+    q = _nibbles_32(blk[..., 8:24]) + 16 * _fifth_bits_32(blk[..., 4:8])
+    return (d[..., None] * q.astype(np.float32) + m[..., None]).reshape(N, K)
+
+
+def decode_q5_k(W, N: int, K: int) -> np.ndarray:
+    """Q5_K: the Q4_K layout plus qh[32].  For chunk c = 0..3 and l = 0..31,
+    value 64c+l is the low nibble of qs[32c+l] plus 16 * bit 2c of qh[l]
+    (sub-block 2c) and value 64c+32+l the high nibble plus 16 * bit 2c+1 of
+    qh[l] (sub-block 2c+1).  y = (F32(d) * sc) * q - F32(dmin) * m: both
+    products exact (at most 22 bits), one rounding in the subtraction."""
+    blk = _rows(W, N, K, Q5_K).reshape(N, K // 256, 176)
+    d = f16_bits_to_f32(_le16(blk[..., 0], blk[..., 1]))
+    dmin = f16_bits_to_f32(_le16(blk[..., 2], blk[..., 3]))
+    sc, mn = q4_k_scale_min(blk[..., 4:16])
+    qh = blk[..., 16:48].astype(np.int64)
+    qs = blk[..., 48:176].astype(np.int64)
+    q = np.empty(blk.shape[:-1] + (256,), dtype=np.float32)
+    sub = np.empty(256, dtype=np.int64)
+    for c in range(4):
+        ql = qs[..., 32 * c: 32 * c + 32]
+        q[..., 64 * c: 64 * c + 32] = (ql & 0x0F) + 16 * ((qh >> (2 * c)) & 1)
+        q[..., 64 * c + 32: 64 * c + 64] = (ql >> 4) + 16 * ((qh >> (2 * c + 1)) & 1)
+        sub[64 * c: 64 * c + 32] = 2 * c
+        sub[64 * c + 32: 64 * c + 64] = 2 * c + 1
+    dsc = d[..., None] * sc.astype(np.float32)       # exact
+    dmm = dmin[..., None] * mn.astype(np.float32)    # exact
+    y = dsc[..., sub] * q - dmm[..., sub]
+    return y.astype(np.float32).reshape(N, K)
+
+
 def decode_f16(W, N: int, K: int) -> np.ndarray:
     b = _rows(W, N, K, F16).reshape(N, K, 2)
     return f16_bits_to_f32(_le16(b[..., 0], b[..., 1]))
@@ -169,7 +248,8 @@ def decode_bf16(W, N: int, K: int) -> np.ndarray:
 
 
 _DECODERS = {F16: decode_f16, BF16: decode_bf16, Q8_0: decode_q8_0,
-             Q4_0: decode_q4_0, Q4_K: decode_q4_k}
+             Q4_0: decode_q4_0, Q4_K: decode_q4_k, Q4_1: decode_q4_1,
+             Q5_0: decode_q5_0, Q5_1: decode_q5_1, Q5_K: decode_q5_k}
 
 
 def dequant(wtype: int, W, N: int, K: int) -> np.ndarray:

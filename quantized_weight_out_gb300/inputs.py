@@ -22,6 +22,12 @@ Formats written (little-endian, the block layouts of ggml's GGUF types):
   nibble of byte j, value j+16 in the high nibble.
 * Q4_K 144 B / 256 values: fp16 ``d``, fp16 ``dmin``, 12 bytes of 6-bit
   (scale, min) pairs for 8 sub-blocks, 128 bytes of nibbles.
+* Q4_1  20 B / 32 values: fp16 ``d``, fp16 ``m``, 16 bytes of nibbles (as Q4_0).
+* Q5_0  22 B / 32 values: fp16 ``d``, 4 bytes ``qh`` (bit i of the
+  little-endian word = fifth bit of value i), 16 bytes of nibbles.
+* Q5_1  24 B / 32 values: fp16 ``d``, fp16 ``m``, ``qh``, 16 bytes of nibbles.
+* Q5_K 176 B / 256 values: the Q4_K header, 32 bytes ``qh`` (bit 2c / 2c+1 of
+  ``qh[l]`` = fifth bit of value 64c+l / 64c+32+l), 128 bytes of nibbles.
 * F16 / BF16: 2 B per value.
 
 The generator recipes follow the workload descriptions of the llama.cpp fork's
@@ -40,11 +46,15 @@ import numpy as np
 # ----------------------------------------------------------------------------
 # weight type codes (the C ABI uses the same integers)
 F16, BF16, Q8_0, Q4_0, Q4_K = 1, 2, 3, 4, 5
-TYPE_NAMES = {F16: "f16", BF16: "bf16", Q8_0: "q8_0", Q4_0: "q4_0", Q4_K: "q4_k"}
+Q4_1, Q5_0, Q5_1, Q5_K = 6, 7, 8, 9
+TYPE_NAMES = {F16: "f16", BF16: "bf16", Q8_0: "q8_0", Q4_0: "q4_0", Q4_K: "q4_k",
+              Q4_1: "q4_1", Q5_0: "q5_0", Q5_1: "q5_1", Q5_K: "q5_k"}
 NAME_TO_TYPE = {v: k for k, v in TYPE_NAMES.items()}
+ALL_TYPES = [Q8_0, Q4_0, Q4_K, F16, BF16, Q4_1, Q5_0, Q5_1, Q5_K]
 
 # (values per block, bytes per block)
-BLOCK = {F16: (1, 2), BF16: (1, 2), Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144)}
+BLOCK = {F16: (1, 2), BF16: (1, 2), Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144),
+         Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q5_K: (256, 176)}
 
 
 def row_bytes(wtype: int, K: int) -> int:
@@ -221,6 +231,73 @@ def pack_q4_k(d_bits, dmin_bits, sc, m, q) -> np.ndarray:
     return out
 
 
+def _pack_nibbles_32(q: np.ndarray) -> np.ndarray:
+    """[B, 32] values 0..15 -> [B, 16] bytes: value j < 16 in the low nibble
+    of byte j, value j + 16 in the high nibble."""
+    q = np.asarray(q, dtype=np.uint8)
+    return (q[:, :16] & 15) | ((q[:, 16:] & 15) << 4)
+
+
+def _pack_fifth_bits_32(q: np.ndarray) -> np.ndarray:
+    """[B, 32] values 0..31 -> [B, 4] bytes of the little-endian word whose
+    bit i is bit 4 of value i."""
+    hb = (np.asarray(q, dtype=np.uint64) >> np.uint64(4)) & np.uint64(1)
+    word = np.zeros(hb.shape[0], dtype=np.uint64)
+    for i in range(32):
+        word |= hb[:, i] << np.uint64(i)
+    return np.stack([((word >> np.uint64(8 * b)) & np.uint64(0xFF)).astype(np.uint8)
+                     for b in range(4)], axis=-1)
+
+
+def pack_q4_1(d_bits, m_bits, q) -> np.ndarray:
+    """Q4_1 blocks [B, 20] from fp16 d, fp16 m and values q [B, 32] in 0..15."""
+    B = len(d_bits)
+    out = np.empty((B, 20), dtype=np.uint8)
+    out[:, 0:2] = _f16_le(np.asarray(d_bits, dtype=np.uint16))
+    out[:, 2:4] = _f16_le(np.asarray(m_bits, dtype=np.uint16))
+    out[:, 4:20] = _pack_nibbles_32(q)
+    return out
+
+
+def pack_q5_0(d_bits, q) -> np.ndarray:
+    """Q5_0 blocks [B, 22] from fp16 d and values q [B, 32] in 0..31."""
+    B = len(d_bits)
+    out = np.empty((B, 22), dtype=np.uint8)
+    out[:, 0:2] = _f16_le(np.asarray(d_bits, dtype=np.uint16))
+    out[:, 2:6] = _pack_fifth_bits_32(q)
+    out[:, 6:22] = _pack_nibbles_32(np.asarray(q) & 15)
+    return out
+
+
+def pack_q5_1(d_bits, m_bits, q) -> np.ndarray:
+    """Q5_1 blocks [B, 24] from fp16 d, fp16 m and values q [B, 32] in 0..31."""
+    B = len(d_bits)
+    out = np.empty((B, 24), dtype=np.uint8)
+    out[:, 0:2] = _f16_le(np.asarray(d_bits, dtype=np.uint16))
+    out[:, 2:4] = _f16_le(np.asarray(m_bits, dtype=np.uint16))
+    out[:, 4:8] = _pack_fifth_bits_32(q)
+    out[:, 8:24] = _pack_nibbles_32(np.asarray(q) & 15)
+    return out
+
+
+def pack_q5_k(d_bits, dmin_bits, sc, m, q) -> np.ndarray:
+    """Q5_K super-blocks [B, 176]: the Q4_K packing of (d, dmin, sc, m) and of
+    the low nibbles of q [B, 256] (values 0..31), plus qh[32] whose bit 2c of
+    byte l is bit 4 of value 64c+l and bit 2c+1 that of value 64c+32+l."""
+    q = np.asarray(q, dtype=np.uint8)
+    k4 = pack_q4_k(d_bits, dmin_bits, sc, m, q & 15)
+    B = k4.shape[0]
+    qh = np.zeros((B, 32), dtype=np.uint8)
+    for c in range(4):
+        qh |= ((q[:, 64 * c: 64 * c + 32] >> 4) & 1) << (2 * c)
+        qh |= ((q[:, 64 * c + 32: 64 * c + 64] >> 4) & 1) << (2 * c + 1)
+    out = np.empty((B, 176), dtype=np.uint8)
+    out[:, 0:16] = k4[:, 0:16]
+    out[:, 16:48] = qh
+    out[:, 48:176] = k4[:, 16:144]
+    return out
+
+
 # ----------------------------------------------------------------------------
 # weights and activations for one call
 
@@ -236,6 +313,29 @@ def gen_weight(wtype: int, N: int, K: int, seed: int, stream: int) -> np.ndarray
         m = uniform_int(seed, stream, nb * 8, 64, field=4).reshape(nb, 8)
         q = uniform_int(seed, stream, nb * 256, 16, field=5).reshape(nb, 256)
         return pack_q4_k(f32_to_f16_bits(d), f32_to_f16_bits(dmin), sc, m, q).reshape(-1)
+    if wtype == Q5_K:
+        nb = N * K // 256
+        d = np.abs(normal_f32(seed, stream, nb, 1e-3, field=1))
+        dmin = np.abs(normal_f32(seed, stream, nb, 1e-3, field=2))
+        sc = uniform_int(seed, stream, nb * 8, 64, field=3).reshape(nb, 8)
+        m = uniform_int(seed, stream, nb * 8, 64, field=4).reshape(nb, 8)
+        q = uniform_int(seed, stream, nb * 256, 32, field=5).reshape(nb, 256)
+        return pack_q5_k(f32_to_f16_bits(d), f32_to_f16_bits(dmin), sc, m, q).reshape(-1)
+    if wtype in (Q4_1, Q5_0, Q5_1):
+        # fields drawn directly (the pages give no workload of these types):
+        # a block of N(0, 0.02) weights spans about 0.08, so d ~ 0.08 / levels
+        nb = N * K // 32
+        levels = 16 if wtype == Q4_1 else 32
+        dsig = 0.08 / (levels - 1)
+        q = uniform_int(seed, stream, nb * 32, levels, field=5).reshape(nb, 32)
+        if wtype == Q5_0:
+            d = normal_f32(seed, stream, nb, dsig, field=1)          # signed, like Q4_0's mx/-8
+            return pack_q5_0(f32_to_f16_bits(d), q).reshape(-1)
+        d = np.abs(normal_f32(seed, stream, nb, dsig, field=1))
+        m = normal_f32(seed, stream, nb, 0.04, field=2)
+        if wtype == Q4_1:
+            return pack_q4_1(f32_to_f16_bits(d), f32_to_f16_bits(m), q).reshape(-1)
+        return pack_q5_1(f32_to_f16_bits(d), f32_to_f16_bits(m), q).reshape(-1)
     x = normal_f32(seed, stream, N * K, 0.02)
     if wtype == Q8_0:
         return quantize_q8_0(x, N, K)

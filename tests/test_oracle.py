@@ -96,6 +96,53 @@ def test_q4_k_hand_superblock(golden_dir):
     assert math.fsum(float(x) for x in y) == float(kv["sum"][0])
 
 
+@pytest.mark.parametrize("name,decode,zeros", [
+    ("q4_1_block.txt", oracle.decode_q4_1, [2, 29]),
+    ("q5_0_block.txt", oracle.decode_q5_0, [0, 31]),
+    ("q5_1_block.txt", oracle.decode_q5_1, [19]),
+])
+def test_32_value_hand_blocks(golden_dir, name, decode, zeros):
+    rows = dict((r[0], r[1:]) for r in _read(golden_dir, name))
+    W = np.frombuffer(bytes.fromhex(rows["hex"][0]), dtype=np.uint8)
+    want = np.array([float(v) for v in rows["values"]], dtype=np.float32)
+    got = decode(W, 1, 32)[0]
+    assert _bits_equal(got, want)      # bitwise, signed zeros included
+    for i in zeros:
+        assert got[i] == 0.0 and np.signbit(got[i]) == np.signbit(want[i])
+
+
+def _q5_k_fixture(golden_dir):
+    rows = _read(golden_dir, "q5_k_superblock.txt")
+    kv, ats, rng = {}, [], None
+    for r in rows:
+        if r[0] == "at":
+            ats.append((int(r[1]), float(r[2])))
+        elif r[0] == "range":
+            rng = (int(r[1]), int(r[2]), float(r[3]))
+        else:
+            kv[r[0]] = r[1:]
+    blk = bytearray(176)
+    blk[0:2] = int(kv["d"][0], 16).to_bytes(2, "little")
+    blk[2:4] = int(kv["dmin"][0], 16).to_bytes(2, "little")
+    blk[4:16] = bytes.fromhex(kv["scales"][0])
+    for l in range(32):
+        blk[16 + l] = 0x55 if l % 2 == 0 else 0xAA
+    for c in range(4):
+        for l in range(32):
+            blk[48 + 32 * c + l] = (l % 16) | (((l + c) % 16) << 4)
+    return np.frombuffer(bytes(blk), dtype=np.uint8), kv, ats, rng
+
+
+def test_q5_k_hand_superblock(golden_dir):
+    W, kv, ats, rng = _q5_k_fixture(golden_dir)
+    y = oracle.decode_q5_k(W, 1, 256)[0]
+    for i, v in ats:
+        assert y[i] == np.float32(v), (i, y[i], v)
+    lo, hi, v = rng
+    assert np.all(y[lo:hi] == np.float32(v))
+    assert math.fsum(float(x) for x in y) == float(kv["sum"][0])
+
+
 def test_half_codes_hand_decoded(golden_dir):
     for kind, code, val in _read(golden_dir, "half_codes.txt"):
         bits = np.array([int(code, 16)], dtype=np.uint16)
@@ -147,6 +194,28 @@ def _all_ones_weight(wtype, N, K, variant=0):
             S = bytes([1, 1, 1, 1, 1, 1, 1, 1, 0x11, 0x11, 0x11, 0x11])
             blk = bytes([0x00, 0x3C, 0x00, 0x3C]) + S + bytes([0x22]) * 128
         return np.frombuffer(blk * (N * K // 256), dtype=np.uint8)
+    if wtype == inputs.Q4_1:     # d = 1, m = 0, nibble 1
+        blk = bytes([0x00, 0x3C, 0x00, 0x00]) + bytes([0x11]) * 16
+        return np.frombuffer(blk * (N * K // 32), dtype=np.uint8)
+    if wtype == inputs.Q5_0:     # d = 1, q = 17 (nibble 1, fifth bit set): 17 - 16 = 1
+        blk = bytes([0x00, 0x3C]) + bytes([0xFF]) * 4 + bytes([0x11]) * 16
+        return np.frombuffer(blk * (N * K // 32), dtype=np.uint8)
+    if wtype == inputs.Q5_1:
+        if variant == 0:         # d = 1, m = 0, q = 1
+            blk = bytes([0x00, 0x3C, 0x00, 0x00]) + bytes(4) + bytes([0x11]) * 16
+        else:                    # d = 0.5, m = -7, q = 16 (fifth bit only): 8 - 7 = 1
+            blk = bytes([0x00, 0x38, 0x00, 0xC7]) + bytes([0xFF]) * 4 + bytes(16)
+        return np.frombuffer(blk * (N * K // 32), dtype=np.uint8)
+    if wtype == inputs.Q5_K:
+        if variant == 0:         # d = 1, sc = 1, q = 1 (nibble only), dmin = 0
+            S = bytes([1, 1, 1, 1, 0, 0, 0, 0, 1, 1, 1, 1])
+            blk = bytes([0x00, 0x3C, 0x00, 0x00]) + S + bytes(32) + bytes([0x11]) * 128
+        else:                    # d = 1, sc = 1, q = 17 (fifth bit), dmin = 1, m = 16: 17 - 16
+            # m = 16 = 0b010000: sub-blocks 0..3 keep it in S[4..7] & 63; 4..7 take
+            # their low nibble (0) from S[8..11] >> 4 and their top bits (01) from S[4..7] >> 6
+            S = bytes([1, 1, 1, 1, 0x50, 0x50, 0x50, 0x50, 0x01, 0x01, 0x01, 0x01])
+            blk = bytes([0x00, 0x3C, 0x00, 0x3C]) + S + bytes([0xFF]) * 32 + bytes([0x11]) * 128
+        return np.frombuffer(blk * (N * K // 256), dtype=np.uint8)
     if wtype == inputs.F16:
         return np.frombuffer(bytes([0x00, 0x3C]) * (N * K), dtype=np.uint8)
     if wtype == inputs.BF16:
@@ -155,7 +224,8 @@ def _all_ones_weight(wtype, N, K, variant=0):
 
 
 CASES = [(inputs.Q8_0, 0), (inputs.Q4_0, 0), (inputs.Q4_K, 0), (inputs.Q4_K, 1),
-         (inputs.F16, 0), (inputs.BF16, 0)]
+         (inputs.F16, 0), (inputs.BF16, 0), (inputs.Q4_1, 0), (inputs.Q5_0, 0),
+         (inputs.Q5_1, 0), (inputs.Q5_1, 1), (inputs.Q5_K, 0), (inputs.Q5_K, 1)]
 
 
 @pytest.mark.parametrize("wtype,variant", CASES)
@@ -169,7 +239,7 @@ def test_all_ones_times_one_hot(wtype, variant):
     assert np.all(oracle.out_prod(wtype, W, N, K, dY, T) == 1.0)
 
 
-@pytest.mark.parametrize("wtype", [inputs.Q8_0, inputs.Q4_0, inputs.Q4_K, inputs.F16, inputs.BF16])
+@pytest.mark.parametrize("wtype", inputs.ALL_TYPES)
 def test_one_hot_selects_rows(wtype):
     """One-hot dY[t] = e_{n0(t)} gives dX[t, :] = deq(W)[n0(t), :] exactly:
     the contraction runs over the rows of W, not its columns."""
@@ -185,9 +255,11 @@ def test_one_hot_selects_rows(wtype):
         assert np.array_equal(ref[t], Wd[n0[t]].astype(np.float64))
 
 
-def test_q4_k_min_path_closed_form():
+@pytest.mark.parametrize("wtype", [inputs.Q4_K, inputs.Q5_K])
+def test_k_quant_min_path_closed_form(wtype):
     """q = 0 everywhere: dX[t, k] = -sum_n dY[t, n] * dmin_n * m_{n, k // 32}."""
     N, K, T = 20, 512, 3
+    pack = inputs.pack_q4_k if wtype == inputs.Q4_K else inputs.pack_q5_k
     nb = N * K // 256
     rng = np.random.default_rng(3)
     d = inputs.f32_to_f16_bits(np.abs(rng.normal(0, 1e-2, nb)).astype(np.float32))
@@ -195,7 +267,7 @@ def test_q4_k_min_path_closed_form():
     dmin = inputs.f32_to_f16_bits(dmin_f)
     sc = rng.integers(0, 64, (nb, 8))
     m = rng.integers(0, 64, (nb, 8))
-    W = inputs.pack_q4_k(d, dmin, sc, m, np.zeros((nb, 256), dtype=np.int64)).reshape(-1)
+    W = pack(d, dmin, sc, m, np.zeros((nb, 256), dtype=np.int64)).reshape(-1)
     dY = rng.normal(0, 1, (T, N)).astype(np.float32)
     dmin_exact = dmin.view(np.float16).astype(np.float64).reshape(N, K // 256)
     m_r = m.reshape(N, K // 256, 8)
@@ -205,7 +277,7 @@ def test_q4_k_min_path_closed_form():
             b, j = divmod(k // 32, 8)
             want[t, k] = -math.fsum(float(dY[t, n]) * float(dmin_exact[n, b]) * int(m_r[n, b, j])
                                     for n in range(N))
-    got = oracle.out_prod(inputs.Q4_K, W, N, K, dY, T)
+    got = oracle.out_prod(wtype, W, N, K, dY, T)
     assert np.allclose(got, want, rtol=1e-12, atol=1e-15)
 
 
@@ -262,11 +334,48 @@ def _py_decode(wtype, raw, N, K):
                         # F32 evaluation: both products exact, one rounding
                         v = np.float32(np.float32(d * sc) * q) - np.float32(dmin * m)
                         out[n][256 * b + 64 * c + 32 * half + l] = float(v)
+        elif wtype in (inputs.Q4_1, inputs.Q5_0, inputs.Q5_1):
+            bb = {inputs.Q4_1: 20, inputs.Q5_0: 22, inputs.Q5_1: 24}[wtype]
+            for b in range(K // 32):
+                blk = row[bb * b: bb * b + bb]
+                d = _py_f16(blk[0], blk[1])
+                m = _py_f16(blk[2], blk[3]) if wtype != inputs.Q5_0 else 0.0
+                qh_at = {inputs.Q4_1: None, inputs.Q5_0: 2, inputs.Q5_1: 4}[wtype]
+                qs_at = {inputs.Q4_1: 4, inputs.Q5_0: 6, inputs.Q5_1: 8}[wtype]
+                qh = int.from_bytes(bytes(blk[qh_at:qh_at + 4]), "little") if qh_at else 0
+                for i in range(32):
+                    byte = blk[qs_at + (i % 16)]
+                    q = (byte & 15) if i < 16 else (byte >> 4)
+                    q += 16 * ((qh >> i) & 1)
+                    if wtype == inputs.Q5_0:
+                        out[n][32 * b + i] = d * (q - 16)
+                    else:   # F32 evaluation: exact product, one rounding in the sum
+                        out[n][32 * b + i] = float(np.float32(np.float32(d * q) + np.float32(m)))
+        elif wtype == inputs.Q5_K:
+            for b in range(K // 256):
+                blk = row[176 * b: 176 * b + 176]
+                d = _py_f16(blk[0], blk[1])
+                dmin = _py_f16(blk[2], blk[3])
+                S = blk[4:16]
+                for j in range(8):
+                    if j < 4:
+                        sc, m = S[j] & 63, S[j + 4] & 63
+                    else:
+                        sc = (S[j + 4] & 15) | ((S[j - 4] >> 6) << 4)
+                        m = (S[j + 4] >> 4) | ((S[j] >> 6) << 4)
+                    c, half = divmod(j, 2)
+                    for l in range(32):
+                        byte = blk[48 + 32 * c + l]
+                        q = ((byte >> 4) if half else (byte & 15)) + 16 * ((blk[16 + l] >> j) & 1)
+                        v = np.float32(np.float32(d * sc) * q) - np.float32(dmin * m)
+                        out[n][256 * b + 64 * c + 32 * half + l] = float(v)
     return out
 
 
 BRUTE = [(inputs.Q8_0, 40, 64, 3), (inputs.Q4_0, 33, 96, 2), (inputs.Q4_K, 12, 512, 2),
-         (inputs.F16, 24, 40, 3), (inputs.BF16, 24, 40, 3), (inputs.Q8_0, 7, 32, 1)]
+         (inputs.F16, 24, 40, 3), (inputs.BF16, 24, 40, 3), (inputs.Q8_0, 7, 32, 1),
+         (inputs.Q4_1, 21, 64, 2), (inputs.Q5_0, 19, 96, 2), (inputs.Q5_1, 17, 64, 2),
+         (inputs.Q5_K, 10, 512, 2)]
 
 
 @pytest.mark.parametrize("wtype,N,K,T", BRUTE)
@@ -340,6 +449,9 @@ def test_sizes():
     assert 256 * 272 == 69_632 and 4096 * 2304 == 9_437_184
     assert 14336 * 2304 == 33_030_144 and 5120 * 34816 == 178_257_920
     assert oracle.row_bytes(oracle.Q4_K, 300) == 0 and oracle.row_bytes(oracle.Q8_0, 48) == 0
+    # 20 B / 32, 22 B / 32, 24 B / 32, 176 B / 256
+    assert oracle.row_bytes(oracle.Q4_1, 4096) == 2560 and oracle.row_bytes(oracle.Q5_0, 4096) == 2816
+    assert oracle.row_bytes(oracle.Q5_1, 4096) == 3072 and oracle.row_bytes(oracle.Q5_K, 4096) == 2816
 
 
 def test_q4_k_pack_roundtrip_through_oracle():
@@ -383,6 +495,47 @@ def _mut_q4_k_wrong_high_bits(W, N, K):
         return qop.decode_q4_k(W, N, K)
     finally:
         qop.q4_k_scale_min = real
+
+
+def _mut_q5_0_high_bits_from_low_half(W, N, K):
+    """Values j + 16 take bit j of qh instead of bit j + 16."""
+    blk = qop._rows(W, N, K, qop.Q5_0).reshape(N, K // 32, 22)
+    d = qop.f16_bits_to_f32(qop._le16(blk[..., 0], blk[..., 1]))
+    bits = qop._fifth_bits_32(blk[..., 2:6])
+    bits = np.concatenate([bits[..., :16], bits[..., :16]], axis=-1)
+    q = qop._nibbles_32(blk[..., 6:22]) + 16 * bits
+    return (d[..., None] * (q - 16).astype(np.float32)).reshape(N, K)
+
+
+def _mut_q5_1_min_subtracted(W, N, K):
+    blk = qop._rows(W, N, K, qop.Q5_1).reshape(N, K // 32, 24)
+    d = qop.f16_bits_to_f32(qop._le16(blk[..., 0], blk[..., 1]))
+    m = qop.f16_bits_to_f32(qop._le16(blk[..., 2], blk[..., 3]))
+    q = qop._nibbles_32(blk[..., 8:24]) + 16 * qop._fifth_bits_32(blk[..., 4:8])
+    return (d[..., None] * q.astype(np.float32) - m[..., None]).reshape(N, K)
+
+
+def _mut_q5_k_swapped_qh_bits(W, N, K):
+    """The low-nibble half takes bit 2c+1 and the high half bit 2c."""
+    blk = np.array(qop._rows(W, N, K, qop.Q5_K).reshape(N, K // 256, 176))
+    qh = blk[..., 16:48].astype(np.int64)
+    swapped = ((qh & 0x55) << 1) | ((qh & 0xAA) >> 1)
+    blk[..., 16:48] = swapped.astype(np.uint8)
+    return qop.decode_q5_k(blk.reshape(-1), N, K)
+
+
+def test_new_type_mutants_are_caught(golden_dir):
+    rows = dict((r[0], r[1:]) for r in _read(golden_dir, "q5_0_block.txt"))
+    W = np.frombuffer(bytes.fromhex(rows["hex"][0]), dtype=np.uint8)
+    want = np.array([float(v) for v in rows["values"]], dtype=np.float32)
+    assert not _bits_equal(_mut_q5_0_high_bits_from_low_half(W, 1, 32)[0], want)
+    rows = dict((r[0], r[1:]) for r in _read(golden_dir, "q5_1_block.txt"))
+    W = np.frombuffer(bytes.fromhex(rows["hex"][0]), dtype=np.uint8)
+    want = np.array([float(v) for v in rows["values"]], dtype=np.float32)
+    assert not _bits_equal(_mut_q5_1_min_subtracted(W, 1, 32)[0], want)
+    Wk, kv, ats, rng = _q5_k_fixture(golden_dir)
+    yk = _mut_q5_k_swapped_qh_bits(Wk, 1, 256)[0]
+    assert any(yk[i] != np.float32(v) for i, v in ats)
 
 
 def test_mutants_are_caught(golden_dir):
