@@ -173,23 +173,35 @@ def second_reference(torch, rg, problems, devbuf, stream, dev, flush_buf, reps: 
                 else:
                     torch.mm(dY, w, out=dX)
 
-        times = []
+        def dequant_only():
+            for i, p in enumerate(problems):
+                w = wf[:p.N * p.K].view(p.N, p.K)
+                rg.check(rg.rg_dequant_async(p.wtype, devbuf[i][0], p.N, p.K, w, stream),
+                         "rg_dequant_async")
+
+        times, dq = [], []
         for r in range(2 + reps):
-            if flush_buf is not None:
-                flush_buf.fill_(0.0)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            one()
-            b.record(stream)
-            torch.cuda.synchronize()
-            if r >= 2:
-                times.append(a.elapsed_time(b))
+            for fn, out in ((one, times), (dequant_only, dq)):
+                if flush_buf is not None:
+                    flush_buf.fill_(0.0)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                if r >= 2:
+                    out.append(a.elapsed_time(b))
     finally:
         torch.backends.cuda.matmul.allow_tf32 = tf32
+    dq_ms = statistics.median(dq)
+    dq_bytes = sum(inputs.row_bytes(p.wtype, p.K) * p.N + 4 * p.N * p.K for p in problems)
     return {"ms_per_step": statistics.median(times), "unit": "TFLOP/s", "reps": reps,
             "what": "rg_dequant to a dense F32 copy of W, then cuBLAS SGEMM with TF32 off "
                     "(median of the reps)",
-            "extra_bytes_per_step": sum(8 * p.N * p.K for p in problems)}
+            "extra_bytes_per_step": sum(8 * p.N * p.K for p in problems),
+            "dequant": {"ms_per_step": dq_ms, "bytes_per_step": dq_bytes,
+                        "gbs": dq_bytes / (dq_ms * 1e-3) / 1e9,
+                        "what": "rg_dequant alone (bytes(W) read + 4*N*K written)"}}
 
 
 def parse():

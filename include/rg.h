@@ -54,8 +54,17 @@ typedef enum {
     RG_Q8_0 = 3,  /* 34 B / 32 values: fp16 d, int8 q[32]; value d*q                 */
     RG_Q4_0 = 4,  /* 18 B / 32 values: fp16 d, 16 B nibbles (lo = j, hi = j+16);
                      value d*(q-8)                                                   */
-    RG_Q4_K = 5   /* 144 B / 256 values: fp16 d, fp16 dmin, 12 B of 6-bit (sc, m)
+    RG_Q4_K = 5,  /* 144 B / 256 values: fp16 d, fp16 dmin, 12 B of 6-bit (sc, m)
                      for 8 sub-blocks of 32, 128 B nibbles; value d*sc*q - dmin*m    */
+    RG_Q4_1 = 6,  /* 20 B / 32 values: fp16 d, fp16 m, 16 B nibbles as Q4_0;
+                     value d*q + m                                                   */
+    RG_Q5_0 = 7,  /* 22 B / 32 values: fp16 d, 4 B qh (bit i of the little-endian
+                     word = fifth bit of value i), 16 B nibbles; value d*(q-16)      */
+    RG_Q5_1 = 8,  /* 24 B / 32 values: fp16 d, fp16 m, 4 B qh, 16 B nibbles;
+                     value d*q + m                                                   */
+    RG_Q5_K = 9   /* 176 B / 256 values: the Q4_K header, 32 B qh (bit 2c / 2c+1 of
+                     qh[l] = fifth bit of value 64c+l / 64c+32+l), 128 B nibbles;
+                     value d*sc*q - dmin*m                                           */
 } rg_wtype;
 
 typedef enum {

@@ -88,7 +88,7 @@ int current_dev(DevInfo** out) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int64_t row_bytes_i(int wtype, int64_t K) {
-  if (wtype < RG_F16 || wtype > RG_Q4_K || K < 0) return 0;
+  if (!valid_wtype(wtype) || K < 0) return 0;
   const int bv = block_values(wtype);
   if (K % bv) return 0;
   return K / bv * block_bytes(wtype);
@@ -99,7 +99,7 @@ int64_t row_bytes_i(int wtype, int64_t K) {
 int validate(int wtype, const void* W, int64_t N, int64_t K, const float* dY, int64_t T,
              const float* dX, bool* empty) {
   *empty = false;
-  if (wtype < RG_F16 || wtype > RG_Q4_K) return RG_ERR_TYPE;
+  if (!valid_wtype(wtype)) return RG_ERR_TYPE;
   if (N < 0 || K < 0 || T < 0 || N > kMaxDim || K > kMaxDim || T > kMaxDim) return RG_ERR_ARG;
   const int64_t kmul = is_quant(wtype) ? 256 : 8;
   if (K % kmul) return RG_ERR_SHAPE;
@@ -431,7 +431,7 @@ int rg_select_variant(int wtype, int64_t N, int64_t K, int64_t T) {
 
 int rg_plan(int variant, int wtype, int64_t N, int64_t K, int64_t T, rg_plan_info* out) {
   if (!out) return RG_ERR_ARG;
-  if (wtype < RG_F16 || wtype > RG_Q4_K) return RG_ERR_TYPE;
+  if (!valid_wtype(wtype)) return RG_ERR_TYPE;
   if (variant < RG_VARIANT_AUTO || variant > RG_VARIANT_TC_PAIR) return RG_ERR_TYPE;
   if (N < 0 || K < 0 || T < 0 || N > kMaxDim || K > kMaxDim || T > kMaxDim) return RG_ERR_ARG;
   if (K % (is_quant(wtype) ? 256 : 8)) return RG_ERR_SHAPE;
@@ -478,7 +478,7 @@ int rg_plan(int variant, int wtype, int64_t N, int64_t K, int64_t T, rg_plan_inf
 uint64_t rg_launch_count(void) { return g_launch_count.load(std::memory_order_relaxed); }
 
 int rg_dequant_async(int wtype, const void* W, int64_t N, int64_t K, float* out, void* stream) {
-  if (wtype < RG_F16 || wtype > RG_Q4_K) return RG_ERR_TYPE;
+  if (!valid_wtype(wtype)) return RG_ERR_TYPE;
   if (N < 0 || K < 0 || N > kMaxDim || K > kMaxDim) return RG_ERR_ARG;
   const int64_t kmul = is_quant(wtype) ? 256 : 8;
   if (K % kmul) return RG_ERR_SHAPE;

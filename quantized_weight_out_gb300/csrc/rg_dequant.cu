@@ -43,15 +43,10 @@ cudaError_t launch_dequant(int wtype, const void* W, int64_t N, int64_t K, float
   const int64_t rb = K / block_values(wtype) * block_bytes(wtype);
   const int grid = grid_for(N * (K >> 3), 256, dev);
   const uint8_t* w = static_cast<const uint8_t*>(W);
-  switch (wtype) {
-    case RG_F16: dequant_kernel<RG_F16><<<grid, 256, 0, stream>>>(w, N, K, rb, out); break;
-    case RG_BF16: dequant_kernel<RG_BF16><<<grid, 256, 0, stream>>>(w, N, K, rb, out); break;
-    case RG_Q8_0: dequant_kernel<RG_Q8_0><<<grid, 256, 0, stream>>>(w, N, K, rb, out); break;
-    case RG_Q4_0: dequant_kernel<RG_Q4_0><<<grid, 256, 0, stream>>>(w, N, K, rb, out); break;
-    case RG_Q4_K: dequant_kernel<RG_Q4_K><<<grid, 256, 0, stream>>>(w, N, K, rb, out); break;
-    default: return cudaErrorInvalidValue;
-  }
-  return counted(cudaGetLastError());
+  return with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
+    dequant_kernel<decltype(wt)::value><<<grid, 256, 0, stream>>>(w, N, K, rb, out);
+    return counted(cudaGetLastError());
+  });
 }
 
 // dY [T, N] F32 -> [T, ld] 16-bit, round to nearest even.  One thread per 8

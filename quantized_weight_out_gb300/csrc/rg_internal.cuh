@@ -19,14 +19,22 @@ namespace rg {
 // ---------------------------------------------------------------------------
 // storage formats: values per block, bytes per block
 
+__host__ __device__ constexpr bool valid_wtype(int wt) { return wt >= RG_F16 && wt <= RG_Q5_K; }
+__host__ __device__ constexpr bool is_quant(int wt) {
+  return valid_wtype(wt) && wt != RG_F16 && wt != RG_BF16;
+}
 __host__ __device__ constexpr int block_values(int wt) {
-  return wt == RG_Q4_K ? 256 : (wt == RG_Q8_0 || wt == RG_Q4_0) ? 32 : 1;
+  return (wt == RG_Q4_K || wt == RG_Q5_K) ? 256 : is_quant(wt) ? 32 : 1;
 }
 __host__ __device__ constexpr int block_bytes(int wt) {
-  return wt == RG_Q4_K ? 144 : wt == RG_Q8_0 ? 34 : wt == RG_Q4_0 ? 18 : 2;
-}
-__host__ __device__ constexpr bool is_quant(int wt) {
-  return wt == RG_Q8_0 || wt == RG_Q4_0 || wt == RG_Q4_K;
+  return wt == RG_Q4_K   ? 144
+         : wt == RG_Q5_K ? 176
+         : wt == RG_Q8_0 ? 34
+         : wt == RG_Q4_0 ? 18
+         : wt == RG_Q4_1 ? 20
+         : wt == RG_Q5_0 ? 22
+         : wt == RG_Q5_1 ? 24
+                         : 2;
 }
 
 // Everything a kernel needs to report a wait that gave up.
@@ -70,6 +78,14 @@ __device__ __forceinline__ float byte_minus(uint32_t x, float two23_plus_bias) {
   return __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7440u | B)) - two23_plus_bias;
 }
 constexpr float kTwo23 = 8388608.0f;  // 2^23
+
+// Bit i (i = 0..3) of v -> bit 4 of byte i: the fifth bits of four
+// consecutive Q5 values, ready to OR onto their nibbles.  The multiply by
+// 1 + 2^7 + 2^14 + 2^21 places copies of v at bits 0, 7, 14, 21 (no carries
+// between them), so bit 8i of the product is bit i of v.
+__device__ __forceinline__ uint32_t fifth_bits4(uint32_t v) {
+  return (((v & 15u) * 0x00204081u) & 0x01010101u) << 4;
+}
 
 // ---------------------------------------------------------------------------
 // mbarrier
@@ -391,6 +407,47 @@ __device__ __forceinline__ void decode8_f32(const uint8_t* row, int k0, float (&
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int q = half ? (qs[i] >> 4) : (qs[i] & 15);
+      out[i] = ds * static_cast<float>(q) - dm;
+    }
+  } else if constexpr (WT == RG_Q4_1 || WT == RG_Q5_0 || WT == RG_Q5_1) {
+    // 32-value blocks: d (and m), the fifth bits (Q5), 16 bytes of nibbles
+    constexpr int BB = block_bytes(WT);
+    constexpr int QS = WT == RG_Q4_1 ? 4 : WT == RG_Q5_0 ? 6 : 8;
+    const uint8_t* blk = row + (k0 >> 5) * BB;
+    const float d = f16_to_f32(ld_u16(blk));
+    const int j = k0 & 31;  // 0, 8, 16 or 24
+    const uint8_t* qs = blk + QS + (j & 15);
+    const int shift = j >= 16 ? 4 : 0;
+    uint32_t qh = 0;
+    if constexpr (WT != RG_Q4_1) {
+      constexpr int QH = WT == RG_Q5_0 ? 2 : 4;
+      qh = static_cast<uint32_t>(ld_u16(blk + QH)) | (static_cast<uint32_t>(ld_u16(blk + QH + 2)) << 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int q = ((qs[i] >> shift) & 15) | (static_cast<int>((qh >> (j + i)) & 1u) << 4);
+      if constexpr (WT == RG_Q5_0) {
+        out[i] = d * static_cast<float>(q - 16);  // exact
+      } else {
+        // exact product, one rounding of the sum
+        out[i] = fmaf(d, static_cast<float>(q), f16_to_f32(ld_u16(blk + 2)));
+      }
+    }
+  } else if constexpr (WT == RG_Q5_K) {
+    const uint8_t* blk = row + (k0 >> 8) * 176;
+    const float d = f16_to_f32(ld_u16(blk));
+    const float dmin = f16_to_f32(ld_u16(blk + 2));
+    const int e = k0 & 255;
+    const int c = e >> 6, half = (e >> 5) & 1, l0 = e & 31;
+    int sc, m;
+    q4k_scale_min(blk + 4, 2 * c + half, sc, m);
+    const float ds = d * static_cast<float>(sc);
+    const float dm = dmin * static_cast<float>(m);
+    const uint8_t* qh = blk + 16 + l0;
+    const uint8_t* qs = blk + 48 + 32 * c + l0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int q = (half ? (qs[i] >> 4) : (qs[i] & 15)) + 16 * ((qh[i] >> (2 * c + half)) & 1);
       out[i] = ds * static_cast<float>(q) - dm;
     }
   }

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "../../include/rg.h"
 
@@ -29,6 +30,24 @@ extern std::atomic<unsigned long long> g_launch_count;
 inline cudaError_t counted(cudaError_t e) {
   if (e == cudaSuccess) g_launch_count.fetch_add(1, std::memory_order_relaxed);
   return e;
+}
+
+// f(std::integral_constant<int, WT>{}) for the run-time weight type wtype;
+// `fallback` for a type the library does not know (callers validate first).
+template <class R, class F>
+R with_wtype(int wtype, R fallback, F&& f) {
+  switch (wtype) {
+    case RG_F16: return f(std::integral_constant<int, RG_F16>{});
+    case RG_BF16: return f(std::integral_constant<int, RG_BF16>{});
+    case RG_Q8_0: return f(std::integral_constant<int, RG_Q8_0>{});
+    case RG_Q4_0: return f(std::integral_constant<int, RG_Q4_0>{});
+    case RG_Q4_K: return f(std::integral_constant<int, RG_Q4_K>{});
+    case RG_Q4_1: return f(std::integral_constant<int, RG_Q4_1>{});
+    case RG_Q5_0: return f(std::integral_constant<int, RG_Q5_0>{});
+    case RG_Q5_1: return f(std::integral_constant<int, RG_Q5_1>{});
+    case RG_Q5_K: return f(std::integral_constant<int, RG_Q5_K>{});
+    default: return fallback;
+  }
 }
 
 // All launchers enqueue on `stream` and return cudaSuccess or the launch

@@ -103,15 +103,10 @@ cudaError_t launch_simt32(int wtype, const void* W, int64_t N, int64_t K, const 
   if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
   const uint8_t* w = static_cast<const uint8_t*>(W);
   const int n = static_cast<int>(N), k = static_cast<int>(K), t = static_cast<int>(T);
-  switch (wtype) {
-    case RG_F16: simt32_kernel<RG_F16><<<grid, 256, 0, stream>>>(w, rb, n, k, dY, t, dX, beta); break;
-    case RG_BF16: simt32_kernel<RG_BF16><<<grid, 256, 0, stream>>>(w, rb, n, k, dY, t, dX, beta); break;
-    case RG_Q8_0: simt32_kernel<RG_Q8_0><<<grid, 256, 0, stream>>>(w, rb, n, k, dY, t, dX, beta); break;
-    case RG_Q4_0: simt32_kernel<RG_Q4_0><<<grid, 256, 0, stream>>>(w, rb, n, k, dY, t, dX, beta); break;
-    case RG_Q4_K: simt32_kernel<RG_Q4_K><<<grid, 256, 0, stream>>>(w, rb, n, k, dY, t, dX, beta); break;
-    default: return cudaErrorInvalidValue;
-  }
-  return counted(cudaGetLastError());
+  return with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
+    simt32_kernel<decltype(wt)::value><<<grid, 256, 0, stream>>>(w, rb, n, k, dY, t, dX, beta);
+    return counted(cudaGetLastError());
+  });
 }
 
 }  // namespace rg

@@ -28,7 +28,7 @@ constexpr int THREADS = 256;   // 8 consumer warps (plus one producer warp)
 // Raw bytes one lane needs from a row for its 8 values (a 256-value tile).
 template <int WT>
 struct Raw {
-  uint32_t v[WT == RG_Q4_K ? 6 : WT == RG_Q8_0 || WT == RG_Q4_0 ? 3 : 4];
+  uint32_t v[WT == RG_Q5_K ? 8 : WT == RG_Q4_K ? 6 : (WT == RG_Q8_0 || WT == RG_Q4_0 || WT == RG_Q4_1) ? 3 : 4];
 };
 
 // The bytes one lane needs for its 8 values, from a row tile staged in
@@ -46,11 +46,39 @@ __device__ __forceinline__ void load_raw_smem(const uint8_t* tile, int lane, Raw
     r.v[0] = *reinterpret_cast<const uint16_t*>(blk);
     r.v[1] = static_cast<uint32_t>(q16[0]) | (static_cast<uint32_t>(q16[1]) << 16);
     r.v[2] = static_cast<uint32_t>(q16[2]) | (static_cast<uint32_t>(q16[3]) << 16);
+  } else if constexpr (WT == RG_Q4_1) {
+    const uint8_t* blk = tile + 20 * (lane >> 2);
+    const uint32_t* q = reinterpret_cast<const uint32_t*>(blk + 4 + 8 * (lane & 1));
+    r.v[0] = *reinterpret_cast<const uint32_t*>(blk);  // d | m << 16
+    r.v[1] = q[0];
+    r.v[2] = q[1];
+  } else if constexpr (WT == RG_Q5_0) {
+    const uint8_t* blk = tile + 22 * (lane >> 2);
+    const uint16_t* h16 = reinterpret_cast<const uint16_t*>(blk + 2);
+    const uint16_t* q16 = reinterpret_cast<const uint16_t*>(blk + 6 + 8 * (lane & 1));
+    r.v[0] = *reinterpret_cast<const uint16_t*>(blk);
+    r.v[1] = static_cast<uint32_t>(h16[0]) | (static_cast<uint32_t>(h16[1]) << 16);
+    r.v[2] = static_cast<uint32_t>(q16[0]) | (static_cast<uint32_t>(q16[1]) << 16);
+    r.v[3] = static_cast<uint32_t>(q16[2]) | (static_cast<uint32_t>(q16[3]) << 16);
+  } else if constexpr (WT == RG_Q5_1) {
+    const uint8_t* blk = tile + 24 * (lane >> 2);
+    const uint2 q = *reinterpret_cast<const uint2*>(blk + 8 + 8 * (lane & 1));
+    r.v[0] = *reinterpret_cast<const uint32_t*>(blk);      // d | m << 16
+    r.v[1] = *reinterpret_cast<const uint32_t*>(blk + 4);  // qh
+    r.v[2] = q.x;
+    r.v[3] = q.y;
   } else {
+    // Q4_K, Q5_K: the header, this lane's 8 bytes of nibbles (and of qh)
+    constexpr int QS = WT == RG_Q5_K ? 48 : 16;
     const uint4 h = *reinterpret_cast<const uint4*>(tile);
     const int c = lane >> 3, l0 = 8 * (lane & 3);
-    const uint2 q = *reinterpret_cast<const uint2*>(tile + 16 + 32 * c + l0);
+    const uint2 q = *reinterpret_cast<const uint2*>(tile + QS + 32 * c + l0);
     r.v[0] = h.x; r.v[1] = h.y; r.v[2] = h.z; r.v[3] = h.w; r.v[4] = q.x; r.v[5] = q.y;
+    if constexpr (WT == RG_Q5_K) {
+      const uint2 qh = *reinterpret_cast<const uint2*>(tile + 16 + l0);
+      r.v[6] = qh.x;
+      r.v[7] = qh.y;
+    }
   }
 }
 
@@ -92,6 +120,30 @@ __device__ __forceinline__ void decode_raw(const Raw<WT>& r, int lane, float (&w
       w[4 * j + 2] = d * byte_minus<2>(x, kTwo23 + 8.0f);
       w[4 * j + 3] = d * byte_minus<3>(x, kTwo23 + 8.0f);
     }
+  } else if constexpr (WT == RG_Q4_1 || WT == RG_Q5_0 || WT == RG_Q5_1) {
+    // values 8(lane & 3) .. +7 of block lane >> 2: nibbles (low for the
+    // first 16 values of the block, high for the rest) and the fifth bits
+    constexpr int Q0 = WT == RG_Q4_1 ? 1 : 2;
+    const float d = f16_to_f32(static_cast<uint16_t>(r.v[0] & 0xFFFFu));
+    const float m = WT == RG_Q5_0 ? 0.0f : f16_to_f32(static_cast<uint16_t>(r.v[0] >> 16));
+    const int j0 = 8 * (lane & 3);
+    const int shift = j0 >= 16 ? 4 : 0;
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      uint32_t x = (r.v[Q0 + jj] >> shift) & 0x0F0F0F0Fu;
+      if constexpr (WT != RG_Q4_1) x |= fifth_bits4(r.v[1] >> (j0 + 4 * jj));
+      if constexpr (WT == RG_Q5_0) {
+        w[4 * jj + 0] = d * byte_minus<0>(x, kTwo23 + 16.0f);
+        w[4 * jj + 1] = d * byte_minus<1>(x, kTwo23 + 16.0f);
+        w[4 * jj + 2] = d * byte_minus<2>(x, kTwo23 + 16.0f);
+        w[4 * jj + 3] = d * byte_minus<3>(x, kTwo23 + 16.0f);
+      } else {  // exact product, one rounding of the sum
+        w[4 * jj + 0] = fmaf(d, byte_minus<0>(x, kTwo23), m);
+        w[4 * jj + 1] = fmaf(d, byte_minus<1>(x, kTwo23), m);
+        w[4 * jj + 2] = fmaf(d, byte_minus<2>(x, kTwo23), m);
+        w[4 * jj + 3] = fmaf(d, byte_minus<3>(x, kTwo23), m);
+      }
+    }
   } else {
     const float d = f16_to_f32(static_cast<uint16_t>(r.v[0] & 0xFFFFu));
     const float dmin = f16_to_f32(static_cast<uint16_t>(r.v[0] >> 16));
@@ -112,7 +164,8 @@ __device__ __forceinline__ void decode_raw(const Raw<WT>& r, int lane, float (&w
     const float ndm = -(dmin * static_cast<float>(m));
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
-      const uint32_t x = (r.v[4 + jj] >> (4 * half)) & 0x0F0F0F0Fu;
+      uint32_t x = (r.v[4 + jj] >> (4 * half)) & 0x0F0F0F0Fu;
+      if constexpr (WT == RG_Q5_K) x |= ((r.v[6 + jj] >> j) & 0x01010101u) << 4;
       w[4 * jj + 0] = fmaf(ds, byte_minus<0>(x, kTwo23), ndm);
       w[4 * jj + 1] = fmaf(ds, byte_minus<1>(x, kTwo23), ndm);
       w[4 * jj + 2] = fmaf(ds, byte_minus<2>(x, kTwo23), ndm);
@@ -231,12 +284,73 @@ __device__ __forceinline__ void row_block(const uint8_t* row, int g, const float
         }
       }
     }
+  } else if constexpr (WT == RG_Q4_1 || WT == RG_Q5_0 || WT == RG_Q5_1) {
+    // block g at byte X = g * (20, 22 or 24): d (and m), qh (Q5), 16 bytes
+    // of nibbles.  Q5_0's X is even only: off2 = it starts 2 bytes into a word.
+    constexpr int BB = block_bytes(WT);
+    const int X = BB * g;
+    const uint32_t* wp = reinterpret_cast<const uint32_t*>(row + (X & ~3));
+    const bool off2 = WT == RG_Q5_0 && (X & 2) != 0;
+    constexpr int NW = WT == RG_Q4_1 ? 5 : 6;
+    uint32_t w[NW];
+#pragma unroll
+    for (int i = 0; i < NW; ++i) w[i] = wp[i];
+    float d, m = 0.0f;
+    uint32_t qh = 0, q[4];
+    if constexpr (WT == RG_Q5_0) {
+      d = f16_to_f32(static_cast<uint16_t>(off2 ? (w[0] >> 16) : (w[0] & 0xFFFFu)));
+      qh = off2 ? w[1] : __funnelshift_r(w[0], w[1], 16);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) q[j] = off2 ? w[2 + j] : __funnelshift_r(w[1 + j], w[2 + j], 16);
+    } else {
+      d = f16_to_f32(static_cast<uint16_t>(w[0] & 0xFFFFu));
+      m = f16_to_f32(static_cast<uint16_t>(w[0] >> 16));
+      constexpr int Q0 = WT == RG_Q4_1 ? 1 : 2;
+      if constexpr (WT == RG_Q5_1) qh = w[1];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) q[j] = w[Q0 + j];
+    }
+    // y * (d*q + m) = (y*d)*q + y*m; the y*m terms go to msum (subtracted, so negated)
+    f32x2 yd[TB];
+#pragma unroll
+    for (int t = 0; t < TB; ++t) {
+      yd[t] = pack2(y[t] * d, y[t] * d);
+      if constexpr (WT != RG_Q5_0) msum[t] = fmaf(y[t], -m, msum[t]);
+    }
+    const float bias = WT == RG_Q5_0 ? 16.0f : 0.0f;
+    const f32x2 nb = pack2(-(kTwo23 + bias), -(kTwo23 + bias));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t lo = q[j] & 0x0F0F0F0Fu, hi = (q[j] >> 4) & 0x0F0F0F0Fu;  // values 4j.., 16+4j..
+      if constexpr (WT != RG_Q4_1) {
+        lo |= fifth_bits4(qh >> (4 * j));
+        hi |= fifth_bits4(qh >> (16 + 4 * j));
+      }
+      const f32x2 l01 = bytes2<0>(lo, nb), l23 = bytes2<2>(lo, nb);
+      const f32x2 h01 = bytes2<0>(hi, nb), h23 = bytes2<2>(hi, nb);
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        acc[t][2 * j] = fma2(yd[t], l01, acc[t][2 * j]);
+        acc[t][2 * j + 1] = fma2(yd[t], l23, acc[t][2 * j + 1]);
+        acc[t][8 + 2 * j] = fma2(yd[t], h01, acc[t][8 + 2 * j]);
+        acc[t][9 + 2 * j] = fma2(yd[t], h23, acc[t][9 + 2 * j]);
+      }
+    }
   } else {
     // sub-block g = 2c + h: nibble h of bytes 32c .. 32c+31 of the quants
+    // (Q5_K: plus bit g of qh[l] as the fifth bit)
+    constexpr int QS = WT == RG_Q5_K ? 48 : 16;
     const int c = g >> 1, h = g & 1;
     const uint4 hd = *reinterpret_cast<const uint4*>(row);
-    const uint4 qa = *reinterpret_cast<const uint4*>(row + 16 + 32 * c);
-    const uint4 qb = *reinterpret_cast<const uint4*>(row + 32 + 32 * c);
+    const uint4 qa = *reinterpret_cast<const uint4*>(row + QS + 32 * c);
+    const uint4 qb = *reinterpret_cast<const uint4*>(row + QS + 16 + 32 * c);
+    uint32_t hw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if constexpr (WT == RG_Q5_K) {
+      const uint4 ha = *reinterpret_cast<const uint4*>(row + 16);
+      const uint4 hb2 = *reinterpret_cast<const uint4*>(row + 32);
+      hw[0] = ha.x; hw[1] = ha.y; hw[2] = ha.z; hw[3] = ha.w;
+      hw[4] = hb2.x; hw[5] = hb2.y; hw[6] = hb2.z; hw[7] = hb2.w;
+    }
     const float d = f16_to_f32(static_cast<uint16_t>(hd.x & 0xFFFFu));
     const float dmin = f16_to_f32(static_cast<uint16_t>(hd.x >> 16));
     // the 6-bit scale and min of sub-block g from header bytes 4..15
@@ -263,7 +377,8 @@ __device__ __forceinline__ void row_block(const uint8_t* row, int g, const float
     const uint32_t qw[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const uint32_t x = (qw[j] >> (4 * h)) & 0x0F0F0F0Fu;
+      uint32_t x = (qw[j] >> (4 * h)) & 0x0F0F0F0Fu;
+      if constexpr (WT == RG_Q5_K) x |= ((hw[j] >> g) & 0x01010101u) << 4;
       const f32x2 q01 = bytes2<0>(x, nb), q23 = bytes2<2>(x, nb);
 #pragma unroll
       for (int t = 0; t < TB; ++t) {
@@ -314,7 +429,7 @@ __device__ __forceinline__ void consume_rows(int g, const uint8_t* stage_buf, co
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       unpack2(acc[t][i], v[2 * i], v[2 * i + 1]);
-      if constexpr (WT == RG_Q4_K) {
+      if constexpr (WT != RG_Q8_0 && WT != RG_Q4_0 && WT != RG_Q5_0) {
         v[2 * i] -= msum[t];
         v[2 * i + 1] -= msum[t];
       }
@@ -589,14 +704,9 @@ SmalltPlan plan_smallt(int wtype, int64_t N, int64_t K, int64_t T, const DevInfo
   p.tb = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
   p.n_ktiles = static_cast<int>((K + 255) / 256);
   p.n_tchunks = static_cast<int>((T + p.tb - 1) / p.tb);
-  int per_sm = 1;
-  switch (wtype) {
-    case RG_F16: per_sm = smallt_residency_tb<RG_F16>(p.tb, dev); break;
-    case RG_BF16: per_sm = smallt_residency_tb<RG_BF16>(p.tb, dev); break;
-    case RG_Q8_0: per_sm = smallt_residency_tb<RG_Q8_0>(p.tb, dev); break;
-    case RG_Q4_0: per_sm = smallt_residency_tb<RG_Q4_0>(p.tb, dev); break;
-    default: per_sm = smallt_residency_tb<RG_Q4_K>(p.tb, dev); break;
-  }
+  const int per_sm = with_wtype(wtype, 1, [&](auto wt) {
+    return smallt_residency_tb<decltype(wt)::value>(p.tb, dev);
+  });
   // one wave of resident CTAs; rows split no finer than 64 per CTA and no
   // coarser than the staged slice of dY allows
   const int64_t capacity = static_cast<int64_t>(dev.num_sms) * per_sm;
@@ -651,15 +761,9 @@ cudaError_t launch_smallt(int wtype, const void* W, int64_t N, int64_t K, const 
                           int64_t T, float* dX, float beta, float* part, const SmalltPlan& p,
                           const DevInfo& dev, cudaStream_t stream) {
   if (p.n_tchunks > 65535 || p.n_splits > 65535) return cudaErrorInvalidConfiguration;
-  cudaError_t e;
-  switch (wtype) {
-    case RG_F16: e = launch_smallt_w<RG_F16>(W, N, K, dY, T, part, p, dev, stream); break;
-    case RG_BF16: e = launch_smallt_w<RG_BF16>(W, N, K, dY, T, part, p, dev, stream); break;
-    case RG_Q8_0: e = launch_smallt_w<RG_Q8_0>(W, N, K, dY, T, part, p, dev, stream); break;
-    case RG_Q4_0: e = launch_smallt_w<RG_Q4_0>(W, N, K, dY, T, part, p, dev, stream); break;
-    case RG_Q4_K: e = launch_smallt_w<RG_Q4_K>(W, N, K, dY, T, part, p, dev, stream); break;
-    default: return cudaErrorInvalidValue;
-  }
+  const cudaError_t e = with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
+    return launch_smallt_w<decltype(wt)::value>(W, N, K, dY, T, part, p, dev, stream);
+  });
   if (e != cudaSuccess) return e;
   return launch_reduce_partials(part, p.n_splits, T * K, dX, beta, dev, stream);
 }

@@ -52,11 +52,20 @@ constexpr int B_STAGE = B_ROWS * 128;     // 16 KB: 128 rows of t x 64 16-bit va
 constexpr int SMEM_BUDGET = 224 * 1024;
 
 // Bytes of one packed W row that a 128-value tile loads (16-byte multiples):
-// Q8_0 4 blocks = 136 B inside a 144 B window, Q4_0 72 B inside 80 B, Q4_K
-// the whole 144 B super-block (its header holds every sub-block's scale).
+// Q8_0 4 blocks = 136 B inside a 144 B window, Q4_0 72 B inside 80 B, Q4_1
+// exactly 80 B, Q5_0 88 B and Q5_1 96 B inside 112 B (the wider row stride
+// puts eight consecutive rows in distinct shared-memory bank groups), Q4_K
+// and Q5_K the whole super-block (its header holds every sub-block's scale).
 template <int WT>
 __host__ __device__ constexpr int p_row_bytes() {
-  return WT == RG_Q8_0 ? 144 : WT == RG_Q4_0 ? 80 : WT == RG_Q4_K ? 144 : 0;
+  return WT == RG_Q8_0   ? 144
+         : WT == RG_Q4_0 ? 80
+         : WT == RG_Q4_K ? 144
+         : WT == RG_Q4_1 ? 80
+         : WT == RG_Q5_0 ? 112
+         : WT == RG_Q5_1 ? 112
+         : WT == RG_Q5_K ? 176
+                         : 0;
 }
 
 template <int WT, int CG, int BT>
@@ -250,6 +259,109 @@ __device__ __forceinline__ void dec_q4_k_part(const uint8_t* row, uint8_t* A, in
   st_a_chunk(A, n, cb + 5, hi[4], hi[5], hi[6], hi[7]);
 }
 
+// Q4_1 / Q5_0 / Q5_1 block at byte S of a row window: fp16 d (then fp16 m
+// for Q4_1 and Q5_1), the fifth bits qh (Q5), 16 bytes of nibbles.  Writes
+// its 32 values as chunks 4b .. 4b+3 of row n: d*(q-16) (Q5_0) rounded once,
+// or fma(q, d, m) rounded once (Q4_1, Q5_1; d and m are exact fp16 fields).
+template <int WT, int S>
+__device__ __forceinline__ void dec_q41_q5_block(const uint8_t* row, uint8_t* A, int n, int b) {
+  constexpr int QH = WT == RG_Q5_0 ? 2 : WT == RG_Q5_1 ? 4 : -1;
+  constexpr int QS = WT == RG_Q4_1 ? 4 : WT == RG_Q5_0 ? 6 : 8;
+  constexpr int C0 = S / 16;
+  constexpr int XQ = S - 16 * C0 + QS + 12;  // the last quant word, relative to chunk C0
+  constexpr int LAST = (XQ & 3) == 0 ? XQ + 3 : (XQ & ~3) + 7;  // last byte word_at reads
+  constexpr int C1 = C0 + LAST / 16;
+  static_assert(16 * C1 + 16 <= p_row_bytes<WT>(), "reads stay inside the row window");
+  const auto r = load_chunks<C0, C1>(row);
+  constexpr int X = S - 16 * C0;
+  const uint32_t dm = r.word_at(X);
+  const __half2 d2 = __half2half2(__ushort_as_half(static_cast<uint16_t>(dm & 0xFFFFu)));
+  const __half2 m2 = __half2half2(__ushort_as_half(static_cast<uint16_t>(dm >> 16)));
+  uint32_t qh = 0;
+  if constexpr (QH >= 0) qh = r.word_at(X + QH);
+  const __half2 off = __float2half2_rn(WT == RG_Q5_0 ? 1040.0f : 1024.0f);  // 1024 (+16)
+  uint32_t lo[8], hi[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w = r.word_at(X + QS + 4 * j);
+    uint32_t xl = w & 0x0F0F0F0Fu, xh = (w >> 4) & 0x0F0F0F0Fu;
+    if constexpr (QH >= 0) {
+      xl |= fifth_bits4(qh >> (4 * j));
+      xh |= fifth_bits4(qh >> (16 + 4 * j));
+    }
+    if constexpr (WT == RG_Q5_0) {
+      four_scaled(xl, off, d2, lo[2 * j], lo[2 * j + 1]);
+      four_scaled(xh, off, d2, hi[2 * j], hi[2 * j + 1]);
+    } else {
+      four_affine(xl, off, d2, m2, lo[2 * j], lo[2 * j + 1]);
+      four_affine(xh, off, d2, m2, hi[2 * j], hi[2 * j + 1]);
+    }
+  }
+  st_a_chunk(A, n, 4 * b, lo[0], lo[1], lo[2], lo[3]);
+  st_a_chunk(A, n, 4 * b + 1, lo[4], lo[5], lo[6], lo[7]);
+  st_a_chunk(A, n, 4 * b + 2, hi[0], hi[1], hi[2], hi[3]);
+  st_a_chunk(A, n, 4 * b + 3, hi[4], hi[5], hi[6], hi[7]);
+}
+
+// Q5_K: as dec_q4_k_part, with the fifth bit of each value from qh: bit 2c
+// (low nibbles) or 2c+1 (high nibbles) of qh[l]; this part covers l = 16HH ..
+// 16HH+15, i.e. qh bytes 16HH .. 16HH+15 at window offset 16.
+template <int H2, int CL, int HH>
+__device__ __forceinline__ void dec_q5_k_part(const uint8_t* row, uint8_t* A, int n) {
+  constexpr int c = 2 * H2 + CL;
+  const uint4 hdr = *reinterpret_cast<const uint4*>(row);
+  const uint4 hv = *reinterpret_cast<const uint4*>(row + 16 + 16 * HH);
+  const uint4 qv = *reinterpret_cast<const uint4*>(row + 48 + 32 * c + 16 * HH);
+  const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x & 0xFFFFu)));
+  const float dmin = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x >> 16)));
+  int sc[2], m[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = 2 * c + h;
+    if (j < 4) {
+      sc[h] = byte_of(hdr.y, hdr.z, hdr.w, j) & 63;
+      m[h] = byte_of(hdr.y, hdr.z, hdr.w, j + 4) & 63;
+    } else {
+      const uint32_t e = byte_of(hdr.y, hdr.z, hdr.w, j + 4);
+      sc[h] = (e & 15) | ((byte_of(hdr.y, hdr.z, hdr.w, j - 4) >> 6) << 4);
+      m[h] = (e >> 4) | ((byte_of(hdr.y, hdr.z, hdr.w, j) >> 6) << 4);
+    }
+  }
+  const __half2 magic = __float2half2_rn(1024.0f);
+  const __half2 ds0 = __float2half2_rn(d * static_cast<float>(sc[0]));
+  const __half2 nm0 = __float2half2_rn(-(dmin * static_cast<float>(m[0])));
+  const __half2 ds1 = __float2half2_rn(d * static_cast<float>(sc[1]));
+  const __half2 nm1 = __float2half2_rn(-(dmin * static_cast<float>(m[1])));
+  const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+  const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+  uint32_t lo[8], hi[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t xl = (qw[j] & 0x0F0F0F0Fu) | (((hw[j] >> (2 * c)) & 0x01010101u) << 4);
+    const uint32_t xh = ((qw[j] >> 4) & 0x0F0F0F0Fu) | (((hw[j] >> (2 * c + 1)) & 0x01010101u) << 4);
+    four_affine(xl, magic, ds0, nm0, lo[2 * j], lo[2 * j + 1]);
+    four_affine(xh, magic, ds1, nm1, hi[2 * j], hi[2 * j + 1]);
+  }
+  constexpr int cb = 8 * CL + 2 * HH;
+  st_a_chunk(A, n, cb, lo[0], lo[1], lo[2], lo[3]);
+  st_a_chunk(A, n, cb + 1, lo[4], lo[5], lo[6], lo[7]);
+  st_a_chunk(A, n, cb + 4, hi[0], hi[1], hi[2], hi[3]);
+  st_a_chunk(A, n, cb + 5, hi[4], hi[5], hi[6], hi[7]);
+}
+
+// Block b (32-value types) or part b (Q4_K, Q5_K: chunk b >> 1 of the
+// half, 16 bytes b & 1) of row n of a stage.
+template <int WT, int ODD, int B>
+__device__ __forceinline__ void dec_item(const uint8_t* row, uint8_t* A, int n) {
+  if constexpr (WT == RG_Q8_0) dec_q8_block<8 * ODD + 34 * B>(row, A, n, B);
+  else if constexpr (WT == RG_Q4_0) dec_q4_0_block<8 * ODD + 18 * B>(row, A, n, B);
+  else if constexpr (WT == RG_Q4_1) dec_q41_q5_block<WT, 20 * B>(row, A, n, B);
+  else if constexpr (WT == RG_Q5_0) dec_q41_q5_block<WT, 8 * ODD + 22 * B>(row, A, n, B);
+  else if constexpr (WT == RG_Q5_1) dec_q41_q5_block<WT, 24 * B>(row, A, n, B);
+  else if constexpr (WT == RG_Q4_K) dec_q4_k_part<ODD, B / 2, B % 2>(row, A, n);
+  else dec_q5_k_part<ODD, B / 2, B % 2>(row, A, n);
+}
+
 // One warp decodes a whole stage: P holds BC packed rows (row stride
 // p_row_bytes) of this CTA's 128-value tile, A receives the fp16 operand.
 // Item i of lane l is row n = l + 32*(i & 1) and block (or Q4_K part) i >> 1:
@@ -265,29 +377,11 @@ __device__ __forceinline__ void decode_stage_warp(const uint8_t* __restrict__ P,
     if ((i & (NPART - 1)) != part) continue;  // this warp's share of the items
     const int n = lane + 32 * (i & 1);
     const uint8_t* row = P + n * PR;
-    constexpr int dummy = 0;
-    (void)dummy;
     switch (i >> 1) {
-      case 0:
-        if constexpr (WT == RG_Q8_0) dec_q8_block<8 * ODD + 0>(row, A, n, 0);
-        else if constexpr (WT == RG_Q4_0) dec_q4_0_block<8 * ODD + 0>(row, A, n, 0);
-        else dec_q4_k_part<ODD, 0, 0>(row, A, n);
-        break;
-      case 1:
-        if constexpr (WT == RG_Q8_0) dec_q8_block<8 * ODD + 34>(row, A, n, 1);
-        else if constexpr (WT == RG_Q4_0) dec_q4_0_block<8 * ODD + 18>(row, A, n, 1);
-        else dec_q4_k_part<ODD, 0, 1>(row, A, n);
-        break;
-      case 2:
-        if constexpr (WT == RG_Q8_0) dec_q8_block<8 * ODD + 68>(row, A, n, 2);
-        else if constexpr (WT == RG_Q4_0) dec_q4_0_block<8 * ODD + 36>(row, A, n, 2);
-        else dec_q4_k_part<ODD, 1, 0>(row, A, n);
-        break;
-      default:
-        if constexpr (WT == RG_Q8_0) dec_q8_block<8 * ODD + 102>(row, A, n, 3);
-        else if constexpr (WT == RG_Q4_0) dec_q4_0_block<8 * ODD + 54>(row, A, n, 3);
-        else dec_q4_k_part<ODD, 1, 1>(row, A, n);
-        break;
+      case 0: dec_item<WT, ODD, 0>(row, A, n); break;
+      case 1: dec_item<WT, ODD, 1>(row, A, n); break;
+      case 2: dec_item<WT, ODD, 2>(row, A, n); break;
+      default: dec_item<WT, ODD, 3>(row, A, n); break;
     }
   }
 }
@@ -297,6 +391,10 @@ template <int WT>
 __device__ __forceinline__ int p_window_start(int kt) {
   if constexpr (WT == RG_Q8_0) return (kt * 136) & ~15;
   if constexpr (WT == RG_Q4_0) return (kt * 72) & ~15;
+  if constexpr (WT == RG_Q4_1) return kt * 80;
+  if constexpr (WT == RG_Q5_0) return (kt * 88) & ~15;
+  if constexpr (WT == RG_Q5_1) return kt * 96;
+  if constexpr (WT == RG_Q5_K) return (kt >> 1) * 176;
   return (kt >> 1) * 144;  // Q4_K: the whole super-block
 }
 
@@ -743,7 +841,9 @@ cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint
   CUresult r;
   if (is_quant(wtype)) {
     const uint64_t rb = static_cast<uint64_t>(K / block_values(wtype) * block_bytes(wtype));
-    const uint32_t box_bytes = wtype == RG_Q4_0 ? 80u : 144u;
+    const uint32_t box_bytes = static_cast<uint32_t>(with_wtype(wtype, 0, [](auto wt) {
+      return tc::p_row_bytes<decltype(wt)::value>();
+    }));
     r = encode_tiled(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rb / 4, static_cast<uint64_t>(N), rb,
                      box_bytes / 4, tc::BC, CU_TENSOR_MAP_SWIZZLE_NONE);
   } else {
@@ -757,15 +857,10 @@ cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint
                    tc::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   const int t = static_cast<int>(T), k = static_cast<int>(K);
-  cudaError_t e;
-  switch (wtype) {
-    case RG_F16: e = launch_tc_w<RG_F16>(mw, my, dX, beta, t, k, p, partial, dev, stream, inject_stall); break;
-    case RG_BF16: e = launch_tc_w<RG_BF16>(mw, my, dX, beta, t, k, p, partial, dev, stream, inject_stall); break;
-    case RG_Q8_0: e = launch_tc_w<RG_Q8_0>(mw, my, dX, beta, t, k, p, partial, dev, stream, inject_stall); break;
-    case RG_Q4_0: e = launch_tc_w<RG_Q4_0>(mw, my, dX, beta, t, k, p, partial, dev, stream, inject_stall); break;
-    case RG_Q4_K: e = launch_tc_w<RG_Q4_K>(mw, my, dX, beta, t, k, p, partial, dev, stream, inject_stall); break;
-    default: return cudaErrorInvalidValue;
-  }
+  const cudaError_t e = with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
+    return launch_tc_w<decltype(wt)::value>(mw, my, dX, beta, t, k, p, partial, dev, stream,
+                                            inject_stall);
+  });
   if (e != cudaSuccess || p.n_splits == 1) return e;
   return launch_reduce_partials(partial, p.n_splits, T * K, dX, beta, dev, stream);
 }

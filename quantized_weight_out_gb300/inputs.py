@@ -414,4 +414,8 @@ WORKLOADS = {
     "layer7b_t8192": _layer_sweep(8192),
     # the sweep's largest call alone (profiling a full-size launch)
     "layer7b_gate_t8192": [_layer_sweep(8192)[4]],
+    # the other quantized types on the sweep's q/o shape, one call each
+    "types_4096x4096_t8192": [Problem(f"{TYPE_NAMES[wt]}_4096x4096_t8192", wt, 4096, 4096, 8192,
+                                      1e-3, 0.0, 16 * i)
+                              for i, wt in enumerate([Q4_1, Q5_0, Q5_1, Q5_K])],
 }

@@ -16,7 +16,7 @@ torch = pytest.importorskip("torch")
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
 
-TYPES = [inputs.Q8_0, inputs.Q4_0, inputs.Q4_K, inputs.F16, inputs.BF16]
+TYPES = inputs.ALL_TYPES
 TOL = {1: 5e-3, 2: 5e-3, 3: 1e-5, 4: 5e-3, 5: 5e-3}  # tc, smallt, simt32, tc1, tc2
 ALL_VARIANTS = [1, 2, 3, 4, 5]
 

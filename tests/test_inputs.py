@@ -76,7 +76,7 @@ def test_workloads_and_row_bytes():
 
 def test_row_prefixes_are_smaller_calls():
     """The first rows of every generated input equal a smaller call's."""
-    for wt in (inputs.Q8_0, inputs.Q4_0, inputs.Q4_K, inputs.F16, inputs.BF16):
+    for wt in inputs.ALL_TYPES:
         p = inputs.Problem("x", wt, 40, 512, 12, 1e-3, 1.0, stream_base=32)
         rb = inputs.row_bytes(wt, 512)
         assert np.array_equal(p.weight()[: 7 * rb], p.weight(7))
