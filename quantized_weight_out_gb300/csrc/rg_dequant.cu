@@ -13,22 +13,63 @@
 
 namespace rg {
 
-// One thread per 8 consecutive values of a row: decode, two 16-byte stores.
+// Bytes of a 256-value segment of a stored row (a whole number of blocks).
+template <int WT>
+__host__ __device__ constexpr int seg_bytes() {
+  return 256 / block_values(WT) * block_bytes(WT);
+}
+
+// A warp per group of U rows x one 256-value segment: each lane fetches 16
+// bytes of each of the U row segments with one 16-byte load (U loads in
+// flight), the warp stages them in shared memory, and every warp-wide store
+// writes 512 contiguous bytes of F32.  Segments run fastest along a row, so
+// consecutive warps read and write consecutive memory.
+constexpr int DQ_U = 4;
 template <int WT>
 __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict__ W, int64_t N,
                                                       int64_t K, int64_t rb,
                                                       float* __restrict__ out) {
-  const int64_t gpr = K >> 3;  // 8-value groups per row
-  const int64_t total = N * gpr;
-  for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
-       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t n = g / gpr;
-    const int k0 = static_cast<int>(g - n * gpr) << 3;
-    float v[8];
-    decode8_f32<WT>(W + n * rb, k0, v);
-    float4* o = reinterpret_cast<float4*>(out + n * K + k0);
-    o[0] = make_float4(v[0], v[1], v[2], v[3]);
-    o[1] = make_float4(v[4], v[5], v[6], v[7]);
+  constexpr int SB = seg_bytes<WT>();
+  static_assert(SB % 16 == 0 && SB <= 512, "a segment is at most one 16-byte load per lane");
+  __shared__ __align__(16) uint8_t buf[8][DQ_U][SB];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t segs = (K + 255) >> 8;
+  const int64_t groups = (N + DQ_U - 1) / DQ_U * segs;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * 8;
+  for (int64_t g = blockIdx.x * 8LL + warp; g < groups; g += nwarps) {
+    const int64_t rg = g / segs, sg = g - rg * segs;
+    const int64_t n0 = rg * DQ_U;
+    const int64_t boff = sg * SB + 16 * lane;  // this lane's bytes of the segment
+    uint4 v[DQ_U];
+#pragma unroll
+    for (int u = 0; u < DQ_U; ++u) {
+      v[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (16 * lane < SB && n0 + u < N && boff < rb)
+        v[u] = __ldcs(reinterpret_cast<const uint4*>(W + (n0 + u) * rb + boff));
+    }
+#pragma unroll
+    for (int u = 0; u < DQ_U; ++u)
+      if (16 * lane < SB) *reinterpret_cast<uint4*>(&buf[warp][u][16 * lane]) = v[u];
+    __syncwarp();
+    // lane l stores values 4l .. 4l+3 and 128+4l .. 128+4l+3 of the segment,
+    // so each warp-wide store covers 512 contiguous bytes; it decodes the
+    // 8-value groups holding them (lanes 2i and 2i+1 share a group)
+    const int hl = lane & 1;
+#pragma unroll
+    for (int u = 0; u < DQ_U; ++u) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int kin = 128 * h + 8 * (lane >> 1);  // the group, inside the segment
+        const int64_t k = sg * 256 + kin + 4 * hl;
+        if (n0 + u < N && k < K) {
+          float x[8];
+          decode8_f32<WT>(buf[warp][u], kin, x);
+          __stcs(reinterpret_cast<float4*>(out + (n0 + u) * K + k),
+                 hl ? make_float4(x[4], x[5], x[6], x[7]) : make_float4(x[0], x[1], x[2], x[3]));
+        }
+      }
+    }
+    __syncwarp();
   }
 }
 
@@ -41,7 +82,7 @@ static int grid_for(int64_t work_items, int threads, const DevInfo& dev) {
 cudaError_t launch_dequant(int wtype, const void* W, int64_t N, int64_t K, float* out,
                            const DevInfo& dev, cudaStream_t stream) {
   const int64_t rb = K / block_values(wtype) * block_bytes(wtype);
-  const int grid = grid_for(N * (K >> 3), 256, dev);
+  const int grid = grid_for((N + DQ_U - 1) / DQ_U * ((K + 255) >> 8) * 32, 256, dev);
   const uint8_t* w = static_cast<const uint8_t*>(W);
   return with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
     dequant_kernel<decltype(wt)::value><<<grid, 256, 0, stream>>>(w, N, K, rb, out);
