@@ -38,6 +38,11 @@ Block formats (little-endian), ggml's GGUF block types:
 * Q5_K 176 B / 256: fp16 d, fp16 dmin, 12 B (sc, m) as Q4_K, qh[32], qs[128]:
                    the nibbles of Q4_K plus bit 2c (low) / 2c+1 (high) of
                    qh[l] as the fifth bit;        y = (d*sc)*q - dmin*m
+* Q6_K 210 B / 256: ql[128], qh[64], int8 scales[16], fp16 d.  Value
+                   128h + 32i + l (h = 0..1, i = 0..3, l = 0..31) takes the
+                   low (i < 2) or high (i >= 2) nibble of ql[64h + 32(i%2) + l]
+                   and bits 2i..2i+1 of qh[32h + l] as bits 4..5;
+                                                  y = (d*sc[v/16]) * (q - 32)
 * F16 / BF16: 2 B per value.
 
 Parity pins for each function live in tests/test_oracle.py.
@@ -47,10 +52,11 @@ from __future__ import annotations
 import numpy as np
 
 F16, BF16, Q8_0, Q4_0, Q4_K = 1, 2, 3, 4, 5
-Q4_1, Q5_0, Q5_1, Q5_K = 6, 7, 8, 9
+Q4_1, Q5_0, Q5_1, Q5_K, Q6_K = 6, 7, 8, 9, 10
 
 _BLOCK = {F16: (1, 2), BF16: (1, 2), Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144),
-          Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q5_K: (256, 176)}
+          Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q5_K: (256, 176),
+          Q6_K: (256, 210)}
 
 
 def row_bytes(wtype: int, K: int) -> int:
@@ -237,6 +243,29 @@ def decode_q5_k(W, N: int, K: int) -> np.ndarray:
     return y.astype(np.float32).reshape(N, K)
 
 
+def decode_q6_k(W, N: int, K: int) -> np.ndarray:
+    """Q6_K: value v = 128h + 32i + l (h = 0..1, i = 0..3, l = 0..31):
+    q = nibble | (bits 2i..2i+1 of qh[32h + l]) << 4, the nibble being the low
+    (i = 0, 1) or high (i = 2, 3) half of ql[64h + 32(i % 2) + l];
+    y = (F32(d) * sc[v // 16]) * (q - 32).  Both products are exact: 11 + 7 +
+    5 significant bits."""
+    blk = _rows(W, N, K, Q6_K).reshape(N, K // 256, 210)
+    ql = blk[..., 0:128].astype(np.int64)
+    qh = blk[..., 128:192].astype(np.int64)
+    sc = blk[..., 192:208].view(np.int8).astype(np.float32)
+    d = f16_bits_to_f32(_le16(blk[..., 208], blk[..., 209]))
+    q = np.empty(blk.shape[:-1] + (256,), dtype=np.float32)
+    for h in range(2):
+        for i in range(4):
+            src = ql[..., 64 * h + 32 * (i % 2): 64 * h + 32 * (i % 2) + 32]
+            nib = (src >> 4) if i >= 2 else (src & 0x0F)
+            hb = (qh[..., 32 * h: 32 * h + 32] >> (2 * i)) & 3
+            q[..., 128 * h + 32 * i: 128 * h + 32 * i + 32] = (nib | (hb << 4)) - 32
+    scale = d[..., None] * sc                      # [N, nb, 16], exact
+    y = np.repeat(scale, 16, axis=-1) * q          # exact
+    return y.astype(np.float32).reshape(N, K)
+
+
 def decode_f16(W, N: int, K: int) -> np.ndarray:
     b = _rows(W, N, K, F16).reshape(N, K, 2)
     return f16_bits_to_f32(_le16(b[..., 0], b[..., 1]))
@@ -249,7 +278,8 @@ def decode_bf16(W, N: int, K: int) -> np.ndarray:
 
 _DECODERS = {F16: decode_f16, BF16: decode_bf16, Q8_0: decode_q8_0,
              Q4_0: decode_q4_0, Q4_K: decode_q4_k, Q4_1: decode_q4_1,
-             Q5_0: decode_q5_0, Q5_1: decode_q5_1, Q5_K: decode_q5_k}
+             Q5_0: decode_q5_0, Q5_1: decode_q5_1, Q5_K: decode_q5_k,
+             Q6_K: decode_q6_k}
 
 
 def dequant(wtype: int, W, N: int, K: int) -> np.ndarray:

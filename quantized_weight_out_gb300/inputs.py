@@ -28,6 +28,8 @@ Formats written (little-endian, the block layouts of ggml's GGUF types):
 * Q5_1  24 B / 32 values: fp16 ``d``, fp16 ``m``, ``qh``, 16 bytes of nibbles.
 * Q5_K 176 B / 256 values: the Q4_K header, 32 bytes ``qh`` (bit 2c / 2c+1 of
   ``qh[l]`` = fifth bit of value 64c+l / 64c+32+l), 128 bytes of nibbles.
+* Q6_K 210 B / 256 values: ``ql[128]`` (low 4 bits), ``qh[64]`` (2 high bits
+  each), 16 int8 ``scales``, fp16 ``d``.
 * F16 / BF16: 2 B per value.
 
 The generator recipes follow the workload descriptions of the llama.cpp fork's
@@ -46,15 +48,16 @@ import numpy as np
 # ----------------------------------------------------------------------------
 # weight type codes (the C ABI uses the same integers)
 F16, BF16, Q8_0, Q4_0, Q4_K = 1, 2, 3, 4, 5
-Q4_1, Q5_0, Q5_1, Q5_K = 6, 7, 8, 9
+Q4_1, Q5_0, Q5_1, Q5_K, Q6_K = 6, 7, 8, 9, 10
 TYPE_NAMES = {F16: "f16", BF16: "bf16", Q8_0: "q8_0", Q4_0: "q4_0", Q4_K: "q4_k",
-              Q4_1: "q4_1", Q5_0: "q5_0", Q5_1: "q5_1", Q5_K: "q5_k"}
+              Q4_1: "q4_1", Q5_0: "q5_0", Q5_1: "q5_1", Q5_K: "q5_k", Q6_K: "q6_k"}
 NAME_TO_TYPE = {v: k for k, v in TYPE_NAMES.items()}
-ALL_TYPES = [Q8_0, Q4_0, Q4_K, F16, BF16, Q4_1, Q5_0, Q5_1, Q5_K]
+ALL_TYPES = [Q8_0, Q4_0, Q4_K, F16, BF16, Q4_1, Q5_0, Q5_1, Q5_K, Q6_K]
 
 # (values per block, bytes per block)
 BLOCK = {F16: (1, 2), BF16: (1, 2), Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144),
-         Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q5_K: (256, 176)}
+         Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q5_K: (256, 176),
+         Q6_K: (256, 210)}
 
 
 def row_bytes(wtype: int, K: int) -> int:
@@ -298,6 +301,29 @@ def pack_q5_k(d_bits, dmin_bits, sc, m, q) -> np.ndarray:
     return out
 
 
+def pack_q6_k(d_bits, sc, q) -> np.ndarray:
+    """Q6_K super-blocks [B, 210] from fp16 d, int8 scales sc [B, 16] and
+    values q [B, 256] in 0..63 (value 128h + 32i + l: low bits in the low
+    (i < 2) or high nibble of ql[64h + 32(i % 2) + l], high bits in bits
+    2i..2i+1 of qh[32h + l])."""
+    q = np.asarray(q, dtype=np.uint8)
+    B = q.shape[0]
+    ql = np.zeros((B, 128), dtype=np.uint8)
+    qh = np.zeros((B, 64), dtype=np.uint8)
+    for h in range(2):
+        for i in range(4):
+            v = q[:, 128 * h + 32 * i: 128 * h + 32 * i + 32]
+            at = 64 * h + 32 * (i % 2)
+            ql[:, at: at + 32] |= (v & 15) << (4 if i >= 2 else 0)
+            qh[:, 32 * h: 32 * h + 32] |= ((v >> 4) & 3) << (2 * i)
+    out = np.empty((B, 210), dtype=np.uint8)
+    out[:, 0:128] = ql
+    out[:, 128:192] = qh
+    out[:, 192:208] = np.asarray(sc, dtype=np.int8).view(np.uint8)
+    out[:, 208:210] = _f16_le(np.asarray(d_bits, dtype=np.uint16))
+    return out
+
+
 # ----------------------------------------------------------------------------
 # weights and activations for one call
 
@@ -321,6 +347,13 @@ def gen_weight(wtype: int, N: int, K: int, seed: int, stream: int) -> np.ndarray
         m = uniform_int(seed, stream, nb * 8, 64, field=4).reshape(nb, 8)
         q = uniform_int(seed, stream, nb * 256, 32, field=5).reshape(nb, 256)
         return pack_q5_k(f32_to_f16_bits(d), f32_to_f16_bits(dmin), sc, m, q).reshape(-1)
+    if wtype == Q6_K:
+        # fields drawn directly: |d * sc * (q - 32)| ~ 2e-5 * 64 * 16 ~ 0.02
+        nb = N * K // 256
+        d = np.abs(normal_f32(seed, stream, nb, 2e-5, field=1))
+        sc = uniform_int(seed, stream, nb * 16, 256, field=3).reshape(nb, 16) - 128
+        q = uniform_int(seed, stream, nb * 256, 64, field=5).reshape(nb, 256)
+        return pack_q6_k(f32_to_f16_bits(d), sc, q).reshape(-1)
     if wtype in (Q4_1, Q5_0, Q5_1):
         # fields drawn directly (the pages give no workload of these types):
         # a block of N(0, 0.02) weights spans about 0.08, so d ~ 0.08 / levels

@@ -143,6 +143,35 @@ def test_q5_k_hand_superblock(golden_dir):
     assert math.fsum(float(x) for x in y) == float(kv["sum"][0])
 
 
+def _q6_k_fixture(golden_dir):
+    rows = _read(golden_dir, "q6_k_superblock.txt")
+    kv, ats, subs = {}, [], []
+    for r in rows:
+        if r[0] == "at":
+            ats.append((int(r[1]), float(r[2])))
+        elif r[0] == "subsum":
+            subs.append((int(r[1]), int(r[2]), float(r[3])))
+        else:
+            kv[r[0]] = r[1:]
+    blk = bytearray(210)
+    for x in range(128):
+        blk[x] = (x % 16) | (((x + 3) % 16) << 4)
+    for x in range(64):
+        blk[128 + x] = sum(((x + i) % 4) << (2 * i) for i in range(4))
+    blk[192:208] = bytes.fromhex(kv["scales"][0])
+    blk[208:210] = int(kv["d"][0], 16).to_bytes(2, "little")
+    return np.frombuffer(bytes(blk), dtype=np.uint8), kv, ats, subs
+
+
+def test_q6_k_hand_superblock(golden_dir):
+    W, kv, ats, subs = _q6_k_fixture(golden_dir)
+    y = oracle.decode_q6_k(W, 1, 256)[0]
+    for i, v in ats:
+        assert y[i] == np.float32(v), (i, y[i], v)
+    for lo, hi, v in subs:
+        assert math.fsum(float(x) for x in y[lo:hi]) == v
+
+
 def test_half_codes_hand_decoded(golden_dir):
     for kind, code, val in _read(golden_dir, "half_codes.txt"):
         bits = np.array([int(code, 16)], dtype=np.uint16)
@@ -216,6 +245,12 @@ def _all_ones_weight(wtype, N, K, variant=0):
             S = bytes([1, 1, 1, 1, 0x50, 0x50, 0x50, 0x50, 0x01, 0x01, 0x01, 0x01])
             blk = bytes([0x00, 0x3C, 0x00, 0x3C]) + S + bytes([0xFF]) * 32 + bytes([0x11]) * 128
         return np.frombuffer(blk * (N * K // 256), dtype=np.uint8)
+    if wtype == inputs.Q6_K:
+        # q = 33 = 0b10_0001: nibbles 1 (ql bytes 0x11), high pairs 2 (qh bytes
+        # 0xaa); d * sc * (33 - 32) = 1 with (d, sc) = (1, 1) or (0.5, 2)
+        d, sc = (bytes([0x00, 0x3C]), 1) if variant == 0 else (bytes([0x00, 0x38]), 2)
+        blk = bytes([0x11]) * 128 + bytes([0xAA]) * 64 + bytes([sc]) * 16 + d
+        return np.frombuffer(blk * (N * K // 256), dtype=np.uint8)
     if wtype == inputs.F16:
         return np.frombuffer(bytes([0x00, 0x3C]) * (N * K), dtype=np.uint8)
     if wtype == inputs.BF16:
@@ -225,7 +260,8 @@ def _all_ones_weight(wtype, N, K, variant=0):
 
 CASES = [(inputs.Q8_0, 0), (inputs.Q4_0, 0), (inputs.Q4_K, 0), (inputs.Q4_K, 1),
          (inputs.F16, 0), (inputs.BF16, 0), (inputs.Q4_1, 0), (inputs.Q5_0, 0),
-         (inputs.Q5_1, 0), (inputs.Q5_1, 1), (inputs.Q5_K, 0), (inputs.Q5_K, 1)]
+         (inputs.Q5_1, 0), (inputs.Q5_1, 1), (inputs.Q5_K, 0), (inputs.Q5_K, 1),
+         (inputs.Q6_K, 0), (inputs.Q6_K, 1)]
 
 
 @pytest.mark.parametrize("wtype,variant", CASES)
@@ -369,13 +405,24 @@ def _py_decode(wtype, raw, N, K):
                         q = ((byte >> 4) if half else (byte & 15)) + 16 * ((blk[16 + l] >> j) & 1)
                         v = np.float32(np.float32(d * sc) * q) - np.float32(dmin * m)
                         out[n][256 * b + 64 * c + 32 * half + l] = float(v)
+        elif wtype == inputs.Q6_K:
+            for b in range(K // 256):
+                blk = row[210 * b: 210 * b + 210]
+                d = _py_f16(blk[208], blk[209])
+                for v in range(256):
+                    h, rest = divmod(v, 128)
+                    i, l = divmod(rest, 32)
+                    byte = blk[64 * h + 32 * (i % 2) + l]
+                    q = ((byte >> 4) if i >= 2 else (byte & 15)) | (((blk[128 + 32 * h + l] >> (2 * i)) & 3) << 4)
+                    sc = blk[192 + v // 16] - 256 if blk[192 + v // 16] > 127 else blk[192 + v // 16]
+                    out[n][256 * b + v] = d * sc * (q - 32)
     return out
 
 
 BRUTE = [(inputs.Q8_0, 40, 64, 3), (inputs.Q4_0, 33, 96, 2), (inputs.Q4_K, 12, 512, 2),
          (inputs.F16, 24, 40, 3), (inputs.BF16, 24, 40, 3), (inputs.Q8_0, 7, 32, 1),
          (inputs.Q4_1, 21, 64, 2), (inputs.Q5_0, 19, 96, 2), (inputs.Q5_1, 17, 64, 2),
-         (inputs.Q5_K, 10, 512, 2)]
+         (inputs.Q5_K, 10, 512, 2), (inputs.Q6_K, 9, 512, 2)]
 
 
 @pytest.mark.parametrize("wtype,N,K,T", BRUTE)
@@ -452,6 +499,7 @@ def test_sizes():
     # 20 B / 32, 22 B / 32, 24 B / 32, 176 B / 256
     assert oracle.row_bytes(oracle.Q4_1, 4096) == 2560 and oracle.row_bytes(oracle.Q5_0, 4096) == 2816
     assert oracle.row_bytes(oracle.Q5_1, 4096) == 3072 and oracle.row_bytes(oracle.Q5_K, 4096) == 2816
+    assert oracle.row_bytes(oracle.Q6_K, 4096) == 3360     # 210 B / 256
 
 
 def test_q4_k_pack_roundtrip_through_oracle():
@@ -522,6 +570,22 @@ def _mut_q5_k_swapped_qh_bits(W, N, K):
     swapped = ((qh & 0x55) << 1) | ((qh & 0xAA) >> 1)
     blk[..., 16:48] = swapped.astype(np.uint8)
     return qop.decode_q5_k(blk.reshape(-1), N, K)
+
+
+def _mut_q6_k_pairs_by_parity(W, N, K):
+    """High bits from bits 2*(i % 2) instead of 2i (a plausible index slip)."""
+    blk = np.array(qop._rows(W, N, K, qop.Q6_K).reshape(N, K // 256, 210))
+    qh = blk[..., 128:192].astype(np.int64)
+    pair = lambda x, i: (x >> (2 * i)) & 3  # noqa: E731
+    fixed = pair(qh, 0) | (pair(qh, 1) << 2) | (pair(qh, 0) << 4) | (pair(qh, 1) << 6)
+    blk[..., 128:192] = fixed.astype(np.uint8)
+    return qop.decode_q6_k(blk.reshape(-1), N, K)
+
+
+def test_q6_k_mutant_is_caught(golden_dir):
+    W, kv, ats, subs = _q6_k_fixture(golden_dir)
+    y = _mut_q6_k_pairs_by_parity(W, 1, 256)[0]
+    assert any(y[i] != np.float32(v) for i, v in ats)
 
 
 def test_new_type_mutants_are_caught(golden_dir):
