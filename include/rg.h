@@ -62,9 +62,14 @@ typedef enum {
                      word = fifth bit of value i), 16 B nibbles; value d*(q-16)      */
     RG_Q5_1 = 8,  /* 24 B / 32 values: fp16 d, fp16 m, 4 B qh, 16 B nibbles;
                      value d*q + m                                                   */
-    RG_Q5_K = 9   /* 176 B / 256 values: the Q4_K header, 32 B qh (bit 2c / 2c+1 of
+    RG_Q5_K = 9,  /* 176 B / 256 values: the Q4_K header, 32 B qh (bit 2c / 2c+1 of
                      qh[l] = fifth bit of value 64c+l / 64c+32+l), 128 B nibbles;
                      value d*sc*q - dmin*m                                           */
+    RG_Q6_K = 10  /* 210 B / 256 values: ql[128] low nibbles, qh[64] bit pairs,
+                     int8 scales[16], fp16 d; value d*sc[v/16]*(q-32).  Rows of
+                     210*K/256 bytes are 16-byte aligned only when K % 2048 == 0,
+                     which the tensor-core and small-T variants need (else
+                     RG_ERR_SHAPE; RG_VARIANT_AUTO then runs the SIMT variant)   */
 } rg_wtype;
 
 typedef enum {

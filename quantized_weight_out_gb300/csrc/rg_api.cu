@@ -116,8 +116,12 @@ int validate(int wtype, const void* W, int64_t N, int64_t K, const float* dY, in
   return RG_OK;
 }
 
+// Q6_K rows (210 * K / 256 bytes) are 16-byte aligned, as the tensor-core and
+// small-T kernels' copies need, only when K is a multiple of 2048.
+bool aligned_rows(int wtype, int64_t K) { return wtype != RG_Q6_K || K % 2048 == 0; }
+
 int select_variant(int wtype, int64_t N, int64_t K, int64_t T) {
-  (void)wtype;
+  if (!aligned_rows(wtype, K)) return RG_VARIANT_SIMT32;
   // a few rows of dY, or a problem too small to fill a tensor-core pipeline:
   // the weight-streaming SIMT kernel; else the tensor cores (which split the
   // contraction over idle SMs when the output is small)
@@ -217,6 +221,7 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
   if ((st = current_dev(&dev)) != RG_OK) return st;
   if (N == 0) return from_cuda(launch_scale(dX, T * K, beta, *dev, stream));
   if (variant == RG_VARIANT_AUTO) variant = select_variant(wtype, N, K, T);
+  if (variant != RG_VARIANT_SIMT32 && !aligned_rows(wtype, K)) return RG_ERR_SHAPE;
 
   if (variant == RG_VARIANT_SIMT32)
     return from_cuda(launch_simt32(wtype, W, N, K, dY, T, dX, beta, *dev, stream));
@@ -440,6 +445,8 @@ int rg_plan(int variant, int wtype, int64_t N, int64_t K, int64_t T, rg_plan_inf
   if (st != RG_OK) return st;
   rg_plan_info r{};
   r.variant = variant == RG_VARIANT_AUTO ? select_variant(wtype, N, K, T) : variant;
+  if (r.variant != RG_VARIANT_SIMT32 && !aligned_rows(wtype, K) && T > 0 && K > 0 && N > 0)
+    return RG_ERR_SHAPE;
   r.n_splits = 1;
   if (T == 0 || K == 0 || N == 0) {
     r.launches = (T == 0 || K == 0) ? 0 : 1;

@@ -73,6 +73,26 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
   }
 }
 
+// Q6_K rows (210 bytes per 256 values) are not 16-byte aligned in general:
+// one thread per 8 values, reading its bytes directly.
+template <int WT>
+__global__ void __launch_bounds__(256) dequant_bytes_kernel(const uint8_t* __restrict__ W, int64_t N,
+                                                            int64_t K, int64_t rb,
+                                                            float* __restrict__ out) {
+  const int64_t gpr = K >> 3;  // 8-value groups per row
+  const int64_t total = N * gpr;
+  for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t n = g / gpr;
+    const int k0 = static_cast<int>(g - n * gpr) << 3;
+    float v[8];
+    decode8_f32<WT>(W + n * rb, k0, v);
+    float4* o = reinterpret_cast<float4*>(out + n * K + k0);
+    __stcs(o, make_float4(v[0], v[1], v[2], v[3]));
+    __stcs(o + 1, make_float4(v[4], v[5], v[6], v[7]));
+  }
+}
+
 static int grid_for(int64_t work_items, int threads, const DevInfo& dev) {
   const int64_t blocks = (work_items + threads - 1) / threads;
   const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
@@ -85,7 +105,11 @@ cudaError_t launch_dequant(int wtype, const void* W, int64_t N, int64_t K, float
   const int grid = grid_for((N + DQ_U - 1) / DQ_U * ((K + 255) >> 8) * 32, 256, dev);
   const uint8_t* w = static_cast<const uint8_t*>(W);
   return with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
-    dequant_kernel<decltype(wt)::value><<<grid, 256, 0, stream>>>(w, N, K, rb, out);
+    constexpr int WT = decltype(wt)::value;
+    if constexpr (WT == RG_Q6_K)
+      dequant_bytes_kernel<WT><<<grid_for(N * (K >> 3), 256, dev), 256, 0, stream>>>(w, N, K, rb, out);
+    else
+      dequant_kernel<WT><<<grid, 256, 0, stream>>>(w, N, K, rb, out);
     return counted(cudaGetLastError());
   });
 }

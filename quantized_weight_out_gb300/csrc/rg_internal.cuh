@@ -19,16 +19,17 @@ namespace rg {
 // ---------------------------------------------------------------------------
 // storage formats: values per block, bytes per block
 
-__host__ __device__ constexpr bool valid_wtype(int wt) { return wt >= RG_F16 && wt <= RG_Q5_K; }
+__host__ __device__ constexpr bool valid_wtype(int wt) { return wt >= RG_F16 && wt <= RG_Q6_K; }
 __host__ __device__ constexpr bool is_quant(int wt) {
   return valid_wtype(wt) && wt != RG_F16 && wt != RG_BF16;
 }
 __host__ __device__ constexpr int block_values(int wt) {
-  return (wt == RG_Q4_K || wt == RG_Q5_K) ? 256 : is_quant(wt) ? 32 : 1;
+  return (wt == RG_Q4_K || wt == RG_Q5_K || wt == RG_Q6_K) ? 256 : is_quant(wt) ? 32 : 1;
 }
 __host__ __device__ constexpr int block_bytes(int wt) {
   return wt == RG_Q4_K   ? 144
          : wt == RG_Q5_K ? 176
+         : wt == RG_Q6_K ? 210
          : wt == RG_Q8_0 ? 34
          : wt == RG_Q4_0 ? 18
          : wt == RG_Q4_1 ? 20
@@ -432,6 +433,21 @@ __device__ __forceinline__ void decode8_f32(const uint8_t* row, int k0, float (&
         // exact product, one rounding of the sum
         out[i] = fmaf(d, static_cast<float>(q), f16_to_f32(ld_u16(blk + 2)));
       }
+    }
+  } else if constexpr (WT == RG_Q6_K) {
+    // value v = 128h + 32i + l: nibble of ql[64h + 32(i%2) + l] (high for
+    // i >= 2), bits 2i..2i+1 of qh[32h + l]; (d * sc) * (q - 32) is exact
+    const uint8_t* blk = row + (k0 >> 8) * 210;
+    const int v0 = k0 & 255;
+    const int h = v0 >> 7, i = (v0 >> 5) & 3, l0 = v0 & 31;
+    const uint8_t* ql = blk + 64 * h + 32 * (i & 1) + l0;
+    const uint8_t* qh = blk + 128 + 32 * h + l0;
+    const float ds = f16_to_f32(ld_u16(blk + 208)) *
+                     static_cast<float>(static_cast<int8_t>(blk[192 + (v0 >> 4)]));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int q = ((i >= 2 ? (ql[j] >> 4) : ql[j]) & 15) | (((qh[j] >> (2 * i)) & 3) << 4);
+      out[j] = ds * static_cast<float>(q - 32);
     }
   } else if constexpr (WT == RG_Q5_K) {
     const uint8_t* blk = row + (k0 >> 8) * 176;

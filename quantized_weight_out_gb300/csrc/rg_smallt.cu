@@ -28,7 +28,7 @@ constexpr int THREADS = 256;   // 8 consumer warps (plus one producer warp)
 // Raw bytes one lane needs from a row for its 8 values (a 256-value tile).
 template <int WT>
 struct Raw {
-  uint32_t v[WT == RG_Q5_K ? 8 : WT == RG_Q4_K ? 6 : (WT == RG_Q8_0 || WT == RG_Q4_0 || WT == RG_Q4_1) ? 3 : 4];
+  uint32_t v[WT == RG_Q5_K ? 8 : WT == RG_Q4_K ? 6 : WT == RG_Q6_K ? 5 : (WT == RG_Q8_0 || WT == RG_Q4_0 || WT == RG_Q4_1) ? 3 : 4];
 };
 
 // The bytes one lane needs for its 8 values, from a row tile staged in
@@ -67,6 +67,18 @@ __device__ __forceinline__ void load_raw_smem(const uint8_t* tile, int lane, Raw
     r.v[1] = *reinterpret_cast<const uint32_t*>(blk + 4);  // qh
     r.v[2] = q.x;
     r.v[3] = q.y;
+  } else if constexpr (WT == RG_Q6_K) {
+    // values 8*lane .. +7 = 128h + 32i + l0 .. +7 (tile: the super-block's
+    // first byte, 2-byte aligned): 8 bytes of ql, 8 of qh, one scale, d
+    const int h = lane >> 4, i = (lane >> 2) & 3, l0 = 8 * (lane & 3);
+    const uint16_t* ql = reinterpret_cast<const uint16_t*>(tile + 64 * h + 32 * (i & 1) + l0);
+    const uint16_t* qh = reinterpret_cast<const uint16_t*>(tile + 128 + 32 * h + l0);
+    r.v[0] = static_cast<uint32_t>(ql[0]) | (static_cast<uint32_t>(ql[1]) << 16);
+    r.v[1] = static_cast<uint32_t>(ql[2]) | (static_cast<uint32_t>(ql[3]) << 16);
+    r.v[2] = static_cast<uint32_t>(qh[0]) | (static_cast<uint32_t>(qh[1]) << 16);
+    r.v[3] = static_cast<uint32_t>(qh[2]) | (static_cast<uint32_t>(qh[3]) << 16);
+    r.v[4] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tile + 208)) |
+             (static_cast<uint32_t>(tile[192 + (lane >> 1)]) << 16);
   } else {
     // Q4_K, Q5_K: the header, this lane's 8 bytes of nibbles (and of qh)
     constexpr int QS = WT == RG_Q5_K ? 48 : 16;
@@ -119,6 +131,20 @@ __device__ __forceinline__ void decode_raw(const Raw<WT>& r, int lane, float (&w
       w[4 * j + 1] = d * byte_minus<1>(x, kTwo23 + 8.0f);
       w[4 * j + 2] = d * byte_minus<2>(x, kTwo23 + 8.0f);
       w[4 * j + 3] = d * byte_minus<3>(x, kTwo23 + 8.0f);
+    }
+  } else if constexpr (WT == RG_Q6_K) {
+    // (d * sc) * (q - 32), every step exact
+    const int i = (lane >> 2) & 3;
+    const float ds = f16_to_f32(static_cast<uint16_t>(r.v[4] & 0xFFFFu)) *
+                     static_cast<float>(static_cast<int8_t>((r.v[4] >> 16) & 0xFFu));
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const uint32_t x = ((r.v[jj] >> (i >= 2 ? 4 : 0)) & 0x0F0F0F0Fu) |
+                         (((r.v[2 + jj] >> (2 * i)) & 0x03030303u) << 4);
+      w[4 * jj + 0] = ds * byte_minus<0>(x, kTwo23 + 32.0f);
+      w[4 * jj + 1] = ds * byte_minus<1>(x, kTwo23 + 32.0f);
+      w[4 * jj + 2] = ds * byte_minus<2>(x, kTwo23 + 32.0f);
+      w[4 * jj + 3] = ds * byte_minus<3>(x, kTwo23 + 32.0f);
     }
   } else if constexpr (WT == RG_Q4_1 || WT == RG_Q5_0 || WT == RG_Q5_1) {
     // values 8(lane & 3) .. +7 of block lane >> 2: nibbles (low for the
@@ -176,6 +202,25 @@ __device__ __forceinline__ void decode_raw(const Raw<WT>& r, int lane, float (&w
 
 // Bytes of one row's 256-value tile.
 template <int WT>
+__host__ __device__ constexpr int tile_bytes();
+
+// Bytes a stage holds per row: the 256-value tile, except Q6_K, whose 210-byte
+// super-blocks start at any even offset of a 16-byte grain: a 224-byte
+// window from the grain before (window_offset bytes in).
+template <int WT>
+__host__ __device__ constexpr int stage_row_bytes() {
+  return WT == RG_Q6_K ? 224 : tile_bytes<WT>();
+}
+template <int WT>
+__host__ __device__ constexpr int64_t window_start(int64_t kt) {
+  return WT == RG_Q6_K ? ((kt * 210) & ~int64_t{15}) : kt * tile_bytes<WT>();
+}
+template <int WT>
+__host__ __device__ constexpr int window_offset(int64_t kt) {
+  return WT == RG_Q6_K ? static_cast<int>((kt * 210) & 15) : 0;
+}
+
+template <int WT>
 __host__ __device__ constexpr int tile_bytes() {
   return (256 / block_values(WT)) * block_bytes(WT);
 }
@@ -184,7 +229,7 @@ __host__ __device__ constexpr int tile_bytes() {
 // rows per stage (two per lane) in a 4-deep ring; the row-per-warp consumers
 // 32 rows in an 8-deep ring: the same bytes in flight either way.
 template <int WT, int TB>
-constexpr bool rows_path() { return TB <= 2 && is_quant(WT); }
+constexpr bool rows_path() { return TB <= 2 && is_quant(WT) && WT != RG_Q6_K; }
 template <int WT, int TB>
 constexpr int stage_rows() { return rows_path<WT, TB>() ? 64 : 32; }
 template <int WT, int TB>
@@ -459,7 +504,7 @@ __global__ void __launch_bounds__(THREADS + 32, rows_path<WT, TB>() && TB == 1 ?
     smallt_kernel(const __grid_constant__ CUtensorMap map_w, int N, int K,
                   const float* __restrict__ dY, int T, float* __restrict__ part,
                   int rows_per_split, WaitCtl ctl) {
-  constexpr int TBYTES = tile_bytes<WT>();
+  constexpr int TBYTES = stage_row_bytes<WT>();
   constexpr int BR = stage_rows<WT, TB>(), STAGES = n_stages<WT, TB>();
   extern __shared__ __align__(128) uint8_t sm[];
   uint8_t* stage_buf = sm;                                              // STAGES x BR x TBYTES
@@ -507,7 +552,8 @@ __global__ void __launch_bounds__(THREADS + 32, rows_path<WT, TB>() && TB == 1 ?
         const int s = i % STAGES;
         if (!mbar_wait(empty(s), ph ^ 1u, ctl, abort_flag)) break;
         mbar_arrive_expect_tx(full(s), BR * TBYTES);
-        tma_load_2d(smem_addr(stage_buf + s * BR * TBYTES), &map_w, full(s), kt * (TBYTES / 4),
+        tma_load_2d(smem_addr(stage_buf + s * BR * TBYTES), &map_w, full(s),
+                    static_cast<int>(window_start<WT>(kt) / 4),
                     nbeg + i * BR);
         if (s == STAGES - 1) ph ^= 1u;
       }
@@ -540,7 +586,7 @@ __global__ void __launch_bounds__(THREADS + 32, rows_path<WT, TB>() && TB == 1 ?
                                              abort_flag)))
         break;
       if (kvalid) {
-        const uint8_t* tile = stage_buf + s * BR * TBYTES;
+        const uint8_t* tile = stage_buf + s * BR * TBYTES + window_offset<WT>(kt);
         Raw<WT> raw[BR / CONSUMERS];
 #pragma unroll
         for (int u = 0; u < BR / CONSUMERS; ++u) load_raw_smem<WT>(tile + (warp + CONSUMERS * u) * TBYTES, lane, raw[u]);
@@ -593,7 +639,7 @@ __global__ void __launch_bounds__(THREADS + 32, rows_path<WT, TB>() && TB == 1 ?
 
 template <int WT, int TB>
 constexpr size_t smem_bytes() {
-  return static_cast<size_t>(n_stages<WT, TB>()) * stage_rows<WT, TB>() * tile_bytes<WT>() +
+  return static_cast<size_t>(n_stages<WT, TB>()) * stage_rows<WT, TB>() * stage_row_bytes<WT>() +
          sizeof(float) * TB * MAX_ROWS + (rows_path<WT, TB>() ? 0 : sizeof(float) * 4 * TB * 256) +
          16 * n_stages<WT, TB>();
 }
@@ -734,7 +780,7 @@ static cudaError_t launch_smallt_t(const void* W, int64_t N, int64_t K, const fl
   const uint64_t rb = static_cast<uint64_t>(K / block_values(WT) * block_bytes(WT));
   CUtensorMap map;
   if (encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rb / 4, static_cast<uint64_t>(N), rb,
-                   smt::tile_bytes<WT>() / 4, smt::stage_rows<WT, TB>(),
+                   smt::stage_row_bytes<WT>() / 4, smt::stage_rows<WT, TB>(),
                    CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(p.n_ktiles), static_cast<unsigned>(p.n_splits),

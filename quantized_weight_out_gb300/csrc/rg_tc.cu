@@ -55,7 +55,10 @@ constexpr int SMEM_BUDGET = 224 * 1024;
 // Q8_0 4 blocks = 136 B inside a 144 B window, Q4_0 72 B inside 80 B, Q4_1
 // exactly 80 B, Q5_0 88 B and Q5_1 96 B inside 112 B (the wider row stride
 // puts eight consecutive rows in distinct shared-memory bank groups), Q4_K
-// and Q5_K the whole super-block (its header holds every sub-block's scale).
+// and Q5_K the whole super-block (its header holds every sub-block's scale),
+// Q6_K the whole 210-byte super-block inside a 240-byte window that starts at
+// the 16-byte grain before it (0..14 bytes in; 15 chunks keep eight rows in
+// distinct bank groups).
 template <int WT>
 __host__ __device__ constexpr int p_row_bytes() {
   return WT == RG_Q8_0   ? 144
@@ -65,6 +68,7 @@ __host__ __device__ constexpr int p_row_bytes() {
          : WT == RG_Q5_0 ? 112
          : WT == RG_Q5_1 ? 112
          : WT == RG_Q5_K ? 176
+         : WT == RG_Q6_K ? 240
                          : 0;
 }
 
@@ -75,8 +79,8 @@ struct Cfg {
   static constexpr int P_STAGE = QUANT ? ((BC * p_row_bytes<WT>() + 1023) / 1024) * 1024 : 0;
   static constexpr int STAGE = A_STAGE + B_STAGE + P_STAGE;
   // quantized: five slots, each decoded by two warps; F16/BF16: as deep as fits
-  static constexpr int S = QUANT ? 5 : std::min(8, SMEM_BUDGET / STAGE);
-  static constexpr int WARPS_PER_SLOT = QUANT ? DEC_WARPS / S : 0;
+  static constexpr int S = QUANT ? (WT == RG_Q6_K ? 4 : 5) : std::min(8, SMEM_BUDGET / STAGE);
+  static constexpr int WARPS_PER_SLOT = QUANT ? 2 : 0;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + S * A_STAGE;
   static constexpr int OFF_P = OFF_B + S * B_STAGE;
@@ -97,7 +101,7 @@ struct Cfg {
   static constexpr uint32_t ACC_EMPTY_COUNT = 4 * CG;
   static_assert(BT / CG == B_ROWS, "each CTA holds 128 rows of t in a B stage");
   static_assert(S >= 3, "pipeline depth");
-  static_assert(!QUANT || S * WARPS_PER_SLOT == DEC_WARPS, "decoder warps split evenly over slots");
+  static_assert(!QUANT || S * WARPS_PER_SLOT <= DEC_WARPS, "decoder warps cover the slots");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -349,6 +353,55 @@ __device__ __forceinline__ void dec_q5_k_part(const uint8_t* row, uint8_t* A, in
   st_a_chunk(A, n, cb + 5, hi[4], hi[5], hi[6], hi[7]);
 }
 
+// Q6_K: a whole row's half (128 values, H = the half) from a window whose
+// super-block starts O bytes in.  Value 128H + 32i + l: nibble of
+// ql[64H + 32(i%2) + l] (high for i >= 2) and bits 2i..2i+1 of qh[32H + l]
+// give q; the operand is fp16(d * sc[8H + 2i + l/16]) * (q - 32).
+template <int O, int H>
+__device__ __forceinline__ void dec_q6_k_row(const uint8_t* row, uint8_t* A, int n) {
+  constexpr int QA = O + 64 * H, QHB = O + 128 + 32 * H, QS = O + 192 + 8 * H, QD = O + 208;
+  // the last byte a word_at at offset x (relative to chunk C) reads
+  constexpr auto last = [](int x) { return (x & 3) == 0 ? x + 3 : (x & ~3) + 7; };
+  constexpr int CA = QA / 16, CA1 = CA + last(QA - 16 * CA + 60) / 16;
+  constexpr int CH = QHB / 16, CH1 = CH + last(QHB - 16 * CH + 28) / 16;
+  constexpr int CS = QS / 16, CS1 = (QD + 1) / 16;
+  static_assert(16 * CA1 + 16 <= p_row_bytes<RG_Q6_K>() && 16 * CH1 + 16 <= p_row_bytes<RG_Q6_K>() &&
+                    16 * CS1 + 16 <= p_row_bytes<RG_Q6_K>(),
+                "reads stay inside the row window");
+  const auto ra = load_chunks<CA, CA1>(row);
+  const auto rh = load_chunks<CH, CH1>(row);
+  const auto rs = load_chunks<CS, CS1>(row);
+  constexpr int XA = QA - 16 * CA, XH = QHB - 16 * CH, XS = QS - 16 * CS, XD = QD - 16 * CS;
+  const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(rs.word_at(XD) & 0xFFFFu)));
+  __half2 ds[4][2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int is = 0; is < 2; ++is) {
+      const int sc = static_cast<int8_t>(rs.word_at(XS + 2 * i + is) & 0xFFu);
+      ds[i][is] = __float2half2_rn(d * static_cast<float>(sc));  // exact product, one rounding
+    }
+  const __half2 off = __float2half2_rn(1056.0f);  // 1024 + 32
+#pragma unroll
+  for (int cq = 0; cq < 4; ++cq) {  // l = 8cq .. 8cq+7
+    uint32_t o[4][4];
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const int j = 2 * cq + jj;  // l = 4j .. 4j+3
+      const uint32_t a = ra.word_at(XA + 4 * j), b = ra.word_at(XA + 32 + 4 * j);
+      const uint32_t hq = rh.word_at(XH + 4 * j);
+      const uint32_t x[4] = {(a & 0x0F0F0F0Fu) | ((hq & 0x03030303u) << 4),
+                             (b & 0x0F0F0F0Fu) | (((hq >> 2) & 0x03030303u) << 4),
+                             ((a >> 4) & 0x0F0F0F0Fu) | (((hq >> 4) & 0x03030303u) << 4),
+                             ((b >> 4) & 0x0F0F0F0Fu) | (((hq >> 6) & 0x03030303u) << 4)};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) four_scaled(x[i], off, ds[i][cq >> 1], o[i][2 * jj], o[i][2 * jj + 1]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) st_a_chunk(A, n, 4 * i + cq, o[i][0], o[i][1], o[i][2], o[i][3]);
+  }
+}
+
 // Block b (32-value types) or part b (Q4_K, Q5_K: chunk b >> 1 of the
 // half, 16 bytes b & 1) of row n of a stage.
 template <int WT, int ODD, int B>
@@ -368,10 +421,16 @@ __device__ __forceinline__ void dec_item(const uint8_t* row, uint8_t* A, int n) 
 // eight independent blocks per lane, and the lanes of a load or store sit on
 // consecutive rows, i.e. in distinct bank groups.  ODD = the tile's k index is
 // odd (window offset 8 for Q8_0 / Q4_0, second half of a Q4_K super-block).
-template <int WT, int ODD, int NPART>
+template <int WT, int ODD, int NPART, int O = 0>
 __device__ __forceinline__ void decode_stage_warp(const uint8_t* __restrict__ P,
                                                   uint8_t* __restrict__ A, int lane, int part) {
   constexpr int PR = p_row_bytes<WT>();
+  if constexpr (WT == RG_Q6_K) {
+    static_assert(NPART == 2, "a lane decodes one row's half");
+    const int n = lane + 32 * part;
+    dec_q6_k_row<O, ODD>(P + n * PR, A, n);
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     if ((i & (NPART - 1)) != part) continue;  // this warp's share of the items
@@ -395,6 +454,7 @@ __device__ __forceinline__ int p_window_start(int kt) {
   if constexpr (WT == RG_Q5_0) return (kt * 88) & ~15;
   if constexpr (WT == RG_Q5_1) return kt * 96;
   if constexpr (WT == RG_Q5_K) return (kt >> 1) * 176;
+  if constexpr (WT == RG_Q6_K) return ((kt >> 1) * 210) & ~15;
   return (kt >> 1) * 144;  // Q4_K: the whole super-block
 }
 
@@ -638,7 +698,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr int WPS = C::WARPS_PER_SLOT;
       const int s = (warp - DEC_WARP0) / WPS;
       const int part = (warp - DEC_WARP0) % WPS;
-      {
+      if (s < S) {  // (Q6_K's four slots leave two decoder warps idle)
         // a follower's warps arrive on the issuing CTA's barrier directly
         const uint32_t done_bar = CG == 2 ? mapa_shared(full_dec(s), 0) : full_dec(s);
         const int total = ((n_tiles - unit + n_units - 1) / n_units) * n_chunks;  // stages of this CTA
@@ -651,10 +711,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int g = s; g < total; g += S, ph ^= 1u) {
           const int kt = ku * CG + static_cast<int>(rank);
           if (!__all_sync(0xffffffffu, mbar_wait(full_p(s), ph, ctl, abort_flag))) break;
-          if (kt & 1)
+          if constexpr (WT == RG_Q6_K) {
+            // the super-block starts o bytes into its window: one decoder per o
+            const int o = ((kt >> 1) * 210) & 15;
+            const uint8_t* P = sP + s * C::P_STAGE;
+            uint8_t* Ad = sA + s * A_STAGE;
+#define RG_Q6K_CASE(OO)                                                          \
+  case OO / 2:                                                                   \
+    if (kt & 1) decode_stage_warp<WT, 1, WPS, OO>(P, Ad, lane, part);            \
+    else decode_stage_warp<WT, 0, WPS, OO>(P, Ad, lane, part);                   \
+    break;
+            switch (o >> 1) {
+              RG_Q6K_CASE(0) RG_Q6K_CASE(2) RG_Q6K_CASE(4) RG_Q6K_CASE(6)
+              RG_Q6K_CASE(8) RG_Q6K_CASE(10) RG_Q6K_CASE(12) RG_Q6K_CASE(14)
+              default: break;
+            }
+#undef RG_Q6K_CASE
+          } else if (kt & 1) {
             decode_stage_warp<WT, 1, WPS>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part);
-          else
+          } else {
             decode_stage_warp<WT, 0, WPS>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part);
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {

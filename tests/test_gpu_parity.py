@@ -33,6 +33,14 @@ def _dev():
     return torch.device("cuda:0")
 
 
+def kfit(wtype, K, variant):
+    """Q6_K rows are 16-byte aligned only for K % 2048 == 0, which every
+    variant but the SIMT one needs: round K up for those."""
+    if wtype == inputs.Q6_K and variant != 3:
+        return -(-K // 2048) * 2048
+    return K
+
+
 def run_out_prod(rg, variant, wtype, W, N, K, dY, T, dX0=None, beta=0.0, fill=float("nan")):
     dev = _dev()
     Wd = torch.from_numpy(np.ascontiguousarray(W)).to(dev)
@@ -105,6 +113,7 @@ SHAPES = [  # (N, K, T): N ragged against the 64-row stage, T against 128/256-ro
 @pytest.mark.parametrize("shape", SHAPES)
 def test_out_prod_parity(rg, variant, wtype, shape):
     N, K, T = shape
+    K = kfit(wtype, K, variant)
     W = inputs.gen_weight(wtype, N, K, seed=3, stream=1)
     dY = inputs.normal_f32(3, 2, T * N, 1e-3).reshape(T, N)
     Wd = oracle.dequant(wtype, W, N, K)
@@ -143,7 +152,7 @@ def test_beta_zero_ignores_nan(rg, variant):
 @pytest.mark.parametrize("wtype", TYPES)
 def test_one_hot_f32_variants_equal_rows(rg, variant, wtype):
     """F32 variants: one-hot dY reproduces rows of deq(W) exactly."""
-    N, K, T = 80, 512, 6
+    N, K, T = 80, kfit(wtype, 512, variant), 6
     W = inputs.gen_weight(wtype, N, K, seed=6, stream=1)
     Wd = oracle.dequant(wtype, W, N, K)
     n0 = [(13 * t + 5) % N for t in range(T)]
@@ -159,7 +168,7 @@ def test_one_hot_f32_variants_equal_rows(rg, variant, wtype):
 def test_all_ones_closed_form_tc(rg, variant, wtype):
     """All-ones weight times one-hot dY gives exactly 1 on the tensor cores too."""
     from test_oracle import _all_ones_weight
-    N, K, T = 128, 512, 260
+    N, K, T = 128, kfit(wtype, 512, variant), 260
     W = _all_ones_weight(wtype, N, K).copy()
     dY = np.zeros((T, N), np.float32)
     dY[np.arange(T), (7 * np.arange(T) + 3) % N] = 1.0
@@ -233,7 +242,7 @@ def test_timeout_probe_reports_and_context_survives(rg):
 def test_split_contraction(rg, variant, wtype, beta):
     """Few output tiles and a long contraction: the tensor-core kernel splits
     the rows of W over CTAs and a second kernel adds the partial tiles."""
-    N, K, T = 2050, 512, 100        # ragged N: the last split runs past the end of W
+    N, K, T = 2050, kfit(wtype, 512, variant), 100  # ragged N: the last split runs past W's end
     W = inputs.gen_weight(wtype, N, K, seed=31, stream=1)
     dY = inputs.normal_f32(31, 2, T * N, 1e-3).reshape(T, N)
     dX0 = inputs.normal_f32(31, 3, T * K, 1e-3).reshape(T, K) if beta else None
@@ -243,6 +252,26 @@ def test_split_contraction(rg, variant, wtype, beta):
     got = run_out_prod(rg, variant, wtype, W, N, K, dY, T, dX0, beta)
     extra = np.abs(beta * dX0) * 2.0 ** -24 / 5e-3 if beta else 0.0
     assert_within(got, ref, bnd + extra, 5e-3, f"split variant {variant} type {wtype}")
+
+
+def test_q6_k_unaligned_rows(rg):
+    """K % 2048 != 0: the tensor-core and small-T variants refuse the shape
+    (nothing launched), and the dispatcher runs the SIMT variant instead."""
+    N, K, T = 70, 768, 40                 # rows of 630 bytes: only 2-byte aligned
+    W = inputs.gen_weight(inputs.Q6_K, N, K, seed=41, stream=1)
+    dY = inputs.normal_f32(41, 2, T * N, 1e-3).reshape(T, N)
+    dev, s = _dev(), torch.cuda.current_stream()
+    Wt, dYt = torch.from_numpy(W).to(dev), torch.from_numpy(dY).to(dev)
+    dX = torch.full((T, K), 3.0, device=dev)
+    for v in (1, 2, 4, 5):
+        assert rg.rg_out_prod_variant(v, inputs.Q6_K, Wt, N, K, dYt, T, dX, 0.0, s) == rg.RG_ERR_SHAPE
+    torch.cuda.synchronize()
+    assert bool(torch.all(dX == 3.0))
+    assert rg.rg_select_variant(inputs.Q6_K, N, K, T) == rg.RG_VARIANT_SIMT32
+    got = run_out_prod(rg, 0, inputs.Q6_K, W, N, K, dY, T)
+    Wd = oracle.dequant(inputs.Q6_K, W, N, K)
+    assert_within(got, oracle.out_prod(inputs.Q6_K, W, N, K, dY, T, Wd=Wd),
+                  oracle.abs_bound(dY, Wd), 1e-5, "q6_k simt")
 
 
 # ----------------------------------------------------------------------------
