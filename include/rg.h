@@ -31,9 +31,10 @@
  *  - Sizes: 0 <= T, N, K <= 2^31 - 1.  T == 0 or K == 0 is an empty output
  *    (RG_OK, nothing launched, pointers may be NULL).  N == 0 is an empty
  *    contraction: dX = beta * dX (dX = 0 when beta == 0).
- *  - K must be a multiple of 256 for Q8_0, Q4_0 and Q4_K (whole 256-value
+ *  - K must be a multiple of 256 for the quantized types (whole 256-value
  *    tiles of every block type) and a multiple of 8 for F16 and BF16
- *    (16-byte rows); otherwise RG_ERR_SHAPE.
+ *    (16-byte rows); otherwise RG_ERR_SHAPE.  Q6_K on the tensor-core and
+ *    small-T variants also needs K % 2048 == 0 (16-byte aligned rows).
  *  - Every device-side wait is bounded (about 2 s); a wait that gives up
  *    records RG_ERR_TIMEOUT in a per-device status word that rg_check reads.
  */
@@ -76,7 +77,8 @@ typedef enum {
     RG_OK = 0,
     RG_ERR_ARG = -1,     /* NULL pointer where data is needed, negative or too large size */
     RG_ERR_TYPE = -2,    /* unknown wtype, or unknown variant                              */
-    RG_ERR_SHAPE = -3,   /* K not a multiple of 256 (quantized) or 8 (F16/BF16)            */
+    RG_ERR_SHAPE = -3,   /* K not a multiple of 256 (quantized) or 8 (F16/BF16); Q6_K with
+                            K % 2048 != 0 on a tensor-core or small-T variant               */
     RG_ERR_ALIGN = -4,   /* W, dY, dX or out not 16-byte aligned                           */
     RG_ERR_CUDA = -5,    /* a CUDA runtime/driver call or a launch failed                  */
     RG_ERR_TIMEOUT = -6  /* a bounded device-side wait gave up (reported by rg_check)      */
@@ -213,8 +215,9 @@ int rg_dequant(int wtype, const void* W, int64_t N, int64_t K, float* out);
 int rg_dequant_async(int wtype, const void* W, int64_t N, int64_t K, float* out, void* stream);
 
 /* Stored bytes of one row of K values: K/32*34 (Q8_0), K/32*18 (Q4_0),
- * K/256*144 (Q4_K), 2K (F16, BF16); 0 for an unknown type or a K that is not
- * a whole number of blocks. */
+ * K/32*20 (Q4_1), K/32*22 (Q5_0), K/32*24 (Q5_1), K/256*144 (Q4_K),
+ * K/256*176 (Q5_K), K/256*210 (Q6_K), 2K (F16, BF16); 0 for an unknown type
+ * or a K that is not a whole number of blocks. */
 size_t rg_row_bytes(int wtype, int64_t K);
 
 /* Static, NUL-terminated description of a status code. */
