@@ -32,7 +32,7 @@
  *    (RG_OK, nothing launched, pointers may be NULL).  N == 0 is an empty
  *    contraction: dX = beta * dX (dX = 0 when beta == 0).
  *  - K must be a multiple of 256 for the quantized types (whole 256-value
- *    tiles of every block type) and a multiple of 8 for F16 and BF16
+ *    tiles of every block type) and a multiple of 8 for F32, F16 and BF16
  *    (16-byte rows); otherwise RG_ERR_SHAPE.  Q6_K on the tensor-core and
  *    small-T variants also needs K % 2048 == 0 (16-byte aligned rows).
  *  - Every device-side wait is bounded (about 2 s); a wait that gives up
@@ -66,18 +66,21 @@ typedef enum {
     RG_Q5_K = 9,  /* 176 B / 256 values: the Q4_K header, 32 B qh (bit 2c / 2c+1 of
                      qh[l] = fifth bit of value 64c+l / 64c+32+l), 128 B nibbles;
                      value d*sc*q - dmin*m                                           */
-    RG_Q6_K = 10  /* 210 B / 256 values: ql[128] low nibbles, qh[64] bit pairs,
+    RG_Q6_K = 10, /* 210 B / 256 values: ql[128] low nibbles, qh[64] bit pairs,
                      int8 scales[16], fp16 d; value d*sc[v/16]*(q-32).  Rows of
                      210*K/256 bytes are 16-byte aligned only when K % 2048 == 0,
                      which the tensor-core and small-T variants need (else
                      RG_ERR_SHAPE; RG_VARIANT_AUTO then runs the SIMT variant)   */
+    RG_F32 = 11   /* IEEE binary32, 4 B per value.  The tensor-core variants round W
+                     and dY to bf16 (F32 range, relative error at most 2^-9 each)
+                     in the workspace; the other variants use the F32 values    */
 } rg_wtype;
 
 typedef enum {
     RG_OK = 0,
     RG_ERR_ARG = -1,     /* NULL pointer where data is needed, negative or too large size */
     RG_ERR_TYPE = -2,    /* unknown wtype, or unknown variant                              */
-    RG_ERR_SHAPE = -3,   /* K not a multiple of 256 (quantized) or 8 (F16/BF16); Q6_K with
+    RG_ERR_SHAPE = -3,   /* K not a multiple of 256 (quantized) or 8 (F32/F16/BF16); Q6_K with
                             K % 2048 != 0 on a tensor-core or small-T variant               */
     RG_ERR_ALIGN = -4,   /* W, dY, dX or out not 16-byte aligned                           */
     RG_ERR_CUDA = -5,    /* a CUDA runtime/driver call or a launch failed                  */
@@ -216,7 +219,7 @@ int rg_dequant_async(int wtype, const void* W, int64_t N, int64_t K, float* out,
 
 /* Stored bytes of one row of K values: K/32*34 (Q8_0), K/32*18 (Q4_0),
  * K/32*20 (Q4_1), K/32*22 (Q5_0), K/32*24 (Q5_1), K/256*144 (Q4_K),
- * K/256*176 (Q5_K), K/256*210 (Q6_K), 2K (F16, BF16); 0 for an unknown type
+ * K/256*176 (Q5_K), K/256*210 (Q6_K), 2K (F16, BF16), 4K (F32); 0 for an unknown type
  * or a K that is not a whole number of blocks. */
 size_t rg_row_bytes(int wtype, int64_t K);
 

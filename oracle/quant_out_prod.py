@@ -44,6 +44,7 @@ Block formats (little-endian), ggml's GGUF block types:
                    and bits 2i..2i+1 of qh[32h + l] as bits 4..5;
                                                   y = (d*sc[v/16]) * (q - 32)
 * F16 / BF16: 2 B per value.
+* F32: 4 B per value, the value itself.
 
 Parity pins for each function live in tests/test_oracle.py.
 """
@@ -53,10 +54,11 @@ import numpy as np
 
 F16, BF16, Q8_0, Q4_0, Q4_K = 1, 2, 3, 4, 5
 Q4_1, Q5_0, Q5_1, Q5_K, Q6_K = 6, 7, 8, 9, 10
+F32 = 11
 
 _BLOCK = {F16: (1, 2), BF16: (1, 2), Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144),
           Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q5_K: (256, 176),
-          Q6_K: (256, 210)}
+          Q6_K: (256, 210), F32: (1, 4)}
 
 
 def row_bytes(wtype: int, K: int) -> int:
@@ -271,6 +273,11 @@ def decode_f16(W, N: int, K: int) -> np.ndarray:
     return f16_bits_to_f32(_le16(b[..., 0], b[..., 1]))
 
 
+def decode_f32(W, N: int, K: int) -> np.ndarray:
+    """F32: the stored little-endian binary32 words."""
+    return _rows(W, N, K, F32).reshape(-1).view("<f4").astype(np.float32).reshape(N, K)
+
+
 def decode_bf16(W, N: int, K: int) -> np.ndarray:
     b = _rows(W, N, K, BF16).reshape(N, K, 2)
     return bf16_bits_to_f32(_le16(b[..., 0], b[..., 1]))
@@ -279,7 +286,7 @@ def decode_bf16(W, N: int, K: int) -> np.ndarray:
 _DECODERS = {F16: decode_f16, BF16: decode_bf16, Q8_0: decode_q8_0,
              Q4_0: decode_q4_0, Q4_K: decode_q4_k, Q4_1: decode_q4_1,
              Q5_0: decode_q5_0, Q5_1: decode_q5_1, Q5_K: decode_q5_k,
-             Q6_K: decode_q6_k}
+             Q6_K: decode_q6_k, F32: decode_f32}
 
 
 def dequant(wtype: int, W, N: int, K: int) -> np.ndarray:

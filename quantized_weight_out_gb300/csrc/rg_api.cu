@@ -144,18 +144,26 @@ int cg_force_of(int variant) {
   return variant == RG_VARIANT_TC_SINGLE ? 1 : variant == RG_VARIANT_TC_PAIR ? 2 : 0;
 }
 
-// Tensor-core workspace: the 16-bit dY copy, then (split contraction) the
-// partial-sum slabs, each 256-byte aligned.
-size_t tc_partial_offset(int64_t N, int64_t T) { return tc_workspace(N, T); }
-size_t tc_workspace_total(int variant, int64_t N, int64_t K, int64_t T, const DevInfo& dev) {
+// Tensor-core workspace: the 16-bit dY copy; for F32 W its bf16 copy
+// [N, K]; then (split contraction) the partial-sum slabs; each 256-byte
+// aligned.
+size_t tc_w16_bytes(int wtype, int64_t N, int64_t K) {
+  if (wtype != RG_F32) return 0;
+  return (static_cast<size_t>(N) * static_cast<size_t>(K) * 2 + 255) / 256 * 256;
+}
+size_t tc_partial_offset(int wtype, int64_t N, int64_t K, int64_t T) {
+  return tc_workspace(N, T) + tc_w16_bytes(wtype, N, K);
+}
+size_t tc_workspace_total(int variant, int wtype, int64_t N, int64_t K, int64_t T,
+                          const DevInfo& dev) {
   const int64_t splits = tc_partial_splits(N, K, T, dev, cg_force_of(variant));
   const size_t parts = static_cast<size_t>(splits) * static_cast<size_t>(T) * static_cast<size_t>(K) * 4;
-  return tc_partial_offset(N, T) + (parts + 255) / 256 * 256;
+  return tc_partial_offset(wtype, N, K, T) + (parts + 255) / 256 * 256;
 }
 
 // Workspace bytes of a resolved (non-auto) variant; N, K, T > 0.
 size_t workspace_for(int variant, int wtype, int64_t N, int64_t K, int64_t T, const DevInfo& dev) {
-  if (is_tc(variant)) return tc_workspace_total(variant, N, K, T, dev);
+  if (is_tc(variant)) return tc_workspace_total(variant, wtype, N, K, T, dev);
   if (variant == RG_VARIANT_SMALLT)
     return (plan_smallt(wtype, N, K, T, dev).workspace + 255) / 256 * 256;
   return 0;
@@ -247,16 +255,27 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
     }
     return from_cuda(e);
   }
-  const bool bf16 = wtype == RG_BF16;
+  // F32 W: both operands in bf16 (the F32 range); W's copy is [N, K]
+  const bool bf16 = wtype == RG_BF16 || wtype == RG_F32;
   const int64_t ld = tc_dy16_ld(N);
   e = launch_convert_dy(dY, T, N, ld, bf16, static_cast<uint16_t*>(buf), *dev, stream);
+  const void* Wtc = W;
+  int wtc = wtype;
+  if (wtype == RG_F32) {
+    uint16_t* w16 = reinterpret_cast<uint16_t*>(static_cast<char*>(buf) + tc_workspace(N, T));
+    if (e == cudaSuccess)
+      e = launch_convert_dy(static_cast<const float*>(W), N, K, K, true, w16, *dev, stream);
+    Wtc = w16;
+    wtc = RG_BF16;
+  }
   cudaEvent_t ev0 = t_prof_before, ev1 = t_prof_after;
   t_prof_before = t_prof_after = nullptr;
   if (e == cudaSuccess && ev0) e = cudaEventRecord(ev0, stream);
   if (e == cudaSuccess)
-    e = launch_tc(wtype, W, N, K, static_cast<const uint16_t*>(buf), ld, T, dX, beta,
-                  reinterpret_cast<float*>(static_cast<char*>(buf) + tc_partial_offset(N, T)), *dev,
-                  stream, cg_force_of(variant), env().inject_stall);
+    e = launch_tc(wtc, Wtc, N, K, static_cast<const uint16_t*>(buf), ld, T, dX, beta,
+                  reinterpret_cast<float*>(static_cast<char*>(buf) +
+                                           tc_partial_offset(wtype, N, K, T)),
+                  *dev, stream, cg_force_of(variant), env().inject_stall);
   if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, stream);
   if (own_ws) {
     const cudaError_t f = cudaFreeAsync(buf, stream);
@@ -461,7 +480,8 @@ int rg_plan(int variant, int wtype, int64_t N, int64_t K, int64_t T, rg_plan_inf
     tile_t = p.bt;
     r.n_splits = p.n_splits;
     r.grid = p.grid;
-    r.launches = p.n_splits > 1 ? 3 : 2;  // dY conversion, GEMM, partial reduction
+    // dY conversion (and F32 W's), GEMM, partial reduction
+    r.launches = (p.n_splits > 1 ? 3 : 2) + (wtype == RG_F32 ? 1 : 0);
   } else if (r.variant == RG_VARIANT_SMALLT) {
     const SmalltPlan p = plan_smallt(wtype, N, K, T, *dev);
     r.tile_k = 256;
@@ -512,7 +532,7 @@ const char* rg_strerror(int status) {
     case RG_ERR_ARG: return "invalid argument (null pointer, negative or too large size, small workspace)";
     case RG_ERR_TYPE: return "unknown weight type or variant";
     case RG_ERR_SHAPE:
-      return "K is not a multiple of 256 (quantized types) or 8 (F16/BF16), or Q6_K with "
+      return "K is not a multiple of 256 (quantized types) or 8 (F32/F16/BF16), or Q6_K with "
              "K % 2048 != 0 on a tensor-core or small-T variant";
     case RG_ERR_ALIGN: return "pointer not 16-byte aligned (workspace: 256-byte)";
     case RG_ERR_CUDA: return "CUDA call or kernel launch failed";

@@ -19,9 +19,9 @@ namespace rg {
 // ---------------------------------------------------------------------------
 // storage formats: values per block, bytes per block
 
-__host__ __device__ constexpr bool valid_wtype(int wt) { return wt >= RG_F16 && wt <= RG_Q6_K; }
+__host__ __device__ constexpr bool valid_wtype(int wt) { return wt >= RG_F16 && wt <= RG_F32; }
 __host__ __device__ constexpr bool is_quant(int wt) {
-  return valid_wtype(wt) && wt != RG_F16 && wt != RG_BF16;
+  return valid_wtype(wt) && wt != RG_F16 && wt != RG_BF16 && wt != RG_F32;
 }
 __host__ __device__ constexpr int block_values(int wt) {
   return (wt == RG_Q4_K || wt == RG_Q5_K || wt == RG_Q6_K) ? 256 : is_quant(wt) ? 32 : 1;
@@ -35,6 +35,7 @@ __host__ __device__ constexpr int block_bytes(int wt) {
          : wt == RG_Q4_1 ? 20
          : wt == RG_Q5_0 ? 22
          : wt == RG_Q5_1 ? 24
+         : wt == RG_F32  ? 4
                          : 2;
 }
 
@@ -369,7 +370,12 @@ __device__ __forceinline__ void q4k_scale_min(const uint8_t* S, int j, int& sc, 
 
 template <int WT>
 __device__ __forceinline__ void decode8_f32(const uint8_t* row, int k0, float (&out)[8]) {
-  if constexpr (WT == RG_F16 || WT == RG_BF16) {
+  if constexpr (WT == RG_F32) {
+    const float4 a = *reinterpret_cast<const float4*>(row + 4 * k0);
+    const float4 b = *reinterpret_cast<const float4*>(row + 4 * k0 + 16);
+    out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+    out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+  } else if constexpr (WT == RG_F16 || WT == RG_BF16) {
     const uint4 v = *reinterpret_cast<const uint4*>(row + 2 * k0);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll

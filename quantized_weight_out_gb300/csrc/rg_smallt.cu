@@ -28,14 +28,19 @@ constexpr int THREADS = 256;   // 8 consumer warps (plus one producer warp)
 // Raw bytes one lane needs from a row for its 8 values (a 256-value tile).
 template <int WT>
 struct Raw {
-  uint32_t v[WT == RG_Q5_K ? 8 : WT == RG_Q4_K ? 6 : WT == RG_Q6_K ? 5 : (WT == RG_Q8_0 || WT == RG_Q4_0 || WT == RG_Q4_1) ? 3 : 4];
+  uint32_t v[WT == RG_Q5_K || WT == RG_F32 ? 8 : WT == RG_Q4_K ? 6 : WT == RG_Q6_K ? 5 : (WT == RG_Q8_0 || WT == RG_Q4_0 || WT == RG_Q4_1) ? 3 : 4];
 };
 
 // The bytes one lane needs for its 8 values, from a row tile staged in
 // shared memory (tile: the row's 256-value tile, 16-byte aligned).
 template <int WT>
 __device__ __forceinline__ void load_raw_smem(const uint8_t* tile, int lane, Raw<WT>& r) {
-  if constexpr (WT == RG_F16 || WT == RG_BF16) {
+  if constexpr (WT == RG_F32) {
+    const uint4 a = reinterpret_cast<const uint4*>(tile)[2 * lane];
+    const uint4 b = reinterpret_cast<const uint4*>(tile)[2 * lane + 1];
+    r.v[0] = a.x; r.v[1] = a.y; r.v[2] = a.z; r.v[3] = a.w;
+    r.v[4] = b.x; r.v[5] = b.y; r.v[6] = b.z; r.v[7] = b.w;
+  } else if constexpr (WT == RG_F16 || WT == RG_BF16) {
     const uint4 q = reinterpret_cast<const uint4*>(tile)[lane];
     r.v[0] = q.x; r.v[1] = q.y; r.v[2] = q.z; r.v[3] = q.w;
   } else if constexpr (WT == RG_Q8_0 || WT == RG_Q4_0) {
@@ -102,7 +107,10 @@ __device__ __forceinline__ int byte_at(const uint32_t* w, int i) {
 // rounding as the format definitions (signed zeros kept).
 template <int WT>
 __device__ __forceinline__ void decode_raw(const Raw<WT>& r, int lane, float (&w)[8]) {
-  if constexpr (WT == RG_F16 || WT == RG_BF16) {
+  if constexpr (WT == RG_F32) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = __uint_as_float(r.v[i]);
+  } else if constexpr (WT == RG_F16 || WT == RG_BF16) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint16_t lo = static_cast<uint16_t>(r.v[i] & 0xFFFFu);
@@ -227,13 +235,14 @@ __host__ __device__ constexpr int tile_bytes() {
 
 // The row-per-lane consumers (quantized W, one or two rows of dY) take 64
 // rows per stage (two per lane) in a 4-deep ring; the row-per-warp consumers
-// 32 rows in an 8-deep ring: the same bytes in flight either way.
+// 32 rows in an 8-deep ring (4-deep for F32 W, whose rows are four times
+// wider than the quantized ones).
 template <int WT, int TB>
 constexpr bool rows_path() { return TB <= 2 && is_quant(WT) && WT != RG_Q6_K; }
 template <int WT, int TB>
 constexpr int stage_rows() { return rows_path<WT, TB>() ? 64 : 32; }
 template <int WT, int TB>
-constexpr int n_stages() { return rows_path<WT, TB>() ? 4 : 8; }
+constexpr int n_stages() { return rows_path<WT, TB>() || WT == RG_F32 ? 4 : 8; }
 constexpr int CONSUMERS = 8; // consumer warps; warp 8 is the TMA producer
 constexpr int MAX_ROWS = 512;
 

@@ -30,7 +30,7 @@ Formats written (little-endian, the block layouts of ggml's GGUF types):
   ``qh[l]`` = fifth bit of value 64c+l / 64c+32+l), 128 bytes of nibbles.
 * Q6_K 210 B / 256 values: ``ql[128]`` (low 4 bits), ``qh[64]`` (2 high bits
   each), 16 int8 ``scales``, fp16 ``d``.
-* F16 / BF16: 2 B per value.
+* F16 / BF16: 2 B per value; F32: 4 B per value.
 
 The generator recipes follow the workload descriptions of the llama.cpp fork's
 PR "cuda: out_prod accepts a quantized src0" (the shapes a LoRA backward sees)
@@ -48,16 +48,16 @@ import numpy as np
 # ----------------------------------------------------------------------------
 # weight type codes (the C ABI uses the same integers)
 F16, BF16, Q8_0, Q4_0, Q4_K = 1, 2, 3, 4, 5
-Q4_1, Q5_0, Q5_1, Q5_K, Q6_K = 6, 7, 8, 9, 10
+Q4_1, Q5_0, Q5_1, Q5_K, Q6_K, F32 = 6, 7, 8, 9, 10, 11
 TYPE_NAMES = {F16: "f16", BF16: "bf16", Q8_0: "q8_0", Q4_0: "q4_0", Q4_K: "q4_k",
-              Q4_1: "q4_1", Q5_0: "q5_0", Q5_1: "q5_1", Q5_K: "q5_k", Q6_K: "q6_k"}
+              Q4_1: "q4_1", Q5_0: "q5_0", Q5_1: "q5_1", Q5_K: "q5_k", Q6_K: "q6_k", F32: "f32"}
 NAME_TO_TYPE = {v: k for k, v in TYPE_NAMES.items()}
-ALL_TYPES = [Q8_0, Q4_0, Q4_K, F16, BF16, Q4_1, Q5_0, Q5_1, Q5_K, Q6_K]
+ALL_TYPES = [Q8_0, Q4_0, Q4_K, F16, BF16, Q4_1, Q5_0, Q5_1, Q5_K, Q6_K, F32]
 
 # (values per block, bytes per block)
 BLOCK = {F16: (1, 2), BF16: (1, 2), Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144),
          Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q5_K: (256, 176),
-         Q6_K: (256, 210)}
+         Q6_K: (256, 210), F32: (1, 4)}
 
 
 def row_bytes(wtype: int, K: int) -> int:
@@ -378,6 +378,8 @@ def gen_weight(wtype: int, N: int, K: int, seed: int, stream: int) -> np.ndarray
         return f32_to_f16_bits(x).view(np.uint8).copy()
     if wtype == BF16:
         return f32_to_bf16_bits(x).view(np.uint8).copy()
+    if wtype == F32:
+        return x.astype("<f4").view(np.uint8).copy()
     raise ValueError(f"unknown weight type {wtype}")
 
 
@@ -450,5 +452,5 @@ WORKLOADS = {
     # the other quantized types on the sweep's q/o shape, one call each
     "types_4096x4096_t8192": [Problem(f"{TYPE_NAMES[wt]}_4096x4096_t8192", wt, 4096, 4096, 8192,
                                       1e-3, 0.0, 16 * i)
-                              for i, wt in enumerate([Q4_1, Q5_0, Q5_1, Q5_K, Q6_K])],
+                              for i, wt in enumerate([Q4_1, Q5_0, Q5_1, Q5_K, Q6_K, F32])],
 }

@@ -38,7 +38,7 @@ def test_row_bytes_matches_block_sizes(lib):
     for wt in inputs.ALL_TYPES:
         for K in (0, 8, 32, 256, 4096, 14336, 17408, 300):
             assert rg.rg_row_bytes(wt, K) == inputs.row_bytes(wt, K), (wt, K)
-    assert rg.rg_row_bytes(11, 256) == 0 and rg.rg_row_bytes(inputs.Q8_0, -32) == 0
+    assert rg.rg_row_bytes(12, 256) == 0 and rg.rg_row_bytes(inputs.Q8_0, -32) == 0
     assert rg.rg_row_bytes(0, 256) == 0
 
 
@@ -64,7 +64,7 @@ def test_dispatch(lib):
 
 def test_plan_validates_before_needing_a_device(lib):
     info = rg.rg_plan_info()
-    assert rg.rg_plan(0, 11, 64, 256, 8, info) == rg.RG_ERR_TYPE
+    assert rg.rg_plan(0, 12, 64, 256, 8, info) == rg.RG_ERR_TYPE
     assert rg.rg_plan(6, inputs.Q8_0, 64, 256, 8, info) == rg.RG_ERR_TYPE
     assert rg.rg_plan(0, inputs.Q8_0, 64, 200, 8, info) == rg.RG_ERR_SHAPE
     assert rg.rg_plan(0, inputs.F16, 64, 12, 8, info) == rg.RG_ERR_SHAPE
@@ -79,7 +79,7 @@ BAD = 0x1000  # never dereferenced: every case below fails validation first
 
 
 @pytest.mark.parametrize("args,status", [
-    ((11, BAD, 64, 256, BAD, 8, BAD, 0.0), rg.RG_ERR_TYPE),
+    ((12, BAD, 64, 256, BAD, 8, BAD, 0.0), rg.RG_ERR_TYPE),
     ((0, BAD, 64, 256, BAD, 8, BAD, 0.0), rg.RG_ERR_TYPE),
     ((inputs.Q5_K, BAD, 64, 128, BAD, 8, BAD, 0.0), rg.RG_ERR_SHAPE),
     ((inputs.Q5_0, BAD, 64, 32, BAD, 8, BAD, 0.0), rg.RG_ERR_SHAPE),
@@ -105,11 +105,11 @@ def test_validation_before_any_launch(lib, args, status):
 def test_bad_variant_and_workspace(lib):
     # valid shapes but a bad variant id: rejected (the variant check follows
     # argument validation, and the empty case returns before it)
-    assert rg.rg_out_prod_variant(7, 11, BAD, 64, 256, BAD, 8, BAD, 0.0) == rg.RG_ERR_TYPE
+    assert rg.rg_out_prod_variant(7, 12, BAD, 64, 256, BAD, 8, BAD, 0.0) == rg.RG_ERR_TYPE
 
 
 def test_dequant_validation(lib):
-    assert rg.rg_dequant(11, BAD, 4, 256, BAD) == rg.RG_ERR_TYPE
+    assert rg.rg_dequant(12, BAD, 4, 256, BAD) == rg.RG_ERR_TYPE
     assert rg.rg_dequant(inputs.Q4_K, BAD, 4, 128, BAD) == rg.RG_ERR_SHAPE
     assert rg.rg_dequant(inputs.Q8_0, None, 4, 256, BAD) == rg.RG_ERR_ARG
     assert rg.rg_dequant(inputs.Q8_0, BAD + 1, 4, 256, BAD) == rg.RG_ERR_ALIGN

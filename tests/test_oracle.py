@@ -180,6 +180,15 @@ def test_half_codes_hand_decoded(golden_dir):
         assert _bits_equal(got, np.float32(float(val))), (kind, code, got, val)
 
 
+def test_f32_codes_hand_decoded(golden_dir):
+    for kind, code, val in _read(golden_dir, "f32_codes.txt"):
+        W = np.frombuffer(int(code, 16).to_bytes(4, "little"), dtype=np.uint8)
+        got = oracle.decode_f32(W, 1, 1)[0, 0]
+        assert _bits_equal(got, np.float32(float(val))), (code, got, val)
+        # Python's own binary32 codec, independent of numpy
+        assert float(got) == struct.unpack("<f", int(code, 16).to_bytes(4, "little"))[0]
+
+
 def test_f16_all_codes_against_numpy_and_struct():
     codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     got = oracle.f16_bits_to_f32(codes)
@@ -253,6 +262,8 @@ def _all_ones_weight(wtype, N, K, variant=0):
         return np.frombuffer(blk * (N * K // 256), dtype=np.uint8)
     if wtype == inputs.F16:
         return np.frombuffer(bytes([0x00, 0x3C]) * (N * K), dtype=np.uint8)
+    if wtype == inputs.F32:
+        return np.frombuffer(bytes([0x00, 0x00, 0x80, 0x3F]) * (N * K), dtype=np.uint8)
     if wtype == inputs.BF16:
         return np.frombuffer(bytes([0x80, 0x3F]) * (N * K), dtype=np.uint8)
     raise ValueError(wtype)
@@ -261,7 +272,7 @@ def _all_ones_weight(wtype, N, K, variant=0):
 CASES = [(inputs.Q8_0, 0), (inputs.Q4_0, 0), (inputs.Q4_K, 0), (inputs.Q4_K, 1),
          (inputs.F16, 0), (inputs.BF16, 0), (inputs.Q4_1, 0), (inputs.Q5_0, 0),
          (inputs.Q5_1, 0), (inputs.Q5_1, 1), (inputs.Q5_K, 0), (inputs.Q5_K, 1),
-         (inputs.Q6_K, 0), (inputs.Q6_K, 1)]
+         (inputs.Q6_K, 0), (inputs.Q6_K, 1), (inputs.F32, 0)]
 
 
 @pytest.mark.parametrize("wtype,variant", CASES)
@@ -330,7 +341,10 @@ def _py_decode(wtype, raw, N, K):
     out = [[0.0] * K for _ in range(N)]
     for n in range(N):
         row = raw[n * rb:(n + 1) * rb]
-        if wtype in (inputs.F16, inputs.BF16):
+        if wtype == inputs.F32:
+            for k in range(K):
+                out[n][k] = struct.unpack("<f", bytes(row[4 * k: 4 * k + 4]))[0]
+        elif wtype in (inputs.F16, inputs.BF16):
             for k in range(K):
                 lo, hi = row[2 * k], row[2 * k + 1]
                 if wtype == inputs.F16:
@@ -422,7 +436,7 @@ def _py_decode(wtype, raw, N, K):
 BRUTE = [(inputs.Q8_0, 40, 64, 3), (inputs.Q4_0, 33, 96, 2), (inputs.Q4_K, 12, 512, 2),
          (inputs.F16, 24, 40, 3), (inputs.BF16, 24, 40, 3), (inputs.Q8_0, 7, 32, 1),
          (inputs.Q4_1, 21, 64, 2), (inputs.Q5_0, 19, 96, 2), (inputs.Q5_1, 17, 64, 2),
-         (inputs.Q5_K, 10, 512, 2), (inputs.Q6_K, 9, 512, 2)]
+         (inputs.Q5_K, 10, 512, 2), (inputs.Q6_K, 9, 512, 2), (inputs.F32, 20, 48, 3)]
 
 
 @pytest.mark.parametrize("wtype,N,K,T", BRUTE)
