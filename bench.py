@@ -410,43 +410,48 @@ def run_ours(args):
         d2h = sum(p.T * p.K * 4 for p in problems)
 
         # copies on two side streams, overlapped with compute on `stream`:
-        # H2D(i) -> rg_out_prod(i) -> D2H(i), with the write-after-read hazards
-        # across steps ordered by events
+        # H2D(i) -> rg_out_prod(i) -> D2H(i).  Two sets of device buffers
+        # alternate between steps, so a step's host -> device copies do not
+        # wait for the previous step's calls and read-backs; the hazards on a
+        # set (its previous use) are ordered by events.
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        ev_in = [torch.cuda.Event() for _ in problems]
-        ev_done = [torch.cuda.Event() for _ in problems]
-        ev_out = [torch.cuda.Event() for _ in problems]
+        sets = [devbuf, [(W.clone(), dY.clone(), dX.clone()) for W, dY, dX in devbuf]]
+        ev_in = [[torch.cuda.Event() for _ in problems] for _ in sets]
+        ev_done = [[torch.cuda.Event() for _ in problems] for _ in sets]
+        ev_out = [[torch.cuda.Event() for _ in problems] for _ in sets]
 
-        def e2e_step():
+        def e2e_step(k):
             for i, p in enumerate(problems):
-                W, dY, dX = devbuf[i]
-                s_in.wait_event(ev_done[i])
+                W, dY, dX = sets[k][i]
+                s_in.wait_event(ev_done[k][i])
                 with torch.cuda.stream(s_in):
                     W.copy_(host[i][0], non_blocking=True)
                     dY.copy_(host[i][1], non_blocking=True)
-                ev_in[i].record(s_in)
-                stream.wait_event(ev_in[i])
-                stream.wait_event(ev_out[i])
+                ev_in[k][i].record(s_in)
+                stream.wait_event(ev_in[k][i])
+                stream.wait_event(ev_out[k][i])
                 st = call(p, W, dY, dX)
                 if st != 0:
                     raise RuntimeError(rg.strerror(st))
-                ev_done[i].record(stream)
-                s_out.wait_event(ev_done[i])
+                ev_done[k][i].record(stream)
+                s_out.wait_event(ev_done[k][i])
                 with torch.cuda.stream(s_out):
                     host[i][2].copy_(dX, non_blocking=True)
-                ev_out[i].record(s_out)
+                ev_out[k][i].record(s_out)
 
-        e2e_step()
+        e2e_step(0)
+        e2e_step(1)
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         s_in.wait_event(e0)
-        for _ in range(args.steps):
-            e2e_step()
-        for ev in ev_out:
-            stream.wait_event(ev)
+        for k in range(args.steps):
+            e2e_step(k % 2)
+        for evs_k in ev_out:
+            for ev in evs_k:
+                stream.wait_event(ev)
         e1.record(stream)
         torch.cuda.synchronize()
         ems = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
