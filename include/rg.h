@@ -173,6 +173,31 @@ int rg_out_prod_ws(int variant, int wtype, const void* W, int64_t N, int64_t K,
 int rg_out_prod_noalloc(int wtype, const void* W, int64_t N, int64_t K,
                         const float* dY, int64_t T, float* dX, float beta, void* stream);
 
+/*
+ * The general form: `batch` independent products with their own strides.
+ * For b < batch,
+ *     dX_b[t, k] = beta * dX_b[t, k] + sum_n dY_b[t, n] * deq(W_b)[n, k]
+ * with W_b = W + b * w_batch_bytes (0: one W shared by every batch),
+ * dY_b[t, n] = dY[b * dy_batch + t * dy_t + n * dy_n] and
+ * dX_b[t, k] = dX[b * dx_batch + t * dx_t + k]   (strides in elements).
+ * dY may come transposed (dy_t = 1, dy_n = T), as ggml's out_prod(W, grad^T)
+ * receives grad^T as a strided view: the llama.cpp fork's PR "cuda: out_prod
+ * accepts a quantized src0" runs ggml's OUT_PROD paths for a plain or
+ * transposed src1 and its batch dimensions on the dense copy ("What",
+ * "Measured").  Rules: dy_t, dy_n >= 1; dx_t >= K and a multiple of 4;
+ * w_batch_bytes a multiple of 16 and dx_batch of 4; dY 16-byte aligned when
+ * its rows are contiguous (dy_n == 1, dy_t == N), else 4-byte aligned; every
+ * batch's W and dX 16-byte aligned (else RG_ERR_ALIGN / RG_ERR_ARG, checked
+ * for every batch before anything is launched).  Batches that stack into
+ * one taller dY and dX under a shared W run as one call; others run one
+ * after another on `stream`.  The batches' dX regions must not overlap.
+ * `variant` as for rg_out_prod_variant; batch == 0 is RG_OK.
+ */
+int rg_out_prod_ex(int variant, int wtype, const void* W, int64_t N, int64_t K,
+                   int64_t w_batch_bytes, const float* dY, int64_t T, int64_t dy_t, int64_t dy_n,
+                   int64_t dy_batch, float* dX, int64_t dx_t, int64_t dx_batch, int64_t batch,
+                   float beta, void* stream);
+
 /* The variant RG_VARIANT_AUTO picks for this shape (ignores RG_VARIANT). */
 int rg_select_variant(int wtype, int64_t N, int64_t K, int64_t T);
 

@@ -53,6 +53,8 @@ SIGNATURES = [
     ("rg_profile_next_gemm", _I, [_VP, _VP]),
     ("rg_out_prod_noalloc", _I, [_I, _VP, _I64, _I64, _VP, _I64, _VP, _F, _VP]),
     ("rg_plan", _I, [_I, _I, _I64, _I64, _I64, ctypes.POINTER(rg_plan_info)]),
+    ("rg_out_prod_ex", _I, [_I, _I, _VP, _I64, _I64, _I64, _VP, _I64, _I64, _I64, _I64, _VP, _I64,
+                            _I64, _I64, _F, _VP]),
     ("rg_launch_count", ctypes.c_uint64, []),
 ]
 
@@ -114,6 +116,13 @@ def rg_out_prod_variant(variant, wtype, W, N, K, dY, T, dX, beta, stream=None) -
 def rg_out_prod_noalloc(wtype, W, N, K, dY, T, dX, beta, stream=None) -> int:
     return load().rg_out_prod_noalloc(wtype, _ptr(W), N, K, _ptr(dY), T, _ptr(dX), beta,
                                       _stream(stream))
+
+
+def rg_out_prod_ex(variant, wtype, W, N, K, w_batch_bytes, dY, T, dy_t, dy_n, dy_batch, dX, dx_t,
+                   dx_batch, batch, beta, stream=None) -> int:
+    return load().rg_out_prod_ex(variant, wtype, _ptr(W), N, K, w_batch_bytes, _ptr(dY), T, dy_t,
+                                 dy_n, dy_batch, _ptr(dX), dx_t, dx_batch, batch, beta,
+                                 _stream(stream))
 
 
 def rg_workspace_bytes(variant, wtype, N, K, T) -> int:

@@ -94,10 +94,14 @@ int64_t row_bytes_i(int wtype, int64_t K) {
   return K / bv * block_bytes(wtype);
 }
 
+bool contiguous_dy(const Layout& lay, int64_t N) { return lay.dy_n == 1 && lay.dy_t == N; }
+
 // Shared validation of the OUT_PROD arguments.  Returns RG_OK and sets
-// *empty when there is nothing to launch.
+// *empty when there is nothing to launch.  Strided dY needs 4-byte
+// alignment, row-contiguous dY 16-byte (vector loads); dX rows must be
+// 16-byte aligned (dx_t a multiple of 4, at least K).
 int validate(int wtype, const void* W, int64_t N, int64_t K, const float* dY, int64_t T,
-             const float* dX, bool* empty) {
+             const float* dX, const Layout& lay, bool* empty) {
   *empty = false;
   if (!valid_wtype(wtype)) return RG_ERR_TYPE;
   if (N < 0 || K < 0 || T < 0 || N > kMaxDim || K > kMaxDim || T > kMaxDim) return RG_ERR_ARG;
@@ -107,11 +111,16 @@ int validate(int wtype, const void* W, int64_t N, int64_t K, const float* dY, in
     *empty = true;
     return RG_OK;
   }
+  if (lay.dx_t < K) return RG_ERR_ARG;
+  if (lay.dx_t % 4) return RG_ERR_ALIGN;
   if (!dX) return RG_ERR_ARG;
   if (!aligned16(dX)) return RG_ERR_ALIGN;
   if (N > 0) {
+    if (lay.dy_t < 1 || lay.dy_n < 1) return RG_ERR_ARG;
     if (!W || !dY) return RG_ERR_ARG;
-    if (!aligned16(W) || !aligned16(dY)) return RG_ERR_ALIGN;
+    if (!aligned16(W)) return RG_ERR_ALIGN;
+    if (contiguous_dy(lay, N) ? !aligned16(dY) : (reinterpret_cast<uintptr_t>(dY) & 3u) != 0)
+      return RG_ERR_ALIGN;
   }
   return RG_OK;
 }
@@ -220,19 +229,20 @@ int noalloc_scratch(int d, void** out) {
 }
 
 int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float* dY, int64_t T,
-        float* dX, float beta, void* ws, size_t ws_bytes, bool own_ws, cudaStream_t stream) {
+        float* dX, float beta, void* ws, size_t ws_bytes, bool own_ws, cudaStream_t stream,
+        const Layout& lay) {
   bool empty = false;
-  int st = validate(wtype, W, N, K, dY, T, dX, &empty);
+  int st = validate(wtype, W, N, K, dY, T, dX, lay, &empty);
   if (st != RG_OK || empty) return st;
   if (variant < RG_VARIANT_AUTO || variant > RG_VARIANT_TC_PAIR) return RG_ERR_TYPE;
   DevInfo* dev = nullptr;
   if ((st = current_dev(&dev)) != RG_OK) return st;
-  if (N == 0) return from_cuda(launch_scale(dX, T * K, beta, *dev, stream));
+  if (N == 0) return from_cuda(launch_scale(dX, T, K, lay.dx_t, beta, *dev, stream));
   if (variant == RG_VARIANT_AUTO) variant = select_variant(wtype, N, K, T);
   if (variant != RG_VARIANT_SIMT32 && !aligned_rows(wtype, K)) return RG_ERR_SHAPE;
 
   if (variant == RG_VARIANT_SIMT32)
-    return from_cuda(launch_simt32(wtype, W, N, K, dY, T, dX, beta, *dev, stream));
+    return from_cuda(launch_simt32(wtype, W, N, K, dY, T, dX, beta, lay, *dev, stream));
   // the small-T and tensor-core paths take a workspace: partial sums, or the
   // 16-bit copy of dY
   const size_t need = workspace_for(variant, wtype, N, K, T, *dev);
@@ -247,7 +257,7 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
   }
   cudaError_t e = cudaSuccess;
   if (variant == RG_VARIANT_SMALLT) {
-    e = launch_smallt(wtype, W, N, K, dY, T, dX, beta, static_cast<float*>(buf),
+    e = launch_smallt(wtype, W, N, K, dY, T, dX, beta, lay, static_cast<float*>(buf),
                       plan_smallt(wtype, N, K, T, *dev), *dev, stream);
     if (own_ws) {
       const cudaError_t f = cudaFreeAsync(buf, stream);
@@ -258,13 +268,14 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
   // F32 W: both operands in bf16 (the F32 range); W's copy is [N, K]
   const bool bf16 = wtype == RG_BF16 || wtype == RG_F32;
   const int64_t ld = tc_dy16_ld(N);
-  e = launch_convert_dy(dY, T, N, ld, bf16, static_cast<uint16_t*>(buf), *dev, stream);
+  e = launch_convert_dy(dY, T, N, lay.dy_t, lay.dy_n, ld, bf16, static_cast<uint16_t*>(buf), *dev,
+                        stream);
   const void* Wtc = W;
   int wtc = wtype;
   if (wtype == RG_F32) {
     uint16_t* w16 = reinterpret_cast<uint16_t*>(static_cast<char*>(buf) + tc_workspace(N, T));
     if (e == cudaSuccess)
-      e = launch_convert_dy(static_cast<const float*>(W), N, K, K, true, w16, *dev, stream);
+      e = launch_convert_dy(static_cast<const float*>(W), N, K, K, 1, K, true, w16, *dev, stream);
     Wtc = w16;
     wtc = RG_BF16;
   }
@@ -272,7 +283,7 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
   t_prof_before = t_prof_after = nullptr;
   if (e == cudaSuccess && ev0) e = cudaEventRecord(ev0, stream);
   if (e == cudaSuccess)
-    e = launch_tc(wtc, Wtc, N, K, static_cast<const uint16_t*>(buf), ld, T, dX, beta,
+    e = launch_tc(wtc, Wtc, N, K, static_cast<const uint16_t*>(buf), ld, T, dX, lay.dx_t, beta,
                   reinterpret_cast<float*>(static_cast<char*>(buf) +
                                            tc_partial_offset(wtype, N, K, T)),
                   *dev, stream, cg_force_of(variant), env().inject_stall);
@@ -401,13 +412,41 @@ extern "C" {
 int rg_out_prod(int wtype, const void* W, int64_t N, int64_t K, const float* dY, int64_t T,
                 float* dX, float beta, void* stream) {
   return run(env().variant, wtype, W, N, K, dY, T, dX, beta, nullptr, 0, true,
-             static_cast<cudaStream_t>(stream));
+             static_cast<cudaStream_t>(stream), Layout{N, 1, K});
 }
 
 int rg_out_prod_variant(int variant, int wtype, const void* W, int64_t N, int64_t K,
                         const float* dY, int64_t T, float* dX, float beta, void* stream) {
   return run(variant, wtype, W, N, K, dY, T, dX, beta, nullptr, 0, true,
-             static_cast<cudaStream_t>(stream));
+             static_cast<cudaStream_t>(stream), Layout{N, 1, K});
+}
+
+int rg_out_prod_ex(int variant, int wtype, const void* W, int64_t N, int64_t K,
+                   int64_t w_batch_bytes, const float* dY, int64_t T, int64_t dy_t, int64_t dy_n,
+                   int64_t dy_batch, float* dX, int64_t dx_t, int64_t dx_batch, int64_t batch,
+                   float beta, void* stream) {
+  if (batch < 0 || w_batch_bytes < 0 || dy_batch < 0 || dx_batch < 0) return RG_ERR_ARG;
+  if (batch == 0) return RG_OK;
+  if (w_batch_bytes % 16 || dx_batch % 4) return RG_ERR_ALIGN;
+  const Layout lay{dy_t, dy_n, dx_t};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // batches that tile one taller dY / dX under a shared W are one call
+  if (batch > 1 && w_batch_bytes == 0 && dy_n == 1 && dy_batch == T * dy_t &&
+      dx_batch == T * dx_t && T * batch <= kMaxDim)
+    return run(variant, wtype, W, N, K, dY, T * batch, dX, beta, nullptr, 0, true, s, lay);
+  // validate every batch's pointers before the first launch
+  for (int64_t b = 0; b < batch; ++b) {
+    bool empty = false;
+    const int st = validate(wtype, static_cast<const uint8_t*>(W) + b * w_batch_bytes, N, K,
+                            dY + b * dy_batch, T, dX + b * dx_batch, lay, &empty);
+    if (st != RG_OK) return st;
+  }
+  for (int64_t b = 0; b < batch; ++b) {
+    const int st = run(variant, wtype, static_cast<const uint8_t*>(W) + b * w_batch_bytes, N, K,
+                       dY + b * dy_batch, T, dX + b * dx_batch, beta, nullptr, 0, true, s, lay);
+    if (st != RG_OK) return st;
+  }
+  return RG_OK;
 }
 
 size_t rg_workspace_bytes(int variant, int wtype, int64_t N, int64_t K, int64_t T) {
@@ -423,13 +462,13 @@ int rg_out_prod_ws(int variant, int wtype, const void* W, int64_t N, int64_t K, 
                    int64_t T, float* dX, float beta, void* workspace, size_t workspace_bytes,
                    void* stream) {
   return run(variant, wtype, W, N, K, dY, T, dX, beta, workspace, workspace_bytes, false,
-             static_cast<cudaStream_t>(stream));
+             static_cast<cudaStream_t>(stream), Layout{N, 1, K});
 }
 
 int rg_out_prod_noalloc(int wtype, const void* W, int64_t N, int64_t K, const float* dY,
                         int64_t T, float* dX, float beta, void* stream) {
   bool empty = false;
-  int st = validate(wtype, W, N, K, dY, T, dX, &empty);
+  int st = validate(wtype, W, N, K, dY, T, dX, Layout{N, 1, K}, &empty);
   if (st != RG_OK || empty) return st;
   int variant = env().variant;
   if (variant == RG_VARIANT_AUTO) variant = select_variant(wtype, N, K, T);
@@ -446,7 +485,7 @@ int rg_out_prod_noalloc(int wtype, const void* W, int64_t N, int64_t K, const fl
     }
   }
   return run(variant, wtype, W, N, K, dY, T, dX, beta, ws, ws_bytes, false,
-             static_cast<cudaStream_t>(stream));
+             static_cast<cudaStream_t>(stream), Layout{N, 1, K});
 }
 
 int rg_select_variant(int wtype, int64_t N, int64_t K, int64_t T) {

@@ -154,8 +154,59 @@ __global__ void __launch_bounds__(256) convert_dy_kernel(const float* __restrict
   }
 }
 
-cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t ld, bool bf16,
-                              uint16_t* out, const DevInfo& dev, cudaStream_t stream) {
+// Strided dY (a row stride other than N, or a column stride other than 1,
+// e.g. dY given transposed): 32 x 32 tiles through shared memory; the reads
+// run along whichever axis has unit stride (n when dy_n == 1, else t) and
+// the 16-bit writes along n.
+template <bool BF16>
+__global__ void __launch_bounds__(256) convert_dy_tiled_kernel(const float* __restrict__ dY,
+                                                               int64_t T, int64_t N, int64_t dy_t,
+                                                               int64_t dy_n, int64_t ld,
+                                                               uint16_t* __restrict__ out) {
+  __shared__ float tile[32][33];  // [t][n]
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 32, t0 = static_cast<int64_t>(blockIdx.y) * 32;
+  const bool along_n = dy_n == 1 || dy_t != 1;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int a = ty + 8 * j;  // the slow index inside the tile
+    const int64_t t = along_n ? t0 + a : t0 + tx, n = along_n ? n0 + tx : n0 + a;
+    const float v = (t < T && n < N) ? __ldg(dY + t * dy_t + n * dy_n) : 0.0f;
+    if (along_n)
+      tile[a][tx] = v;
+    else
+      tile[tx][a] = v;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int a = ty + 8 * j;
+    const int64_t t = t0 + a, n = n0 + tx;
+    if (t < T && n < N) {
+      if constexpr (BF16) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(tile[a][tx]);
+        out[t * ld + n] = *reinterpret_cast<const uint16_t*>(&h);
+      } else {
+        const __half h = __float2half_rn(tile[a][tx]);
+        out[t * ld + n] = *reinterpret_cast<const uint16_t*>(&h);
+      }
+    }
+  }
+}
+
+cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t dy_t, int64_t dy_n,
+                              int64_t ld, bool bf16, uint16_t* out, const DevInfo& dev,
+                              cudaStream_t stream) {
+  if (dy_n != 1 || dy_t != N) {
+    const int64_t gy = (T + 31) / 32;
+    if (gy > 65535) return cudaErrorInvalidConfiguration;
+    const dim3 grid(static_cast<unsigned>((N + 31) / 32), static_cast<unsigned>(gy));
+    if (bf16)
+      convert_dy_tiled_kernel<true><<<grid, 256, 0, stream>>>(dY, T, N, dy_t, dy_n, ld, out);
+    else
+      convert_dy_tiled_kernel<false><<<grid, 256, 0, stream>>>(dY, T, N, dy_t, dy_n, ld, out);
+    return counted(cudaGetLastError());
+  }
   const int grid = grid_for(T * ((N + 7) >> 3), 256, dev);
   if (bf16)
     convert_dy_kernel<true><<<grid, 256, 0, stream>>>(dY, T, N, ld, out);
@@ -164,16 +215,20 @@ cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t ld,
   return counted(cudaGetLastError());
 }
 
-__global__ void __launch_bounds__(256) scale_kernel(float* __restrict__ x, int64_t count,
-                                                    float beta) {
+__global__ void __launch_bounds__(256) scale_kernel(float* __restrict__ x, int64_t T, int64_t K,
+                                                    int64_t ldx, float beta) {
+  const int64_t count = T * K;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < count;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    x[i] = beta == 0.0f ? 0.0f : beta * x[i];
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = i / K;
+    float* p = x + t * ldx + (i - t * K);
+    *p = beta == 0.0f ? 0.0f : beta * *p;
+  }
 }
 
-cudaError_t launch_scale(float* dX, int64_t count, float beta, const DevInfo& dev,
-                         cudaStream_t stream) {
-  scale_kernel<<<grid_for(count, 256, dev), 256, 0, stream>>>(dX, count, beta);
+cudaError_t launch_scale(float* dX, int64_t T, int64_t K, int64_t dx_t, float beta,
+                         const DevInfo& dev, cudaStream_t stream) {
+  scale_kernel<<<grid_for(T * K, 256, dev), 256, 0, stream>>>(dX, T, K, dx_t, beta);
   return counted(cudaGetLastError());
 }
 

@@ -57,16 +57,23 @@ R with_wtype(int wtype, R fallback, F&& f) {
 cudaError_t launch_dequant(int wtype, const void* W, int64_t N, int64_t K, float* out,
                            const DevInfo& dev, cudaStream_t stream);
 
-// dY [T, N] F32 -> out [T, ld] fp16 (bf16 when `bf16`), rows padded to ld.
-cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t ld, bool bf16,
-                              uint16_t* out, const DevInfo& dev, cudaStream_t stream);
+// Element strides of the caller's activations: dY[t, n] at
+// dY[t * dy_t + n * dy_n], dX[t, k] at dX[t * dx_t + k].
+struct Layout {
+  int64_t dy_t, dy_n, dx_t;
+};
 
-// dX = beta * dX (beta == 0: dX = 0), the N == 0 case.
-cudaError_t launch_scale(float* dX, int64_t count, float beta, const DevInfo& dev,
-                         cudaStream_t stream);
+// dY [T, N] (strided) F32 -> out [T, ld] fp16 (bf16 when `bf16`), rows padded to ld.
+cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t dy_t, int64_t dy_n,
+                              int64_t ld, bool bf16, uint16_t* out, const DevInfo& dev,
+                              cudaStream_t stream);
+
+// dX = beta * dX (beta == 0: dX = 0) over T rows of K, the N == 0 case.
+cudaError_t launch_scale(float* dX, int64_t T, int64_t K, int64_t dx_t, float beta,
+                         const DevInfo& dev, cudaStream_t stream);
 
 cudaError_t launch_simt32(int wtype, const void* W, int64_t N, int64_t K, const float* dY,
-                          int64_t T, float* dX, float beta, const DevInfo& dev,
+                          int64_t T, float* dX, float beta, const Layout& lay, const DevInfo& dev,
                           cudaStream_t stream);
 
 // Small-T path: rows of W split over n_splits CTAs per 256-value tile and
@@ -83,8 +90,8 @@ struct SmalltPlan {
 // Sized so that the grid fills the GPU once at the kernel's residency.
 SmalltPlan plan_smallt(int wtype, int64_t N, int64_t K, int64_t T, const DevInfo& dev);
 cudaError_t launch_smallt(int wtype, const void* W, int64_t N, int64_t K, const float* dY,
-                          int64_t T, float* dX, float beta, float* part, const SmalltPlan& p,
-                          const DevInfo& dev, cudaStream_t stream);
+                          int64_t T, float* dX, float beta, const Layout& lay, float* part,
+                          const SmalltPlan& p, const DevInfo& dev, cudaStream_t stream);
 
 // Tensor-core path.  dy16 is the converted dY with row stride ld_dy16 values.
 struct TcPlan {
@@ -103,14 +110,16 @@ int64_t tc_dy16_ld(int64_t N);
 // part: [n_splits][T][K] F32 partial sums when the plan splits the
 // contraction (tc_partial_splits > 0), else unused.
 cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
-                      int64_t ld_dy16, int64_t T, float* dX, float beta, float* part,
+                      int64_t ld_dy16, int64_t T, float* dX, int64_t dx_t, float beta, float* part,
                       const DevInfo& dev, cudaStream_t stream, int cg_force, int inject_stall);
 // Number of partial-sum slabs the tensor-core plan needs (0 when unsplit).
 int64_t tc_partial_splits(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force);
 
-// dX = beta * dX + sum of n_splits slabs of TK floats, in slab order.
-cudaError_t launch_reduce_partials(const float* part, int n_splits, int64_t TK, float* dX,
-                                   float beta, const DevInfo& dev, cudaStream_t stream);
+// dX = beta * dX + sum of n_splits slabs of [T, K] floats, in a fixed
+// order; dX rows dx_t floats apart (a multiple of 4).
+cudaError_t launch_reduce_partials(const float* part, int n_splits, int64_t T, int64_t K,
+                                   float* dX, int64_t dx_t, float beta, const DevInfo& dev,
+                                   cudaStream_t stream);
 
 // A kernel whose one wait can never complete; it must give up after
 // `limit_ns`, record RG_ERR_TIMEOUT and return.

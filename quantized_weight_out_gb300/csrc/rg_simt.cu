@@ -19,7 +19,8 @@ template <int WT>
 __global__ void __launch_bounds__(256) simt32_kernel(const uint8_t* __restrict__ W, int64_t rb,
                                                      int N, int K,
                                                      const float* __restrict__ dY, int T,
-                                                     float* __restrict__ dX, float beta) {
+                                                     float* __restrict__ dX, float beta,
+                                                     int64_t dy_t, int64_t dy_n, int64_t dx_t) {
   __shared__ float ys[S32_TN][S32_TT + 1];              // [n][t]
   __shared__ __align__(16) float ws[S32_TN][S32_TK];    // [n][k]
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
@@ -39,7 +40,7 @@ __global__ void __launch_bounds__(256) simt32_kernel(const uint8_t* __restrict__
       const int r = idx >> 5, c = idx & 31;
       const int64_t t = t0 + r;
       const int n = n0 + c;
-      ys[c][r] = (t < T && n < N) ? dY[t * N + n] : 0.0f;
+      ys[c][r] = (t < T && n < N) ? dY[t * dy_t + n * dy_n] : 0.0f;
     }
     {
       const int r = tid >> 3, kk = 8 * (tid & 7);
@@ -87,14 +88,14 @@ __global__ void __launch_bounds__(256) simt32_kernel(const uint8_t* __restrict__
     for (int j = 0; j < 4; ++j) {
       const int k = k0 + tx + 16 * j;
       if (k >= K) continue;
-      float* o = dX + t * K + k;
+      float* o = dX + t * dx_t + k;
       *o = beta != 0.0f ? fmaf(beta, *o, acc[i][j]) : acc[i][j];
     }
   }
 }
 
 cudaError_t launch_simt32(int wtype, const void* W, int64_t N, int64_t K, const float* dY,
-                          int64_t T, float* dX, float beta, const DevInfo& dev,
+                          int64_t T, float* dX, float beta, const Layout& lay, const DevInfo& dev,
                           cudaStream_t stream) {
   (void)dev;
   const int64_t rb = K / block_values(wtype) * block_bytes(wtype);
@@ -104,7 +105,8 @@ cudaError_t launch_simt32(int wtype, const void* W, int64_t N, int64_t K, const 
   const uint8_t* w = static_cast<const uint8_t*>(W);
   const int n = static_cast<int>(N), k = static_cast<int>(K), t = static_cast<int>(T);
   return with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
-    simt32_kernel<decltype(wt)::value><<<grid, 256, 0, stream>>>(w, rb, n, k, dY, t, dX, beta);
+    simt32_kernel<decltype(wt)::value><<<grid, 256, 0, stream>>>(w, rb, n, k, dY, t, dX, beta,
+                                                                 lay.dy_t, lay.dy_n, lay.dx_t);
     return counted(cudaGetLastError());
   });
 }

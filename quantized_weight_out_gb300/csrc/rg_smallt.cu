@@ -511,8 +511,8 @@ __device__ __forceinline__ void consume_rows(int g, const uint8_t* stage_buf, co
 template <int WT, int TB>
 __global__ void __launch_bounds__(THREADS + 32, rows_path<WT, TB>() && TB == 1 ? 3 : (TB >= 8 ? 1 : 2))
     smallt_kernel(const __grid_constant__ CUtensorMap map_w, int N, int K,
-                  const float* __restrict__ dY, int T, float* __restrict__ part,
-                  int rows_per_split, WaitCtl ctl) {
+                  const float* __restrict__ dY, int64_t dy_t, int64_t dy_n, int T,
+                  float* __restrict__ part, int rows_per_split, WaitCtl ctl) {
   constexpr int TBYTES = stage_row_bytes<WT>();
   constexpr int BR = stage_rows<WT, TB>(), STAGES = n_stages<WT, TB>();
   extern __shared__ __align__(128) uint8_t sm[];
@@ -548,7 +548,9 @@ __global__ void __launch_bounds__(THREADS + 32, rows_path<WT, TB>() && TB == 1 ?
     // producer's first copies are in flight
     for (int idx = threadIdx.x; idx < TB * MAX_ROWS; idx += THREADS) {
       const int t = idx / MAX_ROWS, r = idx - t * MAX_ROWS;
-      ys[idx] = (t0 + t < T && r < nrows) ? __ldg(dY + static_cast<int64_t>(t0 + t) * N + nbeg + r) : 0.0f;
+      ys[idx] = (t0 + t < T && r < nrows)
+                    ? __ldg(dY + static_cast<int64_t>(t0 + t) * dy_t + static_cast<int64_t>(nbeg + r) * dy_n)
+                    : 0.0f;
     }
     asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");  // the consumer warps only
   }
@@ -654,9 +656,16 @@ constexpr size_t smem_bytes() {
 }
 
 // dX = beta * dX + sum over splits (in split order), four values per thread.
+// dX offset of element i of a [T, K] slab, dX rows ldx floats apart
+__device__ __forceinline__ int64_t dx_at(int64_t i, int64_t K, int64_t ldx) {
+  if (ldx == K) return i;
+  const int64_t t = i / K;
+  return t * ldx + (i - t * K);
+}
+
 __global__ void __launch_bounds__(256) smallt_reduce(const float* __restrict__ part, int n_splits,
-                                                     int64_t TK, float* __restrict__ dX,
-                                                     float beta) {
+                                                     int64_t TK, int64_t K, int64_t ldx,
+                                                     float* __restrict__ dX, float beta) {
   for (int64_t i = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) * 4; i < TK;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x * 4) {
     float4 s = *reinterpret_cast<const float4*>(part + i);
@@ -676,7 +685,7 @@ __global__ void __launch_bounds__(256) smallt_reduce(const float* __restrict__ p
       const float4 v = *reinterpret_cast<const float4*>(part + static_cast<int64_t>(p) * TK + i);
       s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
     }
-    float4* o = reinterpret_cast<float4*>(dX + i);
+    float4* o = reinterpret_cast<float4*>(dX + dx_at(i, K, ldx));
     if (beta != 0.0f) {
       const float4 x = *o;
       s.x = fmaf(beta, x.x, s.x); s.y = fmaf(beta, x.y, s.y);
@@ -691,8 +700,9 @@ __global__ void __launch_bounds__(256) smallt_reduce(const float* __restrict__ p
 // p loading split p0 + p; each group of 32 splits is added by a fixed xor
 // tree and the groups in order.
 __global__ void __launch_bounds__(256) smallt_reduce_wide(const float* __restrict__ part,
-                                                          int n_splits, int64_t TK,
-                                                          float* __restrict__ dX, float beta) {
+                                                          int n_splits, int64_t TK, int64_t K,
+                                                          int64_t ldx, float* __restrict__ dX,
+                                                          float beta) {
   const int lane = threadIdx.x & 31;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   for (int64_t q = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; q * 4 < TK;
@@ -713,7 +723,7 @@ __global__ void __launch_bounds__(256) smallt_reduce_wide(const float* __restric
       s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
     }
     if (lane == 0) {
-      float4* o = reinterpret_cast<float4*>(dX + i);
+      float4* o = reinterpret_cast<float4*>(dX + dx_at(i, K, ldx));
       if (beta != 0.0f) {
         const float4 x = *o;
         s.x = fmaf(beta, x.x, s.x); s.y = fmaf(beta, x.y, s.y);
@@ -779,8 +789,8 @@ SmalltPlan plan_smallt(int wtype, int64_t N, int64_t K, int64_t T, const DevInfo
 
 template <int WT, int TB>
 static cudaError_t launch_smallt_t(const void* W, int64_t N, int64_t K, const float* dY,
-                                   int64_t T, float* part, const SmalltPlan& p, const DevInfo& dev,
-                                   cudaStream_t stream) {
+                                   int64_t T, const Layout& lay, float* part, const SmalltPlan& p,
+                                   const DevInfo& dev, cudaStream_t stream) {
   auto kern = smt::smallt_kernel<WT, TB>;
   constexpr size_t smem = smt::smem_bytes<WT, TB>();
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
@@ -796,46 +806,49 @@ static cudaError_t launch_smallt_t(const void* W, int64_t N, int64_t K, const fl
                   static_cast<unsigned>(p.n_tchunks));
   WaitCtl ctl{dev.status, dev.wait_limit_ns};
   kern<<<grid, smt::THREADS + 32, smem, stream>>>(map, static_cast<int>(N), static_cast<int>(K), dY,
-                                                   static_cast<int>(T), part, p.rows_per_split, ctl);
+                                                   lay.dy_t, lay.dy_n, static_cast<int>(T), part,
+                                                   p.rows_per_split, ctl);
   return counted(cudaGetLastError());
 }
 
 template <int WT>
 static cudaError_t launch_smallt_w(const void* W, int64_t N, int64_t K, const float* dY,
-                                   int64_t T, float* part, const SmalltPlan& p, const DevInfo& dev,
-                                   cudaStream_t stream) {
+                                   int64_t T, const Layout& lay, float* part, const SmalltPlan& p,
+                                   const DevInfo& dev, cudaStream_t stream) {
   switch (p.tb) {
-    case 1: return launch_smallt_t<WT, 1>(W, N, K, dY, T, part, p, dev, stream);
-    case 2: return launch_smallt_t<WT, 2>(W, N, K, dY, T, part, p, dev, stream);
-    case 4: return launch_smallt_t<WT, 4>(W, N, K, dY, T, part, p, dev, stream);
-    default: return launch_smallt_t<WT, 8>(W, N, K, dY, T, part, p, dev, stream);
+    case 1: return launch_smallt_t<WT, 1>(W, N, K, dY, T, lay, part, p, dev, stream);
+    case 2: return launch_smallt_t<WT, 2>(W, N, K, dY, T, lay, part, p, dev, stream);
+    case 4: return launch_smallt_t<WT, 4>(W, N, K, dY, T, lay, part, p, dev, stream);
+    default: return launch_smallt_t<WT, 8>(W, N, K, dY, T, lay, part, p, dev, stream);
   }
 }
 
 cudaError_t launch_smallt(int wtype, const void* W, int64_t N, int64_t K, const float* dY,
-                          int64_t T, float* dX, float beta, float* part, const SmalltPlan& p,
-                          const DevInfo& dev, cudaStream_t stream) {
+                          int64_t T, float* dX, float beta, const Layout& lay, float* part,
+                          const SmalltPlan& p, const DevInfo& dev, cudaStream_t stream) {
   if (p.n_tchunks > 65535 || p.n_splits > 65535) return cudaErrorInvalidConfiguration;
   const cudaError_t e = with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
-    return launch_smallt_w<decltype(wt)::value>(W, N, K, dY, T, part, p, dev, stream);
+    return launch_smallt_w<decltype(wt)::value>(W, N, K, dY, T, lay, part, p, dev, stream);
   });
   if (e != cudaSuccess) return e;
-  return launch_reduce_partials(part, p.n_splits, T * K, dX, beta, dev, stream);
+  return launch_reduce_partials(part, p.n_splits, T, K, dX, lay.dx_t, beta, dev, stream);
 }
 
-cudaError_t launch_reduce_partials(const float* part, int n_splits, int64_t TK, float* dX,
-                                   float beta, const DevInfo& dev, cudaStream_t stream) {
+cudaError_t launch_reduce_partials(const float* part, int n_splits, int64_t T, int64_t K,
+                                   float* dX, int64_t dx_t, float beta, const DevInfo& dev,
+                                   cudaStream_t stream) {
+  const int64_t TK = T * K;
   // latency regime (a warp per four outputs fits in one wave): the wide form
   const int64_t quads = TK / 4;
   if (n_splits >= 4 && quads * 32 <= static_cast<int64_t>(dev.num_sms) * 2048) {
     const int64_t blocks = (quads * 32 + 255) / 256;
     smt::smallt_reduce_wide<<<static_cast<unsigned>(std::max<int64_t>(1, blocks)), 256, 0, stream>>>(
-        part, n_splits, TK, dX, beta);
+        part, n_splits, TK, K, dx_t, dX, beta);
     return counted(cudaGetLastError());
   }
   const int64_t blocks = std::min<int64_t>((quads + 255) / 256, static_cast<int64_t>(dev.num_sms) * 8);
   smt::smallt_reduce<<<static_cast<unsigned>(std::max<int64_t>(1, blocks)), 256, 0, stream>>>(
-      part, n_splits, TK, dX, beta);
+      part, n_splits, TK, K, dx_t, dX, beta);
   return counted(cudaGetLastError());
 }
 

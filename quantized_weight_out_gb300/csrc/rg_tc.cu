@@ -475,7 +475,7 @@ template <int WT, int CG, int BT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     out_prod_tc_kernel(const __grid_constant__ CUtensorMap map_w,
                        const __grid_constant__ CUtensorMap map_y, float* __restrict__ dX,
-                       float beta, int T, int K, int n_kunits, int n_ttiles, int band,
+                       int64_t ldx, float beta, int T, int K, int n_kunits, int n_ttiles, int band,
                        int n_chunks, int n_splits, float* __restrict__ part, WaitCtl ctl,
                        int inject_stall) {
   using C = Cfg<WT, CG, BT>;
@@ -768,6 +768,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // split contraction: raw partial sums to part[split] (beta in the reduce)
       float* out = part ? part + static_cast<int64_t>(tile / n_tiles1) * T * K : dX;
       const float b = part ? 0.0f : beta;
+      const int64_t ldo = part ? static_cast<int64_t>(K) : ldx;  // row stride of `out`
 #pragma unroll 1
       for (int cb = 0; cb < BT / 32; ++cb) {
         const int tb = tt * BT + 32 * cb;
@@ -776,7 +777,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // all loads of the column block first: one round trip, not 32
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            old[i] = (tb + i < T) ? out[static_cast<int64_t>(tb + i) * K + k] : 0.0f;
+            old[i] = (tb + i < T) ? out[static_cast<int64_t>(tb + i) * ldo + k] : 0.0f;
         }
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * eq) << 16) +
@@ -787,7 +788,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int i = 0; i < 32; ++i) {
             if (tb + i < T) {
               const float v = __uint_as_float(r[i]);
-              out[static_cast<int64_t>(tb + i) * K + k] = b != 0.0f ? fmaf(b, old[i], v) : v;
+              out[static_cast<int64_t>(tb + i) * ldo + k] = b != 0.0f ? fmaf(b, old[i], v) : v;
             }
           }
         }
@@ -862,7 +863,7 @@ TcPlan plan_tc(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force
 
 template <int WT, int CG, int BT>
 static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my, float* dX,
-                               float beta, int T, int K, const TcPlan& p, float* part,
+                               int64_t ldx, float beta, int T, int K, const TcPlan& p, float* part,
                                const DevInfo& dev, cudaStream_t stream, int inject) {
   using C = tc::Cfg<WT, CG, BT>;
   auto kern = tc::out_prod_tc_kernel<WT, CG, BT>;
@@ -892,20 +893,21 @@ static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my, flo
   }
   const int units = std::min(p.grid / CG, mc);
   cfg.gridDim = dim3(static_cast<unsigned>(units * CG), 1, 1);
-  return counted(cudaLaunchKernelEx(&cfg, kern, mw, my, dX, beta, T, K, p.n_kunits, p.n_ttiles, p.band,
+  return counted(cudaLaunchKernelEx(&cfg, kern, mw, my, dX, ldx, beta, T, K, p.n_kunits, p.n_ttiles, p.band,
                             p.n_chunks, p.n_splits, part, ctl, inject));
 }
 
 template <int WT>
 static cudaError_t launch_tc_w(const CUtensorMap& mw, const CUtensorMap& my, float* dX,
-                               float beta, int T, int K, const TcPlan& p, float* part,
+                               int64_t ldx, float beta, int T, int K, const TcPlan& p, float* part,
                                const DevInfo& dev, cudaStream_t stream, int inject) {
-  if (p.cg == 2) return launch_tc_t<WT, 2, 256>(mw, my, dX, beta, T, K, p, part, dev, stream, inject);
-  return launch_tc_t<WT, 1, 128>(mw, my, dX, beta, T, K, p, part, dev, stream, inject);
+  if (p.cg == 2)
+    return launch_tc_t<WT, 2, 256>(mw, my, dX, ldx, beta, T, K, p, part, dev, stream, inject);
+  return launch_tc_t<WT, 1, 128>(mw, my, dX, ldx, beta, T, K, p, part, dev, stream, inject);
 }
 
 cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
-                      int64_t ld_dy16, int64_t T, float* dX, float beta, float* part,
+                      int64_t ld_dy16, int64_t T, float* dX, int64_t dx_t, float beta, float* part,
                       const DevInfo& dev, cudaStream_t stream, int cg_force, int inject_stall) {
   TcPlan p = plan_tc(N, K, T, dev, cg_force);
   if (p.n_splits > 1 && part == nullptr) return cudaErrorInvalidValue;
@@ -935,11 +937,11 @@ cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   const int t = static_cast<int>(T), k = static_cast<int>(K);
   const cudaError_t e = with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
-    return launch_tc_w<decltype(wt)::value>(mw, my, dX, beta, t, k, p, partial, dev, stream,
+    return launch_tc_w<decltype(wt)::value>(mw, my, dX, dx_t, beta, t, k, p, partial, dev, stream,
                                             inject_stall);
   });
   if (e != cudaSuccess || p.n_splits == 1) return e;
-  return launch_reduce_partials(partial, p.n_splits, T * K, dX, beta, dev, stream);
+  return launch_reduce_partials(partial, p.n_splits, T, K, dX, dx_t, beta, dev, stream);
 }
 
 int64_t tc_partial_splits(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force) {

@@ -128,3 +128,26 @@ def test_product_path_has_no_cpu_fallback(lib, tmp_path):
         rg._lib = saved
     src = open(os.path.join(ROOT, "quantized_weight_out_gb300", "binding.py")).read()
     assert "oracle" not in src and "numpy" not in src
+
+
+def test_out_prod_ex_validation_before_any_launch(lib):
+    """The strided / batched entry checks every batch on the host first."""
+    A = 0x1000
+    base = dict(variant=0, wtype=inputs.Q8_0, W=A, N=64, K=256, w_batch_bytes=0, dY=A, T=8,
+                dy_t=64, dy_n=1, dy_batch=0, dX=A, dx_t=256, dx_batch=0, batch=2, beta=0.0)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return rg.rg_out_prod_ex(a["variant"], a["wtype"], a["W"], a["N"], a["K"], a["w_batch_bytes"],
+                                 a["dY"], a["T"], a["dy_t"], a["dy_n"], a["dy_batch"], a["dX"],
+                                 a["dx_t"], a["dx_batch"], a["batch"], a["beta"])
+    assert call(batch=0) == rg.RG_OK
+    assert call(batch=-1) == rg.RG_ERR_ARG
+    assert call(dx_t=255) == rg.RG_ERR_ARG              # rows shorter than K
+    assert call(dx_t=258) == rg.RG_ERR_ALIGN            # dX rows not 16-byte aligned
+    assert call(dy_n=0) == rg.RG_ERR_ARG
+    assert call(w_batch_bytes=8) == rg.RG_ERR_ALIGN
+    assert call(dx_batch=6) == rg.RG_ERR_ALIGN
+    assert call(dY=A + 2, dy_t=1, dy_n=8) == rg.RG_ERR_ALIGN
+    assert call(dY=A + 4) == rg.RG_ERR_ALIGN            # contiguous rows need 16-byte alignment
+    assert call(wtype=12) == rg.RG_ERR_TYPE
