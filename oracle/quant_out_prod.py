@@ -311,6 +311,26 @@ def out_prod(wtype: int, W, N: int, K: int, dY, T: int, dX0=None, beta: float = 
     return ref
 
 
+def mul_mat(wtype: int, W, N: int, K: int, X, T: int, Y0=None, beta: float = 0.0,
+            Wd=None) -> np.ndarray:
+    """F64 [T, N]: beta*Y0 + X @ deq(W)^T, the forward mul_mat(W, x) whose
+    backward OUT_PROD computes (llama.cpp fork PR "cuda: out_prod accepts a
+    quantized src0", commit message): Y[t, n] = sum_k X[t, k] * deq(W)[n, k],
+    contracted over the K values of each row of W."""
+    if Wd is None:
+        Wd = dequant(wtype, W, N, K)
+    X = np.asarray(X, dtype=np.float32).reshape(T, K)
+    ref = X.astype(np.float64) @ Wd.astype(np.float64).T
+    if beta != 0.0:
+        ref = ref + float(np.float32(beta)) * np.asarray(Y0, dtype=np.float32).reshape(T, N).astype(np.float64)
+    return ref
+
+
+def mul_mat_bound(X, Wd) -> np.ndarray:
+    """F64 [T, N]: sum_k |X[t, k]| * |deq(W)[n, k]|."""
+    return np.abs(np.asarray(X, dtype=np.float64)) @ np.abs(np.asarray(Wd, dtype=np.float64)).T
+
+
 def abs_bound(dY, Wd) -> np.ndarray:
     """F64 [T, K]: sum_n |dY[t, n]| * |deq(W)[n, k]|."""
     return np.abs(np.asarray(dY, dtype=np.float64)) @ np.abs(np.asarray(Wd, dtype=np.float64))

@@ -647,3 +647,48 @@ def test_dropped_beta_is_caught():
     good = oracle.out_prod(inputs.Q4_K, W, N, K, dY, T, dX0, 1.0)
     dropped = oracle.out_prod(inputs.Q4_K, W, N, K, dY, T)
     assert not np.allclose(good, dropped)
+
+
+# ----------------------------------------------------------------------------
+# the forward mul_mat(W, x) through the same decode
+
+@pytest.mark.parametrize("wtype", [inputs.Q4_K, inputs.Q8_0, inputs.F16])
+def test_mul_mat_one_hot_selects_columns(wtype):
+    """X[t] = e_{k0(t)} gives Y[t, :] = deq(W)[:, k0(t)] exactly: the forward
+    contracts over the K values of each row, not over the rows."""
+    N, K, T = 40, 512, 5
+    W = inputs.gen_weight(wtype, N, K, seed=81, stream=1)
+    Wd = oracle.dequant(wtype, W, N, K)
+    k0 = [(37 * t + 3) % K for t in range(T)]
+    X = np.zeros((T, K), np.float32)
+    X[np.arange(T), k0] = 1.0
+    Y = oracle.mul_mat(wtype, W, N, K, X, T)
+    for t in range(T):
+        assert np.array_equal(Y[t], Wd[:, k0[t]].astype(np.float64))
+
+
+def test_mul_mat_is_the_adjoint_of_out_prod():
+    """<dY, W x> = <W^T dY, x> for the same W: the forward and the backward
+    contract the same decoded matrix along opposite axes."""
+    N, K, T = 48, 768, 6
+    W = inputs.gen_weight(inputs.Q5_K, N, K, seed=82, stream=1)
+    X = inputs.normal_f32(82, 2, T * K, 1.0).reshape(T, K)
+    dY = inputs.normal_f32(82, 3, T * N, 1.0).reshape(T, N)
+    Y = oracle.mul_mat(inputs.Q5_K, W, N, K, X, T)
+    dX = oracle.out_prod(inputs.Q5_K, W, N, K, dY, T)
+    lhs = float(np.sum(dY.astype(np.float64) * Y))
+    rhs = float(np.sum(dX * X.astype(np.float64)))
+    assert abs(lhs - rhs) <= 1e-9 * (abs(lhs) + 1.0)
+
+
+def test_mul_mat_brute_force_and_beta():
+    N, K, T = 9, 64, 3
+    W = inputs.gen_weight(inputs.Q4_0, N, K, seed=83, stream=1)
+    X = inputs.normal_f32(83, 2, T * K, 1.0).reshape(T, K)
+    Y0 = inputs.normal_f32(83, 3, T * N, 1.0).reshape(T, N)
+    Wpy = _py_decode(inputs.Q4_0, bytes(W), N, K)
+    got = oracle.mul_mat(inputs.Q4_0, W, N, K, X, T, Y0, 0.5)
+    for t in range(T):
+        for n in range(N):
+            exact = math.fsum(float(X[t, k]) * Wpy[n][k] for k in range(K)) + 0.5 * float(Y0[t, n])
+            assert abs(got[t, n] - exact) <= 1e-12 * (abs(exact) + 1.0)
