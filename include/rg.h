@@ -198,6 +198,25 @@ int rg_out_prod_ex(int variant, int wtype, const void* W, int64_t N, int64_t K,
                    int64_t dy_batch, float* dX, int64_t dx_t, int64_t dx_batch, int64_t batch,
                    float beta, void* stream);
 
+/*
+ * The forward mul_mat(W, x) through the same resident weight (the op whose
+ * backward rg_out_prod is; llama.cpp fork PR "cuda: out_prod accepts a
+ * quantized src0", commit message):
+ *
+ *     Y[t, n] = beta * Y[t, n] + sum_{k < K} X[t, k] * deq(W)[n, k]
+ *
+ * X: [T, K] F32, Y: [T, N] F32 (read only when beta != 0), both row-major
+ * and 16-byte aligned; W as for rg_out_prod.  N must be a multiple of 8
+ * (RG_ERR_SHAPE).  deq(W)^T is written once per call as a 16-bit [K, N]
+ * operand (fp16; bf16 for F32 and BF16 W) in library-pool memory (2*N*K
+ * bytes, released on `stream` when the call's kernels finish), X is rounded
+ * the same way, and the tensor-core kernel contracts over K with F32
+ * accumulation: |err| <= 5e-3 * sum_k |X||deq W| + 1e-7.  T == 0 or N == 0:
+ * nothing to do; K == 0: Y = beta * Y.
+ */
+int rg_mul_mat(int wtype, const void* W, int64_t N, int64_t K, const float* X, int64_t T, float* Y,
+               float beta, void* stream);
+
 /* The variant RG_VARIANT_AUTO picks for this shape (ignores RG_VARIANT). */
 int rg_select_variant(int wtype, int64_t N, int64_t K, int64_t T);
 

@@ -492,6 +492,53 @@ int rg_select_variant(int wtype, int64_t N, int64_t K, int64_t T) {
   return select_variant(wtype, N, K, T);
 }
 
+int rg_mul_mat(int wtype, const void* W, int64_t N, int64_t K, const float* X, int64_t T, float* Y,
+               float beta, void* stream) {
+  if (!valid_wtype(wtype)) return RG_ERR_TYPE;
+  if (N < 0 || K < 0 || T < 0 || N > kMaxDim || K > kMaxDim || T > kMaxDim) return RG_ERR_ARG;
+  if (K % (is_quant(wtype) ? 256 : 8) || N % 8) return RG_ERR_SHAPE;
+  if (T == 0 || N == 0) return RG_OK;
+  if (!Y) return RG_ERR_ARG;
+  if (!aligned16(Y)) return RG_ERR_ALIGN;
+  if (K > 0) {
+    if (!W || !X) return RG_ERR_ARG;
+    if (!aligned16(W) || !aligned16(X)) return RG_ERR_ALIGN;
+  }
+  DevInfo* dev = nullptr;
+  int st = current_dev(&dev);
+  if (st != RG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return from_cuda(launch_scale(Y, T, N, N, beta, *dev, s));
+  // the tensor-core product with deq(W)^T [K, N] as a dense 16-bit weight of
+  // K rows: Y = X . deq(W)^T is an OUT_PROD over that weight
+  const bool bf16 = wtype == RG_BF16 || wtype == RG_F32;
+  const size_t wt_bytes = (static_cast<size_t>(K) * static_cast<size_t>(N) * 2 + 255) / 256 * 256;
+  const size_t x16 = tc_workspace(K, T);
+  const int64_t splits = tc_partial_splits(K, N, T, *dev, 0);
+  const size_t parts = (static_cast<size_t>(splits) * static_cast<size_t>(T) * static_cast<size_t>(N) * 4 + 255) / 256 * 256;
+  cudaMemPool_t pool{};
+  if ((st = pool_for(dev->device, &pool)) != RG_OK) return st;
+  void* buf = nullptr;
+  if (cudaMallocFromPoolAsync(&buf, wt_bytes + x16 + parts, pool, s) != cudaSuccess) return RG_ERR_CUDA;
+  char* b = static_cast<char*>(buf);
+  uint16_t* wt = reinterpret_cast<uint16_t*>(b);
+  uint16_t* xh = reinterpret_cast<uint16_t*>(b + wt_bytes);
+  float* part = reinterpret_cast<float*>(b + wt_bytes + x16);
+  cudaError_t e = launch_dequant_t16(wtype, W, N, K, bf16, wt, N, *dev, s);
+  const int64_t ld = tc_dy16_ld(K);
+  if (e == cudaSuccess) e = launch_convert_dy(X, T, K, K, 1, ld, bf16, xh, *dev, s);
+  cudaEvent_t ev0 = t_prof_before, ev1 = t_prof_after;
+  t_prof_before = t_prof_after = nullptr;
+  if (e == cudaSuccess && ev0) e = cudaEventRecord(ev0, s);
+  if (e == cudaSuccess)
+    e = launch_tc(bf16 ? RG_BF16 : RG_F16, wt, K, N, xh, ld, T, Y, N, beta, part, *dev, s, 0,
+                  env().inject_stall);
+  if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, s);
+  const cudaError_t f = cudaFreeAsync(buf, s);
+  if (e == cudaSuccess) e = f;
+  return from_cuda(e);
+}
+
 int rg_plan(int variant, int wtype, int64_t N, int64_t K, int64_t T, rg_plan_info* out) {
   if (!out) return RG_ERR_ARG;
   if (!valid_wtype(wtype)) return RG_ERR_TYPE;

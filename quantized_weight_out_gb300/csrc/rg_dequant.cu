@@ -94,6 +94,62 @@ __global__ void __launch_bounds__(256) dequant_bytes_kernel(const uint8_t* __res
   }
 }
 
+// deq(W)^T as 16-bit [K, N] (rows ldo values apart): the dense operand of
+// the forward mul_mat.  A CTA decodes 32 rows x 256 values of W exactly to
+// F32 (warp w: rows w, w+8, ...; lane l: values 8l .. 8l+7), stages them in
+// shared memory, and writes the 256 x 32 transposed tile rounded to fp16 (or
+// bf16: BF16OUT), one output row of 32 values per warp step.
+template <int WT, bool BF16OUT>
+__global__ void __launch_bounds__(256) dequant_t16_kernel(const uint8_t* __restrict__ W, int64_t N,
+                                                          int64_t K, int64_t rb,
+                                                          uint16_t* __restrict__ out, int64_t ldo) {
+  __shared__ __align__(16) float tile[32][260];  // [n][k], rows 16-byte aligned
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t k0 = static_cast<int64_t>(blockIdx.x) * 256, n0 = static_cast<int64_t>(blockIdx.y) * 32;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int nl = warp + 8 * i;
+    const int64_t n = n0 + nl, k = k0 + 8 * lane;
+    float v[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+    if (n < N && k < K) decode8_f32<WT>(W + n * rb, static_cast<int>(k), v);
+    float4* t = reinterpret_cast<float4*>(&tile[nl][8 * lane]);
+    t[0] = make_float4(v[0], v[1], v[2], v[3]);
+    t[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+  __syncthreads();
+  for (int kl = warp; kl < 256; kl += 8) {
+    const int64_t k = k0 + kl, n = n0 + lane;
+    if (k < K && n < N) {
+      const float x = tile[lane][kl];
+      if constexpr (BF16OUT) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(x);
+        out[k * ldo + n] = *reinterpret_cast<const uint16_t*>(&h);
+      } else {
+        const __half h = __float2half_rn(x);
+        out[k * ldo + n] = *reinterpret_cast<const uint16_t*>(&h);
+      }
+    }
+  }
+}
+
+cudaError_t launch_dequant_t16(int wtype, const void* W, int64_t N, int64_t K, bool bf16,
+                               uint16_t* out, int64_t ldo, const DevInfo& dev, cudaStream_t stream) {
+  (void)dev;
+  const int64_t rb = K / block_values(wtype) * block_bytes(wtype);
+  const int64_t gy = (N + 31) / 32;
+  if (gy > 65535) return cudaErrorInvalidConfiguration;
+  const dim3 grid(static_cast<unsigned>((K + 255) / 256), static_cast<unsigned>(gy));
+  const uint8_t* w = static_cast<const uint8_t*>(W);
+  return with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
+    constexpr int WT = decltype(wt)::value;
+    if (bf16)
+      dequant_t16_kernel<WT, true><<<grid, 256, 0, stream>>>(w, N, K, rb, out, ldo);
+    else
+      dequant_t16_kernel<WT, false><<<grid, 256, 0, stream>>>(w, N, K, rb, out, ldo);
+    return counted(cudaGetLastError());
+  });
+}
+
 static int grid_for(int64_t work_items, int threads, const DevInfo& dev) {
   const int64_t blocks = (work_items + threads - 1) / threads;
   const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;

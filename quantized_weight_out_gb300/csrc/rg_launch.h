@@ -63,6 +63,10 @@ struct Layout {
   int64_t dy_t, dy_n, dx_t;
 };
 
+// deq(W)^T as fp16 (bf16 when `bf16`) [K, N], rows ldo values apart.
+cudaError_t launch_dequant_t16(int wtype, const void* W, int64_t N, int64_t K, bool bf16,
+                               uint16_t* out, int64_t ldo, const DevInfo& dev, cudaStream_t stream);
+
 // dY [T, N] (strided) F32 -> out [T, ld] fp16 (bf16 when `bf16`), rows padded to ld.
 cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t dy_t, int64_t dy_n,
                               int64_t ld, bool bf16, uint16_t* out, const DevInfo& dev,

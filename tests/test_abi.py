@@ -151,3 +151,13 @@ def test_out_prod_ex_validation_before_any_launch(lib):
     assert call(dY=A + 2, dy_t=1, dy_n=8) == rg.RG_ERR_ALIGN
     assert call(dY=A + 4) == rg.RG_ERR_ALIGN            # contiguous rows need 16-byte alignment
     assert call(wtype=12) == rg.RG_ERR_TYPE
+
+
+def test_mul_mat_validation(lib):
+    A = 0x1000
+    assert rg.rg_mul_mat(12, A, 64, 256, A, 4, A, 0.0) == rg.RG_ERR_TYPE
+    assert rg.rg_mul_mat(inputs.Q8_0, A, 60, 256, A, 4, A, 0.0) == rg.RG_ERR_SHAPE
+    assert rg.rg_mul_mat(inputs.Q8_0, A, 64, 255, A, 4, A, 0.0) == rg.RG_ERR_SHAPE
+    assert rg.rg_mul_mat(inputs.Q8_0, A, 64, 256, A, 0, A, 0.0) == rg.RG_OK
+    assert rg.rg_mul_mat(inputs.Q8_0, A + 4, 64, 256, A, 4, A, 0.0) == rg.RG_ERR_ALIGN
+    assert rg.rg_mul_mat(inputs.Q8_0, A, 64, 256, A, 4, None, 0.0) == rg.RG_ERR_ARG

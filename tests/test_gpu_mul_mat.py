@@ -1,0 +1,83 @@
+"""rg_mul_mat, the forward Y = X . deq(W)^T, against the oracle."""
+import numpy as np
+import pytest
+
+import oracle
+from quantized_weight_out_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+
+@pytest.fixture(scope="module")
+def rg():
+    from quantized_weight_out_gb300 import binding, build
+    build.build()
+    binding.load()
+    return binding
+
+
+def _run(rg, wtype, W, N, K, X, T, Y0=None, beta=0.0):
+    dev, s = torch.device("cuda:0"), torch.cuda.current_stream()
+    Y = torch.from_numpy(Y0).to(dev) if Y0 is not None else torch.full((T, N), float("nan"), device=dev)
+    rg.check(rg.rg_mul_mat(wtype, torch.from_numpy(W).to(dev), N, K, torch.from_numpy(X).to(dev), T, Y,
+                           beta, s), "rg_mul_mat")
+    rg.check(rg.rg_check(s))
+    return Y.cpu().numpy()
+
+
+@pytest.mark.parametrize("wtype", inputs.ALL_TYPES)
+@pytest.mark.parametrize("shape", [(208, 512, 300), (64, 256, 1), (1000, 768, 130), (72, 1024, 33)])
+def test_mul_mat_parity(rg, wtype, shape):
+    N, K, T = shape
+    W = inputs.gen_weight(wtype, N, K, seed=91, stream=1)
+    X = inputs.normal_f32(91, 2, T * K, 1e-2).reshape(T, K)
+    Wd = oracle.dequant(wtype, W, N, K)
+    ref = oracle.mul_mat(wtype, W, N, K, X, T, Wd=Wd)
+    bnd = oracle.mul_mat_bound(X, Wd)
+    got = _run(rg, wtype, W, N, K, X, T)
+    err = np.abs(got.astype(np.float64) - ref)
+    assert np.all(err <= 5e-3 * bnd + 1e-7), float((err / (bnd + 1e-30)).max())
+
+
+def test_mul_mat_beta_and_one_hot(rg):
+    N, K, T, wtype = 256, 512, 40, inputs.Q4_K
+    W = inputs.gen_weight(wtype, N, K, seed=92, stream=1)
+    Wd = oracle.dequant(wtype, W, N, K)
+    # one-hot X selects columns of deq(W), rounded once to fp16 on the way in
+    k0 = (41 * np.arange(T) + 5) % K
+    X = np.zeros((T, K), np.float32)
+    X[np.arange(T), k0] = 1.0
+    got = _run(rg, wtype, W, N, K, X, T)
+    want = Wd[:, k0].T.astype(np.float16).astype(np.float32)
+    assert np.array_equal(got, want)
+    # beta accumulates
+    X = inputs.normal_f32(92, 2, T * K, 1e-2).reshape(T, K)
+    Y0 = inputs.normal_f32(92, 3, T * N, 1e-3).reshape(T, N)
+    got = _run(rg, wtype, W, N, K, X, T, Y0, 1.0)
+    ref = oracle.mul_mat(wtype, W, N, K, X, T, Y0, 1.0, Wd=Wd)
+    bnd = oracle.mul_mat_bound(X, Wd) + np.abs(Y0) * 2.0 ** -24 / 5e-3
+    assert np.all(np.abs(got - ref) <= 5e-3 * bnd + 1e-7)
+
+
+def test_mul_mat_large_splits_and_waves(rg):
+    """A long contraction (K = 14336) with few outputs splits over CTAs; a
+    wide one runs many pair tiles."""
+    for (N, K, T) in [(256, 14336, 64), (4096, 512, 1100)]:
+        wtype = inputs.Q8_0
+        W = inputs.gen_weight(wtype, N, K, seed=93, stream=1)
+        X = inputs.normal_f32(93, 2, T * K, 1e-2).reshape(T, K)
+        Wd = oracle.dequant(wtype, W, N, K)
+        got = _run(rg, wtype, W, N, K, X, T)
+        ref = oracle.mul_mat(wtype, W, N, K, X, T, Wd=Wd)
+        assert np.all(np.abs(got - ref) <= 5e-3 * oracle.mul_mat_bound(X, Wd) + 1e-7)
+
+
+def test_mul_mat_shape_rules(rg):
+    dev = torch.device("cuda:0")
+    W = torch.zeros(100 * inputs.row_bytes(inputs.Q8_0, 256), dtype=torch.uint8, device=dev)
+    X = torch.zeros((4, 256), device=dev)
+    Y = torch.zeros((4, 100), device=dev)
+    assert rg.rg_mul_mat(inputs.Q8_0, W, 100, 256, X, 4, Y, 0.0) == rg.RG_ERR_SHAPE   # N % 8
+    assert rg.rg_mul_mat(inputs.Q8_0, W, 96, 200, X, 4, Y, 0.0) == rg.RG_ERR_SHAPE    # K % 256
