@@ -211,6 +211,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="layer7b_t8192")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--op", default="out_prod", choices=["out_prod", "mul_mat"],
+                    help="out_prod (the backward, default) or mul_mat (the forward rg_mul_mat)")
     ap.add_argument("--cpu-rows", type=int, default=1024, help="dY rows per call, CPU baseline sample")
     ap.add_argument("--ref-rows", type=int, default=32, help="dY rows per call, reference-arm step")
     ap.add_argument("--ref-wrows", type=int, default=512, help="W rows per call, reference-arm step")
@@ -527,10 +529,102 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def run_mul_mat(args):
+    """The forward Y = X . deq(W)^T (rg_mul_mat) on the workload's shapes:
+    same timing rules as the backward (warm-up, events, clocks, the GEMM
+    alone against the measured peak); inputs resident, no e2e leg."""
+    import torch
+    world, rank, local = _dist()
+    from quantized_weight_out_gb300 import binding as rg
+    from quantized_weight_out_gb300 import build as rgbuild
+    rgbuild.build()
+    rg.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    problems = inputs.WORKLOADS[args.workload]
+    bufs = []
+    for p in problems:
+        X = inputs.normal_f32(p.seed, 2 + p.stream_base, p.T * p.K, 1e-2).reshape(p.T, p.K)
+        bufs.append((torch.from_numpy(p.weight()).to(dev), torch.from_numpy(X).to(dev),
+                     torch.zeros((p.T, p.N), device=dev)))
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        for i, p in enumerate(problems):
+            W, X, Y = bufs[i]
+            if evs is not None:
+                evs[i][0].record(stream)
+                rg.rg_profile_next_gemm(evs[i][2], evs[i][3])
+            st = rg.rg_mul_mat(p.wtype, W, p.N, p.K, X, p.T, Y, 0.0, stream)
+            if evs is not None:
+                evs[i][1].record(stream)
+            if st != 0:
+                raise RuntimeError(f"rg_mul_mat: {rg.strerror(st)}")
+
+    for _ in range(args.warmup):
+        step()
+    rg.check(rg.rg_check(stream), "warmup")
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in problems]
+           for _ in range(args.steps)]
+    for row in evs:
+        for quad in row:
+            for e in quad:
+                e.record(stream)
+    sampler = ClockSampler(_bus_id(torch, dev))
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = rg.rg_launch_count()
+    ev0.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    ev1.record(stream)
+    launches = rg.rg_launch_count() - launches0
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    rg.check(rg.rg_check(stream), "timed region")
+    ms_step = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dev)
+    flops_step = sum(p.flops for p in problems)
+    gemm_ms = sum(statistics.mean(evs[k][i][2].elapsed_time(evs[k][i][3]) for k in range(args.steps))
+                  for i in range(len(problems)))
+    peaks, src = _peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    achieved = flops_step / (gemm_ms * 1e-3) / 1e12
+    calls = []
+    for i, p in enumerate(problems):
+        t = statistics.median(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(args.steps))
+        calls.append({"name": p.name, "wtype": inputs.TYPE_NAMES[p.wtype], "N": p.N, "K": p.K, "T": p.T,
+                      "ms": t, "tflops": p.flops / (t * 1e-3) / 1e12})
+    line = {"metric": "mul_mat TFLOP/s (2*T*N*K / time)", "op": "mul_mat",
+            "value": job_tflops(flops_step, ms_step, world), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": _dtype_name(problems), "data": "synthetic",
+            "config": {"workload": args.workload, "calls": len(problems),
+                       "flops_per_step": flops_step, "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_source": f"{src} bf16_tflops_sustained",
+                         "kernel": "out_prod_tc_kernel on the transposed 16-bit copy of deq(W)"},
+            "gpu_launches": launches, "clocks": clocks, "per_call": calls}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "mul_mat":
+        run_mul_mat(args)
     else:
         run_ours(args)
 
