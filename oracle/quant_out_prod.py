@@ -46,6 +46,9 @@ Block formats (little-endian), ggml's GGUF block types:
 * F16 / BF16: 2 B per value.
 * F32: 4 B per value, the value itself.
 
+The adapter variant (out_prod_lora) adds scale * (dY @ B) @ A for a
+low-rank adapter A [r, K], B [N, r] beside the resident W; see its docstring.
+
 Parity pins for each function live in tests/test_oracle.py.
 """
 from __future__ import annotations
@@ -334,6 +337,41 @@ def mul_mat_bound(X, Wd) -> np.ndarray:
 def abs_bound(dY, Wd) -> np.ndarray:
     """F64 [T, K]: sum_n |dY[t, n]| * |deq(W)[n, k]|."""
     return np.abs(np.asarray(dY, dtype=np.float64)) @ np.abs(np.asarray(Wd, dtype=np.float64))
+
+
+def out_prod_lora(wtype: int, W, N: int, K: int, dY, T: int, lora_a, lora_b, r: int,
+                  scale: float, dX0=None, beta: float = 0.0, Wd=None) -> np.ndarray:
+    """F64 [T, K]: the input gradient through the resident base weight AND a
+    low-rank adapter beside it,
+
+        dX = beta*dX0 + dY @ deq(W) + scale * (dY @ B) @ A,
+
+    for the forward y = x deq(W)^T + scale * (x A^T) B^T with A [r, K] (the
+    adapter's down projection) and B [N, r] (its up projection).  The pages
+    name the use (llama.cpp fork PR "cuda: out_prod accepts a quantized src0",
+    commit message: a LoRA training on a resident Q4_K_M base) without the
+    adapter's formula; this is the plain low-rank-adapter reading.
+
+    Steps, in this order: (1) the base term as out_prod; (2) U = dY @ B over
+    the N outputs, F64 (every F32 x F32 product exact); (3) scale * U @ A over
+    the r ranks, F64, added to (1)."""
+    ref = out_prod(wtype, W, N, K, dY, T, dX0, beta, Wd)
+    if r == 0:
+        return ref
+    dY64 = np.asarray(dY, dtype=np.float32).reshape(T, N).astype(np.float64)
+    A = np.asarray(lora_a, dtype=np.float32).reshape(r, K).astype(np.float64)
+    B = np.asarray(lora_b, dtype=np.float32).reshape(N, r).astype(np.float64)
+    U = dY64 @ B
+    return ref + float(np.float32(scale)) * (U @ A)
+
+
+def lora_bound(dY, lora_a, lora_b, scale: float) -> np.ndarray:
+    """F64 [T, K]: |scale| * sum_j (sum_n |dY[t, n]| |B[n, j]|) |A[j, k]|, the
+    adapter term's share of the acceptance bound."""
+    dY = np.abs(np.asarray(dY, dtype=np.float64))
+    A = np.abs(np.asarray(lora_a, dtype=np.float64))
+    B = np.abs(np.asarray(lora_b, dtype=np.float64))
+    return abs(float(np.float32(scale))) * ((dY @ B) @ A)
 
 
 def out_prod_at(Wd, dY, ts, ks, dX0=None, beta: float = 0.0):

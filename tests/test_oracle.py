@@ -692,3 +692,124 @@ def test_mul_mat_brute_force_and_beta():
         for n in range(N):
             exact = math.fsum(float(X[t, k]) * Wpy[n][k] for k in range(K)) + 0.5 * float(Y0[t, n])
             assert abs(got[t, n] - exact) <= 1e-12 * (abs(exact) + 1.0)
+
+
+# ----------------------------------------------------------------------------
+# the input gradient through the base weight plus a low-rank adapter
+
+def _lora_fixture(golden_dir):
+    rows = dict((r[0], r[1:]) for r in _read(golden_dir, "lora_tiny.txt"))
+    N, K, T, R = (int(rows[x][0]) for x in ("N", "K", "T", "R"))
+    W = np.array([int(c, 16) for c in rows["W"]], np.uint16).view(np.uint8)
+    f = lambda key: np.array([float(v) for v in rows[key]], np.float32)  # noqa: E731
+    return (N, K, T, R, float(rows["scale"][0]), float(rows["beta"][0]), W,
+            f("dY").reshape(T, N), f("B").reshape(N, R), f("A").reshape(R, K),
+            f("dX0").reshape(T, K), f("dX").reshape(T, K))
+
+
+def test_lora_hand_example(golden_dir):
+    N, K, T, R, s, beta, W, dY, B, A, dX0, want = _lora_fixture(golden_dir)
+    got = oracle.out_prod_lora(inputs.F16, W, N, K, dY, T, A, B, R, s, dX0, beta)
+    assert np.array_equal(got, want.astype(np.float64))
+
+
+def test_lora_without_adapter_is_out_prod():
+    """scale 0, or rank 0, leaves the base gradient bit for bit."""
+    N, K, T, R = 24, 256, 3, 4
+    W = inputs.gen_weight(inputs.Q4_K, N, K, seed=91, stream=1)
+    dY = inputs.normal_f32(91, 2, T * N, 1.0).reshape(T, N)
+    A = inputs.normal_f32(91, 3, R * K, 1.0).reshape(R, K)
+    B = inputs.normal_f32(91, 4, N * R, 1.0).reshape(N, R)
+    base = oracle.out_prod(inputs.Q4_K, W, N, K, dY, T)
+    assert np.array_equal(oracle.out_prod_lora(inputs.Q4_K, W, N, K, dY, T, A, B, R, 0.0), base)
+    assert np.array_equal(oracle.out_prod_lora(inputs.Q4_K, W, N, K, dY, T, A[:0], B[:, :0], 0, 2.0),
+                          base)
+
+
+def test_lora_one_hot_row_closed_form():
+    """dY[t] = e_n: dX[t] = deq(W)[n] + scale * sum_j B[n, j] A[j] (the
+    adapter's row n of B A), with one nonzero per sum up to the r ranks."""
+    N, K, T, R = 20, 64, 4, 3
+    W = inputs.gen_weight(inputs.Q8_0, N, K, seed=92, stream=1)
+    Wd = oracle.dequant(inputs.Q8_0, W, N, K)
+    A = inputs.normal_f32(92, 3, R * K, 1.0).reshape(R, K)
+    B = inputs.normal_f32(92, 4, N * R, 1.0).reshape(N, R)
+    rows = [3, 0, 19, 11]
+    dY = np.zeros((T, N), np.float32)
+    dY[np.arange(T), rows] = 1.0
+    got = oracle.out_prod_lora(inputs.Q8_0, W, N, K, dY, T, A, B, R, 0.75)
+    for t, n in enumerate(rows):
+        want = [float(Wd[n, k]) + 0.75 * math.fsum(float(B[n, j]) * float(A[j, k]) for j in range(R))
+                for k in range(K)]
+        assert np.allclose(got[t], want, rtol=1e-15, atol=1e-15)
+
+
+def test_lora_brute_force():
+    """Pure-Python sums with exact rounding over both contractions."""
+    N, K, T, R = 7, 32, 3, 5
+    W = inputs.gen_weight(inputs.Q4_0, N, K, seed=93, stream=1)
+    Wpy = _py_decode(inputs.Q4_0, bytes(W), N, K)
+    dY = inputs.normal_f32(93, 2, T * N, 1.0).reshape(T, N)
+    A = inputs.normal_f32(93, 3, R * K, 1.0).reshape(R, K)
+    B = inputs.normal_f32(93, 4, N * R, 1.0).reshape(N, R)
+    dX0 = inputs.normal_f32(93, 5, T * K, 1.0).reshape(T, K)
+    got = oracle.out_prod_lora(inputs.Q4_0, W, N, K, dY, T, A, B, R, -1.5, dX0, 0.25)
+    for t in range(T):
+        U = [math.fsum(float(dY[t, n]) * float(B[n, j]) for n in range(N)) for j in range(R)]
+        for k in range(K):
+            exact = (math.fsum(float(dY[t, n]) * Wpy[n][k] for n in range(N))
+                     - 1.5 * math.fsum(U[j] * float(A[j, k]) for j in range(R))
+                     + 0.25 * float(dX0[t, k]))
+            assert abs(got[t, k] - exact) <= 1e-12 * (abs(exact) + 1.0)
+
+
+def test_lora_is_the_adjoint_of_the_adapted_forward():
+    """<dY, y(x)> = <dX(dY), x> for y = x deq(W)^T + scale (x A^T) B^T: the
+    backward contracts the adapter's matrices along the opposite axes."""
+    N, K, T, R = 40, 512, 6, 8
+    W = inputs.gen_weight(inputs.Q5_K, N, K, seed=94, stream=1)
+    X = inputs.normal_f32(94, 2, T * K, 1.0).reshape(T, K).astype(np.float64)
+    dY = inputs.normal_f32(94, 3, T * N, 1.0).reshape(T, N)
+    A = inputs.normal_f32(94, 4, R * K, 1.0).reshape(R, K)
+    B = inputs.normal_f32(94, 5, N * R, 1.0).reshape(N, R)
+    Y = oracle.mul_mat(inputs.Q5_K, W, N, K, X.astype(np.float32), T)
+    for t in range(T):   # the adapter's forward, written out on its own
+        for n in range(N):
+            Y[t, n] += 0.5 * sum(float(B[n, j]) * float(np.dot(X[t], A[j].astype(np.float64)))
+                                 for j in range(R))
+    dX = oracle.out_prod_lora(inputs.Q5_K, W, N, K, dY, T, A, B, R, 0.5)
+    lhs = float(np.sum(dY.astype(np.float64) * Y))
+    rhs = float(np.sum(dX * X))
+    assert abs(lhs - rhs) <= 1e-9 * (abs(lhs) + 1.0)
+
+
+def test_lora_bound_covers_terms():
+    N, K, T, R = 16, 64, 2, 3
+    dY = inputs.normal_f32(95, 2, T * N, 1.0).reshape(T, N)
+    A = inputs.normal_f32(95, 3, R * K, 1.0).reshape(R, K)
+    B = inputs.normal_f32(95, 4, N * R, 1.0).reshape(N, R)
+    bnd = oracle.lora_bound(dY, A, B, -2.0)
+    for t in range(T):
+        for k in range(K):
+            terms = [abs(2.0 * float(dY[t, n]) * float(B[n, j]) * float(A[j, k]))
+                     for n in range(N) for j in range(R)]
+            assert abs(bnd[t, k] - math.fsum(terms)) <= 1e-12 * bnd[t, k]
+
+
+@pytest.mark.parametrize("mutant", ["b_transposed_role", "dropped_scale", "a_rows_reversed",
+                                    "u_from_base"])
+def test_lora_mutants_are_caught(golden_dir, mutant):
+    """Plausible mistakes in a copy of the adapter term fail the hand example."""
+    N, K, T, R, s, beta, W, dY, B, A, dX0, want = _lora_fixture(golden_dir)
+    base = oracle.out_prod(inputs.F16, W, N, K, dY, T, dX0, beta)
+    dY64, A64, B64 = dY.astype(np.float64), A.astype(np.float64), B.astype(np.float64)
+    if mutant == "b_transposed_role":
+        term = s * ((dY64 @ B64.T) @ A64)          # square fixture: shapes still fit
+    elif mutant == "dropped_scale":
+        term = (dY64 @ B64) @ A64
+    elif mutant == "a_rows_reversed":
+        term = s * ((dY64 @ B64) @ A64[::-1])
+    else:
+        Wd = oracle.dequant(inputs.F16, W, N, K).astype(np.float64)
+        term = s * (((dY64 @ Wd) @ B64) @ A64)
+    assert not np.array_equal(base + term, want.astype(np.float64))
