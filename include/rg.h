@@ -217,6 +217,36 @@ int rg_out_prod_ex(int variant, int wtype, const void* W, int64_t N, int64_t K,
 int rg_mul_mat(int wtype, const void* W, int64_t N, int64_t K, const float* X, int64_t T, float* Y,
                float beta, void* stream);
 
+/*
+ * The input gradient through the resident weight AND a low-rank adapter
+ * (LoRA) trained beside it (llama.cpp fork PR "cuda: out_prod accepts a
+ * quantized src0", commit message: a LoRA training on a resident quantized
+ * base).  For the forward y = x deq(W)^T + scale * (x A^T) B^T:
+ *
+ *     dX = beta * dX + dY . deq(W) + scale * (dY . B) . A
+ *
+ * lora_a: A [rank, K] F32 row-major (the adapter's down projection);
+ * lora_b: B [N, rank] F32 row-major (its up projection); both 16-byte aligned
+ * (RG_ERR_ALIGN), read only; rank in [0, 1024] (RG_ERR_ARG below 0,
+ * RG_ERR_SHAPE above).  W, dY, dX, T, beta and the variant as for
+ * rg_out_prod_variant (contiguous dY [T, N] and dX [T, K]).  rank == 0 is
+ * rg_out_prod_variant; N == 0 leaves dX = beta * dX.
+ *
+ * Tensor-core variants: U = dY . B is itself an OUT_PROD over B's 16-bit
+ * copy, and the base product's kernel takes U's columns and scale * A's rows
+ * (16-bit, the kind the base operands use) as extra contraction chunks, so
+ * the adapter term lands in the same F32 accumulator as dY . deq(W).  Its
+ * error: |err| <= 5e-3 * sum_n |dY||deq W| + 1e-2 * |scale| *
+ * sum_j (sum_n |dY||B|)|A| + 1e-7 (dY, B, U and A each rounded to 16 bits).
+ * fp16 kinds (quantized and F16 W) need U and scale * A within the fp16
+ * range, like dY.  Other variants: the base product as they compute it, then
+ * U and scale * U . A in F32 (about 1e-5 relative to the same sums).
+ * Workspace from the library's stream-ordered pool, as rg_out_prod.
+ */
+int rg_out_prod_lora(int variant, int wtype, const void* W, int64_t N, int64_t K, const float* dY,
+                     int64_t T, float* dX, float beta, const float* lora_a, const float* lora_b,
+                     int64_t rank, float scale, void* stream);
+
 /* The variant RG_VARIANT_AUTO picks for this shape (ignores RG_VARIANT). */
 int rg_select_variant(int wtype, int64_t N, int64_t K, int64_t T);
 

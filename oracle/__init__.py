@@ -10,5 +10,5 @@ from .quant_out_prod import (  # noqa: F401
     decode_q8_0, decode_q4_0, decode_q4_k, decode_f16, decode_bf16,
     decode_q4_1, decode_q5_0, decode_q5_1, decode_q5_k, decode_q6_k, decode_f32,
     dequant, row_bytes, out_prod, abs_bound, out_prod_at, q4_k_scale_min, mul_mat, mul_mat_bound,
-    out_prod_lora, lora_bound,
+    out_prod_lora, lora_bound, lora_at,
 )

@@ -389,3 +389,19 @@ def out_prod_at(Wd, dY, ts, ks, dX0=None, beta: float = 0.0):
     if beta != 0.0:
         ref = ref + float(np.float32(beta)) * np.asarray(dX0, dtype=np.float32)[ts, ks].astype(np.float64)
     return ref, bnd
+
+
+def lora_at(dY, lora_a, lora_b, scale: float, ts, ks):
+    """The adapter term at pairs (ts[i], ks[i]) one by one: (value, bound) of
+    scale * sum_j (dY[t] . B[:, j]) A[j, k] and of its absolute terms, F64,
+    for parity checks on sizes whose full product is too large to form."""
+    ts = np.asarray(ts, dtype=np.int64)
+    ks = np.asarray(ks, dtype=np.int64)
+    sc = float(np.float32(scale))
+    rows = np.asarray(dY, dtype=np.float32)[ts].astype(np.float64)          # [S, N]
+    B = np.asarray(lora_b, dtype=np.float32).astype(np.float64)             # [N, r]
+    cols = np.asarray(lora_a, dtype=np.float32)[:, ks].T.astype(np.float64)  # [S, r]
+    U = rows @ B                                                             # [S, r]
+    Ua = np.abs(rows) @ np.abs(B)
+    return sc * np.einsum("sr,sr->s", U, cols), abs(sc) * np.einsum("sr,sr->s", Ua, np.abs(cols))
+

@@ -54,6 +54,7 @@ SIGNATURES = [
     ("rg_out_prod_noalloc", _I, [_I, _VP, _I64, _I64, _VP, _I64, _VP, _F, _VP]),
     ("rg_plan", _I, [_I, _I, _I64, _I64, _I64, ctypes.POINTER(rg_plan_info)]),
     ("rg_mul_mat", _I, [_I, _VP, _I64, _I64, _VP, _I64, _VP, _F, _VP]),
+    ("rg_out_prod_lora", _I, [_I, _I, _VP, _I64, _I64, _VP, _I64, _VP, _F, _VP, _VP, _I64, _F, _VP]),
     ("rg_out_prod_ex", _I, [_I, _I, _VP, _I64, _I64, _I64, _VP, _I64, _I64, _I64, _I64, _VP, _I64,
                             _I64, _I64, _F, _VP]),
     ("rg_launch_count", ctypes.c_uint64, []),
@@ -128,6 +129,12 @@ def rg_out_prod_ex(variant, wtype, W, N, K, w_batch_bytes, dY, T, dy_t, dy_n, dy
 
 def rg_mul_mat(wtype, W, N, K, X, T, Y, beta, stream=None) -> int:
     return load().rg_mul_mat(wtype, _ptr(W), N, K, _ptr(X), T, _ptr(Y), beta, _stream(stream))
+
+
+def rg_out_prod_lora(variant, wtype, W, N, K, dY, T, dX, beta, lora_a, lora_b, rank, scale,
+                     stream=None) -> int:
+    return load().rg_out_prod_lora(variant, wtype, _ptr(W), N, K, _ptr(dY), T, _ptr(dX), beta,
+                                   _ptr(lora_a), _ptr(lora_b), rank, scale, _stream(stream))
 
 
 def rg_workspace_bytes(variant, wtype, N, K, T) -> int:

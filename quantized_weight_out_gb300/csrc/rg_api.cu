@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -537,6 +539,94 @@ int rg_mul_mat(int wtype, const void* W, int64_t N, int64_t K, const float* X, i
   const cudaError_t f = cudaFreeAsync(buf, s);
   if (e == cudaSuccess) e = f;
   return from_cuda(e);
+}
+
+int rg_out_prod_lora(int variant, int wtype, const void* W, int64_t N, int64_t K, const float* dY,
+                     int64_t T, float* dX, float beta, const float* lora_a, const float* lora_b,
+                     int64_t rank, float scale, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout lay{N, 1, K};
+  bool empty = false;
+  int st = validate(wtype, W, N, K, dY, T, dX, lay, &empty);
+  if (st != RG_OK) return st;
+  if (rank < 0) return RG_ERR_ARG;
+  if (rank > 1024) return RG_ERR_SHAPE;
+  if (variant < RG_VARIANT_AUTO || variant > RG_VARIANT_TC_PAIR) return RG_ERR_TYPE;
+  // no adapter term: the base product alone (N == 0 makes dY . B zero)
+  if (empty || rank == 0 || N == 0)
+    return run(variant, wtype, W, N, K, dY, T, dX, beta, nullptr, 0, true, s, lay);
+  if (!lora_a || !lora_b) return RG_ERR_ARG;
+  if (!aligned16(lora_a) || !aligned16(lora_b)) return RG_ERR_ALIGN;
+  if (variant == RG_VARIANT_AUTO) variant = select_variant(wtype, N, K, T);
+  if (variant != RG_VARIANT_SIMT32 && !aligned_rows(wtype, K)) return RG_ERR_SHAPE;
+  DevInfo* dev = nullptr;
+  if ((st = current_dev(&dev)) != RG_OK) return st;
+  cudaMemPool_t pool{};
+  if ((st = pool_for(dev->device, &pool)) != RG_OK) return st;
+
+  if (!is_tc(variant)) {
+    // the base product as the variant computes it, then the F32 adapter term
+    if ((st = run(variant, wtype, W, N, K, dY, T, dX, beta, nullptr, 0, true, s, lay)) != RG_OK)
+      return st;
+    const int parts = adapter_down_parts(N, T, rank, *dev);
+    void* buf = nullptr;
+    const size_t bytes = static_cast<size_t>(parts) * static_cast<size_t>(T) * static_cast<size_t>(rank) * 4;
+    if (cudaMallocFromPoolAsync(&buf, bytes, pool, s) != cudaSuccess) return RG_ERR_CUDA;
+    cudaError_t e = launch_adapter_f32(dY, N, T, lora_a, lora_b, rank, K, scale, dX, K,
+                                       static_cast<float*>(buf), parts, *dev, s);
+    const cudaError_t f = cudaFreeAsync(buf, s);
+    return from_cuda(e == cudaSuccess ? f : e);
+  }
+
+  // tensor cores: dY's 16-bit copy gets U = dY . B after its own columns,
+  // scale * A joins W's rows as extra contraction chunks of the base product
+  const bool bf16 = wtype == RG_BF16 || wtype == RG_F32;
+  const int cg = cg_force_of(variant);
+  const int64_t ld = tc_adapter_cols(N, rank);
+  const int64_t r8 = (rank + 7) / 8 * 8;
+  auto up256 = [](size_t b) { return (b + 255) / 256 * 256; };
+  const size_t dy_bytes = up256(static_cast<size_t>(T) * static_cast<size_t>(ld) * 2);
+  const size_t w_bytes = tc_w16_bytes(wtype, N, K);
+  const size_t a_bytes = up256(static_cast<size_t>(rank) * static_cast<size_t>(K) * 2);
+  const size_t b_bytes = up256(static_cast<size_t>(N) * static_cast<size_t>(r8) * 2);
+  const size_t u_bytes = up256(static_cast<size_t>(T) * static_cast<size_t>(r8) * 4);
+  const size_t p_main = static_cast<size_t>(tc_partial_splits(ld, K, T, *dev, cg)) *
+                        static_cast<size_t>(T) * static_cast<size_t>(K) * 4;
+  const size_t p_u = static_cast<size_t>(tc_partial_splits(N, r8, T, *dev, 0)) *
+                     static_cast<size_t>(T) * static_cast<size_t>(r8) * 4;
+  const size_t p_bytes = up256(std::max(p_main, p_u));
+  void* buf = nullptr;
+  if (cudaMallocFromPoolAsync(&buf, dy_bytes + w_bytes + a_bytes + b_bytes + u_bytes + p_bytes,
+                              pool, s) != cudaSuccess)
+    return RG_ERR_CUDA;
+  char* b = static_cast<char*>(buf);
+  uint16_t* dy16 = reinterpret_cast<uint16_t*>(b);
+  uint16_t* w16 = reinterpret_cast<uint16_t*>(b + dy_bytes);
+  uint16_t* a16 = reinterpret_cast<uint16_t*>(b + dy_bytes + w_bytes);
+  uint16_t* b16 = reinterpret_cast<uint16_t*>(b + dy_bytes + w_bytes + a_bytes);
+  float* u32 = reinterpret_cast<float*>(b + dy_bytes + w_bytes + a_bytes + b_bytes);
+  float* part = reinterpret_cast<float*>(b + dy_bytes + w_bytes + a_bytes + b_bytes + u_bytes);
+  cudaError_t e = launch_convert_dy(dY, T, N, N, 1, ld, bf16, dy16, *dev, s);
+  if (e == cudaSuccess) e = launch_convert_dy(lora_b, N, rank, rank, 1, r8, bf16, b16, *dev, s);
+  if (e == cudaSuccess) e = launch_convert_dy(lora_a, rank, K, K, 1, K, bf16, a16, *dev, s, scale);
+  const void* Wtc = W;
+  int wtc = wtype;
+  if (wtype == RG_F32) {
+    if (e == cudaSuccess)
+      e = launch_convert_dy(static_cast<const float*>(W), N, K, K, 1, K, true, w16, *dev, s);
+    Wtc = w16;
+    wtc = RG_BF16;
+  }
+  // U [T, r8] = dY . B over B's 16-bit copy (ranks past `rank` are zero)
+  if (e == cudaSuccess)
+    e = launch_tc(bf16 ? RG_BF16 : RG_F16, b16, N, r8, dy16, ld, T, u32, r8, 0.0f, part, *dev, s,
+                  0, 0);
+  if (e == cudaSuccess) e = launch_adapter_pack(u32, r8, T, rank, N, ld, bf16, dy16, *dev, s);
+  if (e == cudaSuccess)
+    e = launch_tc(wtc, Wtc, N, K, dy16, ld, T, dX, K, beta, part, *dev, s, cg, env().inject_stall,
+                  a16, rank);
+  const cudaError_t f = cudaFreeAsync(buf, s);
+  return from_cuda(e == cudaSuccess ? f : e);
 }
 
 int rg_plan(int variant, int wtype, int64_t N, int64_t K, int64_t T, rg_plan_info* out) {

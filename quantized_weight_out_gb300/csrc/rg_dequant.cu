@@ -150,11 +150,6 @@ cudaError_t launch_dequant_t16(int wtype, const void* W, int64_t N, int64_t K, b
   });
 }
 
-static int grid_for(int64_t work_items, int threads, const DevInfo& dev) {
-  const int64_t blocks = (work_items + threads - 1) / threads;
-  const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
-  return static_cast<int>(std::max<int64_t>(1, std::min(blocks, cap)));
-}
 
 cudaError_t launch_dequant(int wtype, const void* W, int64_t N, int64_t K, float* out,
                            const DevInfo& dev, cudaStream_t stream) {
@@ -171,11 +166,12 @@ cudaError_t launch_dequant(int wtype, const void* W, int64_t N, int64_t K, float
   });
 }
 
-// dY [T, N] F32 -> [T, ld] 16-bit, round to nearest even.  One thread per 8
-// values; 16-byte loads when every row is 16-byte aligned (N % 4 == 0).
+// dY [T, N] F32 -> [T, ld] 16-bit of mul * dY, round to nearest even (mul
+// is 1 for dY itself: exact).  One thread per 8 values; 16-byte loads when
+// every row is 16-byte aligned (N % 4 == 0).
 template <bool BF16>
 __global__ void __launch_bounds__(256) convert_dy_kernel(const float* __restrict__ dY, int64_t T,
-                                                         int64_t N, int64_t ld,
+                                                         int64_t N, int64_t ld, float mul,
                                                          uint16_t* __restrict__ out) {
   const int64_t cpr = (N + 7) >> 3;
   const int64_t total = T * cpr;
@@ -195,6 +191,8 @@ __global__ void __launch_bounds__(256) convert_dy_kernel(const float* __restrict
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = (n0 + i < N) ? src[i] : 0.0f;
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] *= mul;
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -252,8 +250,9 @@ __global__ void __launch_bounds__(256) convert_dy_tiled_kernel(const float* __re
 
 cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t dy_t, int64_t dy_n,
                               int64_t ld, bool bf16, uint16_t* out, const DevInfo& dev,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, float mul) {
   if (dy_n != 1 || dy_t != N) {
+    if (mul != 1.0f) return cudaErrorInvalidValue;  // (strided rows are dY's alone)
     const int64_t gy = (T + 31) / 32;
     if (gy > 65535) return cudaErrorInvalidConfiguration;
     const dim3 grid(static_cast<unsigned>((N + 31) / 32), static_cast<unsigned>(gy));
@@ -265,9 +264,9 @@ cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t dy_
   }
   const int grid = grid_for(T * ((N + 7) >> 3), 256, dev);
   if (bf16)
-    convert_dy_kernel<true><<<grid, 256, 0, stream>>>(dY, T, N, ld, out);
+    convert_dy_kernel<true><<<grid, 256, 0, stream>>>(dY, T, N, ld, mul, out);
   else
-    convert_dy_kernel<false><<<grid, 256, 0, stream>>>(dY, T, N, ld, out);
+    convert_dy_kernel<false><<<grid, 256, 0, stream>>>(dY, T, N, ld, mul, out);
   return counted(cudaGetLastError());
 }
 

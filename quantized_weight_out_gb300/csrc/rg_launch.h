@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <atomic>
 #include <type_traits>
 
@@ -67,10 +68,36 @@ struct Layout {
 cudaError_t launch_dequant_t16(int wtype, const void* W, int64_t N, int64_t K, bool bf16,
                                uint16_t* out, int64_t ldo, const DevInfo& dev, cudaStream_t stream);
 
+// Blocks of a grid-stride kernel over work_items (one per thread): enough
+// for the items, at most eight per SM.
+inline int grid_for(int64_t work_items, int threads, const DevInfo& dev) {
+  const int64_t blocks = (work_items + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
+  return static_cast<int>(std::max<int64_t>(1, std::min(blocks, cap)));
+}
+
 // dY [T, N] (strided) F32 -> out [T, ld] fp16 (bf16 when `bf16`), rows padded to ld.
+// mul != 1 (contiguous rows only) converts mul * dY.
 cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t dy_t, int64_t dy_n,
                               int64_t ld, bool bf16, uint16_t* out, const DevInfo& dev,
-                              cudaStream_t stream);
+                              cudaStream_t stream, float mul = 1.0f);
+
+// --- the low-rank adapter (rg_adapter.cu) ---
+// U [T, rank] (rows ldu floats apart) into columns [roundup8(N),
+// tc_adapter_cols(N, rank)) of the 16-bit dY copy: zeros up to the chunk
+// boundary after N, then U, then zeros.
+cudaError_t launch_adapter_pack(const float* U, int64_t ldu, int64_t T, int64_t rank, int64_t N,
+                                int64_t ld, bool bf16, uint16_t* out, const DevInfo& dev,
+                                cudaStream_t stream);
+// Ranges of n the F32 route splits dY . B into (its workspace holds
+// parts * T * rank floats).
+int adapter_down_parts(int64_t N, int64_t T, int64_t rank, const DevInfo& dev);
+// dX [T, K] (rows dx_t apart) += scale * (dY . B) . A, all F32, dY and A
+// row-contiguous and 16-byte aligned.
+cudaError_t launch_adapter_f32(const float* dY, int64_t N, int64_t T, const float* A,
+                               const float* B, int64_t rank, int64_t K, float scale, float* dX,
+                               int64_t dx_t, float* part, int n_parts, const DevInfo& dev,
+                               cudaStream_t stream);
 
 // dX = beta * dX (beta == 0: dX = 0) over T rows of K, the N == 0 case.
 cudaError_t launch_scale(float* dX, int64_t T, int64_t K, int64_t dx_t, float beta,
@@ -113,9 +140,15 @@ TcPlan plan_tc(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force
 int64_t tc_dy16_ld(int64_t N);
 // part: [n_splits][T][K] F32 partial sums when the plan splits the
 // contraction (tc_partial_splits > 0), else unused.
+// With a low-rank adapter (rank > 0): a16 holds its rows [rank, K] in the
+// 16-bit kind of the product, and dy16 has tc_adapter_cols(N, rank) columns:
+// dY's N values, zeros up to the next multiple of 64, then the rank values
+// of the adapter's projected dY and zeros to the next multiple of 64.
 cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
                       int64_t ld_dy16, int64_t T, float* dX, int64_t dx_t, float beta, float* part,
-                      const DevInfo& dev, cudaStream_t stream, int cg_force, int inject_stall);
+                      const DevInfo& dev, cudaStream_t stream, int cg_force, int inject_stall,
+                      const uint16_t* a16 = nullptr, int64_t rank = 0);
+int64_t tc_adapter_cols(int64_t N, int64_t rank);
 // Number of partial-sum slabs the tensor-core plan needs (0 when unsplit).
 int64_t tc_partial_splits(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force);
 

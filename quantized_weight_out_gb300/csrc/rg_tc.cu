@@ -474,10 +474,11 @@ __device__ __forceinline__ int p_window_start(int kt) {
 template <int WT, int CG, int BT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     out_prod_tc_kernel(const __grid_constant__ CUtensorMap map_w,
-                       const __grid_constant__ CUtensorMap map_y, float* __restrict__ dX,
-                       int64_t ldx, float beta, int T, int K, int n_kunits, int n_ttiles, int band,
-                       int n_chunks, int n_splits, float* __restrict__ part, WaitCtl ctl,
-                       int inject_stall) {
+                       const __grid_constant__ CUtensorMap map_y,
+                       const __grid_constant__ CUtensorMap map_l, int n_main,
+                       float* __restrict__ dX, int64_t ldx, float beta, int T, int K,
+                       int n_kunits, int n_ttiles, int band, int n_chunks, int n_splits,
+                       float* __restrict__ part, WaitCtl ctl, int inject_stall) {
   using C = Cfg<WT, CG, BT>;
   constexpr int S = C::S;
   extern __shared__ uint8_t smem_raw[];
@@ -502,7 +503,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const bool leader = rank == 0;
   const int unit = blockIdx.x / CG, n_units = gridDim.x / CG;
   // work items: (tile, split); a split covers chunks [split * n_chunks, +n_chunks)
-  // of the contraction (chunks past N are zero-filled by TMA and add nothing)
+  // of the contraction (chunks past N are zero-filled by TMA and add nothing).
+  // Chunks from n_main on belong to a low-rank adapter: their A rows are the
+  // adapter's dense 16-bit rows (map_l) and their B columns the adapter's
+  // projected dY, which sit after dY's own columns in the same 16-bit copy;
+  // n_main is past every chunk when there is no adapter.
   const int n_tiles = n_kunits * n_ttiles * n_splits;
   const int n_tiles1 = n_kunits * n_ttiles;
 
@@ -581,23 +586,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (skip_first) {
             skip_first = false;  // fault injection: this stage never fills
           } else {
+            const int gc = cbase + c;  // the contraction chunk
+            const bool adapter = gc >= n_main;
+            const bool dense_a = !C::QUANT || adapter;  // A straight from TMA
             if (leader) {
-              mbar_arrive_expect_tx(full_ab(s), C::AB_BYTES_PAIR);
+              mbar_arrive_expect_tx(full_ab(s), C::QUANT && adapter
+                                                    ? C::AB_BYTES_PAIR + CG * A_STAGE
+                                                    : C::AB_BYTES_PAIR);
               pend_ab |= 1u << s;
             }
             if constexpr (C::QUANT) {
-              mbar_arrive_expect_tx(full_p(s), C::P_BYTES);
-              tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_p(s),
-                          p_window_start<WT>(kt) / 4, (cbase + c) * BC);
-              pend_p |= 1u << s;
-            } else {
+              if (adapter) {
+                mbar_arrive(full_p(s));  // no packed window: the decoders pass
+              } else {
+                mbar_arrive_expect_tx(full_p(s), C::P_BYTES);
+                tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_p(s),
+                            p_window_start<WT>(kt) / 4, gc * BC);
+                pend_p |= 1u << s;
+              }
+            }
+            if (dense_a) {
+              const CUtensorMap* ma = adapter ? &map_l : &map_w;
+              const int row = (adapter ? gc - n_main : gc) * BC;
               const uint32_t a_dst = smem_addr(sA + s * A_STAGE);
               if constexpr (CG == 2) {
-                tma_load_2d_pair(a_dst, &map_w, abar, kt * BM, (cbase + c) * BC);
-                tma_load_2d_pair(a_dst + A_COLBLK, &map_w, abar, kt * BM + 64, (cbase + c) * BC);
+                tma_load_2d_pair(a_dst, ma, abar, kt * BM, row);
+                tma_load_2d_pair(a_dst + A_COLBLK, ma, abar, kt * BM + 64, row);
               } else {
-                tma_load_2d(a_dst, &map_w, abar, kt * BM, (cbase + c) * BC);
-                tma_load_2d(a_dst + A_COLBLK, &map_w, abar, kt * BM + 64, (cbase + c) * BC);
+                tma_load_2d(a_dst, ma, abar, kt * BM, row);
+                tma_load_2d(a_dst + A_COLBLK, ma, abar, kt * BM + 64, row);
               }
             }
             if constexpr (CG == 2)
@@ -707,11 +724,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         while (c >= n_chunks) { c -= n_chunks; tile += n_units; }
         int ku, tt;
         if (tile < n_tiles) coords(tile, ku, tt);
+        // chunks of this tile from c_ad on are the adapter's (TMA fills A)
+        int c_ad = n_main - (tile / n_tiles1) * n_chunks;
         uint32_t ph = 0;
         for (int g = s; g < total; g += S, ph ^= 1u) {
           const int kt = ku * CG + static_cast<int>(rank);
           if (!__all_sync(0xffffffffu, mbar_wait(full_p(s), ph, ctl, abort_flag))) break;
-          if constexpr (WT == RG_Q6_K) {
+          if (c >= c_ad) {
+            // nothing to decode
+          } else if constexpr (WT == RG_Q6_K) {
             // the super-block starts o bytes into its window: one decoder per o
             const int o = ((kt >> 1) * 210) & 15;
             const uint8_t* P = sP + s * C::P_STAGE;
@@ -732,7 +753,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else {
             decode_stage_warp<WT, 0, WPS>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part);
           }
-          fence_proxy_async_smem();
+          if (c < c_ad) fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
             if constexpr (CG == 2)
@@ -744,6 +765,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (c >= n_chunks) {
             while (c >= n_chunks) { c -= n_chunks; tile += n_units; }
             if (tile < n_tiles) coords(tile, ku, tt);
+            c_ad = n_main - (tile / n_tiles1) * n_chunks;
           }
         }
       }
@@ -862,8 +884,9 @@ TcPlan plan_tc(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force
 }
 
 template <int WT, int CG, int BT>
-static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my, float* dX,
-                               int64_t ldx, float beta, int T, int K, const TcPlan& p, float* part,
+static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
+                               const CUtensorMap& ml, int n_main, float* dX, int64_t ldx,
+                               float beta, int T, int K, const TcPlan& p, float* part,
                                const DevInfo& dev, cudaStream_t stream, int inject) {
   using C = tc::Cfg<WT, CG, BT>;
   auto kern = tc::out_prod_tc_kernel<WT, CG, BT>;
@@ -893,23 +916,32 @@ static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my, flo
   }
   const int units = std::min(p.grid / CG, mc);
   cfg.gridDim = dim3(static_cast<unsigned>(units * CG), 1, 1);
-  return counted(cudaLaunchKernelEx(&cfg, kern, mw, my, dX, ldx, beta, T, K, p.n_kunits, p.n_ttiles, p.band,
-                            p.n_chunks, p.n_splits, part, ctl, inject));
+  return counted(cudaLaunchKernelEx(&cfg, kern, mw, my, ml, n_main, dX, ldx, beta, T, K,
+                                    p.n_kunits, p.n_ttiles, p.band, p.n_chunks, p.n_splits, part,
+                                    ctl, inject));
 }
 
 template <int WT>
-static cudaError_t launch_tc_w(const CUtensorMap& mw, const CUtensorMap& my, float* dX,
-                               int64_t ldx, float beta, int T, int K, const TcPlan& p, float* part,
+static cudaError_t launch_tc_w(const CUtensorMap& mw, const CUtensorMap& my,
+                               const CUtensorMap& ml, int n_main, float* dX, int64_t ldx,
+                               float beta, int T, int K, const TcPlan& p, float* part,
                                const DevInfo& dev, cudaStream_t stream, int inject) {
   if (p.cg == 2)
-    return launch_tc_t<WT, 2, 256>(mw, my, dX, ldx, beta, T, K, p, part, dev, stream, inject);
-  return launch_tc_t<WT, 1, 128>(mw, my, dX, ldx, beta, T, K, p, part, dev, stream, inject);
+    return launch_tc_t<WT, 2, 256>(mw, my, ml, n_main, dX, ldx, beta, T, K, p, part, dev, stream,
+                                   inject);
+  return launch_tc_t<WT, 1, 128>(mw, my, ml, n_main, dX, ldx, beta, T, K, p, part, dev, stream,
+                                 inject);
 }
 
 cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
                       int64_t ld_dy16, int64_t T, float* dX, int64_t dx_t, float beta, float* part,
-                      const DevInfo& dev, cudaStream_t stream, int cg_force, int inject_stall) {
-  TcPlan p = plan_tc(N, K, T, dev, cg_force);
+                      const DevInfo& dev, cudaStream_t stream, int cg_force, int inject_stall,
+                      const uint16_t* a16, int64_t rank) {
+  // with an adapter the contraction runs over tc_adapter_cols(N, r) columns
+  // of dy16: dY's N, zeros to the chunk boundary, then the adapter's rank
+  const int64_t n_ext = rank > 0 ? tc_adapter_cols(N, rank) : N;
+  const int n_main = rank > 0 ? static_cast<int>((N + tc::BC - 1) / tc::BC) : (1 << 30);
+  TcPlan p = plan_tc(n_ext, K, T, dev, cg_force);
   if (p.n_splits > 1 && part == nullptr) return cudaErrorInvalidValue;
   float* partial = p.n_splits > 1 ? part : nullptr;
   // band of k units whose slice of W fits comfortably in L2 (48 MB)
@@ -931,17 +963,30 @@ cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint
                      CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  r = encode_tiled(&my, CU_TENSOR_MAP_DATA_TYPE_UINT16, dy16, static_cast<uint64_t>(N),
+  r = encode_tiled(&my, CU_TENSOR_MAP_DATA_TYPE_UINT16, dy16, static_cast<uint64_t>(n_ext),
                    static_cast<uint64_t>(T), static_cast<uint64_t>(ld_dy16) * 2, tc::BC,
                    tc::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // the adapter's rows [rank, K] (16-bit, same kind as the decoded W); without
+  // one the map is a copy that no stage reads
+  CUtensorMap ml = mw;
+  if (rank > 0) {
+    r = encode_tiled(&ml, CU_TENSOR_MAP_DATA_TYPE_UINT16, a16, static_cast<uint64_t>(K),
+                     static_cast<uint64_t>(rank), static_cast<uint64_t>(K) * 2, 64, tc::BC,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   const int t = static_cast<int>(T), k = static_cast<int>(K);
   const cudaError_t e = with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
-    return launch_tc_w<decltype(wt)::value>(mw, my, dX, dx_t, beta, t, k, p, partial, dev, stream,
-                                            inject_stall);
+    return launch_tc_w<decltype(wt)::value>(mw, my, ml, n_main, dX, dx_t, beta, t, k, p, partial,
+                                            dev, stream, inject_stall);
   });
   if (e != cudaSuccess || p.n_splits == 1) return e;
   return launch_reduce_partials(partial, p.n_splits, T, K, dX, dx_t, beta, dev, stream);
+}
+
+int64_t tc_adapter_cols(int64_t N, int64_t r) {
+  return ((N + tc::BC - 1) / tc::BC + (r + tc::BC - 1) / tc::BC) * tc::BC;
 }
 
 int64_t tc_partial_splits(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force) {

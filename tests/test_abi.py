@@ -161,3 +161,24 @@ def test_mul_mat_validation(lib):
     assert rg.rg_mul_mat(inputs.Q8_0, A, 64, 256, A, 0, A, 0.0) == rg.RG_OK
     assert rg.rg_mul_mat(inputs.Q8_0, A + 4, 64, 256, A, 4, A, 0.0) == rg.RG_ERR_ALIGN
     assert rg.rg_mul_mat(inputs.Q8_0, A, 64, 256, A, 4, None, 0.0) == rg.RG_ERR_ARG
+
+
+def test_out_prod_lora_validation(lib):
+    """The adapter entry checks its own arguments after the base product's."""
+    A = 0x1000
+    base = (0, inputs.Q8_0, A, 64, 256, A, 8, A, 0.0)
+
+    def call(*args, a=A, b=A, rank=16, scale=1.0, prefix=base):
+        return rg.rg_out_prod_lora(*prefix, a, b, rank, scale)
+    assert call(rank=-1) == rg.RG_ERR_ARG
+    assert call(rank=1025) == rg.RG_ERR_SHAPE
+    assert call(a=None) == rg.RG_ERR_ARG
+    assert call(b=None) == rg.RG_ERR_ARG
+    assert call(a=A + 4) == rg.RG_ERR_ALIGN
+    assert call(b=A + 8) == rg.RG_ERR_ALIGN
+    assert call(prefix=(9, inputs.Q8_0, A, 64, 256, A, 8, A, 0.0)) == rg.RG_ERR_TYPE
+    assert call(prefix=(0, 12, A, 64, 256, A, 8, A, 0.0)) == rg.RG_ERR_TYPE
+    assert call(prefix=(0, inputs.Q8_0, A, 64, 200, A, 8, A, 0.0)) == rg.RG_ERR_SHAPE
+    # nothing to compute: T == 0 or K == 0, whatever the adapter pointers
+    assert call(a=None, b=None, prefix=(0, inputs.Q8_0, None, 64, 256, None, 0, None, 0.0)) == rg.RG_OK
+    assert call(a=None, b=None, prefix=(0, inputs.Q8_0, None, 64, 0, None, 8, None, 0.0)) == rg.RG_OK

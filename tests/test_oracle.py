@@ -813,3 +813,18 @@ def test_lora_mutants_are_caught(golden_dir, mutant):
         Wd = oracle.dequant(inputs.F16, W, N, K).astype(np.float64)
         term = s * (((dY64 @ Wd) @ B64) @ A64)
     assert not np.array_equal(base + term, want.astype(np.float64))
+
+
+def test_lora_at_matches_full():
+    N, K, T, R = 30, 64, 5, 6
+    W = inputs.gen_weight(inputs.F16, N, K, seed=96, stream=1)
+    dY = inputs.normal_f32(96, 2, T * N, 1.0).reshape(T, N)
+    A = inputs.normal_f32(96, 3, R * K, 1.0).reshape(R, K)
+    B = inputs.normal_f32(96, 4, N * R, 1.0).reshape(N, R)
+    full = (oracle.out_prod_lora(inputs.F16, W, N, K, dY, T, A, B, R, 1.25)
+            - oracle.out_prod(inputs.F16, W, N, K, dY, T))
+    bnd = oracle.lora_bound(dY, A, B, 1.25)
+    ts, ks = [0, 4, 2, 3], [63, 0, 17, 40]
+    v, b = oracle.lora_at(dY, A, B, 1.25, ts, ks)
+    assert np.allclose(v, full[ts, ks], rtol=1e-12, atol=1e-12)
+    assert np.allclose(b, bnd[ts, ks], rtol=1e-12)
