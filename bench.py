@@ -211,8 +211,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="layer7b_t8192")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--op", default="out_prod", choices=["out_prod", "mul_mat"],
-                    help="out_prod (the backward, default) or mul_mat (the forward rg_mul_mat)")
+    ap.add_argument("--op", default="out_prod", choices=["out_prod", "mul_mat", "lora"],
+                    help="out_prod (the backward, default), mul_mat (the forward rg_mul_mat) or "
+                         "lora (the backward through W plus a low-rank adapter)")
+    ap.add_argument("--rank", type=int, default=16, help="adapter rank of --op lora")
     ap.add_argument("--cpu-rows", type=int, default=1024, help="dY rows per call, CPU baseline sample")
     ap.add_argument("--ref-rows", type=int, default=32, help="dY rows per call, reference-arm step")
     ap.add_argument("--ref-wrows", type=int, default=512, help="W rows per call, reference-arm step")
@@ -529,40 +531,22 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def run_mul_mat(args):
-    """The forward Y = X . deq(W)^T (rg_mul_mat) on the workload's shapes:
-    same timing rules as the backward (warm-up, events, clocks, the GEMM
-    alone against the measured peak); inputs resident, no e2e leg."""
-    import torch
-    world, rank, local = _dist()
-    from quantized_weight_out_gb300 import binding as rg
-    from quantized_weight_out_gb300 import build as rgbuild
-    rgbuild.build()
-    rg.load()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    problems = inputs.WORKLOADS[args.workload]
-    bufs = []
-    for p in problems:
-        X = inputs.normal_f32(p.seed, 2 + p.stream_base, p.T * p.K, 1e-2).reshape(p.T, p.K)
-        bufs.append((torch.from_numpy(p.weight()).to(dev), torch.from_numpy(X).to(dev),
-                     torch.zeros((p.T, p.N), device=dev)))
-    stream = torch.cuda.current_stream()
-
+def _timed_calls(torch, rg, problems, call, args, stream, dev, world):
+    """Warm-up, then `args.steps` timed steps of call(i, p) over the problems:
+    per call a pair of events around the call and a pair around its main
+    tensor-core kernel (rg_profile_next_gemm); clocks sampled meanwhile.
+    Returns (ms per step over ranks, launches, clocks, per-call ms, GEMM ms
+    per step)."""
     def step(evs=None):
         for i, p in enumerate(problems):
-            W, X, Y = bufs[i]
             if evs is not None:
                 evs[i][0].record(stream)
                 rg.rg_profile_next_gemm(evs[i][2], evs[i][3])
-            st = rg.rg_mul_mat(p.wtype, W, p.N, p.K, X, p.T, Y, 0.0, stream)
+            st = call(i, p)
             if evs is not None:
                 evs[i][1].record(stream)
             if st != 0:
-                raise RuntimeError(f"rg_mul_mat: {rg.strerror(st)}")
+                raise RuntimeError(f"{p.name}: {rg.strerror(st)}")
 
     for _ in range(args.warmup):
         step()
@@ -590,17 +574,53 @@ def run_mul_mat(args):
     clocks = sampler.stop()
     rg.check(rg.rg_check(stream), "timed region")
     ms_step = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dev)
-    flops_step = sum(p.flops for p in problems)
+    per_call = [statistics.median(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(args.steps))
+                for i in range(len(problems))]
     gemm_ms = sum(statistics.mean(evs[k][i][2].elapsed_time(evs[k][i][3]) for k in range(args.steps))
                   for i in range(len(problems)))
+    return ms_step, launches, clocks, per_call, gemm_ms
+
+
+def _setup_gpu(torch):
+    world, rank, local = _dist()
+    from quantized_weight_out_gb300 import binding as rg
+    from quantized_weight_out_gb300 import build as rgbuild
+    rgbuild.build()
+    rg.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    return rg, world, rank, dev
+
+
+def run_mul_mat(args):
+    """The forward Y = X . deq(W)^T (rg_mul_mat) on the workload's shapes:
+    same timing rules as the backward (warm-up, events, clocks, the GEMM
+    alone against the measured peak); inputs resident, no e2e leg."""
+    import torch
+    rg, world, rank, dev = _setup_gpu(torch)
+    problems = inputs.WORKLOADS[args.workload]
+    bufs = []
+    for p in problems:
+        X = inputs.normal_f32(p.seed, 2 + p.stream_base, p.T * p.K, 1e-2).reshape(p.T, p.K)
+        bufs.append((torch.from_numpy(p.weight()).to(dev), torch.from_numpy(X).to(dev),
+                     torch.zeros((p.T, p.N), device=dev)))
+    stream = torch.cuda.current_stream()
+
+    def call(i, p):
+        W, X, Y = bufs[i]
+        return rg.rg_mul_mat(p.wtype, W, p.N, p.K, X, p.T, Y, 0.0, stream)
+
+    ms_step, launches, clocks, per_call, gemm_ms = _timed_calls(torch, rg, problems, call, args,
+                                                                stream, dev, world)
+    flops_step = sum(p.flops for p in problems)
     peaks, src = _peaks()
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     achieved = flops_step / (gemm_ms * 1e-3) / 1e12
-    calls = []
-    for i, p in enumerate(problems):
-        t = statistics.median(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(args.steps))
-        calls.append({"name": p.name, "wtype": inputs.TYPE_NAMES[p.wtype], "N": p.N, "K": p.K, "T": p.T,
-                      "ms": t, "tflops": p.flops / (t * 1e-3) / 1e12})
+    calls = [{"name": p.name, "wtype": inputs.TYPE_NAMES[p.wtype], "N": p.N, "K": p.K, "T": p.T,
+              "ms": t, "tflops": p.flops / (t * 1e-3) / 1e12} for p, t in zip(problems, per_call)]
     line = {"metric": "mul_mat TFLOP/s (2*T*N*K / time)", "op": "mul_mat",
             "value": job_tflops(flops_step, ms_step, world), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -619,12 +639,75 @@ def run_mul_mat(args):
         torch.distributed.destroy_process_group()
 
 
+def run_lora(args):
+    """The input gradient through the resident weight plus a rank-r adapter
+    (rg_out_prod_lora) on the workload's shapes, beside the base product
+    alone (rg_out_prod) timed the same way, so the adapter's cost shows."""
+    import torch
+    rg, world, rank, dev = _setup_gpu(torch)
+    problems = inputs.WORKLOADS[args.workload]
+    R, scale = args.rank, 0.5
+    bufs = []
+    for p in problems:
+        A = inputs.normal_f32(p.seed, 7 + p.stream_base, R * p.K, 0.05).reshape(R, p.K)
+        B = inputs.normal_f32(p.seed, 8 + p.stream_base, p.N * R, 0.05).reshape(p.N, R)
+        bufs.append((torch.from_numpy(p.weight()).to(dev), torch.from_numpy(p.dy()).to(dev),
+                     torch.zeros((p.T, p.K), device=dev), torch.from_numpy(A).to(dev),
+                     torch.from_numpy(B).to(dev)))
+    stream = torch.cuda.current_stream()
+
+    def call_lora(i, p):
+        W, dY, dX, A, B = bufs[i]
+        return rg.rg_out_prod_lora(0, p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, A, B, R, scale,
+                                   stream)
+
+    def call_base(i, p):
+        W, dY, dX, _, _ = bufs[i]
+        return rg.rg_out_prod_variant(0, p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, stream)
+
+    base_ms, _, _, _, _ = _timed_calls(torch, rg, problems, call_base, args, stream, dev, world)
+    ms_step, launches, clocks, per_call, gemm_ms = _timed_calls(torch, rg, problems, call_lora,
+                                                                args, stream, dev, world)
+    flops = [p.flops + 2 * p.T * R * (p.N + p.K) for p in problems]
+    flops_step = sum(flops)
+    peaks, src = _peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    # the main kernel's tensor work: the base product plus the adapter's
+    # chunks (64 * ceil(r / 64) extra contraction rows)
+    gemm_flops = sum(2 * p.T * p.K * (p.N + 64 * ((R + 63) // 64)) for p in problems)
+    achieved = gemm_flops / (gemm_ms * 1e-3) / 1e12
+    calls = [{"name": p.name, "wtype": inputs.TYPE_NAMES[p.wtype], "N": p.N, "K": p.K, "T": p.T,
+              "rank": R, "ms": t, "tflops": f / (t * 1e-3) / 1e12}
+             for p, t, f in zip(problems, per_call, flops)]
+    line = {"metric": "out_prod+LoRA TFLOP/s (2*T*(N*K + r*(N + K)) / time)", "op": "lora",
+            "value": job_tflops(flops_step, ms_step, world), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": _dtype_name(problems), "data": "synthetic",
+            "config": {"workload": args.workload, "calls": len(problems), "rank": R,
+                       "scale": scale, "flops_per_step": flops_step,
+                       "parallelism": f"replicas x{world}"},
+            "base_only": {"ms_per_step": base_ms,
+                          "adapter_overhead": ms_step / base_ms - 1.0},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_source": f"{src} bf16_tflops_sustained",
+                         "kernel": "out_prod_tc_kernel with the adapter's chunks"},
+            "gpu_launches": launches, "clocks": clocks, "per_call": calls}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
     elif args.op == "mul_mat":
         run_mul_mat(args)
+    elif args.op == "lora":
+        run_lora(args)
     else:
         run_ours(args)
 

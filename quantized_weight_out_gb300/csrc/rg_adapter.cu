@@ -126,7 +126,230 @@ __global__ void __launch_bounds__(256) adapter_up_kernel(const float* __restrict
   *o = d;
 }
 
+// --- dY's 16-bit copy and U = dY . B in one pass over dY (rank <= 32) ---
+//
+// Block: 32 rows of dY, 256 threads, the contraction in chunks of 256 values
+// of n, two chunks in flight: while the warps multiply chunk c out of shared
+// memory, every thread's eight float4 of chunk c + 1 (a warp reads four rows
+// x 128 contiguous bytes per instruction) are on their way into registers
+// and B^T's chunk c + 1 into the other shared buffer (cp.async, zero-filled
+// past N and past the rank).  A chunk's dY values are rounded to 16 bits
+// once: written to the copy in HBM and to the MMA's tile.  Warp w multiplies
+// rows 16 (w & 1).. by chunk quarter w >> 1 with mma.sync m16n8k16 (F32
+// accumulation); the four quarters' U are added in a fixed order at the end
+// and written, rounded to 16 bits, after dY's columns.  U is small: the
+// legacy warp MMA is plenty for it.
+constexpr int AD_TR = 32, AD_NC = 256, AD_LD = AD_NC + 8;  // (+8: conflict-free fragments)
+
+template <int R8>
+constexpr int adapter_smem_bytes() {
+  constexpr int tiles = 2 * (AD_TR + R8) * AD_LD * 2;  // two buffers of dY's and B^T's chunk
+  constexpr int red = 4 * AD_TR * R8 * 4;
+  return tiles > red ? tiles : red;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack16(float a, float b) {
+  if constexpr (BF16) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  if constexpr (BF16)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 16 bytes global -> shared, the first `bytes` (0..16) from src, the rest zero
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// dY [T, N] F32 (rows 16-byte aligned when VEC) -> out [T, ld] 16-bit:
+// columns [0, c_ad) dY (zeros from N on), [c_ad, c_ad + 64) U = dY . B for
+// ranks < rank, zeros after.  bt: B^T [rank, ldb] 16-bit, ldb % 8 == 0.
+template <bool BF16, bool VEC, int R8>
+__global__ void __launch_bounds__(256) convert_dy_adapter_kernel(
+    const float* __restrict__ dY, int64_t T, int64_t N, const uint16_t* __restrict__ bt,
+    int64_t ldb, int rank, int64_t c_ad, int64_t ld, uint16_t* __restrict__ out) {
+  extern __shared__ __align__(16) uint8_t ad_smem[];
+  // buffer b: dY's tile [AD_TR][AD_LD], then B^T's [R8][AD_LD]
+  uint16_t* const buf0 = reinterpret_cast<uint16_t*>(ad_smem);
+  constexpr int BUF = (AD_TR + R8) * AD_LD;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, tq = lane & 3;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * AD_TR;
+  const int lr = tid >> 3, l8 = tid & 7;  // load role: row lr, float4 l8 + 8q
+  const int64_t t = t0 + lr;
+  const bool row_ok = t < T;
+  const float* yrow = dY + t * N;
+  const int mt = warp & 1, ks = warp >> 1;  // MMA role: rows 16 mt.., chunk quarter ks
+  float acc[R8 / 8][4];
+#pragma unroll
+  for (int i = 0; i < R8 / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+
+  float4 v[8];
+  auto load_y = [&](int64_t n0) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int64_t n = n0 + (q * 8 + l8) * 4;
+      if (VEC && row_ok && n + 4 <= N) {
+        v[q] = __ldcs(reinterpret_cast<const float4*>(yrow + n));
+      } else {
+        v[q].x = (row_ok && n < N) ? yrow[n] : 0.0f;
+        v[q].y = (row_ok && n + 1 < N) ? yrow[n + 1] : 0.0f;
+        v[q].z = (row_ok && n + 2 < N) ? yrow[n + 2] : 0.0f;
+        v[q].w = (row_ok && n + 3 < N) ? yrow[n + 3] : 0.0f;
+      }
+    }
+  };
+  auto load_b = [&](int64_t n0, uint16_t* sB) {
+#pragma unroll
+    for (int i = 0; i < R8 / 8; ++i) {
+      const int e = tid + 256 * i;  // 32 sixteen-byte pieces a row
+      const int jj = e >> 5, k = (e & 31) * 8;
+      const int64_t n = n0 + k;
+      const int64_t left = (jj < rank && n < N) ? (N - n) * 2 : 0;
+      const int bytes = left >= 16 ? 16 : static_cast<int>(left);
+      // a zero-byte copy still names a valid address: the row's start
+      const uint16_t* src = bt + static_cast<int64_t>(jj < rank ? jj : 0) * ldb + (bytes ? n : 0);
+      cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(sB + jj * AD_LD + k)), src, bytes);
+    }
+    cp_async_commit();
+  };
+
+  load_y(0);
+  load_b(0, buf0 + AD_TR * AD_LD);
+  int b = 0;
+  for (int64_t n0 = 0; n0 < c_ad; n0 += AD_NC, b ^= 1) {
+    uint16_t* const sY = buf0 + b * BUF;
+    uint16_t* const sB = sY + AD_TR * AD_LD;
+    // chunk n0: rounded once, to the copy and to the tile
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int c = (q * 8 + l8) * 4;
+      const uint2 h = make_uint2(pack16<BF16>(v[q].x, v[q].y), pack16<BF16>(v[q].z, v[q].w));
+      *reinterpret_cast<uint2*>(sY + lr * AD_LD + c) = h;
+      if (row_ok && n0 + c < c_ad) *reinterpret_cast<uint2*>(out + t * ld + n0 + c) = h;
+    }
+    cp_async_wait_all();  // this thread's pieces of B^T's chunk n0
+    __syncthreads();      // every tile of chunk n0 in place; chunk n0 - 256's reads done
+    if (n0 + AD_NC < c_ad) {
+      load_y(n0 + AD_NC);                         // in flight during the MMAs
+      load_b(n0 + AD_NC, buf0 + (b ^ 1) * BUF + AD_TR * AD_LD);
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const int k0 = ks * 64 + kk * 16 + 2 * tq;
+      const uint16_t* ya = sY + (mt * 16 + g) * AD_LD + k0;
+      uint32_t a[4];
+      a[0] = *reinterpret_cast<const uint32_t*>(ya);
+      a[1] = *reinterpret_cast<const uint32_t*>(ya + 8 * AD_LD);
+      a[2] = *reinterpret_cast<const uint32_t*>(ya + 8);
+      a[3] = *reinterpret_cast<const uint32_t*>(ya + 8 * AD_LD + 8);
+#pragma unroll
+      for (int nt = 0; nt < R8 / 8; ++nt) {
+        const uint16_t* bb = sB + (nt * 8 + g) * AD_LD + k0;
+        mma_16816<BF16>(acc[nt], a, *reinterpret_cast<const uint32_t*>(bb),
+                        *reinterpret_cast<const uint32_t*>(bb + 8));
+      }
+    }
+  }
+  __syncthreads();  // the last chunk's reads are done: the buffers become the reduction's
+  // the four chunk quarters' sums, added in order
+  float* red = reinterpret_cast<float*>(ad_smem);  // [4][AD_TR][R8]
+#pragma unroll
+  for (int nt = 0; nt < R8 / 8; ++nt) {
+    const int r0 = mt * 16 + g, j = nt * 8 + 2 * tq;
+    red[(ks * AD_TR + r0) * R8 + j] = acc[nt][0];
+    red[(ks * AD_TR + r0) * R8 + j + 1] = acc[nt][1];
+    red[(ks * AD_TR + r0 + 8) * R8 + j] = acc[nt][2];
+    red[(ks * AD_TR + r0 + 8) * R8 + j + 1] = acc[nt][3];
+  }
+  __syncthreads();
+  // 64 adapter columns a row, 8 per thread: 32 rows x 8 groups
+  {
+    const int r = tid >> 3, j0 = (tid & 7) * 8;
+    const int64_t tr = t0 + r;
+    if (tr < T) {
+      float u[8];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const int j = j0 + x;
+        float sum = 0.0f;
+        if (j < rank && j < R8) {
+          sum = red[r * R8 + j];
+#pragma unroll
+          for (int q = 1; q < 4; ++q) sum += red[(q * AD_TR + r) * R8 + j];
+        }
+        u[x] = sum;
+      }
+      *reinterpret_cast<uint4*>(out + tr * ld + c_ad + j0) =
+          make_uint4(pack16<BF16>(u[0], u[1]), pack16<BF16>(u[2], u[3]),
+                     pack16<BF16>(u[4], u[5]), pack16<BF16>(u[6], u[7]));
+    }
+  }
+}
+
+template <bool BF16, bool VEC, int R8>
+cudaError_t launch_cda(const float* dY, int64_t T, int64_t N, const uint16_t* bt, int64_t ldb,
+                       int rank, int64_t c_ad, int64_t ld, uint16_t* out, cudaStream_t stream) {
+  auto kern = convert_dy_adapter_kernel<BF16, VEC, R8>;
+  constexpr int smem = adapter_smem_bytes<R8>();
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  kern<<<static_cast<unsigned>((T + AD_TR - 1) / AD_TR), 256, smem, stream>>>(dY, T, N, bt, ldb,
+                                                                              rank, c_ad, ld, out);
+  return counted(cudaGetLastError());
+}
+
+template <bool BF16, bool VEC>
+cudaError_t launch_cda_r(const float* dY, int64_t T, int64_t N, const uint16_t* bt, int64_t ldb,
+                         int rank, int64_t c_ad, int64_t ld, uint16_t* out, cudaStream_t stream) {
+  if (rank <= 8) return launch_cda<BF16, VEC, 8>(dY, T, N, bt, ldb, rank, c_ad, ld, out, stream);
+  if (rank <= 16) return launch_cda<BF16, VEC, 16>(dY, T, N, bt, ldb, rank, c_ad, ld, out, stream);
+  return launch_cda<BF16, VEC, 32>(dY, T, N, bt, ldb, rank, c_ad, ld, out, stream);
+}
+
 }  // namespace
+
+cudaError_t launch_convert_dy_adapter(const float* dY, int64_t T, int64_t N, const uint16_t* bt,
+                                      int64_t ldb, int64_t rank, int64_t ld, bool bf16,
+                                      uint16_t* out, cudaStream_t stream) {
+  if (rank < 1 || rank > kAdapterFusedRank || ldb % 8 || ld % 8 || T > 2147483647ll * AD_TR)
+    return cudaErrorInvalidValue;
+  const int64_t c_ad = (N + 63) / 64 * 64;
+  const bool vec = (N & 3) == 0;
+  const int r = static_cast<int>(rank);
+  if (bf16)
+    return vec ? launch_cda_r<true, true>(dY, T, N, bt, ldb, r, c_ad, ld, out, stream)
+               : launch_cda_r<true, false>(dY, T, N, bt, ldb, r, c_ad, ld, out, stream);
+  return vec ? launch_cda_r<false, true>(dY, T, N, bt, ldb, r, c_ad, ld, out, stream)
+             : launch_cda_r<false, false>(dY, T, N, bt, ldb, r, c_ad, ld, out, stream);
+}
 
 cudaError_t launch_adapter_pack(const float* U, int64_t ldu, int64_t T, int64_t rank, int64_t N,
                                 int64_t ld, bool bf16, uint16_t* out, const DevInfo& dev,

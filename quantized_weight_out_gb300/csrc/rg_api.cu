@@ -582,18 +582,23 @@ int rg_out_prod_lora(int variant, int wtype, const void* W, int64_t N, int64_t K
   // scale * A joins W's rows as extra contraction chunks of the base product
   const bool bf16 = wtype == RG_BF16 || wtype == RG_F32;
   const int cg = cg_force_of(variant);
+  const bool fused = rank <= kAdapterFusedRank;
   const int64_t ld = tc_adapter_cols(N, rank);
   const int64_t r8 = (rank + 7) / 8 * 8;
+  const int64_t ldb = (N + 7) / 8 * 8;
   auto up256 = [](size_t b) { return (b + 255) / 256 * 256; };
   const size_t dy_bytes = up256(static_cast<size_t>(T) * static_cast<size_t>(ld) * 2);
   const size_t w_bytes = tc_w16_bytes(wtype, N, K);
   const size_t a_bytes = up256(static_cast<size_t>(rank) * static_cast<size_t>(K) * 2);
-  const size_t b_bytes = up256(static_cast<size_t>(N) * static_cast<size_t>(r8) * 2);
-  const size_t u_bytes = up256(static_cast<size_t>(T) * static_cast<size_t>(r8) * 4);
+  // B as 16 bits: B^T [rank, ldb] for the fused pass, else B [N, r8]
+  const size_t b_bytes = up256(fused ? static_cast<size_t>(rank) * static_cast<size_t>(ldb) * 2
+                                     : static_cast<size_t>(N) * static_cast<size_t>(r8) * 2);
+  const size_t u_bytes = fused ? 0 : up256(static_cast<size_t>(T) * static_cast<size_t>(r8) * 4);
   const size_t p_main = static_cast<size_t>(tc_partial_splits(ld, K, T, *dev, cg)) *
                         static_cast<size_t>(T) * static_cast<size_t>(K) * 4;
-  const size_t p_u = static_cast<size_t>(tc_partial_splits(N, r8, T, *dev, 0)) *
-                     static_cast<size_t>(T) * static_cast<size_t>(r8) * 4;
+  const size_t p_u = fused ? 0
+                           : static_cast<size_t>(tc_partial_splits(N, r8, T, *dev, 0)) *
+                                 static_cast<size_t>(T) * static_cast<size_t>(r8) * 4;
   const size_t p_bytes = up256(std::max(p_main, p_u));
   void* buf = nullptr;
   if (cudaMallocFromPoolAsync(&buf, dy_bytes + w_bytes + a_bytes + b_bytes + u_bytes + p_bytes,
@@ -606,9 +611,21 @@ int rg_out_prod_lora(int variant, int wtype, const void* W, int64_t N, int64_t K
   uint16_t* b16 = reinterpret_cast<uint16_t*>(b + dy_bytes + w_bytes + a_bytes);
   float* u32 = reinterpret_cast<float*>(b + dy_bytes + w_bytes + a_bytes + b_bytes);
   float* part = reinterpret_cast<float*>(b + dy_bytes + w_bytes + a_bytes + b_bytes + u_bytes);
-  cudaError_t e = launch_convert_dy(dY, T, N, N, 1, ld, bf16, dy16, *dev, s);
-  if (e == cudaSuccess) e = launch_convert_dy(lora_b, N, rank, rank, 1, r8, bf16, b16, *dev, s);
-  if (e == cudaSuccess) e = launch_convert_dy(lora_a, rank, K, K, 1, K, bf16, a16, *dev, s, scale);
+  cudaError_t e = launch_convert_dy(lora_a, rank, K, K, 1, K, bf16, a16, *dev, s, scale);
+  if (fused) {
+    // one pass over dY: its 16-bit copy and U behind it
+    if (e == cudaSuccess) e = launch_convert_dy(lora_b, rank, N, 1, rank, ldb, bf16, b16, *dev, s);
+    if (e == cudaSuccess) e = launch_convert_dy_adapter(dY, T, N, b16, ldb, rank, ld, bf16, dy16, s);
+  } else {
+    // U [T, r8] = dY . B as an OUT_PROD over B's 16-bit copy (ranks past
+    // `rank` are zero), then packed behind dY's columns
+    if (e == cudaSuccess) e = launch_convert_dy(dY, T, N, N, 1, ld, bf16, dy16, *dev, s);
+    if (e == cudaSuccess) e = launch_convert_dy(lora_b, N, rank, rank, 1, r8, bf16, b16, *dev, s);
+    if (e == cudaSuccess)
+      e = launch_tc(bf16 ? RG_BF16 : RG_F16, b16, N, r8, dy16, ld, T, u32, r8, 0.0f, part, *dev,
+                    s, 0, 0);
+    if (e == cudaSuccess) e = launch_adapter_pack(u32, r8, T, rank, N, ld, bf16, dy16, *dev, s);
+  }
   const void* Wtc = W;
   int wtc = wtype;
   if (wtype == RG_F32) {
@@ -617,14 +634,13 @@ int rg_out_prod_lora(int variant, int wtype, const void* W, int64_t N, int64_t K
     Wtc = w16;
     wtc = RG_BF16;
   }
-  // U [T, r8] = dY . B over B's 16-bit copy (ranks past `rank` are zero)
-  if (e == cudaSuccess)
-    e = launch_tc(bf16 ? RG_BF16 : RG_F16, b16, N, r8, dy16, ld, T, u32, r8, 0.0f, part, *dev, s,
-                  0, 0);
-  if (e == cudaSuccess) e = launch_adapter_pack(u32, r8, T, rank, N, ld, bf16, dy16, *dev, s);
+  cudaEvent_t ev0 = t_prof_before, ev1 = t_prof_after;
+  t_prof_before = t_prof_after = nullptr;
+  if (e == cudaSuccess && ev0) e = cudaEventRecord(ev0, s);
   if (e == cudaSuccess)
     e = launch_tc(wtc, Wtc, N, K, dy16, ld, T, dX, K, beta, part, *dev, s, cg, env().inject_stall,
                   a16, rank);
+  if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, s);
   const cudaError_t f = cudaFreeAsync(buf, s);
   return from_cuda(e == cudaSuccess ? f : e);
 }

@@ -89,6 +89,16 @@ cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t dy_
 cudaError_t launch_adapter_pack(const float* U, int64_t ldu, int64_t T, int64_t rank, int64_t N,
                                 int64_t ld, bool bf16, uint16_t* out, const DevInfo& dev,
                                 cudaStream_t stream);
+// Ranks up to kAdapterFusedRank take the fused route: launch_convert_dy_adapter
+// writes dY's 16-bit copy and U = dY . B (16-bit operands, F32 accumulation)
+// after it in one pass over dY; bt is B^T [rank, ldb] 16-bit (ldb % 8 == 0),
+// and the copy's columns are as launch_adapter_pack leaves them.  (A rank-64
+// build of it cost more than the separate tensor-core product of U: its warp
+// MMAs and B^T's re-reads from L2 grow with the rank.)
+constexpr int64_t kAdapterFusedRank = 32;
+cudaError_t launch_convert_dy_adapter(const float* dY, int64_t T, int64_t N, const uint16_t* bt,
+                                      int64_t ldb, int64_t rank, int64_t ld, bool bf16,
+                                      uint16_t* out, cudaStream_t stream);
 // Ranges of n the F32 route splits dY . B into (its workspace holds
 // parts * T * rank floats).
 int adapter_down_parts(int64_t N, int64_t T, int64_t rank, const DevInfo& dev);

@@ -70,7 +70,8 @@ def _kfit(wtype, K, variant):
 @pytest.mark.parametrize("wtype", [inputs.Q4_K, inputs.Q8_0, inputs.Q5_0, inputs.Q6_K, inputs.F16,
                                    inputs.BF16, inputs.F32])
 @pytest.mark.parametrize("shape", [(200, 512, 300, 16), (64, 256, 1, 7), (1000, 768, 130, 100),
-                                   (72, 1024, 33, 1)])
+                                   (72, 1024, 33, 1), (201, 512, 77, 32), (130, 256, 40, 33),
+                                   (96, 512, 50, 9)])
 def test_lora_parity(rg, variant, wtype, shape):
     N, K, T, R = shape
     K = _kfit(wtype, K, variant)
@@ -138,7 +139,7 @@ def test_lora_split_contraction(rg):
     _check(got, ref, oracle.abs_bound(dY, Wd), oracle.lora_bound(dY, A, B, 1.0), 1)
 
 
-@pytest.mark.parametrize("R", [16, 64])
+@pytest.mark.parametrize("R", [16, 32, 64])
 def test_lora_layer_size_sampled(rg, R):
     """The gate projection of a 7B layer (N = 14336 rows of K = 4096 Q4_K
     values) at T = 8192 with a rank-R adapter, in the launch configuration
