@@ -43,6 +43,14 @@ Block formats (little-endian), ggml's GGUF block types:
                    low (i < 2) or high (i >= 2) nibble of ql[64h + 32(i%2) + l]
                    and bits 2i..2i+1 of qh[32h + l] as bits 4..5;
                                                   y = (d*sc[v/16]) * (q - 32)
+* Q2_K  84 B / 256: scales[16] (lo nibble sc, hi nibble m), qs[64], fp16 d,
+                   fp16 dmin.  Value 128h + 32j + 16s + l takes bits 2j..2j+1
+                   of qs[32h + 16s + l], byte 8h + 2j + s of scales;
+                                                  y = (d*sc)*q - dmin*m
+* Q3_K 110 B / 256: hmask[32], qs[64], 12 B of sixteen 6-bit scales, fp16 d.
+                   Value 128h + 32j + 16s + l: q = bits 2j..2j+1 of
+                   qs[32h + 16s + l], minus 4 unless bit 4h + j of
+                   hmask[16s + l] is set;         y = (d*(sc - 32)) * q
 * F16 / BF16: 2 B per value.
 * F32: 4 B per value, the value itself.
 
@@ -57,11 +65,11 @@ import numpy as np
 
 F16, BF16, Q8_0, Q4_0, Q4_K = 1, 2, 3, 4, 5
 Q4_1, Q5_0, Q5_1, Q5_K, Q6_K = 6, 7, 8, 9, 10
-F32 = 11
+F32, Q2_K, Q3_K = 11, 12, 13
 
 _BLOCK = {F16: (1, 2), BF16: (1, 2), Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144),
           Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q5_K: (256, 176),
-          Q6_K: (256, 210), F32: (1, 4)}
+          Q6_K: (256, 210), F32: (1, 4), Q2_K: (256, 84), Q3_K: (256, 110)}
 
 
 def row_bytes(wtype: int, K: int) -> int:
@@ -271,6 +279,70 @@ def decode_q6_k(W, N: int, K: int) -> np.ndarray:
     return y.astype(np.float32).reshape(N, K)
 
 
+def decode_q2_k(W, N: int, K: int) -> np.ndarray:
+    """Q2_K: value v = 128h + 32j + 16s + l (h, s = 0..1, j = 0..3,
+    l = 0..15): q = bits 2j..2j+1 of qs[32h + 16s + l]; its sub-block of 16
+    takes scales byte 8h + 2j + s, low nibble sc, high nibble m;
+    y = (F32(d) * sc) * q - F32(dmin) * m.  d * sc * q is exact (11 + 4 + 2
+    bits), the subtraction rounds once."""
+    blk = _rows(W, N, K, Q2_K).reshape(N, K // 256, 84)
+    sb = blk[..., 0:16].astype(np.int64)
+    qs = blk[..., 16:80].astype(np.int64)
+    d = f16_bits_to_f32(_le16(blk[..., 80], blk[..., 81]))
+    dmin = f16_bits_to_f32(_le16(blk[..., 82], blk[..., 83]))
+    q = np.empty(blk.shape[:-1] + (256,), dtype=np.float32)
+    sub = np.empty(256, dtype=np.int64)   # the scales byte of each value
+    for h in range(2):
+        for j in range(4):
+            for s in range(2):
+                v0 = 128 * h + 32 * j + 16 * s
+                q[..., v0: v0 + 16] = (qs[..., 32 * h + 16 * s: 32 * h + 16 * s + 16] >> (2 * j)) & 3
+                sub[v0: v0 + 16] = 8 * h + 2 * j + s
+    dsc = d[..., None] * (sb & 0x0F).astype(np.float32)    # exact
+    dmm = dmin[..., None] * (sb >> 4).astype(np.float32)   # exact
+    y = dsc[..., sub] * q - dmm[..., sub]
+    return y.astype(np.float32).reshape(N, K)
+
+
+def q3_k_scales(S: np.ndarray) -> np.ndarray:
+    """The sixteen 6-bit scales of a Q3_K super-block from its 12 bytes S
+    (last axis): scale i has low 4 bits from S[i] (i < 8, low nibble) or
+    S[i - 8] (high nibble), and high 2 bits from bits 2(i // 4).. of
+    S[8 + i % 4]; the value used is the 6-bit number minus 32."""
+    S = np.asarray(S).astype(np.int64)
+    out = np.empty(S.shape[:-1] + (16,), dtype=np.int64)
+    for i in range(16):
+        lo = (S[..., i] & 0x0F) if i < 8 else (S[..., i - 8] >> 4)
+        hi = (S[..., 8 + i % 4] >> (2 * (i // 4))) & 3
+        out[..., i] = (lo | (hi << 4)) - 32
+    return out
+
+
+def decode_q3_k(W, N: int, K: int) -> np.ndarray:
+    """Q3_K: value v = 128h + 32j + 16s + l: q = (bits 2j..2j+1 of
+    qs[32h + 16s + l]) - (0 if bit 4h + j of hmask[16s + l] is set else 4);
+    y = (F32(d) * sc) * q with sc the sub-block's scale (byte index
+    8h + 2j + s).  Both products are exact (11 + 6 + 3 bits)."""
+    blk = _rows(W, N, K, Q3_K).reshape(N, K // 256, 110)
+    hm = blk[..., 0:32].astype(np.int64)
+    qs = blk[..., 32:96].astype(np.int64)
+    sc = q3_k_scales(blk[..., 96:108]).astype(np.float32)
+    d = f16_bits_to_f32(_le16(blk[..., 108], blk[..., 109]))
+    q = np.empty(blk.shape[:-1] + (256,), dtype=np.float32)
+    sub = np.empty(256, dtype=np.int64)
+    for h in range(2):
+        for j in range(4):
+            for s in range(2):
+                v0 = 128 * h + 32 * j + 16 * s
+                low = (qs[..., 32 * h + 16 * s: 32 * h + 16 * s + 16] >> (2 * j)) & 3
+                high = (hm[..., 16 * s: 16 * s + 16] >> (4 * h + j)) & 1
+                q[..., v0: v0 + 16] = low - 4 * (1 - high)
+                sub[v0: v0 + 16] = 8 * h + 2 * j + s
+    dsc = d[..., None] * sc          # exact
+    y = dsc[..., sub] * q            # exact
+    return y.astype(np.float32).reshape(N, K)
+
+
 def decode_f16(W, N: int, K: int) -> np.ndarray:
     b = _rows(W, N, K, F16).reshape(N, K, 2)
     return f16_bits_to_f32(_le16(b[..., 0], b[..., 1]))
@@ -289,7 +361,7 @@ def decode_bf16(W, N: int, K: int) -> np.ndarray:
 _DECODERS = {F16: decode_f16, BF16: decode_bf16, Q8_0: decode_q8_0,
              Q4_0: decode_q4_0, Q4_K: decode_q4_k, Q4_1: decode_q4_1,
              Q5_0: decode_q5_0, Q5_1: decode_q5_1, Q5_K: decode_q5_k,
-             Q6_K: decode_q6_k, F32: decode_f32}
+             Q6_K: decode_q6_k, F32: decode_f32, Q2_K: decode_q2_k, Q3_K: decode_q3_k}
 
 
 def dequant(wtype: int, W, N: int, K: int) -> np.ndarray:

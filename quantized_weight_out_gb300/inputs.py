@@ -30,6 +30,12 @@ Formats written (little-endian, the block layouts of ggml's GGUF types):
   ``qh[l]`` = fifth bit of value 64c+l / 64c+32+l), 128 bytes of nibbles.
 * Q6_K 210 B / 256 values: ``ql[128]`` (low 4 bits), ``qh[64]`` (2 high bits
   each), 16 int8 ``scales``, fp16 ``d``.
+* Q2_K  84 B / 256 values: 16 bytes of (scale | min << 4), ``qs[64]`` (2 bits
+  each: value 128h + 32j + 16s + l in bits 2j..2j+1 of ``qs[32h + 16s + l]``),
+  fp16 ``d``, fp16 ``dmin``.
+* Q3_K 110 B / 256 values: ``hmask[32]`` (bit 4h + j of ``hmask[16s + l]``:
+  the value's third bit), ``qs[64]`` (low 2 bits as Q2_K), 12 bytes of
+  sixteen 6-bit scales, fp16 ``d``.
 * F16 / BF16: 2 B per value; F32: 4 B per value.
 
 The generator recipes follow the workload descriptions of the llama.cpp fork's
@@ -49,15 +55,17 @@ import numpy as np
 # weight type codes (the C ABI uses the same integers)
 F16, BF16, Q8_0, Q4_0, Q4_K = 1, 2, 3, 4, 5
 Q4_1, Q5_0, Q5_1, Q5_K, Q6_K, F32 = 6, 7, 8, 9, 10, 11
+Q2_K, Q3_K = 12, 13
 TYPE_NAMES = {F16: "f16", BF16: "bf16", Q8_0: "q8_0", Q4_0: "q4_0", Q4_K: "q4_k",
-              Q4_1: "q4_1", Q5_0: "q5_0", Q5_1: "q5_1", Q5_K: "q5_k", Q6_K: "q6_k", F32: "f32"}
+              Q4_1: "q4_1", Q5_0: "q5_0", Q5_1: "q5_1", Q5_K: "q5_k", Q6_K: "q6_k", F32: "f32",
+              Q2_K: "q2_k", Q3_K: "q3_k"}
 NAME_TO_TYPE = {v: k for k, v in TYPE_NAMES.items()}
 ALL_TYPES = [Q8_0, Q4_0, Q4_K, F16, BF16, Q4_1, Q5_0, Q5_1, Q5_K, Q6_K, F32]
 
 # (values per block, bytes per block)
 BLOCK = {F16: (1, 2), BF16: (1, 2), Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144),
          Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q5_K: (256, 176),
-         Q6_K: (256, 210), F32: (1, 4)}
+         Q6_K: (256, 210), F32: (1, 4), Q2_K: (256, 84), Q3_K: (256, 110)}
 
 
 def row_bytes(wtype: int, K: int) -> int:
@@ -324,6 +332,58 @@ def pack_q6_k(d_bits, sc, q) -> np.ndarray:
     return out
 
 
+def pack_q2_k(d_bits, dmin_bits, sc, m, q) -> np.ndarray:
+    """Q2_K super-blocks [B, 84] from fp16 d and dmin, 4-bit scales sc and
+    mins m [B, 16] and values q [B, 256] in 0..3 (value 128h + 32j + 16s + l
+    in bits 2j..2j+1 of qs[32h + 16s + l]; its scales byte 8h + 2j + s)."""
+    q = np.asarray(q, dtype=np.uint8)
+    B = q.shape[0]
+    qs = np.zeros((B, 64), dtype=np.uint8)
+    for h in range(2):
+        for j in range(4):
+            for s in range(2):
+                v0 = 128 * h + 32 * j + 16 * s
+                qs[:, 32 * h + 16 * s: 32 * h + 16 * s + 16] |= (q[:, v0: v0 + 16] & 3) << (2 * j)
+    out = np.empty((B, 84), dtype=np.uint8)
+    out[:, 0:16] = (np.asarray(sc, dtype=np.uint8) & 15) | (np.asarray(m, dtype=np.uint8) << 4)
+    out[:, 16:80] = qs
+    out[:, 80:82] = _f16_le(np.asarray(d_bits, dtype=np.uint16))
+    out[:, 82:84] = _f16_le(np.asarray(dmin_bits, dtype=np.uint16))
+    return out
+
+
+def pack_q3_k(d_bits, sc6, q) -> np.ndarray:
+    """Q3_K super-blocks [B, 110] from fp16 d, 6-bit scales sc6 [B, 16] in
+    0..63 (the scale used is sc6 - 32) and values q [B, 256] in -4..3 (low
+    2 bits as Q2_K, hmask bit set when q >= 0)."""
+    q = np.asarray(q, dtype=np.int64)
+    B = q.shape[0]
+    low = (q & 3).astype(np.uint8)            # q + 4 = low + 4 * bit: low = q mod 4
+    bit = (q >= 0).astype(np.uint8)
+    hm = np.zeros((B, 32), dtype=np.uint8)
+    qs = np.zeros((B, 64), dtype=np.uint8)
+    for h in range(2):
+        for j in range(4):
+            for s in range(2):
+                v0 = 128 * h + 32 * j + 16 * s
+                qs[:, 32 * h + 16 * s: 32 * h + 16 * s + 16] |= low[:, v0: v0 + 16] << (2 * j)
+                hm[:, 16 * s: 16 * s + 16] |= bit[:, v0: v0 + 16] << (4 * h + j)
+    sc6 = np.asarray(sc6, dtype=np.uint8)
+    S = np.zeros((B, 12), dtype=np.uint8)
+    for i in range(16):
+        if i < 8:
+            S[:, i] |= sc6[:, i] & 15
+        else:
+            S[:, i - 8] |= (sc6[:, i] & 15) << 4
+        S[:, 8 + i % 4] |= (sc6[:, i] >> 4) << (2 * (i // 4))
+    out = np.empty((B, 110), dtype=np.uint8)
+    out[:, 0:32] = hm
+    out[:, 32:96] = qs
+    out[:, 96:108] = S
+    out[:, 108:110] = _f16_le(np.asarray(d_bits, dtype=np.uint16))
+    return out
+
+
 # ----------------------------------------------------------------------------
 # weights and activations for one call
 
@@ -354,6 +414,22 @@ def gen_weight(wtype: int, N: int, K: int, seed: int, stream: int) -> np.ndarray
         sc = uniform_int(seed, stream, nb * 16, 256, field=3).reshape(nb, 16) - 128
         q = uniform_int(seed, stream, nb * 256, 64, field=5).reshape(nb, 256)
         return pack_q6_k(f32_to_f16_bits(d), sc, q).reshape(-1)
+    if wtype == Q2_K:
+        # fields drawn directly: |d * sc * q| ~ 5e-4 * 15 * 3 ~ 0.02
+        nb = N * K // 256
+        d = np.abs(normal_f32(seed, stream, nb, 5e-4, field=1))
+        dmin = np.abs(normal_f32(seed, stream, nb, 5e-4, field=2))
+        sc = uniform_int(seed, stream, nb * 16, 16, field=3).reshape(nb, 16)
+        m = uniform_int(seed, stream, nb * 16, 16, field=4).reshape(nb, 16)
+        q = uniform_int(seed, stream, nb * 256, 4, field=5).reshape(nb, 256)
+        return pack_q2_k(f32_to_f16_bits(d), f32_to_f16_bits(dmin), sc, m, q).reshape(-1)
+    if wtype == Q3_K:
+        # fields drawn directly, d signed: |d * (sc - 32) * q| ~ 2e-4 * 32 * 4
+        nb = N * K // 256
+        d = normal_f32(seed, stream, nb, 2e-4, field=1)
+        sc6 = uniform_int(seed, stream, nb * 16, 64, field=3).reshape(nb, 16)
+        q = uniform_int(seed, stream, nb * 256, 8, field=5).reshape(nb, 256) - 4
+        return pack_q3_k(f32_to_f16_bits(d), sc6, q).reshape(-1)
     if wtype in (Q4_1, Q5_0, Q5_1):
         # fields drawn directly (the pages give no workload of these types):
         # a block of N(0, 0.02) weights spans about 0.08, so d ~ 0.08 / levels

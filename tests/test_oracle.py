@@ -172,6 +172,68 @@ def test_q6_k_hand_superblock(golden_dir):
         assert math.fsum(float(x) for x in y[lo:hi]) == v
 
 
+def _k_fixture(golden_dir, name, build):
+    rows = _read(golden_dir, name)
+    kv, ats, subs = {}, [], []
+    for r in rows:
+        if r[0] == "at":
+            ats.append((int(r[1]), float(r[2])))
+        elif r[0] == "subsum":
+            subs.append((int(r[1]), int(r[2]), float(r[3])))
+        else:
+            kv[r[0]] = r[1:]
+    return np.frombuffer(bytes(build(kv)), dtype=np.uint8), ats, subs
+
+
+def _q2_k_bytes(kv):
+    blk = bytearray(84)
+    for b in range(16):
+        blk[b] = ((b % 15) + 1) | ((b % 4) << 4)
+    for x in range(64):
+        blk[16 + x] = sum(((x + j) % 4) << (2 * j) for j in range(4))
+    blk[80:82] = int(kv["d"][0], 16).to_bytes(2, "little")
+    blk[82:84] = int(kv["dmin"][0], 16).to_bytes(2, "little")
+    return blk
+
+
+def _q3_k_bytes(kv):
+    blk = bytearray(110)
+    for x in range(32):
+        blk[x] = 0x0F if x < 16 else 0x33
+    for x in range(64):
+        blk[32 + x] = sum(((x + j) % 4) << (2 * j) for j in range(4))
+    blk[96:108] = bytes.fromhex(kv["scales"][0])
+    blk[108:110] = int(kv["d"][0], 16).to_bytes(2, "little")
+    return blk
+
+
+@pytest.mark.parametrize("name,build,decode", [
+    ("q2_k_superblock.txt", _q2_k_bytes, qop.decode_q2_k),
+    ("q3_k_superblock.txt", _q3_k_bytes, qop.decode_q3_k)])
+def test_q2_q3_k_hand_superblocks(golden_dir, name, build, decode):
+    W, ats, subs = _k_fixture(golden_dir, name, build)
+    y = decode(W, 1, 256)[0]
+    for i, v in ats:
+        assert y[i] == np.float32(v), (i, y[i], v)
+    for lo, hi, v in subs:
+        assert math.fsum(float(x) for x in y[lo:hi]) == v
+
+
+def test_q3_k_scales_unpack_every_field():
+    """Each 6-bit scale set alone to 63 (others 0) lights exactly its own
+    output: the low nibble and the two high bits come from the bytes the
+    definition names."""
+    for i in range(16):
+        S = np.zeros(12, np.uint8)
+        if i < 8:
+            S[i] |= 15
+        else:
+            S[i - 8] |= 15 << 4
+        S[8 + i % 4] |= 3 << (2 * (i // 4))
+        sc = oracle.q3_k_scales(S) + 32
+        assert sc[i] == 63 and np.count_nonzero(sc) == 1, (i, sc)
+
+
 def test_half_codes_hand_decoded(golden_dir):
     for kind, code, val in _read(golden_dir, "half_codes.txt"):
         bits = np.array([int(code, 16)], dtype=np.uint16)
@@ -430,13 +492,43 @@ def _py_decode(wtype, raw, N, K):
                     q = ((byte >> 4) if i >= 2 else (byte & 15)) | (((blk[128 + 32 * h + l] >> (2 * i)) & 3) << 4)
                     sc = blk[192 + v // 16] - 256 if blk[192 + v // 16] > 127 else blk[192 + v // 16]
                     out[n][256 * b + v] = d * sc * (q - 32)
+        elif wtype == inputs.Q2_K:
+            for b in range(K // 256):
+                blk = row[84 * b: 84 * b + 84]
+                d, dmin = _py_f16(blk[80], blk[81]), _py_f16(blk[82], blk[83])
+                for v in range(256):
+                    h, rest = divmod(v, 128)
+                    j, rest = divmod(rest, 32)
+                    s, l = divmod(rest, 16)
+                    q = (blk[16 + 32 * h + 16 * s + l] >> (2 * j)) & 3
+                    sb = blk[8 * h + 2 * j + s]
+                    # F32 evaluation: exact product, one rounding in the difference
+                    val = np.float32(np.float32(d * (sb & 15)) * q) - np.float32(dmin * (sb >> 4))
+                    out[n][256 * b + v] = float(val)
+        elif wtype == inputs.Q3_K:
+            for b in range(K // 256):
+                blk = row[110 * b: 110 * b + 110]
+                d = _py_f16(blk[108], blk[109])
+                S = blk[96:108]
+                for v in range(256):
+                    h, rest = divmod(v, 128)
+                    j, rest = divmod(rest, 32)
+                    s, l = divmod(rest, 16)
+                    i = 8 * h + 2 * j + s
+                    lo4 = (S[i] & 15) if i < 8 else (S[i - 8] >> 4)
+                    hi2 = (S[8 + i % 4] >> (2 * (i // 4))) & 3
+                    q = (blk[32 + 32 * h + 16 * s + l] >> (2 * j)) & 3
+                    if not (blk[16 * s + l] >> (4 * h + j)) & 1:
+                        q -= 4
+                    out[n][256 * b + v] = d * ((lo4 | (hi2 << 4)) - 32) * q
     return out
 
 
 BRUTE = [(inputs.Q8_0, 40, 64, 3), (inputs.Q4_0, 33, 96, 2), (inputs.Q4_K, 12, 512, 2),
          (inputs.F16, 24, 40, 3), (inputs.BF16, 24, 40, 3), (inputs.Q8_0, 7, 32, 1),
          (inputs.Q4_1, 21, 64, 2), (inputs.Q5_0, 19, 96, 2), (inputs.Q5_1, 17, 64, 2),
-         (inputs.Q5_K, 10, 512, 2), (inputs.Q6_K, 9, 512, 2), (inputs.F32, 20, 48, 3)]
+         (inputs.Q5_K, 10, 512, 2), (inputs.Q6_K, 9, 512, 2), (inputs.F32, 20, 48, 3),
+         (inputs.Q2_K, 11, 512, 2), (inputs.Q3_K, 10, 512, 2)]
 
 
 @pytest.mark.parametrize("wtype,N,K,T", BRUTE)
@@ -594,6 +686,46 @@ def _mut_q6_k_pairs_by_parity(W, N, K):
     fixed = pair(qh, 0) | (pair(qh, 1) << 2) | (pair(qh, 0) << 4) | (pair(qh, 1) << 6)
     blk[..., 128:192] = fixed.astype(np.uint8)
     return qop.decode_q6_k(blk.reshape(-1), N, K)
+
+
+def _mut_q2_k_scale_min_swapped(W, N, K):
+    """The high nibble taken as the scale and the low as the min."""
+    blk = np.array(qop._rows(W, N, K, qop.Q2_K).reshape(N, K // 256, 84))
+    sb = blk[..., 0:16]
+    blk[..., 0:16] = ((sb >> 4) | (sb << 4)).astype(np.uint8)
+    return qop.decode_q2_k(blk.reshape(-1), N, K)
+
+
+def _mut_q3_k_hmask_bit_j(W, N, K):
+    """The third bit read from bit j of hmask for both halves (not 4h + j)."""
+    blk = np.array(qop._rows(W, N, K, qop.Q3_K).reshape(N, K // 256, 110))
+    hm = blk[..., 0:32].astype(np.int64)
+    blk[..., 0:32] = ((hm & 0x0F) | ((hm & 0x0F) << 4)).astype(np.uint8)
+    return qop.decode_q3_k(blk.reshape(-1), N, K)
+
+
+def _mut_q3_k_unbiased_scale(W, N, K):
+    """The 6-bit scale used without subtracting 32."""
+    return qop.decode_q3_k(W, N, K) * 0 + _q3_k_plus32(W, N, K)
+
+
+def _q3_k_plus32(W, N, K):
+    real = qop.q3_k_scales
+    qop.q3_k_scales = lambda S: real(S) + 32
+    try:
+        return qop.decode_q3_k(W, N, K)
+    finally:
+        qop.q3_k_scales = real
+
+
+def test_q2_q3_k_mutants_are_caught(golden_dir):
+    for name, build, mutants in [
+            ("q2_k_superblock.txt", _q2_k_bytes, [_mut_q2_k_scale_min_swapped]),
+            ("q3_k_superblock.txt", _q3_k_bytes, [_mut_q3_k_hmask_bit_j, _mut_q3_k_unbiased_scale])]:
+        W, ats, subs = _k_fixture(golden_dir, name, build)
+        for mut in mutants:
+            y = mut(W, 1, 256)[0]
+            assert any(y[i] != np.float32(v) for i, v in ats), (name, mut.__name__)
 
 
 def test_q6_k_mutant_is_caught(golden_dir):
@@ -828,3 +960,27 @@ def test_lora_at_matches_full():
     v, b = oracle.lora_at(dY, A, B, 1.25, ts, ks)
     assert np.allclose(v, full[ts, ks], rtol=1e-12, atol=1e-12)
     assert np.allclose(b, bnd[ts, ks], rtol=1e-12)
+
+
+def test_q2_q3_k_pack_roundtrip_through_oracle():
+    """The generators' packers place every field where the oracle reads it."""
+    rng = np.random.default_rng(7)
+    B = 3
+    d = rng.integers(0x3000, 0x3c00, B).astype(np.uint16)
+    dmin = rng.integers(0x2c00, 0x3800, B).astype(np.uint16)
+    sc = rng.integers(0, 16, (B, 16))
+    m = rng.integers(0, 16, (B, 16))
+    q = rng.integers(0, 4, (B, 256))
+    W = inputs.pack_q2_k(d, dmin, sc, m, q).reshape(-1)
+    y = oracle.decode_q2_k(W, B, 256)
+    df, mf = qop.f16_bits_to_f32(d), qop.f16_bits_to_f32(dmin)
+    sub = np.array([8 * (v // 128) + 2 * ((v % 128) // 32) + (v % 32) // 16 for v in range(256)])
+    want = (df[:, None] * sc[:, sub].astype(np.float32)) * q.astype(np.float32) \
+        - mf[:, None] * m[:, sub].astype(np.float32)
+    assert _bits_equal(y, want.astype(np.float32))
+    sc6 = rng.integers(0, 64, (B, 16))
+    q3 = rng.integers(-4, 4, (B, 256))
+    W = inputs.pack_q3_k(d, sc6, q3).reshape(-1)
+    y = oracle.decode_q3_k(W, B, 256)
+    want = (df[:, None] * (sc6[:, sub] - 32).astype(np.float32)) * q3.astype(np.float32)
+    assert _bits_equal(y, want.astype(np.float32))
