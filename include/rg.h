@@ -33,8 +33,9 @@
  *    contraction: dX = beta * dX (dX = 0 when beta == 0).
  *  - K must be a multiple of 256 for the quantized types (whole 256-value
  *    tiles of every block type) and a multiple of 8 for F32, F16 and BF16
- *    (16-byte rows); otherwise RG_ERR_SHAPE.  Q6_K on the tensor-core and
- *    small-T variants also needs K % 2048 == 0 (16-byte aligned rows).
+ *    (16-byte rows); otherwise RG_ERR_SHAPE.  On the tensor-core and small-T
+ *    variants Q6_K and Q3_K also need K % 2048 == 0 and Q2_K K % 1024 == 0
+ *    (16-byte aligned rows).
  *  - Every device-side wait is bounded (about 2 s); a wait that gives up
  *    records RG_ERR_TIMEOUT in a per-device status word that rg_check reads.
  */
@@ -71,17 +72,26 @@ typedef enum {
                      210*K/256 bytes are 16-byte aligned only when K % 2048 == 0,
                      which the tensor-core and small-T variants need (else
                      RG_ERR_SHAPE; RG_VARIANT_AUTO then runs the SIMT variant)   */
-    RG_F32 = 11   /* IEEE binary32, 4 B per value.  The tensor-core variants round W
+    RG_F32 = 11,  /* IEEE binary32, 4 B per value.  The tensor-core variants round W
                      and dY to bf16 (F32 range, relative error at most 2^-9 each)
                      in the workspace; the other variants use the F32 values    */
+    RG_Q2_K = 12, /* 84 B / 256 values: scales[16] (lo nibble sc, hi nibble m),
+                     qs[64], fp16 d, fp16 dmin.  Value 128h+32j+16s+l: bits 2j..2j+1
+                     of qs[32h+16s+l], scales byte 8h+2j+s; value d*sc*q - dmin*m.
+                     Rows 16-byte aligned only when K % 1024 == 0 (as Q6_K)     */
+    RG_Q3_K = 13  /* 110 B / 256 values: hmask[32], qs[64], 12 B of sixteen 6-bit
+                     scales, fp16 d.  Value 128h+32j+16s+l: low bits as Q2_K, minus
+                     4 unless bit 4h+j of hmask[16s+l] is set; value d*(sc-32)*q.
+                     Rows 16-byte aligned only when K % 2048 == 0 (as Q6_K)     */
 } rg_wtype;
 
 typedef enum {
     RG_OK = 0,
     RG_ERR_ARG = -1,     /* NULL pointer where data is needed, negative or too large size */
     RG_ERR_TYPE = -2,    /* unknown wtype, or unknown variant                              */
-    RG_ERR_SHAPE = -3,   /* K not a multiple of 256 (quantized) or 8 (F32/F16/BF16); Q6_K with
-                            K % 2048 != 0 on a tensor-core or small-T variant               */
+    RG_ERR_SHAPE = -3,   /* K not a multiple of 256 (quantized) or 8 (F32/F16/BF16); Q6_K or
+                            Q3_K with K % 2048 != 0, Q2_K with K % 1024 != 0, on a
+                            tensor-core or small-T variant                                   */
     RG_ERR_ALIGN = -4,   /* W, dY, dX or out not 16-byte aligned                           */
     RG_ERR_CUDA = -5,    /* a CUDA runtime/driver call or a launch failed                  */
     RG_ERR_TIMEOUT = -6  /* a bounded device-side wait gave up (reported by rg_check)      */
@@ -293,7 +303,8 @@ int rg_dequant_async(int wtype, const void* W, int64_t N, int64_t K, float* out,
 
 /* Stored bytes of one row of K values: K/32*34 (Q8_0), K/32*18 (Q4_0),
  * K/32*20 (Q4_1), K/32*22 (Q5_0), K/32*24 (Q5_1), K/256*144 (Q4_K),
- * K/256*176 (Q5_K), K/256*210 (Q6_K), 2K (F16, BF16), 4K (F32); 0 for an unknown type
+ * K/256*176 (Q5_K), K/256*210 (Q6_K), K/256*84 (Q2_K), K/256*110 (Q3_K), 2K (F16,
+ * BF16), 4K (F32); 0 for an unknown type
  * or a K that is not a whole number of blocks. */
 size_t rg_row_bytes(int wtype, int64_t K);
 

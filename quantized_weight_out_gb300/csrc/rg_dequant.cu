@@ -158,7 +158,7 @@ cudaError_t launch_dequant(int wtype, const void* W, int64_t N, int64_t K, float
   const uint8_t* w = static_cast<const uint8_t*>(W);
   return with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
     constexpr int WT = decltype(wt)::value;
-    if constexpr (WT == RG_Q6_K || WT == RG_F32)
+    if constexpr (WT == RG_Q6_K || WT == RG_F32 || WT == RG_Q2_K || WT == RG_Q3_K)
       dequant_bytes_kernel<WT><<<grid_for(N * (K >> 3), 256, dev), 256, 0, stream>>>(w, N, K, rb, out);
     else
       dequant_kernel<WT><<<grid, 256, 0, stream>>>(w, N, K, rb, out);

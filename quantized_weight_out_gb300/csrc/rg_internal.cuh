@@ -19,17 +19,21 @@ namespace rg {
 // ---------------------------------------------------------------------------
 // storage formats: values per block, bytes per block
 
-__host__ __device__ constexpr bool valid_wtype(int wt) { return wt >= RG_F16 && wt <= RG_F32; }
+__host__ __device__ constexpr bool valid_wtype(int wt) { return wt >= RG_F16 && wt <= RG_Q3_K; }
 __host__ __device__ constexpr bool is_quant(int wt) {
   return valid_wtype(wt) && wt != RG_F16 && wt != RG_BF16 && wt != RG_F32;
 }
 __host__ __device__ constexpr int block_values(int wt) {
-  return (wt == RG_Q4_K || wt == RG_Q5_K || wt == RG_Q6_K) ? 256 : is_quant(wt) ? 32 : 1;
+  return (wt == RG_Q4_K || wt == RG_Q5_K || wt == RG_Q6_K || wt == RG_Q2_K || wt == RG_Q3_K) ? 256
+         : is_quant(wt)                                                                   ? 32
+                                                                                          : 1;
 }
 __host__ __device__ constexpr int block_bytes(int wt) {
   return wt == RG_Q4_K   ? 144
          : wt == RG_Q5_K ? 176
          : wt == RG_Q6_K ? 210
+         : wt == RG_Q2_K ? 84
+         : wt == RG_Q3_K ? 110
          : wt == RG_Q8_0 ? 34
          : wt == RG_Q4_0 ? 18
          : wt == RG_Q4_1 ? 20
@@ -454,6 +458,36 @@ __device__ __forceinline__ void decode8_f32(const uint8_t* row, int k0, float (&
     for (int j = 0; j < 8; ++j) {
       const int q = ((i >= 2 ? (ql[j] >> 4) : ql[j]) & 15) | (((qh[j] >> (2 * i)) & 3) << 4);
       out[j] = ds * static_cast<float>(q - 32);
+    }
+  } else if constexpr (WT == RG_Q2_K) {
+    // value v = 128h + 32j + 16s + l: bits 2j.. of qs[32h + 16s + l], scales
+    // byte 8h + 2j + s; (d * sc) * q exact, minus dmin * m rounded once
+    const uint8_t* blk = row + (k0 >> 8) * 84;
+    const int v0 = k0 & 255;
+    const int h = v0 >> 7, j = (v0 >> 5) & 3, sb = (v0 >> 4) & 1, l0 = v0 & 15;
+    const int b = blk[8 * h + 2 * j + sb];
+    const float ds = f16_to_f32(ld_u16(blk + 80)) * static_cast<float>(b & 15);
+    const float dm = f16_to_f32(ld_u16(blk + 82)) * static_cast<float>(b >> 4);
+    const uint8_t* qs = blk + 16 + 32 * h + 16 * sb + l0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) out[i] = fmaf(ds, static_cast<float>((qs[i] >> (2 * j)) & 3), -dm);
+  } else if constexpr (WT == RG_Q3_K) {
+    // value v = 128h + 32j + 16s + l: bits 2j.. of qs[32h + 16s + l], minus 4
+    // unless bit 4h + j of hmask[16s + l]; (d * (sc - 32)) * q, all exact
+    const uint8_t* blk = row + (k0 >> 8) * 110;
+    const int v0 = k0 & 255;
+    const int h = v0 >> 7, j = (v0 >> 5) & 3, sb = (v0 >> 4) & 1, l0 = v0 & 15;
+    const int si = 8 * h + 2 * j + sb;
+    const uint8_t* S = blk + 96;
+    const int lo4 = si < 8 ? (S[si] & 15) : (S[si - 8] >> 4);
+    const int hi2 = (S[8 + (si & 3)] >> (2 * (si >> 2))) & 3;
+    const float ds = f16_to_f32(ld_u16(blk + 108)) * static_cast<float>((lo4 | (hi2 << 4)) - 32);
+    const uint8_t* qs = blk + 32 + 32 * h + 16 * sb + l0;
+    const uint8_t* hm = blk + 16 * sb + l0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int q = ((qs[i] >> (2 * j)) & 3) - (((hm[i] >> (4 * h + j)) & 1) ? 0 : 4);
+      out[i] = ds * static_cast<float>(q);
     }
   } else if constexpr (WT == RG_Q5_K) {
     const uint8_t* blk = row + (k0 >> 8) * 176;

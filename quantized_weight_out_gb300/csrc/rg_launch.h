@@ -48,6 +48,8 @@ R with_wtype(int wtype, R fallback, F&& f) {
     case RG_Q5_1: return f(std::integral_constant<int, RG_Q5_1>{});
     case RG_Q5_K: return f(std::integral_constant<int, RG_Q5_K>{});
     case RG_Q6_K: return f(std::integral_constant<int, RG_Q6_K>{});
+    case RG_Q2_K: return f(std::integral_constant<int, RG_Q2_K>{});
+    case RG_Q3_K: return f(std::integral_constant<int, RG_Q3_K>{});
     case RG_F32: return f(std::integral_constant<int, RG_F32>{});
     default: return fallback;
   }

@@ -28,7 +28,11 @@ constexpr int THREADS = 256;   // 8 consumer warps (plus one producer warp)
 // Raw bytes one lane needs from a row for its 8 values (a 256-value tile).
 template <int WT>
 struct Raw {
-  uint32_t v[WT == RG_Q5_K || WT == RG_F32 ? 8 : WT == RG_Q4_K ? 6 : WT == RG_Q6_K ? 5 : (WT == RG_Q8_0 || WT == RG_Q4_0 || WT == RG_Q4_1) ? 3 : 4];
+  uint32_t v[WT == RG_Q5_K || WT == RG_F32 ? 8
+             : WT == RG_Q4_K                  ? 6
+             : WT == RG_Q6_K || WT == RG_Q3_K ? 5
+             : (WT == RG_Q8_0 || WT == RG_Q4_0 || WT == RG_Q4_1) ? 3
+                                                                  : 4];
 };
 
 // The bytes one lane needs for its 8 values, from a row tile staged in
@@ -84,6 +88,29 @@ __device__ __forceinline__ void load_raw_smem(const uint8_t* tile, int lane, Raw
     r.v[3] = static_cast<uint32_t>(qh[2]) | (static_cast<uint32_t>(qh[3]) << 16);
     r.v[4] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tile + 208)) |
              (static_cast<uint32_t>(tile[192 + (lane >> 1)]) << 16);
+  } else if constexpr (WT == RG_Q2_K || WT == RG_Q3_K) {
+    // values 8*lane .. +7 = 128h + 32j + 16s + l0 .. +7 (tile: the
+    // super-block's first byte, 2-byte aligned): 8 bytes of qs (and of
+    // hmask), the sub-block's scale byte(s), d (and dmin)
+    const int h = lane >> 4, j = (lane >> 2) & 3, sb = (lane >> 1) & 1, l0 = 8 * (lane & 1);
+    constexpr int QS = WT == RG_Q2_K ? 16 : 32;
+    const uint16_t* q = reinterpret_cast<const uint16_t*>(tile + QS + 32 * h + 16 * sb + l0);
+    r.v[0] = static_cast<uint32_t>(q[0]) | (static_cast<uint32_t>(q[1]) << 16);
+    r.v[1] = static_cast<uint32_t>(q[2]) | (static_cast<uint32_t>(q[3]) << 16);
+    const int si = 8 * h + 2 * j + sb;
+    if constexpr (WT == RG_Q2_K) {
+      r.v[2] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tile + 80)) |
+               (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tile + 82)) << 16);
+      r.v[3] = tile[si];
+    } else {
+      const uint16_t* hm = reinterpret_cast<const uint16_t*>(tile + 16 * sb + l0);
+      r.v[2] = static_cast<uint32_t>(hm[0]) | (static_cast<uint32_t>(hm[1]) << 16);
+      r.v[3] = static_cast<uint32_t>(hm[2]) | (static_cast<uint32_t>(hm[3]) << 16);
+      // d, the byte with the scale's low nibble, the byte with its high bits
+      r.v[4] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tile + 108)) |
+               (static_cast<uint32_t>(tile[96 + (si & 7)]) << 16) |
+               (static_cast<uint32_t>(tile[104 + (si & 3)]) << 24);
+    }
   } else {
     // Q4_K, Q5_K: the header, this lane's 8 bytes of nibbles (and of qh)
     constexpr int QS = WT == RG_Q5_K ? 48 : 16;
@@ -154,6 +181,35 @@ __device__ __forceinline__ void decode_raw(const Raw<WT>& r, int lane, float (&w
       w[4 * jj + 2] = ds * byte_minus<2>(x, kTwo23 + 32.0f);
       w[4 * jj + 3] = ds * byte_minus<3>(x, kTwo23 + 32.0f);
     }
+  } else if constexpr (WT == RG_Q2_K) {
+    // (d * sc) * q exact, minus dmin * m: one rounding, like the definition
+    const int j = (lane >> 2) & 3;
+    const float ds = f16_to_f32(static_cast<uint16_t>(r.v[2] & 0xFFFFu)) * static_cast<float>(r.v[3] & 15u);
+    const float ndm = -(f16_to_f32(static_cast<uint16_t>(r.v[2] >> 16)) * static_cast<float>(r.v[3] >> 4));
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const uint32_t x = (r.v[jj] >> (2 * j)) & 0x03030303u;
+      w[4 * jj + 0] = fmaf(ds, byte_minus<0>(x, kTwo23), ndm);
+      w[4 * jj + 1] = fmaf(ds, byte_minus<1>(x, kTwo23), ndm);
+      w[4 * jj + 2] = fmaf(ds, byte_minus<2>(x, kTwo23), ndm);
+      w[4 * jj + 3] = fmaf(ds, byte_minus<3>(x, kTwo23), ndm);
+    }
+  } else if constexpr (WT == RG_Q3_K) {
+    // q + 4 = low bits | third bit << 2; (d * (sc - 32)) * q, all exact
+    const int h = lane >> 4, j = (lane >> 2) & 3, sb = (lane >> 1) & 1;
+    const int si = 8 * h + 2 * j + sb;
+    const uint32_t lob = (r.v[4] >> 16) & 0xFFu, hib = r.v[4] >> 24;
+    const int sc = static_cast<int>(((si < 8 ? lob : lob >> 4) & 15u) | (((hib >> (2 * (si >> 2))) & 3u) << 4)) - 32;
+    const float ds = f16_to_f32(static_cast<uint16_t>(r.v[4] & 0xFFFFu)) * static_cast<float>(sc);
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const uint32_t x = ((r.v[jj] >> (2 * j)) & 0x03030303u) |
+                         (((r.v[2 + jj] >> (4 * h + j)) & 0x01010101u) << 2);
+      w[4 * jj + 0] = ds * byte_minus<0>(x, kTwo23 + 4.0f);
+      w[4 * jj + 1] = ds * byte_minus<1>(x, kTwo23 + 4.0f);
+      w[4 * jj + 2] = ds * byte_minus<2>(x, kTwo23 + 4.0f);
+      w[4 * jj + 3] = ds * byte_minus<3>(x, kTwo23 + 4.0f);
+    }
   } else if constexpr (WT == RG_Q4_1 || WT == RG_Q5_0 || WT == RG_Q5_1) {
     // values 8(lane & 3) .. +7 of block lane >> 2: nibbles (low for the
     // first 16 values of the block, high for the rest) and the fifth bits
@@ -212,20 +268,25 @@ __device__ __forceinline__ void decode_raw(const Raw<WT>& r, int lane, float (&w
 template <int WT>
 __host__ __device__ constexpr int tile_bytes();
 
-// Bytes a stage holds per row: the 256-value tile, except Q6_K, whose 210-byte
-// super-blocks start at any even offset of a 16-byte grain: a 224-byte
-// window from the grain before (window_offset bytes in).
+// Super-blocks that are not a multiple of 16 bytes (Q6_K 210, Q3_K 110, Q2_K
+// 84) start at an even offset of a 16-byte grain: a stage row holds a window
+// from the grain before (window_offset bytes in), 16-byte multiple wide.
+template <int WT>
+__host__ __device__ constexpr bool windowed() {
+  return WT == RG_Q6_K || WT == RG_Q3_K || WT == RG_Q2_K;
+}
+// Bytes a stage holds per row: the 256-value tile, or its window.
 template <int WT>
 __host__ __device__ constexpr int stage_row_bytes() {
-  return WT == RG_Q6_K ? 224 : tile_bytes<WT>();
+  return WT == RG_Q6_K ? 224 : WT == RG_Q3_K ? 128 : WT == RG_Q2_K ? 96 : tile_bytes<WT>();
 }
 template <int WT>
 __host__ __device__ constexpr int64_t window_start(int64_t kt) {
-  return WT == RG_Q6_K ? ((kt * 210) & ~int64_t{15}) : kt * tile_bytes<WT>();
+  return windowed<WT>() ? ((kt * block_bytes(WT)) & ~int64_t{15}) : kt * tile_bytes<WT>();
 }
 template <int WT>
 __host__ __device__ constexpr int window_offset(int64_t kt) {
-  return WT == RG_Q6_K ? static_cast<int>((kt * 210) & 15) : 0;
+  return windowed<WT>() ? static_cast<int>((kt * block_bytes(WT)) & 15) : 0;
 }
 
 template <int WT>
@@ -238,7 +299,7 @@ __host__ __device__ constexpr int tile_bytes() {
 // 32 rows in an 8-deep ring (4-deep for F32 W, whose rows are four times
 // wider than the quantized ones).
 template <int WT, int TB>
-constexpr bool rows_path() { return TB <= 2 && is_quant(WT) && WT != RG_Q6_K; }
+constexpr bool rows_path() { return TB <= 2 && is_quant(WT) && !windowed<WT>(); }
 template <int WT, int TB>
 constexpr int stage_rows() { return rows_path<WT, TB>() ? 64 : 32; }
 template <int WT, int TB>

@@ -69,6 +69,8 @@ __host__ __device__ constexpr int p_row_bytes() {
          : WT == RG_Q5_1 ? 112
          : WT == RG_Q5_K ? 176
          : WT == RG_Q6_K ? 240
+         : WT == RG_Q3_K ? 128
+         : WT == RG_Q2_K ? 96
                          : 0;
 }
 
@@ -402,6 +404,90 @@ __device__ __forceinline__ void dec_q6_k_row(const uint8_t* row, uint8_t* A, int
   }
 }
 
+// Q2_K: a whole row's half (128 values, H = the half) from a window whose
+// super-block starts O bytes in (O = 0, 4, 8, 12).  Value 128H + 32j + 16s
+// + l: bits 2j..2j+1 of qs[32H + 16s + l]; its scales byte 8H + 2j + s gives
+// sc (low nibble) and m; the operand is fp16(q * fp16(d*sc) - fp16(dmin*m)).
+template <int O, int H>
+__device__ __forceinline__ void dec_q2_k_row(const uint8_t* row, uint8_t* A, int n) {
+  constexpr int QSB = O + 8 * H, QQ = O + 16 + 32 * H, QD = O + 80;
+  static_assert(O % 4 == 0 && QD + 4 <= p_row_bytes<RG_Q2_K>(), "aligned words inside the window");
+  constexpr int CS = QSB / 16, CS1 = (QSB + 7) / 16;
+  constexpr int CQ = QQ / 16, CQ1 = (QQ + 31) / 16;
+  constexpr int CD = QD / 16;
+  const auto rs = load_chunks<CS, CS1>(row);
+  const auto rq = load_chunks<CQ, CQ1>(row);
+  const auto rd = load_chunks<CD, CD>(row);
+  const uint32_t dw = rd.word_at(QD - 16 * CD);
+  const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(dw & 0xFFFFu)));
+  const float dmin = __half2float(__ushort_as_half(static_cast<uint16_t>(dw >> 16)));
+  const uint32_t sw[2] = {rs.word_at(QSB - 16 * CS), rs.word_at(QSB - 16 * CS + 4)};
+  const __half2 magic = __float2half2_rn(1024.0f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int sb = 0; sb < 2; ++sb) {
+      const uint32_t b = (sw[j >> 1] >> (8 * (2 * (j & 1) + sb))) & 0xFFu;  // byte 2j + sb
+      const __half2 ds = __float2half2_rn(d * static_cast<float>(b & 15u));       // exact product
+      const __half2 nm = __float2half2_rn(-(dmin * static_cast<float>(b >> 4)));  // exact product
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {  // l = 8c .. 8c+7
+        const int x = QQ - 16 * CQ + 16 * sb + 8 * c;
+        uint32_t o[4];
+        four_affine((rq.word_at(x) >> (2 * j)) & 0x03030303u, magic, ds, nm, o[0], o[1]);
+        four_affine((rq.word_at(x + 4) >> (2 * j)) & 0x03030303u, magic, ds, nm, o[2], o[3]);
+        st_a_chunk(A, n, 4 * j + 2 * sb + c, o[0], o[1], o[2], o[3]);
+      }
+    }
+}
+
+// Q3_K: a whole row's half from a window whose super-block starts O bytes in
+// (O even).  Value 128H + 32j + 16s + l: q + 4 = (bits 2j..2j+1 of
+// qs[32H + 16s + l]) | (bit 4H + j of hmask[16s + l]) << 2; the sub-block's
+// 6-bit scale i = 8H + 2j + s; the operand is fp16(d * (sc - 32)) * q.
+template <int O, int H>
+__device__ __forceinline__ void dec_q3_k_row(const uint8_t* row, uint8_t* A, int n) {
+  constexpr int QH = O, QQ = O + 32 + 32 * H, QS = O + 96, QD = O + 108;
+  constexpr auto last = [](int x) { return (x & 3) == 0 ? x + 3 : (x & ~3) + 7; };
+  constexpr int CH = QH / 16, CH1 = CH + last(QH - 16 * CH + 28) / 16;
+  constexpr int CQ = QQ / 16, CQ1 = CQ + last(QQ - 16 * CQ + 28) / 16;
+  constexpr int CS = QS / 16, CS1 = CS + last(QD - 16 * CS) / 16;
+  static_assert(O % 2 == 0 && 16 * CH1 + 16 <= p_row_bytes<RG_Q3_K>() &&
+                    16 * CQ1 + 16 <= p_row_bytes<RG_Q3_K>() && 16 * CS1 + 16 <= p_row_bytes<RG_Q3_K>(),
+                "reads stay inside the row window");
+  const auto rh = load_chunks<CH, CH1>(row);
+  const auto rq = load_chunks<CQ, CQ1>(row);
+  const auto rs = load_chunks<CS, CS1>(row);
+  constexpr int XH = QH - 16 * CH, XQ = QQ - 16 * CQ, XS = QS - 16 * CS, XD = QD - 16 * CS;
+  const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(rs.word_at(XD) & 0xFFFFu)));
+  // the scales' low nibbles of this half: bytes 0..7 (H = 0: low nibbles;
+  // H = 1: high nibbles), their high bits: bytes 8..11, bits 2(i / 4)..
+  const uint32_t s_lo[2] = {rs.word_at(XS), rs.word_at(XS + 4)};
+  const uint32_t s_hi = rs.word_at(XS + 8);
+  const __half2 off = __float2half2_rn(1028.0f);  // 1024 + 4
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int sb = 0; sb < 2; ++sb) {
+      const int i = 8 * H + 2 * j + sb;
+      const uint32_t lo = (s_lo[(i & 7) >> 2] >> (8 * (i & 3) + 4 * H)) & 15u;
+      const uint32_t hi = (s_hi >> (8 * (i & 3) + 2 * (i >> 2))) & 3u;
+      const int sc = static_cast<int>(lo | (hi << 4)) - 32;
+      const __half2 ds = __float2half2_rn(d * static_cast<float>(sc));  // exact product, one rounding
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {  // l = 8c .. 8c+7
+        uint32_t o[4];
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          const uint32_t q = (rq.word_at(XQ + 16 * sb + 8 * c + 4 * w) >> (2 * j)) & 0x03030303u;
+          const uint32_t hb = (rh.word_at(XH + 16 * sb + 8 * c + 4 * w) >> (4 * H + j)) & 0x01010101u;
+          four_scaled(q | (hb << 2), off, ds, o[2 * w], o[2 * w + 1]);
+        }
+        st_a_chunk(A, n, 4 * j + 2 * sb + c, o[0], o[1], o[2], o[3]);
+      }
+    }
+}
+
 // Block b (32-value types) or part b (Q4_K, Q5_K: chunk b >> 1 of the
 // half, 16 bytes b & 1) of row n of a stage.
 template <int WT, int ODD, int B>
@@ -425,10 +511,12 @@ template <int WT, int ODD, int NPART, int O = 0>
 __device__ __forceinline__ void decode_stage_warp(const uint8_t* __restrict__ P,
                                                   uint8_t* __restrict__ A, int lane, int part) {
   constexpr int PR = p_row_bytes<WT>();
-  if constexpr (WT == RG_Q6_K) {
+  if constexpr (WT == RG_Q6_K || WT == RG_Q3_K || WT == RG_Q2_K) {
     static_assert(NPART == 2, "a lane decodes one row's half");
     const int n = lane + 32 * part;
-    dec_q6_k_row<O, ODD>(P + n * PR, A, n);
+    if constexpr (WT == RG_Q6_K) dec_q6_k_row<O, ODD>(P + n * PR, A, n);
+    else if constexpr (WT == RG_Q3_K) dec_q3_k_row<O, ODD>(P + n * PR, A, n);
+    else dec_q2_k_row<O, ODD>(P + n * PR, A, n);
     return;
   }
 #pragma unroll
@@ -455,6 +543,8 @@ __device__ __forceinline__ int p_window_start(int kt) {
   if constexpr (WT == RG_Q5_1) return kt * 96;
   if constexpr (WT == RG_Q5_K) return (kt >> 1) * 176;
   if constexpr (WT == RG_Q6_K) return ((kt >> 1) * 210) & ~15;
+  if constexpr (WT == RG_Q3_K) return ((kt >> 1) * 110) & ~15;
+  if constexpr (WT == RG_Q2_K) return ((kt >> 1) * 84) & ~15;
   return (kt >> 1) * 144;  // Q4_K: the whole super-block
 }
 
@@ -732,22 +822,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!__all_sync(0xffffffffu, mbar_wait(full_p(s), ph, ctl, abort_flag))) break;
           if (c >= c_ad) {
             // nothing to decode
-          } else if constexpr (WT == RG_Q6_K) {
-            // the super-block starts o bytes into its window: one decoder per o
-            const int o = ((kt >> 1) * 210) & 15;
+          } else if constexpr (WT == RG_Q6_K || WT == RG_Q3_K || WT == RG_Q2_K) {
+            // the super-block starts o bytes into its window: one decoder per
+            // o (Q6_K, Q3_K: any even o; Q2_K: a multiple of 4)
+            const int o = ((kt >> 1) * block_bytes(WT)) & 15;
             const uint8_t* P = sP + s * C::P_STAGE;
             uint8_t* Ad = sA + s * A_STAGE;
-#define RG_Q6K_CASE(OO)                                                          \
+#define RG_WIN_CASE(OO)                                                          \
   case OO / 2:                                                                   \
-    if (kt & 1) decode_stage_warp<WT, 1, WPS, OO>(P, Ad, lane, part);            \
-    else decode_stage_warp<WT, 0, WPS, OO>(P, Ad, lane, part);                   \
+    if constexpr (WT != RG_Q2_K || OO % 4 == 0) {                                \
+      if (kt & 1) decode_stage_warp<WT, 1, WPS, OO>(P, Ad, lane, part);          \
+      else decode_stage_warp<WT, 0, WPS, OO>(P, Ad, lane, part);                 \
+    }                                                                            \
     break;
             switch (o >> 1) {
-              RG_Q6K_CASE(0) RG_Q6K_CASE(2) RG_Q6K_CASE(4) RG_Q6K_CASE(6)
-              RG_Q6K_CASE(8) RG_Q6K_CASE(10) RG_Q6K_CASE(12) RG_Q6K_CASE(14)
+              RG_WIN_CASE(0) RG_WIN_CASE(2) RG_WIN_CASE(4) RG_WIN_CASE(6)
+              RG_WIN_CASE(8) RG_WIN_CASE(10) RG_WIN_CASE(12) RG_WIN_CASE(14)
               default: break;
             }
-#undef RG_Q6K_CASE
+#undef RG_WIN_CASE
           } else if (kt & 1) {
             decode_stage_warp<WT, 1, WPS>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part);
           } else {

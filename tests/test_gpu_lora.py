@@ -61,14 +61,15 @@ def _check(got, ref, bnd_base, bnd_lora, variant, what=""):
 
 
 def _kfit(wtype, K, variant):
-    if wtype == inputs.Q6_K and variant != 3:
-        return (K + 2047) // 2048 * 2048
+    a = {inputs.Q6_K: 2048, inputs.Q3_K: 2048, inputs.Q2_K: 1024}.get(wtype)
+    if a and variant != 3:
+        return (K + a - 1) // a * a
     return K
 
 
 @pytest.mark.parametrize("variant", [1, 2, 3, 4, 5])
 @pytest.mark.parametrize("wtype", [inputs.Q4_K, inputs.Q8_0, inputs.Q5_0, inputs.Q6_K, inputs.F16,
-                                   inputs.BF16, inputs.F32])
+                                   inputs.BF16, inputs.F32, inputs.Q2_K, inputs.Q3_K])
 @pytest.mark.parametrize("shape", [(200, 512, 300, 16), (64, 256, 1, 7), (1000, 768, 130, 100),
                                    (72, 1024, 33, 1), (201, 512, 77, 32), (130, 256, 40, 33),
                                    (96, 512, 50, 9)])

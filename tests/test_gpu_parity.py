@@ -33,11 +33,16 @@ def _dev():
     return torch.device("cuda:0")
 
 
+ROW_ALIGN_K = {inputs.Q6_K: 2048, inputs.Q3_K: 2048, inputs.Q2_K: 1024}
+
+
 def kfit(wtype, K, variant):
-    """Q6_K rows are 16-byte aligned only for K % 2048 == 0, which every
-    variant but the SIMT one needs: round K up for those."""
-    if wtype == inputs.Q6_K and variant != 3:
-        return -(-K // 2048) * 2048
+    """Q6_K and Q3_K rows are 16-byte aligned only for K % 2048 == 0, Q2_K
+    rows for K % 1024 == 0, which every variant but the SIMT one needs: round
+    K up for those."""
+    a = ROW_ALIGN_K.get(wtype)
+    if a and variant != 3:
+        return -(-K // a) * a
     return K
 
 
@@ -254,24 +259,26 @@ def test_split_contraction(rg, variant, wtype, beta):
     assert_within(got, ref, bnd + extra, 5e-3, f"split variant {variant} type {wtype}")
 
 
-def test_q6_k_unaligned_rows(rg):
-    """K % 2048 != 0: the tensor-core and small-T variants refuse the shape
-    (nothing launched), and the dispatcher runs the SIMT variant instead."""
-    N, K, T = 70, 768, 40                 # rows of 630 bytes: only 2-byte aligned
-    W = inputs.gen_weight(inputs.Q6_K, N, K, seed=41, stream=1)
+@pytest.mark.parametrize("wtype", [inputs.Q6_K, inputs.Q3_K, inputs.Q2_K])
+def test_unaligned_super_block_rows(rg, wtype):
+    """K % 2048 (Q2_K: 1024) != 0: the tensor-core and small-T variants
+    refuse the shape (nothing launched), and the dispatcher runs the SIMT
+    variant instead."""
+    N, K, T = 70, 768, 40                 # Q6_K rows of 630 bytes: only 2-byte aligned
+    W = inputs.gen_weight(wtype, N, K, seed=41, stream=1)
     dY = inputs.normal_f32(41, 2, T * N, 1e-3).reshape(T, N)
     dev, s = _dev(), torch.cuda.current_stream()
     Wt, dYt = torch.from_numpy(W).to(dev), torch.from_numpy(dY).to(dev)
     dX = torch.full((T, K), 3.0, device=dev)
     for v in (1, 2, 4, 5):
-        assert rg.rg_out_prod_variant(v, inputs.Q6_K, Wt, N, K, dYt, T, dX, 0.0, s) == rg.RG_ERR_SHAPE
+        assert rg.rg_out_prod_variant(v, wtype, Wt, N, K, dYt, T, dX, 0.0, s) == rg.RG_ERR_SHAPE
     torch.cuda.synchronize()
     assert bool(torch.all(dX == 3.0))
-    assert rg.rg_select_variant(inputs.Q6_K, N, K, T) == rg.RG_VARIANT_SIMT32
-    got = run_out_prod(rg, 0, inputs.Q6_K, W, N, K, dY, T)
-    Wd = oracle.dequant(inputs.Q6_K, W, N, K)
-    assert_within(got, oracle.out_prod(inputs.Q6_K, W, N, K, dY, T, Wd=Wd),
-                  oracle.abs_bound(dY, Wd), 1e-5, "q6_k simt")
+    assert rg.rg_select_variant(wtype, N, K, T) == rg.RG_VARIANT_SIMT32
+    got = run_out_prod(rg, 0, wtype, W, N, K, dY, T)
+    Wd = oracle.dequant(wtype, W, N, K)
+    assert_within(got, oracle.out_prod(wtype, W, N, K, dY, T, Wd=Wd),
+                  oracle.abs_bound(dY, Wd), 1e-5, "simt")
 
 
 # ----------------------------------------------------------------------------

@@ -322,6 +322,20 @@ def _all_ones_weight(wtype, N, K, variant=0):
         d, sc = (bytes([0x00, 0x3C]), 1) if variant == 0 else (bytes([0x00, 0x38]), 2)
         blk = bytes([0x11]) * 128 + bytes([0xAA]) * 64 + bytes([sc]) * 16 + d
         return np.frombuffer(blk * (N * K // 256), dtype=np.uint8)
+    if wtype == inputs.Q2_K:
+        if variant == 0:         # d = 1, sc = 1, m = 0, q = 1 (every 2-bit field 01)
+            blk = bytes([0x01]) * 16 + bytes([0x55]) * 64 + bytes([0x00, 0x3C, 0x00, 0x00])
+        else:                    # d = 1, sc = 1, q = 3, dmin = 1, m = 2: 3 - 2 = 1
+            blk = bytes([0x21]) * 16 + bytes([0xFF]) * 64 + bytes([0x00, 0x3C, 0x00, 0x3C])
+        return np.frombuffer(blk * (N * K // 256), dtype=np.uint8)
+    if wtype == inputs.Q3_K:
+        if variant == 0:         # d = 1, scale 33 - 32 = 1 (low 1, high 2), q = 1 (bit set)
+            S = bytes([0x11]) * 8 + bytes([0xAA]) * 4
+            blk = bytes([0xFF]) * 32 + bytes([0x55]) * 64 + S + bytes([0x00, 0x3C])
+        else:                    # d = 1, scale 31 - 32 = -1 (low 15, high 1), q = 3 - 4 = -1
+            S = bytes([0xFF]) * 8 + bytes([0x55]) * 4
+            blk = bytes(32) + bytes([0xFF]) * 64 + S + bytes([0x00, 0x3C])
+        return np.frombuffer(blk * (N * K // 256), dtype=np.uint8)
     if wtype == inputs.F16:
         return np.frombuffer(bytes([0x00, 0x3C]) * (N * K), dtype=np.uint8)
     if wtype == inputs.F32:
@@ -334,7 +348,8 @@ def _all_ones_weight(wtype, N, K, variant=0):
 CASES = [(inputs.Q8_0, 0), (inputs.Q4_0, 0), (inputs.Q4_K, 0), (inputs.Q4_K, 1),
          (inputs.F16, 0), (inputs.BF16, 0), (inputs.Q4_1, 0), (inputs.Q5_0, 0),
          (inputs.Q5_1, 0), (inputs.Q5_1, 1), (inputs.Q5_K, 0), (inputs.Q5_K, 1),
-         (inputs.Q6_K, 0), (inputs.Q6_K, 1), (inputs.F32, 0)]
+         (inputs.Q6_K, 0), (inputs.Q6_K, 1), (inputs.F32, 0), (inputs.Q2_K, 0),
+         (inputs.Q2_K, 1), (inputs.Q3_K, 0), (inputs.Q3_K, 1)]
 
 
 @pytest.mark.parametrize("wtype,variant", CASES)
