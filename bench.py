@@ -45,13 +45,17 @@ def _traffic_record():
     None when the kernel source has changed since those counters were taken."""
     import hashlib
     rec = os.path.join(ROOT, "profiles", "tc_traffic.json")
-    src = os.path.join(ROOT, "quantized_weight_out_gb300", "csrc", "rg_tc.cu")
-    if not (os.path.exists(rec) and os.path.exists(src)):
+    csrc = os.path.join(ROOT, "quantized_weight_out_gb300", "csrc")
+    srcs = [os.path.join(csrc, f) for f in ("rg_tc_kernel.cuh", "rg_tc.cu")]
+    if not (os.path.exists(rec) and all(os.path.exists(x) for x in srcs)):
         return None, None
     with open(rec) as f:
         d = json.load(f)
-    with open(src, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()
+    h = hashlib.sha256()
+    for x in srcs:
+        with open(x, "rb") as f:
+            h.update(f.read())
+    sha = h.hexdigest()
     if d.get("source_sha256") != sha:
         return None, d.get("workload")
     return d.get("dram_bytes_per_launch"), d.get("workload")
