@@ -170,8 +170,12 @@ int rg_out_prod_ws(int variant, int wtype, const void* W, int64_t N, int64_t K,
  * exits.  It calls no cudaMalloc, cudaFree or pool routine.
  *
  * Same arguments, layouts and results as rg_out_prod (same kernels, same
- * variant choice).  Limits: when the chosen variant is a tensor-core one, the
- * 16-bit copy of dY, T * (N rounded up to 8) * 2 bytes, must fit the scratch,
+ * variant choice), except that its tensor-core plans never share the last
+ * tiles' contraction over all units (stream-K): those partial slabs would
+ * not fit the scratch.  Where rg_out_prod would, the two results differ in
+ * summation order only, both within the same error bound.  Limits: when the
+ * chosen variant is a tensor-core one, the 16-bit copy of dY, T * (N rounded
+ * up to 8) * 2 bytes (plus any split partial sums), must fit the scratch,
  * else RG_ERR_ARG and nothing is launched (e.g. T = 2048 allows N <= 8192).
  * The scratch is shared by every call on a device and keeps the last call's
  * contents (each call overwrites what it reads; nothing needs clearing), so
@@ -271,7 +275,8 @@ typedef struct rg_plan_info {
   int32_t n_splits;         /* contraction over N split into this many partial sums (1: none) */
   int32_t grid;             /* CTAs of the main kernel (tensor-core: before the residency cap) */
   int32_t launches;         /* kernels one call enqueues */
-  int32_t reserved;         /* 0 */
+  int32_t stream_k;         /* tensor-core variants: 1 when the last tiles' contraction is
+                               shared evenly over all units (stream-K), else 0 */
   int64_t decode_ops;       /* weight values decoded per call: ceil(T / tile_t) * N * K */
   int64_t workspace_bytes;  /* what rg_out_prod_ws needs for this variant */
 } rg_plan_info;

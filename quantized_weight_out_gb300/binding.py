@@ -28,11 +28,11 @@ class rg_plan_info(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int32), ("cta_group", ctypes.c_int32),
                 ("tile_k", ctypes.c_int32), ("tile_t", ctypes.c_int32),
                 ("n_splits", ctypes.c_int32), ("grid", ctypes.c_int32),
-                ("launches", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("launches", ctypes.c_int32), ("stream_k", ctypes.c_int32),
                 ("decode_ops", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
-        return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
+        return {name: getattr(self, name) for name, _ in self._fields_}
 
 
 # (name, restype, argtypes) of every exported function

@@ -172,9 +172,7 @@ size_t tc_partial_offset(int wtype, int64_t N, int64_t K, int64_t T) {
 }
 size_t tc_workspace_total(int variant, int wtype, int64_t N, int64_t K, int64_t T,
                           const DevInfo& dev) {
-  const int64_t splits = tc_partial_splits(N, K, T, dev, cg_force_of(variant));
-  const size_t parts = static_cast<size_t>(splits) * static_cast<size_t>(T) * static_cast<size_t>(K) * 4;
-  return tc_partial_offset(wtype, N, K, T) + (parts + 255) / 256 * 256;
+  return tc_partial_offset(wtype, N, K, T) + tc_partial_bytes(N, K, T, dev, cg_force_of(variant));
 }
 
 // Workspace bytes of a resolved (non-auto) variant; N, K, T > 0.
@@ -474,6 +472,7 @@ int rg_out_prod_ws(int variant, int wtype, const void* W, int64_t N, int64_t K, 
 
 int rg_out_prod_noalloc(int wtype, const void* W, int64_t N, int64_t K, const float* dY,
                         int64_t T, float* dX, float beta, void* stream) {
+  const NoStreamK no_stream_k;  // its partial slabs would not fit the scratch
   bool empty = false;
   int st = validate(wtype, W, N, K, dY, T, dX, Layout{N, 1, K}, &empty);
   if (st != RG_OK || empty) return st;
@@ -521,8 +520,7 @@ int rg_mul_mat(int wtype, const void* W, int64_t N, int64_t K, const float* X, i
   const bool bf16 = wtype == RG_BF16 || wtype == RG_F32;
   const size_t wt_bytes = (static_cast<size_t>(K) * static_cast<size_t>(N) * 2 + 255) / 256 * 256;
   const size_t x16 = tc_workspace(K, T);
-  const int64_t splits = tc_partial_splits(K, N, T, *dev, 0);
-  const size_t parts = (static_cast<size_t>(splits) * static_cast<size_t>(T) * static_cast<size_t>(N) * 4 + 255) / 256 * 256;
+  const size_t parts = tc_partial_bytes(K, N, T, *dev, 0);
   cudaMemPool_t pool{};
   if ((st = pool_for(dev->device, &pool)) != RG_OK) return st;
   void* buf = nullptr;
@@ -549,6 +547,7 @@ int rg_mul_mat(int wtype, const void* W, int64_t N, int64_t K, const float* X, i
 int rg_out_prod_lora(int variant, int wtype, const void* W, int64_t N, int64_t K, const float* dY,
                      int64_t T, float* dX, float beta, const float* lora_a, const float* lora_b,
                      int64_t rank, float scale, void* stream) {
+  const NoStreamK no_stream_k;  // the adapter's kernels are built without it
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Layout lay{N, 1, K};
   bool empty = false;
@@ -599,11 +598,8 @@ int rg_out_prod_lora(int variant, int wtype, const void* W, int64_t N, int64_t K
   const size_t b_bytes = up256(fused ? static_cast<size_t>(rank) * static_cast<size_t>(ldb) * 2
                                      : static_cast<size_t>(N) * static_cast<size_t>(r8) * 2);
   const size_t u_bytes = fused ? 0 : up256(static_cast<size_t>(T) * static_cast<size_t>(r8) * 4);
-  const size_t p_main = static_cast<size_t>(tc_partial_splits(ld, K, T, *dev, cg)) *
-                        static_cast<size_t>(T) * static_cast<size_t>(K) * 4;
-  const size_t p_u = fused ? 0
-                           : static_cast<size_t>(tc_partial_splits(N, r8, T, *dev, 0)) *
-                                 static_cast<size_t>(T) * static_cast<size_t>(r8) * 4;
+  const size_t p_main = tc_partial_bytes(ld, K, T, *dev, cg);
+  const size_t p_u = fused ? 0 : tc_partial_bytes(N, r8, T, *dev, 0);
   const size_t p_bytes = up256(std::max(p_main, p_u));
   void* buf = nullptr;
   if (cudaMallocFromPoolAsync(&buf, dy_bytes + w_bytes + a_bytes + b_bytes + u_bytes + p_bytes,
@@ -677,8 +673,9 @@ int rg_plan(int variant, int wtype, int64_t N, int64_t K, int64_t T, rg_plan_inf
     tile_t = p.bt;
     r.n_splits = p.n_splits;
     r.grid = p.grid;
-    // dY conversion (and F32 W's), GEMM, partial reduction
-    r.launches = (p.n_splits > 1 ? 3 : 2) + (wtype == RG_F32 ? 1 : 0);
+    r.stream_k = p.sk ? 1 : 0;
+    // dY conversion (and F32 W's), GEMM, split reduction or stream-K fixup
+    r.launches = (p.n_splits > 1 || p.sk ? 3 : 2) + (wtype == RG_F32 ? 1 : 0);
   } else if (r.variant == RG_VARIANT_SMALLT) {
     const SmalltPlan p = plan_smallt(wtype, N, K, T, *dev);
     r.tile_k = 256;

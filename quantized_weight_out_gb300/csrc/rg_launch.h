@@ -146,7 +146,20 @@ struct TcPlan {
   int grid;      // persistent CTAs (a multiple of cg), before the occupancy cap
   int band;      // k units per rasterization band (tile order), set at launch
   int n_splits;  // contraction split into this many ranges of n_chunks stages
+  bool sk;       // stream-K: whole waves of tiles, then the last tiles' chunks
+                 // shared evenly over the units (n_splits is 1)
 };
+// While one of these lives, tensor-core plans made on its thread leave
+// stream-K out: the no-alloc entry point's fixed scratch has no room for the
+// partial slabs (a whole tile per unit), and the adapter's kernels are built
+// without stream-K.
+struct NoStreamK {
+  NoStreamK();
+  ~NoStreamK();
+  NoStreamK(const NoStreamK&) = delete;
+  NoStreamK& operator=(const NoStreamK&) = delete;
+};
+
 // cg_force: 0 = choose from the shape, 1 or 2 = that tile configuration.
 TcPlan plan_tc(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force);
 int64_t tc_dy16_ld(int64_t N);
@@ -163,6 +176,17 @@ cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint
 int64_t tc_adapter_cols(int64_t N, int64_t rank);
 // Number of partial-sum slabs the tensor-core plan needs (0 when unsplit).
 int64_t tc_partial_splits(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force);
+// Bytes of the `part` workspace the tensor-core plan needs: the splits'
+// [n_splits][T][K] partial sums, or stream-K's partial slabs (a whole tile
+// per unit), or 0.
+size_t tc_partial_bytes(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force);
+// Stream-K's second pass: every tile the units shared (the plan's last
+// tiles) already holds beta * dX + its first piece in dX; the later pieces'
+// partial sums are added to it in chunk order from the slabs in `part` that
+// `units` units of cg CTAs wrote.
+cudaError_t launch_sk_fixup(const float* part, int units, int cg, int bt, const TcPlan& p, int T,
+                            int K, float* dX, int64_t ldx, const DevInfo& dev,
+                            cudaStream_t stream);
 
 // dX = beta * dX + sum of n_splits slabs of [T, K] floats, in a fixed
 // order; dX rows dx_t floats apart (a multiple of 4).

@@ -555,6 +555,65 @@ __device__ __forceinline__ int p_window_start(int kt) {
   return (kt >> 1) * 144;  // Q4_K: the whole super-block
 }
 
+// --- the work of one persistent unit -------------------------------------------
+//
+// A unit (a CTA pair, or one CTA) works through segments (item, c0, c1):
+// contraction chunks [c0, c1) of work item `item` (a tile, or a tile and a
+// contraction split).  First the data-parallel items u, u + U, ... below
+// n_dp, each whole.  Then, with stream-K, its even share of the remaining
+// n_items - n_dp tiles (fewer than U), whose chunks follow one another tile
+// by tile: chunks [g0(u), g0(u + 1)) of that run, g0(u) = floor(u * Rn / U),
+// Rn = remaining tiles x n_chunks.  A share is shorter than one tile, so it
+// touches at most two tiles: the tail of one and the head of the next, and
+// (Rn >= U, else no sharing) is never empty.  (The planner takes stream-K
+// only while Rn * U < 2^31: 32-bit arithmetic.)
+template <bool SK>
+struct Segs {
+  int item, U, n_dp, nck;
+  uint32_t g, g1;
+  __device__ __forceinline__ Segs(int u, int n_units, int n_items, int n_chunks)
+      : item(u), U(n_units), nck(n_chunks), g(0), g1(0) {
+    n_dp = n_items;
+    if constexpr (!SK) return;
+    n_dp = (n_items / n_units) * n_units;
+    // fewer chunks left than units (a residency cap can make it so): whole
+    // items only, so that every unit's share is non-empty when shared
+    if (static_cast<uint32_t>(n_items - n_dp) * static_cast<uint32_t>(n_chunks) <
+        static_cast<uint32_t>(n_units))
+      n_dp = n_items;
+    const uint32_t rn = static_cast<uint32_t>(n_items - n_dp) * static_cast<uint32_t>(n_chunks);
+    g = static_cast<uint32_t>(u) * rn / static_cast<uint32_t>(n_units);
+    g1 = static_cast<uint32_t>(u + 1) * rn / static_cast<uint32_t>(n_units);
+  }
+  __device__ __forceinline__ bool next(int& it, int& c0, int& c1) {
+    if (item < n_dp) {
+      it = item;
+      c0 = 0;
+      c1 = nck;
+      item += U;
+      return true;
+    }
+    if constexpr (!SK) return false;
+    if (g >= g1) return false;
+    const int x = static_cast<int>(g / static_cast<uint32_t>(nck));
+    it = n_dp + x;
+    c0 = static_cast<int>(g) - x * nck;
+    c1 = min(nck, c0 + static_cast<int>(g1 - g));
+    g += static_cast<uint32_t>(c1 - c0);
+    return true;
+  }
+};
+
+// Stream-K bookkeeping of a shared tile (remainder index x): its chunk run
+// [a, a + nck), a = x * nck, is shared by units sk_unit_of(a) ..
+// sk_unit_of(a + nck - 1), in chunk order.  The first of them ends its share
+// with the tile's head (chunk 0 on); every later one starts its share inside
+// the tile, and since a share is shorter than a tile that is the only piece
+// of a tile it does not begin: its partial sums go to slab u.
+__device__ __forceinline__ int sk_unit_of(uint32_t g, uint32_t rn, int U) {
+  return static_cast<int>(((g + 1) * static_cast<uint32_t>(U) - 1) / rn);
+}
+
 // --- the kernel -----------------------------------------------------------------
 //
 // Barriers (8 bytes each, per stage s unless noted):
@@ -568,7 +627,7 @@ __device__ __forceinline__ int p_window_start(int kt) {
 //   acc_full[2], acc_empty[2]   the two tensor-memory accumulators
 //   drain        local: the MMAs issued so far completed (abort path)
 
-template <int WT, int CG, int BT, bool AD>
+template <int WT, int CG, int BT, bool AD, bool SK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     out_prod_tc_kernel(const __grid_constant__ CUtensorMap map_w,
                        const __grid_constant__ CUtensorMap map_y,
@@ -669,13 +728,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t pend_p = 0, pend_ab = 0, pend_ph = 0;  // stages with copies in flight
     bool ok = true;
     bool skip_first = inject_stall != 0;
-    for (int tile = unit; tile < n_tiles && ok; tile += n_units) {
+    Segs<SK> sg(unit, n_units, n_tiles, n_chunks);
+    int tile = 0, c0 = 0, c1 = 0;
+    while (ok && sg.next(tile, c0, c1)) {
       int ku, tt;
       coords(tile, ku, tt);
       const int cbase = (tile / n_tiles1) * n_chunks;  // first contraction chunk of the split
       const int kt = ku * CG + static_cast<int>(rank);
       const int ty = tt * BT + static_cast<int>(rank) * B_ROWS;
-      for (int c = 0; c < n_chunks; ++c) {
+      for (int c = c0; c < c1; ++c) {
         ok = __all_sync(0xffffffffu, mbar_wait(empty(s), ph ^ 1u, ctl, abort_flag));
         if (!ok) break;
         if (lane == 0) {
@@ -770,15 +831,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      int j = 0;
-      for (int tile = unit; tile < n_tiles && ok; tile += n_units, ++j) {
+      Segs<SK> sg(unit, n_units, n_tiles, n_chunks);
+      int tile = 0, c0 = 0, c1 = 0;
+      for (int j = 0; ok && sg.next(tile, c0, c1); ++j) {
         const int a = j & 1;
         const uint32_t aph = (static_cast<uint32_t>(j) >> 1) & 1u;
         ok = __all_sync(0xffffffffu, wait_any(acc_empty(a), aph ^ 1u));
         if (!ok) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * BT);
-        for (int c = 0; c < n_chunks; ++c) {
+        for (int c = c0; c < c1; ++c) {
           bool got = wait_any(full_ab(s), ph);
           if constexpr (C::QUANT) got = got && wait_any(full_dec(s), ph);
           ok = __all_sync(0xffffffffu, got);
@@ -793,7 +855,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const uint64_t ad = sdesc_sw128(a_base + kk * (UMMA_K * 128), A_COLBLK, 1024);
               // B: K-major, 16 values of n = 32 bytes along the swizzled row; 8-row groups 1 KB apart
               const uint64_t bd = sdesc_sw128(b_base + kk * (UMMA_K * 2), 16, 1024);
-              const uint32_t acc = (c | kk) != 0 ? 1u : 0u;
+              const uint32_t acc = ((c - c0) | kk) != 0 ? 1u : 0u;
               if constexpr (CG == 2)
                 tc_mma_f16_pair(d_tmem, ad, bd, C::IDESC, acc);
               else
@@ -837,27 +899,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (s < S) {  // (Q6_K's four slots leave two decoder warps idle)
         // a follower's warps arrive on the issuing CTA's barrier directly
         const uint32_t done_bar = CG == 2 ? mapa_shared(full_dec(s), 0) : full_dec(s);
-        const int total = ((n_tiles - unit + n_units - 1) / n_units) * n_chunks;  // stages of this CTA
-        // walk this warp's stages s, s + S, ... without per-stage divisions
-        int tile = unit, c = s;
-        while (c >= n_chunks) { c -= n_chunks; tile += n_units; }
-        int ku, tt;
-        if (tile < n_tiles) coords(tile, ku, tt);
-        // chunks of this tile from c_ad on are the adapter's (TMA fills A)
-        int c_ad = 0;
-        if constexpr (AD) c_ad = n_main - (tile / n_tiles1) * n_chunks;
+        // walk this warp's stages s, s + S, ... of the unit's segments
+        // without per-stage divisions (c: the next one, counted from the
+        // current segment's first stage)
+        Segs<SK> sg(unit, n_units, n_tiles, n_chunks);
+        int tile = 0, c0 = 0, c1 = 0;
+        int c = s;
         uint32_t ph = 0;
-        for (int g = s; g < total; g += S, ph ^= 1u) {
+        bool run = true;
+        while (run && sg.next(tile, c0, c1)) {
+          const int len = c1 - c0;
+          if (c >= len) {
+            c -= len;
+            continue;
+          }
+          int ku, tt;
+          coords(tile, ku, tt);
           const int kt = ku * CG + static_cast<int>(rank);
-          if (!__all_sync(0xffffffffu, mbar_wait(full_p(s), ph, ctl, abort_flag))) break;
-          if (AD && c >= c_ad) {
-            // nothing to decode
-          } else if constexpr (WT == RG_Q6_K || WT == RG_Q3_K || WT == RG_Q2_K) {
-            // the super-block starts o bytes into its window: one decoder per
-            // o (Q6_K, Q3_K: any even o; Q2_K: a multiple of 4)
-            const int o = ((kt >> 1) * block_bytes(WT)) & 15;
-            const uint8_t* P = sP + s * C::P_STAGE;
-            uint8_t* Ad = sA + s * A_STAGE;
+          // chunks of this item from c_ad on are the adapter's (TMA fills A)
+          int c_ad = 0;
+          if constexpr (AD) c_ad = n_main - (tile / n_tiles1) * n_chunks;
+          for (; c < len; c += S, ph ^= 1u) {
+            const int cc = c0 + c;  // the chunk of the item
+            if (!__all_sync(0xffffffffu, mbar_wait(full_p(s), ph, ctl, abort_flag))) {
+              run = false;
+              break;
+            }
+            if (AD && cc >= c_ad) {
+              // nothing to decode
+            } else if constexpr (WT == RG_Q6_K || WT == RG_Q3_K || WT == RG_Q2_K) {
+              // the super-block starts o bytes into its window: one decoder per
+              // o (Q6_K, Q3_K: any even o; Q2_K: a multiple of 4)
+              const int o = ((kt >> 1) * block_bytes(WT)) & 15;
+              const uint8_t* P = sP + s * C::P_STAGE;
+              uint8_t* Ad = sA + s * A_STAGE;
 #define RG_WIN_CASE(OO)                                                          \
   case OO / 2:                                                                   \
     if constexpr (WT != RG_Q2_K || OO % 4 == 0) {                                \
@@ -865,31 +940,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       else decode_stage_warp<WT, 0, WPS, OO>(P, Ad, lane, part);                 \
     }                                                                            \
     break;
-            switch (o >> 1) {
-              RG_WIN_CASE(0) RG_WIN_CASE(2) RG_WIN_CASE(4) RG_WIN_CASE(6)
-              RG_WIN_CASE(8) RG_WIN_CASE(10) RG_WIN_CASE(12) RG_WIN_CASE(14)
-              default: break;
-            }
+              switch (o >> 1) {
+                RG_WIN_CASE(0) RG_WIN_CASE(2) RG_WIN_CASE(4) RG_WIN_CASE(6)
+                RG_WIN_CASE(8) RG_WIN_CASE(10) RG_WIN_CASE(12) RG_WIN_CASE(14)
+                default: break;
+              }
 #undef RG_WIN_CASE
-          } else if (kt & 1) {
-            decode_stage_warp<WT, 1, WPS>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part);
-          } else {
-            decode_stage_warp<WT, 0, WPS>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part);
+            } else if (kt & 1) {
+              decode_stage_warp<WT, 1, WPS>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part);
+            } else {
+              decode_stage_warp<WT, 0, WPS>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part);
+            }
+            if (!AD || cc < c_ad) fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if constexpr (CG == 2)
+                mbar_arrive_cluster(done_bar);
+              else
+                mbar_arrive(done_bar);
+            }
           }
-          if (!AD || c < c_ad) fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            if constexpr (CG == 2)
-              mbar_arrive_cluster(done_bar);
-            else
-              mbar_arrive(done_bar);
-          }
-          c += S;
-          if (c >= n_chunks) {
-            while (c >= n_chunks) { c -= n_chunks; tile += n_units; }
-            if (tile < n_tiles) coords(tile, ku, tt);
-            if constexpr (AD) c_ad = n_main - (tile / n_tiles1) * n_chunks;
-          }
+          c -= len;
         }
       }
     }
@@ -897,9 +968,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---------------- epilogue ----------------
     const int eq = warp & 3;  // TMEM lanes 32*eq .. 32*eq+31
     const uint32_t empty_leader = CG == 2 ? mapa_shared(acc_empty(0), 0) : acc_empty(0);
+    // split contraction: raw partial sums to part[split] (beta in the reduce);
+    // stream-K plans never split (part holds their slabs)
+    float* split_part = SK ? nullptr : part;
+    // stream-K: one partial slab per unit ([unit][CTA of the pair]
+    // [epilogue warp][t of the tile][lane]), one warp's piece SLAB_W floats
+    constexpr int SLAB_W = BT * 32;
     bool ok = true;
-    int j = 0;
-    for (int tile = unit; tile < n_tiles && ok; tile += n_units, ++j) {
+    Segs<SK> sg(unit, n_units, n_tiles, n_chunks);
+    int tile = 0, c0 = 0, c1 = 0;
+    for (int j = 0; ok && sg.next(tile, c0, c1); ++j) {
       int ku, tt;
       coords(tile, ku, tt);
       const int kt = ku * CG + static_cast<int>(rank);
@@ -910,41 +988,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const int k = kt * BM + 32 * eq + lane;
       const bool kin = k < K;
-      // split contraction: raw partial sums to part[split] (beta in the reduce)
-      float* out = part ? part + static_cast<int64_t>(tile / n_tiles1) * T * K : dX;
-      const float b = part ? 0.0f : beta;
-      const int64_t ldo = part ? static_cast<int64_t>(K) : ldx;  // row stride of `out`
+      if (!SK || c0 == 0) {
+        // a whole item, or the first piece of a shared tile (the second
+        // kernel adds the others to it): straight to dX (or to its split's slab)
+        float* out = split_part ? split_part + static_cast<int64_t>(tile / n_tiles1) * T * K : dX;
+        const float b = split_part ? 0.0f : beta;
+        const int64_t ldo = split_part ? static_cast<int64_t>(K) : ldx;  // row stride of `out`
 #pragma unroll 1
-      for (int cb = 0; cb < BT / 32; ++cb) {
-        const int tb = tt * BT + 32 * cb;
-        float old[32];
-        if (b != 0.0f && kin) {
-          // all loads of the column block first: one round trip, not 32
+        for (int cb = 0; cb < BT / 32; ++cb) {
+          const int tb = tt * BT + 32 * cb;
+          float old[32];
+          if (b != 0.0f && kin) {
+            // all loads of the column block first: one round trip, not 32
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            old[i] = (tb + i < T) ? out[static_cast<int64_t>(tb + i) * ldo + k] : 0.0f;
-        }
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * eq) << 16) +
-                               static_cast<uint32_t>(a * BT + 32 * cb),
-                           r);
-        if (kin) {
+            for (int i = 0; i < 32; ++i)
+              old[i] = (tb + i < T) ? out[static_cast<int64_t>(tb + i) * ldo + k] : 0.0f;
+          }
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * eq) << 16) +
+                                 static_cast<uint32_t>(a * BT + 32 * cb),
+                             r);
+          if (kin) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (tb + i < T) {
-              const float v = __uint_as_float(r[i]);
-              out[static_cast<int64_t>(tb + i) * ldo + k] = b != 0.0f ? fmaf(b, old[i], v) : v;
+            for (int i = 0; i < 32; ++i) {
+              if (tb + i < T) {
+                const float v = __uint_as_float(r[i]);
+                out[static_cast<int64_t>(tb + i) * ldo + k] = b != 0.0f ? fmaf(b, old[i], v) : v;
+              }
             }
           }
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (CG == 2)
-          mbar_arrive_cluster(empty_leader + 8u * a);
-        else
-          mbar_arrive(acc_empty(a));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (CG == 2)
+            mbar_arrive_cluster(empty_leader + 8u * a);
+          else
+            mbar_arrive(acc_empty(a));
+        }
+      } else if constexpr (SK) {
+        // a later piece of a tile shared by several units: raw partial sums
+        // to its slab; a second kernel adds them, in chunk order, to dX
+        float* mine = part + (static_cast<int64_t>(unit) * CG * 4 + static_cast<int64_t>(rank) * 4 + eq) *
+                                 SLAB_W;
+#pragma unroll 1
+        for (int cb = 0; cb < BT / 32; ++cb) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * eq) << 16) +
+                                 static_cast<uint32_t>(a * BT + 32 * cb),
+                             r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mine[(32 * cb + i) * 32 + lane] = __uint_as_float(r[i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (CG == 2)
+            mbar_arrive_cluster(empty_leader + 8u * a);
+          else
+            mbar_arrive(acc_empty(a));
+        }
       }
     }
   }
@@ -967,13 +1070,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // --- launch templates ---------------------------------------------------------
 
-template <int WT, int CG, int BT, bool AD>
+template <int WT, int CG, int BT, bool AD, bool SK>
 static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
                                const CUtensorMap& ml, int n_main, float* dX, int64_t ldx,
                                float beta, int T, int K, const TcPlan& p, float* part,
                                const DevInfo& dev, cudaStream_t stream, int inject) {
   using C = tc::Cfg<WT, CG, BT>;
-  auto kern = tc::out_prod_tc_kernel<WT, CG, BT, AD>;
+  auto kern = tc::out_prod_tc_kernel<WT, CG, BT, AD, SK>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   WaitCtl ctl{dev.status, dev.wait_limit_ns};
@@ -1000,25 +1103,29 @@ static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
   }
   const int units = std::min(p.grid / CG, mc);
   cfg.gridDim = dim3(static_cast<unsigned>(units * CG), 1, 1);
-  return counted(cudaLaunchKernelEx(&cfg, kern, mw, my, ml, n_main, dX, ldx, beta, T, K,
-                                    p.n_kunits, p.n_ttiles, p.band, p.n_chunks, p.n_splits, part,
-                                    ctl, inject));
+  if (SK && part == nullptr) return cudaErrorInvalidValue;
+  e = counted(cudaLaunchKernelEx(&cfg, kern, mw, my, ml, n_main, dX, ldx, beta, T, K, p.n_kunits,
+                                 p.n_ttiles, p.band, p.n_chunks, p.n_splits, part, ctl, inject));
+  if (e != cudaSuccess || !SK) return e;
+  // stream-K: the shared tiles' pieces, added in chunk order (the same unit
+  // count as the launch: the pieces' slabs follow from it)
+  return launch_sk_fixup(part, units, CG, BT, p, T, K, dX, ldx, dev, stream);
 }
 
-template <int WT, bool AD>
+template <int WT, bool AD, bool SK>
 static cudaError_t launch_tc_w(const CUtensorMap& mw, const CUtensorMap& my,
                                const CUtensorMap& ml, int n_main, float* dX, int64_t ldx,
                                float beta, int T, int K, const TcPlan& p, float* part,
                                const DevInfo& dev, cudaStream_t stream, int inject) {
   if (p.cg == 2)
-    return launch_tc_t<WT, 2, 256, AD>(mw, my, ml, n_main, dX, ldx, beta, T, K, p, part, dev, stream,
+    return launch_tc_t<WT, 2, 256, AD, SK>(mw, my, ml, n_main, dX, ldx, beta, T, K, p, part, dev, stream,
                                    inject);
-  return launch_tc_t<WT, 1, 128, AD>(mw, my, ml, n_main, dX, ldx, beta, T, K, p, part, dev, stream,
+  return launch_tc_t<WT, 1, 128, AD, SK>(mw, my, ml, n_main, dX, ldx, beta, T, K, p, part, dev, stream,
                                  inject);
 }
 
 // The body of launch_tc: AD = an adapter rides along (rank > 0).
-template <bool AD>
+template <bool AD, bool SK>
 static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K,
                                   const uint16_t* dy16, int64_t ld_dy16, int64_t T, float* dX,
                                   int64_t dx_t, float beta, float* part, const DevInfo& dev,
@@ -1029,8 +1136,9 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
   const int64_t n_ext = rank > 0 ? tc_adapter_cols(N, rank) : N;
   const int n_main = rank > 0 ? static_cast<int>((N + tc::BC - 1) / tc::BC) : (1 << 30);
   TcPlan p = plan_tc(n_ext, K, T, dev, cg_force);
-  if (p.n_splits > 1 && part == nullptr) return cudaErrorInvalidValue;
-  float* partial = p.n_splits > 1 ? part : nullptr;
+  if (p.sk != SK) return cudaErrorInvalidValue;  // the dispatcher chose the other build
+  if ((p.n_splits > 1 || p.sk) && part == nullptr) return cudaErrorInvalidValue;
+  float* partial = p.n_splits > 1 || p.sk ? part : nullptr;
   // band of k units whose slice of W fits comfortably in L2 (48 MB)
   const double w_per_value = is_quant(wtype) ? static_cast<double>(block_bytes(wtype)) / block_values(wtype) : 2.0;
   const double slice = static_cast<double>(N) * (tc::BM * p.cg) * w_per_value;
@@ -1065,17 +1173,22 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
   }
   const int t = static_cast<int>(T), k = static_cast<int>(K);
   const cudaError_t e = with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
-    return launch_tc_w<decltype(wt)::value, AD>(mw, my, ml, n_main, dX, dx_t, beta, t, k, p,
+    return launch_tc_w<decltype(wt)::value, AD, SK>(mw, my, ml, n_main, dX, dx_t, beta, t, k, p,
                                                 partial, dev, stream, inject_stall);
   });
   if (e != cudaSuccess || p.n_splits == 1) return e;
   return launch_reduce_partials(partial, p.n_splits, T, K, dX, dx_t, beta, dev, stream);
 }
 
-// launch_tc with an adapter (rg_tc_ad.cu)
+// launch_tc with an adapter (rg_tc_ad.cu; its plans never take stream-K) and
+// the stream-K plans (rg_tc_sk.cu)
 cudaError_t launch_tc_adapter(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
                               int64_t ld_dy16, int64_t T, float* dX, int64_t dx_t, float beta,
                               float* part, const DevInfo& dev, cudaStream_t stream, int cg_force,
                               int inject_stall, const uint16_t* a16, int64_t rank);
+cudaError_t launch_tc_stream_k(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
+                               int64_t ld_dy16, int64_t T, float* dX, int64_t dx_t, float beta,
+                               float* part, const DevInfo& dev, cudaStream_t stream, int cg_force,
+                               int inject_stall);
 
 }  // namespace rg
