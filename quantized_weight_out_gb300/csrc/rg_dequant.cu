@@ -173,6 +173,7 @@ template <bool BF16>
 __global__ void __launch_bounds__(256) convert_dy_kernel(const float* __restrict__ dY, int64_t T,
                                                          int64_t N, int64_t ld, float mul,
                                                          uint16_t* __restrict__ out) {
+  pdl_launch_dependents();  // the tensor-core kernel may be scheduled now (it waits for us)
   const int64_t cpr = (N + 7) >> 3;
   const int64_t total = T * cpr;
   const bool vec = (N & 3) == 0;
@@ -217,6 +218,7 @@ __global__ void __launch_bounds__(256) convert_dy_tiled_kernel(const float* __re
                                                                int64_t T, int64_t N, int64_t dy_t,
                                                                int64_t dy_n, int64_t ld,
                                                                uint16_t* __restrict__ out) {
+  pdl_launch_dependents();  // the tensor-core kernel may be scheduled now (it waits for us)
   __shared__ float tile[32][33];  // [t][n]
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 32, t0 = static_cast<int64_t>(blockIdx.y) * 32;

@@ -173,6 +173,16 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the kernel before it on the stream still
+// runs; pdl_wait() returns once that kernel has completed and its writes are
+// visible, and pdl_launch_dependents() (in the earlier kernel) lets the
+// dependent kernel be scheduled before this one ends.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (the tensor core reads operands through it).
 __device__ __forceinline__ void fence_proxy_async_smem() {

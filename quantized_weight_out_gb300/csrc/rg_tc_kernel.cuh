@@ -722,6 +722,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
+    // this kernel may start before the kernel that wrote its operands (dY's
+    // 16-bit copy, a converted W) has finished: every operand copy comes
+    // after this wait (the other roles read nothing an earlier kernel of the
+    // call writes)
+    pdl_wait();
     const uint32_t ab_bar_leader = CG == 2 ? mapa_shared(full_ab(0), 0) : full_ab(0);
     int s = 0;
     uint32_t ph = 0;
@@ -1084,13 +1089,18 @@ static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
   cfg.blockDim = dim3(tc::NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CG;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // its prologue (barriers, tensor memory, tensor-map prefetch) overlaps the
+  // end of the conversion kernel before it; the producer waits for that
+  // kernel before its first copy
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   // persistent grid: no more clusters than can be resident at once
   static int max_clusters[64] = {0};
   int& mc = max_clusters[dev.device & 63];
