@@ -9,6 +9,7 @@
 #include <algorithm>
 #include <atomic>
 #include <type_traits>
+#include <utility>
 
 #include "../../include/rg.h"
 
@@ -69,6 +70,26 @@ struct Layout {
 // deq(W)^T as fp16 (bf16 when `bf16`) [K, N], rows ldo values apart.
 cudaError_t launch_dequant_t16(int wtype, const void* W, int64_t N, int64_t K, bool bf16,
                                uint16_t* out, int64_t ldo, const DevInfo& dev, cudaStream_t stream);
+
+// Launch `kern` (a plain kernel: no cluster) so that it may be scheduled
+// while the kernel before it on the stream finishes (programmatic stream
+// serialization); the kernel must call pdl_wait() before it reads anything
+// that kernel writes.  A kernel before it that never triggers its
+// dependents (every kernel outside this library) is waited for as usual.
+template <class... P, class... A>
+cudaError_t launch_after_prev(void (*kern)(P...), dim3 grid, dim3 block, cudaStream_t stream,
+                              A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...);
+}
 
 // Blocks of a grid-stride kernel over work_items (one per thread): enough
 // for the items, at most eight per SM.

@@ -727,6 +727,7 @@ __device__ __forceinline__ int64_t dx_at(int64_t i, int64_t K, int64_t ldx) {
 __global__ void __launch_bounds__(256) smallt_reduce(const float* __restrict__ part, int n_splits,
                                                      int64_t TK, int64_t K, int64_t ldx,
                                                      float* __restrict__ dX, float beta) {
+  pdl_wait();  // the partial sums come from the kernel before this one
   for (int64_t i = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) * 4; i < TK;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x * 4) {
     float4 s = *reinterpret_cast<const float4*>(part + i);
@@ -764,6 +765,7 @@ __global__ void __launch_bounds__(256) smallt_reduce_wide(const float* __restric
                                                           int n_splits, int64_t TK, int64_t K,
                                                           int64_t ldx, float* __restrict__ dX,
                                                           float beta) {
+  pdl_wait();  // the partial sums come from the kernel before this one
   const int lane = threadIdx.x & 31;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   for (int64_t q = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; q * 4 < TK;
@@ -903,14 +905,14 @@ cudaError_t launch_reduce_partials(const float* part, int n_splits, int64_t T, i
   const int64_t quads = TK / 4;
   if (n_splits >= 4 && quads * 32 <= static_cast<int64_t>(dev.num_sms) * 2048) {
     const int64_t blocks = (quads * 32 + 255) / 256;
-    smt::smallt_reduce_wide<<<static_cast<unsigned>(std::max<int64_t>(1, blocks)), 256, 0, stream>>>(
-        part, n_splits, TK, K, dx_t, dX, beta);
-    return counted(cudaGetLastError());
+    return counted(launch_after_prev(smt::smallt_reduce_wide,
+                                     dim3(static_cast<unsigned>(std::max<int64_t>(1, blocks))),
+                                     dim3(256), stream, part, n_splits, TK, K, dx_t, dX, beta));
   }
   const int64_t blocks = std::min<int64_t>((quads + 255) / 256, static_cast<int64_t>(dev.num_sms) * 8);
-  smt::smallt_reduce<<<static_cast<unsigned>(std::max<int64_t>(1, blocks)), 256, 0, stream>>>(
-      part, n_splits, TK, K, dx_t, dX, beta);
-  return counted(cudaGetLastError());
+  return counted(launch_after_prev(smt::smallt_reduce,
+                                   dim3(static_cast<unsigned>(std::max<int64_t>(1, blocks))),
+                                   dim3(256), stream, part, n_splits, TK, K, dx_t, dX, beta));
 }
 
 }  // namespace rg

@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(kFixupThreads) sk_fixup_kernel(
     int n_kunits, int n_ttiles, int band, int T, int K, float* __restrict__ dX, int64_t ldx) {
   __shared__ int64_t s_off[256];
   __shared__ int s_meta[3];
+  pdl_wait();  // dX's head pieces and the slabs come from the main kernel before this one
   const int per_slice = bt * 8 / kFixupThreads;  // blocks per slice (4-value groups / threads)
   const int slice = blockIdx.x / per_slice;
   const int x = slice / (cg * 4), req = slice - x * (cg * 4);
@@ -166,10 +167,10 @@ cudaError_t launch_sk_fixup(const float* part, int units, int cg, int bt, const 
   const int R = n_items - n_dp;
   if (R == 0) return cudaSuccess;
   const int blocks = R * cg * 4 * (bt * 8 / kFixupThreads);
-  sk_fixup_kernel<<<blocks, kFixupThreads, 0, stream>>>(part, units, cg, bt, n_dp, R, p.n_chunks,
-                                                         p.n_kunits, p.n_ttiles, p.band, T, K, dX,
-                                                         ldx);
-  return counted(cudaGetLastError());
+  return counted(launch_after_prev(sk_fixup_kernel, dim3(blocks), dim3(kFixupThreads), stream, part,
+                                   units, cg, bt, n_dp, R, static_cast<int>(p.n_chunks),
+                                   static_cast<int>(p.n_kunits), static_cast<int>(p.n_ttiles),
+                                   static_cast<int>(p.band), T, K, dX, ldx));
 }
 
 int64_t tc_adapter_cols(int64_t N, int64_t r) {

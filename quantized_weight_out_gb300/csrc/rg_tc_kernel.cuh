@@ -657,6 +657,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
   const bool leader = rank == 0;
+  // the split reduction or stream-K's second pass may be scheduled as this
+  // kernel's CTAs leave the SMs (it waits for this kernel before reading)
+  pdl_launch_dependents();
   const int unit = blockIdx.x / CG, n_units = gridDim.x / CG;
   // work items: (tile, split); a split covers chunks [split * n_chunks, +n_chunks)
   // of the contraction (chunks past N are zero-filled by TMA and add nothing).
