@@ -51,6 +51,10 @@ Block formats (little-endian), ggml's GGUF block types:
                    Value 128h + 32j + 16s + l: q = bits 2j..2j+1 of
                    qs[32h + 16s + l], minus 4 unless bit 4h + j of
                    hmask[16s + l] is set;         y = (d*(sc - 32)) * q
+* MXFP4 17 B / 32: E8M0 scale byte e, qs[16] (nibbles as Q4_0), each an
+                   E2M1 code (sign bit 3, two exponent bits, one mantissa
+                   bit; the OCP microscaling formats);
+                                                  y = E2M1(nib) * 2^(e - 127)
 * F16 / BF16: 2 B per value.
 * F32: 4 B per value, the value itself.
 
@@ -65,11 +69,12 @@ import numpy as np
 
 F16, BF16, Q8_0, Q4_0, Q4_K = 1, 2, 3, 4, 5
 Q4_1, Q5_0, Q5_1, Q5_K, Q6_K = 6, 7, 8, 9, 10
-F32, Q2_K, Q3_K = 11, 12, 13
+F32, Q2_K, Q3_K, MXFP4 = 11, 12, 13, 14
 
 _BLOCK = {F16: (1, 2), BF16: (1, 2), Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144),
           Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q5_K: (256, 176),
-          Q6_K: (256, 210), F32: (1, 4), Q2_K: (256, 84), Q3_K: (256, 110)}
+          Q6_K: (256, 210), F32: (1, 4), Q2_K: (256, 84), Q3_K: (256, 110),
+          MXFP4: (32, 17)}
 
 
 def row_bytes(wtype: int, K: int) -> int:
@@ -106,6 +111,26 @@ def bf16_bits_to_f32(bits) -> np.ndarray:
     """bfloat16 -> float32: the 16 bits are the top half of the float32 word."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
     return b.view(np.float32)
+
+
+def e8m0_to_f32(e) -> np.ndarray:
+    """OCP MX E8M0 shared scale: 2^(e - 127) for e < 255 (e = 0 gives
+    2^-127, a float32 subnormal), NaN for e = 255."""
+    e = np.asarray(e).astype(np.int64)
+    v = np.ldexp(np.ones(e.shape), e - 127)
+    return np.where(e == 255, np.nan, v).astype(np.float32)
+
+
+def e2m1_to_f32(code) -> np.ndarray:
+    """OCP FP4 E2M1 element: bit 3 sign, bits 1-2 exponent (bias 1), bit 0
+    mantissa; exponent 0 -> (-1)^s * m / 2 (subnormal, signed zero kept),
+    else (-1)^s * 2^(e - 1) * (1 + m / 2)."""
+    c = np.asarray(code).astype(np.int64)
+    s = (c >> 3) & 1
+    e = (c >> 1) & 3
+    m = (c & 1).astype(np.float64)
+    mag = np.where(e == 0, m / 2.0, np.ldexp(1.0 + m / 2.0, e - 1))
+    return np.where(s == 1, -mag, mag).astype(np.float32)
 
 
 def _le16(lo: np.ndarray, hi: np.ndarray) -> np.ndarray:
@@ -343,6 +368,20 @@ def decode_q3_k(W, N: int, K: int) -> np.ndarray:
     return y.astype(np.float32).reshape(N, K)
 
 
+def decode_mxfp4(W, N: int, K: int) -> np.ndarray:
+    """MXFP4: value j (< 16) = low nibble of qs[j], value j+16 = high
+    nibble; y = E2M1(nib) * 2^(e - 127).  Exact in F32: a two-bit significand
+    times a power of two, the smallest magnitude 2^-128 a float32 subnormal
+    (the largest, 6 * 2^127, overflows to inf; e = 255 gives NaN)."""
+    blk = _rows(W, N, K, MXFP4).reshape(N, K // 32, 17)
+    sc = e8m0_to_f32(blk[..., 0]).astype(np.float64)
+    qs = blk[..., 1:17]
+    nib = np.concatenate([qs & 0x0F, qs >> 4], axis=-1)
+    with np.errstate(over="ignore", invalid="ignore"):
+        y = sc[..., None] * e2m1_to_f32(nib).astype(np.float64)
+        return y.astype(np.float32).reshape(N, K)
+
+
 def decode_f16(W, N: int, K: int) -> np.ndarray:
     b = _rows(W, N, K, F16).reshape(N, K, 2)
     return f16_bits_to_f32(_le16(b[..., 0], b[..., 1]))
@@ -361,7 +400,8 @@ def decode_bf16(W, N: int, K: int) -> np.ndarray:
 _DECODERS = {F16: decode_f16, BF16: decode_bf16, Q8_0: decode_q8_0,
              Q4_0: decode_q4_0, Q4_K: decode_q4_k, Q4_1: decode_q4_1,
              Q5_0: decode_q5_0, Q5_1: decode_q5_1, Q5_K: decode_q5_k,
-             Q6_K: decode_q6_k, F32: decode_f32, Q2_K: decode_q2_k, Q3_K: decode_q3_k}
+             Q6_K: decode_q6_k, F32: decode_f32, Q2_K: decode_q2_k, Q3_K: decode_q3_k,
+             MXFP4: decode_mxfp4}
 
 
 def dequant(wtype: int, W, N: int, K: int) -> np.ndarray:

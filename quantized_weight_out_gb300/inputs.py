@@ -55,17 +55,18 @@ import numpy as np
 # weight type codes (the C ABI uses the same integers)
 F16, BF16, Q8_0, Q4_0, Q4_K = 1, 2, 3, 4, 5
 Q4_1, Q5_0, Q5_1, Q5_K, Q6_K, F32 = 6, 7, 8, 9, 10, 11
-Q2_K, Q3_K = 12, 13
+Q2_K, Q3_K, MXFP4 = 12, 13, 14
 TYPE_NAMES = {F16: "f16", BF16: "bf16", Q8_0: "q8_0", Q4_0: "q4_0", Q4_K: "q4_k",
               Q4_1: "q4_1", Q5_0: "q5_0", Q5_1: "q5_1", Q5_K: "q5_k", Q6_K: "q6_k", F32: "f32",
-              Q2_K: "q2_k", Q3_K: "q3_k"}
+              Q2_K: "q2_k", Q3_K: "q3_k", MXFP4: "mxfp4"}
 NAME_TO_TYPE = {v: k for k, v in TYPE_NAMES.items()}
-ALL_TYPES = [Q8_0, Q4_0, Q4_K, F16, BF16, Q4_1, Q5_0, Q5_1, Q5_K, Q6_K, F32, Q2_K, Q3_K]
+ALL_TYPES = [Q8_0, Q4_0, Q4_K, F16, BF16, Q4_1, Q5_0, Q5_1, Q5_K, Q6_K, F32, Q2_K, Q3_K, MXFP4]
 
 # (values per block, bytes per block)
 BLOCK = {F16: (1, 2), BF16: (1, 2), Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144),
          Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q5_K: (256, 176),
-         Q6_K: (256, 210), F32: (1, 4), Q2_K: (256, 84), Q3_K: (256, 110)}
+         Q6_K: (256, 210), F32: (1, 4), Q2_K: (256, 84), Q3_K: (256, 110),
+         MXFP4: (32, 17)}
 
 
 def row_bytes(wtype: int, K: int) -> int:
@@ -384,6 +385,17 @@ def pack_q3_k(d_bits, sc6, q) -> np.ndarray:
     return out
 
 
+def pack_mxfp4(e, q) -> np.ndarray:
+    """MXFP4 blocks [nb, 17] from E8M0 scale bytes e [nb] and 4-bit E2M1
+    codes q [nb, 32] (value j < 16 in the low nibble of byte j, value j + 16
+    in its high nibble)."""
+    e = np.asarray(e, dtype=np.uint8)
+    out = np.zeros((e.shape[0], 17), dtype=np.uint8)
+    out[:, 0] = e
+    out[:, 1:17] = _pack_nibbles_32(q)
+    return out
+
+
 # ----------------------------------------------------------------------------
 # weights and activations for one call
 
@@ -430,6 +442,14 @@ def gen_weight(wtype: int, N: int, K: int, seed: int, stream: int) -> np.ndarray
         sc6 = uniform_int(seed, stream, nb * 16, 64, field=3).reshape(nb, 16)
         q = uniform_int(seed, stream, nb * 256, 8, field=5).reshape(nb, 256) - 4
         return pack_q3_k(f32_to_f16_bits(d), sc6, q).reshape(-1)
+    if wtype == MXFP4:
+        # fields drawn directly: a scale 2^(e - 127) with e in 118..121 and
+        # uniform codes give |y| <= 6 * 2^-6 ~ 0.09 (most near 0.01), every
+        # nonzero value a normal fp16 (the tensor-core operand)
+        nb = N * K // 32
+        e = 118 + uniform_int(seed, stream, nb, 4, field=1)
+        q = uniform_int(seed, stream, nb * 32, 16, field=5).reshape(nb, 32)
+        return pack_mxfp4(e, q).reshape(-1)
     if wtype in (Q4_1, Q5_0, Q5_1):
         # fields drawn directly (the pages give no workload of these types):
         # a block of N(0, 0.02) weights spans about 0.08, so d ~ 0.08 / levels

@@ -219,6 +219,51 @@ def test_q2_q3_k_hand_superblocks(golden_dir, name, build, decode):
         assert math.fsum(float(x) for x in y[lo:hi]) == v
 
 
+def _mxfp4_fixture(golden_dir):
+    rows = _read(golden_dir, "mxfp4_blocks.txt")
+    out = []
+    for i in range(0, len(rows), 2):
+        assert rows[i][0] == "hex" and rows[i + 1][0] == "values"
+        W = np.frombuffer(bytes.fromhex(rows[i][1]), dtype=np.uint8)
+        out.append((W, np.array([float(v) for v in rows[i + 1][1:]], dtype=np.float32)))
+    return out
+
+
+def _same_values(got, want):
+    """Bitwise equal, except that any NaN matches a NaN."""
+    nan = np.isnan(want)
+    return np.array_equal(np.isnan(got), nan) and _bits_equal(got[~nan], want[~nan])
+
+
+def test_mxfp4_hand_blocks(golden_dir):
+    """Scales 1, 4, 2^-7, 2^-127 (a float32 subnormal) and NaN; every E2M1
+    code in both nibble halves, signed zeros included."""
+    blocks = _mxfp4_fixture(golden_dir)
+    assert len(blocks) == 5
+    for W, want in blocks:
+        assert _same_values(oracle.decode_mxfp4(W, 1, 32)[0], want)
+    W = np.concatenate([w for w, _ in blocks])          # five blocks in one row
+    assert _same_values(oracle.decode_mxfp4(W, 1, 160)[0], np.concatenate([v for _, v in blocks]))
+
+
+def test_e2m1_codes_against_the_element_table():
+    """The OCP FP4 (E2M1) element table: codes 0..7 are 0, 0.5, 1, 1.5, 2,
+    3, 4, 6 and codes 8..15 their negatives (code 8 is -0.0)."""
+    table = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    want = np.array(table + [-v for v in table], dtype=np.float32)
+    assert _bits_equal(oracle.e2m1_to_f32(np.arange(16)), want)
+
+
+def test_e8m0_scales_against_ldexp():
+    """E8M0: 2^(e - 127), e = 0 the float32 subnormal 2^-127, e = 255 NaN;
+    checked against math.ldexp packed by struct."""
+    got = oracle.e8m0_to_f32(np.arange(256))
+    for e in range(255):
+        want = struct.unpack("<f", struct.pack("<f", math.ldexp(1.0, e - 127)))[0]
+        assert got[e] == want and got[e] > 0, e
+    assert np.isnan(got[255])
+
+
 def test_q3_k_scales_unpack_every_field():
     """Each 6-bit scale set alone to 63 (others 0) lights exactly its own
     output: the low nibble and the two high bits come from the bytes the
@@ -336,6 +381,9 @@ def _all_ones_weight(wtype, N, K, variant=0):
             S = bytes([0xFF]) * 8 + bytes([0x55]) * 4
             blk = bytes(32) + bytes([0xFF]) * 64 + S + bytes([0x00, 0x3C])
         return np.frombuffer(blk * (N * K // 256), dtype=np.uint8)
+    if wtype == inputs.MXFP4:    # scale 2^0, E2M1 code 2 (1.0) in both nibbles
+        blk = bytes([0x7F]) + bytes([0x22]) * 16
+        return np.frombuffer(blk * (N * K // 32), dtype=np.uint8)
     if wtype == inputs.F16:
         return np.frombuffer(bytes([0x00, 0x3C]) * (N * K), dtype=np.uint8)
     if wtype == inputs.F32:
@@ -349,7 +397,7 @@ CASES = [(inputs.Q8_0, 0), (inputs.Q4_0, 0), (inputs.Q4_K, 0), (inputs.Q4_K, 1),
          (inputs.F16, 0), (inputs.BF16, 0), (inputs.Q4_1, 0), (inputs.Q5_0, 0),
          (inputs.Q5_1, 0), (inputs.Q5_1, 1), (inputs.Q5_K, 0), (inputs.Q5_K, 1),
          (inputs.Q6_K, 0), (inputs.Q6_K, 1), (inputs.F32, 0), (inputs.Q2_K, 0),
-         (inputs.Q2_K, 1), (inputs.Q3_K, 0), (inputs.Q3_K, 1)]
+         (inputs.Q2_K, 1), (inputs.Q3_K, 0), (inputs.Q3_K, 1), (inputs.MXFP4, 0)]
 
 
 @pytest.mark.parametrize("wtype,variant", CASES)
@@ -520,6 +568,15 @@ def _py_decode(wtype, raw, N, K):
                     # F32 evaluation: exact product, one rounding in the difference
                     val = np.float32(np.float32(d * (sb & 15)) * q) - np.float32(dmin * (sb >> 4))
                     out[n][256 * b + v] = float(val)
+        elif wtype == inputs.MXFP4:
+            e2m1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+            for b in range(K // 32):
+                blk = row[17 * b: 17 * b + 17]
+                scale = 2.0 ** (blk[0] - 127) if blk[0] != 255 else float("nan")
+                for j in range(32):
+                    code = (blk[1 + j % 16] >> (4 * (j // 16))) & 15
+                    mag = e2m1[code & 7] * scale
+                    out[n][32 * b + j] = -mag if code & 8 else mag
         elif wtype == inputs.Q3_K:
             for b in range(K // 256):
                 blk = row[110 * b: 110 * b + 110]
@@ -543,7 +600,7 @@ BRUTE = [(inputs.Q8_0, 40, 64, 3), (inputs.Q4_0, 33, 96, 2), (inputs.Q4_K, 12, 5
          (inputs.F16, 24, 40, 3), (inputs.BF16, 24, 40, 3), (inputs.Q8_0, 7, 32, 1),
          (inputs.Q4_1, 21, 64, 2), (inputs.Q5_0, 19, 96, 2), (inputs.Q5_1, 17, 64, 2),
          (inputs.Q5_K, 10, 512, 2), (inputs.Q6_K, 9, 512, 2), (inputs.F32, 20, 48, 3),
-         (inputs.Q2_K, 11, 512, 2), (inputs.Q3_K, 10, 512, 2)]
+         (inputs.Q2_K, 11, 512, 2), (inputs.Q3_K, 10, 512, 2), (inputs.MXFP4, 13, 96, 2)]
 
 
 @pytest.mark.parametrize("wtype,N,K,T", BRUTE)
@@ -747,6 +804,43 @@ def test_q6_k_mutant_is_caught(golden_dir):
     W, kv, ats, subs = _q6_k_fixture(golden_dir)
     y = _mut_q6_k_pairs_by_parity(W, 1, 256)[0]
     assert any(y[i] != np.float32(v) for i, v in ats)
+
+
+def _mut_mxfp4_bias_128(W, N, K):
+    """The scale as 2^(e - 128)."""
+    blk = qop._rows(W, N, K, qop.MXFP4).reshape(N, K // 32, 17)
+    sc = np.ldexp(1.0, blk[..., 0].astype(np.int64) - 128)
+    nib = np.concatenate([blk[..., 1:17] & 0x0F, blk[..., 1:17] >> 4], axis=-1)
+    return (sc[..., None] * qop.e2m1_to_f32(nib)).astype(np.float32).reshape(N, K)
+
+
+def _mut_mxfp4_no_subnormal_elements(W, N, K):
+    """E2M1 exponent 0 read as a normal number (code 1 -> 0.75)."""
+    real = qop.e2m1_to_f32
+
+    def bad(code):
+        c = np.asarray(code).astype(np.int64)
+        e, m = (c >> 1) & 3, (c & 1).astype(np.float64)
+        mag = np.where((c & 7) == 0, 0.0, np.ldexp(1.0 + m / 2.0, e - 1))
+        return np.where((c >> 3) & 1 == 1, -mag, mag).astype(np.float32)
+    qop.e2m1_to_f32 = bad
+    try:
+        return qop.decode_mxfp4(W, N, K)
+    finally:
+        qop.e2m1_to_f32 = real
+
+
+def _mut_mxfp4_swapped_nibbles(W, N, K):
+    blk = qop._rows(W, N, K, qop.MXFP4).reshape(N, K // 32, 17)
+    sc = qop.e8m0_to_f32(blk[..., 0]).astype(np.float64)
+    nib = np.concatenate([blk[..., 1:17] >> 4, blk[..., 1:17] & 0x0F], axis=-1)
+    return (sc[..., None] * qop.e2m1_to_f32(nib)).astype(np.float32).reshape(N, K)
+
+
+def test_mxfp4_mutants_are_caught(golden_dir):
+    W, want = _mxfp4_fixture(golden_dir)[0]
+    for mut in (_mut_mxfp4_bias_128, _mut_mxfp4_no_subnormal_elements, _mut_mxfp4_swapped_nibbles):
+        assert not _same_values(mut(W, 1, 32)[0], want), mut.__name__
 
 
 def test_new_type_mutants_are_caught(golden_dir):
