@@ -79,10 +79,17 @@ typedef enum {
                      qs[64], fp16 d, fp16 dmin.  Value 128h+32j+16s+l: bits 2j..2j+1
                      of qs[32h+16s+l], scales byte 8h+2j+s; value d*sc*q - dmin*m.
                      Rows 16-byte aligned only when K % 1024 == 0 (as Q6_K)     */
-    RG_Q3_K = 13  /* 110 B / 256 values: hmask[32], qs[64], 12 B of sixteen 6-bit
+    RG_Q3_K = 13, /* 110 B / 256 values: hmask[32], qs[64], 12 B of sixteen 6-bit
                      scales, fp16 d.  Value 128h+32j+16s+l: low bits as Q2_K, minus
                      4 unless bit 4h+j of hmask[16s+l] is set; value d*(sc-32)*q.
                      Rows 16-byte aligned only when K % 2048 == 0 (as Q6_K)     */
+    RG_MXFP4 = 14 /* 17 B / 32 values: E8M0 scale byte e, 16 B nibbles as Q4_0, each
+                     an E2M1 code (OCP microscaling: bit 3 sign, 2 exponent bits,
+                     1 mantissa bit: 0, 0.5, 1, 1.5, 2, 3, 4, 6); value
+                     E2M1(q) * 2^(e-127) (e = 255: NaN).  Rows 16-byte aligned
+                     only when K % 512 == 0, which the tensor-core and small-T
+                     variants need.  The tensor-core variants round the values
+                     to fp16: block scales outside 2^-24..2^15 lose them       */
 } rg_wtype;
 
 typedef enum {
@@ -90,8 +97,8 @@ typedef enum {
     RG_ERR_ARG = -1,     /* NULL pointer where data is needed, negative or too large size */
     RG_ERR_TYPE = -2,    /* unknown wtype, or unknown variant                              */
     RG_ERR_SHAPE = -3,   /* K not a multiple of 256 (quantized) or 8 (F32/F16/BF16); Q6_K or
-                            Q3_K with K % 2048 != 0, Q2_K with K % 1024 != 0, on a
-                            tensor-core or small-T variant                                   */
+                            Q3_K with K % 2048 != 0, Q2_K with K % 1024 != 0, MXFP4 with
+                            K % 512 != 0, on a tensor-core or small-T variant                */
     RG_ERR_ALIGN = -4,   /* W, dY, dX or out not 16-byte aligned                           */
     RG_ERR_CUDA = -5,    /* a CUDA runtime/driver call or a launch failed                  */
     RG_ERR_TIMEOUT = -6  /* a bounded device-side wait gave up (reported by rg_check)      */

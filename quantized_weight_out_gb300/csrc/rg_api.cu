@@ -129,10 +129,12 @@ int validate(int wtype, const void* W, int64_t N, int64_t K, const float* dY, in
 
 // Q6_K and Q3_K rows (210 and 110 bytes per 256 values) are 16-byte aligned,
 // as the tensor-core and small-T kernels' copies need, only when K is a
-// multiple of 2048; Q2_K rows (84 bytes per 256) when K is a multiple of 1024.
+// multiple of 2048; Q2_K rows (84 bytes per 256) when K is a multiple of 1024;
+// MXFP4 rows (17 bytes per 32) when K is a multiple of 512.
 bool aligned_rows(int wtype, int64_t K) {
   if (wtype == RG_Q6_K || wtype == RG_Q3_K) return K % 2048 == 0;
   if (wtype == RG_Q2_K) return K % 1024 == 0;
+  if (wtype == RG_MXFP4) return K % 512 == 0;
   return true;
 }
 

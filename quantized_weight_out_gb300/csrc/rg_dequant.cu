@@ -73,9 +73,10 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
   }
 }
 
-// Q6_K rows (210 bytes per 256 values) are not 16-byte aligned in general,
-// and an F32 segment is wider than a warp's one 16-byte load per lane: one
-// thread per 8 values, reading its bytes directly.
+// Q6_K, Q3_K, Q2_K and MXFP4 rows (210, 110, 84 and 136 bytes per 256
+// values) are not 16-byte aligned in general, and an F32 segment is wider
+// than a warp's one 16-byte load per lane: one thread per 8 values, reading
+// its bytes directly.
 template <int WT>
 __global__ void __launch_bounds__(256) dequant_bytes_kernel(const uint8_t* __restrict__ W, int64_t N,
                                                             int64_t K, int64_t rb,
@@ -158,7 +159,7 @@ cudaError_t launch_dequant(int wtype, const void* W, int64_t N, int64_t K, float
   const uint8_t* w = static_cast<const uint8_t*>(W);
   return with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
     constexpr int WT = decltype(wt)::value;
-    if constexpr (WT == RG_Q6_K || WT == RG_F32 || WT == RG_Q2_K || WT == RG_Q3_K)
+    if constexpr (WT == RG_Q6_K || WT == RG_F32 || WT == RG_Q2_K || WT == RG_Q3_K || WT == RG_MXFP4)
       dequant_bytes_kernel<WT><<<grid_for(N * (K >> 3), 256, dev), 256, 0, stream>>>(w, N, K, rb, out);
     else
       dequant_kernel<WT><<<grid, 256, 0, stream>>>(w, N, K, rb, out);

@@ -19,7 +19,7 @@ namespace rg {
 // ---------------------------------------------------------------------------
 // storage formats: values per block, bytes per block
 
-__host__ __device__ constexpr bool valid_wtype(int wt) { return wt >= RG_F16 && wt <= RG_Q3_K; }
+__host__ __device__ constexpr bool valid_wtype(int wt) { return wt >= RG_F16 && wt <= RG_MXFP4; }
 __host__ __device__ constexpr bool is_quant(int wt) {
   return valid_wtype(wt) && wt != RG_F16 && wt != RG_BF16 && wt != RG_F32;
 }
@@ -39,6 +39,7 @@ __host__ __device__ constexpr int block_bytes(int wt) {
          : wt == RG_Q4_1 ? 20
          : wt == RG_Q5_0 ? 22
          : wt == RG_Q5_1 ? 24
+         : wt == RG_MXFP4 ? 17
          : wt == RG_F32  ? 4
                          : 2;
 }
@@ -382,9 +383,33 @@ __device__ __forceinline__ void q4k_scale_min(const uint8_t* S, int j, int& sc, 
   }
 }
 
+// OCP microscaling fields (MXFP4).  E8M0 scale: 2^(e - 127), the float32
+// with biased exponent e; e = 0 is the subnormal 2^-127, e = 255 NaN.
+__device__ __forceinline__ float e8m0_f32(uint32_t e) {
+  return e == 0 ? __uint_as_float(0x00400000u)
+                : (e == 255 ? __uint_as_float(0x7FC00000u) : __uint_as_float(e << 23));
+}
+// E2M1 element (4-bit code): bit 3 sign, bits 2-1 exponent (bias 1), bit 0
+// mantissa: 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives (code 8: -0.0).
+__device__ __forceinline__ float e2m1_f32(uint32_t c) {
+  const uint32_t m = c & 7u;
+  const uint32_t mag = m >= 2u ? (((m >> 1) + 126u) << 23) | ((m & 1u) << 22) : (m ? 0x3F000000u : 0u);
+  return __uint_as_float(mag | ((c & 8u) << 28));
+}
+
 template <int WT>
 __device__ __forceinline__ void decode8_f32(const uint8_t* row, int k0, float (&out)[8]) {
-  if constexpr (WT == RG_F32) {
+  if constexpr (WT == RG_MXFP4) {
+    // E2M1(code) * 2^(e - 127): an exact product (a power of two times a
+    // two-bit significand; subnormal and overflowing results as IEEE gives)
+    const uint8_t* blk = row + (k0 >> 5) * 17;
+    const float sc = e8m0_f32(blk[0]);
+    const int j = k0 & 31;  // 0, 8, 16 or 24
+    const uint8_t* qs = blk + 1 + (j & 15);
+    const int shift = j >= 16 ? 4 : 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) out[i] = e2m1_f32((qs[i] >> shift) & 15u) * sc;
+  } else if constexpr (WT == RG_F32) {
     const float4 a = *reinterpret_cast<const float4*>(row + 4 * k0);
     const float4 b = *reinterpret_cast<const float4*>(row + 4 * k0 + 16);
     out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;

@@ -51,6 +51,7 @@ R with_wtype(int wtype, R fallback, F&& f) {
     case RG_Q6_K: return f(std::integral_constant<int, RG_Q6_K>{});
     case RG_Q2_K: return f(std::integral_constant<int, RG_Q2_K>{});
     case RG_Q3_K: return f(std::integral_constant<int, RG_Q3_K>{});
+    case RG_MXFP4: return f(std::integral_constant<int, RG_MXFP4>{});
     case RG_F32: return f(std::integral_constant<int, RG_F32>{});
     default: return fallback;
   }

@@ -31,8 +31,8 @@ struct Raw {
   uint32_t v[WT == RG_Q5_K || WT == RG_F32 ? 8
              : WT == RG_Q4_K                  ? 6
              : WT == RG_Q6_K || WT == RG_Q3_K ? 5
-             : (WT == RG_Q8_0 || WT == RG_Q4_0 || WT == RG_Q4_1) ? 3
-                                                                  : 4];
+             : (WT == RG_Q8_0 || WT == RG_Q4_0 || WT == RG_Q4_1 || WT == RG_MXFP4) ? 3
+                                                                                    : 4];
 };
 
 // The bytes one lane needs for its 8 values, from a row tile staged in
@@ -55,6 +55,16 @@ __device__ __forceinline__ void load_raw_smem(const uint8_t* tile, int lane, Raw
     r.v[0] = *reinterpret_cast<const uint16_t*>(blk);
     r.v[1] = static_cast<uint32_t>(q16[0]) | (static_cast<uint32_t>(q16[1]) << 16);
     r.v[2] = static_cast<uint32_t>(q16[2]) | (static_cast<uint32_t>(q16[3]) << 16);
+  } else if constexpr (WT == RG_MXFP4) {
+    // values 8(lane & 3) .. +7 of block lane >> 2 (17-byte blocks from an
+    // 8-byte aligned tile): the scale byte and 8 bytes of nibbles
+    const uint8_t* blk = tile + 17 * (lane >> 2);
+    const uint8_t* q = blk + 1 + 8 * (lane & 1);
+    r.v[0] = blk[0];
+    r.v[1] = static_cast<uint32_t>(q[0]) | (static_cast<uint32_t>(q[1]) << 8) |
+             (static_cast<uint32_t>(q[2]) << 16) | (static_cast<uint32_t>(q[3]) << 24);
+    r.v[2] = static_cast<uint32_t>(q[4]) | (static_cast<uint32_t>(q[5]) << 8) |
+             (static_cast<uint32_t>(q[6]) << 16) | (static_cast<uint32_t>(q[7]) << 24);
   } else if constexpr (WT == RG_Q4_1) {
     const uint8_t* blk = tile + 20 * (lane >> 2);
     const uint32_t* q = reinterpret_cast<const uint32_t*>(blk + 4 + 8 * (lane & 1));
@@ -167,6 +177,17 @@ __device__ __forceinline__ void decode_raw(const Raw<WT>& r, int lane, float (&w
       w[4 * j + 2] = d * byte_minus<2>(x, kTwo23 + 8.0f);
       w[4 * j + 3] = d * byte_minus<3>(x, kTwo23 + 8.0f);
     }
+  } else if constexpr (WT == RG_MXFP4) {
+    // E2M1(code) * 2^(e - 127): exact (low nibbles for the first 16 values
+    // of the block, high nibbles for the rest)
+    const float sc = e8m0_f32(r.v[0]);
+    const int shift = (lane & 2) ? 4 : 0;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint32_t x = r.v[1 + j] >> shift;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) w[4 * j + b] = e2m1_f32((x >> (8 * b)) & 15u) * sc;
+    }
   } else if constexpr (WT == RG_Q6_K) {
     // (d * sc) * (q - 32), every step exact
     const int i = (lane >> 2) & 3;
@@ -268,25 +289,27 @@ __device__ __forceinline__ void decode_raw(const Raw<WT>& r, int lane, float (&w
 template <int WT>
 __host__ __device__ constexpr int tile_bytes();
 
-// Super-blocks that are not a multiple of 16 bytes (Q6_K 210, Q3_K 110, Q2_K
-// 84) start at an even offset of a 16-byte grain: a stage row holds a window
-// from the grain before (window_offset bytes in), 16-byte multiple wide.
+// Tiles that are not a multiple of 16 bytes (the super-blocks of Q6_K 210,
+// Q3_K 110, Q2_K 84; eight MXFP4 blocks, 136) start at an even offset of a
+// 16-byte grain: a stage row holds a window from the grain before
+// (window_offset bytes in), 16-byte multiple wide.
 template <int WT>
 __host__ __device__ constexpr bool windowed() {
-  return WT == RG_Q6_K || WT == RG_Q3_K || WT == RG_Q2_K;
+  return WT == RG_Q6_K || WT == RG_Q3_K || WT == RG_Q2_K || WT == RG_MXFP4;
 }
 // Bytes a stage holds per row: the 256-value tile, or its window.
 template <int WT>
 __host__ __device__ constexpr int stage_row_bytes() {
-  return WT == RG_Q6_K ? 224 : WT == RG_Q3_K ? 128 : WT == RG_Q2_K ? 96 : tile_bytes<WT>();
+  return WT == RG_Q6_K ? 224 : WT == RG_Q3_K ? 128 : WT == RG_Q2_K ? 96 : WT == RG_MXFP4 ? 144
+                                                                                            : tile_bytes<WT>();
 }
 template <int WT>
 __host__ __device__ constexpr int64_t window_start(int64_t kt) {
-  return windowed<WT>() ? ((kt * block_bytes(WT)) & ~int64_t{15}) : kt * tile_bytes<WT>();
+  return windowed<WT>() ? ((kt * tile_bytes<WT>()) & ~int64_t{15}) : kt * tile_bytes<WT>();
 }
 template <int WT>
 __host__ __device__ constexpr int window_offset(int64_t kt) {
-  return windowed<WT>() ? static_cast<int>((kt * block_bytes(WT)) & 15) : 0;
+  return windowed<WT>() ? static_cast<int>((kt * tile_bytes<WT>()) & 15) : 0;
 }
 
 template <int WT>

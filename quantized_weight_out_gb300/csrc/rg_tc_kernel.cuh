@@ -65,7 +65,8 @@ constexpr int SMEM_BUDGET = 224 * 1024;
 // and Q5_K the whole super-block (its header holds every sub-block's scale),
 // Q6_K the whole 210-byte super-block inside a 240-byte window that starts at
 // the 16-byte grain before it (0..14 bytes in; 15 chunks keep eight rows in
-// distinct bank groups).
+// distinct bank groups), MXFP4 four 17-byte blocks (68 B, 0, 4, 8 or 12
+// bytes into the grain) inside 112 B (7 chunks: distinct bank groups).
 template <int WT>
 __host__ __device__ constexpr int p_row_bytes() {
   return WT == RG_Q8_0   ? 144
@@ -78,6 +79,7 @@ __host__ __device__ constexpr int p_row_bytes() {
          : WT == RG_Q6_K ? 240
          : WT == RG_Q3_K ? 128
          : WT == RG_Q2_K ? 96
+         : WT == RG_MXFP4 ? 112
                          : 0;
 }
 
@@ -218,6 +220,51 @@ __device__ __forceinline__ void dec_q4_0_block(const uint8_t* row, uint8_t* A, i
     const uint32_t w = r.word_at(X + 2 + 4 * j);
     four_scaled(w & 0x0F0F0F0Fu, off, d2, lo[2 * j], lo[2 * j + 1]);
     four_scaled((w >> 4) & 0x0F0F0F0Fu, off, d2, hi[2 * j], hi[2 * j + 1]);
+  }
+  st_a_chunk(A, n, 4 * b, lo[0], lo[1], lo[2], lo[3]);
+  st_a_chunk(A, n, 4 * b + 1, lo[4], lo[5], lo[6], lo[7]);
+  st_a_chunk(A, n, 4 * b + 2, hi[0], hi[1], hi[2], hi[3]);
+  st_a_chunk(A, n, 4 * b + 3, hi[4], hi[5], hi[6], hi[7]);
+}
+
+// Four E2M1 codes in the low nibbles of the bytes of x (high nibbles zero)
+// -> two half2 (the codes of bytes 0, 1 and 2, 3), exact: a byte lookup
+// gives each magnitude's fp16 high byte (every low byte is zero), the code's
+// sign bit becomes that byte's top bit.
+__device__ __forceinline__ void e2m1x4_f16(uint32_t x, uint32_t& o01, uint32_t& o23) {
+  const uint32_t t = x & 0x07070707u;
+  const uint32_t u = t | (t >> 4);
+  const uint32_t sel = (u & 0xFFu) | ((u >> 8) & 0xFF00u);  // nibble k: magnitude of byte k
+  // fp16 high bytes of 0, 0.5, 1, 1.5 | 2, 3, 4, 6
+  const uint32_t hb = __byte_perm(0x3E3C3800u, 0x46444240u, sel) | ((x & 0x08080808u) << 4);
+  o01 = __byte_perm(hb, 0u, 0x1404);
+  o23 = __byte_perm(hb, 0u, 0x3424);
+}
+
+// MXFP4 block at byte S of a row window: E8M0 scale byte, 16 bytes of
+// nibbles (low = value j, high = value j + 16).  Writes its 32 values,
+// E2M1(q) * 2^(e - 127) rounded once to fp16, as chunks 4b .. 4b+3 of row n.
+template <int S>
+__device__ __forceinline__ void dec_mxfp4_block(const uint8_t* row, uint8_t* A, int n, int b) {
+  constexpr int C0 = S / 16;
+  constexpr int X = S - 16 * C0;
+  // the last word read: the one holding byte X + 16 and, unaligned, the next
+  constexpr int C1 = C0 + ((X + 1) % 4 == 0 ? X + 16 : X + 20) / 16;
+  static_assert(16 * C1 + 16 <= p_row_bytes<RG_MXFP4>(), "reads stay inside the row window");
+  const auto r = load_chunks<C0, C1>(row);
+  const uint32_t e = r.word_at(X & ~3) >> (8 * (X & 3)) & 0xFFu;
+  const __half2 sc = __float2half2_rn(e8m0_f32(e));
+  uint32_t lo[8], hi[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w = r.word_at(X + 1 + 4 * j);
+    uint32_t a0, a1, b0, b1;
+    e2m1x4_f16(w & 0x0F0F0F0Fu, a0, a1);
+    e2m1x4_f16((w >> 4) & 0x0F0F0F0Fu, b0, b1);
+    lo[2 * j] = h2_as_u32(__hmul2(u32_as_h2(a0), sc));
+    lo[2 * j + 1] = h2_as_u32(__hmul2(u32_as_h2(a1), sc));
+    hi[2 * j] = h2_as_u32(__hmul2(u32_as_h2(b0), sc));
+    hi[2 * j + 1] = h2_as_u32(__hmul2(u32_as_h2(b1), sc));
   }
   st_a_chunk(A, n, 4 * b, lo[0], lo[1], lo[2], lo[3]);
   st_a_chunk(A, n, 4 * b + 1, lo[4], lo[5], lo[6], lo[7]);
@@ -497,9 +544,10 @@ __device__ __forceinline__ void dec_q3_k_row(const uint8_t* row, uint8_t* A, int
 
 // Block b (32-value types) or part b (Q4_K, Q5_K: chunk b >> 1 of the
 // half, 16 bytes b & 1) of row n of a stage.
-template <int WT, int ODD, int B>
+template <int WT, int ODD, int B, int O = 0>
 __device__ __forceinline__ void dec_item(const uint8_t* row, uint8_t* A, int n) {
-  if constexpr (WT == RG_Q8_0) dec_q8_block<8 * ODD + 34 * B>(row, A, n, B);
+  if constexpr (WT == RG_MXFP4) dec_mxfp4_block<O + 17 * B>(row, A, n, B);
+  else if constexpr (WT == RG_Q8_0) dec_q8_block<8 * ODD + 34 * B>(row, A, n, B);
   else if constexpr (WT == RG_Q4_0) dec_q4_0_block<8 * ODD + 18 * B>(row, A, n, B);
   else if constexpr (WT == RG_Q4_1) dec_q41_q5_block<WT, 20 * B>(row, A, n, B);
   else if constexpr (WT == RG_Q5_0) dec_q41_q5_block<WT, 8 * ODD + 22 * B>(row, A, n, B);
@@ -532,10 +580,10 @@ __device__ __forceinline__ void decode_stage_warp(const uint8_t* __restrict__ P,
     const int n = lane + 32 * (i & 1);
     const uint8_t* row = P + n * PR;
     switch (i >> 1) {
-      case 0: dec_item<WT, ODD, 0>(row, A, n); break;
-      case 1: dec_item<WT, ODD, 1>(row, A, n); break;
-      case 2: dec_item<WT, ODD, 2>(row, A, n); break;
-      default: dec_item<WT, ODD, 3>(row, A, n); break;
+      case 0: dec_item<WT, ODD, 0, O>(row, A, n); break;
+      case 1: dec_item<WT, ODD, 1, O>(row, A, n); break;
+      case 2: dec_item<WT, ODD, 2, O>(row, A, n); break;
+      default: dec_item<WT, ODD, 3, O>(row, A, n); break;
     }
   }
 }
@@ -552,6 +600,7 @@ __device__ __forceinline__ int p_window_start(int kt) {
   if constexpr (WT == RG_Q6_K) return ((kt >> 1) * 210) & ~15;
   if constexpr (WT == RG_Q3_K) return ((kt >> 1) * 110) & ~15;
   if constexpr (WT == RG_Q2_K) return ((kt >> 1) * 84) & ~15;
+  if constexpr (WT == RG_MXFP4) return (kt * 68) & ~15;
   return (kt >> 1) * 144;  // Q4_K: the whole super-block
 }
 
@@ -954,7 +1003,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 default: break;
               }
 #undef RG_WIN_CASE
-            } else if (kt & 1) {
+            } else if constexpr (WT == RG_MXFP4) {
+              // the tile's four blocks start o = 0, 4, 8 or 12 bytes into the window
+              const uint8_t* P = sP + s * C::P_STAGE;
+              uint8_t* Ad = sA + s * A_STAGE;
+              switch ((kt * 68) & 12) {
+                case 0: decode_stage_warp<WT, 0, WPS, 0>(P, Ad, lane, part); break;
+                case 4: decode_stage_warp<WT, 0, WPS, 4>(P, Ad, lane, part); break;
+                case 8: decode_stage_warp<WT, 0, WPS, 8>(P, Ad, lane, part); break;
+                default: decode_stage_warp<WT, 0, WPS, 12>(P, Ad, lane, part); break;
+              }
+          } else if (kt & 1) {
               decode_stage_warp<WT, 1, WPS>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part);
             } else {
               decode_stage_warp<WT, 0, WPS>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part);

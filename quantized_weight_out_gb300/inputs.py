@@ -548,5 +548,6 @@ WORKLOADS = {
     # the other quantized types on the sweep's q/o shape, one call each
     "types_4096x4096_t8192": [Problem(f"{TYPE_NAMES[wt]}_4096x4096_t8192", wt, 4096, 4096, 8192,
                                       1e-3, 0.0, 16 * i)
-                              for i, wt in enumerate([Q4_1, Q5_0, Q5_1, Q5_K, Q6_K, F32, Q2_K, Q3_K])],
+                              for i, wt in enumerate([Q4_1, Q5_0, Q5_1, Q5_K, Q6_K, F32, Q2_K, Q3_K,
+                                                      MXFP4])],
 }

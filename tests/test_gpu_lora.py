@@ -61,7 +61,7 @@ def _check(got, ref, bnd_base, bnd_lora, variant, what=""):
 
 
 def _kfit(wtype, K, variant):
-    a = {inputs.Q6_K: 2048, inputs.Q3_K: 2048, inputs.Q2_K: 1024}.get(wtype)
+    a = {inputs.Q6_K: 2048, inputs.Q3_K: 2048, inputs.Q2_K: 1024, inputs.MXFP4: 512}.get(wtype)
     if a and variant != 3:
         return (K + a - 1) // a * a
     return K
@@ -69,7 +69,7 @@ def _kfit(wtype, K, variant):
 
 @pytest.mark.parametrize("variant", [1, 2, 3, 4, 5])
 @pytest.mark.parametrize("wtype", [inputs.Q4_K, inputs.Q8_0, inputs.Q5_0, inputs.Q6_K, inputs.F16,
-                                   inputs.BF16, inputs.F32, inputs.Q2_K, inputs.Q3_K])
+                                   inputs.BF16, inputs.F32, inputs.Q2_K, inputs.Q3_K, inputs.MXFP4])
 @pytest.mark.parametrize("shape", [(200, 512, 300, 16), (64, 256, 1, 7), (1000, 768, 130, 100),
                                    (72, 1024, 33, 1), (201, 512, 77, 32), (130, 256, 40, 33),
                                    (96, 512, 50, 9)])

@@ -33,13 +33,13 @@ def _dev():
     return torch.device("cuda:0")
 
 
-ROW_ALIGN_K = {inputs.Q6_K: 2048, inputs.Q3_K: 2048, inputs.Q2_K: 1024}
+ROW_ALIGN_K = {inputs.Q6_K: 2048, inputs.Q3_K: 2048, inputs.Q2_K: 1024, inputs.MXFP4: 512}
 
 
 def kfit(wtype, K, variant):
     """Q6_K and Q3_K rows are 16-byte aligned only for K % 2048 == 0, Q2_K
-    rows for K % 1024 == 0, which every variant but the SIMT one needs: round
-    K up for those."""
+    rows for K % 1024 == 0 and MXFP4 rows for K % 512 == 0, which every
+    variant but the SIMT one needs: round K up for those."""
     a = ROW_ALIGN_K.get(wtype)
     if a and variant != 3:
         return -(-K // a) * a
@@ -259,9 +259,9 @@ def test_split_contraction(rg, variant, wtype, beta):
     assert_within(got, ref, bnd + extra, 5e-3, f"split variant {variant} type {wtype}")
 
 
-@pytest.mark.parametrize("wtype", [inputs.Q6_K, inputs.Q3_K, inputs.Q2_K])
+@pytest.mark.parametrize("wtype", [inputs.Q6_K, inputs.Q3_K, inputs.Q2_K, inputs.MXFP4])
 def test_unaligned_super_block_rows(rg, wtype):
-    """K % 2048 (Q2_K: 1024) != 0: the tensor-core and small-T variants
+    """K % 2048 (Q2_K: 1024, MXFP4: 512) != 0: the tensor-core and small-T variants
     refuse the shape (nothing launched), and the dispatcher runs the SIMT
     variant instead."""
     N, K, T = 70, 768, 40                 # Q6_K rows of 630 bytes: only 2-byte aligned
