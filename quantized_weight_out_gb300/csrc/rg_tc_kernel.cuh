@@ -241,35 +241,46 @@ __device__ __forceinline__ void e2m1x4_f16(uint32_t x, uint32_t& o01, uint32_t& 
   o23 = __byte_perm(hb, 0u, 0x3424);
 }
 
-// MXFP4 block at byte S of a row window: E8M0 scale byte, 16 bytes of
-// nibbles (low = value j, high = value j + 16).  Writes its 32 values,
-// E2M1(q) * 2^(e - 127) rounded once to fp16, as chunks 4b .. 4b+3 of row n.
-template <int S>
-__device__ __forceinline__ void dec_mxfp4_block(const uint8_t* row, uint8_t* A, int n, int b) {
-  constexpr int C0 = S / 16;
-  constexpr int X = S - 16 * C0;
-  // the last word read: the one holding byte X + 16 and, unaligned, the next
-  constexpr int C1 = C0 + ((X + 1) % 4 == 0 ? X + 16 : X + 20) / 16;
-  static_assert(16 * C1 + 16 <= p_row_bytes<RG_MXFP4>(), "reads stay inside the row window");
-  const auto r = load_chunks<C0, C1>(row);
-  const uint32_t e = r.word_at(X & ~3) >> (8 * (X & 3)) & 0xFFu;
+// MXFP4 block B of a 128-value tile whose blocks start o = 0, 4, 8 or 12
+// bytes into the row window (a run-time value: one code path for every
+// offset, so the decoders' instructions stay few).  Block B begins at byte
+// o + 17B: its 16-byte chunk and the next are loaded, the five words from
+// the block's own word on are selected by (o + 17B) mod 16 / 4 (the shift
+// inside a word, B mod 4, is fixed).  Writes its 32 values,
+// E2M1(q) * 2^(e - 127) rounded once to fp16, as chunks 4B .. 4B+3 of row n.
+template <int B>
+__device__ __forceinline__ void dec_mxfp4_block(const uint8_t* row, uint8_t* A, int n, int o) {
+  constexpr int SH = B & 3;  // (o + 17B) mod 4
+  const int S = o + 17 * B;
+  const uint4 c0 = *reinterpret_cast<const uint4*>(row + (S & ~15));
+  const uint4 c1 = *reinterpret_cast<const uint4*>(row + (S & ~15) + 16);
+  const uint32_t q[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const int j0 = (S & 15) >> 2;  // 0..3: the block's first word in q
+  uint32_t w[5];
+#pragma unroll
+  for (int k = 0; k < 5; ++k)
+    w[k] = j0 == 0 ? q[k] : j0 == 1 ? q[k + 1] : j0 == 2 ? q[k + 2] : q[k + 3];
+  const uint32_t e = (w[0] >> (8 * SH)) & 0xFFu;
   const __half2 sc = __float2half2_rn(e8m0_f32(e));
   uint32_t lo[8], hi[8];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const uint32_t w = r.word_at(X + 1 + 4 * j);
+    // qs word j: bytes SH + 1 + 4j .. + 3 of w
+    constexpr int X = SH + 1;
+    const uint32_t v = (X & 3) == 0 ? w[(X >> 2) + j]
+                                    : __funnelshift_r(w[(X >> 2) + j], w[(X >> 2) + j + 1], 8 * (X & 3));
     uint32_t a0, a1, b0, b1;
-    e2m1x4_f16(w & 0x0F0F0F0Fu, a0, a1);
-    e2m1x4_f16((w >> 4) & 0x0F0F0F0Fu, b0, b1);
+    e2m1x4_f16(v & 0x0F0F0F0Fu, a0, a1);
+    e2m1x4_f16((v >> 4) & 0x0F0F0F0Fu, b0, b1);
     lo[2 * j] = h2_as_u32(__hmul2(u32_as_h2(a0), sc));
     lo[2 * j + 1] = h2_as_u32(__hmul2(u32_as_h2(a1), sc));
     hi[2 * j] = h2_as_u32(__hmul2(u32_as_h2(b0), sc));
     hi[2 * j + 1] = h2_as_u32(__hmul2(u32_as_h2(b1), sc));
   }
-  st_a_chunk(A, n, 4 * b, lo[0], lo[1], lo[2], lo[3]);
-  st_a_chunk(A, n, 4 * b + 1, lo[4], lo[5], lo[6], lo[7]);
-  st_a_chunk(A, n, 4 * b + 2, hi[0], hi[1], hi[2], hi[3]);
-  st_a_chunk(A, n, 4 * b + 3, hi[4], hi[5], hi[6], hi[7]);
+  st_a_chunk(A, n, 4 * B, lo[0], lo[1], lo[2], lo[3]);
+  st_a_chunk(A, n, 4 * B + 1, lo[4], lo[5], lo[6], lo[7]);
+  st_a_chunk(A, n, 4 * B + 2, hi[0], hi[1], hi[2], hi[3]);
+  st_a_chunk(A, n, 4 * B + 3, hi[4], hi[5], hi[6], hi[7]);
 }
 
 __device__ __forceinline__ uint32_t byte_of(uint32_t h1, uint32_t h2, uint32_t h3, int i) {
@@ -544,9 +555,9 @@ __device__ __forceinline__ void dec_q3_k_row(const uint8_t* row, uint8_t* A, int
 
 // Block b (32-value types) or part b (Q4_K, Q5_K: chunk b >> 1 of the
 // half, 16 bytes b & 1) of row n of a stage.
-template <int WT, int ODD, int B, int O = 0>
-__device__ __forceinline__ void dec_item(const uint8_t* row, uint8_t* A, int n) {
-  if constexpr (WT == RG_MXFP4) dec_mxfp4_block<O + 17 * B>(row, A, n, B);
+template <int WT, int ODD, int B>
+__device__ __forceinline__ void dec_item(const uint8_t* row, uint8_t* A, int n, int o) {
+  if constexpr (WT == RG_MXFP4) dec_mxfp4_block<B>(row, A, n, o);
   else if constexpr (WT == RG_Q8_0) dec_q8_block<8 * ODD + 34 * B>(row, A, n, B);
   else if constexpr (WT == RG_Q4_0) dec_q4_0_block<8 * ODD + 18 * B>(row, A, n, B);
   else if constexpr (WT == RG_Q4_1) dec_q41_q5_block<WT, 20 * B>(row, A, n, B);
@@ -562,9 +573,12 @@ __device__ __forceinline__ void dec_item(const uint8_t* row, uint8_t* A, int n) 
 // eight independent blocks per lane, and the lanes of a load or store sit on
 // consecutive rows, i.e. in distinct bank groups.  ODD = the tile's k index is
 // odd (window offset 8 for Q8_0 / Q4_0, second half of a Q4_K super-block).
+// o: MXFP4's run-time window offset (0, 4, 8 or 12); O: the super-block
+// offset of the row-half decoders.
 template <int WT, int ODD, int NPART, int O = 0>
 __device__ __forceinline__ void decode_stage_warp(const uint8_t* __restrict__ P,
-                                                  uint8_t* __restrict__ A, int lane, int part) {
+                                                  uint8_t* __restrict__ A, int lane, int part,
+                                                  int o = 0) {
   constexpr int PR = p_row_bytes<WT>();
   if constexpr (WT == RG_Q6_K || WT == RG_Q3_K || WT == RG_Q2_K) {
     static_assert(NPART == 2, "a lane decodes one row's half");
@@ -580,10 +594,10 @@ __device__ __forceinline__ void decode_stage_warp(const uint8_t* __restrict__ P,
     const int n = lane + 32 * (i & 1);
     const uint8_t* row = P + n * PR;
     switch (i >> 1) {
-      case 0: dec_item<WT, ODD, 0, O>(row, A, n); break;
-      case 1: dec_item<WT, ODD, 1, O>(row, A, n); break;
-      case 2: dec_item<WT, ODD, 2, O>(row, A, n); break;
-      default: dec_item<WT, ODD, 3, O>(row, A, n); break;
+      case 0: dec_item<WT, ODD, 0>(row, A, n, o); break;
+      case 1: dec_item<WT, ODD, 1>(row, A, n, o); break;
+      case 2: dec_item<WT, ODD, 2>(row, A, n, o); break;
+      default: dec_item<WT, ODD, 3>(row, A, n, o); break;
     }
   }
 }
@@ -1004,15 +1018,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
 #undef RG_WIN_CASE
             } else if constexpr (WT == RG_MXFP4) {
-              // the tile's four blocks start o = 0, 4, 8 or 12 bytes into the window
-              const uint8_t* P = sP + s * C::P_STAGE;
-              uint8_t* Ad = sA + s * A_STAGE;
-              switch ((kt * 68) & 12) {
-                case 0: decode_stage_warp<WT, 0, WPS, 0>(P, Ad, lane, part); break;
-                case 4: decode_stage_warp<WT, 0, WPS, 4>(P, Ad, lane, part); break;
-                case 8: decode_stage_warp<WT, 0, WPS, 8>(P, Ad, lane, part); break;
-                default: decode_stage_warp<WT, 0, WPS, 12>(P, Ad, lane, part); break;
-              }
+              // the tile's four blocks start (kt * 68) mod 16 = 0, 4, 8 or 12
+              // bytes into the window
+              decode_stage_warp<WT, 0, WPS>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part,
+                                            (kt * 68) & 12);
           } else if (kt & 1) {
               decode_stage_warp<WT, 1, WPS>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part);
             } else {
