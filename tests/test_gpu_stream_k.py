@@ -53,7 +53,12 @@ def _sampled(rg, case, seed):
     W = inputs.gen_weight(wtype, N, K, seed=seed, stream=1)
     dY = inputs.normal_f32(seed, 2, T * N, 1e-3).reshape(T, N)
     dX0 = inputs.normal_f32(seed, 3, T * K, 1e-3).reshape(T, K) if beta else None
+    torch.cuda.synchronize()
+    before = rg.rg_launch_count()
     got = _call(rg, variant, wtype, W, N, K, dY, T, dX0, beta)
+    # the dY conversion, the main kernel and the pass over the shared tiles
+    # (and F32 W's conversion)
+    assert rg.rg_launch_count() - before == info.launches
     again = _call(rg, variant, wtype, W, N, K, dY, T, dX0, beta)
     assert np.array_equal(got.view(np.uint32), again.view(np.uint32)), "not deterministic"
     Wd = oracle.dequant(wtype, W, N, K)
