@@ -109,10 +109,12 @@ typedef enum {
     RG_VARIANT_AUTO = 0,   /* the shape dispatcher's choice (what rg_out_prod runs)        */
     RG_VARIANT_TC = 1,     /* fused decode + tcgen05 tensor-core GEMM, fp16/bf16 operands,
                               F32 accumulation in tensor memory                             */
-    RG_VARIANT_SMALLT = 2, /* small-T, weight-bandwidth-bound: a warp streams whole rows
-                              of W (vector loads), exact F32 decode in registers, F32 FMA
-                              with up to 8 dY rows; rows split over many CTAs, partial
-                              sums added in a fixed order by a second kernel          */
+    RG_VARIANT_SMALLT = 2, /* small-T, weight-bandwidth-bound: TMA streams row stages
+                              of W; exact F32 decode and F32 FMA with up to 8 dY rows
+                              (Q4_K: nibbles as exact fp16 operands of warp-level MMAs,
+                              dY*scale rounded to fp16 once, F32 accumulation); rows
+                              split over many CTAs, partial sums added in a fixed order
+                              by a second kernel                                      */
     RG_VARIANT_SIMT32 = 3, /* exact F32 decode and F32 FMA with blocked accumulation: the
                               full-precision variant (slow; a correctness reference)        */
     RG_VARIANT_TC_SINGLE = 4, /* RG_VARIANT_TC with one-CTA 128 x 128 tiles                */

@@ -321,14 +321,37 @@ __host__ __device__ constexpr int tile_bytes() {
 // rows per stage (two per lane) in a 4-deep ring; the row-per-warp consumers
 // 32 rows in an 8-deep ring (4-deep for F32 W, whose rows are four times
 // wider than the quantized ones).
+// Q4_K at up to eight rows of dY goes through the warp-level MMA consumer
+// (consume_q4k_mma), also with 64-row stages in a 4-deep ring.
 template <int WT, int TB>
-constexpr bool rows_path() { return TB <= 2 && is_quant(WT) && !windowed<WT>(); }
+constexpr bool mma_path() { return WT == RG_Q4_K; }
 template <int WT, int TB>
-constexpr int stage_rows() { return rows_path<WT, TB>() ? 64 : 32; }
+constexpr bool rows_path() {
+  return TB <= 2 && is_quant(WT) && !windowed<WT>() && !mma_path<WT, TB>();
+}
 template <int WT, int TB>
-constexpr int n_stages() { return rows_path<WT, TB>() || WT == RG_F32 ? 4 : 8; }
+constexpr int stage_rows() { return rows_path<WT, TB>() || mma_path<WT, TB>() ? 64 : 32; }
+template <int WT, int TB>
+constexpr int n_stages() {
+  return rows_path<WT, TB>() || mma_path<WT, TB>() || WT == RG_F32 ? 4 : 8;
+}
 constexpr int CONSUMERS = 8; // consumer warps; warp 8 is the TMA producer
 constexpr int MAX_ROWS = 512;
+
+// Shared memory after the staged dY slice: the MMA consumer's scaled dY
+// table (two stage buffers of [sub-block][dY row][64 rows + 16 pad] fp16,
+// rows in fragment order, see table_pos),
+// its min-term partials [warp][4][2][TB] and the per-row maxima [8]; the
+// row-per-warp consumers' reduction buffer [4][TB][256].
+constexpr int YDS_STRIDE = 80;  // 40 words: lines 8 banks apart
+template <int TB>
+constexpr int yds_elems() { return 2 * 8 * TB * YDS_STRIDE; }
+template <int WT, int TB>
+constexpr int aux_bytes() {
+  return rows_path<WT, TB>() ? 0
+         : mma_path<WT, TB>() ? 2 * yds_elems<TB>() + 4 * (CONSUMERS * 4 * 2 * TB) + 4 * 8
+                              : 4 * 4 * TB * 256;
+}
 
 // --- one and two rows of dY: a block per warp, a row per lane ---------------
 // Warp g of the eight consumers owns block g of every row's 256-value tile
@@ -588,12 +611,230 @@ __device__ __forceinline__ void consume_rows(int g, const uint8_t* stage_buf, co
   }
 }
 
+// --- Q4_K, one to eight rows of dY: the warp-level tensor-core MMA ---------
+// mma.m16n8k16 computes D[k][t] += sum over 16 rows n of A[k][n] * B[n][t]
+// with A = the nibbles q of W (an fp16 register holds rows n and n + 1 of
+// one column k) and B = fp16(y * 2^s * d * sc), the dY row t times the
+// sub-block's scale; the min term sum_n y * dmin * m stays in F32.
+//  * A nibble q in the low bits of an fp16 is the subnormal q * 2^-24,
+//    exactly; a high nibble left in place is 16q * 2^-24.  So the operand
+//    pair of two rows costs one byte permute (one byte of each row) and one
+//    AND per nibble, 0.75 integer instructions a value, against about 2.5
+//    for an F32 value; the MMA takes the multiply-adds off the FMA pipe.
+//  * 2^s puts max|y| of the CTA's slice in [2, 4), so y * d * sc stays in
+//    fp16's normal range wherever d * sc * q does (the tensor-core variant's
+//    precondition); the result is scaled back exactly.
+//  * Warp w owns the 32 columns k = 64 (w >> 1) + 32 h + 4 g + 2 (w & 1) + j
+//    (g = 0..7, h, j = 0, 1): bytes 2 (w & 1) and 2 (w & 1) + 1 of word g
+//    of the 64-value chunk w >> 1, both nibbles, i.e. two accumulator tiles.
+//  * Per stage, the CTA first decodes each row's eight scales and mins
+//    (thread 4r + q: sub-blocks q and q + 4 of stage row r) into the fp16
+//    table B is loaded from, then every warp runs its MMAs over the 64 rows.
+
+// D += A * B for one m16n8k16 tile (fp16 operands, F32 accumulation).
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 2^s of dY row t from the bits of the slice's max|y| (clamped to F32's
+// normal powers; zero rows get 2^127, whose products are still zero), and
+// 2^-s, exactly (2^-127 is the subnormal 1 << 22).
+__device__ __forceinline__ int row_scale_exp(int max_bits) {
+  return min(max(255 - ((max_bits >> 23) & 255), 1), 254);
+}
+__device__ __forceinline__ float row_scale(int max_bits) {
+  return __int_as_float(row_scale_exp(max_bits) << 23);
+}
+__device__ __forceinline__ float row_unscale(int max_bits) {
+  const int fe = row_scale_exp(max_bits);
+  return __int_as_float(fe < 254 ? (254 - fe) << 23 : 1 << 22);
+}
+// Position of stage row r in its 16-row group of the scaled dY table: rows
+// 2c, 2c + 1, 2c + 8, 2c + 9 at 4c .. 4c + 3, so that fragment thread c loads
+// both of its B registers with one 8-byte read.
+__device__ __forceinline__ int table_pos(int r) {
+  return (r & ~15) | (4 * ((r & 7) >> 1) + (r & 1) + 2 * ((r >> 3) & 1));
+}
+
+// Named barrier 1 over the consumer warps that also returns, to every one of
+// them, whether any thread passed `any` true: a decision they all share (the
+// producer may set the abort flag between two warps' own reads of it).
+__device__ __forceinline__ bool consumers_sync_any(bool any) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(any)), "n"(THREADS)
+      : "memory");
+  return r != 0;
+}
+
+template <int TB, int BR, int STAGES_>
+__device__ __forceinline__ void consume_q4k_mma(int warp, int lane, const uint8_t* stage_buf,
+                                                float* ys, uint8_t* aux, uint32_t bar0,
+                                                int n_tiles, int nrows, int kt, int K, int t0, int T,
+                                                int split, float* part, WaitCtl ctl,
+                                                volatile int* abort_flag) {
+  constexpr int TBYTES = 144;  // Q4_K super-block: d, dmin, 12 scale bytes, 128 nibble bytes
+  static_assert(BR % 16 == 0 && BR == 64, "64-row stages: one scale-pass thread per (row, q)");
+  uint16_t* yds = reinterpret_cast<uint16_t*>(aux);
+  float* mred = reinterpret_cast<float*>(aux + 2 * yds_elems<TB>());
+  int* smax = reinterpret_cast<int*>(mred + CONSUMERS * 4 * 2 * TB);
+  const int tid = warp * 32 + lane;
+
+  // the slice's max|y| per dY row (NaN ignored), then y *= 2^s in place
+  {
+    float mx[TB];
+#pragma unroll
+    for (int t = 0; t < TB; ++t) {
+      mx[t] = 0.0f;
+      for (int r = tid; r < MAX_ROWS; r += THREADS) mx[t] = fmaxf(mx[t], fabsf(ys[t * MAX_ROWS + r]));
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) mx[t] = fmaxf(mx[t], __shfl_xor_sync(0xffffffffu, mx[t], o));
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int t = 0; t < TB; ++t) atomicMax(smax + t, __float_as_int(mx[t]));  // non-negative: int order
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");
+#pragma unroll
+  for (int t = 0; t < TB; ++t) {
+    const float f = row_scale(smax[t]);
+    for (int r = tid; r < MAX_ROWS; r += THREADS) ys[t * MAX_ROWS + r] *= f;
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");
+
+  const int srow = tid >> 2, q = tid & 3;        // scale pass: sub-blocks q, q + 4 of row srow
+  const int c4 = warp >> 1, bp = warp & 1;       // MMA: chunk c4, bytes 2bp and 2bp + 1 of a word
+  const int g = lane >> 2, c = lane & 3;         // the fragment's group and thread in group
+  // byte b of x into the low half, byte b of y into the high half
+  const uint32_t sel0 = static_cast<uint32_t>(2 * bp) * 0x0011u + static_cast<uint32_t>(4 + 2 * bp) * 0x1100u;
+  const uint32_t sel1 = sel0 + 0x1111u;
+  float acc[2][4];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[h][e] = 0.0f;
+  float msum[TB][2];
+#pragma unroll
+  for (int t = 0; t < TB; ++t) msum[t][0] = msum[t][1] = 0.0f;
+
+  for (int i = 0; i < n_tiles; ++i) {
+    const int s = i % STAGES_;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8u * s, static_cast<uint32_t>(i / STAGES_) & 1u,
+                                                      ctl, abort_flag));
+    uint16_t* Y = yds + (i & 1) * (8 * TB * YDS_STRIDE);
+    const uint8_t* stage = stage_buf + s * BR * TBYTES;
+    if (ok) {
+      // scales and mins of sub-blocks q and q + 4; a row past the slice (the
+      // next slice's, or TMA's zero fill past N) gets zero entries
+      const bool live = i * BR + srow < nrows;
+      uint4 hd = *reinterpret_cast<const uint4*>(stage + srow * TBYTES);
+      if (!live) hd = make_uint4(0u, 0u, 0u, 0u);
+      const float d = f16_to_f32(static_cast<uint16_t>(hd.x & 0xFFFFu));
+      const float dmin = f16_to_f32(static_cast<uint16_t>(hd.x >> 16));
+      const uint32_t b0 = hd.y >> (8 * q), b1 = hd.z >> (8 * q), b2 = hd.w >> (8 * q);
+      const float ds0 = d * static_cast<float>(b0 & 63u);
+      const float ds1 = d * static_cast<float>((b2 & 15u) | ((b0 >> 2) & 48u));
+      const float dm0 = dmin * static_cast<float>(b1 & 63u);
+      const float dm1 = dmin * static_cast<float>(((b2 >> 4) & 15u) | ((b1 >> 2) & 48u));
+      const float* yr = ys + i * BR + srow;
+      const int pos = table_pos(srow);
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        const float y = yr[t * MAX_ROWS];
+        Y[(q * TB + t) * YDS_STRIDE + pos] = __half_as_ushort(__float2half_rn(y * ds0));
+        Y[((q + 4) * TB + t) * YDS_STRIDE + pos] = __half_as_ushort(__float2half_rn(y * ds1));
+        msum[t][0] = fmaf(y, dm0, msum[t][0]);
+        msum[t][1] = fmaf(y, dm1, msum[t][1]);
+      }
+    }
+    // every consumer warp arrives, with or without its stage, and all take
+    // the same abort decision
+    if (consumers_sync_any(!ok || *abort_flag != 0)) break;
+    const uint8_t* wq = stage + 16 + 32 * c4 + 4 * g;
+#pragma unroll
+    for (int grp = 0; grp < BR / 16; ++grp) {
+      const int R = 16 * grp + 2 * c;  // rows R, R + 1 (k-pair 2c) and R + 8, R + 9 (2c + 8)
+      const uint32_t wa = *reinterpret_cast<const uint32_t*>(wq + R * TBYTES);
+      const uint32_t wb = *reinterpret_cast<const uint32_t*>(wq + (R + 1) * TBYTES);
+      const uint32_t wc = *reinterpret_cast<const uint32_t*>(wq + (R + 8) * TBYTES);
+      const uint32_t wd = *reinterpret_cast<const uint32_t*>(wq + (R + 9) * TBYTES);
+      const uint32_t p0 = __byte_perm(wa, wb, sel0), p1 = __byte_perm(wa, wb, sel1);
+      const uint32_t r0 = __byte_perm(wc, wd, sel0), r1 = __byte_perm(wc, wd, sel1);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t M = h ? 0x00F000F0u : 0x000F000Fu;
+        uint2 yv = make_uint2(0u, 0u);  // B: rows R, R + 1 and R + 8, R + 9 at dY row g
+        if (g < TB)
+          yv = *reinterpret_cast<const uint2*>(Y + ((2 * c4 + h) * TB + g) * YDS_STRIDE + 16 * grp + 4 * c);
+        mma_16816(acc[h], p0 & M, p1 & M, r0 & M, r1 & M, yv.x, yv.y);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar0 + 8u * (STAGES_ + s));
+  }
+
+  // the min terms of each sub-block over the slice's rows, in a fixed order:
+  // lanes of one q (xor 4, 8, 16), then the eight warps
+#pragma unroll
+  for (int t = 0; t < TB; ++t)
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+      for (int o = 4; o <= 16; o <<= 1) msum[t][jj] += __shfl_xor_sync(0xffffffffu, msum[t][jj], o);
+  if (lane < 4) {
+#pragma unroll
+    for (int t = 0; t < TB; ++t)
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) mred[((warp * 4 + lane) * 2 + jj) * TB + t] = msum[t][jj];
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");
+  // one thread per (sub-block j, dY row t) adds the eight warps in order
+  // (the table's space is free now)
+  float* mtot = reinterpret_cast<float*>(aux);
+  if (tid < 8 * TB) {
+    const int j = tid / TB, t = tid - j * TB;  // sub-block j: scale-pass thread q = j & 3, slot j >> 2
+    float m = 0.0f;
+#pragma unroll
+    for (int w = 0; w < CONSUMERS; ++w) m += mred[((w * 4 + (j & 3)) * 2 + (j >> 2)) * TB + t];
+    mtot[j * TB + t] = m;
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");
+  // this lane's outputs: dY rows 2c, 2c + 1 at columns k and k + 1 of each tile
+  const float inv0 = 2 * c < TB ? row_unscale(smax[2 * c]) : 0.0f;
+  const float inv1 = 2 * c + 1 < TB ? row_unscale(smax[2 * c + 1]) : 0.0f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = 2 * c4 + h;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int t = 2 * c + (e & 1);
+      const int gk = kt * 256 + 64 * c4 + 32 * h + 4 * g + 2 * bp + (e >> 1);
+      if (t < TB && t0 + t < T && gk < K) {
+        const float v = (acc[h][e] * (h ? 1048576.0f : 16777216.0f) - mtot[j * TB + t]) *  // 2^20, 2^24
+                        ((e & 1) ? inv1 : inv0);
+        part[(static_cast<int64_t>(split) * T + t0 + t) * K + gk] = v;
+      }
+    }
+  }
+}
+
 // grid (ceil(K/256), n_splits, ceil(T/TB)); partial sums of rows
 // [split * rows_per_split, +rows_per_split) to part[(split * T + t) * K + k].
 // A producer warp streams the CTA's rows of W, tile by tile of BR rows, into
 // an 8-stage ring with TMA; eight consumer warps decode from shared memory.
 template <int WT, int TB>
-__global__ void __launch_bounds__(THREADS + 32, rows_path<WT, TB>() && TB == 1 ? 3 : (TB >= 8 ? 1 : 2))
+__global__ void __launch_bounds__(THREADS + 32, mma_path<WT, TB>() ? (TB <= 2 ? 4 : TB == 4 ? 3 : 2)
+                                                : rows_path<WT, TB>() && TB == 1 ? 3
+                                                : TB >= 8                        ? 1
+                                                                                 : 2)
     smallt_kernel(const __grid_constant__ CUtensorMap map_w, int N, int K,
                   const float* __restrict__ dY, int64_t dy_t, int64_t dy_n, int T,
                   float* __restrict__ part, int rows_per_split, WaitCtl ctl) {
@@ -602,11 +843,14 @@ __global__ void __launch_bounds__(THREADS + 32, rows_path<WT, TB>() && TB == 1 ?
   extern __shared__ __align__(128) uint8_t sm[];
   uint8_t* stage_buf = sm;                                              // STAGES x BR x TBYTES
   float* ys = reinterpret_cast<float*>(sm + STAGES * BR * TBYTES);      // [TB][MAX_ROWS]
-  float* red = ys + TB * MAX_ROWS;                                      // [4][TB][256] (8 values a lane)
-  uint64_t* bars =
-      reinterpret_cast<uint64_t*>(red + (rows_path<WT, TB>() ? 0 : 4 * TB * 256));  // full[S], empty[S]
+  float* red = ys + TB * MAX_ROWS;                                      // aux_bytes<WT, TB>()
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) +
+                                               aux_bytes<WT, TB>());    // full[S], empty[S]
   __shared__ int abort_flag_s;
   volatile int* abort_flag = &abort_flag_s;
+  // the reduction kernel after this one may be scheduled now (it waits for
+  // this grid to complete before reading the partial sums)
+  pdl_launch_dependents();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kt = blockIdx.x, split = blockIdx.y;
@@ -624,6 +868,10 @@ __global__ void __launch_bounds__(THREADS + 32, rows_path<WT, TB>() && TB == 1 ?
       mbar_init(empty(s), CONSUMERS);
     }
     abort_flag_s = 0;
+    if constexpr (mma_path<WT, TB>()) {
+      int* smax = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(red) + aux_bytes<WT, TB>() - 32);
+      for (int t = 0; t < 8; ++t) smax[t] = 0;
+    }
     fence_mbar_init();
   }
   __syncthreads();
@@ -660,7 +908,12 @@ __global__ void __launch_bounds__(THREADS + 32, rows_path<WT, TB>() && TB == 1 ?
     __syncwarp();
   }
 
-  if constexpr (rows_path<WT, TB>()) {
+  if constexpr (mma_path<WT, TB>()) {
+    if (warp < CONSUMERS)
+      consume_q4k_mma<TB, BR, STAGES>(warp, lane, stage_buf, ys, reinterpret_cast<uint8_t*>(red), bar0,
+                                      n_tiles, nrows, kt, K, t0, T, split, part, ctl, abort_flag);
+    return;
+  } else if constexpr (rows_path<WT, TB>()) {
     // quantized, one and two rows of dY: a block per warp, a row per lane
     if (warp < CONSUMERS)
       consume_rows<WT, TB, TBYTES, BR, STAGES>(warp, stage_buf, ys, bar0, n_tiles, nrows, lane, kt,
@@ -735,8 +988,7 @@ __global__ void __launch_bounds__(THREADS + 32, rows_path<WT, TB>() && TB == 1 ?
 template <int WT, int TB>
 constexpr size_t smem_bytes() {
   return static_cast<size_t>(n_stages<WT, TB>()) * stage_rows<WT, TB>() * stage_row_bytes<WT>() +
-         sizeof(float) * TB * MAX_ROWS + (rows_path<WT, TB>() ? 0 : sizeof(float) * 4 * TB * 256) +
-         16 * n_stages<WT, TB>();
+         sizeof(float) * TB * MAX_ROWS + aux_bytes<WT, TB>() + 16 * n_stages<WT, TB>();
 }
 
 // dX = beta * dX + sum over splits (in split order), four values per thread.

@@ -153,10 +153,19 @@ def test_beta_zero_ignores_nan(rg, variant):
     assert np.isfinite(got).all()
 
 
+def _q4_k_scale_part(W, N, K):
+    """d * sc * q of every Q4_K value (the decode with dmin zeroed)."""
+    Wz = W.copy().reshape(-1, 144)
+    Wz[:, 2:4] = 0
+    return oracle.dequant(inputs.Q4_K, Wz.reshape(-1), N, K)
+
+
 @pytest.mark.parametrize("variant", [2, 3])
 @pytest.mark.parametrize("wtype", TYPES)
 def test_one_hot_f32_variants_equal_rows(rg, variant, wtype):
-    """F32 variants: one-hot dY reproduces rows of deq(W) exactly."""
+    """F32 variants: one-hot dY reproduces rows of deq(W) exactly.  Q4_K on
+    the small-T variant multiplies in the MMA with fp16(y * d * sc): one
+    rounding of the scale part, 2^-11 relative, and the F32 subtraction."""
     N, K, T = 80, kfit(wtype, 512, variant), 6
     W = inputs.gen_weight(wtype, N, K, seed=6, stream=1)
     Wd = oracle.dequant(wtype, W, N, K)
@@ -164,8 +173,43 @@ def test_one_hot_f32_variants_equal_rows(rg, variant, wtype):
     dY = np.zeros((T, N), np.float32)
     dY[np.arange(T), n0] = 1.0
     got = run_out_prod(rg, variant, wtype, W, N, K, dY, T)
+    if variant == 2 and wtype == inputs.Q4_K:
+        dsq = _q4_k_scale_part(W, N, K).astype(np.float64)
+        for t in range(T):
+            err = np.abs(got[t].astype(np.float64) - Wd[n0[t]])
+            lim = 2.0 ** -11 * dsq[n0[t]] + 2.0 ** -23 * (np.abs(Wd[n0[t]]) + dsq[n0[t]])
+            assert np.all(err <= lim), (t, float((err - lim).max()))
+        return
     for t in range(T):
         assert np.array_equal(np.abs(got[t]), np.abs(Wd[n0[t]])), (t,)
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8, 11])
+def test_smallt_q4_k_mma_rows(rg, T):
+    """The small-T Q4_K consumer (warp-level MMA, one to eight dY rows a
+    pass): ragged N against the 64-row stages and the row splits, three
+    k tiles, one dY row all zero (exact zeros out), one tiny (1e-30) and
+    one large (1e3) row, each kept in fp16's normal range by the row's
+    power-of-two scale."""
+    wtype, N, K = inputs.Q4_K, 1000, 768
+    W = inputs.gen_weight(wtype, N, K, seed=31, stream=1)
+    dY = inputs.normal_f32(31, 2, T * N, 1e-3).reshape(T, N)
+    if T >= 3:
+        dY[1] = 0.0
+        dY[2] *= np.float32(1e-27)
+    if T >= 4:
+        dY[3] *= np.float32(1e6)
+    Wd = oracle.dequant(wtype, W, N, K)
+    ref = oracle.out_prod(wtype, W, N, K, dY, T, Wd=Wd)
+    bnd = oracle.abs_bound(dY, Wd)
+    got = run_out_prod(rg, 2, wtype, W, N, K, dY, T)
+    assert_within(got, ref, bnd, 5e-3, f"T {T}")
+    if T >= 3:
+        assert np.all(got[1] == 0.0)
+        # the tiny and large rows on their own scale (no absolute slack)
+        for t in range(2, min(T, 4)):
+            err = np.abs(got[t].astype(np.float64) - ref[t])
+            assert np.all(err <= 5e-3 * bnd[t]), (t, float((err / bnd[t]).max()))
 
 
 @pytest.mark.parametrize("variant", [4, 5])
