@@ -687,7 +687,7 @@ int rg_plan(int variant, int wtype, int64_t N, int64_t K, int64_t T, rg_plan_inf
     tile_t = p.tb;
     r.n_splits = p.n_splits;
     r.grid = p.n_ktiles * p.n_splits * p.n_tchunks;
-    r.launches = 2;  // row-split partial sums, their reduction
+    r.launches = p.n_splits > 1 ? 2 : 1;  // row-split partial sums and their reduction, or dX directly
   } else {
     r.tile_k = 64;
     tile_t = 64;

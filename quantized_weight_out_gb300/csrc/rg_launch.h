@@ -148,9 +148,9 @@ struct SmalltPlan {
   int tb;              // dY rows per pass: 1, 2, 4 or 8
   int n_ktiles;        // ceil(K / 256)
   int n_tchunks;       // ceil(T / tb)
-  int n_splits;        // CTAs along N per tile
+  int n_splits;        // CTAs along N per tile (1: the kernel writes dX itself)
   int rows_per_split;  // rows of W per CTA (multiple of 8)
-  size_t workspace;    // bytes of partial sums
+  size_t workspace;    // bytes of partial sums (0 for one slice)
 };
 // Sized so that the grid fills the GPU once at the kernel's residency.
 SmalltPlan plan_smallt(int wtype, int64_t N, int64_t K, int64_t T, const DevInfo& dev);

@@ -338,6 +338,20 @@ constexpr int n_stages() {
 constexpr int CONSUMERS = 8; // consumer warps; warp 8 is the TMA producer
 constexpr int MAX_ROWS = 512;
 
+// Where a CTA's sums go: partial sums p[(split * T + t) * ld + k] for the
+// reduction kernel (beta 0), or, when one CTA holds all N rows, dX itself
+// (ld = dX's row stride) with beta * dX added.
+struct SmtOut {
+  float* p;
+  int64_t ld;
+  float beta;
+};
+__device__ __forceinline__ void smt_store(const SmtOut& o, int split, int T, int t, int k, float v) {
+  float* q = o.p + (static_cast<int64_t>(split) * T + t) * o.ld + k;
+  if (o.beta != 0.0f) v = fmaf(o.beta, *q, v);
+  *q = v;
+}
+
 // Shared memory after the staged dY slice: the MMA consumer's scaled dY
 // table (two stage buffers of [sub-block][dY row][64 rows + 16 pad] fp16,
 // rows in fragment order, see table_pos),
@@ -556,7 +570,7 @@ template <int WT, int TB, int TBYTES, int BR, int STAGES_>
 __device__ __forceinline__ void consume_rows(int g, const uint8_t* stage_buf, const float* ys,
                                              uint32_t bar0,
                                              int n_tiles, int nrows, int lane, int kt, int K,
-                                             int t0, int T, int split, float* part, WaitCtl ctl,
+                                             int t0, int T, int split, SmtOut out, WaitCtl ctl,
                                              volatile int* abort_flag) {
   f32x2 acc[TB][16];
   float msum[TB];
@@ -607,7 +621,7 @@ __device__ __forceinline__ void consume_rows(int g, const uint8_t* stage_buf, co
       }
     }
     const int gt = t0 + t, gk = kt * 256 + 32 * g + lane;
-    if (gt < T && gk < K) part[(static_cast<int64_t>(split) * T + gt) * K + gk] = v[0];
+    if (gt < T && gk < K) smt_store(out, split, T, gt, gk, v[0]);
   }
 }
 
@@ -678,7 +692,7 @@ template <int TB, int BR, int STAGES_>
 __device__ __forceinline__ void consume_q4k_mma(int warp, int lane, const uint8_t* stage_buf,
                                                 float* ys, uint8_t* aux, uint32_t bar0,
                                                 int n_tiles, int nrows, int kt, int K, int t0, int T,
-                                                int split, float* part, WaitCtl ctl,
+                                                int split, SmtOut out, WaitCtl ctl,
                                                 volatile int* abort_flag) {
   constexpr int TBYTES = 144;  // Q4_K super-block: d, dmin, 12 scale bytes, 128 nibble bytes
   static_assert(BR % 16 == 0 && BR == 64, "64-row stages: one scale-pass thread per (row, q)");
@@ -820,14 +834,14 @@ __device__ __forceinline__ void consume_q4k_mma(int warp, int lane, const uint8_
       if (t < TB && t0 + t < T && gk < K) {
         const float v = (acc[h][e] * (h ? 1048576.0f : 16777216.0f) - mtot[j * TB + t]) *  // 2^20, 2^24
                         ((e & 1) ? inv1 : inv0);
-        part[(static_cast<int64_t>(split) * T + t0 + t) * K + gk] = v;
+        smt_store(out, split, T, t0 + t, gk, v);
       }
     }
   }
 }
 
-// grid (ceil(K/256), n_splits, ceil(T/TB)); partial sums of rows
-// [split * rows_per_split, +rows_per_split) to part[(split * T + t) * K + k].
+// grid (ceil(K/256), n_splits, ceil(T/TB)); the sums over rows
+// [split * rows_per_split, +rows_per_split) to `out` (partial sums, or dX).
 // A producer warp streams the CTA's rows of W, tile by tile of BR rows, into
 // an 8-stage ring with TMA; eight consumer warps decode from shared memory.
 template <int WT, int TB>
@@ -837,7 +851,7 @@ __global__ void __launch_bounds__(THREADS + 32, mma_path<WT, TB>() ? (TB <= 2 ? 
                                                                                  : 2)
     smallt_kernel(const __grid_constant__ CUtensorMap map_w, int N, int K,
                   const float* __restrict__ dY, int64_t dy_t, int64_t dy_n, int T,
-                  float* __restrict__ part, int rows_per_split, WaitCtl ctl) {
+                  SmtOut out, int rows_per_split, WaitCtl ctl) {
   constexpr int TBYTES = stage_row_bytes<WT>();
   constexpr int BR = stage_rows<WT, TB>(), STAGES = n_stages<WT, TB>();
   extern __shared__ __align__(128) uint8_t sm[];
@@ -911,13 +925,13 @@ __global__ void __launch_bounds__(THREADS + 32, mma_path<WT, TB>() ? (TB <= 2 ? 
   if constexpr (mma_path<WT, TB>()) {
     if (warp < CONSUMERS)
       consume_q4k_mma<TB, BR, STAGES>(warp, lane, stage_buf, ys, reinterpret_cast<uint8_t*>(red), bar0,
-                                      n_tiles, nrows, kt, K, t0, T, split, part, ctl, abort_flag);
+                                      n_tiles, nrows, kt, K, t0, T, split, out, ctl, abort_flag);
     return;
   } else if constexpr (rows_path<WT, TB>()) {
     // quantized, one and two rows of dY: a block per warp, a row per lane
     if (warp < CONSUMERS)
       consume_rows<WT, TB, TBYTES, BR, STAGES>(warp, stage_buf, ys, bar0, n_tiles, nrows, lane, kt,
-                                               K, t0, T, split, part, ctl, abort_flag);
+                                               K, t0, T, split, out, ctl, abort_flag);
     return;
   } else {
   float acc[TB][8];
@@ -979,7 +993,7 @@ __global__ void __launch_bounds__(THREADS + 32, mma_path<WT, TB>() ? (TB <= 2 ? 
     if (gt < T && gk < K) {
       const float sum = ((red[(0 * TB + t) * 256 + kk] + red[(1 * TB + t) * 256 + kk]) +
                          red[(2 * TB + t) * 256 + kk]) + red[(3 * TB + t) * 256 + kk];
-      part[(static_cast<int64_t>(split) * T + gt) * K + gk] = sum;
+      smt_store(out, split, T, gt, gk, sum);
     }
   }
   }
@@ -1102,17 +1116,37 @@ static int smallt_residency_tb(int tb, const DevInfo& dev) {
   }
 }
 
+// At most this many rows of W, one CTA per tile takes them all.
+constexpr int64_t kOneSliceRows = 256;
+
 SmalltPlan plan_smallt(int wtype, int64_t N, int64_t K, int64_t T, const DevInfo& dev) {
   SmalltPlan p{};
-  p.tb = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
+  const int tb_max = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
   p.n_ktiles = static_cast<int>((K + 255) / 256);
+  auto capacity_at = [&](int tb) {
+    const int per_sm = with_wtype(wtype, 1, [&](auto wt) {
+      return smallt_residency_tb<decltype(wt)::value>(tb, dev);
+    });
+    return static_cast<int64_t>(dev.num_sms) * per_sm;
+  };
+  if (N <= kOneSliceRows) {
+    // few rows of W: one CTA takes all of them for its tile and writes dX
+    // itself (no partial sums, no second kernel), with as few dY rows per
+    // pass as keep the tiles within one wave
+    int tb = 1;
+    while (tb < tb_max && static_cast<int64_t>(p.n_ktiles) * ((T + tb - 1) / tb) > capacity_at(tb)) tb *= 2;
+    p.tb = tb;
+    p.n_tchunks = static_cast<int>((T + tb - 1) / tb);
+    p.rows_per_split = static_cast<int>((N + 7) / 8 * 8);
+    p.n_splits = 1;
+    p.workspace = 0;
+    return p;
+  }
+  p.tb = tb_max;
   p.n_tchunks = static_cast<int>((T + p.tb - 1) / p.tb);
-  const int per_sm = with_wtype(wtype, 1, [&](auto wt) {
-    return smallt_residency_tb<decltype(wt)::value>(p.tb, dev);
-  });
   // one wave of resident CTAs; rows split no finer than 64 per CTA and no
   // coarser than the staged slice of dY allows
-  const int64_t capacity = static_cast<int64_t>(dev.num_sms) * per_sm;
+  const int64_t capacity = capacity_at(p.tb);
   const int64_t tiles = static_cast<int64_t>(p.n_ktiles) * p.n_tchunks;
   int64_t splits = std::max<int64_t>(1, capacity / tiles);
   splits = std::min<int64_t>(splits, (N + 63) / 64);
@@ -1121,14 +1155,17 @@ SmalltPlan plan_smallt(int wtype, int64_t N, int64_t K, int64_t T, const DevInfo
   rows = (rows + 7) / 8 * 8;
   p.rows_per_split = static_cast<int>(rows);
   p.n_splits = static_cast<int>((N + rows - 1) / rows);
-  p.workspace = static_cast<size_t>(p.n_splits) * static_cast<size_t>(T) * static_cast<size_t>(K) * 4;
+  // a single slice writes dX directly
+  p.workspace = p.n_splits == 1 ? 0
+                                : static_cast<size_t>(p.n_splits) * static_cast<size_t>(T) *
+                                      static_cast<size_t>(K) * 4;
   return p;
 }
 
 template <int WT, int TB>
 static cudaError_t launch_smallt_t(const void* W, int64_t N, int64_t K, const float* dY,
-                                   int64_t T, const Layout& lay, float* part, const SmalltPlan& p,
-                                   const DevInfo& dev, cudaStream_t stream) {
+                                   int64_t T, float* dX, float beta, const Layout& lay, float* part,
+                                   const SmalltPlan& p, const DevInfo& dev, cudaStream_t stream) {
   auto kern = smt::smallt_kernel<WT, TB>;
   constexpr size_t smem = smt::smem_bytes<WT, TB>();
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
@@ -1143,21 +1180,24 @@ static cudaError_t launch_smallt_t(const void* W, int64_t N, int64_t K, const fl
   const dim3 grid(static_cast<unsigned>(p.n_ktiles), static_cast<unsigned>(p.n_splits),
                   static_cast<unsigned>(p.n_tchunks));
   WaitCtl ctl{dev.status, dev.wait_limit_ns};
+  // one slice of rows: the sums are dX itself; else partial sums for the
+  // reduction kernel
+  const smt::SmtOut out = p.n_splits == 1 ? smt::SmtOut{dX, lay.dx_t, beta} : smt::SmtOut{part, K, 0.0f};
   kern<<<grid, smt::THREADS + 32, smem, stream>>>(map, static_cast<int>(N), static_cast<int>(K), dY,
-                                                   lay.dy_t, lay.dy_n, static_cast<int>(T), part,
+                                                   lay.dy_t, lay.dy_n, static_cast<int>(T), out,
                                                    p.rows_per_split, ctl);
   return counted(cudaGetLastError());
 }
 
 template <int WT>
 static cudaError_t launch_smallt_w(const void* W, int64_t N, int64_t K, const float* dY,
-                                   int64_t T, const Layout& lay, float* part, const SmalltPlan& p,
-                                   const DevInfo& dev, cudaStream_t stream) {
+                                   int64_t T, float* dX, float beta, const Layout& lay, float* part,
+                                   const SmalltPlan& p, const DevInfo& dev, cudaStream_t stream) {
   switch (p.tb) {
-    case 1: return launch_smallt_t<WT, 1>(W, N, K, dY, T, lay, part, p, dev, stream);
-    case 2: return launch_smallt_t<WT, 2>(W, N, K, dY, T, lay, part, p, dev, stream);
-    case 4: return launch_smallt_t<WT, 4>(W, N, K, dY, T, lay, part, p, dev, stream);
-    default: return launch_smallt_t<WT, 8>(W, N, K, dY, T, lay, part, p, dev, stream);
+    case 1: return launch_smallt_t<WT, 1>(W, N, K, dY, T, dX, beta, lay, part, p, dev, stream);
+    case 2: return launch_smallt_t<WT, 2>(W, N, K, dY, T, dX, beta, lay, part, p, dev, stream);
+    case 4: return launch_smallt_t<WT, 4>(W, N, K, dY, T, dX, beta, lay, part, p, dev, stream);
+    default: return launch_smallt_t<WT, 8>(W, N, K, dY, T, dX, beta, lay, part, p, dev, stream);
   }
 }
 
@@ -1166,9 +1206,9 @@ cudaError_t launch_smallt(int wtype, const void* W, int64_t N, int64_t K, const 
                           const SmalltPlan& p, const DevInfo& dev, cudaStream_t stream) {
   if (p.n_tchunks > 65535 || p.n_splits > 65535) return cudaErrorInvalidConfiguration;
   const cudaError_t e = with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
-    return launch_smallt_w<decltype(wt)::value>(W, N, K, dY, T, lay, part, p, dev, stream);
+    return launch_smallt_w<decltype(wt)::value>(W, N, K, dY, T, dX, beta, lay, part, p, dev, stream);
   });
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || p.n_splits == 1) return e;  // one slice: the kernel wrote dX
   return launch_reduce_partials(part, p.n_splits, T, K, dX, lay.dx_t, beta, dev, stream);
 }
 

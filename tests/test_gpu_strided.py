@@ -51,6 +51,36 @@ def test_transposed_dy_and_padded_dx(rg, variant, wtype):
     _check(out[:, :K], ref, bnd, TOL[variant], f"variant {variant}")
 
 
+@pytest.mark.parametrize("wtype", [inputs.Q4_K, inputs.Q8_0, inputs.F16])
+def test_small_t_one_slice_writes_dx(rg, wtype):
+    """At most 256 rows of W: one small-T kernel per call takes all the rows
+    of its tile and writes dX itself (beta applied, padded rows, padding
+    untouched), with no partial sums and no second kernel."""
+    N, K, T, beta = 200, 512, 6, -0.5
+    info = rg.rg_plan_info()
+    rg.check(rg.rg_plan(2, wtype, N, K, T, info), "rg_plan")
+    assert info.n_splits == 1 and info.launches == 1 and info.workspace_bytes == 0, info.as_dict()
+    W = inputs.gen_weight(wtype, N, K, seed=53, stream=1)
+    dY = inputs.normal_f32(53, 2, T * N, 1e-3).reshape(T, N)
+    dX0 = inputs.normal_f32(53, 3, T * K, 1e-3).reshape(T, K)
+    dev, s = torch.device("cuda:0"), torch.cuda.current_stream()
+    ldx = K + 4
+    buf = torch.full((T, ldx), 7.0, device=dev)
+    buf[:, :K] = torch.from_numpy(dX0).to(dev)
+    torch.cuda.synchronize()
+    before = rg.rg_launch_count()
+    rg.check(rg.rg_out_prod_ex(2, wtype, torch.from_numpy(W).to(dev), N, K, 0,
+                               torch.from_numpy(dY).to(dev), T, N, 1, 0, buf, ldx, 0, 1, beta, s))
+    rg.check(rg.rg_check(s))
+    assert rg.rg_launch_count() - before == 1
+    out = buf.cpu().numpy()
+    assert np.all(out[:, K:] == 7.0)
+    Wd = oracle.dequant(wtype, W, N, K)
+    ref = oracle.out_prod(wtype, W, N, K, dY, T, dX0, beta, Wd=Wd)
+    bnd = oracle.abs_bound(dY, Wd) + np.abs(beta * dX0) * 2.0 ** -24 / 5e-3
+    _check(out[:, :K], ref, bnd, 5e-3, "one slice")
+
+
 @pytest.mark.parametrize("variant", [0, 2, 3])
 def test_padded_dy_rows(rg, variant):
     """dY rows N + 5 floats apart (only 4-byte aligned)."""
