@@ -114,7 +114,7 @@ typedef enum {
                               (Q4_K: nibbles as exact fp16 operands of warp-level MMAs,
                               dY*scale rounded to fp16 once, F32 accumulation); rows
                               split over many CTAs, partial sums added in a fixed order
-                              by a second kernel                                      */
+                              by a second kernel (N <= 256: one kernel writes dX)     */
     RG_VARIANT_SIMT32 = 3, /* exact F32 decode and F32 FMA with blocked accumulation: the
                               full-precision variant (slow; a correctness reference)        */
     RG_VARIANT_TC_SINGLE = 4, /* RG_VARIANT_TC with one-CTA 128 x 128 tiles                */

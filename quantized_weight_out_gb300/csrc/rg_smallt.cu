@@ -4,17 +4,20 @@
 // role of the in-place decoder the Retrograd page "CUDA status", section
 // "Limitations", keeps for small outputs).
 //
-// Every weight value is read from memory once per pass of up to 8 dY rows,
-// decoded exactly to F32 in registers, and multiplied in F32 by each dY row.
+// Every weight value is read from memory once per pass of up to 8 dY rows.
 //  * A producer warp streams the CTA's rows of W (its 256-value tile of each
-//    row) with TMA into an 8-stage shared-memory ring of 32-row tiles, so
-//    enough bytes are in flight without holding them in registers.
-//  * A consumer warp takes whole rows: lane l owns values 8l .. 8l+7, reads
-//    their bytes from shared memory and decodes them in registers.
+//    row) with TMA into a shared-memory ring of row stages, so enough bytes
+//    are in flight without holding them in registers.
+//  * Eight consumer warps decode from shared memory: Q4_K through the
+//    warp-level tensor-core MMA with the nibbles themselves as exact fp16
+//    operands (consume_q4k_mma); other quantized types at one or two dY rows
+//    a block per warp and a row per lane in F32 (consume_rows); the rest
+//    eight values a lane, decoded exactly to F32, F32 FMAs.
 //  * The rows are split over many CTAs (grid.y) so that the whole GPU streams
-//    W; each CTA sums its eight warps in a fixed order and writes its partial
-//    tile to a workspace, and a second kernel adds the partials in split
-//    order together with beta * dX: deterministic, no atomics.
+//    W; each CTA writes its partial tile to a workspace, and a second kernel
+//    adds the partials in split order together with beta * dX:
+//    deterministic, no atomics.  With at most 256 rows of W one CTA per tile
+//    takes them all and writes beta * dX + sum into dX itself.
 #include <algorithm>
 
 #include "rg_internal.cuh"
