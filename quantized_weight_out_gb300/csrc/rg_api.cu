@@ -268,7 +268,7 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
   cudaError_t e = cudaSuccess;
   if (variant == RG_VARIANT_SMALLT) {
     e = launch_smallt(wtype, W, N, K, dY, T, dX, beta, lay, static_cast<float*>(buf),
-                      plan_smallt(wtype, N, K, T, *dev), *dev, stream);
+                      plan_smallt(wtype, N, K, T, *dev), *dev, stream, env().inject_stall);
     if (own_ws) {
       const cudaError_t f = cudaFreeAsync(buf, stream);
       if (e == cudaSuccess) e = f;

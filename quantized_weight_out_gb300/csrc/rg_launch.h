@@ -154,9 +154,12 @@ struct SmalltPlan {
 };
 // Sized so that the grid fills the GPU once at the kernel's residency.
 SmalltPlan plan_smallt(int wtype, int64_t N, int64_t K, int64_t T, const DevInfo& dev);
+// inject_stall (debug): the producer skips its first stage, whose wait then
+// runs out (the bounded-wait path, tested without a fault)
 cudaError_t launch_smallt(int wtype, const void* W, int64_t N, int64_t K, const float* dY,
                           int64_t T, float* dX, float beta, const Layout& lay, float* part,
-                          const SmalltPlan& p, const DevInfo& dev, cudaStream_t stream);
+                          const SmalltPlan& p, const DevInfo& dev, cudaStream_t stream,
+                          int inject_stall = 0);
 
 // Tensor-core path.  dy16 is the converted dY with row stride ld_dy16 values.
 struct TcPlan {

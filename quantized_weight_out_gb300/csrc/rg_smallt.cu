@@ -854,7 +854,7 @@ __global__ void __launch_bounds__(THREADS + 32, mma_path<WT, TB>() ? (TB <= 2 ? 
                                                                                  : 2)
     smallt_kernel(const __grid_constant__ CUtensorMap map_w, int N, int K,
                   const float* __restrict__ dY, int64_t dy_t, int64_t dy_n, int T,
-                  SmtOut out, int rows_per_split, WaitCtl ctl) {
+                  SmtOut out, int rows_per_split, WaitCtl ctl, int inject_stall) {
   constexpr int TBYTES = stage_row_bytes<WT>();
   constexpr int BR = stage_rows<WT, TB>(), STAGES = n_stages<WT, TB>();
   extern __shared__ __align__(128) uint8_t sm[];
@@ -907,20 +907,27 @@ __global__ void __launch_bounds__(THREADS + 32, mma_path<WT, TB>() ? (TB <= 2 ? 
   if (warp == CONSUMERS) {
     // ---------------- producer ----------------
     if (lane == 0) {
-      uint32_t ph = 0;
+      uint32_t ph = 0, pend = 0, pend_ph = 0;  // slots with a copy started, and its parity
+      bool skip = inject_stall != 0;
       for (int i = 0; i < n_tiles; ++i) {
         const int s = i % STAGES;
         if (!mbar_wait(empty(s), ph ^ 1u, ctl, abort_flag)) break;
-        mbar_arrive_expect_tx(full(s), BR * TBYTES);
-        tma_load_2d(smem_addr(stage_buf + s * BR * TBYTES), &map_w, full(s),
-                    static_cast<int>(window_start<WT>(kt) / 4),
-                    nbeg + i * BR);
+        if (skip) {
+          skip = false;  // fault injection: the first stage never fills
+        } else {
+          mbar_arrive_expect_tx(full(s), BR * TBYTES);
+          tma_load_2d(smem_addr(stage_buf + s * BR * TBYTES), &map_w, full(s),
+                      static_cast<int>(window_start<WT>(kt) / 4), nbeg + i * BR);
+          pend |= 1u << s;
+          pend_ph = (pend_ph & ~(1u << s)) | (ph << s);
+        }
         if (s == STAGES - 1) ph ^= 1u;
       }
-      // drain: the copies started land before the CTA leaves
+      // drain: every copy started lands before the CTA leaves (a consumed
+      // one's phase is past, and its wait returns at once)
       volatile int no_abort = 0;
-      for (int i = max(0, n_tiles - STAGES); i < n_tiles; ++i)
-        (void)mbar_wait(full(i % STAGES), static_cast<uint32_t>(i / STAGES) & 1u, ctl, &no_abort);
+      for (int s = 0; s < STAGES; ++s)
+        if (pend & (1u << s)) (void)mbar_wait(full(s), (pend_ph >> s) & 1u, ctl, &no_abort);
     }
     __syncwarp();
   }
@@ -1168,7 +1175,8 @@ SmalltPlan plan_smallt(int wtype, int64_t N, int64_t K, int64_t T, const DevInfo
 template <int WT, int TB>
 static cudaError_t launch_smallt_t(const void* W, int64_t N, int64_t K, const float* dY,
                                    int64_t T, float* dX, float beta, const Layout& lay, float* part,
-                                   const SmalltPlan& p, const DevInfo& dev, cudaStream_t stream) {
+                                   const SmalltPlan& p, const DevInfo& dev, cudaStream_t stream,
+                                   int inject_stall) {
   auto kern = smt::smallt_kernel<WT, TB>;
   constexpr size_t smem = smt::smem_bytes<WT, TB>();
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
@@ -1188,28 +1196,31 @@ static cudaError_t launch_smallt_t(const void* W, int64_t N, int64_t K, const fl
   const smt::SmtOut out = p.n_splits == 1 ? smt::SmtOut{dX, lay.dx_t, beta} : smt::SmtOut{part, K, 0.0f};
   kern<<<grid, smt::THREADS + 32, smem, stream>>>(map, static_cast<int>(N), static_cast<int>(K), dY,
                                                    lay.dy_t, lay.dy_n, static_cast<int>(T), out,
-                                                   p.rows_per_split, ctl);
+                                                   p.rows_per_split, ctl, inject_stall);
   return counted(cudaGetLastError());
 }
 
 template <int WT>
 static cudaError_t launch_smallt_w(const void* W, int64_t N, int64_t K, const float* dY,
                                    int64_t T, float* dX, float beta, const Layout& lay, float* part,
-                                   const SmalltPlan& p, const DevInfo& dev, cudaStream_t stream) {
+                                   const SmalltPlan& p, const DevInfo& dev, cudaStream_t stream,
+                                   int inject_stall) {
   switch (p.tb) {
-    case 1: return launch_smallt_t<WT, 1>(W, N, K, dY, T, dX, beta, lay, part, p, dev, stream);
-    case 2: return launch_smallt_t<WT, 2>(W, N, K, dY, T, dX, beta, lay, part, p, dev, stream);
-    case 4: return launch_smallt_t<WT, 4>(W, N, K, dY, T, dX, beta, lay, part, p, dev, stream);
-    default: return launch_smallt_t<WT, 8>(W, N, K, dY, T, dX, beta, lay, part, p, dev, stream);
+    case 1: return launch_smallt_t<WT, 1>(W, N, K, dY, T, dX, beta, lay, part, p, dev, stream, inject_stall);
+    case 2: return launch_smallt_t<WT, 2>(W, N, K, dY, T, dX, beta, lay, part, p, dev, stream, inject_stall);
+    case 4: return launch_smallt_t<WT, 4>(W, N, K, dY, T, dX, beta, lay, part, p, dev, stream, inject_stall);
+    default: return launch_smallt_t<WT, 8>(W, N, K, dY, T, dX, beta, lay, part, p, dev, stream, inject_stall);
   }
 }
 
 cudaError_t launch_smallt(int wtype, const void* W, int64_t N, int64_t K, const float* dY,
                           int64_t T, float* dX, float beta, const Layout& lay, float* part,
-                          const SmalltPlan& p, const DevInfo& dev, cudaStream_t stream) {
+                          const SmalltPlan& p, const DevInfo& dev, cudaStream_t stream,
+                          int inject_stall) {
   if (p.n_tchunks > 65535 || p.n_splits > 65535) return cudaErrorInvalidConfiguration;
   const cudaError_t e = with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
-    return launch_smallt_w<decltype(wt)::value>(W, N, K, dY, T, dX, beta, lay, part, p, dev, stream);
+    return launch_smallt_w<decltype(wt)::value>(W, N, K, dY, T, dX, beta, lay, part, p, dev, stream,
+                                                inject_stall);
   });
   if (e != cudaSuccess || p.n_splits == 1) return e;  // one slice: the kernel wrote dX
   return launch_reduce_partials(part, p.n_splits, T, K, dX, lay.dx_t, beta, dev, stream);

@@ -285,6 +285,54 @@ def test_timeout_probe_reports_and_context_survives(rg):
                   oracle.abs_bound(dY, Wd), 5e-3)
 
 
+_STALL_CHILD = r"""
+import sys
+import numpy as np
+import torch
+sys.path[:0] = sys.argv[1:3]
+import oracle
+from quantized_weight_out_gb300 import binding as rg, inputs
+rg.load()
+dev, s = torch.device("cuda:0"), torch.cuda.current_stream()
+def call(variant, wtype, N, K, T):
+    W = inputs.gen_weight(wtype, N, K, seed=8, stream=1)
+    dY = inputs.normal_f32(8, 2, T * N, 1e-3).reshape(T, N)
+    dX = torch.empty((T, K), device=dev)
+    rg.check(rg.rg_out_prod_variant(variant, wtype, torch.from_numpy(W).to(dev), N, K,
+                                    torch.from_numpy(dY).to(dev), T, dX, 0.0, s))
+    return W, dY, dX
+# the three small-T consumers: Q4_K (MMA, row splits), Q8_0 (a row per lane,
+# one slice), F16 (eight values a lane)
+for wtype, N, K, T in ((inputs.Q4_K, 1000, 512, 1), (inputs.Q8_0, 200, 256, 2),
+                       (inputs.F16, 300, 256, 5)):
+    call(2, wtype, N, K, T)
+    st = rg.rg_check(s)
+    assert st == rg.RG_ERR_TIMEOUT, (wtype, st)
+W, dY, dX = call(3, inputs.Q8_0, 64, 256, 6)  # the SIMT variant waits on nothing
+assert rg.rg_check(s) == rg.RG_OK
+Wd = oracle.dequant(inputs.Q8_0, W, 64, 256)
+err = np.abs(dX.cpu().numpy() - oracle.out_prod(inputs.Q8_0, W, 64, 256, dY, 6, Wd=Wd))
+assert np.all(err <= 1e-5 * oracle.abs_bound(dY, Wd) + 1e-7)
+print("stall ok")
+"""
+
+
+def test_small_t_stalled_stage_times_out_and_context_survives(rg):
+    """A child process whose small-T producers skip their first stage
+    (RG_DEBUG_INJECT_STALL, with a 300 ms wait limit): every consumer's wait
+    runs out, all warps leave together, rg_check reports RG_ERR_TIMEOUT for
+    each consumer kind, and the context still computes exactly afterwards.
+    No fault: the stage is a flag that nothing sets."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, RG_DEBUG_INJECT_STALL="1", RG_WAIT_TIMEOUT_MS="300")
+    r = subprocess.run([sys.executable, "-c", _STALL_CHILD, root, os.path.join(root, "tests")],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "stall ok" in r.stdout, (r.stdout[-2000:], r.stderr[-2000:])
+
+
 @pytest.mark.parametrize("variant", [1, 4, 5])
 @pytest.mark.parametrize("wtype", TYPES)
 @pytest.mark.parametrize("beta", [0.0, 1.0])
