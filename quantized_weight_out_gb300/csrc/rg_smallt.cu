@@ -848,7 +848,7 @@ __device__ __forceinline__ void consume_q4k_mma(int warp, int lane, const uint8_
 // A producer warp streams the CTA's rows of W, tile by tile of BR rows, into
 // an 8-stage ring with TMA; eight consumer warps decode from shared memory.
 template <int WT, int TB>
-__global__ void __launch_bounds__(THREADS + 32, mma_path<WT, TB>() ? (TB <= 2 ? 4 : TB == 4 ? 3 : 2)
+__global__ void __launch_bounds__(THREADS + 32, mma_path<WT, TB>() ? (TB <= 4 ? 3 : 2)
                                                 : rows_path<WT, TB>() && TB == 1 ? 3
                                                 : TB >= 8                        ? 1
                                                                                  : 2)
