@@ -630,8 +630,8 @@ __device__ __forceinline__ void consume_rows(int g, const uint8_t* stage_buf, co
 
 // --- Q4_K, one to eight rows of dY: the warp-level tensor-core MMA ---------
 // mma.m16n8k16 computes D[k][t] += sum over 16 rows n of A[k][n] * B[n][t]
-// with A = the nibbles q of W (an fp16 register holds rows n and n + 1 of
-// one column k) and B = fp16(y * 2^s * d * sc), the dY row t times the
+// with A = the nibbles q of W (a 32-bit register holds the fp16 values of
+// rows n and n + 1 in one column k) and B = fp16(y * 2^s * d * sc), the dY row t times the
 // sub-block's scale; the min term sum_n y * dmin * m stays in F32.
 //  * A nibble q in the low bits of an fp16 is the subnormal q * 2^-24,
 //    exactly; a high nibble left in place is 16q * 2^-24.  So the operand
@@ -698,7 +698,7 @@ __device__ __forceinline__ void consume_q4k_mma(int warp, int lane, const uint8_
                                                 int split, SmtOut out, WaitCtl ctl,
                                                 volatile int* abort_flag) {
   constexpr int TBYTES = 144;  // Q4_K super-block: d, dmin, 12 scale bytes, 128 nibble bytes
-  static_assert(BR % 16 == 0 && BR == 64, "64-row stages: one scale-pass thread per (row, q)");
+  static_assert(BR == 64, "64-row stages: one scale-pass thread per (row, q), four MMA row groups");
   uint16_t* yds = reinterpret_cast<uint16_t*>(aux);
   float* mred = reinterpret_cast<float*>(aux + 2 * yds_elems<TB>());
   int* smax = reinterpret_cast<int*>(mred + CONSUMERS * 4 * 2 * TB);
