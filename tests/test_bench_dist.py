@@ -70,3 +70,17 @@ def test_reference_arm_prints_on_rank0_only(tmp_path):
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_cpu_sample_takes_the_rows_a_call_has():
+    """The CPU baseline's sample asks for 1024 rows of dY; a call with fewer
+    (the Q8_0 256x256, T = 32 workload) contributes all of its rows, and the
+    one-shot baseline repeats so tiny a sample until a second has passed
+    (the reference arm's per-step sample runs once)."""
+    import bench
+    from quantized_weight_out_gb300 import inputs
+    wl = inputs.WORKLOADS["q8_0_256x256_t32"]
+    f, dt, desc = bench.oracle_sample(wl, 1024)
+    assert f == 2 * 32 * 256 * 256 and "1 pass" in desc
+    f, dt, desc = bench.oracle_sample(wl, 1024, min_seconds=0.2)
+    assert dt >= 0.2 and f % (2 * 32 * 256 * 256) == 0 and f > 2 * 32 * 256 * 256
