@@ -11,11 +11,15 @@ ABI with inputs resident in HBM.  Prints one JSON line (rank 0).
   e2e         the same with host inputs: pinned host -> device copies of W
               and dY and the device -> host copy of dX inside the timed loop
   roofline    the tensor-core kernel's achieved TFLOP/s over the measured
-              dense bf16/fp16 peak (MEASURED_PEAKS.json, sustained figure)
+              dense bf16/fp16 peak (MEASURED_PEAKS.json: the burst figure,
+              or the sustained one for a seconds-long region under the power
+              cap), and the whole step's fraction of the same peak
+  per_config  the method's other workloads, one call each, with their
+              roofline fractions (default workload only; --no-configs)
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
 
 --impl reference times the CPU oracle itself (the only baseline this method
-has; its pages publish no GPU throughput) on a bounded sample per step.
+has; its pages publish no GPU throughput) on the same sample per step.
 Multi-GPU (torchrun): every rank runs its own replica of the workload
 (replicas only: the calls are independent); the step time is the max over
 ranks.
@@ -38,6 +42,7 @@ sys.path.insert(0, ROOT)
 from quantized_weight_out_gb300 import inputs  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
+METRIC = "out_prod TFLOP/s (2*T*N*K / time)"
 
 
 def _traffic_record():
@@ -165,7 +170,7 @@ def oracle_sample(problems, t_rows: int, n_rows: int | None = None, min_seconds:
 # ---------------------------------------------------------------------------
 # the route the method replaces: a dense F32 copy of W, then a full-F32 GEMM
 
-def second_reference(torch, rg, problems, devbuf, stream, dev, flush_buf, reps: int = 5):
+def second_reference(torch, rg, problems, devbuf, stream, dev, flush, reps: int = 5):
     """Time rg_dequant into a dense F32 [N, K] buffer followed by cuBLAS SGEMM
     (TF32 off) for every call of the workload, on the resident inputs.  dX
     buffers are overwritten (the timed leg has already run)."""
@@ -193,8 +198,8 @@ def second_reference(torch, rg, problems, devbuf, stream, dev, flush_buf, reps: 
         times, dq = [], []
         for r in range(2 + reps):
             for fn, out in ((one, times), (dequant_only, dq)):
-                if flush_buf is not None:
-                    flush_buf.fill_(0.0)
+                if flush is not None:
+                    flush()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
                 fn()
@@ -226,9 +231,11 @@ def parse():
                     help="out_prod (the backward, default), mul_mat (the forward rg_mul_mat) or "
                          "lora (the backward through W plus a low-rank adapter)")
     ap.add_argument("--rank", type=int, default=16, help="adapter rank of --op lora")
-    ap.add_argument("--cpu-rows", type=int, default=1024, help="dY rows per call, CPU baseline sample")
-    ap.add_argument("--ref-rows", type=int, default=32, help="dY rows per call, reference-arm step")
-    ap.add_argument("--ref-wrows", type=int, default=512, help="W rows per call, reference-arm step")
+    ap.add_argument("--cpu-rows", type=int, default=1024,
+                    help="dY rows per call of the CPU oracle's sample (the CPU baseline and the "
+                         "reference arm's step; fewer when steps + warm-ups exceed 60)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config block (the other workloads, one call each)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-second-ref", action="store_true",
@@ -278,33 +285,219 @@ def _dtype_name(problems):
         "f16" if all(p.wtype != inputs.BF16 for p in problems) else "f16+bf16"
 
 
+# The BASELINE-table configs the default JSON line also reports, one call
+# each (C1-C4 of the method's workloads, and one row of dY over the two
+# largest layer weights: the weight-streaming small-T path).
+PER_CONFIG = ["q8_0_256x256_t32", "q4_0_4096x4096_t512", "q4_k_14336x4096_t2048",
+              "f16_5120x17408_t4096_beta1", "bf16_5120x17408_t4096_beta1",
+              "smallt_q4_k_14336x4096_t1", "smallt_q8_0_4096x14336_t1"]
+
+
+def choose_peak(peaks: dict, clocks, timed_s: float):
+    """The dense tensor peak that matches how the timed region ran: the burst
+    figure (a short GEMM at full clock) unless the region lasted seconds with
+    the power cap active, which is how the sustained figure was measured.
+    Returns (TFLOP/s, which figure)."""
+    burst = float(peaks.get("bf16_tflops", peaks.get("bf16_tflops_sustained", 0.0)))
+    sustained = float(peaks.get("bf16_tflops_sustained", burst))
+    capped = bool(clocks) and "sw_power_cap" in (clocks.get("reasons") or [])
+    if timed_s >= 1.0 and capped:
+        return sustained, "bf16_tflops_sustained"
+    return burst, "bf16_tflops"
+
+
+def sample_rows(steps: int, warmup: int, full: int = 1024, budget_steps: int = 60) -> int:
+    """dY rows per call of the CPU oracle's sample: `full`, or fewer (a
+    multiple of 64, at least 64) when the reference arm's steps + warm-ups
+    would otherwise run past a few minutes (about 2 s a step at 1024 rows on
+    16 cores).  The reference arm and the CPU baseline take the same rows."""
+    n = steps + warmup
+    if n <= budget_steps:
+        return full
+    return max(64, (full * budget_steps // n) // 64 * 64)
+
+
+def _l2_policy(step_bytes: int) -> str:
+    if step_bytes >= 2 * L2_BYTES:
+        return f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step > 129 MB); no flush"
+    return (f"inputs fit in L2 ({step_bytes / 1e6:.1f} MB per step): between steps a "
+            f"{2 * L2_BYTES >> 20} MB write then a read of it leaves L2 holding clean lines; "
+            "step time = sum of the calls' event times")
+
+
+def workload_config(workload: str, problems, world: int) -> dict:
+    """The JSON line's `config`, the same for both arms."""
+    step_bytes = sum(p.algorithmic_bytes() for p in problems)
+    return {"workload": workload, "calls": len(problems),
+            "flops_per_step": sum(p.flops for p in problems),
+            "algorithmic_bytes_per_step": step_bytes, "l2": _l2_policy(step_bytes),
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
         return
     problems = inputs.WORKLOADS[args.workload]
-    rows = args.ref_rows
+    rows = sample_rows(args.steps, args.warmup, args.cpu_rows)
     for _ in range(args.warmup):
-        oracle_sample(problems, rows, args.ref_wrows)
+        oracle_sample(problems, rows)
     times, flops = [], 0
     for _ in range(args.steps):
-        f, dt, desc = oracle_sample(problems, rows, args.ref_wrows)
+        f, dt, desc = oracle_sample(problems, rows)
         times.append(dt)
         flops = f
     ms = 1e3 * sum(times) / len(times)
     value = flops / (ms * 1e-3) / 1e12
     cores = os.cpu_count()
-    line = {"impl": "reference", "metric": "out_prod TFLOP/s (2*T*N*K / time)", "value": value,
+    line = {"impl": "reference", "metric": METRIC, "value": value,
             "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "sample_rows_per_call": rows,
-                       "sample_w_rows_per_call": args.ref_wrows},
+            "config": workload_config(args.workload, problems, world),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+class L2Flush:
+    """Evicts L2 between timed steps: a write of twice its size, then a read
+    of the same buffer, so that the lines left behind are clean and a timed
+    call does not stream its inputs behind the write-back of dirty lines."""
+
+    def __init__(self, torch, dev):
+        self.torch = torch
+        self.buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def __call__(self, v: float = 0.0):
+        self.buf.fill_(v)
+        self.torch.sum(self.buf, (0,), keepdim=True, out=self.sink)
+
+
+def time_calls(torch, rg, problems, devbuf, steps: int, warmup: int, forced: int, stream, dev,
+               world: int) -> dict:
+    """Warm-up, then `steps` timed steps of every call of `problems` on its
+    resident buffers (W, dY, dX): events around every call and around its
+    tensor-core GEMM kernel (rg_profile_next_gemm), the library's launch
+    count over the region, nvidia-smi clocks sampled meanwhile.  Inputs that
+    fit in L2 are flushed between steps (outside the calls, whose event times
+    then make up the step time)."""
+    variants = [forced if forced else rg.rg_select_variant(p.wtype, p.N, p.K, p.T) for p in problems]
+    is_tc = [v in (rg.RG_VARIANT_TC, rg.RG_VARIANT_TC_SINGLE, rg.RG_VARIANT_TC_PAIR) for v in variants]
+    plans = []
+    for p in problems:
+        info = rg.rg_plan_info()
+        rg.check(rg.rg_plan(forced, p.wtype, p.N, p.K, p.T, info), "rg_plan")
+        plans.append(info.as_dict())
+    step_bytes = sum(p.algorithmic_bytes() for p in problems)
+    flush = L2Flush(torch, dev) if step_bytes < 2 * L2_BYTES else None
+
+    def call(p, W, dY, dX):
+        if forced:
+            return rg.rg_out_prod_variant(forced, p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, stream)
+        return rg.rg_out_prod(p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, stream)
+
+    def step(events=None):
+        for i, p in enumerate(problems):
+            W, dY, dX = devbuf[i]
+            if events is not None:
+                events[i][0].record(stream)
+                if is_tc[i]:  # the library records these around its GEMM kernel
+                    rg.rg_profile_next_gemm(events[i][2], events[i][3])
+            st = call(p, W, dY, dX)
+            if events is not None:
+                events[i][1].record(stream)
+            if st != 0:
+                raise RuntimeError(f"{p.name}: {rg.strerror(st)}")
+
+    for _ in range(warmup):
+        step()
+        if flush is not None:
+            flush()
+    rg.check(rg.rg_check(stream), "warmup")
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in problems]
+           for _ in range(steps)]
+    # torch creates an event's handle at its first record; record every event
+    # once so the library gets real handles (its later records are the ones timed)
+    for row in evs:
+        for quad in row:
+            for e in quad:
+                e.record(stream)
+    sampler = ClockSampler(_bus_id(torch, dev))
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = rg.rg_launch_count()
+    ev0.record(stream)
+    for s in range(steps):
+        step(evs[s])
+        if flush is not None:
+            flush(float(s))
+    ev1.record(stream)
+    launches = rg.rg_launch_count() - launches0
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    rg.check(rg.rg_check(stream), "timed region")
+    per_call = [[evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(steps)]
+                for i in range(len(problems))]
+    per_gemm = [[evs[s][i][2].elapsed_time(evs[s][i][3]) for s in range(steps)] if is_tc[i] else []
+                for i in range(len(problems))]
+    ms_total = ev0.elapsed_time(ev1)
+    if flush is not None:
+        ms_total = sum(sum(c) for c in per_call)
+    planned = steps * sum(pl["launches"] for pl in plans)
+    if launches != planned:
+        raise RuntimeError(f"{launches} kernel launches in the timed region, the plans say {planned}")
+    return {"ms_total": ms_total, "per_call": per_call, "per_gemm": per_gemm, "launches": launches,
+            "clocks": clocks, "variants": variants, "is_tc": is_tc, "plans": plans,
+            "flush": flush, "step_bytes": step_bytes, "timed_s": ev0.elapsed_time(ev1) * 1e-3}
+
+
+def tc_launch_bytes(p) -> int:
+    """Algorithmic bytes of one tensor-core GEMM launch: the packed W, dY's
+    16-bit copy (2TN), dX written (4TK; read as well when beta != 0)."""
+    return p.w_bytes + 2 * p.T * p.N + 4 * p.T * p.K * (2 if p.beta != 0.0 else 1)
+
+
+def config_entry(torch, rg, workload: str, steps: int, warmup: int, stream, dev, peaks: dict) -> dict:
+    """One BASELINE config measured on its own (resident inputs, flushed L2
+    when they fit in it): time, TFLOP/s, effective GB/s and the fractions of
+    its roofline, max(2TNK / tensor peak, algorithmic bytes / HBM bandwidth)."""
+    problems = inputs.WORKLOADS[workload]
+    devbuf = []
+    for p in problems:
+        dX0 = p.dx0()
+        devbuf.append((torch.from_numpy(p.weight()).to(dev), torch.from_numpy(p.dy()).to(dev),
+                       torch.from_numpy(dX0).to(dev) if dX0 is not None
+                       else torch.zeros((p.T, p.K), device=dev)))
+    r = time_calls(torch, rg, problems, devbuf, steps, warmup, 0, stream, dev, 1)
+    peak, kind = choose_peak(peaks, r["clocks"], r["timed_s"])
+    hbm = float(peaks["hbm_gbs"])
+    p = problems[0]
+    t_ms = statistics.median(r["per_call"][0])
+    t = t_ms * 1e-3
+    e = {"workload": workload, "wtype": inputs.TYPE_NAMES[p.wtype], "N": p.N, "K": p.K, "T": p.T,
+         "beta": p.beta, "variant": int(r["variants"][0]), "plan": r["plans"][0], "steps": steps,
+         "ms": t_ms, "tflops": p.flops / t / 1e12, "effective_gbs": p.algorithmic_bytes() / t / 1e9,
+         "roofline_frac": max(p.flops / (peak * 1e12), p.algorithmic_bytes() / (hbm * 1e9)) / t,
+         "bound": "tensor" if p.flops / (peak * 1e12) >= p.algorithmic_bytes() / (hbm * 1e9) else "hbm",
+         "peak_tflops": peak, "peak_kind": kind, "hbm_gbs": hbm,
+         "l2": _l2_policy(r["step_bytes"]),
+         "sm_mhz": (r["clocks"] or {}).get("sm_mhz"), "clock_reasons": (r["clocks"] or {}).get("reasons")}
+    if r["is_tc"][0]:
+        g_ms = statistics.median(r["per_gemm"][0])
+        e["gemm_ms"] = g_ms
+        e["kernel_frac"] = p.flops / (g_ms * 1e-3) / 1e12 / peak
+        e["step_frac"] = p.flops / t / 1e12 / peak
+    del devbuf
+    torch.cuda.empty_cache()
+    return e
 
 
 def run_ours(args):
@@ -336,87 +529,19 @@ def run_ours(args):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     forced = rg.VARIANTS[args.variant]
-    variants = [forced if forced else rg.rg_select_variant(p.wtype, p.N, p.K, p.T) for p in problems]
+
+    r = time_calls(torch, rg, problems, devbuf, args.steps, args.warmup, forced, stream, dev, world)
+    per_call, per_gemm, is_tc, plans = r["per_call"], r["per_gemm"], r["is_tc"], r["plans"]
+    variants, clocks, launches, step_bytes = r["variants"], r["clocks"], r["launches"], r["step_bytes"]
+    ms_total = max_over_ranks(r["ms_total"], dev)
+    ms_step = ms_total / args.steps
+    flops_step = sum(p.flops for p in problems)
+    value = job_tflops(flops_step, ms_step, world)
 
     def call(p, W, dY, dX):
         if forced:
             return rg.rg_out_prod_variant(forced, p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, stream)
         return rg.rg_out_prod(p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, stream)
-
-    is_tc = [v in (rg.RG_VARIANT_TC, rg.RG_VARIANT_TC_SINGLE, rg.RG_VARIANT_TC_PAIR) for v in variants]
-    plans = []
-    for p in problems:
-        info = rg.rg_plan_info()
-        rg.check(rg.rg_plan(forced, p.wtype, p.N, p.K, p.T, info), "rg_plan")
-        plans.append(info.as_dict())
-
-    # inputs that fit in L2: a write of twice its size between steps, outside
-    # the timed calls (the step time is then the sum of the calls' own times)
-    step_bytes = sum(p.algorithmic_bytes() for p in problems)
-    flush_buf = None
-    if step_bytes < 2 * L2_BYTES:
-        flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-
-    def step(events=None):
-        for i, p in enumerate(problems):
-            W, dY, dX = devbuf[i]
-            if events is not None:
-                events[i][0].record(stream)
-                if is_tc[i]:  # the library records these around its GEMM kernel
-                    rg.rg_profile_next_gemm(events[i][2], events[i][3])
-            st = call(p, W, dY, dX)
-            if events is not None:
-                events[i][1].record(stream)
-            if st != 0:
-                raise RuntimeError(f"rg_out_prod: {rg.strerror(st)}")
-
-    for _ in range(args.warmup):
-        step()
-        if flush_buf is not None:
-            flush_buf.fill_(0.0)
-    rg.check(rg.rg_check(stream), "warmup")
-
-    per_call = [[] for _ in problems]
-    per_gemm = [[] for _ in problems]
-    sampler = ClockSampler(_bus_id(torch, dev))
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    sampler.start()
-    time.sleep(0.3)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)]
-            for _ in problems] for _ in range(args.steps)]
-    # torch creates an event's handle at its first record; record every event
-    # once so the library gets real handles (its later records are the ones timed)
-    for row in evs:
-        for quad in row:
-            for e in quad:
-                e.record(stream)
-    torch.cuda.synchronize()
-    launches0 = rg.rg_launch_count()
-    ev0.record(stream)
-    for s in range(args.steps):
-        step(evs[s])
-        if flush_buf is not None:
-            flush_buf.fill_(float(s))
-    ev1.record(stream)
-    launches = rg.rg_launch_count() - launches0
-    torch.cuda.synchronize()
-    clocks = sampler.stop()
-    rg.check(rg.rg_check(stream), "timed region")
-    ms_total = ev0.elapsed_time(ev1)
-    for s in range(args.steps):
-        for i in range(len(problems)):
-            per_call[i].append(evs[s][i][0].elapsed_time(evs[s][i][1]))
-            if is_tc[i]:
-                per_gemm[i].append(evs[s][i][2].elapsed_time(evs[s][i][3]))
-    if flush_buf is not None:
-        ms_total = sum(sum(c) for c in per_call)
-    ms_total = max_over_ranks(ms_total, dev)
-    ms_step = ms_total / args.steps
-    flops_step = sum(p.flops for p in problems)
-    value = job_tflops(flops_step, ms_step, world)
 
     # end to end: host buffers, copies inside the timed loop
     e2e = None
@@ -475,7 +600,7 @@ def run_ours(args):
 
     # roofline of the tensor-core launches (the dominant kernel)
     peaks, src = _peaks()
-    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    peak, peak_kind = choose_peak(peaks, clocks, r["timed_s"])
     traffic, traffic_wl = _traffic_record()
     if traffic_wl is not None and traffic_wl != args.workload:
         traffic = None
@@ -484,10 +609,16 @@ def run_ours(args):
     gemm_ms = sum(statistics.mean(per_gemm[i]) for i in tc) if tc else 0.0
     call_ms = sum(statistics.mean(per_call[i]) for i in tc) if tc else 0.0
     achieved = tc_flops / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None
+    alg_launch = sum(tc_launch_bytes(problems[i]) for i in tc) / max(1, len(tc))
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak if achieved else None, "traffic": traffic,
+            "frac": achieved / peak if achieved else None,
+            "step_frac": value / world / peak if all(is_tc) else None,
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": alg_launch,
+            "traffic_ratio": traffic / alg_launch if traffic and alg_launch else None,
             "traffic_unit": "bytes per launch (ncu dram read+write, profiles/tc_traffic.json)",
-            "peak_source": f"{src} bf16_tflops_sustained (dense fp16 = bf16 nominal)",
+            "peak_source": f"{src} {peak_kind} (dense fp16 = bf16 nominal); the burst figure unless "
+                           "the timed region lasted seconds under sw_power_cap",
             "kernel": "out_prod_tc_kernel (fused decode + tcgen05 GEMM), events around each launch",
             "launches_per_step": len(tc), "flops_per_launch": tc_flops / max(1, len(tc)),
             "ms_per_launch": gemm_ms / max(1, len(tc)),
@@ -520,35 +651,34 @@ def run_ours(args):
                                            p.algorithmic_bytes() / (peaks["hbm_gbs"] * 1e9)) / t})
 
     second = None if args.no_second_ref else second_reference(torch, rg, problems, devbuf, stream,
-                                                                   dev, flush_buf)
+                                                                   dev, r["flush"])
     if second is not None:
         second["ms_per_step"] = max_over_ranks(second["ms_per_step"], dev)
         second["value"] = job_tflops(flops_step, second["ms_per_step"], world)
 
+    per_config = None
+    if world == 1 and not args.no_configs and args.workload == "layer7b_t8192" and not forced:
+        del host, devbuf
+        torch.cuda.empty_cache()
+        per_config = [config_entry(torch, rg, wl, min(args.steps, 50), max(args.warmup, 3), stream,
+                                   dev, peaks) for wl in PER_CONFIG]
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        f, dt, desc = oracle_sample(problems, args.cpu_rows, min_seconds=1.0)
+        f, dt, desc = oracle_sample(problems, sample_rows(args.steps, args.warmup, args.cpu_rows),
+                                    min_seconds=10.0)
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
                "kind": "oracle", "sample": desc, "seconds": dt}
 
-    planned = args.steps * sum(pl["launches"] for pl in plans)
-    if launches != planned:
-        raise RuntimeError(f"{launches} kernel launches in the timed region, the plans say {planned}")
-    l2 = (f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step > 129 MB); no flush"
-          if flush_buf is None else
-          f"inputs fit in L2 ({step_bytes / 1e6:.1f} MB per step): a {2 * L2_BYTES >> 20} MB write "
-          "between steps flushes it; step time = sum of the calls' event times")
     line = {
-        "metric": "out_prod TFLOP/s (2*T*N*K / time)", "value": value, "unit": "TFLOP/s",
+        "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": _dtype_name(problems), "data": "synthetic",
-        "config": {"workload": args.workload, "calls": len(problems),
-                   "flops_per_step": flops_step, "algorithmic_bytes_per_step": step_bytes,
-                   "l2": l2, "parallelism": f"replicas x{world}"},
+        "config": workload_config(args.workload, problems, world),
         "effective_gbs": world * step_bytes / (ms_step * 1e-3) / 1e9,
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-        "clocks": clocks, "second_reference": second, "per_call": calls,
+        "clocks": clocks, "second_reference": second, "per_call": calls, "per_config": per_config,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -642,7 +772,7 @@ def run_mul_mat(args):
                                                                 stream, dev, world)
     flops_step = sum(p.flops for p in problems)
     peaks, src = _peaks()
-    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    peak, peak_kind = choose_peak(peaks, clocks, ms_step * args.steps * 1e-3)
     achieved = flops_step / (gemm_ms * 1e-3) / 1e12
     calls = [{"name": p.name, "wtype": inputs.TYPE_NAMES[p.wtype], "N": p.N, "K": p.K, "T": p.T,
               "ms": t, "tflops": p.flops / (t * 1e-3) / 1e12} for p, t in zip(problems, per_call)]
@@ -655,7 +785,7 @@ def run_mul_mat(args):
                        "flops_per_step": flops_step, "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": None,
-                         "peak_source": f"{src} bf16_tflops_sustained",
+                         "peak_source": f"{src} {peak_kind}",
                          "kernel": "out_prod_tc_kernel on the transposed 16-bit copy of deq(W)"},
             "gpu_launches": launches, "clocks": clocks, "per_call": calls}
     if rank == 0:
@@ -696,7 +826,7 @@ def run_lora(args):
     flops = [p.flops + 2 * p.T * R * (p.N + p.K) for p in problems]
     flops_step = sum(flops)
     peaks, src = _peaks()
-    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    peak, peak_kind = choose_peak(peaks, clocks, ms_step * args.steps * 1e-3)
     # the main kernel's tensor work: the base product plus the adapter's
     # chunks (64 * ceil(r / 64) extra contraction rows)
     gemm_flops = sum(2 * p.T * p.K * (p.N + 64 * ((R + 63) // 64)) for p in problems)
@@ -716,7 +846,7 @@ def run_lora(args):
                           "adapter_overhead": ms_step / base_ms - 1.0},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": None,
-                         "peak_source": f"{src} bf16_tflops_sustained",
+                         "peak_source": f"{src} {peak_kind}",
                          "kernel": "out_prod_tc_kernel with the adapter's chunks"},
             "gpu_launches": launches, "clocks": clocks, "per_call": calls}
     if rank == 0:

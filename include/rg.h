@@ -38,6 +38,8 @@
  *    (16-byte aligned rows).
  *  - Every device-side wait is bounded (about 2 s); a wait that gives up
  *    records RG_ERR_TIMEOUT in a per-device status word that rg_check reads.
+ *    The outputs of a call whose kernels gave up are undefined (partly
+ *    written); the context stays usable.
  */
 #ifndef RG_H
 #define RG_H
@@ -101,7 +103,11 @@ typedef enum {
                             K % 512 != 0, on a tensor-core or small-T variant                */
     RG_ERR_ALIGN = -4,   /* W, dY, dX or out not 16-byte aligned                           */
     RG_ERR_CUDA = -5,    /* a CUDA runtime/driver call or a launch failed                  */
-    RG_ERR_TIMEOUT = -6  /* a bounded device-side wait gave up (reported by rg_check)      */
+    RG_ERR_TIMEOUT = -6, /* a bounded device-side wait gave up (reported by rg_check)      */
+    RG_ERR_RANGE = -7    /* a finite dY value lay outside the 16-bit operand kind's range
+                            (fp16: |dY| >= 65520) and became inf in the tensor-core
+                            operand copy: the call's dX holds inf or NaN (reported by
+                            rg_check; rerun with RG_VARIANT_SIMT32 or a scaled dY)       */
 } rg_status;
 
 /* Kernel variants of rg_out_prod_variant. */
@@ -327,7 +333,11 @@ const char* rg_strerror(int status);
 
 /* Synchronizes `stream`, then reads and clears the current device's status
  * word.  Returns RG_ERR_TIMEOUT if a kernel gave up a bounded wait since the
- * last check, RG_ERR_CUDA if the stream reports an error, else RG_OK. */
+ * last check, RG_ERR_RANGE if a dY value overflowed the tensor-core operand
+ * kind since the last check (the conversion of dY checks every value; the
+ * decoded weight values' fp16 range is a precondition of the quantized and
+ * F16 types, not checked), RG_ERR_CUDA if the stream reports an error, else
+ * RG_OK.  The first error recorded since the last check wins. */
 int rg_check(void* stream);
 
 /* Library version, (major << 16) | minor. */

@@ -18,7 +18,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "librg.so")
 
 RG_OK, RG_ERR_ARG, RG_ERR_TYPE, RG_ERR_SHAPE = 0, -1, -2, -3
-RG_ERR_ALIGN, RG_ERR_CUDA, RG_ERR_TIMEOUT = -4, -5, -6
+RG_ERR_ALIGN, RG_ERR_CUDA, RG_ERR_TIMEOUT, RG_ERR_RANGE = -4, -5, -6, -7
 RG_VARIANT_AUTO, RG_VARIANT_TC, RG_VARIANT_SMALLT, RG_VARIANT_SIMT32 = 0, 1, 2, 3
 RG_VARIANT_TC_SINGLE, RG_VARIANT_TC_PAIR = 4, 5
 VARIANTS = {"auto": 0, "tc": 1, "smallt": 2, "simt32": 3, "tc1": 4, "tc2": 5}

@@ -296,7 +296,7 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
     e = launch_tc(wtc, Wtc, N, K, static_cast<const uint16_t*>(buf), ld, T, dX, lay.dx_t, beta,
                   reinterpret_cast<float*>(static_cast<char*>(buf) +
                                            tc_partial_offset(wtype, N, K, T)),
-                  *dev, stream, cg_force_of(variant), env().inject_stall);
+                  *dev, stream, cg_force_of(variant));
   if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, stream);
   if (own_ws) {
     const cudaError_t f = cudaFreeAsync(buf, stream);
@@ -541,8 +541,7 @@ int rg_mul_mat(int wtype, const void* W, int64_t N, int64_t K, const float* X, i
   t_prof_before = t_prof_after = nullptr;
   if (e == cudaSuccess && ev0) e = cudaEventRecord(ev0, s);
   if (e == cudaSuccess)
-    e = launch_tc(bf16 ? RG_BF16 : RG_F16, wt, K, N, xh, ld, T, Y, N, beta, part, *dev, s, 0,
-                  env().inject_stall);
+    e = launch_tc(bf16 ? RG_BF16 : RG_F16, wt, K, N, xh, ld, T, Y, N, beta, part, *dev, s, 0);
   if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, s);
   const cudaError_t f = cudaFreeAsync(buf, s);
   if (e == cudaSuccess) e = f;
@@ -629,7 +628,7 @@ int rg_out_prod_lora(int variant, int wtype, const void* W, int64_t N, int64_t K
     if (e == cudaSuccess) e = launch_convert_dy(lora_b, N, rank, rank, 1, r8, bf16, b16, *dev, s);
     if (e == cudaSuccess)
       e = launch_tc(bf16 ? RG_BF16 : RG_F16, b16, N, r8, dy16, ld, T, u32, r8, 0.0f, part, *dev,
-                    s, 0, 0);
+                    s, 0);
     if (e == cudaSuccess) e = launch_adapter_pack(u32, r8, T, rank, N, ld, bf16, dy16, *dev, s);
   }
   const void* Wtc = W;
@@ -644,8 +643,7 @@ int rg_out_prod_lora(int variant, int wtype, const void* W, int64_t N, int64_t K
   t_prof_before = t_prof_after = nullptr;
   if (e == cudaSuccess && ev0) e = cudaEventRecord(ev0, s);
   if (e == cudaSuccess)
-    e = launch_tc(wtc, Wtc, N, K, dy16, ld, T, dX, K, beta, part, *dev, s, cg, env().inject_stall,
-                  a16, rank);
+    e = launch_tc(wtc, Wtc, N, K, dy16, ld, T, dX, K, beta, part, *dev, s, cg, a16, rank);
   if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, s);
   const cudaError_t f = cudaFreeAsync(buf, s);
   return from_cuda(e == cudaSuccess ? f : e);
@@ -736,6 +734,8 @@ const char* rg_strerror(int status) {
     case RG_ERR_ALIGN: return "pointer not 16-byte aligned (workspace: 256-byte)";
     case RG_ERR_CUDA: return "CUDA call or kernel launch failed";
     case RG_ERR_TIMEOUT: return "a bounded device-side wait gave up";
+    case RG_ERR_RANGE:
+      return "a dY value lay outside the 16-bit tensor-core operand range (fp16: |dY| >= 65520)";
     default: return "unknown status";
   }
 }

@@ -173,11 +173,12 @@ cudaError_t launch_dequant(int wtype, const void* W, int64_t N, int64_t K, float
 template <bool BF16>
 __global__ void __launch_bounds__(256) convert_dy_kernel(const float* __restrict__ dY, int64_t T,
                                                          int64_t N, int64_t ld, float mul,
-                                                         uint16_t* __restrict__ out) {
+                                                         uint16_t* __restrict__ out, int* status) {
   pdl_launch_dependents();  // the tensor-core kernel may be scheduled now (it waits for us)
   const int64_t cpr = (N + 7) >> 3;
   const int64_t total = T * cpr;
   const bool vec = (N & 3) == 0;
+  bool over = false;
   for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
        g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t t = g / cpr;
@@ -205,9 +206,11 @@ __global__ void __launch_bounds__(256) convert_dy_kernel(const float* __restrict
         const __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
         w[i] = *reinterpret_cast<const uint32_t*>(&h);
       }
+      over |= overflowed16<BF16>(v[2 * i], w[i] & 0xFFFFu) | overflowed16<BF16>(v[2 * i + 1], w[i] >> 16);
     }
     *reinterpret_cast<uint4*>(out + t * ld + n0) = make_uint4(w[0], w[1], w[2], w[3]);
   }
+  if (over) report_range(status);
 }
 
 // Strided dY (a row stride other than N, or a column stride other than 1,
@@ -218,7 +221,8 @@ template <bool BF16>
 __global__ void __launch_bounds__(256) convert_dy_tiled_kernel(const float* __restrict__ dY,
                                                                int64_t T, int64_t N, int64_t dy_t,
                                                                int64_t dy_n, int64_t ld,
-                                                               uint16_t* __restrict__ out) {
+                                                               uint16_t* __restrict__ out,
+                                                               int* status) {
   pdl_launch_dependents();  // the tensor-core kernel may be scheduled now (it waits for us)
   __shared__ float tile[32][33];  // [t][n]
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
@@ -235,20 +239,25 @@ __global__ void __launch_bounds__(256) convert_dy_tiled_kernel(const float* __re
       tile[tx][a] = v;
   }
   __syncthreads();
+  bool over = false;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int a = ty + 8 * j;
     const int64_t t = t0 + a, n = n0 + tx;
     if (t < T && n < N) {
+      uint16_t bits;
       if constexpr (BF16) {
         const __nv_bfloat16 h = __float2bfloat16_rn(tile[a][tx]);
-        out[t * ld + n] = *reinterpret_cast<const uint16_t*>(&h);
+        bits = *reinterpret_cast<const uint16_t*>(&h);
       } else {
         const __half h = __float2half_rn(tile[a][tx]);
-        out[t * ld + n] = *reinterpret_cast<const uint16_t*>(&h);
+        bits = *reinterpret_cast<const uint16_t*>(&h);
       }
+      out[t * ld + n] = bits;
+      over |= overflowed16<BF16>(tile[a][tx], bits);
     }
   }
+  if (over) report_range(status);
 }
 
 cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t dy_t, int64_t dy_n,
@@ -260,16 +269,18 @@ cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t dy_
     if (gy > 65535) return cudaErrorInvalidConfiguration;
     const dim3 grid(static_cast<unsigned>((N + 31) / 32), static_cast<unsigned>(gy));
     if (bf16)
-      convert_dy_tiled_kernel<true><<<grid, 256, 0, stream>>>(dY, T, N, dy_t, dy_n, ld, out);
+      convert_dy_tiled_kernel<true><<<grid, 256, 0, stream>>>(dY, T, N, dy_t, dy_n, ld, out,
+                                                              dev.status);
     else
-      convert_dy_tiled_kernel<false><<<grid, 256, 0, stream>>>(dY, T, N, dy_t, dy_n, ld, out);
+      convert_dy_tiled_kernel<false><<<grid, 256, 0, stream>>>(dY, T, N, dy_t, dy_n, ld, out,
+                                                               dev.status);
     return counted(cudaGetLastError());
   }
   const int grid = grid_for(T * ((N + 7) >> 3), 256, dev);
   if (bf16)
-    convert_dy_kernel<true><<<grid, 256, 0, stream>>>(dY, T, N, ld, mul, out);
+    convert_dy_kernel<true><<<grid, 256, 0, stream>>>(dY, T, N, ld, mul, out, dev.status);
   else
-    convert_dy_kernel<false><<<grid, 256, 0, stream>>>(dY, T, N, ld, mul, out);
+    convert_dy_kernel<false><<<grid, 256, 0, stream>>>(dY, T, N, ld, mul, out, dev.status);
   return counted(cudaGetLastError());
 }
 

@@ -66,6 +66,18 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 __device__ __forceinline__ void report_timeout(int* status) {
   atomicCAS(status, 0, (int)RG_ERR_TIMEOUT);
 }
+__device__ __forceinline__ void report_range(int* status) {
+  atomicCAS(status, 0, (int)RG_ERR_RANGE);
+}
+
+// Whether the finite F32 value v became +-inf when rounded to the 16-bit
+// operand kind (bits16: fp16, or bf16 when BF16): a value beyond the kind's
+// range (fp16: |v| >= 65520), which the tensor cores would carry as inf.
+template <bool BF16>
+__device__ __forceinline__ bool overflowed16(float v, uint32_t bits16) {
+  constexpr uint32_t INF = BF16 ? 0x7F80u : 0x7C00u;
+  return (bits16 & 0x7FFFu) == INF && fabsf(v) <= 3.40282347e38f;  // false for NaN and inf
+}
 
 // fp16 bits -> F32 (exact: every binary16 value is a float32).
 __device__ __forceinline__ float f16_to_f32(uint16_t h) {

@@ -196,7 +196,7 @@ int64_t tc_dy16_ld(int64_t N);
 // of the adapter's projected dY and zeros to the next multiple of 64.
 cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
                       int64_t ld_dy16, int64_t T, float* dX, int64_t dx_t, float beta, float* part,
-                      const DevInfo& dev, cudaStream_t stream, int cg_force, int inject_stall,
+                      const DevInfo& dev, cudaStream_t stream, int cg_force,
                       const uint16_t* a16 = nullptr, int64_t rank = 0);
 int64_t tc_adapter_cols(int64_t N, int64_t rank);
 // Number of partial-sum slabs the tensor-core plan needs (0 when unsplit).

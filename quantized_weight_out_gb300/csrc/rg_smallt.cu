@@ -638,9 +638,13 @@ __device__ __forceinline__ void consume_rows(int g, const uint8_t* stage_buf, co
 //    pair of two rows costs one byte permute (one byte of each row) and one
 //    AND per nibble, 0.75 integer instructions a value, against about 2.5
 //    for an F32 value; the MMA takes the multiply-adds off the FMA pipe.
-//  * 2^s puts max|y| of the CTA's slice in [2, 4), so y * d * sc stays in
-//    fp16's normal range wherever d * sc * q does (the tensor-core variant's
-//    precondition); the result is scaled back exactly.
+//  * 2^s puts max|y| of the CTA's slice in [2, 4), so the largest row's
+//    y * d * sc stays in fp16's range wherever d * sc * q does (the
+//    tensor-core variant's precondition); the result is scaled back exactly.
+//    Rows whose |y| lies many octaves below the slice's maximum give fp16
+//    subnormal operands and keep fewer significant bits: a term q * y * d * sc
+//    then carries an absolute error up to q * 2^-25 * 2^-s, which the
+//    bound's sum of |y| |deq W| covers through the slice's large rows.
 //  * Warp w owns the 32 columns k = 64 (w >> 1) + 32 h + 4 g + 2 (w & 1) + j
 //    (g = 0..7, h, j = 0, 1): bytes 2 (w & 1) and 2 (w & 1) + 1 of word g
 //    of the 64-value chunk w >> 1, both nibbles, i.e. two accumulator tiles.
@@ -741,6 +745,7 @@ __device__ __forceinline__ void consume_q4k_mma(int warp, int lane, const uint8_
   float msum[TB][2];
 #pragma unroll
   for (int t = 0; t < TB; ++t) msum[t][0] = msum[t][1] = 0.0f;
+  bool aborted = false;  // taken by every consumer warp alike
 
   for (int i = 0; i < n_tiles; ++i) {
     const int s = i % STAGES_;
@@ -774,7 +779,10 @@ __device__ __forceinline__ void consume_q4k_mma(int warp, int lane, const uint8_
     }
     // every consumer warp arrives, with or without its stage, and all take
     // the same abort decision
-    if (consumers_sync_any(!ok || *abort_flag != 0)) break;
+    if (consumers_sync_any(!ok || *abort_flag != 0)) {
+      aborted = true;
+      break;
+    }
     const uint8_t* wq = stage + 16 + 32 * c4 + 4 * g;
 #pragma unroll
     for (int grp = 0; grp < BR / 16; ++grp) {
@@ -798,6 +806,9 @@ __device__ __forceinline__ void consume_q4k_mma(int warp, int lane, const uint8_
     if (lane == 0) mbar_arrive(bar0 + 8u * (STAGES_ + s));
   }
 
+  // a wait that gave up: no partial sums reach `out` (all consumer warps
+  // leave here together, so the named barriers below stay matched)
+  if (aborted) return;
   // the min terms of each sub-block over the slice's rows, in a fixed order:
   // lanes of one q (xor 4, 8, 16), then the eight warps
 #pragma unroll

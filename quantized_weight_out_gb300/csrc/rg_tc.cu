@@ -83,16 +83,16 @@ TcPlan plan_tc(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force
 
 cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
                       int64_t ld_dy16, int64_t T, float* dX, int64_t dx_t, float beta, float* part,
-                      const DevInfo& dev, cudaStream_t stream, int cg_force, int inject_stall,
-                      const uint16_t* a16, int64_t rank) {
+                      const DevInfo& dev, cudaStream_t stream, int cg_force, const uint16_t* a16,
+                      int64_t rank) {
   if (rank > 0)
     return launch_tc_adapter(wtype, W, N, K, dy16, ld_dy16, T, dX, dx_t, beta, part, dev, stream,
-                             cg_force, inject_stall, a16, rank);
+                             cg_force, a16, rank);
   if (plan_tc(N, K, T, dev, cg_force).sk)
     return launch_tc_stream_k(wtype, W, N, K, dy16, ld_dy16, T, dX, dx_t, beta, part, dev, stream,
-                              cg_force, inject_stall);
+                              cg_force);
   return launch_tc_impl<false, false>(wtype, W, N, K, dy16, ld_dy16, T, dX, dx_t, beta, part, dev,
-                                      stream, cg_force, inject_stall, nullptr, 0);
+                                      stream, cg_force, nullptr, 0);
 }
 
 // Warp slices of the shared tiles: slice (x, req) is tile x (item n_dp + x

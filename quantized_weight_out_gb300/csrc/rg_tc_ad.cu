@@ -7,9 +7,9 @@ namespace rg {
 cudaError_t launch_tc_adapter(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
                               int64_t ld_dy16, int64_t T, float* dX, int64_t dx_t, float beta,
                               float* part, const DevInfo& dev, cudaStream_t stream, int cg_force,
-                              int inject_stall, const uint16_t* a16, int64_t rank) {
-  return launch_tc_impl<true, false>(wtype, W, N, K, dy16, ld_dy16, T, dX, dx_t, beta, part, dev, stream,
-                              cg_force, inject_stall, a16, rank);
+                              const uint16_t* a16, int64_t rank) {
+  return launch_tc_impl<true, false>(wtype, W, N, K, dy16, ld_dy16, T, dX, dx_t, beta, part, dev,
+                                     stream, cg_force, a16, rank);
 }
 
 }  // namespace rg

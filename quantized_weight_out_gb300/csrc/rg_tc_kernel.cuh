@@ -697,7 +697,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                        const __grid_constant__ CUtensorMap map_l, int n_main,
                        float* __restrict__ dX, int64_t ldx, float beta, int T, int K,
                        int n_kunits, int n_ttiles, int band, int n_chunks, int n_splits,
-                       float* __restrict__ part, WaitCtl ctl, int inject_stall) {
+                       float* __restrict__ part, WaitCtl ctl) {
   using C = Cfg<WT, CG, BT>;
   constexpr int S = C::S;
   extern __shared__ uint8_t smem_raw[];
@@ -798,7 +798,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t ph = 0;
     uint32_t pend_p = 0, pend_ab = 0, pend_ph = 0;  // stages with copies in flight
     bool ok = true;
-    bool skip_first = inject_stall != 0;
     Segs<SK> sg(unit, n_units, n_tiles, n_chunks);
     int tile = 0, c0 = 0, c1 = 0;
     while (ok && sg.next(tile, c0, c1)) {
@@ -812,68 +811,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) break;
         if (lane == 0) {
           const uint32_t abar = ab_bar_leader + 8u * s;
-          if (skip_first) {
-            skip_first = false;  // fault injection: this stage never fills
-          } else {
-            const int gc = cbase + c;  // the contraction chunk
-            if constexpr (!AD) {
-              if (leader) {
-                mbar_arrive_expect_tx(full_ab(s), C::AB_BYTES_PAIR);
-                pend_ab |= 1u << s;
+          const int gc = cbase + c;  // the contraction chunk
+          if constexpr (!AD) {
+            if (leader) {
+              mbar_arrive_expect_tx(full_ab(s), C::AB_BYTES_PAIR);
+              pend_ab |= 1u << s;
+            }
+            if constexpr (C::QUANT) {
+              mbar_arrive_expect_tx(full_p(s), C::P_BYTES);
+              tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_p(s),
+                          p_window_start<WT>(kt) / 4, gc * BC);
+              pend_p |= 1u << s;
+            } else {
+              const uint32_t a_dst = smem_addr(sA + s * A_STAGE);
+              if constexpr (CG == 2) {
+                tma_load_2d_pair(a_dst, &map_w, abar, kt * BM, gc * BC);
+                tma_load_2d_pair(a_dst + A_COLBLK, &map_w, abar, kt * BM + 64, gc * BC);
+              } else {
+                tma_load_2d(a_dst, &map_w, abar, kt * BM, gc * BC);
+                tma_load_2d(a_dst + A_COLBLK, &map_w, abar, kt * BM + 64, gc * BC);
               }
-              if constexpr (C::QUANT) {
+            }
+          } else {
+            const bool adapter = gc >= n_main;
+            const bool dense_a = !C::QUANT || adapter;  // A straight from TMA
+            if (leader) {
+              mbar_arrive_expect_tx(full_ab(s), C::QUANT && adapter
+                                                    ? C::AB_BYTES_PAIR + CG * A_STAGE
+                                                    : C::AB_BYTES_PAIR);
+              pend_ab |= 1u << s;
+            }
+            if constexpr (C::QUANT) {
+              if (adapter) {
+                mbar_arrive(full_p(s));  // no packed window: the decoders pass
+              } else {
                 mbar_arrive_expect_tx(full_p(s), C::P_BYTES);
                 tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_p(s),
                             p_window_start<WT>(kt) / 4, gc * BC);
                 pend_p |= 1u << s;
-              } else {
-                const uint32_t a_dst = smem_addr(sA + s * A_STAGE);
-                if constexpr (CG == 2) {
-                  tma_load_2d_pair(a_dst, &map_w, abar, kt * BM, gc * BC);
-                  tma_load_2d_pair(a_dst + A_COLBLK, &map_w, abar, kt * BM + 64, gc * BC);
-                } else {
-                  tma_load_2d(a_dst, &map_w, abar, kt * BM, gc * BC);
-                  tma_load_2d(a_dst + A_COLBLK, &map_w, abar, kt * BM + 64, gc * BC);
-                }
-              }
-            } else {
-              const bool adapter = gc >= n_main;
-              const bool dense_a = !C::QUANT || adapter;  // A straight from TMA
-              if (leader) {
-                mbar_arrive_expect_tx(full_ab(s), C::QUANT && adapter
-                                                      ? C::AB_BYTES_PAIR + CG * A_STAGE
-                                                      : C::AB_BYTES_PAIR);
-                pend_ab |= 1u << s;
-              }
-              if constexpr (C::QUANT) {
-                if (adapter) {
-                  mbar_arrive(full_p(s));  // no packed window: the decoders pass
-                } else {
-                  mbar_arrive_expect_tx(full_p(s), C::P_BYTES);
-                  tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_p(s),
-                              p_window_start<WT>(kt) / 4, gc * BC);
-                  pend_p |= 1u << s;
-                }
-              }
-              if (dense_a) {
-                const CUtensorMap* ma = adapter ? &map_l : &map_w;
-                const int row = (adapter ? gc - n_main : gc) * BC;
-                const uint32_t a_dst = smem_addr(sA + s * A_STAGE);
-                if constexpr (CG == 2) {
-                  tma_load_2d_pair(a_dst, ma, abar, kt * BM, row);
-                  tma_load_2d_pair(a_dst + A_COLBLK, ma, abar, kt * BM + 64, row);
-                } else {
-                  tma_load_2d(a_dst, ma, abar, kt * BM, row);
-                  tma_load_2d(a_dst + A_COLBLK, ma, abar, kt * BM + 64, row);
-                }
               }
             }
-            if constexpr (CG == 2)
-              tma_load_2d_pair(smem_addr(sB + s * B_STAGE), &map_y, abar, (cbase + c) * BC, ty);
-            else
-              tma_load_2d(smem_addr(sB + s * B_STAGE), &map_y, abar, (cbase + c) * BC, ty);
-            pend_ph = (pend_ph & ~(1u << s)) | (ph << s);
+            if (dense_a) {
+              const CUtensorMap* ma = adapter ? &map_l : &map_w;
+              const int row = (adapter ? gc - n_main : gc) * BC;
+              const uint32_t a_dst = smem_addr(sA + s * A_STAGE);
+              if constexpr (CG == 2) {
+                tma_load_2d_pair(a_dst, ma, abar, kt * BM, row);
+                tma_load_2d_pair(a_dst + A_COLBLK, ma, abar, kt * BM + 64, row);
+              } else {
+                tma_load_2d(a_dst, ma, abar, kt * BM, row);
+                tma_load_2d(a_dst + A_COLBLK, ma, abar, kt * BM + 64, row);
+              }
+            }
           }
+          if constexpr (CG == 2)
+            tma_load_2d_pair(smem_addr(sB + s * B_STAGE), &map_y, abar, (cbase + c) * BC, ty);
+          else
+            tma_load_2d(smem_addr(sB + s * B_STAGE), &map_y, abar, (cbase + c) * BC, ty);
+          pend_ph = (pend_ph & ~(1u << s)) | (ph << s);
         }
         __syncwarp();
         if (++s == S) { s = 0; ph ^= 1u; }
@@ -1150,7 +1145,7 @@ template <int WT, int CG, int BT, bool AD, bool SK>
 static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
                                const CUtensorMap& ml, int n_main, float* dX, int64_t ldx,
                                float beta, int T, int K, const TcPlan& p, float* part,
-                               const DevInfo& dev, cudaStream_t stream, int inject) {
+                               const DevInfo& dev, cudaStream_t stream) {
   using C = tc::Cfg<WT, CG, BT>;
   auto kern = tc::out_prod_tc_kernel<WT, CG, BT, AD, SK>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
@@ -1186,7 +1181,7 @@ static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
   cfg.gridDim = dim3(static_cast<unsigned>(units * CG), 1, 1);
   if (SK && part == nullptr) return cudaErrorInvalidValue;
   e = counted(cudaLaunchKernelEx(&cfg, kern, mw, my, ml, n_main, dX, ldx, beta, T, K, p.n_kunits,
-                                 p.n_ttiles, p.band, p.n_chunks, p.n_splits, part, ctl, inject));
+                                 p.n_ttiles, p.band, p.n_chunks, p.n_splits, part, ctl));
   if (e != cudaSuccess || !SK) return e;
   // stream-K: the shared tiles' pieces, added in chunk order (the same unit
   // count as the launch: the pieces' slabs follow from it)
@@ -1197,12 +1192,12 @@ template <int WT, bool AD, bool SK>
 static cudaError_t launch_tc_w(const CUtensorMap& mw, const CUtensorMap& my,
                                const CUtensorMap& ml, int n_main, float* dX, int64_t ldx,
                                float beta, int T, int K, const TcPlan& p, float* part,
-                               const DevInfo& dev, cudaStream_t stream, int inject) {
+                               const DevInfo& dev, cudaStream_t stream) {
   if (p.cg == 2)
-    return launch_tc_t<WT, 2, 256, AD, SK>(mw, my, ml, n_main, dX, ldx, beta, T, K, p, part, dev, stream,
-                                   inject);
-  return launch_tc_t<WT, 1, 128, AD, SK>(mw, my, ml, n_main, dX, ldx, beta, T, K, p, part, dev, stream,
-                                 inject);
+    return launch_tc_t<WT, 2, 256, AD, SK>(mw, my, ml, n_main, dX, ldx, beta, T, K, p, part, dev,
+                                           stream);
+  return launch_tc_t<WT, 1, 128, AD, SK>(mw, my, ml, n_main, dX, ldx, beta, T, K, p, part, dev,
+                                         stream);
 }
 
 // The body of launch_tc: AD = an adapter rides along (rank > 0).
@@ -1210,8 +1205,8 @@ template <bool AD, bool SK>
 static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K,
                                   const uint16_t* dy16, int64_t ld_dy16, int64_t T, float* dX,
                                   int64_t dx_t, float beta, float* part, const DevInfo& dev,
-                                  cudaStream_t stream, int cg_force, int inject_stall,
-                                  const uint16_t* a16, int64_t rank) {
+                                  cudaStream_t stream, int cg_force, const uint16_t* a16,
+                                  int64_t rank) {
   // with an adapter the contraction runs over tc_adapter_cols(N, r) columns
   // of dy16: dY's N, zeros to the chunk boundary, then the adapter's rank
   const int64_t n_ext = rank > 0 ? tc_adapter_cols(N, rank) : N;
@@ -1255,7 +1250,7 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
   const int t = static_cast<int>(T), k = static_cast<int>(K);
   const cudaError_t e = with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
     return launch_tc_w<decltype(wt)::value, AD, SK>(mw, my, ml, n_main, dX, dx_t, beta, t, k, p,
-                                                partial, dev, stream, inject_stall);
+                                                partial, dev, stream);
   });
   if (e != cudaSuccess || p.n_splits == 1) return e;
   return launch_reduce_partials(partial, p.n_splits, T, K, dX, dx_t, beta, dev, stream);
@@ -1266,10 +1261,9 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
 cudaError_t launch_tc_adapter(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
                               int64_t ld_dy16, int64_t T, float* dX, int64_t dx_t, float beta,
                               float* part, const DevInfo& dev, cudaStream_t stream, int cg_force,
-                              int inject_stall, const uint16_t* a16, int64_t rank);
+                              const uint16_t* a16, int64_t rank);
 cudaError_t launch_tc_stream_k(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
                                int64_t ld_dy16, int64_t T, float* dX, int64_t dx_t, float beta,
-                               float* part, const DevInfo& dev, cudaStream_t stream, int cg_force,
-                               int inject_stall);
+                               float* part, const DevInfo& dev, cudaStream_t stream, int cg_force);
 
 }  // namespace rg

@@ -9,10 +9,9 @@ namespace rg {
 
 cudaError_t launch_tc_stream_k(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
                                int64_t ld_dy16, int64_t T, float* dX, int64_t dx_t, float beta,
-                               float* part, const DevInfo& dev, cudaStream_t stream, int cg_force,
-                               int inject_stall) {
+                               float* part, const DevInfo& dev, cudaStream_t stream, int cg_force) {
   return launch_tc_impl<false, true>(wtype, W, N, K, dy16, ld_dy16, T, dX, dx_t, beta, part, dev,
-                                     stream, cg_force, inject_stall, nullptr, 0);
+                                     stream, cg_force, nullptr, 0);
 }
 
 }  // namespace rg

@@ -34,6 +34,14 @@ def test_every_declared_symbol_is_exported(lib):
     assert sorted(n for n, _, _ in rg.SIGNATURES) == names
 
 
+def test_noalloc_scratch_size_matches_the_header():
+    """The binding's copy of RG_NOALLOC_SCRATCH_BYTES is the header's."""
+    src = open(os.path.join(ROOT, "include", "rg.h")).read()
+    m = re.search(r"#define\s+RG_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", src)
+    assert m, "RG_NOALLOC_SCRATCH_BYTES not found in include/rg.h"
+    assert rg.RG_NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
 def test_row_bytes_matches_block_sizes(lib):
     for wt in inputs.ALL_TYPES:
         for K in (0, 8, 32, 256, 4096, 14336, 17408, 300):

@@ -84,3 +84,33 @@ def test_cpu_sample_takes_the_rows_a_call_has():
     assert f == 2 * 32 * 256 * 256 and "1 pass" in desc
     f, dt, desc = bench.oracle_sample(wl, 1024, min_seconds=0.2)
     assert dt >= 0.2 and f % (2 * 32 * 256 * 256) == 0 and f > 2 * 32 * 256 * 256
+
+
+def test_peak_follows_the_clock_record():
+    """The burst peak for a short region or one without the power cap; the
+    sustained peak only for a seconds-long region under sw_power_cap."""
+    import bench
+    peaks = {"bf16_tflops": 1926.9, "bf16_tflops_sustained": 1715.2, "hbm_gbs": 6800.7}
+    assert bench.choose_peak(peaks, {"reasons": []}, 0.06) == (1926.9, "bf16_tflops")
+    assert bench.choose_peak(peaks, {"reasons": []}, 5.0) == (1926.9, "bf16_tflops")
+    assert bench.choose_peak(peaks, {"reasons": ["sw_power_cap"]}, 0.2)[1] == "bf16_tflops"
+    assert bench.choose_peak(peaks, {"reasons": ["sw_power_cap"]}, 3.0) == (1715.2,
+                                                                            "bf16_tflops_sustained")
+    assert bench.choose_peak(peaks, None, 3.0)[1] == "bf16_tflops"
+
+
+def test_reference_arm_and_cpu_baseline_share_sample_and_config():
+    """Both CPU numbers time the same rows of every call, and the reference
+    arm's config is the GPU arm's, key for key."""
+    import bench
+    from quantized_weight_out_gb300 import inputs
+    assert bench.sample_rows(20, 5) == 1024
+    assert bench.sample_rows(500, 3) == 64
+    r = bench.sample_rows(100, 20)
+    assert 64 <= r < 1024 and r % 64 == 0
+    wl = inputs.WORKLOADS["layer7b_t8192"]
+    c = bench.workload_config("layer7b_t8192", wl, 1)
+    assert c["flops_per_step"] == sum(p.flops for p in wl)
+    assert "no flush" in c["l2"]
+    c1 = bench.workload_config("q8_0_256x256_t32", inputs.WORKLOADS["q8_0_256x256_t32"], 1)
+    assert "clean lines" in c1["l2"]

@@ -404,3 +404,38 @@ def test_plan_of_empty_shapes(rg):
     assert info.launches == 0 and info.decode_ops == 0
     rg.check(rg.rg_plan(0, inputs.Q8_0, 0, 256, 8, info))
     assert info.launches == 1 and info.decode_ops == 0
+
+
+# ----------------------------------------------------------------------------
+# the fp16 operand range
+
+@pytest.mark.parametrize("strided", [False, True])
+def test_dy_beyond_fp16_range_is_reported_not_silent(rg, strided):
+    """One |dY| = 1e5 element, beyond fp16's largest value: the tensor-core
+    call on an fp16 kind (Q4_K W) reports RG_ERR_RANGE through rg_check (the
+    read clears it), so an inf in dX never goes unreported; the bf16 kind
+    (BF16 W) takes the same dY within its bound, and so does the SIMT
+    variant for the Q4_K weight.  Strided: dY given transposed (the tiled
+    conversion)."""
+    N, K, T = 300, 512, 64
+    dY = inputs.normal_f32(61, 2, T * N, 1e-3).reshape(T, N)
+    dY[5, 17] = -1.0e5
+    dev, s = _dev(), torch.cuda.current_stream()
+    for wtype, variant, expect in ((inputs.Q4_K, 1, rg.RG_ERR_RANGE), (inputs.BF16, 1, rg.RG_OK),
+                                   (inputs.Q4_K, 3, rg.RG_OK)):
+        W = inputs.gen_weight(wtype, N, K, seed=61, stream=1)
+        Wt = torch.from_numpy(W).to(dev)
+        dX = torch.full((T, K), float("nan"), device=dev)
+        if strided:
+            dYt = torch.from_numpy(np.ascontiguousarray(dY.T)).to(dev)   # [N, T]: dY[t, n] at n*T + t
+            st = rg.rg_out_prod_ex(variant, wtype, Wt, N, K, 0, dYt, T, 1, T, 0, dX, K, 0, 1, 0.0, s)
+        else:
+            st = rg.rg_out_prod_variant(variant, wtype, Wt, N, K, torch.from_numpy(dY).to(dev), T,
+                                        dX, 0.0, s)
+        assert st == rg.RG_OK
+        assert rg.rg_check(s) == expect, (wtype, variant)
+        assert rg.rg_check(s) == rg.RG_OK          # read and cleared
+        if expect == rg.RG_OK:
+            Wd = oracle.dequant(wtype, W, N, K)
+            assert_within(dX.cpu().numpy(), oracle.out_prod(wtype, W, N, K, dY, T, Wd=Wd),
+                          oracle.abs_bound(dY, Wd), TOL[variant], f"range {wtype} {variant}")

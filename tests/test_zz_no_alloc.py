@@ -59,6 +59,37 @@ def test_noalloc_matches_rg_out_prod_on_consecutive_calls(rg):
         assert np.all(np.abs(got.astype(np.float64) - ref) <= lim)
 
 
+def test_noalloc_small_t_matches_rg_out_prod_on_consecutive_calls(rg):
+    """The small-T variant through the fixed scratch: one dY row over a
+    14336-row Q4_K weight (rows split over CTAs, whose partial sums sit in the
+    scratch before the reduction adds them), then four rows through the
+    warp-level MMA consumer, which again leaves partial sums there."""
+    dev = torch.device("cuda:0")
+    s = torch.cuda.current_stream()
+    cases = [(inputs.Q4_K, 14336, 4096, 1, 23, 0.0), (inputs.Q4_K, 4096, 4096, 4, 24, 1.0)]
+    outs = []
+    for wtype, N, K, T, seed, beta in cases:
+        assert rg.rg_select_variant(wtype, N, K, T) == rg.RG_VARIANT_SMALLT
+        info = rg.rg_plan_info()
+        rg.check(rg.rg_plan(0, wtype, N, K, T, info), "rg_plan")
+        assert info.n_splits > 1 and 0 < info.workspace_bytes <= rg.RG_NOALLOC_SCRATCH_BYTES
+        W, dY, dX0 = _case(wtype, N, K, T, seed, beta)
+        Wt, dYt = torch.from_numpy(W).to(dev), torch.from_numpy(dY).to(dev)
+        a = torch.from_numpy(dX0).to(dev)
+        b = torch.from_numpy(dX0).to(dev)
+        rg.check(rg.rg_out_prod(wtype, Wt, N, K, dYt, T, a, beta, s), "rg_out_prod")
+        rg.check(rg.rg_out_prod_noalloc(wtype, Wt, N, K, dYt, T, b, beta, s), "rg_out_prod_noalloc")
+        rg.check(rg.rg_check(s), "rg_check")
+        outs.append((wtype, N, K, T, beta, W, dY, dX0, a.cpu().numpy(), b.cpu().numpy()))
+    for wtype, N, K, T, beta, W, dY, dX0, ref_gpu, got in outs:
+        # same kernels, same plan: the same fixed-order sums
+        assert np.array_equal(got, ref_gpu)
+        Wd = oracle.dequant(wtype, W, N, K)
+        lim = 5e-3 * oracle.abs_bound(dY, Wd) + 1e-7 + np.abs(beta * dX0) * 2.0 ** -24
+        ref = oracle.out_prod(wtype, W, N, K, dY, T, dX0, beta, Wd=Wd)
+        assert np.all(np.abs(got.astype(np.float64) - ref) <= lim)
+
+
 def test_noalloc_rejects_oversized_scratch_without_launching(rg):
     dev = torch.device("cuda:0")
     s = torch.cuda.current_stream()
