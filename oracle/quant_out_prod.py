@@ -55,6 +55,11 @@ Block formats (little-endian), ggml's GGUF block types:
                    E2M1 code (sign bit 3, two exponent bits, one mantissa
                    bit; the OCP microscaling formats);
                                                   y = E2M1(nib) * 2^(e - 127)
+* NVFP4 36 B / 64: d[4] (one FP8 E4M3 scale per 16-value micro-block),
+                   qs[32]; micro-block s holds values 16s .. 16s+15: value
+                   16s + j (j < 8) is the low nibble of qs[8s + j], value
+                   16s + j + 8 its high nibble; each nibble an E2M1 element
+                   as in MXFP4;                   y = E2M1(nib) * E4M3(d[s])
 * F16 / BF16: 2 B per value.
 * F32: 4 B per value, the value itself.
 
@@ -69,12 +74,12 @@ import numpy as np
 
 F16, BF16, Q8_0, Q4_0, Q4_K = 1, 2, 3, 4, 5
 Q4_1, Q5_0, Q5_1, Q5_K, Q6_K = 6, 7, 8, 9, 10
-F32, Q2_K, Q3_K, MXFP4 = 11, 12, 13, 14
+F32, Q2_K, Q3_K, MXFP4, NVFP4 = 11, 12, 13, 14, 15
 
 _BLOCK = {F16: (1, 2), BF16: (1, 2), Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144),
           Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q5_K: (256, 176),
           Q6_K: (256, 210), F32: (1, 4), Q2_K: (256, 84), Q3_K: (256, 110),
-          MXFP4: (32, 17)}
+          MXFP4: (32, 17), NVFP4: (64, 36)}
 
 
 def row_bytes(wtype: int, K: int) -> int:
@@ -130,6 +135,21 @@ def e2m1_to_f32(code) -> np.ndarray:
     e = (c >> 1) & 3
     m = (c & 1).astype(np.float64)
     mag = np.where(e == 0, m / 2.0, np.ldexp(1.0 + m / 2.0, e - 1))
+    return np.where(s == 1, -mag, mag).astype(np.float32)
+
+
+def e4m3_to_f32(code) -> np.ndarray:
+    """FP8 E4M3 (the OCP 8-bit floating-point format with four exponent and
+    three mantissa bits; NVFP4's micro-block scale): bit 7 sign, bits 3-6
+    exponent (bias 7), bits 0-2 mantissa; exponent 0 -> (-1)^s * 2^-6 * m/8
+    (subnormal, signed zero kept); exponent 15 with mantissa 7 -> NaN (the
+    format has no infinities); else (-1)^s * 2^(e - 7) * (1 + m/8), up to 448."""
+    c = np.asarray(code).astype(np.int64)
+    s = (c >> 7) & 1
+    e = (c >> 3) & 15
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1.0 + m / 8.0, e - 7))
+    mag = np.where((e == 15) & ((c & 7) == 7), np.nan, mag)
     return np.where(s == 1, -mag, mag).astype(np.float32)
 
 
@@ -382,6 +402,22 @@ def decode_mxfp4(W, N: int, K: int) -> np.ndarray:
         return y.astype(np.float32).reshape(N, K)
 
 
+def decode_nvfp4(W, N: int, K: int) -> np.ndarray:
+    """NVFP4: 36-byte blocks of 64 values, four micro-blocks of 16 with an
+    E4M3 scale each (bytes 0-3), then qs[32]: micro-block s takes qs[8s ..
+    8s+7], value 16s + j (j < 8) the low nibble of qs[8s + j] and value
+    16s + j + 8 its high nibble; y = E2M1(nib) * E4M3(d[s]).  Exact in F32:
+    a two-bit significand times a four-bit one, magnitudes 2^-10 .. 2688
+    (a NaN scale gives NaN values)."""
+    blk = _rows(W, N, K, NVFP4).reshape(N, K // 64, 36)
+    sc = e4m3_to_f32(blk[..., 0:4]).astype(np.float64)            # [N, B, 4]
+    qs = blk[..., 4:36].reshape(N, K // 64, 4, 8)                  # [N, B, s, j]
+    nib = np.concatenate([qs & 0x0F, qs >> 4], axis=-1)            # [N, B, s, 16]
+    with np.errstate(invalid="ignore"):
+        y = sc[..., None] * e2m1_to_f32(nib).astype(np.float64)
+        return y.astype(np.float32).reshape(N, K)
+
+
 def decode_f16(W, N: int, K: int) -> np.ndarray:
     b = _rows(W, N, K, F16).reshape(N, K, 2)
     return f16_bits_to_f32(_le16(b[..., 0], b[..., 1]))
@@ -401,7 +437,7 @@ _DECODERS = {F16: decode_f16, BF16: decode_bf16, Q8_0: decode_q8_0,
              Q4_0: decode_q4_0, Q4_K: decode_q4_k, Q4_1: decode_q4_1,
              Q5_0: decode_q5_0, Q5_1: decode_q5_1, Q5_K: decode_q5_k,
              Q6_K: decode_q6_k, F32: decode_f32, Q2_K: decode_q2_k, Q3_K: decode_q3_k,
-             MXFP4: decode_mxfp4}
+             MXFP4: decode_mxfp4, NVFP4: decode_nvfp4}
 
 
 def dequant(wtype: int, W, N: int, K: int) -> np.ndarray:

@@ -36,6 +36,11 @@ Formats written (little-endian, the block layouts of ggml's GGUF types):
 * Q3_K 110 B / 256 values: ``hmask[32]`` (bit 4h + j of ``hmask[16s + l]``:
   the value's third bit), ``qs[64]`` (low 2 bits as Q2_K), 12 bytes of
   sixteen 6-bit scales, fp16 ``d``.
+* MXFP4 17 B / 32 values: E8M0 scale byte, 16 bytes of E2M1 nibbles (as Q4_0).
+* NVFP4 36 B / 64 values: four E4M3 scale bytes (one per 16 values), 32
+  bytes of E2M1 nibbles; the 16 values of scale s in bytes 8s .. 8s+7,
+  value 16s + j (j < 8) in the low nibble of byte 8s + j, 16s + j + 8 in
+  its high nibble.
 * F16 / BF16: 2 B per value; F32: 4 B per value.
 
 The generator recipes follow the workload descriptions of the llama.cpp fork's
@@ -55,10 +60,10 @@ import numpy as np
 # weight type codes (the C ABI uses the same integers)
 F16, BF16, Q8_0, Q4_0, Q4_K = 1, 2, 3, 4, 5
 Q4_1, Q5_0, Q5_1, Q5_K, Q6_K, F32 = 6, 7, 8, 9, 10, 11
-Q2_K, Q3_K, MXFP4 = 12, 13, 14
+Q2_K, Q3_K, MXFP4, NVFP4 = 12, 13, 14, 15
 TYPE_NAMES = {F16: "f16", BF16: "bf16", Q8_0: "q8_0", Q4_0: "q4_0", Q4_K: "q4_k",
               Q4_1: "q4_1", Q5_0: "q5_0", Q5_1: "q5_1", Q5_K: "q5_k", Q6_K: "q6_k", F32: "f32",
-              Q2_K: "q2_k", Q3_K: "q3_k", MXFP4: "mxfp4"}
+              Q2_K: "q2_k", Q3_K: "q3_k", MXFP4: "mxfp4", NVFP4: "nvfp4"}
 NAME_TO_TYPE = {v: k for k, v in TYPE_NAMES.items()}
 ALL_TYPES = [Q8_0, Q4_0, Q4_K, F16, BF16, Q4_1, Q5_0, Q5_1, Q5_K, Q6_K, F32, Q2_K, Q3_K, MXFP4]
 
@@ -66,7 +71,7 @@ ALL_TYPES = [Q8_0, Q4_0, Q4_K, F16, BF16, Q4_1, Q5_0, Q5_1, Q5_K, Q6_K, F32, Q2_
 BLOCK = {F16: (1, 2), BF16: (1, 2), Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144),
          Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q5_K: (256, 176),
          Q6_K: (256, 210), F32: (1, 4), Q2_K: (256, 84), Q3_K: (256, 110),
-         MXFP4: (32, 17)}
+         MXFP4: (32, 17), NVFP4: (64, 36)}
 
 
 def row_bytes(wtype: int, K: int) -> int:
@@ -396,6 +401,18 @@ def pack_mxfp4(e, q) -> np.ndarray:
     return out
 
 
+def pack_nvfp4(d, q) -> np.ndarray:
+    """NVFP4 blocks [nb, 36] from E4M3 scale bytes d [nb, 4] and 4-bit E2M1
+    codes q [nb, 64]: the 16 codes of scale s go to bytes 4 + 8s .. 11 + 8s,
+    code 16s + j (j < 8) in the low nibble, 16s + j + 8 in the high one."""
+    d = np.asarray(d, dtype=np.uint8)
+    q = np.asarray(q, dtype=np.uint8).reshape(-1, 4, 16)
+    out = np.zeros((d.shape[0], 36), dtype=np.uint8)
+    out[:, 0:4] = d
+    out[:, 4:36] = (q[..., :8] | (q[..., 8:] << 4)).reshape(-1, 32)
+    return out
+
+
 # ----------------------------------------------------------------------------
 # weights and activations for one call
 
@@ -450,6 +467,14 @@ def gen_weight(wtype: int, N: int, K: int, seed: int, stream: int) -> np.ndarray
         e = 118 + uniform_int(seed, stream, nb, 4, field=1)
         q = uniform_int(seed, stream, nb * 32, 16, field=5).reshape(nb, 32)
         return pack_mxfp4(e, q).reshape(-1)
+    if wtype == NVFP4:
+        # fields drawn directly: E4M3 scale bytes 0x00..0x0f (zero, the
+        # subnormals m/8 * 2^-6 and the first binade 2^-6 (1 + m/8)) and
+        # uniform E2M1 codes give |y| <= 6 * 0.0293 ~ 0.18 (most near 0.02)
+        nb = N * K // 64
+        d = uniform_int(seed, stream, nb * 4, 16, field=1).reshape(nb, 4)
+        q = uniform_int(seed, stream, nb * 64, 16, field=5).reshape(nb, 64)
+        return pack_nvfp4(d, q).reshape(-1)
     if wtype in (Q4_1, Q5_0, Q5_1):
         # fields drawn directly (the pages give no workload of these types):
         # a block of N(0, 0.02) weights spans about 0.08, so d ~ 0.08 / levels
@@ -545,6 +570,9 @@ WORKLOADS = {
     "layer7b_t8192": _layer_sweep(8192),
     # the sweep's largest call alone (profiling a full-size launch)
     "layer7b_gate_t8192": [_layer_sweep(8192)[4]],
+    # one row of dY (a decode-time gradient): the weight-streaming small-T path
+    "smallt_q4_k_14336x4096_t1": [Problem("smallt_q4_k_14336x4096_t1", Q4_K, 14336, 4096, 1, 1e-3)],
+    "smallt_q8_0_4096x14336_t1": [Problem("smallt_q8_0_4096x14336_t1", Q8_0, 4096, 14336, 1, 1e-3)],
     # the other quantized types on the sweep's q/o shape, one call each
     "types_4096x4096_t8192": [Problem(f"{TYPE_NAMES[wt]}_4096x4096_t8192", wt, 4096, 4096, 8192,
                                       1e-3, 0.0, 16 * i)

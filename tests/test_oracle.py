@@ -246,6 +246,72 @@ def test_mxfp4_hand_blocks(golden_dir):
     assert _same_values(oracle.decode_mxfp4(W, 1, 160)[0], np.concatenate([v for _, v in blocks]))
 
 
+def _nvfp4_fixture(golden_dir):
+    rows = _read(golden_dir, "nvfp4_blocks.txt")
+    out = []
+    for i in range(0, len(rows), 2):
+        assert rows[i][0] == "hex" and rows[i + 1][0] == "values"
+        W = np.frombuffer(bytes.fromhex(rows[i][1]), dtype=np.uint8)
+        out.append((W, np.array([float(v) for v in rows[i + 1][1:]], dtype=np.float32)))
+    return out
+
+
+def test_nvfp4_hand_blocks(golden_dir):
+    """Scales 1, 2, 0.5, +0, the smallest and largest subnormal, the smallest
+    normal, 240, 448, -1, -0.0 and NaN; every E2M1 code in both nibble
+    halves of a micro-block, signed zeros included."""
+    blocks = _nvfp4_fixture(golden_dir)
+    assert len(blocks) == 3
+    for W, want in blocks:
+        assert _same_values(oracle.decode_nvfp4(W, 1, 64)[0], want)
+    W = np.concatenate([w for w, _ in blocks] + [blocks[0][0]])   # four blocks: a 256-value row
+    want = np.concatenate([v for _, v in blocks] + [blocks[0][1]])
+    assert _same_values(oracle.decode_nvfp4(W, 1, 256)[0], want)
+    assert _same_values(oracle.dequant(oracle.NVFP4, np.concatenate([W, W]), 2, 256),
+                        np.stack([want, want]))
+
+
+def test_e4m3_codes_against_torch_float8():
+    """All 256 E4M3 bytes against torch's float8_e4m3fn (the same OCP
+    format: no infinities, NaN at 0x7f and 0xff)."""
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch has no float8_e4m3fn")
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).float().numpy()
+    assert _same_values(oracle.e4m3_to_f32(codes), want)
+
+
+def test_e4m3_codes_against_ldexp():
+    """E4M3 from math.ldexp: normals (1 + m/8) * 2^(e-7), subnormals
+    m * 2^-9, the sign, 0x7f / 0xff NaN."""
+    got = oracle.e4m3_to_f32(np.arange(256))
+    for c in range(256):
+        s, e, m = c >> 7, (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            assert np.isnan(got[c])
+            continue
+        mag = math.ldexp(m, -9) if e == 0 else math.ldexp(8 + m, e - 10)
+        want = struct.unpack("<f", struct.pack("<f", -mag if s else mag))[0]
+        assert got[c] == want and math.copysign(1.0, float(got[c])) == (-1.0 if s else 1.0), c
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def test_nvfp4_pack_roundtrip_through_oracle():
+    """The generator's packer places every scale and code where the
+    oracle reads it: y[16s + j] = E2M1(q[16s + j]) * E4M3(d[s])."""
+    rng = np.random.default_rng(8)
+    nb = 5
+    d = rng.integers(0, 0x7F, (nb, 4))
+    q = rng.integers(0, 16, (nb, 64))
+    W = inputs.pack_nvfp4(d, q).reshape(-1)
+    y = oracle.decode_nvfp4(W, 1, 64 * nb).reshape(nb, 64)
+    sub = np.arange(64) // 16
+    want = (oracle.e2m1_to_f32(q).astype(np.float64) *
+            oracle.e4m3_to_f32(d)[:, sub].astype(np.float64)).astype(np.float32)
+    assert _same_values(y, want)
+
+
 def test_e2m1_codes_against_the_element_table():
     """The OCP FP4 (E2M1) element table: codes 0..7 are 0, 0.5, 1, 1.5, 2,
     3, 4, 6 and codes 8..15 their negatives (code 8 is -0.0)."""
@@ -384,6 +450,9 @@ def _all_ones_weight(wtype, N, K, variant=0):
     if wtype == inputs.MXFP4:    # scale 2^0, E2M1 code 2 (1.0) in both nibbles
         blk = bytes([0x7F]) + bytes([0x22]) * 16
         return np.frombuffer(blk * (N * K // 32), dtype=np.uint8)
+    if wtype == inputs.NVFP4:    # E4M3 scales 1.0 (0x38), E2M1 code 2 (1.0) in both nibbles
+        blk = bytes([0x38]) * 4 + bytes([0x22]) * 32
+        return np.frombuffer(blk * (N * K // 64), dtype=np.uint8)
     if wtype == inputs.F16:
         return np.frombuffer(bytes([0x00, 0x3C]) * (N * K), dtype=np.uint8)
     if wtype == inputs.F32:
@@ -397,7 +466,8 @@ CASES = [(inputs.Q8_0, 0), (inputs.Q4_0, 0), (inputs.Q4_K, 0), (inputs.Q4_K, 1),
          (inputs.F16, 0), (inputs.BF16, 0), (inputs.Q4_1, 0), (inputs.Q5_0, 0),
          (inputs.Q5_1, 0), (inputs.Q5_1, 1), (inputs.Q5_K, 0), (inputs.Q5_K, 1),
          (inputs.Q6_K, 0), (inputs.Q6_K, 1), (inputs.F32, 0), (inputs.Q2_K, 0),
-         (inputs.Q2_K, 1), (inputs.Q3_K, 0), (inputs.Q3_K, 1), (inputs.MXFP4, 0)]
+         (inputs.Q2_K, 1), (inputs.Q3_K, 0), (inputs.Q3_K, 1), (inputs.MXFP4, 0),
+         (inputs.NVFP4, 0)]
 
 
 @pytest.mark.parametrize("wtype,variant", CASES)
@@ -577,6 +647,22 @@ def _py_decode(wtype, raw, N, K):
                     code = (blk[1 + j % 16] >> (4 * (j // 16))) & 15
                     mag = e2m1[code & 7] * scale
                     out[n][32 * b + j] = -mag if code & 8 else mag
+        elif wtype == inputs.NVFP4:
+            e2m1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+            for b in range(K // 64):
+                blk = row[36 * b: 36 * b + 36]
+                for v in range(64):
+                    s, j = divmod(v, 16)
+                    code = (blk[4 + 8 * s + j % 8] >> (4 * (j // 8))) & 15
+                    e8 = blk[s]
+                    ex, mt = (e8 >> 3) & 15, e8 & 7
+                    if ex == 15 and mt == 7:
+                        scale = float("nan")
+                    else:
+                        scale = mt / 8 * 2.0 ** -6 if ex == 0 else (1 + mt / 8) * 2.0 ** (ex - 7)
+                        scale = -scale if e8 & 0x80 else scale
+                    mag = e2m1[code & 7] * scale
+                    out[n][64 * b + v] = -mag if code & 8 else mag
         elif wtype == inputs.Q3_K:
             for b in range(K // 256):
                 blk = row[110 * b: 110 * b + 110]
@@ -600,7 +686,8 @@ BRUTE = [(inputs.Q8_0, 40, 64, 3), (inputs.Q4_0, 33, 96, 2), (inputs.Q4_K, 12, 5
          (inputs.F16, 24, 40, 3), (inputs.BF16, 24, 40, 3), (inputs.Q8_0, 7, 32, 1),
          (inputs.Q4_1, 21, 64, 2), (inputs.Q5_0, 19, 96, 2), (inputs.Q5_1, 17, 64, 2),
          (inputs.Q5_K, 10, 512, 2), (inputs.Q6_K, 9, 512, 2), (inputs.F32, 20, 48, 3),
-         (inputs.Q2_K, 11, 512, 2), (inputs.Q3_K, 10, 512, 2), (inputs.MXFP4, 13, 96, 2)]
+         (inputs.Q2_K, 11, 512, 2), (inputs.Q3_K, 10, 512, 2), (inputs.MXFP4, 13, 96, 2),
+         (inputs.NVFP4, 11, 256, 2)]
 
 
 @pytest.mark.parametrize("wtype,N,K,T", BRUTE)
@@ -843,6 +930,59 @@ def test_mxfp4_mutants_are_caught(golden_dir):
         assert not _same_values(mut(W, 1, 32)[0], want), mut.__name__
 
 
+def _mut_nvfp4_q4_0_nibble_order(W, N, K):
+    """Nibbles ordered over the whole 64-value block (low = j, high = j + 32)."""
+    blk = qop._rows(W, N, K, qop.NVFP4).reshape(N, K // 64, 36)
+    sc = qop.e4m3_to_f32(blk[..., 0:4]).astype(np.float64)
+    qs = blk[..., 4:36]
+    nib = np.concatenate([qs & 0x0F, qs >> 4], axis=-1)              # [.., 64]
+    y = sc[..., np.arange(64) // 16] * qop.e2m1_to_f32(nib).astype(np.float64)
+    return y.astype(np.float32).reshape(N, K)
+
+
+def _mut_nvfp4_scale_bias_8(W, N, K):
+    """E4M3 scales decoded with exponent bias 8."""
+    blk = qop._rows(W, N, K, qop.NVFP4).reshape(N, K // 64, 36)
+    sc = qop.e4m3_to_f32(blk[..., 0:4]).astype(np.float64) / 2.0
+    qs = blk[..., 4:36].reshape(N, K // 64, 4, 8)
+    nib = np.concatenate([qs & 0x0F, qs >> 4], axis=-1)
+    return (sc[..., None] * qop.e2m1_to_f32(nib)).astype(np.float32).reshape(N, K)
+
+
+def _mut_nvfp4_normal_subnormals(W, N, K):
+    """E4M3 exponent 0 read as a normal binade, (1 + m/8) * 2^-7."""
+    real = qop.e4m3_to_f32
+
+    def bad(code):
+        c = np.asarray(code).astype(np.int64)
+        e, m = (c >> 3) & 15, (c & 7).astype(np.float64)
+        mag = np.ldexp(1.0 + m / 8.0, e - 7)
+        mag = np.where((e == 15) & ((c & 7) == 7), np.nan, mag)
+        return np.where((c >> 7) & 1 == 1, -mag, mag).astype(np.float32)
+    qop.e4m3_to_f32 = bad
+    try:
+        return qop.decode_nvfp4(W, N, K)
+    finally:
+        qop.e4m3_to_f32 = real
+
+
+def _mut_nvfp4_scale_per_32(W, N, K):
+    """One scale per 32 values (d[0], d[1] over the block's halves)."""
+    blk = qop._rows(W, N, K, qop.NVFP4).reshape(N, K // 64, 36)
+    sc = qop.e4m3_to_f32(blk[..., 0:4]).astype(np.float64)
+    qs = blk[..., 4:36].reshape(N, K // 64, 4, 8)
+    nib = np.concatenate([qs & 0x0F, qs >> 4], axis=-1).reshape(N, K // 64, 64)
+    y = sc[..., np.arange(64) // 32] * qop.e2m1_to_f32(nib).astype(np.float64)
+    return y.astype(np.float32).reshape(N, K)
+
+
+def test_nvfp4_mutants_are_caught(golden_dir):
+    blocks = _nvfp4_fixture(golden_dir)
+    for mut in (_mut_nvfp4_q4_0_nibble_order, _mut_nvfp4_scale_bias_8,
+                _mut_nvfp4_normal_subnormals, _mut_nvfp4_scale_per_32):
+        assert any(not _same_values(mut(W, 1, 64)[0], want) for W, want in blocks), mut.__name__
+
+
 def test_new_type_mutants_are_caught(golden_dir):
     rows = dict((r[0], r[1:]) for r in _read(golden_dir, "q5_0_block.txt"))
     W = np.frombuffer(bytes.fromhex(rows["hex"][0]), dtype=np.uint8)
@@ -1035,6 +1175,48 @@ def test_lora_bound_covers_terms():
             terms = [abs(2.0 * float(dY[t, n]) * float(B[n, j]) * float(A[j, k]))
                      for n in range(N) for j in range(R)]
             assert abs(bnd[t, k] - math.fsum(terms)) <= 1e-12 * bnd[t, k]
+
+
+def _mul_mat_bound_matches_terms(bound_fn) -> bool:
+    """Whether bound_fn(X, Wd)[t, n] equals the exact sum of the absolute
+    terms |X[t, k] * deq(W)[n, k]| over the K values of row n (the forward's
+    contraction), written out one term at a time; signed inputs, so a dropped
+    absolute value shows, and N != K, so a transposed operand shows."""
+    N, K, T = 7, 256, 3
+    W = inputs.gen_weight(inputs.Q8_0, N, K, seed=97, stream=1)
+    Wd = oracle.dequant(inputs.Q8_0, W, N, K)
+    X = inputs.normal_f32(97, 2, T * K, 1.0).reshape(T, K)
+    try:
+        bnd = np.asarray(bound_fn(X, Wd), dtype=np.float64)
+    except ValueError:  # mismatched shapes
+        return False
+    if bnd.shape != (T, N):
+        return False
+    for t in range(T):
+        for n in range(N):
+            exact = math.fsum(abs(float(X[t, k]) * float(Wd[n, k])) for k in range(K))
+            if not abs(bnd[t, n] - exact) <= 1e-12 * exact:
+                return False
+    return True
+
+
+def test_mul_mat_bound_covers_terms():
+    assert _mul_mat_bound_matches_terms(oracle.mul_mat_bound)
+
+
+@pytest.mark.parametrize("mutant", ["no_abs_x", "no_abs_w", "signed", "w_not_transposed_sq"])
+def test_mul_mat_bound_mutants_are_caught(mutant):
+    """Plausible mistakes in a copy of the forward bound fail the term check."""
+    def fn(X, Wd):
+        X64, W64 = np.asarray(X, dtype=np.float64), np.asarray(Wd, dtype=np.float64)
+        if mutant == "no_abs_x":
+            return X64 @ np.abs(W64).T
+        if mutant == "no_abs_w":
+            return np.abs(X64) @ W64.T
+        if mutant == "signed":
+            return np.abs(X64 @ W64.T)
+        return np.abs(X64) @ np.abs(W64)   # the backward's orientation: shapes do not fit
+    assert not _mul_mat_bound_matches_terms(fn)
 
 
 @pytest.mark.parametrize("mutant", ["b_transposed_role", "dropped_scale", "a_rows_reversed",
