@@ -462,6 +462,36 @@ def out_prod(wtype: int, W, N: int, K: int, dY, T: int, dX0=None, beta: float = 
     return ref
 
 
+def batch_weight(i2: int, i3: int, n2: int, n3: int, w_n2: int, w_n3: int):
+    """Which weight (j2, j3) batch (i2, i3) of a batched OUT_PROD reads when
+    there are w_n2 x w_n3 weights for n2 x n3 gradient batches: ggml's
+    broadcast rule for out_prod, each weight serving a run of consecutive
+    batches, j = i / (n / w_n) per dimension (the batched OUT_PROD whose
+    broadcasting cases the llama.cpp fork's PR "cuda: out_prod accepts a
+    quantized src0", section "Measured", reports skipped)."""
+    if n2 % w_n2 or n3 % w_n3:
+        raise ValueError("weight batch counts must divide the gradient's")
+    return i2 // (n2 // w_n2), i3 // (n3 // w_n3)
+
+
+def out_prod_batched(wtype: int, Ws, N: int, K: int, dYs, T: int, dX0s=None,
+                     beta: float = 0.0):
+    """F64 [n3][n2][T, K]: every batch (i2, i3) as out_prod with the weight
+    batch_weight picks.  Ws[j3][j2] are the stored weights, dYs[i3][i2] the
+    [T, N] gradients, dX0s[i3][i2] the old outputs (beta != 0)."""
+    n3, n2 = len(dYs), len(dYs[0])
+    w_n3, w_n2 = len(Ws), len(Ws[0])
+    out = []
+    for i3 in range(n3):
+        row = []
+        for i2 in range(n2):
+            j2, j3 = batch_weight(i2, i3, n2, n3, w_n2, w_n3)
+            row.append(out_prod(wtype, Ws[j3][j2], N, K, dYs[i3][i2], T,
+                                None if dX0s is None else dX0s[i3][i2], beta))
+        out.append(row)
+    return out
+
+
 def mul_mat(wtype: int, W, N: int, K: int, X, T: int, Y0=None, beta: float = 0.0,
             Wd=None) -> np.ndarray:
     """F64 [T, N]: beta*Y0 + X @ deq(W)^T, the forward mul_mat(W, x) whose

@@ -1275,3 +1275,46 @@ def test_q2_q3_k_pack_roundtrip_through_oracle():
     y = oracle.decode_q3_k(W, B, 256)
     want = (df[:, None] * (sc6[:, sub] - 32).astype(np.float32)) * q3.astype(np.float32)
     assert _bits_equal(y, want.astype(np.float32))
+
+
+# ----------------------------------------------------------------------------
+# batched OUT_PROD: which weight a batch reads
+
+def test_batch_weight_hand_table():
+    """Eight gradient batches over two weights: the first four read weight 0,
+    the next four weight 1 (a run of consecutive batches per weight, as a
+    grouped k/v projection shares one weight among neighbouring heads); the
+    second dimension the same way, independently."""
+    assert [oracle.batch_weight(i, 0, 8, 1, 2, 1)[0] for i in range(8)] == [0, 0, 0, 0, 1, 1, 1, 1]
+    assert [oracle.batch_weight(i, 0, 6, 1, 3, 1)[0] for i in range(6)] == [0, 0, 1, 1, 2, 2]
+    assert [oracle.batch_weight(0, i, 1, 4, 1, 4)[1] for i in range(4)] == [0, 1, 2, 3]
+    assert [oracle.batch_weight(2, i, 4, 6, 2, 2) for i in range(6)] == \
+        [(1, 0), (1, 0), (1, 0), (1, 1), (1, 1), (1, 1)]
+    with pytest.raises(ValueError):
+        oracle.batch_weight(0, 0, 6, 1, 4, 1)
+
+
+def test_batched_out_prod_picks_weights_by_value():
+    """Closed form: weight (j2, j3) is the constant c = 1 + j2 + 4 j3 (F16),
+    dY is one-hot, so every output of batch (i2, i3) equals the constant of
+    the weight that batch reads."""
+    N, K, T = 16, 32, 3
+    n2, n3, w_n2, w_n3 = 4, 2, 2, 1
+    consts = [[1.0 + j2 + 4 * j3 for j2 in range(w_n2)] for j3 in range(w_n3)]
+    Ws = [[np.frombuffer(inputs.f32_to_f16_bits(np.full(N * K, c, np.float32)).tobytes(),
+                         dtype=np.uint8) for c in row] for row in consts]
+    dY = np.zeros((T, N), np.float32)
+    dY[np.arange(T), [3, 7, 11]] = 1.0
+    out = oracle.out_prod_batched(inputs.F16, Ws, N, K, [[dY] * n2 for _ in range(n3)], T)
+    want = {(0, 0): 1.0, (1, 0): 1.0, (2, 0): 2.0, (3, 0): 2.0,
+            (0, 1): 1.0, (1, 1): 1.0, (2, 1): 2.0, (3, 1): 2.0}
+    for (i2, i3), c in want.items():
+        assert np.all(out[i3][i2] == c), (i2, i3)
+
+
+def test_batch_weight_mutant_is_caught():
+    """Interleaving the weights (i % w_n, the other plausible reading) fails
+    the hand table."""
+    def interleaved(i2, i3, n2, n3, w_n2, w_n3):
+        return i2 % w_n2, i3 % w_n3
+    assert [interleaved(i, 0, 8, 1, 2, 1)[0] for i in range(8)] != [0, 0, 0, 0, 1, 1, 1, 1]
