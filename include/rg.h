@@ -85,13 +85,22 @@ typedef enum {
                      scales, fp16 d.  Value 128h+32j+16s+l: low bits as Q2_K, minus
                      4 unless bit 4h+j of hmask[16s+l] is set; value d*(sc-32)*q.
                      Rows 16-byte aligned only when K % 2048 == 0 (as Q6_K)     */
-    RG_MXFP4 = 14 /* 17 B / 32 values: E8M0 scale byte e, 16 B nibbles as Q4_0, each
+    RG_MXFP4 = 14,/* 17 B / 32 values: E8M0 scale byte e, 16 B nibbles as Q4_0, each
                      an E2M1 code (OCP microscaling: bit 3 sign, 2 exponent bits,
                      1 mantissa bit: 0, 0.5, 1, 1.5, 2, 3, 4, 6); value
                      E2M1(q) * 2^(e-127) (e = 255: NaN).  Rows 16-byte aligned
                      only when K % 512 == 0, which the tensor-core and small-T
                      variants need.  The tensor-core variants round the values
                      to fp16: block scales outside 2^-24..2^15 lose them       */
+    RG_NVFP4 = 15 /* 36 B / 64 values: four FP8 E4M3 scale bytes d[s] (sign, 4
+                     exponent bits with bias 7, 3 mantissa bits; 0x7f NaN), one
+                     per 16 values, then 32 B of E2M1 codes (as MXFP4): the 16
+                     values of d[s] in bytes 4+8s .. 11+8s, value 16s+j (j < 8)
+                     the low nibble of byte 4+8s+j, 16s+j+8 its high nibble;
+                     value E2M1(q) * E4M3(d[s]).  NVIDIA's second-level,
+                     tensor-wide F32 scale is not part of the block (fold it
+                     into dY or the result).  Every value is exact in fp16
+                     (2^-10 .. 2688), so the tensor-core operands are too    */
 } rg_wtype;
 
 typedef enum {
@@ -228,6 +237,33 @@ int rg_out_prod_ex(int variant, int wtype, const void* W, int64_t N, int64_t K,
                    float beta, void* stream);
 
 /*
+ * ggml's full OUT_PROD surface: two batch dimensions, and fewer weights than
+ * batches, each weight serving a run of consecutive batches (the broadcast a
+ * grouped projection needs, e.g. grouped-query attention's shared k/v
+ * weights).  For i3 < n3, i2 < n2:
+ *     dX_b[t, k] = beta * dX_b[t, k] + sum_n dY_b[t, n] * deq(W_b)[n, k],
+ *     W_b = W + (i2 / (n2 / w_n2)) * w_s2 + (i3 / (n3 / w_n3)) * w_s3   (bytes),
+ *     dY_b[t, n] = dY[i2 * dy_s2 + i3 * dy_s3 + t * dy_t + n * dy_n],
+ *     dX_b[t, k] = dX[i2 * dx_s2 + i3 * dx_s3 + t * dx_t + k]            (elements).
+ * This is the broadcast rule of ggml's out_prod (a weight batch count that
+ * divides the gradient's, per dimension), whose CUDA route the llama.cpp
+ * fork's PR "cuda: out_prod accepts a quantized src0" runs on the dense copy
+ * and whose broadcasting cases its "Measured" section reports skipped.
+ * Rules: w_n2, w_n3 >= 1 dividing n2, n3 (else RG_ERR_SHAPE); strides >= 0;
+ * w_s2, w_s3 multiples of 16 and dx_s2, dx_s3 of 4 (else RG_ERR_ALIGN); the
+ * row rules of rg_out_prod_ex for every batch, all checked before anything
+ * is launched.  Consecutive batches (i2 fastest) that read the same weight
+ * and whose dY and dX rows continue one another's run as one call with
+ * more rows; the others in turn on `stream`.  The batches' dX regions must
+ * not overlap.  n2 == 0 or n3 == 0 is RG_OK.
+ */
+int rg_out_prod_batched(int variant, int wtype, const void* W, int64_t N, int64_t K, int64_t w_n2,
+                        int64_t w_n3, int64_t w_s2, int64_t w_s3, const float* dY, int64_t T,
+                        int64_t dy_t, int64_t dy_n, int64_t dy_s2, int64_t dy_s3, float* dX,
+                        int64_t dx_t, int64_t dx_s2, int64_t dx_s3, int64_t n2, int64_t n3,
+                        float beta, void* stream);
+
+/*
  * The forward mul_mat(W, x) through the same resident weight (the op whose
  * backward rg_out_prod is; llama.cpp fork PR "cuda: out_prod accepts a
  * quantized src0", commit message):
@@ -236,15 +272,23 @@ int rg_out_prod_ex(int variant, int wtype, const void* W, int64_t N, int64_t K,
  *
  * X: [T, K] F32, Y: [T, N] F32 (read only when beta != 0), both row-major
  * and 16-byte aligned; W as for rg_out_prod.  N must be a multiple of 8
- * (RG_ERR_SHAPE).  deq(W)^T is written once per call as a 16-bit [K, N]
- * operand (fp16; bf16 for F32 and BF16 W) in library-pool memory (2*N*K
- * bytes, released on `stream` when the call's kernels finish), X is rounded
- * the same way, and the tensor-core kernel contracts over K with F32
- * accumulation: |err| <= 5e-3 * sum_k |X||deq W| + 1e-7.  T == 0 or N == 0:
- * nothing to do; K == 0: Y = beta * Y.
+ * (RG_ERR_SHAPE).  X is rounded once to a 16-bit copy (fp16; bf16 for F32
+ * and BF16 W) and the tensor-core kernel decodes W's blocks straight into
+ * its operand tiles, now contracting over the K values of each row, with
+ * F32 accumulation: |err| <= 5e-3 * sum_k |X||deq W| + 1e-7; no copy of
+ * deq(W) exists (F32 W: a bf16 copy of W, as rg_out_prod makes).  Rows that
+ * are not 16-byte aligned (Q6_K and Q3_K with K % 2048 != 0, Q2_K with
+ * K % 1024 != 0, MXFP4 with K % 512 != 0) instead decode deq(W)^T once per
+ * call into a transient 16-bit [K, N] copy (2*N*K bytes).  Workspace from
+ * the library's stream-ordered pool (rg_mul_mat_workspace_bytes).  T == 0
+ * or N == 0: nothing to do; K == 0: Y = beta * Y.
  */
 int rg_mul_mat(int wtype, const void* W, int64_t N, int64_t K, const float* X, int64_t T, float* Y,
                float beta, void* stream);
+
+/* Device workspace bytes one rg_mul_mat call of this shape takes from the
+ * pool on the current device (0 for an invalid or empty shape). */
+size_t rg_mul_mat_workspace_bytes(int wtype, int64_t N, int64_t K, int64_t T);
 
 /*
  * The input gradient through the resident weight AND a low-rank adapter
@@ -323,9 +367,9 @@ int rg_dequant_async(int wtype, const void* W, int64_t N, int64_t K, float* out,
 
 /* Stored bytes of one row of K values: K/32*34 (Q8_0), K/32*18 (Q4_0),
  * K/32*20 (Q4_1), K/32*22 (Q5_0), K/32*24 (Q5_1), K/256*144 (Q4_K),
- * K/256*176 (Q5_K), K/256*210 (Q6_K), K/256*84 (Q2_K), K/256*110 (Q3_K), 2K (F16,
- * BF16), 4K (F32); 0 for an unknown type
- * or a K that is not a whole number of blocks. */
+ * K/256*176 (Q5_K), K/256*210 (Q6_K), K/256*84 (Q2_K), K/256*110 (Q3_K),
+ * K/32*17 (MXFP4), K/64*36 (NVFP4), 2K (F16, BF16), 4K (F32); 0 for an
+ * unknown type or a K that is not a whole number of blocks. */
 size_t rg_row_bytes(int wtype, int64_t K);
 
 /* Static, NUL-terminated description of a status code. */

@@ -58,6 +58,9 @@ SIGNATURES = [
     ("rg_out_prod_ex", _I, [_I, _I, _VP, _I64, _I64, _I64, _VP, _I64, _I64, _I64, _I64, _VP, _I64,
                             _I64, _I64, _F, _VP]),
     ("rg_launch_count", ctypes.c_uint64, []),
+    ("rg_mul_mat_workspace_bytes", _SZ, [_I, _I64, _I64, _I64]),
+    ("rg_out_prod_batched", _I, [_I, _I, _VP, _I64, _I64, _I64, _I64, _I64, _I64, _VP, _I64, _I64,
+                                 _I64, _I64, _I64, _VP, _I64, _I64, _I64, _I64, _I64, _F, _VP]),
 ]
 
 RG_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -127,8 +130,19 @@ def rg_out_prod_ex(variant, wtype, W, N, K, w_batch_bytes, dY, T, dy_t, dy_n, dy
                                  _stream(stream))
 
 
+def rg_out_prod_batched(variant, wtype, W, N, K, w_n2, w_n3, w_s2, w_s3, dY, T, dy_t, dy_n, dy_s2,
+                        dy_s3, dX, dx_t, dx_s2, dx_s3, n2, n3, beta, stream=None) -> int:
+    return load().rg_out_prod_batched(variant, wtype, _ptr(W), N, K, w_n2, w_n3, w_s2, w_s3,
+                                      _ptr(dY), T, dy_t, dy_n, dy_s2, dy_s3, _ptr(dX), dx_t, dx_s2,
+                                      dx_s3, n2, n3, beta, _stream(stream))
+
+
 def rg_mul_mat(wtype, W, N, K, X, T, Y, beta, stream=None) -> int:
     return load().rg_mul_mat(wtype, _ptr(W), N, K, _ptr(X), T, _ptr(Y), beta, _stream(stream))
+
+
+def rg_mul_mat_workspace_bytes(wtype, N, K, T) -> int:
+    return load().rg_mul_mat_workspace_bytes(wtype, N, K, T)
 
 
 def rg_out_prod_lora(variant, wtype, W, N, K, dY, T, dX, beta, lora_a, lora_b, rank, scale,

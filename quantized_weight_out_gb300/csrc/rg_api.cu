@@ -278,8 +278,8 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
   // F32 W: both operands in bf16 (the F32 range); W's copy is [N, K]
   const bool bf16 = wtype == RG_BF16 || wtype == RG_F32;
   const int64_t ld = tc_dy16_ld(N);
-  e = launch_convert_dy(dY, T, N, lay.dy_t, lay.dy_n, ld, bf16, static_cast<uint16_t*>(buf), *dev,
-                        stream);
+  uint16_t* dy16 = static_cast<uint16_t*>(buf);
+  e = launch_convert_dy(dY, T, N, lay.dy_t, lay.dy_n, ld, bf16, dy16, *dev, stream);
   const void* Wtc = W;
   int wtc = wtype;
   if (wtype == RG_F32) {
@@ -293,7 +293,7 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
   t_prof_before = t_prof_after = nullptr;
   if (e == cudaSuccess && ev0) e = cudaEventRecord(ev0, stream);
   if (e == cudaSuccess)
-    e = launch_tc(wtc, Wtc, N, K, static_cast<const uint16_t*>(buf), ld, T, dX, lay.dx_t, beta,
+    e = launch_tc(wtc, Wtc, N, K, dy16, ld, T, dX, lay.dx_t, beta,
                   reinterpret_cast<float*>(static_cast<char*>(buf) +
                                            tc_partial_offset(wtype, N, K, T)),
                   *dev, stream, cg_force_of(variant));
@@ -431,32 +431,59 @@ int rg_out_prod_variant(int variant, int wtype, const void* W, int64_t N, int64_
              static_cast<cudaStream_t>(stream), Layout{N, 1, K});
 }
 
+int rg_out_prod_batched(int variant, int wtype, const void* W, int64_t N, int64_t K, int64_t w_n2,
+                        int64_t w_n3, int64_t w_s2, int64_t w_s3, const float* dY, int64_t T,
+                        int64_t dy_t, int64_t dy_n, int64_t dy_s2, int64_t dy_s3, float* dX,
+                        int64_t dx_t, int64_t dx_s2, int64_t dx_s3, int64_t n2, int64_t n3,
+                        float beta, void* stream) {
+  if (n2 < 0 || n3 < 0 || w_n2 < 1 || w_n3 < 1 || w_s2 < 0 || w_s3 < 0 || dy_s2 < 0 ||
+      dy_s3 < 0 || dx_s2 < 0 || dx_s3 < 0)
+    return RG_ERR_ARG;
+  if (n2 == 0 || n3 == 0) return RG_OK;
+  if (n2 % w_n2 || n3 % w_n3) return RG_ERR_SHAPE;
+  if (w_s2 % 16 || w_s3 % 16 || dx_s2 % 4 || dx_s3 % 4) return RG_ERR_ALIGN;
+  if (n2 > kMaxDim / n3) return RG_ERR_ARG;
+  const Layout lay{dy_t, dy_n, dx_t};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // batch (i2, i3) reads weight (i2 / r2, i3 / r3): each weight serves r2 x r3 batches
+  const int64_t r2 = n2 / w_n2, r3 = n3 / w_n3, total = n2 * n3;
+  auto w_of = [&](int64_t i) {
+    return static_cast<const uint8_t*>(W) + (i % n2) / r2 * w_s2 + (i / n2) / r3 * w_s3;
+  };
+  auto dy_off = [&](int64_t i) { return (i % n2) * dy_s2 + (i / n2) * dy_s3; };
+  auto dx_off = [&](int64_t i) { return (i % n2) * dx_s2 + (i / n2) * dx_s3; };
+  // every batch's pointers before the first launch
+  for (int64_t i = 0; i < total; ++i) {
+    bool empty = false;
+    const int st = validate(wtype, w_of(i), N, K, dY + dy_off(i), T, dX + dx_off(i), lay, &empty);
+    if (st != RG_OK) return st;
+  }
+  // consecutive batches (i2 fastest) that read the same weight and whose dY
+  // and dX rows continue one another's (batch i + c starts c * T rows on)
+  // are one call with that many times T rows
+  for (int64_t i = 0; i < total;) {
+    int64_t c = 1;
+    while (i + c < total && w_of(i + c) == w_of(i) && dy_off(i + c) == dy_off(i) + c * T * dy_t &&
+           dx_off(i + c) == dx_off(i) + c * T * dx_t && T * (c + 1) <= kMaxDim)
+      ++c;
+    const int st = run(variant, wtype, w_of(i), N, K, dY + dy_off(i), T * c, dX + dx_off(i), beta,
+                       nullptr, 0, true, s, lay);
+    if (st != RG_OK) return st;
+    i += c;
+  }
+  return RG_OK;
+}
+
 int rg_out_prod_ex(int variant, int wtype, const void* W, int64_t N, int64_t K,
                    int64_t w_batch_bytes, const float* dY, int64_t T, int64_t dy_t, int64_t dy_n,
                    int64_t dy_batch, float* dX, int64_t dx_t, int64_t dx_batch, int64_t batch,
                    float beta, void* stream) {
-  if (batch < 0 || w_batch_bytes < 0 || dy_batch < 0 || dx_batch < 0) return RG_ERR_ARG;
+  if (batch < 0 || w_batch_bytes < 0) return RG_ERR_ARG;
   if (batch == 0) return RG_OK;
-  if (w_batch_bytes % 16 || dx_batch % 4) return RG_ERR_ALIGN;
-  const Layout lay{dy_t, dy_n, dx_t};
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // batches that tile one taller dY / dX under a shared W are one call
-  if (batch > 1 && w_batch_bytes == 0 && dy_n == 1 && dy_batch == T * dy_t &&
-      dx_batch == T * dx_t && T * batch <= kMaxDim)
-    return run(variant, wtype, W, N, K, dY, T * batch, dX, beta, nullptr, 0, true, s, lay);
-  // validate every batch's pointers before the first launch
-  for (int64_t b = 0; b < batch; ++b) {
-    bool empty = false;
-    const int st = validate(wtype, static_cast<const uint8_t*>(W) + b * w_batch_bytes, N, K,
-                            dY + b * dy_batch, T, dX + b * dx_batch, lay, &empty);
-    if (st != RG_OK) return st;
-  }
-  for (int64_t b = 0; b < batch; ++b) {
-    const int st = run(variant, wtype, static_cast<const uint8_t*>(W) + b * w_batch_bytes, N, K,
-                       dY + b * dy_batch, T, dX + b * dx_batch, beta, nullptr, 0, true, s, lay);
-    if (st != RG_OK) return st;
-  }
-  return RG_OK;
+  // one batch dimension: a weight per batch, or one shared by all of them
+  return rg_out_prod_batched(variant, wtype, W, N, K, w_batch_bytes ? batch : 1, 1, w_batch_bytes, 0,
+                             dY, T, dy_t, dy_n, dy_batch, 0, dX, dx_t, dx_batch, 0, batch, 1, beta,
+                             stream);
 }
 
 size_t rg_workspace_bytes(int variant, int wtype, int64_t N, int64_t K, int64_t T) {
@@ -503,6 +530,34 @@ int rg_select_variant(int wtype, int64_t N, int64_t K, int64_t T) {
   return select_variant(wtype, N, K, T);
 }
 
+namespace {
+
+// Workspace of the forward: X's 16-bit copy [T, round8(K)], F32 W's bf16
+// copy [N, K] (the tensor cores take no F32), a split contraction's partial
+// sums [n_splits][T][N]; each 256-byte aligned.  Plans without stream-K.
+// Rows that TMA cannot read (aligned_rows false) take the transient route:
+// w16 is then the dense 16-bit deq(W)^T [K, N] the OUT_PROD kernel reads.
+struct MmWs {
+  size_t x16, w16, parts;
+  size_t total() const { return x16 + w16 + parts; }
+};
+MmWs mm_workspace(int wtype, int64_t N, int64_t K, int64_t T, const DevInfo& dev) {
+  const NoStreamK no_stream_k;
+  if (!aligned_rows(wtype, K))
+    return MmWs{tc_workspace(K, T), (static_cast<size_t>(K) * static_cast<size_t>(N) * 2 + 255) / 256 * 256,
+                tc_partial_bytes(K, N, T, dev, 0)};
+  return MmWs{tc_workspace(K, T), tc_w16_bytes(wtype, N, K), tc_partial_bytes(K, N, T, dev, 0)};
+}
+
+}  // namespace
+
+size_t rg_mul_mat_workspace_bytes(int wtype, int64_t N, int64_t K, int64_t T) {
+  if (!valid_wtype(wtype) || N <= 0 || K <= 0 || T <= 0) return 0;
+  DevInfo* dev = nullptr;
+  if (current_dev(&dev) != RG_OK) return 0;
+  return mm_workspace(wtype, N, K, T, *dev).total();
+}
+
 int rg_mul_mat(int wtype, const void* W, int64_t N, int64_t K, const float* X, int64_t T, float* Y,
                float beta, void* stream) {
   if (!valid_wtype(wtype)) return RG_ERR_TYPE;
@@ -520,28 +575,41 @@ int rg_mul_mat(int wtype, const void* W, int64_t N, int64_t K, const float* X, i
   if (st != RG_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) return from_cuda(launch_scale(Y, T, N, N, beta, *dev, s));
-  // the tensor-core product with deq(W)^T [K, N] as a dense 16-bit weight of
-  // K rows: Y = X . deq(W)^T is an OUT_PROD over that weight
+  // Y = X . deq(W)^T: the tensor-core kernel decodes W's blocks as the
+  // K-major operand of a contraction over each row's K values; X is rounded
+  // to the 16-bit kind once (F32 W: both W and X to bf16)
+  const NoStreamK no_stream_k;
   const bool bf16 = wtype == RG_BF16 || wtype == RG_F32;
-  const size_t wt_bytes = (static_cast<size_t>(K) * static_cast<size_t>(N) * 2 + 255) / 256 * 256;
-  const size_t x16 = tc_workspace(K, T);
-  const size_t parts = tc_partial_bytes(K, N, T, *dev, 0);
+  const MmWs ws = mm_workspace(wtype, N, K, T, *dev);
   cudaMemPool_t pool{};
   if ((st = pool_for(dev->device, &pool)) != RG_OK) return st;
   void* buf = nullptr;
-  if (cudaMallocFromPoolAsync(&buf, wt_bytes + x16 + parts, pool, s) != cudaSuccess) return RG_ERR_CUDA;
+  if (cudaMallocFromPoolAsync(&buf, ws.total(), pool, s) != cudaSuccess) return RG_ERR_CUDA;
   char* b = static_cast<char*>(buf);
-  uint16_t* wt = reinterpret_cast<uint16_t*>(b);
-  uint16_t* xh = reinterpret_cast<uint16_t*>(b + wt_bytes);
-  float* part = reinterpret_cast<float*>(b + wt_bytes + x16);
-  cudaError_t e = launch_dequant_t16(wtype, W, N, K, bf16, wt, N, *dev, s);
+  uint16_t* xh = reinterpret_cast<uint16_t*>(b);
+  uint16_t* w16 = reinterpret_cast<uint16_t*>(b + ws.x16);
+  float* part = reinterpret_cast<float*>(b + ws.x16 + ws.w16);
   const int64_t ld = tc_dy16_ld(K);
+  const bool fused = aligned_rows(wtype, K);
+  // rows whose 16-byte windows TMA cannot address (Q6_K and Q3_K rows with
+  // K % 2048 != 0, Q2_K K % 1024, MXFP4 K % 512): a transient dense 16-bit
+  // deq(W)^T, contracted by the OUT_PROD kernel as a weight of K rows
+  cudaError_t e = fused ? cudaSuccess : launch_dequant_t16(wtype, W, N, K, bf16, w16, N, *dev, s);
   if (e == cudaSuccess) e = launch_convert_dy(X, T, K, K, 1, ld, bf16, xh, *dev, s);
+  const void* Wtc = W;
+  int wtc = wtype;
+  if (wtype == RG_F32 && fused) {
+    if (e == cudaSuccess)
+      e = launch_convert_dy(static_cast<const float*>(W), N, K, K, 1, K, true, w16, *dev, s);
+    Wtc = w16;
+    wtc = RG_BF16;
+  }
   cudaEvent_t ev0 = t_prof_before, ev1 = t_prof_after;
   t_prof_before = t_prof_after = nullptr;
   if (e == cudaSuccess && ev0) e = cudaEventRecord(ev0, s);
   if (e == cudaSuccess)
-    e = launch_tc(bf16 ? RG_BF16 : RG_F16, wt, K, N, xh, ld, T, Y, N, beta, part, *dev, s, 0);
+    e = fused ? launch_mm(wtc, Wtc, N, K, xh, ld, T, Y, N, beta, part, *dev, s, 0)
+              : launch_tc(bf16 ? RG_BF16 : RG_F16, w16, K, N, xh, ld, T, Y, N, beta, part, *dev, s, 0);
   if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, s);
   const cudaError_t f = cudaFreeAsync(buf, s);
   if (e == cudaSuccess) e = f;

@@ -19,12 +19,13 @@ namespace rg {
 // ---------------------------------------------------------------------------
 // storage formats: values per block, bytes per block
 
-__host__ __device__ constexpr bool valid_wtype(int wt) { return wt >= RG_F16 && wt <= RG_MXFP4; }
+__host__ __device__ constexpr bool valid_wtype(int wt) { return wt >= RG_F16 && wt <= RG_NVFP4; }
 __host__ __device__ constexpr bool is_quant(int wt) {
   return valid_wtype(wt) && wt != RG_F16 && wt != RG_BF16 && wt != RG_F32;
 }
 __host__ __device__ constexpr int block_values(int wt) {
   return (wt == RG_Q4_K || wt == RG_Q5_K || wt == RG_Q6_K || wt == RG_Q2_K || wt == RG_Q3_K) ? 256
+         : wt == RG_NVFP4                                                                 ? 64
          : is_quant(wt)                                                                   ? 32
                                                                                           : 1;
 }
@@ -40,6 +41,7 @@ __host__ __device__ constexpr int block_bytes(int wt) {
          : wt == RG_Q5_0 ? 22
          : wt == RG_Q5_1 ? 24
          : wt == RG_MXFP4 ? 17
+         : wt == RG_NVFP4 ? 36
          : wt == RG_F32  ? 4
                          : 2;
 }
@@ -409,9 +411,33 @@ __device__ __forceinline__ float e2m1_f32(uint32_t c) {
   return __uint_as_float(mag | ((c & 8u) << 28));
 }
 
+// FP8 E4M3 (NVFP4's micro-block scale): bit 7 sign, 4 exponent bits (bias
+// 7), 3 mantissa bits; exponent 0 is m/8 * 2^-6, 0x7f / 0xff NaN, no
+// infinities.  Exact in F32 (and in fp16: 2^-9 .. 448, four significant bits).
+__device__ __forceinline__ float e4m3_f32(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  float mag;
+  if (e == 0)
+    mag = static_cast<float>(m) * 0.001953125f;  // m * 2^-9, exact
+  else
+    mag = __uint_as_float(((e + 120u) << 23) | (m << 20));  // (1 + m/8) * 2^(e - 7)
+  if (e == 15 && m == 7) mag = __uint_as_float(0x7FC00000u);
+  return (c & 0x80u) ? -mag : mag;
+}
+
 template <int WT>
 __device__ __forceinline__ void decode8_f32(const uint8_t* row, int k0, float (&out)[8]) {
-  if constexpr (WT == RG_MXFP4) {
+  if constexpr (WT == RG_NVFP4) {
+    // E2M1(code) * E4M3(d[s]): an exact product (two and four significant
+    // bits); values 8h .. 8h+7 of micro-block s are the low (h = 0) or high
+    // (h = 1) nibbles of its eight bytes
+    const uint8_t* blk = row + (k0 >> 6) * 36;
+    const int v0 = k0 & 63, s = v0 >> 4, shift = (v0 & 8) ? 4 : 0;
+    const float sc = e4m3_f32(blk[s]);
+    const uint8_t* qs = blk + 4 + 8 * s;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) out[i] = e2m1_f32((qs[i] >> shift) & 15u) * sc;
+  } else if constexpr (WT == RG_MXFP4) {
     // E2M1(code) * 2^(e - 127): an exact product (a power of two times a
     // two-bit significand; subnormal and overflowing results as IEEE gives)
     const uint8_t* blk = row + (k0 >> 5) * 17;

@@ -52,6 +52,7 @@ R with_wtype(int wtype, R fallback, F&& f) {
     case RG_Q2_K: return f(std::integral_constant<int, RG_Q2_K>{});
     case RG_Q3_K: return f(std::integral_constant<int, RG_Q3_K>{});
     case RG_MXFP4: return f(std::integral_constant<int, RG_MXFP4>{});
+    case RG_NVFP4: return f(std::integral_constant<int, RG_NVFP4>{});
     case RG_F32: return f(std::integral_constant<int, RG_F32>{});
     default: return fallback;
   }
@@ -198,7 +199,18 @@ cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint
                       int64_t ld_dy16, int64_t T, float* dX, int64_t dx_t, float beta, float* part,
                       const DevInfo& dev, cudaStream_t stream, int cg_force,
                       const uint16_t* a16 = nullptr, int64_t rank = 0);
+// k units per rasterization band of a plan (see launch_tc).
+int tc_band(int wtype, int64_t n_contr, const TcPlan& p);
 int64_t tc_adapter_cols(int64_t N, int64_t rank);
+// The forward mul_mat (rg_mm.cu): Y [T, N] (rows ldy apart) = beta * Y +
+// X . deq(W)^T for W of N rows of K values (decoded inside the tensor-core
+// kernel, contracted over each row's K values), x16 X's 16-bit copy [T, K]
+// (rows ld_x16 apart); part: [n_splits][T][N] partial sums when the plan of
+// (contraction K, output N, T) splits the contraction.  Stream-K is never
+// taken (call it under NoStreamK).
+cudaError_t launch_mm(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* x16,
+                      int64_t ld_x16, int64_t T, float* Y, int64_t ldy, float beta, float* part,
+                      const DevInfo& dev, cudaStream_t stream, int cg_force);
 // Number of partial-sum slabs the tensor-core plan needs (0 when unsplit).
 int64_t tc_partial_splits(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force);
 // Bytes of the `part` workspace the tensor-core plan needs: the splits'

@@ -34,7 +34,8 @@ struct Raw {
   uint32_t v[WT == RG_Q5_K || WT == RG_F32 ? 8
              : WT == RG_Q4_K                  ? 6
              : WT == RG_Q6_K || WT == RG_Q3_K ? 5
-             : (WT == RG_Q8_0 || WT == RG_Q4_0 || WT == RG_Q4_1 || WT == RG_MXFP4) ? 3
+             : (WT == RG_Q8_0 || WT == RG_Q4_0 || WT == RG_Q4_1 || WT == RG_MXFP4 ||
+                WT == RG_NVFP4)                                                       ? 3
                                                                                     : 4];
 };
 
@@ -68,6 +69,16 @@ __device__ __forceinline__ void load_raw_smem(const uint8_t* tile, int lane, Raw
              (static_cast<uint32_t>(q[2]) << 16) | (static_cast<uint32_t>(q[3]) << 24);
     r.v[2] = static_cast<uint32_t>(q[4]) | (static_cast<uint32_t>(q[5]) << 8) |
              (static_cast<uint32_t>(q[6]) << 16) | (static_cast<uint32_t>(q[7]) << 24);
+  } else if constexpr (WT == RG_NVFP4) {
+    // values 8 lane .. +7: micro-block s = (lane & 7) >> 1 of block lane >> 3
+    // (36-byte blocks from a 16-byte aligned tile): its scale byte and its 8
+    // code bytes (low nibbles for even lanes, high for odd)
+    const uint8_t* blk = tile + 36 * (lane >> 3);
+    const int s = (lane & 7) >> 1;
+    const uint32_t* q = reinterpret_cast<const uint32_t*>(blk + 4 + 8 * s);
+    r.v[0] = blk[s];
+    r.v[1] = q[0];
+    r.v[2] = q[1];
   } else if constexpr (WT == RG_Q4_1) {
     const uint8_t* blk = tile + 20 * (lane >> 2);
     const uint32_t* q = reinterpret_cast<const uint32_t*>(blk + 4 + 8 * (lane & 1));
@@ -185,6 +196,16 @@ __device__ __forceinline__ void decode_raw(const Raw<WT>& r, int lane, float (&w
     // of the block, high nibbles for the rest)
     const float sc = e8m0_f32(r.v[0]);
     const int shift = (lane & 2) ? 4 : 0;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint32_t x = r.v[1 + j] >> shift;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) w[4 * j + b] = e2m1_f32((x >> (8 * b)) & 15u) * sc;
+    }
+  } else if constexpr (WT == RG_NVFP4) {
+    // E2M1(code) * E4M3(scale): exact
+    const float sc = e4m3_f32(r.v[0]);
+    const int shift = (lane & 1) ? 4 : 0;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const uint32_t x = r.v[1 + j] >> shift;
@@ -330,7 +351,9 @@ template <int WT, int TB>
 constexpr bool mma_path() { return WT == RG_Q4_K; }
 template <int WT, int TB>
 constexpr bool rows_path() {
-  return TB <= 2 && is_quant(WT) && !windowed<WT>() && !mma_path<WT, TB>();
+  // (NVFP4's 16-value scales do not fit the block-per-warp layout: it takes
+  // the eight-values-a-lane consumer)
+  return TB <= 2 && is_quant(WT) && !windowed<WT>() && !mma_path<WT, TB>() && WT != RG_NVFP4;
 }
 template <int WT, int TB>
 constexpr int stage_rows() { return rows_path<WT, TB>() || mma_path<WT, TB>() ? 64 : 32; }

@@ -95,6 +95,15 @@ cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint
                                       stream, cg_force, nullptr, 0);
 }
 
+int tc_band(int wtype, int64_t n_contr, const TcPlan& p) {
+  // k units whose slice of W (128 cg values of every contraction row, or the
+  // forward's 128 cg rows of n_contr values) fits comfortably in L2 (48 MB)
+  const double w_per_value =
+      is_quant(wtype) ? static_cast<double>(block_bytes(wtype)) / block_values(wtype) : 2.0;
+  const double slice = static_cast<double>(n_contr) * (tc::BM * p.cg) * w_per_value;
+  return static_cast<int>(std::max(1.0, std::min<double>(p.n_kunits, 48.0 * 1024 * 1024 / slice)));
+}
+
 // Warp slices of the shared tiles: slice (x, req) is tile x (item n_dp + x
 // of the plan's banded order), CTA half r and epilogue warp eq (req = 4r +
 // eq): 32 values of k by bt rows of t.  The piece with the tile's first

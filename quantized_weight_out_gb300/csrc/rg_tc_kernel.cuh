@@ -66,7 +66,8 @@ constexpr int SMEM_BUDGET = 224 * 1024;
 // Q6_K the whole 210-byte super-block inside a 240-byte window that starts at
 // the 16-byte grain before it (0..14 bytes in; 15 chunks keep eight rows in
 // distinct bank groups), MXFP4 four 17-byte blocks (68 B, 0, 4, 8 or 12
-// bytes into the grain) inside 112 B (7 chunks: distinct bank groups).
+// bytes into the grain) inside 112 B (7 chunks: distinct bank groups), NVFP4
+// two 36-byte blocks (72 B, 0 or 8 bytes in) inside 80 B (as Q4_0).
 template <int WT>
 __host__ __device__ constexpr int p_row_bytes() {
   return WT == RG_Q8_0   ? 144
@@ -80,17 +81,23 @@ __host__ __device__ constexpr int p_row_bytes() {
          : WT == RG_Q3_K ? 128
          : WT == RG_Q2_K ? 96
          : WT == RG_MXFP4 ? 112
+         : WT == RG_NVFP4 ? 80
                          : 0;
 }
 
-template <int WT, int CG, int BT>
+template <int WT, int CG, int BT, bool FWD = false>
 struct Cfg {
   static constexpr bool QUANT = is_quant(WT);
   static constexpr bool BF = WT == RG_BF16;
-  static constexpr int P_STAGE = QUANT ? ((BC * p_row_bytes<WT>() + 1023) / 1024) * 1024 : 0;
+  // rows of W in a packed-window stage: the OUT_PROD's 64 contraction rows,
+  // or the forward's 128 output rows (FWD: the contraction runs along the rows)
+  static constexpr int P_ROWS = FWD ? 2 * BC : BC;
+  static constexpr int P_STAGE = QUANT ? ((P_ROWS * p_row_bytes<WT>() + 1023) / 1024) * 1024 : 0;
   static constexpr int STAGE = A_STAGE + B_STAGE + P_STAGE;
-  // quantized: five slots, each decoded by two warps; F16/BF16: as deep as fits
-  static constexpr int S = QUANT ? (WT == RG_Q6_K ? 4 : 5) : std::min(8, SMEM_BUDGET / STAGE);
+  // quantized: five slots (the forward: as many as fit, at most five), each
+  // decoded by two warps; F16/BF16: as deep as fits
+  static constexpr int S = QUANT ? (FWD ? std::min(5, SMEM_BUDGET / STAGE) : (WT == RG_Q6_K ? 4 : 5))
+                                 : std::min(8, SMEM_BUDGET / STAGE);
   static constexpr int WARPS_PER_SLOT = QUANT ? 2 : 0;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + S * A_STAGE;
@@ -101,12 +108,14 @@ struct Cfg {
   static constexpr int NUM_BARS = 4 * S + 5;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024 B alignment
-  static constexpr uint32_t P_BYTES = QUANT ? BC * p_row_bytes<WT>() : 0;
+  static constexpr uint32_t P_BYTES = QUANT ? P_ROWS * p_row_bytes<WT>() : 0;
   // operand bytes of one stage over the whole pair (B halves, and A for F16/BF16)
   static constexpr uint32_t AB_BYTES_PAIR = CG * (B_STAGE + (QUANT ? 0 : A_STAGE));
   static constexpr uint32_t TMEM_COLS = 2 * BT;
   static constexpr int MMA_M = BM * CG;
-  static constexpr uint32_t IDESC = idesc_f16(BF, MMA_M, BT, /*A MN-major*/ true, /*B*/ false);
+  // A: the OUT_PROD's deq(W)^T is MN-major (k along a stored row is M); the
+  // forward's deq(W) is K-major (the row is the contraction)
+  static constexpr uint32_t IDESC = idesc_f16(BF, MMA_M, BT, /*A MN-major*/ !FWD, /*B*/ false);
   // the slot's decoder warps of every CTA of the pair
   static constexpr uint32_t FULL_DEC_COUNT = (QUANT ? WARPS_PER_SLOT : 1) * CG;
   static constexpr uint32_t ACC_EMPTY_COUNT = 4 * CG;
@@ -283,6 +292,57 @@ __device__ __forceinline__ void dec_mxfp4_block(const uint8_t* row, uint8_t* A, 
   st_a_chunk(A, n, 4 * B + 3, hi[4], hi[5], hi[6], hi[7]);
 }
 
+// Two E4M3 bytes (bits 0-7 and 8-15 of w) -> their fp16 pair, exactly: the
+// seven magnitude bits shifted into an fp16's exponent and mantissa fields
+// give 2^(e-15) (1 + m/8), or for e = 0 the fp16 subnormal m/8 2^-14, so one
+// multiply by 2^8 (exact) rebiases both to E4M3's 2^(e-7) (1 + m/8) and
+// m 2^-9; then the sign, and NaN for the magnitude code 0x7f.
+__device__ __forceinline__ __half2 e4m3x2_f16(uint32_t w) {
+  const uint32_t mag = ((w & 0x7Fu) << 7) | ((w & 0x7F00u) << 15);
+  uint32_t r = h2_as_u32(__hmul2(u32_as_h2(mag), __float2half2_rn(256.0f))) |
+               ((w & 0x80u) << 8) | ((w & 0x8000u) << 16);
+  if ((w & 0x7Fu) == 0x7Fu) r = (r & 0xFFFF0000u) | 0x7E00u;
+  if ((w & 0x7F00u) == 0x7F00u) r = (r & 0x0000FFFFu) | 0x7E000000u;
+  return u32_as_h2(r);
+}
+
+// NVFP4 item B of a 128-value tile (values 32B .. 32B+31): micro-blocks
+// s0 = 2(B & 1) and s0 + 1 of the 36-byte block B >> 1, which starts
+// o + 36 (B >> 1) bytes into the row window (o = 0 or 8, a run-time value:
+// one code path for both offsets, so the decoders' instructions stay few).
+// The block's bytes lie from chunk 2 (B >> 1) on, word (B >> 1) + o / 4 of
+// them first: its scales (bytes s0, s0 + 1), then the item's 16 code bytes
+// at 4 + 8 s0; micro-block s gives 8 values from the low nibbles of its 8
+// bytes, then 8 from the high nibbles.  E2M1 codes become fp16 by the byte
+// lookup and the product with the scale is exact in fp16 (six significant
+// bits, magnitudes 2^-10 .. 2688).  Writes chunks 4B .. 4B+3 of row n.
+template <int B>
+__device__ __forceinline__ void dec_nvfp4_item(const uint8_t* row, uint8_t* A, int n, int o) {
+  constexpr int C0 = 2 * (B >> 1), J0 = B >> 1, NCH = (B & 1) ? 3 : 2;
+  static_assert(16 * (C0 + NCH) <= p_row_bytes<RG_NVFP4>(), "reads stay inside the row window");
+  const auto r = load_chunks<C0, C0 + NCH - 1>(row);
+  const bool o8 = o != 0;
+  auto word = [&](int k) { return o8 ? r.w[J0 + 2 + k] : r.w[J0 + k]; };  // k-th word of the block
+  const __half2 sc2 = e4m3x2_f16(word(0) >> (16 * (B & 1)));
+  const __half2 sc0 = __low2half2(sc2), sc1 = __high2half2(sc2);
+  uint32_t out[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {  // code word j: bytes 4j .. 4j+3 of the item's 16
+    const uint32_t w = word(1 + 4 * (B & 1) + j);
+    const __half2 sc = j < 2 ? sc0 : sc1;
+    const int c = 2 * (j >> 1);  // chunk of the low nibbles: 0 (s0) or 2 (s1)
+    uint32_t a0, a1, b0, b1;
+    e2m1x4_f16(w & 0x0F0F0F0Fu, a0, a1);
+    e2m1x4_f16((w >> 4) & 0x0F0F0F0Fu, b0, b1);
+    out[c][2 * (j & 1)] = h2_as_u32(__hmul2(u32_as_h2(a0), sc));
+    out[c][2 * (j & 1) + 1] = h2_as_u32(__hmul2(u32_as_h2(a1), sc));
+    out[c + 1][2 * (j & 1)] = h2_as_u32(__hmul2(u32_as_h2(b0), sc));
+    out[c + 1][2 * (j & 1) + 1] = h2_as_u32(__hmul2(u32_as_h2(b1), sc));
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) st_a_chunk(A, n, 4 * B + c, out[c][0], out[c][1], out[c][2], out[c][3]);
+}
+
 __device__ __forceinline__ uint32_t byte_of(uint32_t h1, uint32_t h2, uint32_t h3, int i) {
   const uint32_t w = i < 4 ? h1 : (i < 8 ? h2 : h3);
   return (w >> (8 * (i & 3))) & 0xFFu;
@@ -423,8 +483,9 @@ __device__ __forceinline__ void dec_q5_k_part(const uint8_t* row, uint8_t* A, in
 // Q6_K: a whole row's half (128 values, H = the half) from a window whose
 // super-block starts O bytes in.  Value 128H + 32i + l: nibble of
 // ql[64H + 32(i%2) + l] (high for i >= 2) and bits 2i..2i+1 of qh[32H + l]
-// give q; the operand is fp16(d * sc[8H + 2i + l/16]) * (q - 32).
-template <int O, int H>
+// give q; the operand is fp16(d * sc[8H + 2i + l/16]) * (q - 32).  G >= 0:
+// only the 64 values 64G .. 64G+63 of the half (chunks 8G .. 8G+7).
+template <int O, int H, int G = -1>
 __device__ __forceinline__ void dec_q6_k_row(const uint8_t* row, uint8_t* A, int n) {
   constexpr int QA = O + 64 * H, QHB = O + 128 + 32 * H, QS = O + 192 + 8 * H, QD = O + 208;
   // the last byte a word_at at offset x (relative to chunk C) reads
@@ -462,10 +523,12 @@ __device__ __forceinline__ void dec_q6_k_row(const uint8_t* row, uint8_t* A, int
                              ((a >> 4) & 0x0F0F0F0Fu) | (((hq >> 4) & 0x03030303u) << 4),
                              ((b >> 4) & 0x0F0F0F0Fu) | (((hq >> 6) & 0x03030303u) << 4)};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) four_scaled(x[i], off, ds[i][cq >> 1], o[i][2 * jj], o[i][2 * jj + 1]);
+      for (int i = 0; i < 4; ++i)
+        if (G < 0 || (i >> 1) == G) four_scaled(x[i], off, ds[i][cq >> 1], o[i][2 * jj], o[i][2 * jj + 1]);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) st_a_chunk(A, n, 4 * i + cq, o[i][0], o[i][1], o[i][2], o[i][3]);
+    for (int i = 0; i < 4; ++i)
+      if (G < 0 || (i >> 1) == G) st_a_chunk(A, n, 4 * i + cq, o[i][0], o[i][1], o[i][2], o[i][3]);
   }
 }
 
@@ -473,7 +536,8 @@ __device__ __forceinline__ void dec_q6_k_row(const uint8_t* row, uint8_t* A, int
 // super-block starts O bytes in (O = 0, 4, 8, 12).  Value 128H + 32j + 16s
 // + l: bits 2j..2j+1 of qs[32H + 16s + l]; its scales byte 8H + 2j + s gives
 // sc (low nibble) and m; the operand is fp16(q * fp16(d*sc) - fp16(dmin*m)).
-template <int O, int H>
+// G >= 0: only the 64 values 64G .. 64G+63 of the half.
+template <int O, int H, int G = -1>
 __device__ __forceinline__ void dec_q2_k_row(const uint8_t* row, uint8_t* A, int n) {
   constexpr int QSB = O + 8 * H, QQ = O + 16 + 32 * H, QD = O + 80;
   static_assert(O % 4 == 0 && QD + 4 <= p_row_bytes<RG_Q2_K>(), "aligned words inside the window");
@@ -492,6 +556,7 @@ __device__ __forceinline__ void dec_q2_k_row(const uint8_t* row, uint8_t* A, int
   for (int j = 0; j < 4; ++j)
 #pragma unroll
     for (int sb = 0; sb < 2; ++sb) {
+      if (G >= 0 && (j >> 1) != G) continue;
       const uint32_t b = (sw[j >> 1] >> (8 * (2 * (j & 1) + sb))) & 0xFFu;  // byte 2j + sb
       const __half2 ds = __float2half2_rn(d * static_cast<float>(b & 15u));       // exact product
       const __half2 nm = __float2half2_rn(-(dmin * static_cast<float>(b >> 4)));  // exact product
@@ -510,7 +575,8 @@ __device__ __forceinline__ void dec_q2_k_row(const uint8_t* row, uint8_t* A, int
 // (O even).  Value 128H + 32j + 16s + l: q + 4 = (bits 2j..2j+1 of
 // qs[32H + 16s + l]) | (bit 4H + j of hmask[16s + l]) << 2; the sub-block's
 // 6-bit scale i = 8H + 2j + s; the operand is fp16(d * (sc - 32)) * q.
-template <int O, int H>
+// G >= 0: only the 64 values 64G .. 64G+63 of the half.
+template <int O, int H, int G = -1>
 __device__ __forceinline__ void dec_q3_k_row(const uint8_t* row, uint8_t* A, int n) {
   constexpr int QH = O, QQ = O + 32 + 32 * H, QS = O + 96, QD = O + 108;
   constexpr auto last = [](int x) { return (x & 3) == 0 ? x + 3 : (x & ~3) + 7; };
@@ -534,6 +600,7 @@ __device__ __forceinline__ void dec_q3_k_row(const uint8_t* row, uint8_t* A, int
   for (int j = 0; j < 4; ++j)
 #pragma unroll
     for (int sb = 0; sb < 2; ++sb) {
+      if (G >= 0 && (j >> 1) != G) continue;
       const int i = 8 * H + 2 * j + sb;
       const uint32_t lo = (s_lo[(i & 7) >> 2] >> (8 * (i & 3) + 4 * H)) & 15u;
       const uint32_t hi = (s_hi >> (8 * (i & 3) + 2 * (i >> 2))) & 3u;
@@ -558,6 +625,7 @@ __device__ __forceinline__ void dec_q3_k_row(const uint8_t* row, uint8_t* A, int
 template <int WT, int ODD, int B>
 __device__ __forceinline__ void dec_item(const uint8_t* row, uint8_t* A, int n, int o) {
   if constexpr (WT == RG_MXFP4) dec_mxfp4_block<B>(row, A, n, o);
+  else if constexpr (WT == RG_NVFP4) dec_nvfp4_item<B>(row, A, n, o);
   else if constexpr (WT == RG_Q8_0) dec_q8_block<8 * ODD + 34 * B>(row, A, n, B);
   else if constexpr (WT == RG_Q4_0) dec_q4_0_block<8 * ODD + 18 * B>(row, A, n, B);
   else if constexpr (WT == RG_Q4_1) dec_q41_q5_block<WT, 20 * B>(row, A, n, B);
@@ -573,7 +641,7 @@ __device__ __forceinline__ void dec_item(const uint8_t* row, uint8_t* A, int n, 
 // eight independent blocks per lane, and the lanes of a load or store sit on
 // consecutive rows, i.e. in distinct bank groups.  ODD = the tile's k index is
 // odd (window offset 8 for Q8_0 / Q4_0, second half of a Q4_K super-block).
-// o: MXFP4's run-time window offset (0, 4, 8 or 12); O: the super-block
+// o: the MXFP4 and NVFP4 run-time window offset (0, 4, 8 or 12; 0 or 8); O: the super-block
 // offset of the row-half decoders.
 template <int WT, int ODD, int NPART, int O = 0>
 __device__ __forceinline__ void decode_stage_warp(const uint8_t* __restrict__ P,
@@ -602,6 +670,74 @@ __device__ __forceinline__ void decode_stage_warp(const uint8_t* __restrict__ P,
   }
 }
 
+// The forward's stage (FWD kernels): 128 rows of W by the 64 values HV of a
+// 128-value tile (HV = 0: values 0..63, 1: 64..127), decoded into a K-major
+// operand tile (row n: 128 bytes, chunk c at c ^ (n mod 8), rows 8 apart by
+// 1024 bytes): the OUT_PROD decoders' own layout once the half's column
+// block is taken as the tile (A - HV column blocks), with 128 rows instead
+// of 64.  Warp `part` of the slot's two takes rows lane + 32 (2 part + r),
+// r = 0, 1, and of each row the items (blocks, Q4_K parts) of half HV.
+template <int WT, int ODD, int HV, int O = 0>
+__device__ __forceinline__ void decode_stage_fwd(const uint8_t* __restrict__ P, uint8_t* __restrict__ A,
+                                                 int lane, int part, int o = 0) {
+  constexpr int PR = p_row_bytes<WT>();
+  uint8_t* Ah = A - HV * A_COLBLK;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int n = lane + 32 * (2 * part + r);
+    const uint8_t* row = P + n * PR;
+    if constexpr (WT == RG_Q6_K) {
+      dec_q6_k_row<O, ODD, HV>(row, Ah, n);
+    } else if constexpr (WT == RG_Q3_K) {
+      dec_q3_k_row<O, ODD, HV>(row, Ah, n);
+    } else if constexpr (WT == RG_Q2_K) {
+      dec_q2_k_row<O, ODD, HV>(row, Ah, n);
+    } else {
+      dec_item<WT, ODD, 2 * HV>(row, Ah, n, o);
+      dec_item<WT, ODD, 2 * HV + 1>(row, Ah, n, o);
+    }
+  }
+}
+
+// decode_stage_fwd for the run-time tile kw of the row (its parity, and the
+// block offset of the row-half and MXFP4 decoders) and half hv.
+template <int WT>
+__device__ __forceinline__ void decode_fwd_stage(const uint8_t* __restrict__ P, uint8_t* __restrict__ A,
+                                                 int lane, int part, int kw, int hv) {
+  if constexpr (WT == RG_Q6_K || WT == RG_Q3_K || WT == RG_Q2_K) {
+    const int o = ((kw >> 1) * block_bytes(WT)) & 15;
+#define RG_FWD_CASE(OO)                                                                        \
+  case OO / 2:                                                                                 \
+    if constexpr (WT != RG_Q2_K || OO % 4 == 0) {                                              \
+      if (kw & 1) {                                                                            \
+        if (hv) decode_stage_fwd<WT, 1, 1, OO>(P, A, lane, part);                              \
+        else decode_stage_fwd<WT, 1, 0, OO>(P, A, lane, part);                                 \
+      } else {                                                                                 \
+        if (hv) decode_stage_fwd<WT, 0, 1, OO>(P, A, lane, part);                              \
+        else decode_stage_fwd<WT, 0, 0, OO>(P, A, lane, part);                                 \
+      }                                                                                        \
+    }                                                                                          \
+    break;
+    switch (o >> 1) {
+      RG_FWD_CASE(0) RG_FWD_CASE(2) RG_FWD_CASE(4) RG_FWD_CASE(6)
+      RG_FWD_CASE(8) RG_FWD_CASE(10) RG_FWD_CASE(12) RG_FWD_CASE(14)
+      default: break;
+    }
+#undef RG_FWD_CASE
+  } else if constexpr (WT == RG_MXFP4 || WT == RG_NVFP4) {
+    // the tile's blocks start 0, 4, 8 or 12 (MXFP4) or 0 or 8 (NVFP4) bytes into the window
+    const int o = WT == RG_MXFP4 ? (kw * 68) & 12 : (kw & 1) * 8;
+    if (hv) decode_stage_fwd<WT, 0, 1>(P, A, lane, part, o);
+    else decode_stage_fwd<WT, 0, 0>(P, A, lane, part, o);
+  } else if (kw & 1) {
+    if (hv) decode_stage_fwd<WT, 1, 1>(P, A, lane, part);
+    else decode_stage_fwd<WT, 1, 0>(P, A, lane, part);
+  } else {
+    if (hv) decode_stage_fwd<WT, 0, 1>(P, A, lane, part);
+    else decode_stage_fwd<WT, 0, 0>(P, A, lane, part);
+  }
+}
+
 // Byte offset (16-byte multiple) of the window a 128-value tile kt loads from a packed row.
 template <int WT>
 __device__ __forceinline__ int p_window_start(int kt) {
@@ -615,6 +751,7 @@ __device__ __forceinline__ int p_window_start(int kt) {
   if constexpr (WT == RG_Q3_K) return ((kt >> 1) * 110) & ~15;
   if constexpr (WT == RG_Q2_K) return ((kt >> 1) * 84) & ~15;
   if constexpr (WT == RG_MXFP4) return (kt * 68) & ~15;
+  if constexpr (WT == RG_NVFP4) return (kt * 72) & ~15;
   return (kt >> 1) * 144;  // Q4_K: the whole super-block
 }
 
@@ -690,7 +827,7 @@ __device__ __forceinline__ int sk_unit_of(uint32_t g, uint32_t rn, int U) {
 //   acc_full[2], acc_empty[2]   the two tensor-memory accumulators
 //   drain        local: the MMAs issued so far completed (abort path)
 
-template <int WT, int CG, int BT, bool AD, bool SK>
+template <int WT, int CG, int BT, bool AD, bool SK, bool FWD = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     out_prod_tc_kernel(const __grid_constant__ CUtensorMap map_w,
                        const __grid_constant__ CUtensorMap map_y,
@@ -698,7 +835,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                        float* __restrict__ dX, int64_t ldx, float beta, int T, int K,
                        int n_kunits, int n_ttiles, int band, int n_chunks, int n_splits,
                        float* __restrict__ part, WaitCtl ctl) {
-  using C = Cfg<WT, CG, BT>;
+  using C = Cfg<WT, CG, BT, FWD>;
+  static_assert(!FWD || (!AD && !SK), "the forward runs without an adapter or stream-K");
   constexpr int S = C::S;
   extern __shared__ uint8_t smem_raw[];
   // align inside the shared window (pointer arithmetic keeps the shared space)
@@ -819,12 +957,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if constexpr (C::QUANT) {
               mbar_arrive_expect_tx(full_p(s), C::P_BYTES);
-              tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_p(s),
-                          p_window_start<WT>(kt) / 4, gc * BC);
+              if constexpr (FWD)  // the window of the 128-value tile holding chunk gc, 128 rows
+                tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_p(s),
+                            p_window_start<WT>(gc >> 1) / 4, kt * BM);
+              else
+                tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_p(s),
+                            p_window_start<WT>(kt) / 4, gc * BC);
               pend_p |= 1u << s;
             } else {
               const uint32_t a_dst = smem_addr(sA + s * A_STAGE);
-              if constexpr (CG == 2) {
+              if constexpr (FWD) {
+                // 64 values of 128 rows: the K-major, 128-byte swizzled operand itself
+                if constexpr (CG == 2)
+                  tma_load_2d_pair(a_dst, &map_w, abar, gc * BC, kt * BM);
+                else
+                  tma_load_2d(a_dst, &map_w, abar, gc * BC, kt * BM);
+              } else if constexpr (CG == 2) {
                 tma_load_2d_pair(a_dst, &map_w, abar, kt * BM, gc * BC);
                 tma_load_2d_pair(a_dst + A_COLBLK, &map_w, abar, kt * BM + 64, gc * BC);
               } else {
@@ -917,8 +1065,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t b_base = smem_addr(sB + s * B_STAGE);
 #pragma unroll
             for (int kk = 0; kk < BC / UMMA_K; ++kk) {
-              // A: MN-major, k-column blocks 8 KB apart (LBO), 8-row groups of n 1 KB apart (SBO)
-              const uint64_t ad = sdesc_sw128(a_base + kk * (UMMA_K * 128), A_COLBLK, 1024);
+              // A: MN-major, k-column blocks 8 KB apart (LBO), 8-row groups of n 1 KB apart
+              // (SBO); the forward's K-major A as B below (16 values = 32 bytes along a row)
+              const uint64_t ad = FWD ? sdesc_sw128(a_base + kk * (UMMA_K * 2), 16, 1024)
+                                      : sdesc_sw128(a_base + kk * (UMMA_K * 128), A_COLBLK, 1024);
               // B: K-major, 16 values of n = 32 bytes along the swizzled row; 8-row groups 1 KB apart
               const uint64_t bd = sdesc_sw128(b_base + kk * (UMMA_K * 2), 16, 1024);
               const uint32_t acc = ((c - c0) | kk) != 0 ? 1u : 0u;
@@ -991,7 +1141,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               run = false;
               break;
             }
-            if (AD && cc >= c_ad) {
+            if constexpr (FWD) {
+              // chunk gf: values 64 gf .. 64 gf + 63 of this CTA's 128 rows of W
+              const int gf = (tile / n_tiles1) * n_chunks + cc;
+              decode_fwd_stage<WT>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part, gf >> 1, gf & 1);
+            } else if (AD && cc >= c_ad) {
               // nothing to decode
             } else if constexpr (WT == RG_Q6_K || WT == RG_Q3_K || WT == RG_Q2_K) {
               // the super-block starts o bytes into its window: one decoder per
@@ -1012,11 +1166,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 default: break;
               }
 #undef RG_WIN_CASE
-            } else if constexpr (WT == RG_MXFP4) {
-              // the tile's four blocks start (kt * 68) mod 16 = 0, 4, 8 or 12
-              // bytes into the window
+            } else if constexpr (WT == RG_MXFP4 || WT == RG_NVFP4) {
+              // the tile's blocks start (kt * 68) mod 16 = 0, 4, 8 or 12 (MXFP4)
+              // or (kt * 72) mod 16 = 0 or 8 (NVFP4) bytes into the window
               decode_stage_warp<WT, 0, WPS>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part,
-                                            (kt * 68) & 12);
+                                            WT == RG_MXFP4 ? (kt * 68) & 12 : (kt & 1) * 8);
           } else if (kt & 1) {
               decode_stage_warp<WT, 1, WPS>(sP + s * C::P_STAGE, sA + s * A_STAGE, lane, part);
             } else {
@@ -1141,13 +1295,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // --- launch templates ---------------------------------------------------------
 
-template <int WT, int CG, int BT, bool AD, bool SK>
+template <int WT, int CG, int BT, bool AD, bool SK, bool FWD>
 static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
                                const CUtensorMap& ml, int n_main, float* dX, int64_t ldx,
                                float beta, int T, int K, const TcPlan& p, float* part,
                                const DevInfo& dev, cudaStream_t stream) {
-  using C = tc::Cfg<WT, CG, BT>;
-  auto kern = tc::out_prod_tc_kernel<WT, CG, BT, AD, SK>;
+  using C = tc::Cfg<WT, CG, BT, FWD>;
+  auto kern = tc::out_prod_tc_kernel<WT, CG, BT, AD, SK, FWD>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   WaitCtl ctl{dev.status, dev.wait_limit_ns};
@@ -1188,20 +1342,24 @@ static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
   return launch_sk_fixup(part, units, CG, BT, p, T, K, dX, ldx, dev, stream);
 }
 
-template <int WT, bool AD, bool SK>
+template <int WT, bool AD, bool SK, bool FWD>
 static cudaError_t launch_tc_w(const CUtensorMap& mw, const CUtensorMap& my,
                                const CUtensorMap& ml, int n_main, float* dX, int64_t ldx,
                                float beta, int T, int K, const TcPlan& p, float* part,
                                const DevInfo& dev, cudaStream_t stream) {
   if (p.cg == 2)
-    return launch_tc_t<WT, 2, 256, AD, SK>(mw, my, ml, n_main, dX, ldx, beta, T, K, p, part, dev,
-                                           stream);
-  return launch_tc_t<WT, 1, 128, AD, SK>(mw, my, ml, n_main, dX, ldx, beta, T, K, p, part, dev,
-                                         stream);
+    return launch_tc_t<WT, 2, 256, AD, SK, FWD>(mw, my, ml, n_main, dX, ldx, beta, T, K, p, part,
+                                                dev, stream);
+  return launch_tc_t<WT, 1, 128, AD, SK, FWD>(mw, my, ml, n_main, dX, ldx, beta, T, K, p, part, dev,
+                                              stream);
 }
 
-// The body of launch_tc: AD = an adapter rides along (rank > 0).
-template <bool AD, bool SK>
+// The body of launch_tc: AD = an adapter rides along (rank > 0).  W is N
+// rows of K values either way; FWD (the forward mul_mat) contracts over the
+// K values of each row into an output N wide, the OUT_PROD over the N rows
+// into an output K wide.  dy16 (dY's or X's 16-bit copy) has one row of the
+// contraction's length per row of the output's T.
+template <bool AD, bool SK, bool FWD = false>
 static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K,
                                   const uint16_t* dy16, int64_t ld_dy16, int64_t T, float* dX,
                                   int64_t dx_t, float beta, float* part, const DevInfo& dev,
@@ -1209,16 +1367,14 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
                                   int64_t rank) {
   // with an adapter the contraction runs over tc_adapter_cols(N, r) columns
   // of dy16: dY's N, zeros to the chunk boundary, then the adapter's rank
-  const int64_t n_ext = rank > 0 ? tc_adapter_cols(N, rank) : N;
+  const int64_t n_ext = FWD ? K : rank > 0 ? tc_adapter_cols(N, rank) : N;
+  const int64_t k_out = FWD ? N : K;  // the output's width
   const int n_main = rank > 0 ? static_cast<int>((N + tc::BC - 1) / tc::BC) : (1 << 30);
-  TcPlan p = plan_tc(n_ext, K, T, dev, cg_force);
+  TcPlan p = plan_tc(n_ext, k_out, T, dev, cg_force);
   if (p.sk != SK) return cudaErrorInvalidValue;  // the dispatcher chose the other build
   if ((p.n_splits > 1 || p.sk) && part == nullptr) return cudaErrorInvalidValue;
   float* partial = p.n_splits > 1 || p.sk ? part : nullptr;
-  // band of k units whose slice of W fits comfortably in L2 (48 MB)
-  const double w_per_value = is_quant(wtype) ? static_cast<double>(block_bytes(wtype)) / block_values(wtype) : 2.0;
-  const double slice = static_cast<double>(N) * (tc::BM * p.cg) * w_per_value;
-  p.band = static_cast<int>(std::max(1.0, std::min<double>(p.n_kunits, 48.0 * 1024 * 1024 / slice)));
+  p.band = tc_band(wtype, n_ext, p);
   CUtensorMap mw, my;
   CUresult r;
   if (is_quant(wtype)) {
@@ -1226,12 +1382,13 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
     const uint32_t box_bytes = static_cast<uint32_t>(with_wtype(wtype, 0, [](auto wt) {
       return tc::p_row_bytes<decltype(wt)::value>();
     }));
+    // a stage's packed windows: 64 contraction rows, or the forward's 128 output rows
     r = encode_tiled(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rb / 4, static_cast<uint64_t>(N), rb,
-                     box_bytes / 4, tc::BC, CU_TENSOR_MAP_SWIZZLE_NONE);
+                     box_bytes / 4, FWD ? 2 * tc::BC : tc::BC, CU_TENSOR_MAP_SWIZZLE_NONE);
   } else {
     r = encode_tiled(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, W, static_cast<uint64_t>(K),
-                     static_cast<uint64_t>(N), static_cast<uint64_t>(K) * 2, 64, tc::BC,
-                     CU_TENSOR_MAP_SWIZZLE_128B);
+                     static_cast<uint64_t>(N), static_cast<uint64_t>(K) * 2, 64,
+                     FWD ? 2 * tc::BC : tc::BC, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   r = encode_tiled(&my, CU_TENSOR_MAP_DATA_TYPE_UINT16, dy16, static_cast<uint64_t>(n_ext),
@@ -1247,13 +1404,13 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
                      CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  const int t = static_cast<int>(T), k = static_cast<int>(K);
+  const int t = static_cast<int>(T), k = static_cast<int>(k_out);
   const cudaError_t e = with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
-    return launch_tc_w<decltype(wt)::value, AD, SK>(mw, my, ml, n_main, dX, dx_t, beta, t, k, p,
-                                                partial, dev, stream);
+    return launch_tc_w<decltype(wt)::value, AD, SK, FWD>(mw, my, ml, n_main, dX, dx_t, beta, t, k,
+                                                        p, partial, dev, stream);
   });
   if (e != cudaSuccess || p.n_splits == 1) return e;
-  return launch_reduce_partials(partial, p.n_splits, T, K, dX, dx_t, beta, dev, stream);
+  return launch_reduce_partials(partial, p.n_splits, T, k_out, dX, dx_t, beta, dev, stream);
 }
 
 // launch_tc with an adapter (rg_tc_ad.cu; its plans never take stream-K) and

@@ -65,7 +65,8 @@ TYPE_NAMES = {F16: "f16", BF16: "bf16", Q8_0: "q8_0", Q4_0: "q4_0", Q4_K: "q4_k"
               Q4_1: "q4_1", Q5_0: "q5_0", Q5_1: "q5_1", Q5_K: "q5_k", Q6_K: "q6_k", F32: "f32",
               Q2_K: "q2_k", Q3_K: "q3_k", MXFP4: "mxfp4", NVFP4: "nvfp4"}
 NAME_TO_TYPE = {v: k for k, v in TYPE_NAMES.items()}
-ALL_TYPES = [Q8_0, Q4_0, Q4_K, F16, BF16, Q4_1, Q5_0, Q5_1, Q5_K, Q6_K, F32, Q2_K, Q3_K, MXFP4]
+ALL_TYPES = [Q8_0, Q4_0, Q4_K, F16, BF16, Q4_1, Q5_0, Q5_1, Q5_K, Q6_K, F32, Q2_K, Q3_K, MXFP4,
+             NVFP4]
 
 # (values per block, bytes per block)
 BLOCK = {F16: (1, 2), BF16: (1, 2), Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144),
@@ -577,5 +578,5 @@ WORKLOADS = {
     "types_4096x4096_t8192": [Problem(f"{TYPE_NAMES[wt]}_4096x4096_t8192", wt, 4096, 4096, 8192,
                                       1e-3, 0.0, 16 * i)
                               for i, wt in enumerate([Q4_1, Q5_0, Q5_1, Q5_K, Q6_K, F32, Q2_K, Q3_K,
-                                                      MXFP4])],
+                                                      MXFP4, NVFP4])],
 }

@@ -46,7 +46,7 @@ def test_row_bytes_matches_block_sizes(lib):
     for wt in inputs.ALL_TYPES:
         for K in (0, 8, 32, 256, 4096, 14336, 17408, 300):
             assert rg.rg_row_bytes(wt, K) == inputs.row_bytes(wt, K), (wt, K)
-    assert rg.rg_row_bytes(15, 256) == 0 and rg.rg_row_bytes(inputs.Q8_0, -32) == 0
+    assert rg.rg_row_bytes(16, 256) == 0 and rg.rg_row_bytes(inputs.Q8_0, -32) == 0
     assert rg.rg_row_bytes(0, 256) == 0
 
 
@@ -76,14 +76,15 @@ def test_dispatch(lib):
     # MXFP4 rows (136 B per 256 values) need K % 512 == 0
     assert rg.rg_select_variant(inputs.MXFP4, 4096, 4608, 2048) == rg.RG_VARIANT_TC
     assert rg.rg_select_variant(inputs.MXFP4, 4096, 4352, 2048) == rg.RG_VARIANT_SIMT32
-    assert rg.rg_workspace_bytes(rg.RG_VARIANT_TC, inputs.Q4_K, 14336, 4096, 2048) == 2048 * 14336 * 2
+    # (with a device the plan may add partial-sum slabs after the 16-bit copy of dY)
+    assert rg.rg_workspace_bytes(rg.RG_VARIANT_TC, inputs.Q4_K, 14336, 4096, 2048) >= 2048 * 14336 * 2
     assert rg.rg_workspace_bytes(rg.RG_VARIANT_TC, inputs.Q4_K, 13, 4096, 3) == 3 * 16 * 2 + 160
     assert rg.rg_workspace_bytes(rg.RG_VARIANT_SIMT32, inputs.Q4_K, 14336, 4096, 8) == 0
 
 
 def test_plan_validates_before_needing_a_device(lib):
     info = rg.rg_plan_info()
-    assert rg.rg_plan(0, 15, 64, 256, 8, info) == rg.RG_ERR_TYPE
+    assert rg.rg_plan(0, 16, 64, 256, 8, info) == rg.RG_ERR_TYPE
     assert rg.rg_plan(6, inputs.Q8_0, 64, 256, 8, info) == rg.RG_ERR_TYPE
     assert rg.rg_plan(0, inputs.Q8_0, 64, 200, 8, info) == rg.RG_ERR_SHAPE
     assert rg.rg_plan(0, inputs.F16, 64, 12, 8, info) == rg.RG_ERR_SHAPE
@@ -98,7 +99,7 @@ BAD = 0x1000  # never dereferenced: every case below fails validation first
 
 
 @pytest.mark.parametrize("args,status", [
-    ((15, BAD, 64, 256, BAD, 8, BAD, 0.0), rg.RG_ERR_TYPE),
+    ((16, BAD, 64, 256, BAD, 8, BAD, 0.0), rg.RG_ERR_TYPE),
     ((0, BAD, 64, 256, BAD, 8, BAD, 0.0), rg.RG_ERR_TYPE),
     ((inputs.Q5_K, BAD, 64, 128, BAD, 8, BAD, 0.0), rg.RG_ERR_SHAPE),
     ((inputs.Q5_0, BAD, 64, 32, BAD, 8, BAD, 0.0), rg.RG_ERR_SHAPE),
@@ -124,11 +125,11 @@ def test_validation_before_any_launch(lib, args, status):
 def test_bad_variant_and_workspace(lib):
     # valid shapes but a bad variant id: rejected (the variant check follows
     # argument validation, and the empty case returns before it)
-    assert rg.rg_out_prod_variant(7, 15, BAD, 64, 256, BAD, 8, BAD, 0.0) == rg.RG_ERR_TYPE
+    assert rg.rg_out_prod_variant(7, 16, BAD, 64, 256, BAD, 8, BAD, 0.0) == rg.RG_ERR_TYPE
 
 
 def test_dequant_validation(lib):
-    assert rg.rg_dequant(15, BAD, 4, 256, BAD) == rg.RG_ERR_TYPE
+    assert rg.rg_dequant(16, BAD, 4, 256, BAD) == rg.RG_ERR_TYPE
     assert rg.rg_dequant(inputs.Q4_K, BAD, 4, 128, BAD) == rg.RG_ERR_SHAPE
     assert rg.rg_dequant(inputs.Q8_0, None, 4, 256, BAD) == rg.RG_ERR_ARG
     assert rg.rg_dequant(inputs.Q8_0, BAD + 1, 4, 256, BAD) == rg.RG_ERR_ALIGN
@@ -169,12 +170,38 @@ def test_out_prod_ex_validation_before_any_launch(lib):
     assert call(dx_batch=6) == rg.RG_ERR_ALIGN
     assert call(dY=A + 2, dy_t=1, dy_n=8) == rg.RG_ERR_ALIGN
     assert call(dY=A + 4) == rg.RG_ERR_ALIGN            # contiguous rows need 16-byte alignment
-    assert call(wtype=15) == rg.RG_ERR_TYPE
+    assert call(wtype=16) == rg.RG_ERR_TYPE
+
+
+def test_out_prod_batched_validation_before_any_launch(lib):
+    """The two-dimension batched entry: weight counts must divide the
+    gradient's batch counts, strides be non-negative and aligned, and every
+    batch pass the row rules, all before any launch."""
+    A = 0x1000
+    base = dict(variant=0, wtype=inputs.Q8_0, W=A, N=64, K=256, w_n2=2, w_n3=1, w_s2=64 * 272,
+                w_s3=0, dY=A, T=8, dy_t=64, dy_n=1, dy_s2=8 * 64, dy_s3=0, dX=A, dx_t=256,
+                dx_s2=8 * 256, dx_s3=0, n2=4, n3=1, beta=0.0)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return rg.rg_out_prod_batched(*[a[k] for k in base])
+    assert call(n2=0) == rg.RG_OK and call(n3=0) == rg.RG_OK
+    assert call(n2=-1) == rg.RG_ERR_ARG
+    assert call(w_n2=0) == rg.RG_ERR_ARG
+    assert call(w_n2=3) == rg.RG_ERR_SHAPE              # 3 weights for 4 batches
+    assert call(n3=3, w_n3=2) == rg.RG_ERR_SHAPE
+    assert call(w_s2=-16) == rg.RG_ERR_ARG
+    assert call(w_s2=8) == rg.RG_ERR_ALIGN
+    assert call(dx_s3=2, n3=2) == rg.RG_ERR_ALIGN
+    assert call(dx_t=255) == rg.RG_ERR_ARG
+    assert call(dY=A + 4) == rg.RG_ERR_ALIGN
+    assert call(W=A + 8, w_n2=1) == rg.RG_ERR_ALIGN
+    assert call(wtype=16) == rg.RG_ERR_TYPE
 
 
 def test_mul_mat_validation(lib):
     A = 0x1000
-    assert rg.rg_mul_mat(15, A, 64, 256, A, 4, A, 0.0) == rg.RG_ERR_TYPE
+    assert rg.rg_mul_mat(16, A, 64, 256, A, 4, A, 0.0) == rg.RG_ERR_TYPE
     assert rg.rg_mul_mat(inputs.Q8_0, A, 60, 256, A, 4, A, 0.0) == rg.RG_ERR_SHAPE
     assert rg.rg_mul_mat(inputs.Q8_0, A, 64, 255, A, 4, A, 0.0) == rg.RG_ERR_SHAPE
     assert rg.rg_mul_mat(inputs.Q8_0, A, 64, 256, A, 0, A, 0.0) == rg.RG_OK
@@ -196,7 +223,7 @@ def test_out_prod_lora_validation(lib):
     assert call(a=A + 4) == rg.RG_ERR_ALIGN
     assert call(b=A + 8) == rg.RG_ERR_ALIGN
     assert call(prefix=(9, inputs.Q8_0, A, 64, 256, A, 8, A, 0.0)) == rg.RG_ERR_TYPE
-    assert call(prefix=(0, 15, A, 64, 256, A, 8, A, 0.0)) == rg.RG_ERR_TYPE
+    assert call(prefix=(0, 16, A, 64, 256, A, 8, A, 0.0)) == rg.RG_ERR_TYPE
     assert call(prefix=(0, inputs.Q8_0, A, 64, 200, A, 8, A, 0.0)) == rg.RG_ERR_SHAPE
     # nothing to compute: T == 0 or K == 0, whatever the adapter pointers
     assert call(a=None, b=None, prefix=(0, inputs.Q8_0, None, 64, 256, None, 0, None, 0.0)) == rg.RG_OK

@@ -28,8 +28,13 @@ def _run(rg, wtype, W, N, K, X, T, Y0=None, beta=0.0):
 
 
 @pytest.mark.parametrize("wtype", inputs.ALL_TYPES)
-@pytest.mark.parametrize("shape", [(208, 512, 300), (64, 256, 1), (1000, 768, 130), (72, 1024, 33)])
+@pytest.mark.parametrize("shape", [(208, 512, 300), (64, 256, 1), (1000, 768, 130), (72, 1024, 33),
+                                   (136, 2048, 290)])
 def test_mul_mat_parity(rg, wtype, shape):
+    """Every weight type on ragged shapes (rows against the 128-row units,
+    T against the 256-row tiles, K from one 256-value tile up); K that the
+    type's rows do not align to runs the transient-copy route, the rest the
+    fused decoder."""
     N, K, T = shape
     W = inputs.gen_weight(wtype, N, K, seed=91, stream=1)
     X = inputs.normal_f32(91, 2, T * K, 1e-2).reshape(T, K)
@@ -42,17 +47,21 @@ def test_mul_mat_parity(rg, wtype, shape):
 
 
 def test_mul_mat_beta_and_one_hot(rg):
-    N, K, T, wtype = 256, 512, 40, inputs.Q4_K
+    # one-hot X selects columns of deq(W): Q8_0's decoded operand is the exact
+    # product d * q rounded once to fp16, i.e. fp16(deq W)
+    N, K, T, wtype = 256, 512, 40, inputs.Q8_0
     W = inputs.gen_weight(wtype, N, K, seed=92, stream=1)
     Wd = oracle.dequant(wtype, W, N, K)
-    # one-hot X selects columns of deq(W), rounded once to fp16 on the way in
     k0 = (41 * np.arange(T) + 5) % K
     X = np.zeros((T, K), np.float32)
     X[np.arange(T), k0] = 1.0
     got = _run(rg, wtype, W, N, K, X, T)
     want = Wd[:, k0].T.astype(np.float16).astype(np.float32)
     assert np.array_equal(got, want)
-    # beta accumulates
+    # beta accumulates (Q4_K)
+    wtype = inputs.Q4_K
+    W = inputs.gen_weight(wtype, N, K, seed=92, stream=1)
+    Wd = oracle.dequant(wtype, W, N, K)
     X = inputs.normal_f32(92, 2, T * K, 1e-2).reshape(T, K)
     Y0 = inputs.normal_f32(92, 3, T * N, 1e-3).reshape(T, N)
     got = _run(rg, wtype, W, N, K, X, T, Y0, 1.0)
@@ -72,6 +81,20 @@ def test_mul_mat_large_splits_and_waves(rg):
         got = _run(rg, wtype, W, N, K, X, T)
         ref = oracle.mul_mat(wtype, W, N, K, X, T, Wd=Wd)
         assert np.all(np.abs(got - ref) <= 5e-3 * oracle.mul_mat_bound(X, Wd) + 1e-7)
+
+
+@pytest.mark.parametrize("wtype", [inputs.Q4_K, inputs.Q8_0, inputs.F16, inputs.Q6_K, inputs.NVFP4])
+def test_mul_mat_holds_no_copy_of_the_weight(rg, wtype):
+    """The fused forward's workspace is X's 16-bit copy (and a split's partial
+    sums): far below the 2 N K bytes a dense 16-bit deq(W) would take, on the
+    layer-sized shape it is timed on."""
+    N, K, T = 14336, 4096, 8192
+    ws = rg.rg_mul_mat_workspace_bytes(wtype, N, K, T)
+    x16 = T * K * 2
+    assert x16 <= ws < x16 + 2 * N * K // 4, (ws, x16)
+    # rows TMA cannot address (Q6_K at K % 2048 != 0) take the transient copy
+    if wtype == inputs.Q6_K:
+        assert rg.rg_mul_mat_workspace_bytes(wtype, 4096, 2304, 512) >= 2 * 4096 * 2304
 
 
 def test_mul_mat_shape_rules(rg):

@@ -139,3 +139,98 @@ def test_strided_batches_run_in_turn(rg):
     for b in range(B):
         _check(got[:, b * K:(b + 1) * K], oracle.out_prod(wtype, W, N, K, dYs[b], T, Wd=Wd),
                oracle.abs_bound(dYs[b], Wd), 5e-3, f"batch {b}")
+
+
+def _batched_case(wtype, N, K, T, n2, n3, w_n2, w_n3, seed):
+    Ws = [[inputs.gen_weight(wtype, N, K, seed=seed + 10 * j3 + j2, stream=1) for j2 in range(w_n2)]
+          for j3 in range(w_n3)]
+    dYs = [[inputs.normal_f32(seed + 100 + 10 * i3 + i2, 2, T * N, 1e-3).reshape(T, N)
+            for i2 in range(n2)] for i3 in range(n3)]
+    return Ws, dYs
+
+
+@pytest.mark.parametrize("n2,w_n2,n3,w_n3", [(8, 4, 1, 1), (8, 2, 1, 1), (4, 2, 3, 1), (2, 1, 4, 2)])
+def test_batched_broadcast_stacks_each_weights_run(rg, n2, w_n2, n3, w_n3):
+    """Fewer weights than gradient batches (ratio 2 and 4 along dim 2, and two
+    batch dims): batch (i2, i3) reads weight (i2 / (n2 / w_n2), i3 / (n3 /
+    w_n3)).  dY and dX batches are stacked in memory, so the batches one weight
+    serves run as one call (counted by the library's launches), and every
+    batch matches the oracle's batched product."""
+    wtype, N, K, T = inputs.Q4_K, 320, 512, 48
+    rb = inputs.row_bytes(wtype, K)
+    Ws, dYs = _batched_case(wtype, N, K, T, n2, n3, w_n2, w_n3, 80)
+    dev, s = torch.device("cuda:0"), torch.cuda.current_stream()
+    Wall = torch.from_numpy(np.concatenate([w for row in Ws for w in row])).to(dev)   # [j3][j2]
+    dYall = torch.from_numpy(np.concatenate([d for row in dYs for d in row])).to(dev)  # [i3][i2][T, N]
+    dX = torch.full((n3 * n2 * T, K), float("nan"), device=dev)
+    r2, r3 = n2 // w_n2, n3 // w_n3
+    # calls: runs of consecutive batches (i2 fastest) reading one weight
+    runs = 0
+    prev = None
+    for i3 in range(n3):
+        for i2 in range(n2):
+            w = oracle.batch_weight(i2, i3, n2, n3, w_n2, w_n3)
+            runs += w != prev
+            prev = w
+    info = rg.rg_plan_info()
+    torch.cuda.synchronize()
+    before = rg.rg_launch_count()
+    rg.check(rg.rg_out_prod_batched(0, wtype, Wall, N, K, w_n2, w_n3, N * rb, w_n2 * N * rb,
+                                    dYall, T, N, 1, T * N, n2 * T * N, dX, K, T * K, n2 * T * K,
+                                    n2, n3, 0.0, s), "rg_out_prod_batched")
+    rg.check(rg.rg_check(s))
+    launches = rg.rg_launch_count() - before
+    expect = 0
+    # each run is one call over T * (its batches) rows
+    lens, prev, cur = [], None, 0
+    for i3 in range(n3):
+        for i2 in range(n2):
+            w = oracle.batch_weight(i2, i3, n2, n3, w_n2, w_n3)
+            if w != prev and cur:
+                lens.append(cur)
+                cur = 0
+            prev = w
+            cur += 1
+    lens.append(cur)
+    assert len(lens) == runs
+    for c in lens:
+        rg.check(rg.rg_plan(0, wtype, N, K, T * c, info))
+        expect += info.launches
+    assert launches == expect
+    got = dX.cpu().numpy().reshape(n3, n2, T, K)
+    ref = oracle.out_prod_batched(wtype, Ws, N, K, dYs, T)
+    for i3 in range(n3):
+        for i2 in range(n2):
+            j2, j3 = oracle.batch_weight(i2, i3, n2, n3, w_n2, w_n3)
+            Wd = oracle.dequant(wtype, Ws[j3][j2], N, K)
+            _check(got[i3, i2], ref[i3][i2], oracle.abs_bound(dYs[i3][i2], Wd), 5e-3, f"({i2}, {i3})")
+
+
+def test_batched_transposed_gradients_run_in_turn(rg):
+    """Two batch dims with dY given transposed per batch (not stackable) and
+    beta = 1 on an interleaved dX: each batch is its own call, and each
+    matches the oracle."""
+    wtype, N, K, T = inputs.Q8_0, 128, 256, 40
+    n2, n3, w_n2, w_n3 = 4, 2, 2, 2
+    rb = inputs.row_bytes(wtype, K)
+    Ws, dYs = _batched_case(wtype, N, K, T, n2, n3, w_n2, w_n3, 90)
+    dX0s = [[inputs.normal_f32(95 + 10 * i3 + i2, 3, T * K, 1e-3).reshape(T, K) for i2 in range(n2)]
+            for i3 in range(n3)]
+    dev, s = torch.device("cuda:0"), torch.cuda.current_stream()
+    Wall = torch.from_numpy(np.concatenate([w for row in Ws for w in row])).to(dev)
+    dYT = torch.from_numpy(np.concatenate([np.ascontiguousarray(d.T) for row in dYs for d in row])).to(dev)
+    # dX: [T, n3, n2, K] (batches interleaved inside each row)
+    out = np.stack([np.stack(row, axis=1) for row in dX0s], axis=1)    # [T, n3, n2, K]
+    dX = torch.from_numpy(np.ascontiguousarray(out)).to(dev)
+    rg.check(rg.rg_out_prod_batched(0, wtype, Wall, N, K, w_n2, w_n3, N * rb, w_n2 * N * rb,
+                                    dYT, T, 1, T, N * T, n2 * N * T, dX, n3 * n2 * K, K, n2 * K,
+                                    n2, n3, 1.0, s), "rg_out_prod_batched")
+    rg.check(rg.rg_check(s))
+    got = dX.cpu().numpy()
+    ref = oracle.out_prod_batched(wtype, Ws, N, K, dYs, T, dX0s, 1.0)
+    for i3 in range(n3):
+        for i2 in range(n2):
+            j2, j3 = oracle.batch_weight(i2, i3, n2, n3, w_n2, w_n3)
+            Wd = oracle.dequant(wtype, Ws[j3][j2], N, K)
+            bnd = oracle.abs_bound(dYs[i3][i2], Wd) + np.abs(dX0s[i3][i2]) * 2.0 ** -24 / 5e-3
+            _check(got[:, i3, i2, :], ref[i3][i2], bnd, 5e-3, f"({i2}, {i3})")
