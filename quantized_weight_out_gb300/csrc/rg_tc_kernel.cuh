@@ -85,6 +85,16 @@ __host__ __device__ constexpr int p_row_bytes() {
                          : 0;
 }
 
+// Bytes of one packed W row that the forward's 64-value stage copies: Q4_K
+// the 16-byte header and the chunk's 32 nibble bytes (two copies into two
+// regions of the stage); Q8_0 its two 34-byte blocks inside an 80-byte
+// window (0, 4, 8 or 12 bytes in); the other types their whole 128-value
+// window.
+template <int WT>
+__host__ __device__ constexpr int p_fwd_row_bytes() {
+  return WT == RG_Q4_K ? 48 : WT == RG_Q8_0 ? 80 : p_row_bytes<WT>();
+}
+
 template <int WT, int CG, int BT, bool FWD = false>
 struct Cfg {
   static constexpr bool QUANT = is_quant(WT);
@@ -92,7 +102,8 @@ struct Cfg {
   // rows of W in a packed-window stage: the OUT_PROD's 64 contraction rows,
   // or the forward's 128 output rows (FWD: the contraction runs along the rows)
   static constexpr int P_ROWS = FWD ? 2 * BC : BC;
-  static constexpr int P_STAGE = QUANT ? ((P_ROWS * p_row_bytes<WT>() + 1023) / 1024) * 1024 : 0;
+  static constexpr int P_ROW = FWD ? p_fwd_row_bytes<WT>() : p_row_bytes<WT>();
+  static constexpr int P_STAGE = QUANT ? ((P_ROWS * P_ROW + 1023) / 1024) * 1024 : 0;
   static constexpr int STAGE = A_STAGE + B_STAGE + P_STAGE;
   // quantized: five slots (the forward: as many as fit, at most five), each
   // decoded by two warps; F16/BF16: as deep as fits
@@ -108,7 +119,7 @@ struct Cfg {
   static constexpr int NUM_BARS = 4 * S + 5;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024 B alignment
-  static constexpr uint32_t P_BYTES = QUANT ? P_ROWS * p_row_bytes<WT>() : 0;
+  static constexpr uint32_t P_BYTES = QUANT ? P_ROWS * P_ROW : 0;
   // operand bytes of one stage over the whole pair (B halves, and A for F16/BF16)
   static constexpr uint32_t AB_BYTES_PAIR = CG * (B_STAGE + (QUANT ? 0 : A_STAGE));
   static constexpr uint32_t TMEM_COLS = 2 * BT;
@@ -351,11 +362,14 @@ __device__ __forceinline__ uint32_t byte_of(uint32_t h1, uint32_t h2, uint32_t h
 // Q4_K: 16 bytes of nibbles of chunk c (values 64c + 16hh .. +15 from the low
 // nibbles, sub-block 2c; 64c + 32 + 16hh .. +15 from the high nibbles,
 // sub-block 2c+1) of the super-block at `row`; chunk cl of this CTA's half.
+// `q32`: the chunk's 32 nibble bytes (row + 16 + 32c in a whole super-block;
+// the forward copies them apart from the 16-byte header `row`).
 template <int H2, int CL, int HH>
-__device__ __forceinline__ void dec_q4_k_part(const uint8_t* row, uint8_t* A, int n) {
+__device__ __forceinline__ void dec_q4_k_part(const uint8_t* row, const uint8_t* q32, uint8_t* A,
+                                              int n) {
   constexpr int c = 2 * H2 + CL;
   const uint4 hdr = *reinterpret_cast<const uint4*>(row);
-  const uint4 qv = *reinterpret_cast<const uint4*>(row + 16 + 32 * c + 16 * HH);
+  const uint4 qv = *reinterpret_cast<const uint4*>(q32 + 16 * HH);
   const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x & 0xFFFFu)));
   const float dmin = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x >> 16)));
   int sc[2], m[2];
@@ -631,7 +645,7 @@ __device__ __forceinline__ void dec_item(const uint8_t* row, uint8_t* A, int n, 
   else if constexpr (WT == RG_Q4_1) dec_q41_q5_block<WT, 20 * B>(row, A, n, B);
   else if constexpr (WT == RG_Q5_0) dec_q41_q5_block<WT, 8 * ODD + 22 * B>(row, A, n, B);
   else if constexpr (WT == RG_Q5_1) dec_q41_q5_block<WT, 24 * B>(row, A, n, B);
-  else if constexpr (WT == RG_Q4_K) dec_q4_k_part<ODD, B / 2, B % 2>(row, A, n);
+  else if constexpr (WT == RG_Q4_K) dec_q4_k_part<ODD, B / 2, B % 2>(row, row + 16 + 32 * (2 * ODD + B / 2), A, n);
   else dec_q5_k_part<ODD, B / 2, B % 2>(row, A, n);
 }
 
@@ -686,7 +700,13 @@ __device__ __forceinline__ void decode_stage_fwd(const uint8_t* __restrict__ P, 
   for (int r = 0; r < 2; ++r) {
     const int n = lane + 32 * (2 * part + r);
     const uint8_t* row = P + n * PR;
-    if constexpr (WT == RG_Q6_K) {
+    if constexpr (WT == RG_Q4_K) {
+      // the 16-byte headers of the stage's 128 rows, then their 32 nibble bytes
+      const uint8_t* hdr = P + n * 16;
+      const uint8_t* q32 = P + 128 * 16 + n * 32;
+      dec_q4_k_part<ODD, HV, 0>(hdr, q32, Ah, n);
+      dec_q4_k_part<ODD, HV, 1>(hdr, q32, Ah, n);
+    } else if constexpr (WT == RG_Q6_K) {
       dec_q6_k_row<O, ODD, HV>(row, Ah, n);
     } else if constexpr (WT == RG_Q3_K) {
       dec_q3_k_row<O, ODD, HV>(row, Ah, n);
@@ -696,6 +716,20 @@ __device__ __forceinline__ void decode_stage_fwd(const uint8_t* __restrict__ P, 
       dec_item<WT, ODD, 2 * HV>(row, Ah, n, o);
       dec_item<WT, ODD, 2 * HV + 1>(row, Ah, n, o);
     }
+  }
+}
+
+// The forward's Q8_0 stage: 128 rows' two blocks of the 64-value chunk,
+// starting O bytes into each row's 80-byte window, as chunks 0..7.
+template <int O>
+__device__ __forceinline__ void decode_stage_fwd_q8(const uint8_t* __restrict__ P, uint8_t* __restrict__ A,
+                                                    int lane, int part) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int n = lane + 32 * (2 * part + r);
+    const uint8_t* row = P + n * p_fwd_row_bytes<RG_Q8_0>();
+    dec_q8_block<O>(row, A, n, 0);
+    dec_q8_block<O + 34>(row, A, n, 1);
   }
 }
 
@@ -724,6 +758,14 @@ __device__ __forceinline__ void decode_fwd_stage(const uint8_t* __restrict__ P, 
       default: break;
     }
 #undef RG_FWD_CASE
+  } else if constexpr (WT == RG_Q8_0) {
+    // the 64-value chunk's two blocks start (68 gf) mod 16 bytes into its window
+    switch ((((2 * kw + hv) * 68) & 15) >> 2) {
+      case 0: decode_stage_fwd_q8<0>(P, A, lane, part); break;
+      case 1: decode_stage_fwd_q8<4>(P, A, lane, part); break;
+      case 2: decode_stage_fwd_q8<8>(P, A, lane, part); break;
+      default: decode_stage_fwd_q8<12>(P, A, lane, part); break;
+    }
   } else if constexpr (WT == RG_MXFP4 || WT == RG_NVFP4) {
     // the tile's blocks start 0, 4, 8 or 12 (MXFP4) or 0 or 8 (NVFP4) bytes into the window
     const int o = WT == RG_MXFP4 ? (kw * 68) & 12 : (kw & 1) * 8;
@@ -894,6 +936,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fence_mbar_init();
     tma_prefetch_map(&map_w);
     tma_prefetch_map(&map_y);
+    if constexpr (AD || (FWD && WT == RG_Q4_K)) tma_prefetch_map(&map_l);
   }
   if (warp == 1) {
     if constexpr (CG == 2) {
@@ -957,10 +1000,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if constexpr (C::QUANT) {
               mbar_arrive_expect_tx(full_p(s), C::P_BYTES);
-              if constexpr (FWD)  // the window of the 128-value tile holding chunk gc, 128 rows
+              if constexpr (FWD && WT == RG_Q4_K) {
+                // the super-block headers, then the chunk's nibbles (map_l), 128 rows each
+                const int sb = (gc >> 2) * 144;
+                tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_p(s), sb / 4, kt * BM);
+                tma_load_2d(smem_addr(sP + s * C::P_STAGE) + 128 * 16, &map_l, full_p(s),
+                            (sb + 16 + 32 * (gc & 3)) / 4, kt * BM);
+              } else if constexpr (FWD && WT == RG_Q8_0) {  // the chunk's two blocks
+                tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_p(s), ((gc * 68) & ~15) / 4,
+                            kt * BM);
+              } else if constexpr (FWD) {  // the window of the 128-value tile holding chunk gc
                 tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_p(s),
                             p_window_start<WT>(gc >> 1) / 4, kt * BM);
-              else
+              } else
                 tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_p(s),
                             p_window_start<WT>(kt) / 4, gc * BC);
               pend_p |= 1u << s;
@@ -1375,7 +1427,7 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
   if ((p.n_splits > 1 || p.sk) && part == nullptr) return cudaErrorInvalidValue;
   float* partial = p.n_splits > 1 || p.sk ? part : nullptr;
   p.band = tc_band(wtype, n_ext, p);
-  CUtensorMap mw, my;
+  CUtensorMap mw, my, mq;
   CUresult r;
   if (is_quant(wtype)) {
     const uint64_t rb = static_cast<uint64_t>(K / block_values(wtype) * block_bytes(wtype));
@@ -1383,8 +1435,14 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
       return tc::p_row_bytes<decltype(wt)::value>();
     }));
     // a stage's packed windows: 64 contraction rows, or the forward's 128 output rows
+    // (the forward's Q4_K: the 16-byte headers here, the 32 nibble bytes in map_l)
+    const bool split = FWD && wtype == RG_Q4_K;
+    const uint32_t box_words = split ? 4 : (FWD && wtype == RG_Q8_0) ? 20 : box_bytes / 4;
     r = encode_tiled(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rb / 4, static_cast<uint64_t>(N), rb,
-                     box_bytes / 4, FWD ? 2 * tc::BC : tc::BC, CU_TENSOR_MAP_SWIZZLE_NONE);
+                     box_words, FWD ? 2 * tc::BC : tc::BC, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (r == CUDA_SUCCESS && split)
+      r = encode_tiled(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rb / 4, static_cast<uint64_t>(N), rb, 8,
+                       2 * tc::BC, CU_TENSOR_MAP_SWIZZLE_NONE);
   } else {
     r = encode_tiled(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, W, static_cast<uint64_t>(K),
                      static_cast<uint64_t>(N), static_cast<uint64_t>(K) * 2, 64,
@@ -1395,9 +1453,9 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
                    static_cast<uint64_t>(T), static_cast<uint64_t>(ld_dy16) * 2, tc::BC,
                    tc::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  // the adapter's rows [rank, K] (16-bit, same kind as the decoded W); without
-  // one the map is a copy that no stage reads
-  CUtensorMap ml = mw;
+  // the adapter's rows [rank, K] (16-bit, same kind as the decoded W), or the
+  // forward's Q4_K nibble copies; else a copy that no stage reads
+  CUtensorMap ml = (FWD && wtype == RG_Q4_K) ? mq : mw;
   if (rank > 0) {
     r = encode_tiled(&ml, CU_TENSOR_MAP_DATA_TYPE_UINT16, a16, static_cast<uint64_t>(K),
                      static_cast<uint64_t>(rank), static_cast<uint64_t>(K) * 2, 64, tc::BC,
