@@ -105,15 +105,19 @@ struct Cfg {
   static constexpr int P_ROW = FWD ? p_fwd_row_bytes<WT>() : p_row_bytes<WT>();
   static constexpr int P_STAGE = QUANT ? ((P_ROWS * P_ROW + 1023) / 1024) * 1024 : 0;
   static constexpr int STAGE = A_STAGE + B_STAGE + P_STAGE;
-  // quantized: five slots (the forward: as many as fit, at most five), each
+  // the epilogue's staging for its bulk stores: per epilogue warp two halves
+  // of 16 rows of t by 32 values of k, F32
+  static constexpr int EPI_BYTES = 4 * 2 * 16 * 32 * 4;
+  // quantized: five slots (Q6_K four; fewer when they do not fit), each
   // decoded by two warps; F16/BF16: as deep as fits
-  static constexpr int S = QUANT ? (FWD ? std::min(5, SMEM_BUDGET / STAGE) : (WT == RG_Q6_K ? 4 : 5))
-                                 : std::min(8, SMEM_BUDGET / STAGE);
+  static constexpr int S = QUANT ? std::min(WT == RG_Q6_K && !FWD ? 4 : 5, (SMEM_BUDGET - EPI_BYTES) / STAGE)
+                                 : std::min(8, (SMEM_BUDGET - EPI_BYTES) / STAGE);
   static constexpr int WARPS_PER_SLOT = QUANT ? 2 : 0;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + S * A_STAGE;
   static constexpr int OFF_P = OFF_B + S * B_STAGE;
-  static constexpr int OFF_BAR = OFF_P + S * P_STAGE;
+  static constexpr int OFF_EPI = OFF_P + S * P_STAGE;
+  static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
   // barriers: full_p, full_ab, full_dec, empty (S each), acc_full[2],
   // acc_empty[2], drain
   static constexpr int NUM_BARS = 4 * S + 5;
@@ -873,7 +877,8 @@ template <int WT, int CG, int BT, bool AD, bool SK, bool FWD = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     out_prod_tc_kernel(const __grid_constant__ CUtensorMap map_w,
                        const __grid_constant__ CUtensorMap map_y,
-                       const __grid_constant__ CUtensorMap map_l, int n_main,
+                       const __grid_constant__ CUtensorMap map_l,
+                       const __grid_constant__ CUtensorMap map_x, int n_main,
                        float* __restrict__ dX, int64_t ldx, float beta, int T, int K,
                        int n_kunits, int n_ttiles, int band, int n_chunks, int n_splits,
                        float* __restrict__ part, WaitCtl ctl) {
@@ -1251,6 +1256,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // stream-K: one partial slab per unit ([unit][CTA of the pair]
     // [epilogue warp][t of the tile][lane]), one warp's piece SLAB_W floats
     constexpr int SLAB_W = BT * 32;
+    float* stg = reinterpret_cast<float*>(smem + C::OFF_EPI) + eq * (2 * 16 * 32);
     bool ok = true;
     Segs<SK> sg(unit, n_units, n_tiles, n_chunks);
     int tile = 0, c0 = 0, c1 = 0;
@@ -1271,11 +1277,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float* out = split_part ? split_part + static_cast<int64_t>(tile / n_tiles1) * T * K : dX;
         const float b = split_part ? 0.0f : beta;
         const int64_t ldo = split_part ? static_cast<int64_t>(K) : ldx;  // row stride of `out`
+        // dX with beta 0 or 1: 16 x 32 boxes staged in shared memory and
+        // written by bulk tensor stores (beta 1: bulk adds into dX), so the
+        // warp issues 16 shared stores a box instead of 16 global ones a row
+        // of lanes; a split's partial sums and any other beta are stored
+        // element by element
+        const bool bulk = split_part == nullptr && (b == 0.0f || b == 1.0f);
 #pragma unroll 1
         for (int cb = 0; cb < BT / 32; ++cb) {
           const int tb = tt * BT + 32 * cb;
           float old[32];
-          if (b != 0.0f && kin) {
+          if (!bulk && b != 0.0f && kin) {
             // all loads of the column block first: one round trip, not 32
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -1285,7 +1297,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * eq) << 16) +
                                  static_cast<uint32_t>(a * BT + 32 * cb),
                              r);
-          if (kin) {
+          if (bulk) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              float* half = stg + h * (16 * 32);
+              // the store issued from this half two halves ago has read it
+              if (lane == 0) bulk_wait_read_1();
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) half[i * 32 + lane] = __uint_as_float(r[16 * h + i]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                const int x = kt * BM + 32 * eq, y = tb + 16 * h;
+                if (x < K && y < T) {
+                  if (b == 0.0f)
+                    tma_store_2d(&map_x, smem_addr(half), x, y);
+                  else
+                    tma_add_2d(&map_x, smem_addr(half), x, y);
+                }
+                bulk_commit();
+              }
+            }
+          } else if (kin) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               if (tb + i < T) {
@@ -1327,6 +1361,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
+    // the bulk stores have completed (their staging is freed with the CTA)
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -1349,7 +1386,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 template <int WT, int CG, int BT, bool AD, bool SK, bool FWD>
 static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
-                               const CUtensorMap& ml, int n_main, float* dX, int64_t ldx,
+                               const CUtensorMap& ml, const CUtensorMap& mx, int n_main, float* dX,
+                               int64_t ldx,
                                float beta, int T, int K, const TcPlan& p, float* part,
                                const DevInfo& dev, cudaStream_t stream) {
   using C = tc::Cfg<WT, CG, BT, FWD>;
@@ -1386,7 +1424,7 @@ static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
   const int units = std::min(p.grid / CG, mc);
   cfg.gridDim = dim3(static_cast<unsigned>(units * CG), 1, 1);
   if (SK && part == nullptr) return cudaErrorInvalidValue;
-  e = counted(cudaLaunchKernelEx(&cfg, kern, mw, my, ml, n_main, dX, ldx, beta, T, K, p.n_kunits,
+  e = counted(cudaLaunchKernelEx(&cfg, kern, mw, my, ml, mx, n_main, dX, ldx, beta, T, K, p.n_kunits,
                                  p.n_ttiles, p.band, p.n_chunks, p.n_splits, part, ctl));
   if (e != cudaSuccess || !SK) return e;
   // stream-K: the shared tiles' pieces, added in chunk order (the same unit
@@ -1396,14 +1434,14 @@ static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
 
 template <int WT, bool AD, bool SK, bool FWD>
 static cudaError_t launch_tc_w(const CUtensorMap& mw, const CUtensorMap& my,
-                               const CUtensorMap& ml, int n_main, float* dX, int64_t ldx,
-                               float beta, int T, int K, const TcPlan& p, float* part,
+                               const CUtensorMap& ml, const CUtensorMap& mx, int n_main, float* dX,
+                               int64_t ldx, float beta, int T, int K, const TcPlan& p, float* part,
                                const DevInfo& dev, cudaStream_t stream) {
   if (p.cg == 2)
-    return launch_tc_t<WT, 2, 256, AD, SK, FWD>(mw, my, ml, n_main, dX, ldx, beta, T, K, p, part,
+    return launch_tc_t<WT, 2, 256, AD, SK, FWD>(mw, my, ml, mx, n_main, dX, ldx, beta, T, K, p, part,
                                                 dev, stream);
-  return launch_tc_t<WT, 1, 128, AD, SK, FWD>(mw, my, ml, n_main, dX, ldx, beta, T, K, p, part, dev,
-                                              stream);
+  return launch_tc_t<WT, 1, 128, AD, SK, FWD>(mw, my, ml, mx, n_main, dX, ldx, beta, T, K, p, part,
+                                              dev, stream);
 }
 
 // The body of launch_tc: AD = an adapter rides along (rank > 0).  W is N
@@ -1462,10 +1500,16 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
                      CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
+  // the output for the epilogue's bulk stores: F32 [T, k_out], rows dx_t apart, 32 x 16 boxes
+  CUtensorMap mx;
+  r = encode_tiled(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dX, static_cast<uint64_t>(k_out),
+                   static_cast<uint64_t>(T), static_cast<uint64_t>(dx_t) * 4, 32, 16,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   const int t = static_cast<int>(T), k = static_cast<int>(k_out);
   const cudaError_t e = with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
-    return launch_tc_w<decltype(wt)::value, AD, SK, FWD>(mw, my, ml, n_main, dX, dx_t, beta, t, k,
-                                                        p, partial, dev, stream);
+    return launch_tc_w<decltype(wt)::value, AD, SK, FWD>(mw, my, ml, mx, n_main, dX, dx_t, beta, t,
+                                                        k, p, partial, dev, stream);
   });
   if (e != cudaSuccess || p.n_splits == 1) return e;
   return launch_reduce_partials(partial, p.n_splits, T, k_out, dX, dx_t, beta, dev, stream);
