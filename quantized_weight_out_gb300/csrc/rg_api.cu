@@ -313,13 +313,13 @@ namespace {
 // microseconds, and a training step calls with the same tensors every time.
 struct MapKey {
   const void* base;
-  uint64_t dim0, dim1, stride1;
+  uint64_t dim0, dim1, stride1, dim2, stride2;
   uint32_t box0, box1;
   int dtype, swizzle, device;
   bool operator==(const MapKey& o) const {
     return base == o.base && dim0 == o.dim0 && dim1 == o.dim1 && stride1 == o.stride1 &&
-           box0 == o.box0 && box1 == o.box1 && dtype == o.dtype && swizzle == o.swizzle &&
-           device == o.device;
+           dim2 == o.dim2 && stride2 == o.stride2 && box0 == o.box0 && box1 == o.box1 &&
+           dtype == o.dtype && swizzle == o.swizzle && device == o.device;
   }
 };
 struct MapEntry {
@@ -360,11 +360,12 @@ cudaError_t ensure_smem_attr(const void* func, int bytes) {
 
 CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                       uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes, uint32_t box0,
-                      uint32_t box1, CUtensorMapSwizzle swizzle) {
+                      uint32_t box1, CUtensorMapSwizzle swizzle, uint64_t dim2,
+                      uint64_t stride2_bytes) {
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return CUDA_ERROR_INVALID_CONTEXT;
-  const MapKey key{base, dim0, dim1, stride1_bytes, box0, box1, static_cast<int>(dtype),
-                   static_cast<int>(swizzle), device};
+  const MapKey key{base, dim0, dim1, stride1_bytes, dim2, stride2_bytes, box0, box1,
+                   static_cast<int>(dtype), static_cast<int>(swizzle), device};
   {
     std::lock_guard<std::mutex> lk(g_map_mu);
     for (MapEntry& m : g_maps)
@@ -375,7 +376,7 @@ CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, const void* b
       }
   }
   const CUresult r = encode_tiled_uncached(map, dtype, base, dim0, dim1, stride1_bytes, box0, box1,
-                                           swizzle);
+                                           swizzle, dim2, stride2_bytes);
   if (r != CUDA_SUCCESS) return r;
   std::lock_guard<std::mutex> lk(g_map_mu);
   MapEntry* slot = &g_maps[0];
@@ -389,7 +390,8 @@ CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, const void* b
 
 CUresult encode_tiled_uncached(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                                uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes, uint32_t box0,
-                               uint32_t box1, CUtensorMapSwizzle swizzle) {
+                               uint32_t box1, CUtensorMapSwizzle swizzle, uint64_t dim2,
+                               uint64_t stride2_bytes) {
   using Fn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                           const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
                           CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
@@ -404,11 +406,11 @@ CUresult encode_tiled_uncached(CUtensorMap* map, CUtensorMapDataType dtype, cons
     return reinterpret_cast<Fn>(p);
   }();
   if (!fn) return CUDA_ERROR_NOT_FOUND;
-  const cuuint64_t dims[2] = {dim0, dim1};
-  const cuuint64_t strides[1] = {stride1_bytes};
-  const cuuint32_t box[2] = {box0, box1};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+  const cuuint64_t dims[3] = {dim0, dim1, dim2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, dtype, dim2 > 1 ? 3 : 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }

@@ -238,12 +238,15 @@ cudaError_t launch_wait_probe(const DevInfo& dev, unsigned long long limit_ns,
 
 // cuTensorMapEncodeTiled (resolved from the driver at first use), through a
 // small cache of recently encoded maps keyed by address, shape and device.
+// dim2 > 1: a third dimension (rows of planes stride2_bytes apart), box 1 deep.
 CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                       uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes, uint32_t box0,
-                      uint32_t box1, CUtensorMapSwizzle swizzle);
+                      uint32_t box1, CUtensorMapSwizzle swizzle, uint64_t dim2 = 1,
+                      uint64_t stride2_bytes = 0);
 CUresult encode_tiled_uncached(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                                uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes, uint32_t box0,
-                               uint32_t box1, CUtensorMapSwizzle swizzle);
+                               uint32_t box1, CUtensorMapSwizzle swizzle, uint64_t dim2 = 1,
+                               uint64_t stride2_bytes = 0);
 
 // Raise `func`'s dynamic shared memory limit to `bytes` on the current device,
 // once per (kernel, device).

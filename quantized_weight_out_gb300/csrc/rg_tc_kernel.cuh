@@ -878,7 +878,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     out_prod_tc_kernel(const __grid_constant__ CUtensorMap map_w,
                        const __grid_constant__ CUtensorMap map_y,
                        const __grid_constant__ CUtensorMap map_l,
-                       const __grid_constant__ CUtensorMap map_x, int n_main,
+                       const __grid_constant__ CUtensorMap map_x,
+                       const __grid_constant__ CUtensorMap map_p, int n_main,
                        float* __restrict__ dX, int64_t ldx, float beta, int T, int K,
                        int n_kunits, int n_ttiles, int band, int n_chunks, int n_splits,
                        float* __restrict__ part, WaitCtl ctl) {
@@ -1277,12 +1278,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float* out = split_part ? split_part + static_cast<int64_t>(tile / n_tiles1) * T * K : dX;
         const float b = split_part ? 0.0f : beta;
         const int64_t ldo = split_part ? static_cast<int64_t>(K) : ldx;  // row stride of `out`
-        // dX with beta 0 or 1: 16 x 32 boxes staged in shared memory and
-        // written by bulk tensor stores (beta 1: bulk adds into dX), so the
-        // warp issues 16 shared stores a box instead of 16 global ones a row
-        // of lanes; a split's partial sums and any other beta are stored
-        // element by element
-        const bool bulk = split_part == nullptr && (b == 0.0f || b == 1.0f);
+        // dX with beta 0 or 1, or a split's partial sums: 16 x 32 boxes staged
+        // in shared memory and written by bulk tensor stores (beta 1: bulk
+        // adds into dX; a split's slab: a 3-D map, the split the third
+        // coordinate), so the warp issues 16 shared stores a box instead of
+        // 16 global ones a row of lanes; other beta are stored element by
+        // element
+        const bool bulk = b == 0.0f || b == 1.0f;
+        const int split = tile / n_tiles1;
 #pragma unroll 1
         for (int cb = 0; cb < BT / 32; ++cb) {
           const int tb = tt * BT + 32 * cb;
@@ -1311,7 +1314,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (lane == 0) {
                 const int x = kt * BM + 32 * eq, y = tb + 16 * h;
                 if (x < K && y < T) {
-                  if (b == 0.0f)
+                  if (split_part)
+                    tma_store_3d(&map_p, smem_addr(half), x, y, split);
+                  else if (b == 0.0f)
                     tma_store_2d(&map_x, smem_addr(half), x, y);
                   else
                     tma_add_2d(&map_x, smem_addr(half), x, y);
@@ -1348,8 +1353,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * eq) << 16) +
                                  static_cast<uint32_t>(a * BT + 32 * cb),
                              r);
+          // rows 32cb .. 32cb+31 of the piece are 4 KB of the slab: two staged
+          // 2 KB halves, each one bulk copy
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mine[(32 * cb + i) * 32 + lane] = __uint_as_float(r[i]);
+          for (int h = 0; h < 2; ++h) {
+            float* half = stg + h * (16 * 32);
+            if (lane == 0) bulk_wait_read_1();
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) half[i * 32 + lane] = __uint_as_float(r[16 * h + i]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              bulk_store(mine + (32 * cb + 16 * h) * 32, smem_addr(half), 16 * 32 * 4);
+              bulk_commit();
+            }
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -1386,8 +1405,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 template <int WT, int CG, int BT, bool AD, bool SK, bool FWD>
 static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
-                               const CUtensorMap& ml, const CUtensorMap& mx, int n_main, float* dX,
-                               int64_t ldx,
+                               const CUtensorMap& ml, const CUtensorMap& mx, const CUtensorMap& mp,
+                               int n_main, float* dX, int64_t ldx,
                                float beta, int T, int K, const TcPlan& p, float* part,
                                const DevInfo& dev, cudaStream_t stream) {
   using C = tc::Cfg<WT, CG, BT, FWD>;
@@ -1424,7 +1443,7 @@ static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
   const int units = std::min(p.grid / CG, mc);
   cfg.gridDim = dim3(static_cast<unsigned>(units * CG), 1, 1);
   if (SK && part == nullptr) return cudaErrorInvalidValue;
-  e = counted(cudaLaunchKernelEx(&cfg, kern, mw, my, ml, mx, n_main, dX, ldx, beta, T, K, p.n_kunits,
+  e = counted(cudaLaunchKernelEx(&cfg, kern, mw, my, ml, mx, mp, n_main, dX, ldx, beta, T, K, p.n_kunits,
                                  p.n_ttiles, p.band, p.n_chunks, p.n_splits, part, ctl));
   if (e != cudaSuccess || !SK) return e;
   // stream-K: the shared tiles' pieces, added in chunk order (the same unit
@@ -1434,14 +1453,14 @@ static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
 
 template <int WT, bool AD, bool SK, bool FWD>
 static cudaError_t launch_tc_w(const CUtensorMap& mw, const CUtensorMap& my,
-                               const CUtensorMap& ml, const CUtensorMap& mx, int n_main, float* dX,
-                               int64_t ldx, float beta, int T, int K, const TcPlan& p, float* part,
-                               const DevInfo& dev, cudaStream_t stream) {
+                               const CUtensorMap& ml, const CUtensorMap& mx, const CUtensorMap& mp,
+                               int n_main, float* dX, int64_t ldx, float beta, int T, int K,
+                               const TcPlan& p, float* part, const DevInfo& dev, cudaStream_t stream) {
   if (p.cg == 2)
-    return launch_tc_t<WT, 2, 256, AD, SK, FWD>(mw, my, ml, mx, n_main, dX, ldx, beta, T, K, p, part,
-                                                dev, stream);
-  return launch_tc_t<WT, 1, 128, AD, SK, FWD>(mw, my, ml, mx, n_main, dX, ldx, beta, T, K, p, part,
-                                              dev, stream);
+    return launch_tc_t<WT, 2, 256, AD, SK, FWD>(mw, my, ml, mx, mp, n_main, dX, ldx, beta, T, K, p,
+                                                part, dev, stream);
+  return launch_tc_t<WT, 1, 128, AD, SK, FWD>(mw, my, ml, mx, mp, n_main, dX, ldx, beta, T, K, p,
+                                              part, dev, stream);
 }
 
 // The body of launch_tc: AD = an adapter rides along (rank > 0).  W is N
@@ -1506,10 +1525,19 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
                    static_cast<uint64_t>(T), static_cast<uint64_t>(dx_t) * 4, 32, 16,
                    CU_TENSOR_MAP_SWIZZLE_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // a split contraction's partial sums [n_splits][T][k_out], the split the third dimension
+  CUtensorMap mp = mx;
+  if (p.n_splits > 1) {
+    r = encode_tiled(&mp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, partial, static_cast<uint64_t>(k_out),
+                     static_cast<uint64_t>(T), static_cast<uint64_t>(k_out) * 4, 32, 16,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, static_cast<uint64_t>(p.n_splits),
+                     static_cast<uint64_t>(T) * static_cast<uint64_t>(k_out) * 4);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   const int t = static_cast<int>(T), k = static_cast<int>(k_out);
   const cudaError_t e = with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
-    return launch_tc_w<decltype(wt)::value, AD, SK, FWD>(mw, my, ml, mx, n_main, dX, dx_t, beta, t,
-                                                        k, p, partial, dev, stream);
+    return launch_tc_w<decltype(wt)::value, AD, SK, FWD>(mw, my, ml, mx, mp, n_main, dX, dx_t, beta,
+                                                        t, k, p, partial, dev, stream);
   });
   if (e != cudaSuccess || p.n_splits == 1) return e;
   return launch_reduce_partials(partial, p.n_splits, T, k_out, dX, dx_t, beta, dev, stream);
