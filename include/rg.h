@@ -126,8 +126,9 @@ typedef enum {
                               F32 accumulation in tensor memory                             */
     RG_VARIANT_SMALLT = 2, /* small-T, weight-bandwidth-bound: TMA streams row stages
                               of W; exact F32 decode and F32 FMA with up to 8 dY rows
-                              (Q4_K: nibbles as exact fp16 operands of warp-level MMAs,
-                              dY*scale rounded to fp16 once, F32 accumulation); rows
+                              (Q4_K, Q8_0: the weight integers as exact fp16 operands of
+                              warp-level MMAs, dY*scale rounded to fp16 once, F32
+                              accumulation); rows
                               split over many CTAs, partial sums added in a fixed order
                               by a second kernel (N <= 256: one kernel writes dX)     */
     RG_VARIANT_SIMT32 = 3, /* exact F32 decode and F32 FMA with blocked accumulation: the

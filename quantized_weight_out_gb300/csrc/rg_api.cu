@@ -141,12 +141,12 @@ bool aligned_rows(int wtype, int64_t K) {
 int select_variant(int wtype, int64_t N, int64_t K, int64_t T) {
   if (!aligned_rows(wtype, K)) return RG_VARIANT_SIMT32;
   // a few rows of dY, or a problem too small to fill a tensor-core pipeline:
-  // the weight-streaming kernel (for Q4_K, whose warp-level MMA consumer
-  // costs little more at four rows than at one, up to four rows at any
-  // size); else the tensor cores (which split the contraction over idle SMs
-  // when the output is small)
+  // the weight-streaming kernel (for Q4_K and Q8_0, whose warp-level MMA
+  // consumer costs little more at four rows than at one, up to four rows at
+  // any size); else the tensor cores (which split the contraction over idle
+  // SMs when the output is small)
   const double flops = 2.0 * static_cast<double>(T) * static_cast<double>(N) * static_cast<double>(K);
-  if (T <= 2 || (wtype == RG_Q4_K && T <= 4) || (T <= 32 && flops <= 268435456.0))
+  if (T <= 2 || ((wtype == RG_Q4_K || wtype == RG_Q8_0) && T <= 4) || (T <= 32 && flops <= 268435456.0))
     return RG_VARIANT_SMALLT;
   return RG_VARIANT_TC;
 }

@@ -8,9 +8,9 @@
 //  * A producer warp streams the CTA's rows of W (its 256-value tile of each
 //    row) with TMA into a shared-memory ring of row stages, so enough bytes
 //    are in flight without holding them in registers.
-//  * Eight consumer warps decode from shared memory: Q4_K through the
-//    warp-level tensor-core MMA with the nibbles themselves as exact fp16
-//    operands (consume_q4k_mma); other quantized types at one or two dY rows
+//  * Eight consumer warps decode from shared memory: Q4_K and Q8_0 through
+//    the warp-level tensor-core MMA with the weight integers themselves as
+//    exact fp16 operands (consume_mma); other quantized types at one or two dY rows
 //    a block per warp and a row per lane in F32 (consume_rows); the rest
 //    eight values a lane, decoded exactly to F32, F32 FMAs.
 //  * The rows are split over many CTAs (grid.y) so that the whole GPU streams
@@ -345,10 +345,10 @@ __host__ __device__ constexpr int tile_bytes() {
 // rows per stage (two per lane) in a 4-deep ring; the row-per-warp consumers
 // 32 rows in an 8-deep ring (4-deep for F32 W, whose rows are four times
 // wider than the quantized ones).
-// Q4_K at up to eight rows of dY goes through the warp-level MMA consumer
-// (consume_q4k_mma), also with 64-row stages in a 4-deep ring.
+// Q4_K and Q8_0 at up to eight rows of dY go through the warp-level MMA
+// consumer (consume_mma), also with 64-row stages in a 4-deep ring.
 template <int WT, int TB>
-constexpr bool mma_path() { return WT == RG_Q4_K; }
+constexpr bool mma_path() { return WT == RG_Q4_K || WT == RG_Q8_0; }
 template <int WT, int TB>
 constexpr bool rows_path() {
   // (NVFP4's 16-value scales do not fit the block-per-warp layout: it takes
@@ -674,6 +674,12 @@ __device__ __forceinline__ void consume_rows(int g, const uint8_t* stage_buf, co
 //  * Per stage, the CTA first decodes each row's eight scales and mins
 //    (thread 4r + q: sub-blocks q and q + 4 of stage row r) into the fp16
 //    table B is loaded from, then every warp runs its MMAs over the 64 rows.
+//
+// Q8_0 takes the same path with its eight 32-value blocks in place of the
+// sub-blocks: B = fp16(y * 2^s * d) per (row, block), no min term, and A the
+// int8 values as fp16 integers (1024 + 128 + q from one XOR into the
+// exponent bits, less 1152 in one packed subtraction: exact for every q, so
+// the only rounding before the F32 sums is B's).  Warp w owns block w.
 
 // D += A * B for one m16n8k16 tile (fp16 operands, F32 accumulation).
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -718,13 +724,28 @@ __device__ __forceinline__ bool consumers_sync_any(bool any) {
   return r != 0;
 }
 
-template <int TB, int BR, int STAGES_>
-__device__ __forceinline__ void consume_q4k_mma(int warp, int lane, const uint8_t* stage_buf,
-                                                float* ys, uint8_t* aux, uint32_t bar0,
-                                                int n_tiles, int nrows, int kt, int K, int t0, int T,
-                                                int split, SmtOut out, WaitCtl ctl,
-                                                volatile int* abort_flag) {
-  constexpr int TBYTES = 144;  // Q4_K super-block: d, dmin, 12 scale bytes, 128 nibble bytes
+// Q8_0's int8 q into the fp16 pair of one operand register: x holds byte q
+// of row n in bits 0..7 and of row n + 1 in bits 16..23 (other bits zero);
+// 0x6400 | (q ^ 0x80) is the fp16 value 1024 + 128 + q, exactly, and one
+// packed subtraction of 1152 leaves q.
+__device__ __forceinline__ uint32_t q8_pair(uint32_t x) {
+  const uint32_t biased = x ^ 0x64806480u;
+  uint32_t r;
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(biased), "r"(0x64806480u));
+  return r;
+}
+
+template <int WT, int TB, int BR, int STAGES_>
+__device__ __forceinline__ void consume_mma(int warp, int lane, const uint8_t* stage_buf,
+                                            float* ys, uint8_t* aux, uint32_t bar0,
+                                            int n_tiles, int nrows, int kt, int K, int t0, int T,
+                                            int split, SmtOut out, WaitCtl ctl,
+                                            volatile int* abort_flag) {
+  static_assert(WT == RG_Q4_K || WT == RG_Q8_0, "the MMA consumer takes Q4_K and Q8_0");
+  constexpr bool K4 = WT == RG_Q4_K;
+  // Q4_K super-block: d, dmin, 12 scale bytes, 128 nibble bytes; Q8_0: eight
+  // blocks of d and 32 int8 values
+  constexpr int TBYTES = K4 ? 144 : 272;
   static_assert(BR == 64, "64-row stages: one scale-pass thread per (row, q), four MMA row groups");
   uint16_t* yds = reinterpret_cast<uint16_t*>(aux);
   float* mred = reinterpret_cast<float*>(aux + 2 * yds_elems<TB>());
@@ -776,7 +797,23 @@ __device__ __forceinline__ void consume_q4k_mma(int warp, int lane, const uint8_
                                                       ctl, abort_flag));
     uint16_t* Y = yds + (i & 1) * (8 * TB * YDS_STRIDE);
     const uint8_t* stage = stage_buf + s * BR * TBYTES;
-    if (ok) {
+    if (ok && !K4) {
+      // the scales of blocks q and q + 4; a row past the slice (the next
+      // slice's, or TMA's zero fill past N) gets zero entries
+      const bool live = i * BR + srow < nrows;
+      const uint8_t* rowp = stage + srow * TBYTES;
+      const float d0 = live ? f16_to_f32(*reinterpret_cast<const uint16_t*>(rowp + 34 * q)) : 0.0f;
+      const float d1 = live ? f16_to_f32(*reinterpret_cast<const uint16_t*>(rowp + 34 * (q + 4))) : 0.0f;
+      const float* yr = ys + i * BR + srow;
+      const int pos = table_pos(srow);
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        const float y = yr[t * MAX_ROWS];
+        Y[(q * TB + t) * YDS_STRIDE + pos] = __half_as_ushort(__float2half_rn(y * d0));
+        Y[((q + 4) * TB + t) * YDS_STRIDE + pos] = __half_as_ushort(__float2half_rn(y * d1));
+      }
+    }
+    if (ok && K4) {
       // scales and mins of sub-blocks q and q + 4; a row past the slice (the
       // next slice's, or TMA's zero fill past N) gets zero entries
       const bool live = i * BR + srow < nrows;
@@ -806,6 +843,32 @@ __device__ __forceinline__ void consume_q4k_mma(int warp, int lane, const uint8_
       aborted = true;
       break;
     }
+    if constexpr (!K4) {
+      // warp w: block w; M row g is column 2g + h of the block, M row g + 8
+      // column 16 + 2g + h (h: the accumulator tile); 16-bit loads of the
+      // byte pairs (the blocks' values sit at even, not 4-byte, offsets)
+      const uint8_t* wq = stage + 34 * warp + 2 + 2 * g;
+#pragma unroll
+      for (int grp = 0; grp < BR / 16; ++grp) {
+        const int R = 16 * grp + 2 * c;
+        uint32_t x[8];  // rows R, R + 1, R + 8, R + 9, low and high pair each
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const uint8_t* rp = wq + (R + (r & 1) + 8 * (r >> 1)) * TBYTES;
+          x[2 * r] = *reinterpret_cast<const uint16_t*>(rp);
+          x[2 * r + 1] = *reinterpret_cast<const uint16_t*>(rp + 16);
+        }
+        uint2 yv = make_uint2(0u, 0u);  // B: rows R, R + 1 and R + 8, R + 9 at dY row g
+        if (g < TB) yv = *reinterpret_cast<const uint2*>(Y + (warp * TB + g) * YDS_STRIDE + 16 * grp + 4 * c);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          // byte h of each row's pair into the two halves (bytes 2 and 6: zero)
+          const uint32_t sel = h ? 0x6521u : 0x6420u;
+          mma_16816(acc[h], q8_pair(__byte_perm(x[0], x[2], sel)), q8_pair(__byte_perm(x[1], x[3], sel)),
+                    q8_pair(__byte_perm(x[4], x[6], sel)), q8_pair(__byte_perm(x[5], x[7], sel)), yv.x, yv.y);
+        }
+      }
+    } else {
     const uint8_t* wq = stage + 16 + 32 * c4 + 4 * g;
 #pragma unroll
     for (int grp = 0; grp < BR / 16; ++grp) {
@@ -825,6 +888,7 @@ __device__ __forceinline__ void consume_q4k_mma(int warp, int lane, const uint8_
         mma_16816(acc[h], p0 & M, p1 & M, r0 & M, r1 & M, yv.x, yv.y);
       }
     }
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar0 + 8u * (STAGES_ + s));
   }
@@ -832,6 +896,21 @@ __device__ __forceinline__ void consume_q4k_mma(int warp, int lane, const uint8_
   // a wait that gave up: no partial sums reach `out` (all consumer warps
   // leave here together, so the named barriers below stay matched)
   if (aborted) return;
+  if constexpr (!K4) {
+    // this lane's outputs: dY rows 2c, 2c + 1 at M rows g and g + 8 of both tiles
+    const float inv0 = 2 * c < TB ? row_unscale(smax[2 * c]) : 0.0f;
+    const float inv1 = 2 * c + 1 < TB ? row_unscale(smax[2 * c + 1]) : 0.0f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int t = 2 * c + (e & 1);
+        const int gk = kt * 256 + 32 * warp + 16 * (e >> 1) + 2 * g + h;
+        if (t < TB && t0 + t < T && gk < K)
+          smt_store(out, split, T, t0 + t, gk, acc[h][e] * ((e & 1) ? inv1 : inv0));
+      }
+    return;
+  } else {
   // the min terms of each sub-block over the slice's rows, in a fixed order:
   // lanes of one q (xor 4, 8, 16), then the eight warps
 #pragma unroll
@@ -874,6 +953,7 @@ __device__ __forceinline__ void consume_q4k_mma(int warp, int lane, const uint8_
         smt_store(out, split, T, t0 + t, gk, v);
       }
     }
+  }
   }
 }
 
@@ -968,7 +1048,7 @@ __global__ void __launch_bounds__(THREADS + 32, mma_path<WT, TB>() ? (TB <= 4 ? 
 
   if constexpr (mma_path<WT, TB>()) {
     if (warp < CONSUMERS)
-      consume_q4k_mma<TB, BR, STAGES>(warp, lane, stage_buf, ys, reinterpret_cast<uint8_t*>(red), bar0,
+      consume_mma<WT, TB, BR, STAGES>(warp, lane, stage_buf, ys, reinterpret_cast<uint8_t*>(red), bar0,
                                       n_tiles, nrows, kt, K, t0, T, split, out, ctl, abort_flag);
     return;
   } else if constexpr (rows_path<WT, TB>()) {

@@ -64,7 +64,9 @@ def test_dispatch(lib):
     assert rg.rg_select_variant(inputs.Q4_K, 14336, 4096, 2048) == rg.RG_VARIANT_TC
     assert rg.rg_select_variant(inputs.Q4_K, 14336, 4096, 4) == rg.RG_VARIANT_SMALLT
     assert rg.rg_select_variant(inputs.Q4_K, 14336, 4096, 5) == rg.RG_VARIANT_TC
-    assert rg.rg_select_variant(inputs.Q8_0, 14336, 4096, 4) == rg.RG_VARIANT_TC
+    assert rg.rg_select_variant(inputs.Q8_0, 14336, 4096, 4) == rg.RG_VARIANT_SMALLT
+    assert rg.rg_select_variant(inputs.Q8_0, 14336, 4096, 5) == rg.RG_VARIANT_TC
+    assert rg.rg_select_variant(inputs.Q4_0, 14336, 4096, 4) == rg.RG_VARIANT_TC
     # Q6_K rows are 16-byte aligned only for K % 2048 == 0; other K run on the SIMT variant
     assert rg.rg_select_variant(inputs.Q6_K, 4096, 4096, 2048) == rg.RG_VARIANT_TC
     assert rg.rg_select_variant(inputs.Q6_K, 4096, 5120, 2048) == rg.RG_VARIANT_SIMT32

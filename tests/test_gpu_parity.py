@@ -165,7 +165,9 @@ def _q4_k_scale_part(W, N, K):
 def test_one_hot_f32_variants_equal_rows(rg, variant, wtype):
     """F32 variants: one-hot dY reproduces rows of deq(W) exactly.  Q4_K on
     the small-T variant multiplies in the MMA with fp16(y * d * sc): one
-    rounding of the scale part, 2^-11 relative, and the F32 subtraction."""
+    rounding of the scale part, 2^-11 relative, and the F32 subtraction.
+    Q8_0's MMA operands are exact there (fp16(2^s * d) = 2^s * d, q an fp16
+    integer), so its rows come out exactly too."""
     N, K, T = 80, kfit(wtype, 512, variant), 6
     W = inputs.gen_weight(wtype, N, K, seed=6, stream=1)
     Wd = oracle.dequant(wtype, W, N, K)
@@ -184,14 +186,15 @@ def test_one_hot_f32_variants_equal_rows(rg, variant, wtype):
         assert np.array_equal(np.abs(got[t]), np.abs(Wd[n0[t]])), (t,)
 
 
+@pytest.mark.parametrize("wtype", [inputs.Q4_K, inputs.Q8_0])
 @pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8, 11])
-def test_smallt_q4_k_mma_rows(rg, T):
-    """The small-T Q4_K consumer (warp-level MMA, one to eight dY rows a
-    pass): ragged N against the 64-row stages and the row splits, three
-    k tiles, one dY row all zero (exact zeros out), one tiny (1e-30) and
-    one large (1e3) row, each kept in fp16's normal range by the row's
-    power-of-two scale."""
-    wtype, N, K = inputs.Q4_K, 1000, 768
+def test_smallt_mma_rows(rg, T, wtype):
+    """The small-T MMA consumer of Q4_K and Q8_0 (warp-level MMA, one to
+    eight dY rows a pass): ragged N against the 64-row stages and the row
+    splits, three k tiles, one dY row all zero (exact zeros out), one tiny
+    (1e-30) and one large (1e3) row, each kept in fp16's normal range by the
+    row's power-of-two scale."""
+    N, K = 1000, 768
     W = inputs.gen_weight(wtype, N, K, seed=31, stream=1)
     dY = inputs.normal_f32(31, 2, T * N, 1e-3).reshape(T, N)
     if T >= 3:
