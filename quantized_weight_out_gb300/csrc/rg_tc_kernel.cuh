@@ -105,13 +105,19 @@ struct Cfg {
   static constexpr int P_ROW = FWD ? p_fwd_row_bytes<WT>() : p_row_bytes<WT>();
   static constexpr int P_STAGE = QUANT ? ((P_ROWS * P_ROW + 1023) / 1024) * 1024 : 0;
   static constexpr int STAGE = A_STAGE + B_STAGE + P_STAGE;
-  // the epilogue's staging for its bulk stores: per epilogue warp two halves
-  // of 16 rows of t by 32 values of k, F32
-  static constexpr int EPI_BYTES = 4 * 2 * 16 * 32 * 4;
   // quantized: five slots (Q6_K four; fewer when they do not fit), each
   // decoded by two warps; F16/BF16: as deep as fits
-  static constexpr int S = QUANT ? std::min(WT == RG_Q6_K && !FWD ? 4 : 5, (SMEM_BUDGET - EPI_BYTES) / STAGE)
-                                 : std::min(8, (SMEM_BUDGET - EPI_BYTES) / STAGE);
+  static constexpr int S_MAX = QUANT ? (WT == RG_Q6_K && !FWD ? 4 : 5) : 8;
+  // the epilogue's staging for its bulk stores: per epilogue warp two boxes
+  // of EPI_ROWS rows of t by 32 values of k, F32 (16 KB for 16 rows); in the
+  // forward, boxes of 8 rows where the 8 KB they save buys one more stage
+  // slot (Q8_0's forward 4 -> 5 slots: 14 % faster; the OUT_PROD's Q5_K
+  // measured 9 % slower with the same trade, so it keeps 16 rows)
+  static constexpr int slots_with(int epi_bytes) { return std::min(S_MAX, (SMEM_BUDGET - epi_bytes) / STAGE); }
+  static constexpr int EPI_ROWS =
+      FWD && slots_with(4 * 2 * 8 * 32 * 4) > slots_with(4 * 2 * 16 * 32 * 4) ? 8 : 16;
+  static constexpr int EPI_BYTES = 4 * 2 * EPI_ROWS * 32 * 4;
+  static constexpr int S = slots_with(EPI_BYTES);
   static constexpr int WARPS_PER_SLOT = QUANT ? 2 : 0;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + S * A_STAGE;
@@ -1257,7 +1263,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // stream-K: one partial slab per unit ([unit][CTA of the pair]
     // [epilogue warp][t of the tile][lane]), one warp's piece SLAB_W floats
     constexpr int SLAB_W = BT * 32;
-    float* stg = reinterpret_cast<float*>(smem + C::OFF_EPI) + eq * (2 * 16 * 32);
+    constexpr int ER = C::EPI_ROWS;  // rows of t in a staged box
+    float* stg = reinterpret_cast<float*>(smem + C::OFF_EPI) + eq * (2 * ER * 32);
     bool ok = true;
     Segs<SK> sg(unit, n_units, n_tiles, n_chunks);
     int tile = 0, c0 = 0, c1 = 0;
@@ -1302,17 +1309,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                              r);
           if (bulk) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              float* half = stg + h * (16 * 32);
-              // the store issued from this half two halves ago has read it
+            for (int h = 0; h < 32 / ER; ++h) {
+              float* half = stg + (h & 1) * (ER * 32);
+              // the store issued from this box two boxes ago has read it
               if (lane == 0) bulk_wait_read_1();
               __syncwarp();
 #pragma unroll
-              for (int i = 0; i < 16; ++i) half[i * 32 + lane] = __uint_as_float(r[16 * h + i]);
+              for (int i = 0; i < ER; ++i) half[i * 32 + lane] = __uint_as_float(r[ER * h + i]);
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
-                const int x = kt * BM + 32 * eq, y = tb + 16 * h;
+                const int x = kt * BM + 32 * eq, y = tb + ER * h;
                 if (x < K && y < T) {
                   if (split_part)
                     tma_store_3d(&map_p, smem_addr(half), x, y, split);
@@ -1353,19 +1360,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * eq) << 16) +
                                  static_cast<uint32_t>(a * BT + 32 * cb),
                              r);
-          // rows 32cb .. 32cb+31 of the piece are 4 KB of the slab: two staged
-          // 2 KB halves, each one bulk copy
+          // rows 32cb .. 32cb+31 of the piece are 4 KB of the slab: staged
+          // boxes of ER rows, each one bulk copy
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float* half = stg + h * (16 * 32);
+          for (int h = 0; h < 32 / ER; ++h) {
+            float* half = stg + (h & 1) * (ER * 32);
             if (lane == 0) bulk_wait_read_1();
             __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) half[i * 32 + lane] = __uint_as_float(r[16 * h + i]);
+            for (int i = 0; i < ER; ++i) half[i * 32 + lane] = __uint_as_float(r[ER * h + i]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              bulk_store(mine + (32 * cb + 16 * h) * 32, smem_addr(half), 16 * 32 * 4);
+              bulk_store(mine + (32 * cb + ER * h) * 32, smem_addr(half), ER * 32 * 4);
               bulk_commit();
             }
           }
@@ -1519,17 +1526,22 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
                      CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  // the output for the epilogue's bulk stores: F32 [T, k_out], rows dx_t apart, 32 x 16 boxes
+  // the output for the epilogue's bulk stores: F32 [T, k_out], rows dx_t
+  // apart, boxes of 32 values by the kernel's staged rows
+  const uint32_t er = static_cast<uint32_t>(with_wtype(wtype, 16, [&](auto wt) {
+    constexpr int W_ = decltype(wt)::value;
+    return p.cg == 2 ? tc::Cfg<W_, 2, 256, FWD>::EPI_ROWS : tc::Cfg<W_, 1, 128, FWD>::EPI_ROWS;
+  }));
   CUtensorMap mx;
   r = encode_tiled(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dX, static_cast<uint64_t>(k_out),
-                   static_cast<uint64_t>(T), static_cast<uint64_t>(dx_t) * 4, 32, 16,
+                   static_cast<uint64_t>(T), static_cast<uint64_t>(dx_t) * 4, 32, er,
                    CU_TENSOR_MAP_SWIZZLE_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   // a split contraction's partial sums [n_splits][T][k_out], the split the third dimension
   CUtensorMap mp = mx;
   if (p.n_splits > 1) {
     r = encode_tiled(&mp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, partial, static_cast<uint64_t>(k_out),
-                     static_cast<uint64_t>(T), static_cast<uint64_t>(k_out) * 4, 32, 16,
+                     static_cast<uint64_t>(T), static_cast<uint64_t>(k_out) * 4, 32, er,
                      CU_TENSOR_MAP_SWIZZLE_NONE, static_cast<uint64_t>(p.n_splits),
                      static_cast<uint64_t>(T) * static_cast<uint64_t>(k_out) * 4);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
