@@ -380,11 +380,16 @@ class L2Flush:
 def time_calls(torch, rg, problems, devbuf, steps: int, warmup: int, forced: int, stream, dev,
                world: int) -> dict:
     """Warm-up, then `steps` timed steps of every call of `problems` on its
-    resident buffers (W, dY, dX): events around every call and around its
-    tensor-core GEMM kernel (rg_profile_next_gemm), the library's launch
-    count over the region, nvidia-smi clocks sampled meanwhile.  Inputs that
-    fit in L2 are flushed between steps (outside the calls, whose event times
-    then make up the step time)."""
+    resident buffers (W, dY, dX) with nothing recorded inside a call: their
+    time is the step time, the library's launch count over them the launch
+    count.  Then the same steps once more with events around every call and
+    around its tensor-core GEMM kernel (rg_profile_next_gemm): the per-call
+    and per-kernel times.  (An event between the dY conversion and the GEMM
+    stops the GEMM's programmatic early launch: about 3 % of a layer step, so
+    the step is timed without those events.)  nvidia-smi clocks are sampled
+    over both.  Inputs that fit in L2 are flushed between steps (outside the
+    calls, whose event times then make up the step time: the first pass
+    records events around each call, none inside)."""
     variants = [forced if forced else rg.rg_select_variant(p.wtype, p.N, p.K, p.T) for p in problems]
     is_tc = [v in (rg.RG_VARIANT_TC, rg.RG_VARIANT_TC_SINGLE, rg.RG_VARIANT_TC_PAIR) for v in variants]
     plans = []
@@ -400,12 +405,12 @@ def time_calls(torch, rg, problems, devbuf, steps: int, warmup: int, forced: int
             return rg.rg_out_prod_variant(forced, p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, stream)
         return rg.rg_out_prod(p.wtype, W, p.N, p.K, dY, p.T, dX, p.beta, stream)
 
-    def step(events=None):
+    def step(events=None, kernels=False):
         for i, p in enumerate(problems):
             W, dY, dX = devbuf[i]
             if events is not None:
                 events[i][0].record(stream)
-                if is_tc[i]:  # the library records these around its GEMM kernel
+                if kernels and is_tc[i]:  # the library records these around its GEMM kernel
                     rg.rg_profile_next_gemm(events[i][2], events[i][3])
             st = call(p, W, dY, dX)
             if events is not None:
@@ -418,14 +423,18 @@ def time_calls(torch, rg, problems, devbuf, steps: int, warmup: int, forced: int
         if flush is not None:
             flush()
     rg.check(rg.rg_check(stream), "warmup")
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in problems]
-           for _ in range(steps)]
-    # torch creates an event's handle at its first record; record every event
-    # once so the library gets real handles (its later records are the ones timed)
-    for row in evs:
-        for quad in row:
-            for e in quad:
-                e.record(stream)
+    def new_events():
+        evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in problems]
+               for _ in range(steps)]
+        # torch creates an event's handle at its first record; record every event
+        # once so the library gets real handles (its later records are the ones timed)
+        for row in evs:
+            for quad in row:
+                for e in quad:
+                    e.record(stream)
+        return evs
+
+    evs1, evs = new_events(), new_events()
     sampler = ClockSampler(_bus_id(torch, dev))
     if world > 1:
         torch.distributed.barrier()
@@ -436,21 +445,29 @@ def time_calls(torch, rg, problems, devbuf, steps: int, warmup: int, forced: int
     launches0 = rg.rg_launch_count()
     ev0.record(stream)
     for s in range(steps):
-        step(evs[s])
+        step(evs1[s] if flush is not None else None)
         if flush is not None:
             flush(float(s))
     ev1.record(stream)
     launches = rg.rg_launch_count() - launches0
     torch.cuda.synchronize()
-    clocks = sampler.stop()
     rg.check(rg.rg_check(stream), "timed region")
+    # the same steps with events around every call and its tensor-core kernel
+    for s in range(steps):
+        step(evs[s], kernels=True)
+        if flush is not None:
+            flush(float(s))
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    rg.check(rg.rg_check(stream), "timed kernels")
     per_call = [[evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(steps)]
                 for i in range(len(problems))]
     per_gemm = [[evs[s][i][2].elapsed_time(evs[s][i][3]) for s in range(steps)] if is_tc[i] else []
                 for i in range(len(problems))]
     ms_total = ev0.elapsed_time(ev1)
     if flush is not None:
-        ms_total = sum(sum(c) for c in per_call)
+        ms_total = sum(evs1[s][i][0].elapsed_time(evs1[s][i][1]) for s in range(steps)
+                       for i in range(len(problems)))
     planned = steps * sum(pl["launches"] for pl in plans)
     if launches != planned:
         raise RuntimeError(f"{launches} kernel launches in the timed region, the plans say {planned}")
@@ -619,7 +636,8 @@ def run_ours(args):
             "traffic_unit": "bytes per launch (ncu dram read+write, profiles/tc_traffic.json)",
             "peak_source": f"{src} {peak_kind} (dense fp16 = bf16 nominal); the burst figure unless "
                            "the timed region lasted seconds under sw_power_cap",
-            "kernel": "out_prod_tc_kernel (fused decode + tcgen05 GEMM), events around each launch",
+            "kernel": "out_prod_tc_kernel (fused decode + tcgen05 GEMM), events around each launch "
+                      "in a second pass of the same steps (the value's pass records none inside a call)",
             "launches_per_step": len(tc), "flops_per_launch": tc_flops / max(1, len(tc)),
             "ms_per_launch": gemm_ms / max(1, len(tc)),
             "dy_conversion_share_of_calls": (call_ms - gemm_ms) / call_ms if call_ms > 0 else None}
@@ -687,11 +705,12 @@ def run_ours(args):
 
 
 def _timed_calls(torch, rg, problems, call, args, stream, dev, world):
-    """Warm-up, then `args.steps` timed steps of call(i, p) over the problems:
-    per call a pair of events around the call and a pair around its main
-    tensor-core kernel (rg_profile_next_gemm); clocks sampled meanwhile.
-    Returns (ms per step over ranks, launches, clocks, per-call ms, GEMM ms
-    per step)."""
+    """Warm-up, then `args.steps` timed steps of call(i, p) over the problems
+    with nothing recorded inside a call (the step time and the launch count),
+    then the same steps again with a pair of events around each call and a
+    pair around its main tensor-core kernel (rg_profile_next_gemm); clocks
+    sampled over both.  Returns (ms per step over ranks, launches, clocks,
+    per-call ms, GEMM ms per step)."""
     def step(evs=None):
         for i, p in enumerate(problems):
             if evs is not None:
@@ -722,12 +741,16 @@ def _timed_calls(torch, rg, problems, call, args, stream, dev, world):
     launches0 = rg.rg_launch_count()
     ev0.record(stream)
     for k in range(args.steps):
-        step(evs[k])
+        step()
     ev1.record(stream)
     launches = rg.rg_launch_count() - launches0
     torch.cuda.synchronize()
-    clocks = sampler.stop()
     rg.check(rg.rg_check(stream), "timed region")
+    for k in range(args.steps):
+        step(evs[k])
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    rg.check(rg.rg_check(stream), "timed kernels")
     ms_step = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dev)
     per_call = [statistics.median(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(args.steps))
                 for i in range(len(problems))]
@@ -786,7 +809,8 @@ def run_mul_mat(args):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": None,
                          "peak_source": f"{src} {peak_kind}",
-                         "kernel": "out_prod_tc_kernel on the transposed 16-bit copy of deq(W)"},
+                         "kernel": "out_prod_tc_kernel with FWD (W decoded in the kernel as the "
+                                   "K-major operand), events around each launch in a second pass"},
             "gpu_launches": launches, "clocks": clocks, "per_call": calls}
     if rank == 0:
         print(json.dumps(line), flush=True)

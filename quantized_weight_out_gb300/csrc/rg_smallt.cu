@@ -993,7 +993,12 @@ __global__ void __launch_bounds__(THREADS + 32, mma_path<WT, TB>() ? (TB <= 4 ? 
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
 
-  if (threadIdx.x == 0) {
+  // the producer's lane initialises the ring and starts its first copies
+  // before the block-wide barrier (fresh slots need no wait)
+  const bool producer = threadIdx.x == THREADS;
+  uint32_t pend = 0;                         // slots with a copy started
+  const int n_pre = min(STAGES, n_tiles);
+  if (producer) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), CONSUMERS);
@@ -1004,37 +1009,40 @@ __global__ void __launch_bounds__(THREADS + 32, mma_path<WT, TB>() ? (TB <= 4 ? 
       for (int t = 0; t < 8; ++t) smax[t] = 0;
     }
     fence_mbar_init();
+    for (int i = 0; i < n_pre; ++i) {
+      if (i == 0 && inject_stall != 0) continue;  // fault injection: the first stage never fills
+      mbar_arrive_expect_tx(full(i), BR * TBYTES);
+      tma_load_2d(smem_addr(stage_buf + i * BR * TBYTES), &map_w, full(i),
+                  static_cast<int>(window_start<WT>(kt) / 4), nbeg + i * BR);
+      pend |= 1u << i;
+    }
   }
-  __syncthreads();
   if (warp < CONSUMERS) {
     // this CTA's slice of dY, [TB][nrows], staged by the consumers while the
-    // producer's first copies are in flight
+    // producer sets up the ring and starts its first copies
     for (int idx = threadIdx.x; idx < TB * MAX_ROWS; idx += THREADS) {
       const int t = idx / MAX_ROWS, r = idx - t * MAX_ROWS;
       ys[idx] = (t0 + t < T && r < nrows)
                     ? __ldg(dY + static_cast<int64_t>(t0 + t) * dy_t + static_cast<int64_t>(nbeg + r) * dy_n)
                     : 0.0f;
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");  // the consumer warps only
   }
+  __syncthreads();  // the ring's barriers and the staged slice of dY
 
   if (warp == CONSUMERS) {
     // ---------------- producer ----------------
     if (lane == 0) {
-      uint32_t ph = 0, pend = 0, pend_ph = 0;  // slots with a copy started, and its parity
-      bool skip = inject_stall != 0;
-      for (int i = 0; i < n_tiles; ++i) {
+      // the copies after the first STAGES (which started before the barrier,
+      // phase 0), each into a slot its consumers have released
+      uint32_t ph = n_pre == STAGES ? 1u : 0u, pend_ph = 0;  // the phase of each started copy
+      for (int i = n_pre; i < n_tiles; ++i) {
         const int s = i % STAGES;
         if (!mbar_wait(empty(s), ph ^ 1u, ctl, abort_flag)) break;
-        if (skip) {
-          skip = false;  // fault injection: the first stage never fills
-        } else {
-          mbar_arrive_expect_tx(full(s), BR * TBYTES);
-          tma_load_2d(smem_addr(stage_buf + s * BR * TBYTES), &map_w, full(s),
-                      static_cast<int>(window_start<WT>(kt) / 4), nbeg + i * BR);
-          pend |= 1u << s;
-          pend_ph = (pend_ph & ~(1u << s)) | (ph << s);
-        }
+        mbar_arrive_expect_tx(full(s), BR * TBYTES);
+        tma_load_2d(smem_addr(stage_buf + s * BR * TBYTES), &map_w, full(s),
+                    static_cast<int>(window_start<WT>(kt) / 4), nbeg + i * BR);
+        pend |= 1u << s;
+        pend_ph = (pend_ph & ~(1u << s)) | (ph << s);
         if (s == STAGES - 1) ph ^= 1u;
       }
       // drain: every copy started lands before the CTA leaves (a consumed
