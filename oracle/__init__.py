@@ -12,5 +12,5 @@ from .quant_out_prod import (  # noqa: F401
     decode_q2_k, decode_q3_k, q3_k_scales, decode_mxfp4, e8m0_to_f32, e2m1_to_f32,
     decode_nvfp4, e4m3_to_f32,
     dequant, row_bytes, out_prod, abs_bound, out_prod_at, q4_k_scale_min, mul_mat, mul_mat_bound,
-    out_prod_lora, lora_bound, lora_at, batch_weight, out_prod_batched,
+    out_prod_lora, lora_bound, lora_at, batch_weight, out_prod_batched, mul_mat_at,
 )

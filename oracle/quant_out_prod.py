@@ -569,6 +569,22 @@ def out_prod_at(Wd, dY, ts, ks, dX0=None, beta: float = 0.0):
     return ref, bnd
 
 
+def mul_mat_at(Wd, X, ts, ns, Y0=None, beta: float = 0.0):
+    """Selected outputs of the forward one by one: (ref, bound) at pairs
+    (ts[i], ns[i]), each the F64 dot product of row ts[i] of X with row ns[i]
+    of deq(W) (plus beta*Y0 there; see mul_mat), and sum_k |X| |deq(W)|, for
+    parity checks on sizes whose full product is too large to form."""
+    ts = np.asarray(ts, dtype=np.int64)
+    ns = np.asarray(ns, dtype=np.int64)
+    rows = np.asarray(X, dtype=np.float32)[ts].astype(np.float64)    # [S, K]
+    wrow = np.asarray(Wd, dtype=np.float32)[ns].astype(np.float64)   # [S, K]
+    ref = np.einsum("sk,sk->s", rows, wrow)
+    bnd = np.einsum("sk,sk->s", np.abs(rows), np.abs(wrow))
+    if beta != 0.0:
+        ref = ref + float(np.float32(beta)) * np.asarray(Y0, dtype=np.float32)[ts, ns].astype(np.float64)
+    return ref, bnd
+
+
 def lora_at(dY, lora_a, lora_b, scale: float, ts, ks):
     """The adapter term at pairs (ts[i], ks[i]) one by one: (value, bound) of
     scale * sum_j (dY[t] . B[:, j]) A[j, k] and of its absolute terms, F64,

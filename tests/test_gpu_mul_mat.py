@@ -104,3 +104,28 @@ def test_mul_mat_shape_rules(rg):
     Y = torch.zeros((4, 100), device=dev)
     assert rg.rg_mul_mat(inputs.Q8_0, W, 100, 256, X, 4, Y, 0.0) == rg.RG_ERR_SHAPE   # N % 8
     assert rg.rg_mul_mat(inputs.Q8_0, W, 96, 200, X, 4, Y, 0.0) == rg.RG_ERR_SHAPE    # K % 256
+
+
+@pytest.mark.parametrize("idx", range(len(inputs.WORKLOADS["layer7b_t8192"])))
+def test_mul_mat_full_size_sampled(rg, idx):
+    """The forward at the layer sweep's full sizes, as bench.py --op mul_mat
+    times it (same X generator, rg_mul_mat's own plan): 4096 random (t, n)
+    outputs plus the whole first and last rows against the oracle, one by one."""
+    p = inputs.WORKLOADS["layer7b_t8192"][idx]
+    dev, s = torch.device("cuda:0"), torch.cuda.current_stream()
+    W = p.weight()
+    X = inputs.normal_f32(p.seed, 2 + p.stream_base, p.T * p.K, 1e-2).reshape(p.T, p.K)
+    Y = torch.full((p.T, p.N), float("nan"), device=dev)
+    rg.check(rg.rg_mul_mat(p.wtype, torch.from_numpy(W).to(dev), p.N, p.K, torch.from_numpy(X).to(dev),
+                           p.T, Y, 0.0, s), "rg_mul_mat")
+    rg.check(rg.rg_check(s))
+    got = Y.cpu().numpy()
+    assert np.isfinite(got).all()
+    Wd = oracle.dequant(p.wtype, W, p.N, p.K)
+    rng = np.random.default_rng(idx + 31)
+    ts = np.concatenate([rng.integers(0, p.T, 4096), np.zeros(p.N, np.int64), np.full(p.N, p.T - 1, np.int64)])
+    ns = np.concatenate([rng.integers(0, p.N, 4096), np.arange(p.N), np.arange(p.N)])
+    ref, bnd = oracle.mul_mat_at(Wd, X, ts, ns)
+    err = np.abs(got[ts, ns].astype(np.float64) - ref)
+    lim = 5e-3 * bnd + 1e-7
+    assert np.all(err <= lim), (p.name, int((err > lim).sum()), float((err / (bnd + 1e-30)).max()))

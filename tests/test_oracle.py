@@ -733,6 +733,26 @@ def test_linearity_and_beta():
     assert np.array_equal(oracle.out_prod(inputs.Q4_K, W, N, K, d1, T, nan0, 0.0), base)
 
 
+def test_mul_mat_at_matches_full():
+    """The sampled forward against the full one (itself pinned by one-hot
+    rows, the adjoint identity and brute force) and the pinned bound; the
+    operands swapped (deq(W) rows against X's columns) must not pass."""
+    N, K, T = 40, 512, 9
+    W = inputs.gen_weight(inputs.Q4_K, N, K, seed=10, stream=1)
+    X = inputs.normal_f32(10, 2, T * K, 1.0).reshape(T, K)
+    Y0 = inputs.normal_f32(10, 3, T * N, 1.0).reshape(T, N)
+    Wd = oracle.dequant(inputs.Q4_K, W, N, K)
+    full = oracle.mul_mat(inputs.Q4_K, W, N, K, X, T, Y0, 0.5, Wd=Wd)
+    bnd = oracle.mul_mat_bound(X, Wd)
+    ts = np.array([0, 8, 3, 3, 5])
+    ns = np.array([0, 39, 17, 18, 1])
+    ref, b = oracle.mul_mat_at(Wd, X, ts, ns, Y0, 0.5)
+    assert np.allclose(ref, full[ts, ns], rtol=1e-13, atol=1e-15)
+    assert np.allclose(b, bnd[ts, ns], rtol=1e-13)
+    bad, _ = oracle.mul_mat_at(Wd, X, ns % T, ts % N, Y0, 0.5)
+    assert not np.allclose(bad, full[ts, ns], rtol=1e-6)
+
+
 def test_out_prod_at_matches_full():
     N, K, T = 64, 256, 7
     W = inputs.gen_weight(inputs.Q8_0, N, K, seed=9, stream=1)
