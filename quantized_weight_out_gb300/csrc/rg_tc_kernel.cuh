@@ -88,12 +88,16 @@ __host__ __device__ constexpr int p_row_bytes() {
 // Bytes of one packed W row that the forward's 64-value stage copies: Q4_K
 // the 16-byte header and the chunk's 32 nibble bytes (two copies into two
 // regions of the stage); Q8_0 its two 34-byte blocks inside an 80-byte
-// window (0, 4, 8 or 12 bytes in); the other types their whole 128-value
-// window.
+// window (0, 4, 8 or 12 bytes in); Q6_K three windows that each start at
+// the same offset (0..14) into their first 16-byte grain: the half's 64
+// bytes of low bits (80), its 32 bytes of high bits (48), and the 16
+// scales and d (32); the other types their whole 128-value window.
 template <int WT>
 __host__ __device__ constexpr int p_fwd_row_bytes() {
-  return WT == RG_Q4_K ? 48 : WT == RG_Q8_0 ? 80 : p_row_bytes<WT>();
+  return WT == RG_Q4_K ? 48 : WT == RG_Q8_0 ? 80 : WT == RG_Q6_K ? 80 + 48 + 32 : p_row_bytes<WT>();
 }
+// The forward's Q6_K windows, bytes a row: low bits, high bits, scales and d.
+constexpr int Q6F_A = 80, Q6F_H = 48, Q6F_S = 32;
 
 template <int WT, int CG, int BT, bool FWD = false>
 struct Cfg {
@@ -200,6 +204,9 @@ struct RowWords {
     const int i = x >> 2, sh = x & 3;
     return sh == 0 ? w[i] : __funnelshift_r(w[i], w[i + 1], 8 * sh);
   }
+  // the byte at x, and the 16 bits at an even x, from one word
+  __device__ __forceinline__ uint32_t byte_at(int x) const { return (w[x >> 2] >> (8 * (x & 3))) & 0xFFu; }
+  __device__ __forceinline__ uint32_t half_at(int x) const { return (w[x >> 2] >> (8 * (x & 2))) & 0xFFFFu; }
 };
 template <int C0, int C1>
 __device__ __forceinline__ RowWords<4 * (C1 - C0 + 1)> load_chunks(const uint8_t* row) {
@@ -508,29 +515,38 @@ __device__ __forceinline__ void dec_q5_k_part(const uint8_t* row, uint8_t* A, in
 // super-block starts O bytes in.  Value 128H + 32i + l: nibble of
 // ql[64H + 32(i%2) + l] (high for i >= 2) and bits 2i..2i+1 of qh[32H + l]
 // give q; the operand is fp16(d * sc[8H + 2i + l/16]) * (q - 32).  G >= 0:
-// only the 64 values 64G .. 64G+63 of the half (chunks 8G .. 8G+7).
-template <int O, int H, int G = -1>
-__device__ __forceinline__ void dec_q6_k_row(const uint8_t* row, uint8_t* A, int n) {
-  constexpr int QA = O + 64 * H, QHB = O + 128 + 32 * H, QS = O + 192 + 8 * H, QD = O + 208;
+// only the 64 values 64G .. 64G+63 of the half (chunks 8G .. 8G+7).  SP (the
+// forward's split copy): the half's low bits at row, its high bits at rowh
+// and the scales and d at rows, each window starting O bytes in.
+template <int O, int H, int G = -1, bool SP = false>
+__device__ __forceinline__ void dec_q6_k_row(const uint8_t* row, uint8_t* A, int n,
+                                             const uint8_t* rowh = nullptr, const uint8_t* rows = nullptr) {
+  constexpr int QA = SP ? O : O + 64 * H, QHB = SP ? O : O + 128 + 32 * H;
+  constexpr int QS = SP ? O + 8 * H : O + 192 + 8 * H, QD = SP ? O + 16 : O + 208;
   // the last byte a word_at at offset x (relative to chunk C) reads
   constexpr auto last = [](int x) { return (x & 3) == 0 ? x + 3 : (x & ~3) + 7; };
   constexpr int CA = QA / 16, CA1 = CA + last(QA - 16 * CA + 60) / 16;
   constexpr int CH = QHB / 16, CH1 = CH + last(QHB - 16 * CH + 28) / 16;
   constexpr int CS = QS / 16, CS1 = (QD + 1) / 16;
-  static_assert(16 * CA1 + 16 <= p_row_bytes<RG_Q6_K>() && 16 * CH1 + 16 <= p_row_bytes<RG_Q6_K>() &&
-                    16 * CS1 + 16 <= p_row_bytes<RG_Q6_K>(),
+  static_assert(16 * CA1 + 16 <= (SP ? Q6F_A : p_row_bytes<RG_Q6_K>()) &&
+                    16 * CH1 + 16 <= (SP ? Q6F_H : p_row_bytes<RG_Q6_K>()) &&
+                    16 * CS1 + 16 <= (SP ? Q6F_S : p_row_bytes<RG_Q6_K>()),
                 "reads stay inside the row window");
   const auto ra = load_chunks<CA, CA1>(row);
-  const auto rh = load_chunks<CH, CH1>(row);
-  const auto rs = load_chunks<CS, CS1>(row);
+  const auto rh = load_chunks<CH, CH1>(SP ? rowh : row);
+  const auto rs = load_chunks<CS, CS1>(SP ? rows : row);
   constexpr int XA = QA - 16 * CA, XH = QHB - 16 * CH, XS = QS - 16 * CS, XD = QD - 16 * CS;
-  const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(rs.word_at(XD) & 0xFFFFu)));
+  // (the split windows end at the scales and d: read them a byte or 16 bits
+  // at a time, from the one word that holds them)
+  static_assert(XD % 2 == 0, "d at an even offset");
+  const float d = __half2float(__ushort_as_half(
+      static_cast<uint16_t>(SP ? rs.half_at(XD) : rs.word_at(XD) & 0xFFFFu)));
   __half2 ds[4][2];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int is = 0; is < 2; ++is) {
-      const int sc = static_cast<int8_t>(rs.word_at(XS + 2 * i + is) & 0xFFu);
+      const int sc = static_cast<int8_t>(SP ? rs.byte_at(XS + 2 * i + is) : rs.word_at(XS + 2 * i + is) & 0xFFu);
       ds[i][is] = __float2half2_rn(d * static_cast<float>(sc));  // exact product, one rounding
     }
   const __half2 off = __float2half2_rn(1056.0f);  // 1024 + 32
@@ -717,7 +733,9 @@ __device__ __forceinline__ void decode_stage_fwd(const uint8_t* __restrict__ P, 
       dec_q4_k_part<ODD, HV, 0>(hdr, q32, Ah, n);
       dec_q4_k_part<ODD, HV, 1>(hdr, q32, Ah, n);
     } else if constexpr (WT == RG_Q6_K) {
-      dec_q6_k_row<O, ODD, HV>(row, Ah, n);
+      // the three windows of the stage's 128 rows, one region each
+      dec_q6_k_row<O, ODD, HV, true>(P + n * Q6F_A, Ah, n, P + 128 * Q6F_A + n * Q6F_H,
+                                     P + 128 * (Q6F_A + Q6F_H) + n * Q6F_S);
     } else if constexpr (WT == RG_Q3_K) {
       dec_q3_k_row<O, ODD, HV>(row, Ah, n);
     } else if constexpr (WT == RG_Q2_K) {
@@ -885,7 +903,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                        const __grid_constant__ CUtensorMap map_y,
                        const __grid_constant__ CUtensorMap map_l,
                        const __grid_constant__ CUtensorMap map_x,
-                       const __grid_constant__ CUtensorMap map_p, int n_main,
+                       const __grid_constant__ CUtensorMap map_p,
+                       const __grid_constant__ CUtensorMap map_q, int n_main,
                        float* __restrict__ dX, int64_t ldx, float beta, int T, int K,
                        int n_kunits, int n_ttiles, int band, int n_chunks, int n_splits,
                        float* __restrict__ part, WaitCtl ctl) {
@@ -948,7 +967,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fence_mbar_init();
     tma_prefetch_map(&map_w);
     tma_prefetch_map(&map_y);
-    if constexpr (AD || (FWD && WT == RG_Q4_K)) tma_prefetch_map(&map_l);
+    if constexpr (AD || (FWD && (WT == RG_Q4_K || WT == RG_Q6_K))) tma_prefetch_map(&map_l);
+    if constexpr (FWD && WT == RG_Q6_K) tma_prefetch_map(&map_q);
   }
   if (warp == 1) {
     if constexpr (CG == 2) {
@@ -1018,6 +1038,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_p(s), sb / 4, kt * BM);
                 tma_load_2d(smem_addr(sP + s * C::P_STAGE) + 128 * 16, &map_l, full_p(s),
                             (sb + 16 + 32 * (gc & 3)) / 4, kt * BM);
+              } else if constexpr (FWD && WT == RG_Q6_K) {
+                // the half's low bits, its high bits, the scales and d (three
+                // windows, 128 rows each, one region of the stage apiece)
+                const int sb = (gc >> 2) * 210, h = (gc >> 1) & 1;
+                const uint32_t dst = smem_addr(sP + s * C::P_STAGE);
+                tma_load_2d(dst, &map_w, full_p(s), ((sb + 64 * h) & ~15) / 4, kt * BM);
+                tma_load_2d(dst + 128 * Q6F_A, &map_l, full_p(s), ((sb + 128 + 32 * h) & ~15) / 4, kt * BM);
+                tma_load_2d(dst + 128 * (Q6F_A + Q6F_H), &map_q, full_p(s), ((sb + 192) & ~15) / 4, kt * BM);
               } else if constexpr (FWD && WT == RG_Q8_0) {  // the chunk's two blocks
                 tma_load_2d(smem_addr(sP + s * C::P_STAGE), &map_w, full_p(s), ((gc * 68) & ~15) / 4,
                             kt * BM);
@@ -1413,7 +1441,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 template <int WT, int CG, int BT, bool AD, bool SK, bool FWD>
 static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
                                const CUtensorMap& ml, const CUtensorMap& mx, const CUtensorMap& mp,
-                               int n_main, float* dX, int64_t ldx,
+                               const CUtensorMap& mq, int n_main, float* dX, int64_t ldx,
                                float beta, int T, int K, const TcPlan& p, float* part,
                                const DevInfo& dev, cudaStream_t stream) {
   using C = tc::Cfg<WT, CG, BT, FWD>;
@@ -1450,7 +1478,7 @@ static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
   const int units = std::min(p.grid / CG, mc);
   cfg.gridDim = dim3(static_cast<unsigned>(units * CG), 1, 1);
   if (SK && part == nullptr) return cudaErrorInvalidValue;
-  e = counted(cudaLaunchKernelEx(&cfg, kern, mw, my, ml, mx, mp, n_main, dX, ldx, beta, T, K, p.n_kunits,
+  e = counted(cudaLaunchKernelEx(&cfg, kern, mw, my, ml, mx, mp, mq, n_main, dX, ldx, beta, T, K, p.n_kunits,
                                  p.n_ttiles, p.band, p.n_chunks, p.n_splits, part, ctl));
   if (e != cudaSuccess || !SK) return e;
   // stream-K: the shared tiles' pieces, added in chunk order (the same unit
@@ -1461,12 +1489,13 @@ static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
 template <int WT, bool AD, bool SK, bool FWD>
 static cudaError_t launch_tc_w(const CUtensorMap& mw, const CUtensorMap& my,
                                const CUtensorMap& ml, const CUtensorMap& mx, const CUtensorMap& mp,
-                               int n_main, float* dX, int64_t ldx, float beta, int T, int K,
-                               const TcPlan& p, float* part, const DevInfo& dev, cudaStream_t stream) {
+                               const CUtensorMap& mq, int n_main, float* dX, int64_t ldx, float beta,
+                               int T, int K, const TcPlan& p, float* part, const DevInfo& dev,
+                               cudaStream_t stream) {
   if (p.cg == 2)
-    return launch_tc_t<WT, 2, 256, AD, SK, FWD>(mw, my, ml, mx, mp, n_main, dX, ldx, beta, T, K, p,
+    return launch_tc_t<WT, 2, 256, AD, SK, FWD>(mw, my, ml, mx, mp, mq, n_main, dX, ldx, beta, T, K, p,
                                                 part, dev, stream);
-  return launch_tc_t<WT, 1, 128, AD, SK, FWD>(mw, my, ml, mx, mp, n_main, dX, ldx, beta, T, K, p,
+  return launch_tc_t<WT, 1, 128, AD, SK, FWD>(mw, my, ml, mx, mp, mq, n_main, dX, ldx, beta, T, K, p,
                                               part, dev, stream);
 }
 
@@ -1491,7 +1520,7 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
   if ((p.n_splits > 1 || p.sk) && part == nullptr) return cudaErrorInvalidValue;
   float* partial = p.n_splits > 1 || p.sk ? part : nullptr;
   p.band = tc_band(wtype, n_ext, p);
-  CUtensorMap mw, my, mq;
+  CUtensorMap mw, my, mq, m3;
   CUresult r;
   if (is_quant(wtype)) {
     const uint64_t rb = static_cast<uint64_t>(K / block_values(wtype) * block_bytes(wtype));
@@ -1501,12 +1530,17 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
     // a stage's packed windows: 64 contraction rows, or the forward's 128 output rows
     // (the forward's Q4_K: the 16-byte headers here, the 32 nibble bytes in map_l)
     const bool split = FWD && wtype == RG_Q4_K;
-    const uint32_t box_words = split ? 4 : (FWD && wtype == RG_Q8_0) ? 20 : box_bytes / 4;
+    const bool split6 = FWD && wtype == RG_Q6_K;  // three windows: low bits, high bits, scales
+    const uint32_t box_words = split ? 4 : (FWD && wtype == RG_Q8_0) ? 20 : split6 ? tc::Q6F_A / 4
+                                                                              : box_bytes / 4;
     r = encode_tiled(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rb / 4, static_cast<uint64_t>(N), rb,
                      box_words, FWD ? 2 * tc::BC : tc::BC, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (r == CUDA_SUCCESS && split)
-      r = encode_tiled(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rb / 4, static_cast<uint64_t>(N), rb, 8,
-                       2 * tc::BC, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (r == CUDA_SUCCESS && (split || split6))
+      r = encode_tiled(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rb / 4, static_cast<uint64_t>(N), rb,
+                       split ? 8 : tc::Q6F_H / 4, 2 * tc::BC, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (r == CUDA_SUCCESS && split6)
+      r = encode_tiled(&m3, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rb / 4, static_cast<uint64_t>(N), rb,
+                       tc::Q6F_S / 4, 2 * tc::BC, CU_TENSOR_MAP_SWIZZLE_NONE);
   } else {
     r = encode_tiled(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, W, static_cast<uint64_t>(K),
                      static_cast<uint64_t>(N), static_cast<uint64_t>(K) * 2, 64,
@@ -1519,7 +1553,9 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   // the adapter's rows [rank, K] (16-bit, same kind as the decoded W), or the
   // forward's Q4_K nibble copies; else a copy that no stage reads
-  CUtensorMap ml = (FWD && wtype == RG_Q4_K) ? mq : mw;
+  CUtensorMap ml = (FWD && (wtype == RG_Q4_K || wtype == RG_Q6_K)) ? mq : mw;
+  // the forward Q6_K's scales window; else a copy that no stage reads
+  if (!(FWD && wtype == RG_Q6_K)) m3 = mw;
   if (rank > 0) {
     r = encode_tiled(&ml, CU_TENSOR_MAP_DATA_TYPE_UINT16, a16, static_cast<uint64_t>(K),
                      static_cast<uint64_t>(rank), static_cast<uint64_t>(K) * 2, 64, tc::BC,
@@ -1548,7 +1584,7 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
   }
   const int t = static_cast<int>(T), k = static_cast<int>(k_out);
   const cudaError_t e = with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
-    return launch_tc_w<decltype(wt)::value, AD, SK, FWD>(mw, my, ml, mx, mp, n_main, dX, dx_t, beta,
+    return launch_tc_w<decltype(wt)::value, AD, SK, FWD>(mw, my, ml, mx, mp, m3, n_main, dX, dx_t, beta,
                                                         t, k, p, partial, dev, stream);
   });
   if (e != cudaSuccess || p.n_splits == 1) return e;
