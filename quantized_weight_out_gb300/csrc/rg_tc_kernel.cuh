@@ -204,9 +204,6 @@ struct RowWords {
     const int i = x >> 2, sh = x & 3;
     return sh == 0 ? w[i] : __funnelshift_r(w[i], w[i + 1], 8 * sh);
   }
-  // the byte at x, and the 16 bits at an even x, from one word
-  __device__ __forceinline__ uint32_t byte_at(int x) const { return (w[x >> 2] >> (8 * (x & 3))) & 0xFFu; }
-  __device__ __forceinline__ uint32_t half_at(int x) const { return (w[x >> 2] >> (8 * (x & 2))) & 0xFFFFu; }
 };
 template <int C0, int C1>
 __device__ __forceinline__ RowWords<4 * (C1 - C0 + 1)> load_chunks(const uint8_t* row) {
@@ -515,38 +512,29 @@ __device__ __forceinline__ void dec_q5_k_part(const uint8_t* row, uint8_t* A, in
 // super-block starts O bytes in.  Value 128H + 32i + l: nibble of
 // ql[64H + 32(i%2) + l] (high for i >= 2) and bits 2i..2i+1 of qh[32H + l]
 // give q; the operand is fp16(d * sc[8H + 2i + l/16]) * (q - 32).  G >= 0:
-// only the 64 values 64G .. 64G+63 of the half (chunks 8G .. 8G+7).  SP (the
-// forward's split copy): the half's low bits at row, its high bits at rowh
-// and the scales and d at rows, each window starting O bytes in.
-template <int O, int H, int G = -1, bool SP = false>
-__device__ __forceinline__ void dec_q6_k_row(const uint8_t* row, uint8_t* A, int n,
-                                             const uint8_t* rowh = nullptr, const uint8_t* rows = nullptr) {
-  constexpr int QA = SP ? O : O + 64 * H, QHB = SP ? O : O + 128 + 32 * H;
-  constexpr int QS = SP ? O + 8 * H : O + 192 + 8 * H, QD = SP ? O + 16 : O + 208;
+// only the 64 values 64G .. 64G+63 of the half (chunks 8G .. 8G+7).
+template <int O, int H, int G = -1>
+__device__ __forceinline__ void dec_q6_k_row(const uint8_t* row, uint8_t* A, int n) {
+  constexpr int QA = O + 64 * H, QHB = O + 128 + 32 * H, QS = O + 192 + 8 * H, QD = O + 208;
   // the last byte a word_at at offset x (relative to chunk C) reads
   constexpr auto last = [](int x) { return (x & 3) == 0 ? x + 3 : (x & ~3) + 7; };
   constexpr int CA = QA / 16, CA1 = CA + last(QA - 16 * CA + 60) / 16;
   constexpr int CH = QHB / 16, CH1 = CH + last(QHB - 16 * CH + 28) / 16;
   constexpr int CS = QS / 16, CS1 = (QD + 1) / 16;
-  static_assert(16 * CA1 + 16 <= (SP ? Q6F_A : p_row_bytes<RG_Q6_K>()) &&
-                    16 * CH1 + 16 <= (SP ? Q6F_H : p_row_bytes<RG_Q6_K>()) &&
-                    16 * CS1 + 16 <= (SP ? Q6F_S : p_row_bytes<RG_Q6_K>()),
+  static_assert(16 * CA1 + 16 <= p_row_bytes<RG_Q6_K>() && 16 * CH1 + 16 <= p_row_bytes<RG_Q6_K>() &&
+                    16 * CS1 + 16 <= p_row_bytes<RG_Q6_K>(),
                 "reads stay inside the row window");
   const auto ra = load_chunks<CA, CA1>(row);
-  const auto rh = load_chunks<CH, CH1>(SP ? rowh : row);
-  const auto rs = load_chunks<CS, CS1>(SP ? rows : row);
+  const auto rh = load_chunks<CH, CH1>(row);
+  const auto rs = load_chunks<CS, CS1>(row);
   constexpr int XA = QA - 16 * CA, XH = QHB - 16 * CH, XS = QS - 16 * CS, XD = QD - 16 * CS;
-  // (the split windows end at the scales and d: read them a byte or 16 bits
-  // at a time, from the one word that holds them)
-  static_assert(XD % 2 == 0, "d at an even offset");
-  const float d = __half2float(__ushort_as_half(
-      static_cast<uint16_t>(SP ? rs.half_at(XD) : rs.word_at(XD) & 0xFFFFu)));
+  const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(rs.word_at(XD) & 0xFFFFu)));
   __half2 ds[4][2];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int is = 0; is < 2; ++is) {
-      const int sc = static_cast<int8_t>(SP ? rs.byte_at(XS + 2 * i + is) : rs.word_at(XS + 2 * i + is) & 0xFFu);
+      const int sc = static_cast<int8_t>(rs.word_at(XS + 2 * i + is) & 0xFFu);
       ds[i][is] = __float2half2_rn(d * static_cast<float>(sc));  // exact product, one rounding
     }
   const __half2 off = __float2half2_rn(1056.0f);  // 1024 + 32
@@ -569,6 +557,55 @@ __device__ __forceinline__ void dec_q6_k_row(const uint8_t* row, uint8_t* A, int
 #pragma unroll
     for (int i = 0; i < 4; ++i)
       if (G < 0 || (i >> 1) == G) st_a_chunk(A, n, 4 * i + cq, o[i][0], o[i][1], o[i][2], o[i][3]);
+  }
+}
+
+// The forward's Q6_K chunk, values 64G .. 64G+63 of half H of a super-block,
+// from its three split windows (the half's low bits at pa, high bits at ph,
+// the scales and d at ps), each starting O bytes in; O (even) and H are run
+// time values, so one instance serves every super-block (instances per
+// offset made the forward instruction-fetch bound).  Words at O + 4j: an
+// aligned 32-bit load, or (U: O % 4 == 2) the two aligned words around it and
+// one 16-bit funnel shift; the scales and d by 16-bit loads.
+template <bool U, int G>
+__device__ __forceinline__ void dec_q6_k_fwd(const uint8_t* pa, const uint8_t* ph, const uint8_t* ps, int O,
+                                             int H, uint8_t* A, int n) {
+  auto word = [&](const uint8_t* base, int j) -> uint32_t {
+    if constexpr (!U) {
+      return *reinterpret_cast<const uint32_t*>(base + O + 4 * j);
+    } else {
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(base + O - 2);
+      return __funnelshift_r(w[j], w[j + 1], 16);
+    }
+  };
+  const float d = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(ps + O + 16)));
+  // scales 8H + 4G .. 8H + 4G + 3: quarters i = 2G, 2G + 1, values l < 16 and l >= 16
+  const uint8_t* psc = ps + O + 8 * H + 4 * G;
+  const uint32_t s01 = *reinterpret_cast<const uint16_t*>(psc), s23 = *reinterpret_cast<const uint16_t*>(psc + 2);
+  __half2 ds[2][2];
+  ds[0][0] = __float2half2_rn(d * static_cast<float>(static_cast<int8_t>(s01 & 0xFFu)));
+  ds[0][1] = __float2half2_rn(d * static_cast<float>(static_cast<int8_t>(s01 >> 8)));
+  ds[1][0] = __float2half2_rn(d * static_cast<float>(static_cast<int8_t>(s23 & 0xFFu)));
+  ds[1][1] = __float2half2_rn(d * static_cast<float>(static_cast<int8_t>(s23 >> 8)));
+  const __half2 off = __float2half2_rn(1056.0f);  // 1024 + 32
+#pragma unroll
+  for (int cq = 0; cq < 4; ++cq) {  // l = 8cq .. 8cq+7
+    uint32_t o[2][4];
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const int j = 2 * cq + jj;  // l = 4j .. 4j+3
+      const uint32_t a = word(pa, j), b = word(pa, j + 8), hq = word(ph, j);
+      // quarter i = 2G + e: the low (G = 0) or high (G = 1) nibbles of a (e = 0)
+      // or b (e = 1), bits 2i..2i+1 of hq above them
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const uint32_t q = e ? b : a;
+        const uint32_t x = ((q >> (4 * G)) & 0x0F0F0F0Fu) | (((hq >> (2 * (2 * G + e))) & 0x03030303u) << 4);
+        four_scaled(x, off, ds[e][cq >> 1], o[e][2 * jj], o[e][2 * jj + 1]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) st_a_chunk(A, n, 4 * (2 * G + e) + cq, o[e][0], o[e][1], o[e][2], o[e][3]);
   }
 }
 
@@ -732,18 +769,29 @@ __device__ __forceinline__ void decode_stage_fwd(const uint8_t* __restrict__ P, 
       const uint8_t* q32 = P + 128 * 16 + n * 32;
       dec_q4_k_part<ODD, HV, 0>(hdr, q32, Ah, n);
       dec_q4_k_part<ODD, HV, 1>(hdr, q32, Ah, n);
-    } else if constexpr (WT == RG_Q6_K) {
-      // the three windows of the stage's 128 rows, one region each
-      dec_q6_k_row<O, ODD, HV, true>(P + n * Q6F_A, Ah, n, P + 128 * Q6F_A + n * Q6F_H,
-                                     P + 128 * (Q6F_A + Q6F_H) + n * Q6F_S);
     } else if constexpr (WT == RG_Q3_K) {
       dec_q3_k_row<O, ODD, HV>(row, Ah, n);
     } else if constexpr (WT == RG_Q2_K) {
       dec_q2_k_row<O, ODD, HV>(row, Ah, n);
     } else {
+      static_assert(WT != RG_Q6_K, "the forward's Q6_K stage is decode_stage_fwd_q6");
       dec_item<WT, ODD, 2 * HV>(row, Ah, n, o);
       dec_item<WT, ODD, 2 * HV + 1>(row, Ah, n, o);
     }
+  }
+}
+
+// The forward's Q6_K stage: 128 rows of the chunk, the super-block O bytes
+// into its windows, half H, quarter G (of the half) HV.
+template <bool U, int HV>
+__device__ __forceinline__ void decode_stage_fwd_q6(const uint8_t* __restrict__ P, uint8_t* __restrict__ A,
+                                                    int lane, int part, int O, int H) {
+  uint8_t* Ah = A - HV * A_COLBLK;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int n = lane + 32 * (2 * part + r);
+    dec_q6_k_fwd<U, HV>(P + n * Q6F_A, P + 128 * Q6F_A + n * Q6F_H, P + 128 * (Q6F_A + Q6F_H) + n * Q6F_S, O, H,
+                        Ah, n);
   }
 }
 
@@ -766,7 +814,17 @@ __device__ __forceinline__ void decode_stage_fwd_q8(const uint8_t* __restrict__ 
 template <int WT>
 __device__ __forceinline__ void decode_fwd_stage(const uint8_t* __restrict__ P, uint8_t* __restrict__ A,
                                                  int lane, int part, int kw, int hv) {
-  if constexpr (WT == RG_Q6_K || WT == RG_Q3_K || WT == RG_Q2_K) {
+  if constexpr (WT == RG_Q6_K) {
+    // the super-block's offset into its grain, at run time (four instances)
+    const int o = ((kw >> 1) * block_bytes(WT)) & 15;
+    if (o & 2) {
+      if (hv) decode_stage_fwd_q6<true, 1>(P, A, lane, part, o, kw & 1);
+      else decode_stage_fwd_q6<true, 0>(P, A, lane, part, o, kw & 1);
+    } else {
+      if (hv) decode_stage_fwd_q6<false, 1>(P, A, lane, part, o, kw & 1);
+      else decode_stage_fwd_q6<false, 0>(P, A, lane, part, o, kw & 1);
+    }
+  } else if constexpr (WT == RG_Q3_K || WT == RG_Q2_K) {
     const int o = ((kw >> 1) * block_bytes(WT)) & 15;
 #define RG_FWD_CASE(OO)                                                                        \
   case OO / 2:                                                                                 \
