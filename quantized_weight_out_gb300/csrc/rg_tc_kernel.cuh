@@ -91,10 +91,14 @@ __host__ __device__ constexpr int p_row_bytes() {
 // window (0, 4, 8 or 12 bytes in); Q6_K three windows that each start at
 // the same offset (0..14) into their first 16-byte grain: the half's 64
 // bytes of low bits (80), its 32 bytes of high bits (48), and the 16
-// scales and d (32); the other types their whole 128-value window.
+// scales and d (32); Q3_K and Q2_K their 128-value window, widened to an odd
+// number of 16-byte grains (144, 112: the forward decoders' 32-bit loads of
+// one row a lane then fall in 8 bank groups, not 1 or 4); the other types
+// their whole 128-value window.
 template <int WT>
 __host__ __device__ constexpr int p_fwd_row_bytes() {
-  return WT == RG_Q4_K ? 48 : WT == RG_Q8_0 ? 80 : WT == RG_Q6_K ? 80 + 48 + 32 : p_row_bytes<WT>();
+  return WT == RG_Q4_K ? 48 : WT == RG_Q8_0 ? 80 : WT == RG_Q6_K ? 80 + 48 + 32
+         : WT == RG_Q3_K ? 144 : WT == RG_Q2_K ? 112 : p_row_bytes<WT>();
 }
 // The forward's Q6_K windows, bytes a row: low bits, high bits, scales and d.
 constexpr int Q6F_A = 80, Q6F_H = 48, Q6F_S = 32;
@@ -697,6 +701,81 @@ __device__ __forceinline__ void dec_q3_k_row(const uint8_t* row, uint8_t* A, int
     }
 }
 
+// The forward's Q2_K chunk (values 64G .. 64G+63 of half H) from a row
+// window whose super-block starts O bytes in; O (0, 4, 8, 12) and H at run
+// time (one instance for every super-block), every word an aligned 32-bit
+// load.  Values as dec_q2_k_row.
+template <int G>
+__device__ __forceinline__ void dec_q2_k_fwd(const uint8_t* row, int O, int H, uint8_t* A, int n) {
+  const uint8_t* b = row + O;
+  const uint32_t dw = *reinterpret_cast<const uint32_t*>(b + 80);
+  const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(dw & 0xFFFFu)));
+  const float dmin = __half2float(__ushort_as_half(static_cast<uint16_t>(dw >> 16)));
+  const uint32_t sw = *reinterpret_cast<const uint32_t*>(b + 8 * H + 4 * G);  // scale bytes 8H + 4G ..
+  const uint8_t* qb = b + 16 + 32 * H;
+  const __half2 magic = __float2half2_rn(1024.0f);
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+    for (int sb = 0; sb < 2; ++sb) {
+      const int j = 2 * G + jj;
+      const uint32_t sc = (sw >> (8 * (2 * jj + sb))) & 0xFFu;  // scales byte 8H + 2j + sb
+      const __half2 ds = __float2half2_rn(d * static_cast<float>(sc & 15u));       // exact product
+      const __half2 nm = __float2half2_rn(-(dmin * static_cast<float>(sc >> 4)));  // exact product
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {  // l = 8c .. 8c+7
+        const uint32_t* qw = reinterpret_cast<const uint32_t*>(qb + 16 * sb + 8 * c);
+        uint32_t o[4];
+        four_affine((qw[0] >> (2 * j)) & 0x03030303u, magic, ds, nm, o[0], o[1]);
+        four_affine((qw[1] >> (2 * j)) & 0x03030303u, magic, ds, nm, o[2], o[3]);
+        st_a_chunk(A, n, 4 * j + 2 * sb + c, o[0], o[1], o[2], o[3]);
+      }
+    }
+}
+
+// The forward's Q3_K chunk (values 64G .. 64G+63 of half H) from a row
+// window whose super-block starts O bytes in; O (even) and H at run time,
+// words at O + x by an aligned 32-bit load or (U: O % 4 == 2) the two
+// aligned words around them and one 16-bit funnel shift.  Values as
+// dec_q3_k_row.
+template <bool U, int G>
+__device__ __forceinline__ void dec_q3_k_fwd(const uint8_t* row, int O, int H, uint8_t* A, int n) {
+  auto word = [&](int x) -> uint32_t {
+    if constexpr (!U) {
+      return *reinterpret_cast<const uint32_t*>(row + O + x);
+    } else {
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(row + O - 2 + x);
+      return __funnelshift_r(w[0], w[1], 16);
+    }
+  };
+  const float d = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(row + O + 108)));
+  const uint32_t s_lo[2] = {word(96), word(100)};
+  const uint32_t s_hi = word(104);
+  const __half2 off = __float2half2_rn(1028.0f);  // 1024 + 4
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+    for (int sb = 0; sb < 2; ++sb) {
+      const int j = 2 * G + jj, il = 2 * j + sb;  // the sub-block 8H + il
+      const uint32_t lo = (s_lo[il >> 2] >> (8 * (il & 3) + 4 * H)) & 15u;
+      const uint32_t hi = (s_hi >> (8 * (il & 3) + 2 * (2 * H + (il >> 2)))) & 3u;
+      const int sc = static_cast<int>(lo | (hi << 4)) - 32;
+      const __half2 ds = __float2half2_rn(d * static_cast<float>(sc));  // exact product, one rounding
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {  // l = 8c .. 8c+7
+        uint32_t o[4];
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          const int x = 16 * sb + 8 * c + 4 * w;
+          const uint32_t q = (word(32 + 32 * H + x) >> (2 * j)) & 0x03030303u;
+          const uint32_t hb = (word(x) >> (4 * H + j)) & 0x01010101u;
+          four_scaled(q | (hb << 2), off, ds, o[2 * w], o[2 * w + 1]);
+        }
+        st_a_chunk(A, n, 4 * j + 2 * sb + c, o[0], o[1], o[2], o[3]);
+      }
+    }
+}
+
 // Block b (32-value types) or part b (Q4_K, Q5_K: chunk b >> 1 of the
 // half, 16 bytes b & 1) of row n of a stage.
 template <int WT, int ODD, int B>
@@ -769,15 +848,26 @@ __device__ __forceinline__ void decode_stage_fwd(const uint8_t* __restrict__ P, 
       const uint8_t* q32 = P + 128 * 16 + n * 32;
       dec_q4_k_part<ODD, HV, 0>(hdr, q32, Ah, n);
       dec_q4_k_part<ODD, HV, 1>(hdr, q32, Ah, n);
-    } else if constexpr (WT == RG_Q3_K) {
-      dec_q3_k_row<O, ODD, HV>(row, Ah, n);
-    } else if constexpr (WT == RG_Q2_K) {
-      dec_q2_k_row<O, ODD, HV>(row, Ah, n);
     } else {
-      static_assert(WT != RG_Q6_K, "the forward's Q6_K stage is decode_stage_fwd_q6");
+      static_assert(WT != RG_Q6_K && WT != RG_Q3_K && WT != RG_Q2_K,
+                    "the forward's K-quant stages are decode_stage_fwd_q6 and decode_stage_fwd_k");
       dec_item<WT, ODD, 2 * HV>(row, Ah, n, o);
       dec_item<WT, ODD, 2 * HV + 1>(row, Ah, n, o);
     }
+  }
+}
+
+// The forward's Q3_K and Q2_K stages: 128 rows of the chunk from their
+// whole windows, the super-block O bytes in, half H, quarter HV.
+template <int WT, bool U, int HV>
+__device__ __forceinline__ void decode_stage_fwd_k(const uint8_t* __restrict__ P, uint8_t* __restrict__ A,
+                                                   int lane, int part, int O, int H) {
+  uint8_t* Ah = A - HV * A_COLBLK;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int n = lane + 32 * (2 * part + r);
+    if constexpr (WT == RG_Q3_K) dec_q3_k_fwd<U, HV>(P + n * p_fwd_row_bytes<WT>(), O, H, Ah, n);
+    else dec_q2_k_fwd<HV>(P + n * p_fwd_row_bytes<WT>(), O, H, Ah, n);
   }
 }
 
@@ -825,25 +915,20 @@ __device__ __forceinline__ void decode_fwd_stage(const uint8_t* __restrict__ P, 
       else decode_stage_fwd_q6<false, 0>(P, A, lane, part, o, kw & 1);
     }
   } else if constexpr (WT == RG_Q3_K || WT == RG_Q2_K) {
+    // the super-block's offset into its grain (even; Q2_K a multiple of 4) at
+    // run time: two instances (Q2_K) or four (Q3_K)
     const int o = ((kw >> 1) * block_bytes(WT)) & 15;
-#define RG_FWD_CASE(OO)                                                                        \
-  case OO / 2:                                                                                 \
-    if constexpr (WT != RG_Q2_K || OO % 4 == 0) {                                              \
-      if (kw & 1) {                                                                            \
-        if (hv) decode_stage_fwd<WT, 1, 1, OO>(P, A, lane, part);                              \
-        else decode_stage_fwd<WT, 1, 0, OO>(P, A, lane, part);                                 \
-      } else {                                                                                 \
-        if (hv) decode_stage_fwd<WT, 0, 1, OO>(P, A, lane, part);                              \
-        else decode_stage_fwd<WT, 0, 0, OO>(P, A, lane, part);                                 \
-      }                                                                                        \
-    }                                                                                          \
-    break;
-    switch (o >> 1) {
-      RG_FWD_CASE(0) RG_FWD_CASE(2) RG_FWD_CASE(4) RG_FWD_CASE(6)
-      RG_FWD_CASE(8) RG_FWD_CASE(10) RG_FWD_CASE(12) RG_FWD_CASE(14)
-      default: break;
+    bool shifted = false;
+    if constexpr (WT == RG_Q3_K) shifted = (o & 2) != 0;
+    if constexpr (WT == RG_Q3_K) {
+      if (shifted) {
+        if (hv) decode_stage_fwd_k<WT, true, 1>(P, A, lane, part, o, kw & 1);
+        else decode_stage_fwd_k<WT, true, 0>(P, A, lane, part, o, kw & 1);
+        return;
+      }
     }
-#undef RG_FWD_CASE
+    if (hv) decode_stage_fwd_k<WT, false, 1>(P, A, lane, part, o, kw & 1);
+    else decode_stage_fwd_k<WT, false, 0>(P, A, lane, part, o, kw & 1);
   } else if constexpr (WT == RG_Q8_0) {
     // the 64-value chunk's two blocks start (68 gf) mod 16 bytes into its window
     switch ((((2 * kw + hv) * 68) & 15) >> 2) {
@@ -1583,7 +1668,7 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
   if (is_quant(wtype)) {
     const uint64_t rb = static_cast<uint64_t>(K / block_values(wtype) * block_bytes(wtype));
     const uint32_t box_bytes = static_cast<uint32_t>(with_wtype(wtype, 0, [](auto wt) {
-      return tc::p_row_bytes<decltype(wt)::value>();
+      return FWD ? tc::p_fwd_row_bytes<decltype(wt)::value>() : tc::p_row_bytes<decltype(wt)::value>();
     }));
     // a stage's packed windows: 64 contraction rows, or the forward's 128 output rows
     // (the forward's Q4_K: the 16-byte headers here, the 32 nibble bytes in map_l)
