@@ -106,12 +106,16 @@ def test_mul_mat_shape_rules(rg):
     assert rg.rg_mul_mat(inputs.Q8_0, W, 96, 200, X, 4, Y, 0.0) == rg.RG_ERR_SHAPE    # K % 256
 
 
-@pytest.mark.parametrize("idx", range(len(inputs.WORKLOADS["layer7b_t8192"])))
-def test_mul_mat_full_size_sampled(rg, idx):
-    """The forward at the layer sweep's full sizes, as bench.py --op mul_mat
-    times it (same X generator, rg_mul_mat's own plan): 4096 random (t, n)
-    outputs plus the whole first and last rows against the oracle, one by one."""
-    p = inputs.WORKLOADS["layer7b_t8192"][idx]
+FULL_FWD = [(w, i) for w in ("layer7b_t8192", "types_4096x4096_t8192") for i in range(len(inputs.WORKLOADS[w]))]
+
+
+@pytest.mark.parametrize("workload,idx", FULL_FWD)
+def test_mul_mat_full_size_sampled(rg, workload, idx):
+    """The forward at full size, as bench.py --op mul_mat times it (same X
+    generator, rg_mul_mat's own plan): the layer sweep's shapes and every
+    weight type at 4096 x 4096, T = 8192; 4096 random (t, n) outputs plus the
+    whole first and last rows against the oracle, one by one."""
+    p = inputs.WORKLOADS[workload][idx]
     dev, s = torch.device("cuda:0"), torch.cuda.current_stream()
     W = p.weight()
     X = inputs.normal_f32(p.seed, 2 + p.stream_base, p.T * p.K, 1e-2).reshape(p.T, p.K)
