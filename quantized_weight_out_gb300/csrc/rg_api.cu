@@ -279,7 +279,12 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
   const bool bf16 = wtype == RG_BF16 || wtype == RG_F32;
   const int64_t ld = tc_dy16_ld(N);
   uint16_t* dy16 = static_cast<uint16_t*>(buf);
-  e = launch_convert_dy(dY, T, N, lay.dy_t, lay.dy_n, ld, bf16, dy16, *dev, stream);
+  // a contraction split in two with beta 0: the conversion zeroes dX and the
+  // two halves add themselves into it (no partial sums, no reduction kernel)
+  const bool halves = tc_adds_halves(N, K, T, beta, lay.dy_n == 1 && lay.dy_t == N, *dev,
+                                     cg_force_of(variant));
+  e = launch_convert_dy(dY, T, N, lay.dy_t, lay.dy_n, ld, bf16, dy16, *dev, stream, 1.0f,
+                        halves ? dX : nullptr, K, lay.dx_t);
   const void* Wtc = W;
   int wtc = wtype;
   if (wtype == RG_F32) {
@@ -296,7 +301,7 @@ int run(int variant, int wtype, const void* W, int64_t N, int64_t K, const float
     e = launch_tc(wtc, Wtc, N, K, dy16, ld, T, dX, lay.dx_t, beta,
                   reinterpret_cast<float*>(static_cast<char*>(buf) +
                                            tc_partial_offset(wtype, N, K, T)),
-                  *dev, stream, cg_force_of(variant));
+                  *dev, stream, cg_force_of(variant), nullptr, 0, halves);
   if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, stream);
   if (own_ws) {
     const cudaError_t f = cudaFreeAsync(buf, stream);
@@ -748,7 +753,8 @@ int rg_plan(int variant, int wtype, int64_t N, int64_t K, int64_t T, rg_plan_inf
     r.grid = p.grid;
     r.stream_k = p.sk ? 1 : 0;
     // dY conversion (and F32 W's), GEMM, split reduction or stream-K fixup
-    r.launches = (p.n_splits > 1 || p.sk ? 3 : 2) + (wtype == RG_F32 ? 1 : 0);
+    // (a split in two adds its halves into dX, for beta 0: no third kernel)
+    r.launches = (p.sk || p.n_splits > 2 ? 3 : 2) + (wtype == RG_F32 ? 1 : 0);
   } else if (r.variant == RG_VARIANT_SMALLT) {
     const SmalltPlan p = plan_smallt(wtype, N, K, T, *dev);
     r.tile_k = 256;

@@ -173,7 +173,9 @@ cudaError_t launch_dequant(int wtype, const void* W, int64_t N, int64_t K, float
 template <bool BF16>
 __global__ void __launch_bounds__(256) convert_dy_kernel(const float* __restrict__ dY, int64_t T,
                                                          int64_t N, int64_t ld, float mul,
-                                                         uint16_t* __restrict__ out, int* status) {
+                                                         uint16_t* __restrict__ out, int* status,
+                                                         float* __restrict__ zero, int64_t zk,
+                                                         int64_t zld) {
   pdl_launch_dependents();  // the tensor-core kernel may be scheduled now (it waits for us)
   const int64_t cpr = (N + 7) >> 3;
   const int64_t total = T * cpr;
@@ -211,6 +213,16 @@ __global__ void __launch_bounds__(256) convert_dy_kernel(const float* __restrict
     *reinterpret_cast<uint4*>(out + t * ld + n0) = make_uint4(w[0], w[1], w[2], w[3]);
   }
   if (over) report_range(status);
+  // dX zeroed for a contraction split in two whose halves are both added into
+  // it (T rows of zk values, zld apart; zk and zld multiples of 4)
+  if (zero != nullptr) {
+    const int64_t q4 = zk >> 2;
+    for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < T * q4;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      const int64_t t = g / q4;
+      *reinterpret_cast<float4*>(zero + t * zld + 4 * (g - t * q4)) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+  }
 }
 
 // Strided dY (a row stride other than N, or a column stride other than 1,
@@ -262,7 +274,8 @@ __global__ void __launch_bounds__(256) convert_dy_tiled_kernel(const float* __re
 
 cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t dy_t, int64_t dy_n,
                               int64_t ld, bool bf16, uint16_t* out, const DevInfo& dev,
-                              cudaStream_t stream, float mul) {
+                              cudaStream_t stream, float mul, float* zero, int64_t zk, int64_t zld) {
+  if (zero != nullptr && (dy_n != 1 || dy_t != N || (zk & 3) || (zld & 3))) return cudaErrorInvalidValue;
   if (dy_n != 1 || dy_t != N) {
     if (mul != 1.0f) return cudaErrorInvalidValue;  // (strided rows are dY's alone)
     const int64_t gy = (T + 31) / 32;
@@ -278,9 +291,9 @@ cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t dy_
   }
   const int grid = grid_for(T * ((N + 7) >> 3), 256, dev);
   if (bf16)
-    convert_dy_kernel<true><<<grid, 256, 0, stream>>>(dY, T, N, ld, mul, out, dev.status);
+    convert_dy_kernel<true><<<grid, 256, 0, stream>>>(dY, T, N, ld, mul, out, dev.status, zero, zk, zld);
   else
-    convert_dy_kernel<false><<<grid, 256, 0, stream>>>(dY, T, N, ld, mul, out, dev.status);
+    convert_dy_kernel<false><<<grid, 256, 0, stream>>>(dY, T, N, ld, mul, out, dev.status, zero, zk, zld);
   return counted(cudaGetLastError());
 }
 

@@ -103,9 +103,12 @@ inline int grid_for(int64_t work_items, int threads, const DevInfo& dev) {
 
 // dY [T, N] (strided) F32 -> out [T, ld] fp16 (bf16 when `bf16`), rows padded to ld.
 // mul != 1 (contiguous rows only) converts mul * dY.
+// zero (optional, row-contiguous dY only): T rows of zk floats, zld apart,
+// set to zero by the same kernel (zk, zld multiples of 4)
 cudaError_t launch_convert_dy(const float* dY, int64_t T, int64_t N, int64_t dy_t, int64_t dy_n,
                               int64_t ld, bool bf16, uint16_t* out, const DevInfo& dev,
-                              cudaStream_t stream, float mul = 1.0f);
+                              cudaStream_t stream, float mul = 1.0f, float* zero = nullptr,
+                              int64_t zk = 0, int64_t zld = 0);
 
 // --- the low-rank adapter (rg_adapter.cu) ---
 // U [T, rank] (rows ldu floats apart) into columns [roundup8(N),
@@ -195,10 +198,19 @@ int64_t tc_dy16_ld(int64_t N);
 // 16-bit kind of the product, and dy16 has tc_adapter_cols(N, rank) columns:
 // dY's N values, zeros up to the next multiple of 64, then the rank values
 // of the adapter's projected dY and zeros to the next multiple of 64.
+// zeroed: dX was zeroed by the dY conversion and the plan splits the
+// contraction in two (tc_adds_halves): both halves are bulk-added into dX,
+// no partial sums, no reduction kernel.
 cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
                       int64_t ld_dy16, int64_t T, float* dX, int64_t dx_t, float beta, float* part,
                       const DevInfo& dev, cudaStream_t stream, int cg_force,
-                      const uint16_t* a16 = nullptr, int64_t rank = 0);
+                      const uint16_t* a16 = nullptr, int64_t rank = 0, bool zeroed = false);
+// Whether an OUT_PROD with this beta runs its two contraction halves as adds
+// into a dX the conversion zeroed: beta 0, row-contiguous dY, a plan split in
+// exactly two (two adds onto an exact zero are order-independent; with more
+// halves, or beta * dX under them, the order would show in the bits).
+bool tc_adds_halves(int64_t N, int64_t K, int64_t T, float beta, bool dy_rows, const DevInfo& dev,
+                    int cg_force);
 // k units per rasterization band of a plan (see launch_tc).
 int tc_band(int wtype, int64_t n_contr, const TcPlan& p);
 int64_t tc_adapter_cols(int64_t N, int64_t rank);

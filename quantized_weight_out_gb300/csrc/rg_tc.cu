@@ -84,7 +84,8 @@ TcPlan plan_tc(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force
 cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* dy16,
                       int64_t ld_dy16, int64_t T, float* dX, int64_t dx_t, float beta, float* part,
                       const DevInfo& dev, cudaStream_t stream, int cg_force, const uint16_t* a16,
-                      int64_t rank) {
+                      int64_t rank, bool zeroed) {
+  if (zeroed && rank > 0) return cudaErrorInvalidValue;
   if (rank > 0)
     return launch_tc_adapter(wtype, W, N, K, dy16, ld_dy16, T, dX, dx_t, beta, part, dev, stream,
                              cg_force, a16, rank);
@@ -92,7 +93,14 @@ cudaError_t launch_tc(int wtype, const void* W, int64_t N, int64_t K, const uint
     return launch_tc_stream_k(wtype, W, N, K, dy16, ld_dy16, T, dX, dx_t, beta, part, dev, stream,
                               cg_force);
   return launch_tc_impl<false, false>(wtype, W, N, K, dy16, ld_dy16, T, dX, dx_t, beta, part, dev,
-                                      stream, cg_force, nullptr, 0);
+                                      stream, cg_force, nullptr, 0, zeroed);
+}
+
+bool tc_adds_halves(int64_t N, int64_t K, int64_t T, float beta, bool dy_rows, const DevInfo& dev,
+                    int cg_force) {
+  if (beta != 0.0f || !dy_rows) return false;
+  const TcPlan p = plan_tc(N, K, T, dev, cg_force);
+  return p.n_splits == 2 && !p.sk;
 }
 
 int tc_band(int wtype, int64_t n_contr, const TcPlan& p) {

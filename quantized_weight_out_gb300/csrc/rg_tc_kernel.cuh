@@ -1647,12 +1647,16 @@ static cudaError_t launch_tc_w(const CUtensorMap& mw, const CUtensorMap& my,
 // K values of each row into an output N wide, the OUT_PROD over the N rows
 // into an output K wide.  dy16 (dY's or X's 16-bit copy) has one row of the
 // contraction's length per row of the output's T.
+// zeroed: dX was set to zero before this launch (by the dY conversion) and
+// the plan splits the contraction in two: both halves are added into dX by
+// the epilogue's bulk adds (two adds onto an exact zero give the same bits
+// in either order), no partial sums and no reduction kernel.
 template <bool AD, bool SK, bool FWD = false>
 static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K,
                                   const uint16_t* dy16, int64_t ld_dy16, int64_t T, float* dX,
                                   int64_t dx_t, float beta, float* part, const DevInfo& dev,
                                   cudaStream_t stream, int cg_force, const uint16_t* a16,
-                                  int64_t rank) {
+                                  int64_t rank, bool zeroed = false) {
   // with an adapter the contraction runs over tc_adapter_cols(N, r) columns
   // of dy16: dY's N, zeros to the chunk boundary, then the adapter's rank
   const int64_t n_ext = FWD ? K : rank > 0 ? tc_adapter_cols(N, rank) : N;
@@ -1660,8 +1664,10 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
   const int n_main = rank > 0 ? static_cast<int>((N + tc::BC - 1) / tc::BC) : (1 << 30);
   TcPlan p = plan_tc(n_ext, k_out, T, dev, cg_force);
   if (p.sk != SK) return cudaErrorInvalidValue;  // the dispatcher chose the other build
-  if ((p.n_splits > 1 || p.sk) && part == nullptr) return cudaErrorInvalidValue;
-  float* partial = p.n_splits > 1 || p.sk ? part : nullptr;
+  if (zeroed && (p.n_splits != 2 || p.sk)) return cudaErrorInvalidValue;
+  if ((p.n_splits > 1 || p.sk) && part == nullptr && !zeroed) return cudaErrorInvalidValue;
+  float* partial = (p.n_splits > 1 || p.sk) && !zeroed ? part : nullptr;
+  if (zeroed) beta = 1.0f;  // each half adds itself to dX
   p.band = tc_band(wtype, n_ext, p);
   CUtensorMap mw, my, mq, m3;
   CUresult r;
@@ -1718,7 +1724,7 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   // a split contraction's partial sums [n_splits][T][k_out], the split the third dimension
   CUtensorMap mp = mx;
-  if (p.n_splits > 1) {
+  if (p.n_splits > 1 && partial != nullptr) {
     r = encode_tiled(&mp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, partial, static_cast<uint64_t>(k_out),
                      static_cast<uint64_t>(T), static_cast<uint64_t>(k_out) * 4, 32, er,
                      CU_TENSOR_MAP_SWIZZLE_NONE, static_cast<uint64_t>(p.n_splits),
@@ -1730,7 +1736,7 @@ static cudaError_t launch_tc_impl(int wtype, const void* W, int64_t N, int64_t K
     return launch_tc_w<decltype(wt)::value, AD, SK, FWD>(mw, my, ml, mx, mp, m3, n_main, dX, dx_t, beta,
                                                         t, k, p, partial, dev, stream);
   });
-  if (e != cudaSuccess || p.n_splits == 1) return e;
+  if (e != cudaSuccess || p.n_splits == 1 || zeroed) return e;
   return launch_reduce_partials(partial, p.n_splits, T, k_out, dX, dx_t, beta, dev, stream);
 }
 
