@@ -334,7 +334,9 @@ typedef struct rg_plan_info {
   int32_t tile_t;           /* ... by rows along T (dY rows one pass over W serves) */
   int32_t n_splits;         /* contraction over N split into this many partial sums (1: none) */
   int32_t grid;             /* CTAs of the main kernel (tensor-core: before the residency cap) */
-  int32_t launches;         /* kernels one call enqueues */
+  int32_t launches;         /* kernels one call enqueues, for beta 0 and row-contiguous dY (a
+                               contraction split in two then adds both halves into dX; with
+                               beta != 0 or strided dY it adds a reduction kernel) */
   int32_t stream_k;         /* tensor-core variants: 1 when the last tiles' contraction is
                                shared evenly over all units (stream-K), else 0 */
   int64_t decode_ops;       /* weight values decoded per call: ceil(T / tile_t) * N * K */
