@@ -602,7 +602,12 @@ int rg_mul_mat(int wtype, const void* W, int64_t N, int64_t K, const float* X, i
   // K % 2048 != 0, Q2_K K % 1024, MXFP4 K % 512): a transient dense 16-bit
   // deq(W)^T, contracted by the OUT_PROD kernel as a weight of K rows
   cudaError_t e = fused ? cudaSuccess : launch_dequant_t16(wtype, W, N, K, bf16, w16, N, *dev, s);
-  if (e == cudaSuccess) e = launch_convert_dy(X, T, K, K, 1, ld, bf16, xh, *dev, s);
+  // a contraction split in two with beta 0: X's conversion zeroes Y and the
+  // two halves add themselves into it
+  const TcPlan mp = plan_tc(K, N, T, *dev, 0);
+  const bool halves = fused && beta == 0.0f && mp.n_splits == 2 && !mp.sk;
+  if (e == cudaSuccess)
+    e = launch_convert_dy(X, T, K, K, 1, ld, bf16, xh, *dev, s, 1.0f, halves ? Y : nullptr, N, N);
   const void* Wtc = W;
   int wtc = wtype;
   if (wtype == RG_F32 && fused) {
@@ -615,7 +620,7 @@ int rg_mul_mat(int wtype, const void* W, int64_t N, int64_t K, const float* X, i
   t_prof_before = t_prof_after = nullptr;
   if (e == cudaSuccess && ev0) e = cudaEventRecord(ev0, s);
   if (e == cudaSuccess)
-    e = fused ? launch_mm(wtc, Wtc, N, K, xh, ld, T, Y, N, beta, part, *dev, s, 0)
+    e = fused ? launch_mm(wtc, Wtc, N, K, xh, ld, T, Y, N, beta, part, *dev, s, 0, halves)
               : launch_tc(bf16 ? RG_BF16 : RG_F16, w16, K, N, xh, ld, T, Y, N, beta, part, *dev, s, 0);
   if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, s);
   const cudaError_t f = cudaFreeAsync(buf, s);

@@ -220,9 +220,10 @@ int64_t tc_adapter_cols(int64_t N, int64_t rank);
 // (rows ld_x16 apart); part: [n_splits][T][N] partial sums when the plan of
 // (contraction K, output N, T) splits the contraction.  Stream-K is never
 // taken (call it under NoStreamK).
+// zeroed: as launch_tc's (Y zeroed by X's conversion, a plan split in two).
 cudaError_t launch_mm(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* x16,
                       int64_t ld_x16, int64_t T, float* Y, int64_t ldy, float beta, float* part,
-                      const DevInfo& dev, cudaStream_t stream, int cg_force);
+                      const DevInfo& dev, cudaStream_t stream, int cg_force, bool zeroed = false);
 // Number of partial-sum slabs the tensor-core plan needs (0 when unsplit).
 int64_t tc_partial_splits(int64_t N, int64_t K, int64_t T, const DevInfo& dev, int cg_force);
 // Bytes of the `part` workspace the tensor-core plan needs: the splits'

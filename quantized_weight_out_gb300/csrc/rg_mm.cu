@@ -8,9 +8,9 @@ namespace rg {
 
 cudaError_t launch_mm(int wtype, const void* W, int64_t N, int64_t K, const uint16_t* x16,
                       int64_t ld_x16, int64_t T, float* Y, int64_t ldy, float beta, float* part,
-                      const DevInfo& dev, cudaStream_t stream, int cg_force) {
+                      const DevInfo& dev, cudaStream_t stream, int cg_force, bool zeroed) {
   return launch_tc_impl<false, false, true>(wtype, W, N, K, x16, ld_x16, T, Y, ldy, beta, part, dev,
-                                            stream, cg_force, nullptr, 0);
+                                            stream, cg_force, nullptr, 0, zeroed);
 }
 
 }  // namespace rg

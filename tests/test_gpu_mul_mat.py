@@ -133,3 +133,27 @@ def test_mul_mat_full_size_sampled(rg, workload, idx):
     err = np.abs(got[ts, ns].astype(np.float64) - ref)
     lim = 5e-3 * bnd + 1e-7
     assert np.all(err <= lim), (p.name, int((err > lim).sum()), float((err / (bnd + 1e-30)).max()))
+
+
+@pytest.mark.parametrize("wtype", [inputs.Q4_0, inputs.Q8_0, inputs.F16])
+def test_mul_mat_split_in_two(rg, wtype):
+    """A forward whose plan splits the contraction in two (4096 x 4096 at
+    T = 512): with beta 0 both halves are added into the Y that X's
+    conversion zeroed (a NaN-filled Y must not show through), with beta 1
+    into partial sums and a reduction; sampled outputs against the oracle."""
+    N, K, T = 4096, 4096, 512
+    W = inputs.gen_weight(wtype, N, K, seed=94, stream=1)
+    X = inputs.normal_f32(94, 2, T * K, 1e-2).reshape(T, K)
+    Wd = oracle.dequant(wtype, W, N, K)
+    rng = np.random.default_rng(95)
+    ts = np.concatenate([rng.integers(0, T, 4096), np.full(N, T - 1, np.int64)])
+    ns = np.concatenate([rng.integers(0, N, 4096), np.arange(N)])
+    got = _run(rg, wtype, W, N, K, X, T)
+    assert np.isfinite(got).all()
+    ref, bnd = oracle.mul_mat_at(Wd, X, ts, ns)
+    assert np.all(np.abs(got[ts, ns].astype(np.float64) - ref) <= 5e-3 * bnd + 1e-7)
+    Y0 = inputs.normal_f32(94, 3, T * N, 1e-3).reshape(T, N)
+    got = _run(rg, wtype, W, N, K, X, T, Y0, 1.0)
+    ref, bnd = oracle.mul_mat_at(Wd, X, ts, ns, Y0, 1.0)
+    lim = 5e-3 * bnd + 1e-7 + np.abs(Y0[ts, ns]) * 2.0 ** -24
+    assert np.all(np.abs(got[ts, ns].astype(np.float64) - ref) <= lim)
