@@ -524,9 +524,10 @@ __device__ __forceinline__ void dec_q6_k_row(const uint8_t* row, uint8_t* A, int
   constexpr auto last = [](int x) { return (x & 3) == 0 ? x + 3 : (x & ~3) + 7; };
   constexpr int CA = QA / 16, CA1 = CA + last(QA - 16 * CA + 60) / 16;
   constexpr int CH = QHB / 16, CH1 = CH + last(QHB - 16 * CH + 28) / 16;
-  constexpr int CS = QS / 16, CS1 = (QD + 1) / 16;
+  // (d's word_at covers the scales' too: QS + 7 < QD)
+  constexpr int CS = QS / 16, CS1 = CS + last(QD - 16 * CS) / 16;
   static_assert(16 * CA1 + 16 <= p_row_bytes<RG_Q6_K>() && 16 * CH1 + 16 <= p_row_bytes<RG_Q6_K>() &&
-                    16 * CS1 + 16 <= p_row_bytes<RG_Q6_K>(),
+                    16 * CS1 + 16 <= p_row_bytes<RG_Q6_K>() && QS + 7 < QD,
                 "reads stay inside the row window");
   const auto ra = load_chunks<CA, CA1>(row);
   const auto rh = load_chunks<CH, CH1>(row);
