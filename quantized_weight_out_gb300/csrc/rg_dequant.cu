@@ -181,12 +181,10 @@ __global__ void __launch_bounds__(256) convert_dy_kernel(const float* __restrict
   const int64_t total = T * cpr;
   const bool vec = (N & 3) == 0;
   bool over = false;
-  for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
-       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t t = g / cpr;
-    const int64_t n0 = (g - t * cpr) << 3;
+  // eight values from row t, columns 8c on (zeros past N)
+  auto load8 = [&](int64_t t, int64_t c, float (&v)[8]) {
+    const int64_t n0 = c << 3;
     const float* src = dY + t * N + n0;
-    float v[8];
     if (vec && n0 + 8 <= N) {
       const float4 a = __ldcs(reinterpret_cast<const float4*>(src));
       const float4 b = __ldcs(reinterpret_cast<const float4*>(src) + 1);
@@ -196,6 +194,8 @@ __global__ void __launch_bounds__(256) convert_dy_kernel(const float* __restrict
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = (n0 + i < N) ? src[i] : 0.0f;
     }
+  };
+  auto store8 = [&](int64_t t, int64_t c, float (&v)[8]) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] *= mul;
     uint32_t w[4];
@@ -210,7 +210,35 @@ __global__ void __launch_bounds__(256) convert_dy_kernel(const float* __restrict
       }
       over |= overflowed16<BF16>(v[2 * i], w[i] & 0xFFFFu) | overflowed16<BF16>(v[2 * i + 1], w[i] >> 16);
     }
-    *reinterpret_cast<uint4*>(out + t * ld + n0) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(out + t * ld + (c << 3)) = make_uint4(w[0], w[1], w[2], w[3]);
+  };
+  // a grid-stride walk over the groups of eight, two groups an iteration
+  // with both groups' loads in flight; the row and column are carried from
+  // one group to the next instead of divided out each time
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t st = stride / cpr, sr = stride - st * cpr;
+  auto advance = [&](int64_t& t, int64_t& c) {
+    t += st;
+    c += sr;
+    if (c >= cpr) {
+      c -= cpr;
+      ++t;
+    }
+  };
+  int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  int64_t t = g / cpr, c = g - t * cpr;
+  for (; g < total; g += 2 * stride) {
+    int64_t t1 = t, c1 = c;
+    advance(t1, c1);
+    const bool two = g + stride < total;
+    float v0[8], v1[8];
+    load8(t, c, v0);
+    if (two) load8(t1, c1, v1);
+    store8(t, c, v0);
+    if (two) store8(t1, c1, v1);
+    t = t1;
+    c = c1;
+    advance(t, c);
   }
   if (over) report_range(status);
   // dX zeroed for a contraction split in two whose halves are both added into
