@@ -1223,8 +1223,10 @@ __global__ void __launch_bounds__(256) smallt_reduce_wide(const float* __restric
 // Resident CTAs per SM of smallt_kernel<WT, TB> on this device (queried once).
 template <int WT, int TB>
 static int smallt_residency(const DevInfo& dev) {
-  static int cache[64] = {0};
-  int& c = cache[dev.device & 63];
+  // per device; threads that race on the first call store the same value
+  static std::atomic<int> cache[64];
+  std::atomic<int>& slot = cache[dev.device & 63];
+  int c = slot.load(std::memory_order_relaxed);
   if (c == 0) {
     auto kern = smt::smallt_kernel<WT, TB>;
     constexpr size_t smem = smt::smem_bytes<WT, TB>();
@@ -1233,6 +1235,7 @@ static int smallt_residency(const DevInfo& dev) {
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, smt::THREADS + 32, smem) != cudaSuccess ||
         n <= 0)
       n = 1;
+    slot.store(n, std::memory_order_relaxed);
     c = n;
   }
   return c;

@@ -1610,13 +1610,16 @@ static cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& my,
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   // persistent grid: no more clusters than can be resident at once
-  static int max_clusters[64] = {0};
-  int& mc = max_clusters[dev.device & 63];
+  // (per device; threads that race on the first call store the same value)
+  static std::atomic<int> max_clusters[64];
+  std::atomic<int>& mc_slot = max_clusters[dev.device & 63];
+  int mc = mc_slot.load(std::memory_order_relaxed);
   if (mc == 0) {
     cfg.gridDim = dim3(static_cast<unsigned>(CG * (dev.num_sms / CG)), 1, 1);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0)
       n = dev.num_sms / CG;
+    mc_slot.store(n, std::memory_order_relaxed);
     mc = n;
   }
   const int units = std::min(p.grid / CG, mc);
