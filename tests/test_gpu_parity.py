@@ -215,6 +215,29 @@ def test_smallt_mma_rows(rg, T, wtype):
             assert np.all(err <= 5e-3 * bnd[t]), (t, float((err / bnd[t]).max()))
 
 
+@pytest.mark.parametrize("wtype", [inputs.Q4_K, inputs.Q8_0])
+@pytest.mark.parametrize("T", [1, 4])
+def test_smallt_mma_rows_spanning_octaves(rg, T, wtype):
+    """dY whose elements spread over nine decades inside every row slice
+    (|y| = |N(0, 1)| * 10^u, u uniform in [-9, 0]): the entries of the
+    small-T MMA consumer's fp16 table far below the slice's maximum are
+    subnormal and keep fewer bits, yet the result stays within 5e-3 of the
+    bound with no absolute slack, the bound's sum being carried by the
+    slice's large rows."""
+    N, K = 1000, 768
+    W = inputs.gen_weight(wtype, N, K, seed=33, stream=1)
+    g = inputs.normal_f32(33, 2, T * N, 1.0)
+    u = inputs.uniform01(inputs.stream_key(33, 4), 0, T * N)
+    dY = (g * 10.0 ** (-9.0 * u)).astype(np.float32).reshape(T, N)
+    Wd = oracle.dequant(wtype, W, N, K)
+    ref = oracle.out_prod(wtype, W, N, K, dY, T, Wd=Wd)
+    bnd = oracle.abs_bound(dY, Wd)
+    assert rg.rg_select_variant(wtype, N, K, T) == rg.RG_VARIANT_SMALLT
+    got = run_out_prod(rg, 2, wtype, W, N, K, dY, T)
+    err = np.abs(got.astype(np.float64) - ref)
+    assert np.all(err <= 5e-3 * bnd), float((err / bnd).max())
+
+
 @pytest.mark.parametrize("variant", [4, 5])
 @pytest.mark.parametrize("wtype", TYPES)
 def test_all_ones_closed_form_tc(rg, variant, wtype):
