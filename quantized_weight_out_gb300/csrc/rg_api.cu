@@ -810,8 +810,9 @@ const char* rg_strerror(int status) {
     case RG_ERR_ARG: return "invalid argument (null pointer, negative or too large size, small workspace)";
     case RG_ERR_TYPE: return "unknown weight type or variant";
     case RG_ERR_SHAPE:
-      return "K is not a multiple of 256 (quantized types) or 8 (F32/F16/BF16), or Q6_K with "
-             "K % 2048 != 0 on a tensor-core or small-T variant";
+      return "K is not a multiple of 256 (quantized types) or 8 (F32/F16/BF16); or rows not "
+             "16-byte aligned on a tensor-core or small-T variant (Q6_K, Q3_K: K % 2048 != 0; "
+             "Q2_K: K % 1024 != 0; MXFP4: K % 512 != 0); or a batch or N rule of the call";
     case RG_ERR_ALIGN: return "pointer not 16-byte aligned (workspace: 256-byte)";
     case RG_ERR_CUDA: return "CUDA call or kernel launch failed";
     case RG_ERR_TIMEOUT: return "a bounded device-side wait gave up";
