@@ -273,22 +273,36 @@ int rg_out_prod_batched(int variant, int wtype, const void* W, int64_t N, int64_
  *
  * X: [T, K] F32, Y: [T, N] F32 (read only when beta != 0), both row-major
  * and 16-byte aligned; W as for rg_out_prod.  N must be a multiple of 8
- * (RG_ERR_SHAPE).  X is rounded once to a 16-bit copy (fp16; bf16 for F32
- * and BF16 W) and the tensor-core kernel decodes W's blocks straight into
- * its operand tiles, now contracting over the K values of each row, with
- * F32 accumulation: |err| <= 5e-3 * sum_k |X||deq W| + 1e-7; no copy of
- * deq(W) exists (F32 W: a bf16 copy of W, as rg_out_prod makes).  Rows that
- * are not 16-byte aligned (Q6_K and Q3_K with K % 2048 != 0, Q2_K with
- * K % 1024 != 0, MXFP4 with K % 512 != 0) instead decode deq(W)^T once per
- * call into a transient 16-bit [K, N] copy (2*N*K bytes).  Workspace from
- * the library's stream-ordered pool (rg_mul_mat_workspace_bytes).  T == 0
- * or N == 0: nothing to do; K == 0: Y = beta * Y.
+ * (RG_ERR_SHAPE).  Two routes, chosen by the shape:
+ *   - one or two rows of X with 16-byte aligned rows of W (see below): W
+ *     is streamed once, each row's values decoded exactly to F32 and
+ *     multiplied with X in F32 (|err| far below the bound that follows);
+ *     one launch, no workspace;
+ *   - otherwise X is rounded once to a 16-bit copy (fp16; bf16 for F32 and
+ *     BF16 W) and the tensor-core kernel decodes W's blocks straight into
+ *     its operand tiles, now contracting over the K values of each row, with
+ *     F32 accumulation: |err| <= 5e-3 * sum_k |X||deq W| + 1e-7; no copy of
+ *     deq(W) exists (F32 W: a bf16 copy of W, as rg_out_prod makes).  Rows
+ *     that are not 16-byte aligned (Q6_K and Q3_K with K % 2048 != 0, Q2_K
+ *     with K % 1024 != 0, MXFP4 with K % 512 != 0) instead decode deq(W)^T
+ *     once per call into a transient 16-bit [K, N] copy (2*N*K bytes).
+ * Workspace from the library's stream-ordered pool
+ * (rg_mul_mat_workspace_bytes).  T == 0 or N == 0: nothing to do; K == 0:
+ * Y = beta * Y.
  */
 int rg_mul_mat(int wtype, const void* W, int64_t N, int64_t K, const float* X, int64_t T, float* Y,
                float beta, void* stream);
 
+/* rg_mul_mat with its route named: RG_VARIANT_AUTO (rg_mul_mat's choice),
+ * RG_VARIANT_TC (the tensor-core kernel, any T) or RG_VARIANT_SMALLT (W
+ * streamed once per four rows of X, any T; RG_ERR_SHAPE for rows that are
+ * not 16-byte aligned).  Other variants: RG_ERR_TYPE. */
+int rg_mul_mat_variant(int variant, int wtype, const void* W, int64_t N, int64_t K, const float* X,
+                       int64_t T, float* Y, float beta, void* stream);
+
 /* Device workspace bytes one rg_mul_mat call of this shape takes from the
- * pool on the current device (0 for an invalid or empty shape). */
+ * pool on the current device (0 for an invalid or empty shape, and for the
+ * one-or-two-row route, which takes none). */
 size_t rg_mul_mat_workspace_bytes(int wtype, int64_t N, int64_t K, int64_t T);
 
 /*

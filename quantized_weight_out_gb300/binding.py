@@ -54,6 +54,7 @@ SIGNATURES = [
     ("rg_out_prod_noalloc", _I, [_I, _VP, _I64, _I64, _VP, _I64, _VP, _F, _VP]),
     ("rg_plan", _I, [_I, _I, _I64, _I64, _I64, ctypes.POINTER(rg_plan_info)]),
     ("rg_mul_mat", _I, [_I, _VP, _I64, _I64, _VP, _I64, _VP, _F, _VP]),
+    ("rg_mul_mat_variant", _I, [_I, _I, _VP, _I64, _I64, _VP, _I64, _VP, _F, _VP]),
     ("rg_out_prod_lora", _I, [_I, _I, _VP, _I64, _I64, _VP, _I64, _VP, _F, _VP, _VP, _I64, _F, _VP]),
     ("rg_out_prod_ex", _I, [_I, _I, _VP, _I64, _I64, _I64, _VP, _I64, _I64, _I64, _I64, _VP, _I64,
                             _I64, _I64, _F, _VP]),
@@ -139,6 +140,11 @@ def rg_out_prod_batched(variant, wtype, W, N, K, w_n2, w_n3, w_s2, w_s3, dY, T, 
 
 def rg_mul_mat(wtype, W, N, K, X, T, Y, beta, stream=None) -> int:
     return load().rg_mul_mat(wtype, _ptr(W), N, K, _ptr(X), T, _ptr(Y), beta, _stream(stream))
+
+
+def rg_mul_mat_variant(variant, wtype, W, N, K, X, T, Y, beta, stream=None) -> int:
+    return load().rg_mul_mat_variant(variant, wtype, _ptr(W), N, K, _ptr(X), T, _ptr(Y), beta,
+                                     _stream(stream))
 
 
 def rg_mul_mat_workspace_bytes(wtype, N, K, T) -> int:

@@ -558,8 +558,18 @@ MmWs mm_workspace(int wtype, int64_t N, int64_t K, int64_t T, const DevInfo& dev
 
 }  // namespace
 
+namespace {
+
+// The forward's automatic choice: one or two rows of X stream W once
+// (small-T); from three rows the tensor-core kernel, whose time barely
+// grows with T at these sizes, is faster.
+bool mm_smallt(int wtype, int64_t K, int64_t T) { return T <= 2 && aligned_rows(wtype, K); }
+
+}  // namespace
+
 size_t rg_mul_mat_workspace_bytes(int wtype, int64_t N, int64_t K, int64_t T) {
   if (!valid_wtype(wtype) || N <= 0 || K <= 0 || T <= 0) return 0;
+  if (mm_smallt(wtype, K, T)) return 0;
   DevInfo* dev = nullptr;
   if (current_dev(&dev) != RG_OK) return 0;
   return mm_workspace(wtype, N, K, T, *dev).total();
@@ -567,7 +577,14 @@ size_t rg_mul_mat_workspace_bytes(int wtype, int64_t N, int64_t K, int64_t T) {
 
 int rg_mul_mat(int wtype, const void* W, int64_t N, int64_t K, const float* X, int64_t T, float* Y,
                float beta, void* stream) {
+  return rg_mul_mat_variant(RG_VARIANT_AUTO, wtype, W, N, K, X, T, Y, beta, stream);
+}
+
+int rg_mul_mat_variant(int variant, int wtype, const void* W, int64_t N, int64_t K, const float* X,
+                       int64_t T, float* Y, float beta, void* stream) {
   if (!valid_wtype(wtype)) return RG_ERR_TYPE;
+  if (variant != RG_VARIANT_AUTO && variant != RG_VARIANT_TC && variant != RG_VARIANT_SMALLT)
+    return RG_ERR_TYPE;
   if (N < 0 || K < 0 || T < 0 || N > kMaxDim || K > kMaxDim || T > kMaxDim) return RG_ERR_ARG;
   if (K % (is_quant(wtype) ? 256 : 8) || N % 8) return RG_ERR_SHAPE;
   if (T == 0 || N == 0) return RG_OK;
@@ -582,6 +599,17 @@ int rg_mul_mat(int wtype, const void* W, int64_t N, int64_t K, const float* X, i
   if (st != RG_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) return from_cuda(launch_scale(Y, T, N, N, beta, *dev, s));
+  if (variant == RG_VARIANT_AUTO) variant = mm_smallt(wtype, K, T) ? RG_VARIANT_SMALLT : RG_VARIANT_TC;
+  if (variant == RG_VARIANT_SMALLT) {
+    // W streamed once per four rows of X, F32 products: one launch
+    if (!aligned_rows(wtype, K)) return RG_ERR_SHAPE;
+    cudaEvent_t ev0 = t_prof_before, ev1 = t_prof_after;
+    t_prof_before = t_prof_after = nullptr;
+    cudaError_t e = ev0 ? cudaEventRecord(ev0, s) : cudaSuccess;
+    if (e == cudaSuccess) e = launch_smallt_fwd(wtype, W, N, K, X, T, Y, beta, *dev, s);
+    if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, s);
+    return from_cuda(e);
+  }
   // Y = X . deq(W)^T: the tensor-core kernel decodes W's blocks as the
   // K-major operand of a contraction over each row's K values; X is rounded
   // to the 16-bit kind once (F32 W: both W and X to bf16)

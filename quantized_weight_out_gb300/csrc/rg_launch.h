@@ -164,6 +164,11 @@ cudaError_t launch_smallt(int wtype, const void* W, int64_t N, int64_t K, const 
                           int64_t T, float* dX, float beta, const Layout& lay, float* part,
                           const SmalltPlan& p, const DevInfo& dev, cudaStream_t stream,
                           int inject_stall = 0);
+// The forward Y = beta * Y + X . deq(W)^T streaming W once per four rows of
+// X (rg_mul_mat's route for one or two rows): one launch, no workspace.  X [T, K] and Y [T, N] row-major; W's rows
+// must be 16-byte aligned (aligned_rows).
+cudaError_t launch_smallt_fwd(int wtype, const void* W, int64_t N, int64_t K, const float* X, int64_t T,
+                              float* Y, float beta, const DevInfo& dev, cudaStream_t stream);
 
 // Tensor-core path.  dy16 is the converted dY with row stride ld_dy16 values.
 struct TcPlan {

@@ -1137,6 +1137,165 @@ constexpr size_t smem_bytes() {
          sizeof(float) * TB * MAX_ROWS + aux_bytes<WT, TB>() + 16 * n_stages<WT, TB>();
 }
 
+// --- the forward at a few rows of X -----------------------------------------
+// Y[t, n] = beta * Y[t, n] + sum_k X[t, k] * deq(W)[n, k], up to four rows
+// of X a pass (rg_mul_mat's route for one or two rows): every weight value
+// is read once a pass, so the call streams W like the small-T OUT_PROD,
+// with the roles of the two axes swapped.  A CTA owns a
+// block of rows (8, 16 or 32) along the whole of K: a producer warp copies,
+// tile by tile, the block's 256-value tiles (or their 16-byte windows) into
+// a ring; consumer warp w takes rows w, w + 8, ... of the block, each lane
+// decodes its 8 values of a row exactly to F32 and multiplies them with its
+// 8 values of each row of X, and the 32 lanes' partial sums of a row meet in
+// a fixed butterfly at the end: no partial sums in memory, no second kernel
+// and no 16-bit copy of X.
+template <int WT>
+constexpr int fwd_rows() { return WT == RG_F32 ? 16 : 32; }
+template <int WT>
+constexpr int fwd_stages() {
+  return stage_row_bytes<WT>() * fwd_rows<WT>() * 8 <= 72 * 1024 ? 8 : 4;
+}
+template <int WT>
+constexpr size_t fwd_smem_bytes() {
+  return static_cast<size_t>(fwd_stages<WT>()) * fwd_rows<WT>() * stage_row_bytes<WT>() + 16 * fwd_stages<WT>();
+}
+
+// grid (ceil(N / rows), ceil(T / TB)); rows = the tensor map's box height
+// (8, 16 or 32, at most fwd_rows<WT>()), a multiple of 8.
+template <int WT, int TB>
+__global__ void __launch_bounds__(THREADS + 32, 3)
+    smallt_fwd_kernel(const __grid_constant__ CUtensorMap map_w, int N, int K,
+                      const float* __restrict__ X, int T, float* __restrict__ Y, float beta, int rows,
+                      WaitCtl ctl) {
+  constexpr int TBYTES = stage_row_bytes<WT>();
+  constexpr int RMAX = fwd_rows<WT>(), STAGES = fwd_stages<WT>(), UMAX = RMAX / CONSUMERS;
+  extern __shared__ __align__(128) uint8_t sm[];
+  uint8_t* stage_buf = sm;  // STAGES x RMAX x TBYTES
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + STAGES * RMAX * TBYTES);  // full[S], empty[S]
+  __shared__ int abort_flag_s;
+  volatile int* abort_flag = &abort_flag_s;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * rows, t0 = blockIdx.y * TB;
+  const int n_kt = (K + 255) / 256;
+  const uint32_t bar0 = smem_addr(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  const uint32_t stage_tx = static_cast<uint32_t>(rows) * TBYTES;
+
+  // the producer's lane initialises the ring and starts its first copies
+  // before the block-wide barrier (fresh slots need no wait)
+  const bool producer = threadIdx.x == THREADS;
+  uint32_t pend = 0;
+  const int n_pre = min(STAGES, n_kt);
+  if (producer) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), CONSUMERS);
+    }
+    abort_flag_s = 0;
+    fence_mbar_init();
+    for (int i = 0; i < n_pre; ++i) {
+      mbar_arrive_expect_tx(full(i), stage_tx);
+      tma_load_2d(smem_addr(stage_buf + i * RMAX * TBYTES), &map_w, full(i),
+                  static_cast<int>(window_start<WT>(i) / 4), n0);
+      pend |= 1u << i;
+    }
+  }
+  __syncthreads();  // the ring's barriers
+
+  if (warp == CONSUMERS) {
+    if (lane == 0) {
+      uint32_t ph = n_pre == STAGES ? 1u : 0u, pend_ph = 0;  // the phase of each started copy
+      for (int i = n_pre; i < n_kt; ++i) {
+        const int s = i % STAGES;
+        if (!mbar_wait(empty(s), ph ^ 1u, ctl, abort_flag)) break;
+        mbar_arrive_expect_tx(full(s), stage_tx);
+        tma_load_2d(smem_addr(stage_buf + s * RMAX * TBYTES), &map_w, full(s),
+                    static_cast<int>(window_start<WT>(i) / 4), n0);
+        pend |= 1u << s;
+        pend_ph = (pend_ph & ~(1u << s)) | (ph << s);
+        if (s == STAGES - 1) ph ^= 1u;
+      }
+      // every copy started lands before the CTA leaves
+      volatile int no_abort = 0;
+      for (int s = 0; s < STAGES; ++s)
+        if (pend & (1u << s)) (void)mbar_wait(full(s), (pend_ph >> s) & 1u, ctl, &no_abort);
+    }
+    __syncwarp();
+    return;
+  }
+
+  const int upw = rows / CONSUMERS;  // rows of the block this warp takes
+  float acc[UMAX][TB];
+#pragma unroll
+  for (int u = 0; u < UMAX; ++u)
+#pragma unroll
+    for (int t = 0; t < TB; ++t) acc[u][t] = 0.0f;
+  bool ok = true;
+  for (int i = 0; i < n_kt; ++i) {
+    const int s = i % STAGES;
+    // this lane's 8 values of each row of X in tile i (zeros past K and T;
+    // K is a multiple of 8, so a lane's 8 values are all in or all out)
+    const int k0 = i * 256 + 8 * lane;
+    const bool kv = k0 < K;
+    float x[TB][8];
+#pragma unroll
+    for (int t = 0; t < TB; ++t) {
+      float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f), b = a;
+      if (kv && t0 + t < T) {
+        const float4* p = reinterpret_cast<const float4*>(X + static_cast<int64_t>(t0 + t) * K + k0);
+        a = __ldg(p);
+        b = __ldg(p + 1);
+      }
+      x[t][0] = a.x; x[t][1] = a.y; x[t][2] = a.z; x[t][3] = a.w;
+      x[t][4] = b.x; x[t][5] = b.y; x[t][6] = b.z; x[t][7] = b.w;
+    }
+    if (!__all_sync(0xffffffffu, mbar_wait(full(s), static_cast<uint32_t>(i / STAGES) & 1u, ctl,
+                                           abort_flag))) {
+      ok = false;
+      break;
+    }
+    if (kv) {
+      const uint8_t* tile = stage_buf + s * RMAX * TBYTES + window_offset<WT>(i);
+#pragma unroll
+      for (int u = 0; u < UMAX; ++u) {
+        if (u < upw) {
+          Raw<WT> raw;
+          load_raw_smem<WT>(tile + (warp + CONSUMERS * u) * TBYTES, lane, raw);
+          float w[8];
+          decode_raw<WT>(raw, lane, w);
+#pragma unroll
+          for (int t = 0; t < TB; ++t)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[u][t] = fmaf(x[t][q], w[q], acc[u][t]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty(s));
+  }
+  if (!ok) return;  // a wait that gave up: Y is left as it was (rg_check reports it)
+  // the 32 lanes' partial sums of each row in a fixed butterfly (every lane
+  // ends with the same bits); lane 0 writes
+#pragma unroll
+  for (int u = 0; u < UMAX; ++u) {
+    if (u < upw) {
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        float v = acc[u][t];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        const int n = n0 + warp + CONSUMERS * u;
+        if (lane == 0 && n < N && t0 + t < T) {
+          float* y = Y + static_cast<int64_t>(t0 + t) * N + n;
+          *y = beta != 0.0f ? fmaf(beta, *y, v) : v;
+        }
+      }
+    }
+  }
+}
+
 // dX = beta * dX + sum over splits (in split order), four values per thread.
 // dX offset of element i of a [T, K] slab, dX rows ldx floats apart
 __device__ __forceinline__ int64_t dx_at(int64_t i, int64_t K, int64_t ldx) {
@@ -1349,6 +1508,53 @@ cudaError_t launch_smallt(int wtype, const void* W, int64_t N, int64_t K, const 
   });
   if (e != cudaSuccess || p.n_splits == 1) return e;  // one slice: the kernel wrote dX
   return launch_reduce_partials(part, p.n_splits, T, K, dX, lay.dx_t, beta, dev, stream);
+}
+
+template <int WT, int TB>
+static cudaError_t launch_smallt_fwd_t(const void* W, int64_t N, int64_t K, const float* X, int64_t T,
+                                       float* Y, float beta, const DevInfo& dev, cudaStream_t stream) {
+  auto kern = smt::smallt_fwd_kernel<WT, TB>;
+  constexpr size_t smem = smt::fwd_smem_bytes<WT>();
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  // per device; threads that race on the first call store the same value
+  static std::atomic<int> cache[64];
+  std::atomic<int>& slot = cache[dev.device & 63];
+  int per_sm = slot.load(std::memory_order_relaxed);
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, smt::THREADS + 32, smem) != cudaSuccess ||
+        per_sm <= 0)
+      per_sm = 1;
+    slot.store(per_sm, std::memory_order_relaxed);
+  }
+  // blocks of rows: the largest of 32 (16 for F32), 16 and 8 rows that still
+  // gives at least half a wave of CTAs
+  const int64_t n_tchunks = (T + TB - 1) / TB;
+  const int64_t half_wave = static_cast<int64_t>(dev.num_sms) * per_sm / 2;
+  int rows = smt::fwd_rows<WT>();
+  while (rows > 8 && (N + rows - 1) / rows * n_tchunks < half_wave) rows /= 2;
+  const int64_t n_blocks = (N + rows - 1) / rows;
+  if (n_blocks > 0x7FFFFFFF || n_tchunks > 65535) return cudaErrorInvalidConfiguration;
+  const uint64_t rb = static_cast<uint64_t>(K / block_values(WT) * block_bytes(WT));
+  CUtensorMap map;
+  if (encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rb / 4, static_cast<uint64_t>(N), rb,
+                   smt::stage_row_bytes<WT>() / 4, static_cast<uint32_t>(rows),
+                   CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  WaitCtl ctl{dev.status, dev.wait_limit_ns};
+  kern<<<dim3(static_cast<unsigned>(n_blocks), static_cast<unsigned>(n_tchunks)), smt::THREADS + 32, smem,
+         stream>>>(map, static_cast<int>(N), static_cast<int>(K), X, static_cast<int>(T), Y, beta, rows, ctl);
+  return counted(cudaGetLastError());
+}
+
+cudaError_t launch_smallt_fwd(int wtype, const void* W, int64_t N, int64_t K, const float* X, int64_t T,
+                              float* Y, float beta, const DevInfo& dev, cudaStream_t stream) {
+  return with_wtype(wtype, cudaErrorInvalidValue, [&](auto wt) {
+    constexpr int WT = decltype(wt)::value;
+    return T <= 1   ? launch_smallt_fwd_t<WT, 1>(W, N, K, X, T, Y, beta, dev, stream)
+           : T <= 2 ? launch_smallt_fwd_t<WT, 2>(W, N, K, X, T, Y, beta, dev, stream)
+                    : launch_smallt_fwd_t<WT, 4>(W, N, K, X, T, Y, beta, dev, stream);
+  });
 }
 
 cudaError_t launch_reduce_partials(const float* part, int n_splits, int64_t T, int64_t K,

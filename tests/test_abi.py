@@ -209,6 +209,13 @@ def test_mul_mat_validation(lib):
     assert rg.rg_mul_mat(inputs.Q8_0, A, 64, 256, A, 0, A, 0.0) == rg.RG_OK
     assert rg.rg_mul_mat(inputs.Q8_0, A + 4, 64, 256, A, 4, A, 0.0) == rg.RG_ERR_ALIGN
     assert rg.rg_mul_mat(inputs.Q8_0, A, 64, 256, A, 4, None, 0.0) == rg.RG_ERR_ARG
+    # the forward's routes: auto, tensor core and small-T; no SIMT or forced tile shape
+    for v in (rg.RG_VARIANT_SIMT32, rg.RG_VARIANT_TC_SINGLE, rg.RG_VARIANT_TC_PAIR, 9, -1):
+        assert rg.rg_mul_mat_variant(v, inputs.Q8_0, A, 64, 256, A, 4, A, 0.0) == rg.RG_ERR_TYPE
+    assert rg.rg_mul_mat_variant(rg.RG_VARIANT_SMALLT, inputs.Q8_0, A, 60, 256, A, 1, A, 0.0) == rg.RG_ERR_SHAPE
+    # one or two rows of X with aligned rows take no workspace
+    for T in (1, 2):
+        assert rg.rg_mul_mat_workspace_bytes(inputs.Q4_K, 14336, 4096, T) == 0
 
 
 def test_out_prod_lora_validation(lib):
