@@ -295,8 +295,9 @@ int rg_mul_mat(int wtype, const void* W, int64_t N, int64_t K, const float* X, i
 
 /* rg_mul_mat with its route named: RG_VARIANT_AUTO (rg_mul_mat's choice),
  * RG_VARIANT_TC (the tensor-core kernel, any T) or RG_VARIANT_SMALLT (W
- * streamed once per four rows of X, any T; RG_ERR_SHAPE for rows that are
- * not 16-byte aligned).  Other variants: RG_ERR_TYPE. */
+ * streamed once per four rows of X, up to 262140 rows; RG_ERR_SHAPE beyond
+ * that and for rows that are not 16-byte aligned).  Other variants:
+ * RG_ERR_TYPE. */
 int rg_mul_mat_variant(int variant, int wtype, const void* W, int64_t N, int64_t K, const float* X,
                        int64_t T, float* Y, float beta, void* stream);
 

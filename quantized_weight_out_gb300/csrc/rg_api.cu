@@ -593,6 +593,9 @@ int rg_mul_mat_variant(int variant, int wtype, const void* W, int64_t N, int64_t
   if (K > 0) {
     if (!W || !X) return RG_ERR_ARG;
     if (!aligned16(W) || !aligned16(X)) return RG_ERR_ALIGN;
+    // the named small-T route: 16-byte aligned rows, a grid row per four rows of X
+    if (variant == RG_VARIANT_SMALLT && (!aligned_rows(wtype, K) || (T + 3) / 4 > 65535))
+      return RG_ERR_SHAPE;
   }
   DevInfo* dev = nullptr;
   int st = current_dev(&dev);
@@ -602,7 +605,6 @@ int rg_mul_mat_variant(int variant, int wtype, const void* W, int64_t N, int64_t
   if (variant == RG_VARIANT_AUTO) variant = mm_smallt(wtype, K, T) ? RG_VARIANT_SMALLT : RG_VARIANT_TC;
   if (variant == RG_VARIANT_SMALLT) {
     // W streamed once per four rows of X, F32 products: one launch
-    if (!aligned_rows(wtype, K)) return RG_ERR_SHAPE;
     cudaEvent_t ev0 = t_prof_before, ev1 = t_prof_after;
     t_prof_before = t_prof_after = nullptr;
     cudaError_t e = ev0 ? cudaEventRecord(ev0, s) : cudaSuccess;

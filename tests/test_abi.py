@@ -213,6 +213,11 @@ def test_mul_mat_validation(lib):
     for v in (rg.RG_VARIANT_SIMT32, rg.RG_VARIANT_TC_SINGLE, rg.RG_VARIANT_TC_PAIR, 9, -1):
         assert rg.rg_mul_mat_variant(v, inputs.Q8_0, A, 64, 256, A, 4, A, 0.0) == rg.RG_ERR_TYPE
     assert rg.rg_mul_mat_variant(rg.RG_VARIANT_SMALLT, inputs.Q8_0, A, 60, 256, A, 1, A, 0.0) == rg.RG_ERR_SHAPE
+    # the named small-T route: rows TMA cannot address (Q6_K at K = 256), or
+    # more rows of X than its grid holds, are shape errors before any launch
+    assert rg.rg_mul_mat_variant(rg.RG_VARIANT_SMALLT, inputs.Q6_K, A, 64, 256, A, 1, A, 0.0) == rg.RG_ERR_SHAPE
+    assert rg.rg_mul_mat_variant(rg.RG_VARIANT_SMALLT, inputs.Q8_0, A, 64, 256, A, 4 * 65535 + 1, A,
+                                 0.0) == rg.RG_ERR_SHAPE
     # one or two rows of X with aligned rows take no workspace
     for T in (1, 2):
         assert rg.rg_mul_mat_workspace_bytes(inputs.Q4_K, 14336, 4096, T) == 0
